@@ -1,0 +1,215 @@
+"""Number formats of the MoE path, written from their bit-field definitions (fp64, numpy).
+
+Sources on the pages:
+  * MXFP4 weights = E2M1 codes with one E8M0 scale per 32 along K
+    (moe_b12x_next.py, module docstring and ``_Geometry.__init__``: ``MXFP4_E8M0_K32``).
+  * E8M0 decode is 2^(e-127) (hybrid_loader.py, ``_fp8_ne_transform._deq``).
+  * NVFP4 weights = E2M1 with an E4M3 scale per 16 and a per-expert fp32 global scale
+    (hybrid_loader.py, ``_deq_nv`` and the NVFP4 ``weight_scale_2`` tensors).
+  * NF3 = 3-bit codes into an 8-entry LUT, 8 codes per 3 bytes, scale per 32
+    (hybrid_loader.py, ``_NF3_VALS`` and ``_unpack_nf3``).
+  * MXFP8 activations (E4M3 codes + E8M0 scale per 32) are produced inside the kernel
+    (moe_b12x_next.py, module docstring "in-kernel MXFP8 activations"); the pages do not print
+    the scale rule, so the OCP MX v1.0 rule is used: shared exponent = floor(log2 amax) - 8
+    (8 = emax of E4M3), elements rounded to nearest-even and saturated to +-448.
+
+Pinned by tests/test_oracle_codecs.py (hand-worked values in tests/golden/, exhaustive round
+trips, and an independent library cast for the element rounding only).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# ---------------------------------------------------------------------------- E2M1 (FP4)
+
+def e2m1_value(code: int) -> float:
+    """One E2M1 nibble: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0.
+    Exponent 0 is subnormal: m * 0.5."""
+    s = (code >> 3) & 1
+    e = (code >> 1) & 3
+    m = code & 1
+    mag = m * 0.5 if e == 0 else (2.0 ** (e - 1)) * (1.0 + 0.5 * m)
+    return -mag if s else mag
+
+
+E2M1_TABLE = np.array([e2m1_value(c) for c in range(16)], dtype=np.float64)
+
+
+def unpack_fp4(packed: np.ndarray) -> np.ndarray:
+    """[..., n] bytes -> [..., 2n] nibble codes; element 2j is the low nibble of byte j."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = p & 0x0F
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def pack_fp4(codes: np.ndarray) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] & 0x0F) | ((c[..., 1::2] & 0x0F) << 4)
+
+
+# ---------------------------------------------------------------------------- E8M0
+
+def e8m0_value(b) -> np.ndarray:
+    """E8M0 scale byte -> 2^(b-127); 0xFF is NaN."""
+    b = np.asarray(b, dtype=np.int64)
+    v = np.ldexp(1.0, b - 127)
+    return np.where(b == 255, np.nan, v)
+
+
+# ---------------------------------------------------------------------------- E4M3 (fn)
+
+def e4m3_value(code: int) -> float:
+    """E4M3 'fn': sign bit 7, exponent bits 6..3 (bias 7), mantissa bits 2..0.
+    Exponent 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN; there is no infinity."""
+    s = (code >> 7) & 1
+    e = (code >> 3) & 15
+    m = code & 7
+    if e == 15 and m == 7:
+        return float("nan")
+    mag = (m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return -mag if s else mag
+
+
+E4M3_TABLE = np.array([e4m3_value(c) for c in range(256)], dtype=np.float64)
+E4M3_MAX = 448.0
+# positive finite magnitudes, codes 0..126, ascending
+_E4M3_POS = E4M3_TABLE[:127]
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    return E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
+def e4m3_encode_rne_sat(v) -> np.ndarray:
+    """fp64 -> E4M3 code: round to nearest, ties to even mantissa, saturate to +-448.
+    NaN is never produced for finite input (the 'satfinite' rule).  The sign bit is the
+    input's sign, so a negative value that rounds to zero gives -0 (0x80), as IEEE rounding
+    keeps the sign of a zero result."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.minimum(np.abs(v), E4M3_MAX)
+    # index of the largest grid value <= a
+    lo = np.searchsorted(_E4M3_POS, a, side="right") - 1
+    lo = np.clip(lo, 0, 126)
+    hi = np.minimum(lo + 1, 126)
+    dlo = a - _E4M3_POS[lo]
+    dhi = _E4M3_POS[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (lo % 2 == 1))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return np.where(np.signbit(v), code | 0x80, code).astype(np.uint8)
+
+
+# ---------------------------------------------------------------------------- bf16
+
+def bf16_round(v) -> np.ndarray:
+    """fp64 -> nearest bf16 value (ties to even), returned as fp64.  bf16 = 8 significant
+    bits, exponent range of fp32 (normals down to 2^-126, subnormal step 2^-133)."""
+    v = np.asarray(v, dtype=np.float64)
+    out = np.zeros_like(v)
+    nz = (v != 0) & np.isfinite(v)
+    _, ex = np.frexp(v[nz])               # v = f * 2^ex, 0.5 <= |f| < 1
+    e = ex.astype(np.int64) - 1            # floor(log2 |v|)
+    q = np.maximum(e, -126) - 7            # exponent of one unit in the last place
+    r = np.round(np.ldexp(v[nz], -q))      # numpy rounds half to even
+    out[nz] = np.ldexp(r, q)
+    out[~np.isfinite(v)] = v[~np.isfinite(v)]
+    big = np.abs(out) >= 2.0 ** 128
+    out[big] = np.copysign(np.inf, out[big])
+    return out
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16_bits(v) -> np.ndarray:
+    r = bf16_round(v).astype(np.float32)
+    return (r.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def f32_round(v) -> np.ndarray:
+    return np.asarray(v, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------- MXFP8 quantiser
+
+MX_BLOCK = 32
+E4M3_EMAX = 8
+
+
+def biased_exponent(a) -> np.ndarray:
+    """Biased binary exponent field of a non-negative value as an fp32 would store it:
+    floor(log2 a) + 127 for normals, 0 for zero and fp32 subnormals."""
+    a = np.asarray(a, dtype=np.float64)
+    _, ex = np.frexp(a)
+    e = ex.astype(np.int64) - 1 + 127
+    return np.where(a >= 2.0 ** -126, e, 0)
+
+
+def mxfp8_quantize(v: np.ndarray):
+    """Quantise the last axis (a multiple of 32) to MXFP8.
+
+    Per block of 32: amax = max |v|; scale byte s = clamp(E(amax) - 8, 0, 254) where E is the
+    biased exponent (so the scale is 2^(floor(log2 amax) - 8)); code = E4M3 RNE-saturated
+    value of v / 2^(s-127).  An all-zero block has scale byte 0 and zero codes.
+    Returns (codes uint8 [..., K], scale bytes uint8 [..., K/32]).
+    """
+    v = np.asarray(v, dtype=np.float64)
+    K = v.shape[-1]
+    assert K % MX_BLOCK == 0
+    blocks = v.reshape(v.shape[:-1] + (K // MX_BLOCK, MX_BLOCK))
+    amax = np.abs(blocks).max(axis=-1)
+    s = np.clip(biased_exponent(amax) - E4M3_EMAX, 0, 254)
+    scaled = np.ldexp(blocks, (127 - s)[..., None])
+    codes = e4m3_encode_rne_sat(scaled).reshape(v.shape)
+    return codes, s.astype(np.uint8)
+
+
+def mxfp8_dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    vals = e4m3_decode(codes)
+    K = vals.shape[-1]
+    sc = e8m0_value(scales)
+    return (vals.reshape(vals.shape[:-1] + (K // MX_BLOCK, MX_BLOCK)) * sc[..., None]).reshape(vals.shape)
+
+
+# ---------------------------------------------------------------------------- NF3
+
+# The 8-entry NF3 table exactly as printed (hybrid_loader.py, ``_NF3_VALS``).
+NF3_LUT = (-1.0, -0.6047, -0.3563, -0.1275, 0.1275, 0.3563, 0.6047, 1.0)
+NF3_GROUP = 32
+
+
+def nf3_unpack(packed: np.ndarray, n_cols: int) -> np.ndarray:
+    """[R, n_cols/8*3] bytes -> [R, n_cols] codes.  Each 3-byte group b0,b1,b2 forms the
+    24-bit word b0 | b1<<8 | b2<<16 whose bits 3i..3i+2 are code i (hybrid_loader.py,
+    ``_unpack_nf3``)."""
+    p = np.asarray(packed, dtype=np.uint32)
+    R = p.shape[0]
+    p = p.reshape(R, n_cols // 8, 3)
+    w24 = p[..., 0] | (p[..., 1] << 8) | (p[..., 2] << 16)
+    codes = np.stack([(w24 >> (3 * i)) & 7 for i in range(8)], axis=-1)
+    return codes.reshape(R, n_cols).astype(np.uint8)
+
+
+def nf3_pack(codes: np.ndarray) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.uint32)
+    R, n = c.shape
+    c = c.reshape(R, n // 8, 8)
+    w24 = np.zeros((R, n // 8), dtype=np.uint32)
+    for i in range(8):
+        w24 |= (c[..., i] & 7) << (3 * i)
+    out = np.stack([w24 & 0xFF, (w24 >> 8) & 0xFF, (w24 >> 16) & 0xFF], axis=-1)
+    return out.reshape(R, n // 8 * 3).astype(np.uint8)
+
+
+def nf3_dequant(packed: np.ndarray, scale_codes: np.ndarray, n_cols: int) -> np.ndarray:
+    """NF3 weight values as the page's unpack produces them: the LUT entry (held as fp32) times
+    the fp32 value of the E4M3 group scale, the product rounded to bf16
+    (``_unpack_nf3``: ``(nf[codes] * scale.float().repeat_interleave(32, 1)).to(bfloat16)``)."""
+    codes = nf3_unpack(packed, n_cols)
+    lut32 = np.array(NF3_LUT, dtype=np.float32)
+    sc32 = e4m3_decode(scale_codes).astype(np.float32)
+    prod32 = lut32[codes] * np.repeat(sc32, NF3_GROUP, axis=1)      # fp32 multiply
+    return bf16_round(prod32.astype(np.float64))

@@ -1,0 +1,275 @@
+"""The routed-MoE forward by definition, in fp64 on the CPU (test infrastructure only).
+
+out[t] = sum_j w[t,j] * expert_{id[t,j]}(x[t]),  expert(x) = W2 . act(gate(x), up(x))
+
+with gate/up the two halves of fc1 = W13 . x (hybrid_loader.py ``_apply_ref``; vLLM B12xExperts
+``apply``).  Ids outside [0, E), the -1 of CUDA-graph padding rows included, contribute nothing
+(moe_b12x_next.py, knob ``_DIRECT_IDS``: the kernels skip ids outside [0, E) and padding rows
+come out 0).
+
+Readings where the pages are silent (each one is listed with its reason in the design notes):
+  * SwiGLU clamp: gate' = min(gate, L), up' = clamp(up, -L, L),
+    h = gate' * sigmoid(alpha * gate') * (up' + beta), alpha = 1 and beta = 0 unless given;
+    L = +inf means no clamp, which is the plain silu(g) * u of ``_apply_ref``.
+  * W4A8: x is quantised to MXFP8 before fc1, h is quantised to MXFP8 before fc2 (from the
+    unrounded SwiGLU output).  W4A16: x enters as bf16, h is rounded to bf16 before fc2.
+  * The result is accumulated in fp64 over the top-k slots and rounded to bf16 once.
+  * Routing order: the slots of expert e are listed in ascending (t, j) order (stable
+    counting sort).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import codecs as C
+
+W13_UP_GATE = 0
+W13_GATE_UP = 1
+TIER_NVFP4 = 4
+TIER_NF3 = 3
+
+
+# ---------------------------------------------------------------------------- routing
+
+def route(topk_ids: np.ndarray, E: int):
+    """Routing by definition.
+
+    Valid slots are the flat indices f = t*k + j with 0 <= id < E.
+      cnt[e]     number of valid slots with id e
+      off[e]     exclusive prefix sum of cnt (off[E] = S, the number of valid slots)
+      perm[p]    flat slot index at position p; the slots of expert e occupy
+                 off[e] .. off[e+1]-1 in ascending flat order
+      slot_of[f] position of flat slot f in perm, -1 for dropped ids
+    Pinned by tests/test_oracle_moe.py (hand-worked case in tests/golden/routing.txt and a
+    pure-Python brute force).
+    """
+    flat = np.asarray(topk_ids, dtype=np.int64).ravel()
+    valid = (flat >= 0) & (flat < E)
+    cnt = np.bincount(flat[valid], minlength=E).astype(np.int32)
+    off = np.zeros(E + 1, dtype=np.int32)
+    off[1:] = np.cumsum(cnt)
+    key = np.where(valid, flat, E)
+    order = np.argsort(key, kind="stable")
+    S = int(valid.sum())
+    perm = order[:S].astype(np.int32)
+    slot_of = np.full(flat.shape[0], -1, dtype=np.int32)
+    slot_of[perm] = np.arange(S, dtype=np.int32)
+    return cnt, off, perm, slot_of
+
+
+# ---------------------------------------------------------------------------- activation
+
+def swiglu(gate, up, limit=math.inf, alpha=1.0, beta=0.0):
+    """Clamped SwiGLU (reading above).  Pinned by closed forms in tests/test_oracle_moe.py."""
+    g = np.minimum(np.asarray(gate, dtype=np.float64), limit)
+    u = np.clip(np.asarray(up, dtype=np.float64), -limit, limit)
+    return g * (1.0 / (1.0 + np.exp(-alpha * g))) * (u + beta)
+
+
+# ---------------------------------------------------------------------------- weights
+
+def _fp4_values(packed: np.ndarray) -> np.ndarray:
+    return C.E2M1_TABLE[C.unpack_fp4(packed)]
+
+
+def dequant_mxfp4(packed: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """[R, K/2] E2M1 bytes, [R, K/32] E8M0 bytes -> [R, K] fp64: E2M1(code) * 2^(s-127)."""
+    v = _fp4_values(packed)
+    return v * np.repeat(C.e8m0_value(scales), 32, axis=1)
+
+
+def dequant_nvfp4(packed: np.ndarray, scales: np.ndarray, g: float) -> np.ndarray:
+    """[R, K/2] E2M1 bytes, [R, K/16] E4M3 bytes, fp32 global -> E2M1 * E4M3(s) * g.
+    Reading: the per-expert ``weight_scale_2`` multiplies (one global per matrix)."""
+    v = _fp4_values(packed)
+    return v * np.repeat(C.e4m3_decode(scales), 16, axis=1) * float(g)
+
+
+def dequant_nf3(packed: np.ndarray, scales: np.ndarray, K: int) -> np.ndarray:
+    return C.nf3_dequant(packed, scales, K)
+
+
+def tier_local_index(tier: np.ndarray):
+    """Hybrid layer: expert e -> (tier, index among the experts of that tier in ascending e),
+    the compact two-group storage of hybrid_loader.py (``remap``)."""
+    out = {}
+    n = {TIER_NVFP4: 0, TIER_NF3: 0}
+    for e, t in enumerate(np.asarray(tier).tolist()):
+        out[e] = (int(t), n[int(t)])
+        n[int(t)] += 1
+    return out
+
+
+def expert_weights(ck, e: int):
+    """Dequantised (W13 [2I, H], W2 [H, I], kind) of expert e of a synth Checkpoint."""
+    H, I = ck.H, ck.I
+    if ck.quant == "mxfp4":
+        return dequant_mxfp4(ck.w13[e], ck.s13[e]), dequant_mxfp4(ck.w2[e], ck.s2[e]), "mxfp4"
+    if ck.quant == "nvfp4":
+        return (dequant_nvfp4(ck.w13[e], ck.s13[e], ck.g13[e]),
+                dequant_nvfp4(ck.w2[e], ck.s2[e], ck.g2[e]), "nvfp4")
+    if ck.quant == "nf3":
+        return dequant_nf3(ck.w13[e], ck.s13[e], H), dequant_nf3(ck.w2[e], ck.s2[e], I), "nf3"
+    if ck.quant == "hybrid":
+        t, li = tier_local_index(ck.tier)[e]
+        sub = ck.nv if t == TIER_NVFP4 else ck.nf
+        return expert_weights(sub, li)
+    raise ValueError(ck.quant)
+
+
+def split_w13(g13: np.ndarray, I: int, layout: int):
+    """fc1 output [.., 2I] -> (gate, up) according to the stacking order of W13."""
+    first, second = g13[..., :I], g13[..., I:]
+    return (second, first) if layout == W13_UP_GATE else (first, second)
+
+
+# ---------------------------------------------------------------------------- forward
+
+def activation_a8(ck) -> bool:
+    return ck.quant == "mxfp4"
+
+
+def quantize_x(x_bits: np.ndarray, a8: bool):
+    """x as the fc1 kernel sees it: MXFP8 (codes, scales, dequantised values) or bf16 values."""
+    x = C.bf16_bits_to_f64(x_bits)
+    if a8:
+        q, s = C.mxfp8_quantize(x)
+        return q, s, C.mxfp8_dequantize(q, s)
+    return None, None, x
+
+
+def requant_h(h: np.ndarray, a8: bool) -> np.ndarray:
+    if a8:
+        q, s = C.mxfp8_quantize(h)
+        return C.mxfp8_dequantize(q, s)
+    return C.bf16_round(h)
+
+
+def moe_forward(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.0,
+                rows=None, return_f64=False):
+    """Per-expert dgemm form.  ``rows`` restricts the output to a subset of token rows
+    (the other rows are not computed and come back as NaN).  Returns bf16 bit patterns
+    [M, H] (and the unrounded fp64 sum when ``return_f64``).
+    Pinned by tests/test_oracle_moe.py against the brute-force loop, closed forms and the
+    invariants (linearity in the weights, padding rows, token-order invariance, w13 halves)."""
+    x_bits = np.asarray(x_bits)
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    w = np.asarray(topk_w, dtype=np.float64)
+    M, k = ids.shape
+    E, H, I = ck.E, ck.H, ck.I
+    a8 = activation_a8(ck)
+    out = np.zeros((M, H), dtype=np.float64)
+    row_mask = np.ones(M, dtype=bool)
+    if rows is not None:
+        row_mask[:] = False
+        row_mask[np.asarray(rows)] = True
+    _, _, xhat = quantize_x(x_bits[row_mask] if rows is not None else x_bits, a8)
+    if rows is not None:
+        full = np.full((M, H), np.nan)
+        full[row_mask] = xhat
+        xhat = full
+    valid = (ids >= 0) & (ids < E) & row_mask[:, None]
+    for e in np.unique(ids[valid]):
+        sel = valid & (ids == e)
+        t_idx, j_idx = np.nonzero(sel)
+        W13, W2, _ = expert_weights(ck, int(e))
+        G = xhat[t_idx] @ W13.T
+        gate, up = split_w13(G, I, ck.layout)
+        h = swiglu(gate, up, limit, alpha, beta)
+        hh = requant_h(h, a8)
+        y = hh @ W2.T
+        np.add.at(out, t_idx, w[t_idx, j_idx][:, None] * y)
+    out[~row_mask] = np.nan
+    bits = C.f64_to_bf16_bits(np.where(row_mask[:, None], out, 0.0))
+    if return_f64:
+        return bits, out
+    return bits
+
+
+def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.0):
+    """Token by token, slot by slot, element by element (pure Python loops; tiny inputs only).
+    Dequantises each weight element from its own code and scale with scalar decoders."""
+    ids = np.asarray(topk_ids).tolist()
+    w = np.asarray(topk_w, dtype=np.float64).tolist()
+    M = len(ids)
+    E, H, I = ck.E, ck.H, ck.I
+    a8 = activation_a8(ck)
+    _, _, xhat = quantize_x(np.asarray(x_bits), a8)
+    out = [[0.0] * H for _ in range(M)]
+
+    tiers = tier_local_index(ck.tier) if ck.quant == "hybrid" else None
+
+    def weight(mat, e, r, c):
+        """Scalar decode of element (r, c) of expert e's matrix ('w13' or 'w2')."""
+        if tiers is not None:
+            t, li = tiers[e]
+            sub = ck.nv if t == TIER_NVFP4 else ck.nf
+        else:
+            sub, li = ck, e
+        codes = getattr(sub, mat)[li]
+        scales = getattr(sub, "s13" if mat == "w13" else "s2")[li]
+        if sub.quant in ("mxfp4", "nvfp4"):
+            byte = int(codes[r, c // 2])
+            nib = byte & 0xF if c % 2 == 0 else byte >> 4
+            v = C.e2m1_value(nib)
+            if sub.quant == "mxfp4":
+                return v * 2.0 ** (int(scales[r, c // 32]) - 127)
+            g = float((sub.g13 if mat == "w13" else sub.g2)[li])
+            return v * C.e4m3_value(int(scales[r, c // 16])) * g
+        # NF3: bytes 3*(c//8) .. +2 hold codes c//8*8 .. +7
+        b = codes[r, 3 * (c // 8): 3 * (c // 8) + 3]
+        w24 = int(b[0]) | (int(b[1]) << 8) | (int(b[2]) << 16)
+        code = (w24 >> (3 * (c % 8))) & 7
+        prod = np.float32(C.NF3_LUT[code]) * np.float32(C.e4m3_value(int(scales[r, c // 32])))
+        return float(C.bf16_round(float(prod)))
+
+    for t in range(M):
+        for j in range(len(ids[t])):
+            e = ids[t][j]
+            if not (0 <= e < E):
+                continue
+            xt = xhat[t]
+            gate = [0.0] * I
+            up = [0.0] * I
+            for i in range(I):
+                up_row = i if ck.layout == W13_UP_GATE else I + i
+                gate_row = I + i if ck.layout == W13_UP_GATE else i
+                su = 0.0
+                sg = 0.0
+                for c in range(H):
+                    su += weight("w13", e, up_row, c) * xt[c]
+                    sg += weight("w13", e, gate_row, c) * xt[c]
+                up[i] = su
+                gate[i] = sg
+            h = [0.0] * I
+            for i in range(I):
+                g = min(gate[i], limit)
+                u = max(-limit, min(up[i], limit))
+                h[i] = g * (1.0 / (1.0 + math.exp(-alpha * g))) * (u + beta)
+            hh = requant_h(np.array(h), a8).tolist()
+            for r in range(H):
+                s = 0.0
+                for i in range(I):
+                    s += weight("w2", e, r, i) * hh[i]
+                out[t][r] += w[t][j] * s
+    return C.f64_to_bf16_bits(np.array(out))
+
+
+# ---------------------------------------------------------------------------- bounds
+
+def row_errors(got_bits, ref_f64):
+    """Per-row relative L2 error and max|err| / rms(row) of bf16 output against the fp64 sum."""
+    got = C.bf16_bits_to_f64(got_bits)
+    ref = np.asarray(ref_f64, dtype=np.float64)
+    diff = got - ref
+    nref = np.sqrt((ref ** 2).sum(axis=1))
+    rms = np.sqrt((ref ** 2).mean(axis=1))
+    rel = np.sqrt((diff ** 2).sum(axis=1)) / np.where(nref > 0, nref, 1.0)
+    mx = np.abs(diff).max(axis=1) / np.where(rms > 0, rms, 1.0)
+    zero_rows = nref == 0
+    rel[zero_rows] = np.where(np.abs(got[zero_rows]).max(axis=1) == 0, 0.0, np.inf) \
+        if zero_rows.any() else rel[zero_rows]
+    mx[zero_rows] = rel[zero_rows]
+    return rel, mx

@@ -1,0 +1,191 @@
+"""Pins for oracle/codecs.py: hand-worked values (tests/golden/), exhaustive round trips and
+properties fixed by the formats' definitions.  Nothing here re-uses the oracle's own tables to
+produce an expected value."""
+import math
+
+import numpy as np
+import pytest
+
+from conftest import golden_lines
+from oracle import codecs as C
+
+
+def test_golden_scalar_formats():
+    n = 0
+    for f in golden_lines("codecs.txt"):
+        kind = f[0]
+        if kind == "e2m1":
+            got = C.e2m1_value(int(f[1], 16))
+            want = float(f[2])
+            assert got == want and math.copysign(1, got) == math.copysign(1, want), f
+        elif kind == "e8m0":
+            assert float(C.e8m0_value(int(f[1]))) == float(f[2]), f
+        elif kind == "e4m3":
+            got = C.e4m3_value(int(f[1], 16))
+            want = float(f[2])
+            assert got == want and math.copysign(1, got) == math.copysign(1, want), f
+        elif kind == "fp4byte":
+            codes = C.unpack_fp4(np.array([[int(f[1], 16)]], dtype=np.uint8))[0]
+            assert C.E2M1_TABLE[codes].tolist() == [float(f[2]), float(f[3])], f
+        else:
+            raise AssertionError(kind)
+        n += 1
+    assert n > 30
+
+
+def test_e2m1_grid_properties():
+    # magnitudes of the 8 positive codes are the OCP FP4 grid; the sign bit negates
+    mags = [C.e2m1_value(c) for c in range(8)]
+    assert mags == sorted(mags) and len(set(mags)) == 8
+    for c in range(8):
+        assert C.e2m1_value(c | 8) == -C.e2m1_value(c)
+    # E2M1 values times 2 are integers (one mantissa bit, smallest step 0.5)
+    assert all(float(2 * m).is_integer() for m in mags)
+
+
+def test_fp4_pack_roundtrip_exhaustive():
+    codes = np.array([[a, b] for a in range(16) for b in range(16)], dtype=np.uint8).reshape(1, -1)
+    packed = C.pack_fp4(codes)
+    assert packed.shape == (1, 256)
+    assert sorted(packed[0].tolist()) == list(range(256))      # bijection on bytes
+    assert np.array_equal(C.unpack_fp4(packed), codes)
+
+
+def test_e4m3_table_properties():
+    t = C.E4M3_TABLE
+    assert np.isnan(t[0x7F]) and np.isnan(t[0xFF])
+    assert np.isnan(t).sum() == 2                                # only S.1111.111
+    pos = t[:127]
+    assert np.all(np.diff(pos) > 0)                              # strictly increasing grid
+    assert pos[-1] == 448.0 and pos[1] == 2.0 ** -9
+    assert np.array_equal(t[128:255], -pos)                      # sign symmetry
+    # within each binade 8 equal steps; the subnormal step equals the first normal step
+    for e in range(1, 15):
+        b = pos[8 * e: 8 * e + 8]
+        assert np.allclose(np.diff(b), 2.0 ** (e - 10))
+    assert np.allclose(np.diff(pos[:9]), 2.0 ** -9)
+
+
+def test_e4m3_table_matches_library_cast():
+    ml = pytest.importorskip("ml_dtypes")
+    lib = np.arange(256, dtype=np.uint8).view(ml.float8_e4m3fn).astype(np.float64)
+    ok = ~np.isnan(lib)
+    assert np.array_equal(np.isnan(lib), np.isnan(C.E4M3_TABLE))
+    assert np.array_equal(lib[ok], C.E4M3_TABLE[ok])
+
+
+def test_e4m3_encode_roundtrip_every_code():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    assert np.array_equal(C.e4m3_encode_rne_sat(C.e4m3_decode(codes)), codes)
+
+
+def test_e4m3_encode_rounding_and_saturation():
+    pos = C.E4M3_TABLE[:127]
+    mids = (pos[:-1] + pos[1:]) / 2
+    got = C.e4m3_encode_rne_sat(mids)
+    lo = np.arange(126)
+    # ties go to the even code (even mantissa)
+    want = np.where(lo % 2 == 0, lo, lo + 1)
+    assert np.array_equal(got, want)
+    # just above / below a midpoint go to the nearer neighbour
+    assert np.array_equal(C.e4m3_encode_rne_sat(np.nextafter(mids, np.inf)), lo + 1)
+    assert np.array_equal(C.e4m3_encode_rne_sat(np.nextafter(mids, -np.inf)), lo)
+    # saturation: everything >= 448 (incl. what would round to 480) maps to 0x7E
+    assert C.e4m3_encode_rne_sat(np.array([448.0, 463.9, 464.0, 500.0, 1e30])).tolist() == [0x7E] * 5
+    assert C.e4m3_encode_rne_sat(np.array([-1e30])).tolist() == [0xFE]
+
+
+def test_e4m3_encode_matches_library_cast_in_range():
+    ml = pytest.importorskip("ml_dtypes")
+    rng = np.random.default_rng(5)
+    v = np.concatenate([rng.standard_normal(20000) * s for s in (1e-3, 0.1, 1, 10, 100)])
+    v = v[np.abs(v) <= 440].astype(np.float32)        # library cast does not saturate
+    lib = v.astype(ml.float8_e4m3fn).view(np.uint8)
+    got = C.e4m3_encode_rne_sat(v.astype(np.float64))
+    assert np.array_equal(lib, got)
+
+
+def test_bf16_round_matches_library_cast():
+    ml = pytest.importorskip("ml_dtypes")
+    rng = np.random.default_rng(6)
+    v = (rng.standard_normal(50000) * np.exp(rng.uniform(-30, 30, 50000))).astype(np.float32)
+    lib = v.astype(ml.bfloat16).astype(np.float64)
+    assert np.array_equal(C.bf16_round(v.astype(np.float64)), lib)
+
+
+def test_bf16_round_by_definition():
+    # values with <= 8 significant bits are fixed points; ties go to even
+    assert C.bf16_round(np.array([1.0, 1.0 + 2 ** -7, 3.0, -255.0])).tolist() == [1.0, 1.0 + 2 ** -7, 3.0, -255.0]
+    assert C.bf16_round(np.array([1.0 + 2 ** -8])).tolist() == [1.0]                      # tie -> even
+    assert C.bf16_round(np.array([1.0 + 3 * 2 ** -8])).tolist() == [1.0 + 2 ** -6]        # tie -> even
+    assert C.bf16_round(np.array([1.0 + 2 ** -8 + 2 ** -20])).tolist() == [1.0 + 2 ** -7]
+    bits = C.f64_to_bf16_bits(np.array([1.0, -2.0, 0.0]))
+    assert bits.tolist() == [0x3F80, 0xC000, 0x0000]
+    assert C.bf16_bits_to_f64(np.array([0x3F80, 0x4049], dtype=np.uint16)).tolist() == [1.0, 3.140625]
+
+
+def test_mxfp8_golden_blocks():
+    n = 0
+    for f in golden_lines("mxfp8_blocks.txt"):
+        amax, probe, sbyte, code = float(f[0]), float(f[1]), int(f[2]), int(f[3], 16)
+        block = np.zeros(32)
+        block[0] = amax
+        block[1] = probe
+        q, s = C.mxfp8_quantize(block[None, :])
+        assert int(s[0, 0]) == sbyte, f
+        assert int(q[0, 1]) == code, f
+        n += 1
+    assert n >= 10
+
+
+def test_mxfp8_properties():
+    rng = np.random.default_rng(7)
+    v = rng.standard_normal((64, 256)) * np.exp(rng.uniform(-8, 8, (64, 1)))
+    q, s = C.mxfp8_quantize(v)
+    d = C.mxfp8_dequantize(q, s)
+    blocks = v.reshape(64, 8, 32)
+    amax = np.abs(blocks).max(-1)
+    scale = 2.0 ** (s.astype(np.float64) - 127)
+    # amax / scale lies in [256, 512): the block maximum uses the top binade of E4M3
+    r = amax / scale
+    assert np.all((r >= 256) & (r < 512))
+    # per element error <= half an E4M3 step at the element's binade, or the saturation error
+    err = np.abs(d - v).reshape(64, 8, 32)
+    scaled = np.abs(blocks) / scale[..., None]
+    binade = np.floor(np.log2(np.maximum(scaled, 2.0 ** -6)))
+    half_step = 2.0 ** (binade - 3) / 2 * scale[..., None]
+    sat = np.maximum(np.abs(blocks) - 448 * scale[..., None], 0)
+    assert np.all(err <= half_step + sat + 1e-300)
+    # scale-invariance: multiplying a block by 2^j shifts only the scale byte
+    q2, s2 = C.mxfp8_quantize(v * 2.0 ** 5)
+    assert np.array_equal(q2, q) and np.array_equal(s2.astype(int), s.astype(int) + 5)
+
+
+def test_nf3_golden_and_roundtrip():
+    for f in golden_lines("nf3.txt"):
+        if f[0] == "lut":
+            assert C.NF3_LUT[int(f[1])] == float(f[2])
+            continue
+        codes = np.array([[int(c) for c in f[0].split(",")]], dtype=np.uint8)
+        packed = np.array([[int(b, 16) for b in f[1].split(",")]], dtype=np.uint8)
+        assert np.array_equal(C.nf3_pack(codes), packed), f
+        assert np.array_equal(C.nf3_unpack(packed, 8), codes), f
+    rng = np.random.default_rng(8)
+    codes = rng.integers(0, 8, (5, 64)).astype(np.uint8)
+    assert np.array_equal(C.nf3_unpack(C.nf3_pack(codes), 64), codes)
+    raw = rng.integers(0, 256, (3, 24)).astype(np.uint8)
+    assert np.array_equal(C.nf3_pack(C.nf3_unpack(raw, 64)), raw)
+
+
+def test_nf3_dequant_definition():
+    # one group of 32 codes (all code 6 = 0.6047) with scale 2.0 (E4M3 0x40), second group code 0
+    codes = np.concatenate([np.full(32, 6), np.zeros(32)]).astype(np.uint8)[None, :]
+    packed = C.nf3_pack(codes)
+    sc = np.array([[0x40, 0x38]], dtype=np.uint8)
+    d = C.nf3_dequant(packed, sc, 64)
+    # 0.6047 as fp32 times 2 is exact in fp32; rounded to bf16 (8 significant bits)
+    want0 = float(np.float32(0.6047) * np.float32(2.0))
+    m, e = math.frexp(want0)
+    want0 = round(m * 256) / 256 * 2 ** e
+    assert np.all(d[0, :32] == want0)
+    assert np.all(d[0, 32:] == -1.0)

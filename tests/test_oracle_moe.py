@@ -1,0 +1,265 @@
+"""Pins for oracle/moe.py: routing (hand-worked + brute force), SwiGLU closed forms, the forward
+against a brute-force per-element loop, a closed-form layer, and the invariants the method fixes
+(linearity in the router weights, padding rows, token-order invariance, w13 halves)."""
+import math
+
+import numpy as np
+import pytest
+
+from conftest import golden_lines
+from oracle import codecs as C
+from oracle import moe as O
+import synth
+from synth import moe_inputs as S
+
+
+def _ints(s):
+    return [int(v) for v in s.split(",")]
+
+
+# ---------------------------------------------------------------------------- routing
+
+def test_routing_golden():
+    g = {f[0]: f[1:] for f in golden_lines("routing.txt")}
+    E = int(g["E"][0])
+    ids = np.array([_ints(r) for r in g["ids"]], dtype=np.int32)
+    cnt, off, perm, slot_of = O.route(ids, E)
+    assert cnt.tolist() == _ints(g["cnt"][0])
+    assert off.tolist() == _ints(g["off"][0])
+    assert perm.tolist() == _ints(g["perm"][0])
+    assert slot_of.tolist() == _ints(g["slot_of"][0])
+
+
+def _route_bruteforce(ids, E):
+    flat = [int(v) for v in np.asarray(ids).ravel()]
+    buckets = [[] for _ in range(E)]
+    for f, e in enumerate(flat):
+        if 0 <= e < E:
+            buckets[e].append(f)
+    perm = [f for b in buckets for f in b]
+    slot_of = [-1] * len(flat)
+    for p, f in enumerate(perm):
+        slot_of[f] = p
+    cnt = [len(b) for b in buckets]
+    off = [0]
+    for c in cnt:
+        off.append(off[-1] + c)
+    return cnt, off, perm, slot_of
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_routing_bruteforce(seed):
+    rng = np.random.default_rng(seed)
+    E = int(rng.integers(1, 40))
+    M, k = int(rng.integers(0, 50)), int(rng.integers(1, 9))
+    ids = rng.integers(-3, E + 3, (M, k)).astype(np.int32)
+    got = O.route(ids, E)
+    want = _route_bruteforce(ids, E)
+    for a, b in zip(got, want):
+        assert list(np.asarray(a)) == list(b)
+
+
+# ---------------------------------------------------------------------------- SwiGLU
+
+def test_swiglu_closed_forms():
+    sig = lambda z: 1.0 / (1.0 + math.exp(-z))
+    L = 7.0
+    cases = [  # gate, up, expected
+        (0.0, 5.0, 0.0),
+        (1.0, 2.0, 1.0 * sig(1.0) * 2.0),
+        (14.0, 14.0, 7.0 * sig(7.0) * 7.0),              # gate clamped from above, up too
+        (-14.0, -14.0, -14.0 * sig(-14.0) * -7.0),       # gate not clamped from below
+        (7.0, -7.0, 7.0 * sig(7.0) * -7.0),
+    ]
+    for g, u, want in cases:
+        assert O.swiglu(np.array([g]), np.array([u]), L)[0] == pytest.approx(want, rel=1e-15)
+    # no limit: silu(g) * u
+    g = np.linspace(-20, 20, 41)
+    u = np.linspace(-3, 3, 41)
+    assert np.allclose(O.swiglu(g, u), g / (1 + np.exp(-g)) * u, rtol=1e-15)
+    # alpha / beta form
+    assert O.swiglu(np.array([2.0]), np.array([1.0]), 7.0, 1.702, 1.0)[0] == pytest.approx(
+        2.0 * sig(1.702 * 2.0) * 2.0, rel=1e-15)
+
+
+# ---------------------------------------------------------------------------- forward
+
+def _tiny(quant, seed=0, E=6, H=64, I=32, layout=S.W13_UP_GATE):
+    cfg = {"mxfp4": S.CONFIGS["tiny_w4a8"], "nvfp4": S.CONFIGS["w4a16_nvfp4"],
+           "hybrid": S.CONFIGS["hybrid_nvfp4_nf3"]}[quant]
+    if quant == "hybrid":
+        cfg = S.MoEConfig(**{**cfg.__dict__, "n_nvfp4": 2})
+    ck = S.make_checkpoint(cfg, seed=seed, E=E, H=H, I=I, layout=layout)
+    return cfg, ck
+
+
+@pytest.mark.parametrize("quant,layout", [("mxfp4", 0), ("mxfp4", 1), ("nvfp4", 0), ("hybrid", 0)])
+def test_forward_matches_bruteforce(quant, layout):
+    cfg, ck = _tiny(quant, layout=layout)
+    rng = np.random.default_rng(11)
+    M, k = 5, 2
+    x = S.make_x(rng, M, ck.H)
+    ids = S.uniform_topk(rng, M, ck.E, k)
+    ids[4, 1] = -1
+    ids[3, 0] = ck.E          # out of range: dropped
+    w = S.router_weights(rng, M, k, "softmax", 1.0)
+    lim = 7.0 if quant == "mxfp4" else math.inf
+    a, f64 = O.moe_forward(ck, x, ids, w, lim, return_f64=True)
+    b = O.moe_forward_bruteforce(ck, x, ids, w, lim)
+    # both are fp64 sums of the same terms in different orders; the bf16 results agree except
+    # where the fp64 sum sits within rounding noise of a bf16 midpoint
+    da = C.bf16_bits_to_f64(a)
+    db = C.bf16_bits_to_f64(b)
+    assert np.mean(da == db) > 0.999
+    assert np.allclose(da, db, rtol=2 ** -7, atol=0)
+
+
+def test_forward_full_tiny_config_bruteforce():
+    cfg = S.CONFIGS["tiny_w4a8"]
+    ck = S.make_checkpoint(cfg)
+    x, ids, w = S.make_inputs(cfg, 4)
+    a = O.moe_forward(ck, x, ids, w, cfg.swiglu_limit)
+    b = O.moe_forward_bruteforce(ck, x, ids, w, cfg.swiglu_limit)
+    da, db = C.bf16_bits_to_f64(a), C.bf16_bits_to_f64(b)
+    assert np.mean(da == db) > 0.999 and np.allclose(da, db, rtol=2 ** -7, atol=0)
+
+
+def test_forward_closed_form_identity_layer():
+    """W13 up row i = one-hot at column i, gate row i = one-hot at column I+i (E2M1 1.0, scale
+    1.0); W2 row r = one-hot at column r mod I.  Then up = x^[i], gate = x^[I+i],
+    y[r] = q(h)[r mod I] and out = w * y, independent of everything else."""
+    E, H, I = 2, 64, 32
+    ck = S.Checkpoint(quant="mxfp4", E=E, H=H, I=I, layout=S.W13_UP_GATE)
+    w13 = np.zeros((E, 2 * I, H), dtype=np.uint8)
+    for i in range(I):
+        w13[:, i, i] = 0x2                 # +1.0
+        w13[:, I + i, I + i] = 0x2
+    w13[1] = np.where(w13[1] == 0x2, 0x4, 0)   # expert 1: 2.0 everywhere instead
+    ck.w13 = C.pack_fp4(w13)
+    ck.s13 = np.full((E, 2 * I, H // 32), 127, dtype=np.uint8)
+    w2 = np.zeros((E, H, I), dtype=np.uint8)
+    for r in range(H):
+        w2[:, r, r % I] = 0x2
+    ck.w2 = C.pack_fp4(w2)
+    ck.s2 = np.full((E, H, I // 32), 127, dtype=np.uint8)
+    rng = np.random.default_rng(3)
+    x = S.make_x(rng, 3, H)
+    ids = np.array([[0], [1], [-1]], dtype=np.int32)
+    w = np.array([[0.75], [1.5], [9.0]], dtype=np.float32)
+    L = 7.0
+    _, f64 = O.moe_forward(ck, x, ids, w, L, return_f64=True)
+    xv = C.bf16_bits_to_f64(x)
+    for t, scale in ((0, 1.0), (1, 2.0)):
+        q, s = C.mxfp8_quantize(xv[t][None, :])
+        xh = C.mxfp8_dequantize(q, s)[0]
+        up, gate = scale * xh[:I], scale * xh[I:]
+        h = [min(gg, L) / (1 + math.exp(-min(gg, L))) * max(-L, min(uu, L)) for gg, uu in zip(gate, up)]
+        hq, hs = C.mxfp8_quantize(np.array(h)[None, :])
+        hh = C.mxfp8_dequantize(hq, hs)[0]
+        want = float(w[t, 0]) * np.array([hh[r % I] for r in range(H)])
+        assert np.array_equal(f64[t], want)
+    assert np.all(f64[2] == 0.0)
+
+
+def _small_case(seed=21, quant="mxfp4"):
+    cfg, ck = _tiny(quant, seed=seed, E=8, H=128, I=64)
+    rng = np.random.default_rng(seed)
+    M, k = 7, 3
+    x = S.make_x(rng, M, ck.H)
+    ids = S.uniform_topk(rng, M, ck.E, k)
+    w = S.router_weights(rng, M, k, "sigmoid_norm", 2.5)
+    return ck, x, ids, w
+
+
+@pytest.mark.parametrize("quant", ["mxfp4", "nvfp4", "hybrid"])
+def test_linear_in_router_weights(quant):
+    ck, x, ids, w = _small_case(quant=quant)
+    _, f1 = O.moe_forward(ck, x, ids, w, 7.0, return_f64=True)
+    _, f2 = O.moe_forward(ck, x, ids, 3.0 * w.astype(np.float64), 7.0, return_f64=True)
+    assert np.allclose(f2, 3.0 * f1, rtol=1e-13, atol=1e-300)
+    w_a = w.copy()
+    w_a[:, 1:] = 0
+    w_b = w - w_a
+    _, fa = O.moe_forward(ck, x, ids, w_a, 7.0, return_f64=True)
+    _, fb = O.moe_forward(ck, x, ids, w_b, 7.0, return_f64=True)
+    assert np.allclose(fa + fb, f1, rtol=1e-12, atol=1e-12 * np.abs(f1).max())
+
+
+def test_padding_and_invalid_ids():
+    ck, x, ids, w = _small_case()
+    ids2 = ids.copy()
+    ids2[5:, :] = -1                 # padding rows
+    ids2[0, 2] = ck.E                # out of range id
+    ids2[1, 0] = -7
+    out = O.moe_forward(ck, x, ids2, w, 7.0)
+    assert np.all(out[5:] == 0)
+    # a dropped slot contributes exactly what weight 0 on a valid id contributes
+    ids3 = ids2.copy()
+    w3 = w.copy()
+    ids3[0, 2], w3[0, 2] = 0, 0.0
+    ids3[1, 0], w3[1, 0] = 1, 0.0
+    ids3[5:, :], w3[5:, :] = 2, 0.0
+    _, fa = O.moe_forward(ck, x, ids2, w, 7.0, return_f64=True)
+    _, fb = O.moe_forward(ck, x, ids3, w3, 7.0, return_f64=True)
+    assert np.array_equal(fa, fb)
+
+
+def test_token_order_invariance():
+    ck, x, ids, w = _small_case()
+    p = np.array([3, 0, 6, 1, 5, 2, 4])
+    a = O.moe_forward(ck, x, ids, w, 7.0)
+    b = O.moe_forward(ck, x[p], ids[p], w[p], 7.0)
+    assert np.array_equal(a[p], b)
+
+
+def test_swapped_w13_halves_detected():
+    cfg = S.CONFIGS["tiny_w4a8"]
+    ck = S.make_checkpoint(cfg)
+    x, ids, w = S.make_inputs(cfg, 4)
+    a, fa = O.moe_forward(ck, x, ids, w, 7.0, return_f64=True)
+    ck.layout = S.W13_GATE_UP
+    b = O.moe_forward(ck, x, ids, w, 7.0)
+    rel, _ = O.row_errors(b, fa)
+    assert np.all(rel > 0.2)          # far outside the 5e-3 bound
+
+
+def test_zero_expert_contributes_nothing():
+    ck, x, ids, w = _small_case()
+    e = int(ids[0, 0])
+    ck.w13 = ck.w13.copy()
+    ck.w13[e] = 0
+    _, fa = O.moe_forward(ck, x, ids, w, 7.0, return_f64=True)
+    w0 = np.where(ids == e, 0.0, w)
+    _, fb = O.moe_forward(ck, x, ids, w0, 7.0, return_f64=True)
+    assert np.array_equal(fa, fb)
+
+
+def test_row_subset_matches_full():
+    ck, x, ids, w = _small_case()
+    full = O.moe_forward(ck, x, ids, w, 7.0)
+    sub = O.moe_forward(ck, x, ids, w, 7.0, rows=[1, 4])
+    assert np.array_equal(sub[[1, 4]], full[[1, 4]])
+
+
+def test_row_errors_bound_helper():
+    ref = np.array([[1.0, 2.0, 3.0], [0.0, 0.0, 0.0]])
+    got = C.f64_to_bf16_bits(ref)
+    rel, mx = O.row_errors(got, ref)
+    assert rel.tolist() == [0.0, 0.0] and mx.tolist() == [0.0, 0.0]
+    bad = C.f64_to_bf16_bits(ref + np.array([[0.0, 0.0, 0.5], [0.0, 1.0, 0.0]]))
+    rel, mx = O.row_errors(bad, ref)
+    assert rel[0] > 0.1 and np.isinf(rel[1])
+
+
+def test_synth_recipes():
+    cfg = S.CONFIGS["decode_w4a8"]
+    ids, w = S.make_routing(cfg, 16)
+    assert ids.shape == (16, 6) and np.all(ids[12:] == -1) and np.all(ids[:12] >= 0)
+    assert np.allclose(w.sum(1), 2.5, rtol=1e-6)
+    assert all(len(set(r)) == 6 for r in ids[:12].tolist())
+    cfg = S.CONFIGS["prefill_w4a8_ep_i1152"]
+    ids, w = S.make_routing(cfg, 128)
+    assert ids.min() >= 0 and ids.max() < 192
+    cfg = S.CONFIGS["hybrid_nvfp4_nf3"]
+    ck = S.make_checkpoint(cfg, E=16, H=64, I=32)
+    assert (ck.tier == S.TIER_NVFP4).sum() == 16 or ck.nv.E + ck.nf.E == 16
