@@ -1,0 +1,192 @@
+/*
+ * moe_gb300.h - C ABI of the GB300 (sm_103a) routed mixture-of-experts expert computation.
+ *
+ *   out[t] = sum_j w[t,j] * expert_{id[t,j]}(x[t]),
+ *   expert(x) = W2 . act(gate, up),  [up; gate] = W13 . x   (fc1, SwiGLU, fc2)
+ *
+ * Sources (web pages on the routed-MoE serving path):
+ *   - "moe_b12x_next.py" (sglang adapter, docker-images/mia-tp4): module docstring (W4A8 =
+ *     MXFP4 weights + in-kernel MXFP8 activations; w13 stacked [w3 (up); w1 (gate)]; ids
+ *     outside [0, E) skipped, padding rows give 0; deterministic combine = per-slot route
+ *     buffer + top-k sum), class _Geometry (plan_weights -> prepare_weights -> plan_execution
+ *     -> bind -> run), _convert_layer (checkpoint shapes).
+ *   - "hybrid_loader.py" (vLLM, docker-images/glm52-nf3-hybrid): NVFP4 / NF3 tiers, _unpack_nf3,
+ *     _apply_ref (reference two-pass forward), the union staging + single top-k sum.
+ *   - vLLM API page "fused_moe/b12x", class B12xExperts: _prepare_experts, _swiglu_params,
+ *     apply.
+ *
+ * Conventions for every entry point:
+ *   - All tensors are contiguous row-major.  Device pointers are CUDA device memory of the
+ *     current device; "host" pointers are ordinary host memory.  The library never allocates
+ *     device memory: the caller owns the prepared-weight buffer and the scratch buffer and
+ *     passes their sizes (obtained from the *_bytes queries).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Calls return a moe_status; nothing is printed.  On error no kernel was launched unless the
+ *     status is MOE_ERR_CUDA (a launch or copy failed; cudaGetLastError was cleared).
+ *   - Handles are opaque host objects; destroy them with the matching moe_destroy_* call.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = 1,          /* null pointer, negative size, buffer too small            */
+  MOE_ERR_SHAPE = 2,        /* E/H/I/top-k outside what the kernels support             */
+  MOE_ERR_UNSUPPORTED = 3,  /* quant mode / option combination not supported            */
+  MOE_ERR_CAPACITY = 4,     /* M > max_m of the plan                                    */
+  MOE_ERR_CAPTURING = 5,    /* planning / preparing while the stream is being captured  */
+  MOE_ERR_CUDA = 6,         /* a CUDA runtime call failed                               */
+  MOE_ERR_TIMEOUT = 7,      /* a bounded device-side wait gave up (see moe_get_device_error) */
+  MOE_ERR_DEVICE = 8        /* a device-side check failed (see moe_get_device_error)    */
+} moe_status;
+
+typedef enum {
+  /* MXFP4 weights (E2M1 + E8M0 per 32 along K), activations quantised in-kernel to MXFP8
+   * (E4M3 + E8M0 per 32); "W4A8" of moe_b12x_next.py, module docstring. */
+  MOE_W4A8_MXFP4 = 0,
+  /* NVFP4 weights (E2M1 + E4M3 per 16 + one fp32 global per expert and matrix), bf16
+   * activations; the kept tier of hybrid_loader.py (`_build_kept_b12x`, use_a16). */
+  MOE_W4A16_NVFP4 = 1,
+  /* Per-expert tier map: NVFP4 (tier 4) or NF3 (tier 3, 8-entry LUT x E4M3 per 32), bf16
+   * activations, both tiers summed by one top-k sum (hybrid_loader.py, class docstring and
+   * the union-staging path of `_apply_b12x_nf3`). */
+  MOE_W4A16_HYBRID = 2
+} moe_quant_mode;
+
+typedef enum {
+  MOE_W13_UP_GATE = 0,  /* fc1 rows [w3 (up); w1 (gate)]: moe_b12x_next.py docstring       */
+  MOE_W13_GATE_UP = 1   /* fc1 rows [w1 (gate); w3 (up)]: hybrid_loader.py weight_loader    */
+} moe_w13_layout;
+
+#define MOE_TIER_NVFP4 4
+#define MOE_TIER_NF3 3
+
+typedef struct moe_weight_plan moe_weight_plan;
+typedef struct moe_prepared moe_prepared;
+typedef struct moe_plan_s moe_plan_t;
+
+/* Checkpoint-layout expert tensors (device pointers, contiguous), as listed by
+ * moe_b12x_next.py `_convert_layer` (MXFP4) and hybrid_loader.py `create_weights` (NVFP4 / NF3).
+ * For MOE_W4A16_HYBRID the fp4 fields hold the NVFP4 tier compacted over its experts (in
+ * ascending expert id) and the nf3 fields the NF3 tier likewise.
+ *   MXFP4: w13 [E, 2I, H/2] u8 (element 2j = low nibble of byte j), s13 [E, 2I, H/32] u8 E8M0,
+ *          w2 [E, H, I/2] u8, s2 [E, H, I/32] u8 E8M0; g13 = g2 = NULL.
+ *   NVFP4: w13 [E4, 2I, H/2], s13 [E4, 2I, H/16] u8 E4M3, g13 [E4] f32,
+ *          w2 [E4, H, I/2],   s2 [E4, H, I/16] u8 E4M3,  g2 [E4] f32.
+ *   NF3:   nf_w13 [E3, 2I, 3H/8] u8 (8 codes per 3 bytes, hybrid_loader.py _unpack_nf3),
+ *          nf_s13 [E3, 2I, H/32] u8 E4M3, nf_w2 [E3, H, 3I/8] u8, nf_s2 [E3, H, I/32] u8 E4M3. */
+typedef struct {
+  const void* w13;
+  const void* s13;
+  const float* g13;
+  const void* w2;
+  const void* s2;
+  const float* g2;
+  const void* nf_w13;
+  const void* nf_s13;
+  const void* nf_w2;
+  const void* nf_s2;
+} moe_checkpoint;
+
+/* Weight plan: geometry and quant mode of one layer's experts (moe_b12x_next.py,
+ * `_Geometry.__init__` -> fm.plan_weights; B12xExperts `_prepare_experts`).
+ *   E, H, I   experts, hidden size, intermediate size (per rank).  Requires H % 128 == 0,
+ *             I % 64 == 0 (moe_b12x_next.py `create_weights` checks), E >= 1.
+ *   tier_of_expert  host [E] int8 of MOE_TIER_NVFP4 / MOE_TIER_NF3 for MOE_W4A16_HYBRID,
+ *             NULL otherwise.  Copied; the caller keeps ownership.
+ * Errors: MOE_ERR_ARG (null out), MOE_ERR_SHAPE, MOE_ERR_UNSUPPORTED. */
+moe_status moe_plan_weights(int E, int H, int I, int quant_mode, int w13_layout,
+                            const int8_t* tier_of_expert, moe_weight_plan** out);
+
+/* Size in bytes of the device buffer that moe_prepare_weights fills. */
+moe_status moe_prepared_bytes(const moe_weight_plan* wp, size_t* bytes);
+
+/* Repack checkpoint bytes into the device layout the kernels read (moe_b12x_next.py module
+ * docstring: "the checkpoint bytes are repacked ... into ... PreparedExperts"; B12xExperts
+ * `_prepare_experts`, incl. the FP4 zero-sign canonicalisation -0 -> +0).
+ *   src       device checkpoint tensors (read only; not modified).
+ *   dst       device buffer of at least moe_prepared_bytes bytes, 256-byte aligned; owned by the
+ *             caller and referenced (not copied) by the returned handle, so it must outlive it.
+ *   stream    the repack kernels run on it; the handle is usable by moe_run on the same stream
+ *             right away (stream order).
+ * Errors: MOE_ERR_ARG, MOE_ERR_CAPTURING (stream is capturing: B12xExperts refuses to
+ * prepare under graph capture), MOE_ERR_CUDA. */
+moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* src, void* dst,
+                               size_t dst_bytes, void* stream, moe_prepared** out);
+
+/* Execution plan for calls of up to max_m tokens (moe_b12x_next.py `_Geometry.build`:
+ * fm.plan_execution per capacity; knob _DETERMINISTIC).
+ *   topk          router top-k (1..16).
+ *   max_m         capacity; moe_run with M > max_m returns MOE_ERR_CAPACITY.
+ *   swiglu_limit  clamp of the SwiGLU (gate' = min(gate, L), up' = clamp(up, -L, L)); +inf for
+ *                 no clamp.  alpha = 1, beta = 0 unless set with moe_plan_set_swiglu_alpha_beta.
+ *   deterministic 0: fp32 atomic combine (run-to-run ulp differences possible);
+ *                 1: per-slot route buffer + fixed-order top-k sum (bit-stable).
+ * Errors: MOE_ERR_ARG, MOE_ERR_SHAPE, MOE_ERR_UNSUPPORTED. */
+moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, float swiglu_limit,
+                    int deterministic, moe_plan_t** out);
+
+/* Optional alpha / beta of the clamped SwiGLU, h = gate' * sigmoid(alpha gate') * (up' + beta)
+ * (B12xExperts `_swiglu_params`, SWIGLUOAI form). */
+moe_status moe_plan_set_swiglu_alpha_beta(moe_plan_t* plan, float alpha, float beta);
+
+/* Size in bytes of the device scratch buffer moe_run needs (routing tables, quantised
+ * activations, the fc1 -> fc2 intermediate, the combine buffer). */
+moe_status moe_scratch_bytes(const moe_plan_t* plan, size_t* bytes);
+
+/* One MoE layer call (moe_b12x_next.py `_Geometry._run` -> fm.run; hybrid_loader.py
+ * run_w4a16_moe; B12xExperts `apply`).  All pointers are device memory:
+ *   x            [M, H] bf16 hidden states.
+ *   topk_ids     [M, topk] int32; ids outside [0, E) (e.g. -1 padding) contribute nothing.
+ *   topk_weights [M, topk] fp32.
+ *   out          [M, H] bf16, fully overwritten (rows without a valid id become 0).
+ *   scratch      >= moe_scratch_bytes bytes, 256-byte aligned; its contents need no
+ *                initialisation and are clobbered.  Calls that share a scratch buffer must be
+ *                stream-ordered.
+ * No host synchronisation and no allocation: the call can be captured in a CUDA graph.
+ * M == 0 is a no-op.  Errors: MOE_ERR_ARG, MOE_ERR_CAPACITY, MOE_ERR_CUDA. */
+moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* scratch,
+                   size_t scratch_bytes, const void* x, const int32_t* topk_ids,
+                   const float* topk_weights, void* out, int M, void* stream);
+
+/* Size of the device staging buffer moe_run_host needs (x, ids, weights and out of max_m rows). */
+moe_status moe_io_bytes(const moe_plan_t* plan, size_t* bytes);
+
+/* moe_run with HOST inputs and output: copies x / ids / weights host -> device into `io`
+ * (>= moe_io_bytes, device), runs the layer, copies out device -> host and synchronises the
+ * stream before returning.  Pinned host memory makes the copies asynchronous DMA. */
+moe_status moe_run_host(const moe_plan_t* plan, const moe_prepared* weights, void* scratch,
+                        size_t scratch_bytes, void* io, size_t io_bytes, const void* x_host,
+                        const int32_t* ids_host, const float* w_host, void* out_host, int M,
+                        void* stream);
+
+/* Reads and clears the device error word kept in `scratch` (synchronises `stream`).
+ * *code = 0 when no device-side check failed since the last read. */
+moe_status moe_get_device_error(const moe_plan_t* plan, void* scratch, void* stream, int* code);
+
+/* Test hooks: after a moe_run on `stream`, copy routing tables / quantised activations of the
+ * last call to host buffers (synchronises).  cnt [E], off [E+1], perm [S], slot_of [M*topk]
+ * where S = off[E]; xq [M, H] E4M3 codes, xs [M, H/32] E8M0 bytes (W4A8 only). */
+moe_status moe_debug_routing(const moe_plan_t* plan, void* scratch, int M, int32_t* cnt,
+                             int32_t* off, int32_t* perm, int32_t* slot_of, void* stream);
+moe_status moe_debug_actq(const moe_plan_t* plan, void* scratch, int M, uint8_t* xq, uint8_t* xs,
+                          void* stream);
+
+void moe_destroy_weight_plan(moe_weight_plan* wp);
+void moe_destroy_prepared(moe_prepared* p);
+void moe_destroy_plan(moe_plan_t* plan);
+const char* moe_status_str(moe_status s);
+/* Library version string, e.g. "moe_gb300 0.1 sm_103a". */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,421 @@
+// api.cu - host implementation of the C ABI declared in include/moe_gb300.h: plans, buffer
+// sizing, argument checks and the launch sequence of one MoE call.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "moe_common.cuh"
+#include "../../include/moe_gb300.h"
+
+namespace moe {
+// route.cu
+cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int max_tiles,
+                         const RunPtrs& r, cudaStream_t st);
+cudaError_t launch_actq(const void* x, int M, int H, const RunPtrs& r, bool quant_x,
+                        size_t acc_elems, cudaStream_t st);
+// gemm_simt.cu
+struct SimtArgs;
+cudaError_t launch_simt_pipeline(const DevWeights& w, const RunPtrs& r, const PlanDims& d,
+                                 int max_tiles, const void* x, const float* topk_w, void* out,
+                                 int M, cudaStream_t st);
+// prepare.cu
+cudaError_t launch_repack_rows(const void* src, void* dst, int E, int halves, int rows,
+                               int src_cols, int dst_cols, int layout, int canon, cudaStream_t st);
+cudaError_t launch_repack_sf_atoms(const void* src, void* dst, int E, int halves, int rows,
+                                   int kblocks, int row_tiles, int k_tiles, int layout,
+                                   cudaStream_t st);
+cudaError_t launch_repack_nf3(const void* src, void* dst, int E, int halves, int rows, int src_k,
+                              int dst_k, int layout, cudaStream_t st);
+}  // namespace moe
+
+using namespace moe;
+
+struct moe_weight_plan {
+  int E, H, I, Ip, quant, layout;
+  int E4, E3;
+  std::vector<int32_t> tier_map;  // (tier << 24) | local
+  // section offsets in the prepared buffer
+  size_t w13, s13, w2, s2, g13, g2, nf_w13, nf_s13, nf_w2, nf_s2, tmap, total;
+};
+
+struct moe_prepared {
+  DevWeights w;
+};
+
+struct moe_plan_s {
+  PlanDims d;
+  Scratch s;
+  size_t io_x, io_ids, io_w, io_out, io_total;
+};
+
+namespace {
+
+bool capturing(cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return false;
+  return cs != cudaStreamCaptureStatusNone;
+}
+
+moe_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  (void)cudaGetLastError();
+  return MOE_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status check_geometry(int E, int H, int I, int quant) {
+  if (E < 1 || E > 1024) return MOE_ERR_SHAPE;
+  if (H < 128 || H % 128 != 0) return MOE_ERR_SHAPE;
+  if (I < 64 || I % 64 != 0) return MOE_ERR_SHAPE;
+  if ((long long)H * H > (1LL << 40) || (long long)I > (1 << 20)) return MOE_ERR_SHAPE;
+  if (quant < 0 || quant > 2) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_str(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_SHAPE: return "unsupported shape";
+    case MOE_ERR_UNSUPPORTED: return "unsupported mode";
+    case MOE_ERR_CAPACITY: return "M exceeds the plan capacity";
+    case MOE_ERR_CAPTURING: return "stream is capturing";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+const char* moe_version(void) { return "moe_gb300 0.1 sm_103a"; }
+
+moe_status moe_plan_weights(int E, int H, int I, int quant_mode, int w13_layout,
+                            const int8_t* tier_of_expert, moe_weight_plan** out) {
+  if (out == nullptr) return MOE_ERR_ARG;
+  *out = nullptr;
+  moe_status st = check_geometry(E, H, I, quant_mode);
+  if (st != MOE_OK) return st;
+  if (w13_layout != MOE_W13_UP_GATE && w13_layout != MOE_W13_GATE_UP) return MOE_ERR_ARG;
+  if ((quant_mode == MOE_W4A16_HYBRID) != (tier_of_expert != nullptr)) return MOE_ERR_ARG;
+  moe_weight_plan* wp = new (std::nothrow) moe_weight_plan();
+  if (wp == nullptr) return MOE_ERR_ARG;
+  wp->E = E; wp->H = H; wp->I = I; wp->Ip = (int)align_up((size_t)I, 128);
+  wp->quant = quant_mode; wp->layout = w13_layout;
+  wp->E4 = E; wp->E3 = 0;
+  if (quant_mode == MOE_W4A16_HYBRID) {
+    wp->E4 = wp->E3 = 0;
+    wp->tier_map.resize(E);
+    for (int e = 0; e < E; ++e) {
+      if (tier_of_expert[e] == MOE_TIER_NVFP4) {
+        wp->tier_map[e] = (MOE_TIER_NVFP4 << 24) | wp->E4++;
+      } else if (tier_of_expert[e] == MOE_TIER_NF3) {
+        wp->tier_map[e] = (MOE_TIER_NF3 << 24) | wp->E3++;
+      } else {
+        delete wp;
+        return MOE_ERR_ARG;
+      }
+    }
+  }
+  const size_t H_ = H, I_ = I, Ip = wp->Ip;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
+  const size_t E4 = wp->E4, E3 = wp->E3;
+  wp->w13 = take(E4 * 2 * I_ * H_ / 2);
+  wp->w2 = take(E4 * H_ * Ip / 2);
+  if (quant_mode == MOE_W4A8_MXFP4) {
+    wp->s13 = take(E4 * 2 * (size_t)cdiv(I, 128) * (H_ / 128) * 512);
+    wp->s2 = take(E4 * (H_ / 128) * (Ip / 128) * 512);
+    wp->g13 = wp->g2 = 0;
+  } else {
+    wp->s13 = take(E4 * 2 * I_ * H_ / 16);
+    wp->s2 = take(E4 * H_ * Ip / 16);
+    wp->g13 = take(E4 * 4);
+    wp->g2 = take(E4 * 4);
+  }
+  wp->nf_w13 = take(E3 * 2 * I_ * 3 * H_ / 8);
+  wp->nf_s13 = take(E3 * 2 * I_ * H_ / 32);
+  wp->nf_w2 = take(E3 * H_ * 3 * Ip / 8);
+  wp->nf_s2 = take(E3 * H_ * Ip / 32);
+  wp->tmap = take((size_t)E * 4);
+  wp->total = o;
+  *out = wp;
+  return MOE_OK;
+}
+
+moe_status moe_prepared_bytes(const moe_weight_plan* wp, size_t* bytes) {
+  if (wp == nullptr || bytes == nullptr) return MOE_ERR_ARG;
+  *bytes = wp->total;
+  return MOE_OK;
+}
+
+moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* src, void* dst,
+                               size_t dst_bytes, void* stream, moe_prepared** out) {
+  if (wp == nullptr || src == nullptr || dst == nullptr || out == nullptr) return MOE_ERR_ARG;
+  *out = nullptr;
+  if (dst_bytes < wp->total || !aligned(dst, 256)) return MOE_ERR_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (capturing(st)) return MOE_ERR_CAPTURING;
+  const bool fp4 = wp->E4 > 0, nf3 = wp->E3 > 0;
+  if (fp4 && (src->w13 == nullptr || src->s13 == nullptr || src->w2 == nullptr ||
+              src->s2 == nullptr))
+    return MOE_ERR_ARG;
+  if (fp4 && wp->quant != MOE_W4A8_MXFP4 && (src->g13 == nullptr || src->g2 == nullptr))
+    return MOE_ERR_ARG;
+  if (nf3 && (src->nf_w13 == nullptr || src->nf_s13 == nullptr || src->nf_w2 == nullptr ||
+              src->nf_s2 == nullptr))
+    return MOE_ERR_ARG;
+  uint8_t* base = static_cast<uint8_t*>(dst);
+  const int E4 = wp->E4, E3 = wp->E3, H = wp->H, I = wp->I, Ip = wp->Ip, L = wp->layout;
+  cudaError_t e = cudaSuccess;
+  auto chk = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
+  if (fp4) {
+    chk(launch_repack_rows(src->w13, base + wp->w13, E4, 2, I, H / 2, H / 2, L, 1, st));
+    chk(launch_repack_rows(src->w2, base + wp->w2, E4, 1, H, I / 2, Ip / 2, L, 1, st));
+    if (wp->quant == MOE_W4A8_MXFP4) {
+      chk(launch_repack_sf_atoms(src->s13, base + wp->s13, E4, 2, I, H / 32, cdiv(I, 128),
+                                 H / 128, L, st));
+      chk(launch_repack_sf_atoms(src->s2, base + wp->s2, E4, 1, H, I / 32, H / 128, Ip / 128, L,
+                                 st));
+    } else {
+      chk(launch_repack_rows(src->s13, base + wp->s13, E4, 2, I, H / 16, H / 16, L, 0, st));
+      chk(launch_repack_rows(src->s2, base + wp->s2, E4, 1, H, I / 16, Ip / 16, L, 0, st));
+      chk(cudaMemcpyAsync(base + wp->g13, src->g13, (size_t)E4 * 4, cudaMemcpyDeviceToDevice, st));
+      chk(cudaMemcpyAsync(base + wp->g2, src->g2, (size_t)E4 * 4, cudaMemcpyDeviceToDevice, st));
+    }
+  }
+  if (nf3) {
+    chk(launch_repack_nf3(src->nf_w13, base + wp->nf_w13, E3, 2, I, H, H, L, st));
+    chk(launch_repack_nf3(src->nf_w2, base + wp->nf_w2, E3, 1, H, I, Ip, L, st));
+    chk(launch_repack_rows(src->nf_s13, base + wp->nf_s13, E3, 2, I, H / 32, H / 32, L, 0, st));
+    chk(launch_repack_rows(src->nf_s2, base + wp->nf_s2, E3, 1, H, I / 32, Ip / 32, L, 0, st));
+  }
+  if (!wp->tier_map.empty())
+    chk(cudaMemcpyAsync(base + wp->tmap, wp->tier_map.data(), wp->tier_map.size() * 4,
+                        cudaMemcpyHostToDevice, st));
+  if (e != cudaSuccess) return cuda_status(e);
+  moe_prepared* p = new (std::nothrow) moe_prepared();
+  if (p == nullptr) return MOE_ERR_ARG;
+  DevWeights& w = p->w;
+  w.quant = wp->quant; w.E = wp->E; w.H = H; w.I = I; w.Ip = Ip; w.E4 = E4; w.E3 = E3;
+  w.w13 = base + wp->w13; w.s13 = base + wp->s13; w.w2 = base + wp->w2; w.s2 = base + wp->s2;
+  if (wp->quant != MOE_W4A8_MXFP4) {
+    w.g13 = reinterpret_cast<const float*>(base + wp->g13);
+    w.g2 = reinterpret_cast<const float*>(base + wp->g2);
+  }
+  w.nf_w13 = base + wp->nf_w13; w.nf_s13 = base + wp->nf_s13;
+  w.nf_w2 = base + wp->nf_w2; w.nf_s2 = base + wp->nf_s2;
+  w.tier_map = wp->tier_map.empty() ? nullptr : reinterpret_cast<const int32_t*>(base + wp->tmap);
+  *out = p;
+  return MOE_OK;
+}
+
+moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, float swiglu_limit,
+                    int deterministic, moe_plan_t** out) {
+  if (out == nullptr) return MOE_ERR_ARG;
+  *out = nullptr;
+  moe_status st = check_geometry(E, H, I, quant_mode);
+  if (st != MOE_OK) return st;
+  if (topk < 1 || topk > 16 || max_m < 1 || max_m > (1 << 20)) return MOE_ERR_SHAPE;
+  if (std::isnan(swiglu_limit) || swiglu_limit <= 0.f) return MOE_ERR_ARG;
+  moe_plan_t* p = new (std::nothrow) moe_plan_t();
+  if (p == nullptr) return MOE_ERR_ARG;
+  PlanDims& d = p->d;
+  d.E = E; d.H = H; d.I = I; d.Ip = (int)align_up((size_t)I, 128); d.topk = topk; d.max_m = max_m;
+  d.quant = quant_mode; d.deterministic = deterministic ? 1 : 0;
+  d.limit = swiglu_limit; d.alpha = 1.f; d.beta = 0.f;
+  const size_t Sm = (size_t)max_m * topk;
+  Scratch& s = p->s;
+  s.max_tiles = (int)std::min<size_t>(Sm, (Sm + kSimtSlots - 1) / kSimtSlots +
+                                              std::min<size_t>((size_t)E, Sm));
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
+  const bool a8 = quant_mode == MOE_W4A8_MXFP4;
+  s.ctrl = take(64 * 4);
+  s.cnt = take((size_t)E * 4);
+  s.off = take((size_t)(E + 1) * 4);
+  s.perm = take(Sm * 4);
+  s.slot_of = take(Sm * 4);
+  s.tiles = take((size_t)s.max_tiles * 16);
+  s.xq = a8 ? take((size_t)max_m * H) : 0;
+  s.xs = a8 ? take((size_t)max_m * H / 32) : 0;
+  s.g = take(Sm * 2 * I * 4);
+  s.hq = a8 ? take(Sm * d.Ip) : 0;
+  s.hs = a8 ? take(Sm * d.Ip / 32) : 0;
+  s.h16 = a8 ? 0 : take(Sm * d.Ip * 2);
+  s.acc = d.deterministic ? 0 : take((size_t)max_m * H * 4);
+  s.rbuf = d.deterministic ? take(Sm * H * 2) : 0;
+  s.total = o;
+  o = 0;
+  p->io_x = take((size_t)max_m * H * 2);
+  p->io_ids = take(Sm * 4);
+  p->io_w = take(Sm * 4);
+  p->io_out = take((size_t)max_m * H * 2);
+  p->io_total = o;
+  *out = p;
+  return MOE_OK;
+}
+
+moe_status moe_plan_set_swiglu_alpha_beta(moe_plan_t* plan, float alpha, float beta) {
+  if (plan == nullptr || std::isnan(alpha) || std::isnan(beta)) return MOE_ERR_ARG;
+  plan->d.alpha = alpha;
+  plan->d.beta = beta;
+  return MOE_OK;
+}
+
+moe_status moe_scratch_bytes(const moe_plan_t* plan, size_t* bytes) {
+  if (plan == nullptr || bytes == nullptr) return MOE_ERR_ARG;
+  *bytes = plan->s.total;
+  return MOE_OK;
+}
+
+moe_status moe_io_bytes(const moe_plan_t* plan, size_t* bytes) {
+  if (plan == nullptr || bytes == nullptr) return MOE_ERR_ARG;
+  *bytes = plan->io_total;
+  return MOE_OK;
+}
+
+static RunPtrs resolve(const moe_plan_t* plan, void* scratch) {
+  uint8_t* b = static_cast<uint8_t*>(scratch);
+  const Scratch& s = plan->s;
+  const bool a8 = plan->d.quant == MOE_W4A8_MXFP4;
+  RunPtrs r;
+  r.ctrl = reinterpret_cast<int32_t*>(b + s.ctrl);
+  r.cnt = reinterpret_cast<int32_t*>(b + s.cnt);
+  r.off = reinterpret_cast<int32_t*>(b + s.off);
+  r.perm = reinterpret_cast<int32_t*>(b + s.perm);
+  r.slot_of = reinterpret_cast<int32_t*>(b + s.slot_of);
+  r.tiles = reinterpret_cast<int4*>(b + s.tiles);
+  r.xq = a8 ? b + s.xq : nullptr;
+  r.xs = a8 ? b + s.xs : nullptr;
+  r.g = reinterpret_cast<float*>(b + s.g);
+  r.hq = a8 ? b + s.hq : nullptr;
+  r.hs = a8 ? b + s.hs : nullptr;
+  r.h16 = a8 ? nullptr : reinterpret_cast<__nv_bfloat16*>(b + s.h16);
+  r.acc = plan->d.deterministic ? nullptr : reinterpret_cast<float*>(b + s.acc);
+  r.rbuf = plan->d.deterministic ? reinterpret_cast<__nv_bfloat16*>(b + s.rbuf) : nullptr;
+  return r;
+}
+
+moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* scratch,
+                   size_t scratch_bytes, const void* x, const int32_t* topk_ids,
+                   const float* topk_weights, void* out, int M, void* stream) {
+  if (plan == nullptr || weights == nullptr) return MOE_ERR_ARG;
+  if (M < 0) return MOE_ERR_ARG;
+  if (M > plan->d.max_m) return MOE_ERR_CAPACITY;
+  if (M == 0) return MOE_OK;
+  if (scratch == nullptr || x == nullptr || topk_ids == nullptr || topk_weights == nullptr ||
+      out == nullptr)
+    return MOE_ERR_ARG;
+  if (scratch_bytes < plan->s.total || !aligned(scratch, 256) || !aligned(x, 16) ||
+      !aligned(out, 16) || !aligned(topk_ids, 4) || !aligned(topk_weights, 4))
+    return MOE_ERR_ARG;
+  const PlanDims& d = plan->d;
+  const DevWeights& w = weights->w;
+  if (w.E != d.E || w.H != d.H || w.I != d.I || w.quant != d.quant) return MOE_ERR_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const RunPtrs r = resolve(plan, scratch);
+  cudaError_t e = launch_route(topk_ids, M * d.topk, d.E, kSimtSlots, plan->s.max_tiles, r, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  const bool a8 = d.quant == MOE_W4A8_MXFP4;
+  if (a8 || !d.deterministic) {
+    e = launch_actq(x, M, d.H, r, a8, d.deterministic ? 0 : (size_t)M * d.H, st);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  e = launch_simt_pipeline(w, r, d, plan->s.max_tiles, x, topk_weights, out, M, st);
+  return cuda_status(e);
+}
+
+moe_status moe_run_host(const moe_plan_t* plan, const moe_prepared* weights, void* scratch,
+                        size_t scratch_bytes, void* io, size_t io_bytes, const void* x_host,
+                        const int32_t* ids_host, const float* w_host, void* out_host, int M,
+                        void* stream) {
+  if (plan == nullptr) return MOE_ERR_ARG;
+  if (M < 0) return MOE_ERR_ARG;
+  if (M > plan->d.max_m) return MOE_ERR_CAPACITY;
+  if (M == 0) return MOE_OK;
+  if (io == nullptr || io_bytes < plan->io_total || !aligned(io, 256) || x_host == nullptr ||
+      ids_host == nullptr || w_host == nullptr || out_host == nullptr)
+    return MOE_ERR_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* b = static_cast<uint8_t*>(io);
+  const size_t xb = (size_t)M * plan->d.H * 2, kb = (size_t)M * plan->d.topk * 4;
+  cudaError_t e = cudaMemcpyAsync(b + plan->io_x, x_host, xb, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(b + plan->io_ids, ids_host, kb, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(b + plan->io_w, w_host, kb, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  moe_status s = moe_run(plan, weights, scratch, scratch_bytes, b + plan->io_x,
+                         reinterpret_cast<const int32_t*>(b + plan->io_ids),
+                         reinterpret_cast<const float*>(b + plan->io_w), b + plan->io_out, M,
+                         stream);
+  if (s != MOE_OK) return s;
+  e = cudaMemcpyAsync(out_host, b + plan->io_out, xb, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return cuda_status(e);
+}
+
+moe_status moe_get_device_error(const moe_plan_t* plan, void* scratch, void* stream, int* code) {
+  if (plan == nullptr || scratch == nullptr || code == nullptr) return MOE_ERR_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  int32_t* ctrl = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + plan->s.ctrl);
+  cudaError_t e = cudaMemcpyAsync(&v, ctrl, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctrl, 0, 4, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_status(e);
+  *code = v;
+  if (v & kErrTimeout) return MOE_ERR_TIMEOUT;
+  if (v != 0) return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+moe_status moe_debug_routing(const moe_plan_t* plan, void* scratch, int M, int32_t* cnt,
+                             int32_t* off, int32_t* perm, int32_t* slot_of, void* stream) {
+  if (plan == nullptr || scratch == nullptr || M < 0 || M > plan->d.max_m) return MOE_ERR_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const RunPtrs r = resolve(plan, scratch);
+  const int E = plan->d.E;
+  std::vector<int32_t> hoff(E + 1);
+  cudaError_t e = cudaMemcpyAsync(hoff.data(), r.off, (E + 1) * 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_status(e);
+  const int S = hoff[E];
+  if (S < 0 || S > M * plan->d.topk) return MOE_ERR_DEVICE;
+  if (off) std::memcpy(off, hoff.data(), (E + 1) * 4);
+  if (cnt) e = cudaMemcpyAsync(cnt, r.cnt, E * 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && perm && S > 0)
+    e = cudaMemcpyAsync(perm, r.perm, (size_t)S * 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && slot_of && M > 0)
+    e = cudaMemcpyAsync(slot_of, r.slot_of, (size_t)M * plan->d.topk * 4, cudaMemcpyDeviceToHost,
+                        st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return cuda_status(e);
+}
+
+moe_status moe_debug_actq(const moe_plan_t* plan, void* scratch, int M, uint8_t* xq, uint8_t* xs,
+                          void* stream) {
+  if (plan == nullptr || scratch == nullptr || M < 0 || M > plan->d.max_m) return MOE_ERR_ARG;
+  if (plan->d.quant != MOE_W4A8_MXFP4) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const RunPtrs r = resolve(plan, scratch);
+  cudaError_t e = cudaSuccess;
+  if (xq) e = cudaMemcpyAsync(xq, r.xq, (size_t)M * plan->d.H, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && xs)
+    e = cudaMemcpyAsync(xs, r.xs, (size_t)M * plan->d.H / 32, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return cuda_status(e);
+}
+
+void moe_destroy_weight_plan(moe_weight_plan* wp) { delete wp; }
+void moe_destroy_prepared(moe_prepared* p) { delete p; }
+void moe_destroy_plan(moe_plan_t* plan) { delete plan; }
+
+}  // extern "C"

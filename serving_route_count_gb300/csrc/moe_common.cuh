@@ -1,0 +1,161 @@
+// moe_common.cuh - device layouts, scratch layout and small device helpers shared by the
+// kernels of the GB300 routed-MoE library.  Host and device code include it.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_fp4.h>
+#include <stdint.h>
+#include <stddef.h>
+
+namespace moe {
+
+constexpr int kQuantW4A8 = 0;
+constexpr int kQuantNVFP4 = 1;
+constexpr int kQuantHybrid = 2;
+constexpr int kTierNVFP4 = 4;
+constexpr int kTierNF3 = 3;
+
+// Error word bits written by device-side checks (never a trap).
+constexpr int kErrRouteBounds = 1;   // a routing index fell outside its table
+constexpr int kErrTimeout = 2;       // a bounded wait gave up
+constexpr int kErrTileOverflow = 4;  // more GEMM tiles than the plan reserved
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+__host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// ----------------------------------------------------------------------------------------------
+// Prepared (device) weight layout.
+//
+// fc1 rows are stored as two halves [half 0 = up][half 1 = gate] whatever the checkpoint order,
+// each half I rows of H (K) elements.  fc2 rows are H rows of Ip = round_up(I, 128) elements
+// (zero codes beyond I), because the packed-FP4 TMA format needs a row length that is a
+// multiple of 128 elements.
+//
+// FP4 codes: rows of K/2 bytes, element 2j in the low nibble of byte j (checkpoint order).
+// MXFP4 E8M0 scales ("SF atoms"): for each 128-row tile and each 128-wide K tile, 512 bytes
+//   byte(r, kb) = (r % 32) * 16 + (r / 32) * 4 + kb     (r < 128 in the tile, kb < 4 blocks of 32)
+//   atoms ordered [expert][half][row tile][k tile]  (fc1)  /  [expert][row tile][k tile]  (fc2).
+// NVFP4 E4M3 scales: row-major [row][K/16].  NF3: per row a 2-bit plane (K/4 bytes, code c's low
+//   two bits at bits 2*(c%4) of byte c/4) followed by a 1-bit plane (K/8 bytes, bit 2 of code c
+//   at bit c%8 of byte c/8); E4M3 scales row-major [row][K/32].
+// ----------------------------------------------------------------------------------------------
+struct DevWeights {
+  int quant = 0;
+  int E = 0, H = 0, I = 0, Ip = 0;
+  int E4 = 0, E3 = 0;                 // experts in the fp4 tier / the NF3 tier
+  // fp4 tier (MXFP4 or NVFP4)
+  const uint8_t* w13 = nullptr;       // [E4][2][I][H/2]
+  const uint8_t* s13 = nullptr;       // MXFP4 atoms / NVFP4 [E4][2][I][H/16]
+  const uint8_t* w2 = nullptr;        // [E4][H][Ip/2]
+  const uint8_t* s2 = nullptr;        // MXFP4 atoms / NVFP4 [E4][H][Ip/16]
+  const float* g13 = nullptr;         // [E4] NVFP4 global scales
+  const float* g2 = nullptr;
+  // NF3 tier
+  const uint8_t* nf_w13 = nullptr;    // [E3][2][I][3H/8] planes
+  const uint8_t* nf_s13 = nullptr;    // [E3][2][I][H/32]
+  const uint8_t* nf_w2 = nullptr;     // [E3][H][3Ip/8] planes
+  const uint8_t* nf_s2 = nullptr;     // [E3][H][Ip/32]
+  const int32_t* tier_map = nullptr;  // [E]: (tier << 24) | local index
+};
+
+__host__ __device__ inline size_t sf_atom_byte(int row_tiles, int k_tiles, size_t mat, int r,
+                                               int kb) {
+  // mat = expert * halves + half (fc1) or expert (fc2)
+  int rt = r >> 7, rr = r & 127, kt = kb >> 2, kk = kb & 3;
+  size_t atom = (mat * (size_t)row_tiles + rt) * (size_t)k_tiles + kt;
+  return atom * 512 + (size_t)((rr & 31) * 16 + (rr >> 5) * 4 + kk);
+}
+
+// ----------------------------------------------------------------------------------------------
+// Scratch layout of one plan (byte offsets into the caller's scratch buffer).
+// ----------------------------------------------------------------------------------------------
+constexpr int kSimtSlots = 8;       // slots per tile of the CUDA-core GEMMs
+
+struct Scratch {
+  size_t ctrl;      // int32[64]: [0] error word, [1] n_tiles, [2] n_valid_slots
+  size_t cnt;       // int32[E]
+  size_t off;       // int32[E+1]
+  size_t perm;      // int32[Sm]
+  size_t slot_of;   // int32[Sm]
+  size_t tiles;     // int4[max_tiles] {expert, first position, count, 0}
+  size_t xq, xs;    // W4A8: u8 [max_m][H], u8 [max_m][H/32]
+  size_t g;         // fp32 [Sm][2I]   fc1 output
+  size_t hq, hs;    // W4A8: u8 [Sm][Ip], u8 [Sm][Ip/32]
+  size_t h16;       // W4A16: bf16 [Sm][Ip]
+  size_t acc;       // fp32 [max_m][H]  (atomic combine)
+  size_t rbuf;      // bf16 [max_m*topk][H]  (deterministic combine)
+  size_t total;
+  int max_tiles;
+};
+
+struct PlanDims {
+  int E, H, I, Ip, topk, max_m, quant, deterministic;
+  float limit, alpha, beta;
+};
+
+// Pointers of one call, resolved from the scratch base.
+struct RunPtrs {
+  int32_t* ctrl;
+  int32_t* cnt;
+  int32_t* off;
+  int32_t* perm;
+  int32_t* slot_of;
+  int4* tiles;
+  uint8_t* xq;
+  uint8_t* xs;
+  float* g;
+  uint8_t* hq;
+  uint8_t* hs;
+  __nv_bfloat16* h16;
+  float* acc;
+  __nv_bfloat16* rbuf;
+};
+
+// ----------------------------------------------------------------------------------------------
+// Device helpers
+// ----------------------------------------------------------------------------------------------
+// 2^(s-127) for an E8M0 byte (s = 255 is NaN by the format; never produced here).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
+  return s == 0 ? __int_as_float(0x00400000) : __int_as_float((int)(s << 23));
+}
+
+// 2^(127-s): the exact reciprocal of an E8M0 scale in fp32 (s in 0..254).
+__device__ __forceinline__ float e8m0_inv_f32(uint32_t s) {
+  return s == 254 ? __int_as_float(0x00400000) : __int_as_float((int)((254u - s) << 23));
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint8_t b) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// One E2M1 nibble (sign bit 3, exponent bits 2..1 with bias 1, mantissa bit 0) as fp32, times
+// 2^-126: placing the three magnitude bits at fp32 bits 24..22 gives exactly that, subnormal
+// case included (exponent 0 -> fp32 subnormal m * 2^-127 = m * 0.5 * 2^-126).
+__device__ __forceinline__ float e2m1_scaled_down(uint32_t c) {
+  return __int_as_float((int)(((c & 8u) << 28) | ((c & 7u) << 22)));
+}
+// E2M1 value of a nibble.
+__device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
+  return e2m1_scaled_down(c) * 0x1p126f;
+}
+
+// MXFP8 scale byte of a block whose largest magnitude is amax (OCP MX: floor(log2 amax) - 8,
+// biased, clamped to the finite E8M0 range).
+__device__ __forceinline__ uint32_t mx_scale_byte(float amax) {
+  int e = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+  int s = e - 8;
+  return (uint32_t)(s < 0 ? 0 : (s > 254 ? 254 : s));
+}
+
+// fp32 -> E4M3 code (round to nearest even, saturate to +-448).
+__device__ __forceinline__ uint32_t f32_to_e4m3(float a) {
+  return (uint32_t)__nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ void set_error(int32_t* ctrl, int bit) { atomicOr(ctrl, bit); }
+
+}  // namespace moe

@@ -1,0 +1,210 @@
+// route.cu - routing (per-expert histogram, prefix sum, stable slot permutation, GEMM tile
+// list) and MXFP8 activation quantisation.
+//
+// Routing follows the pages' route planners (hybrid_loader.py: packed_route_indices /
+// expert_offsets / block_expert_ids handed to run_w4a16_moe; moe_b12x_next.py knob
+// _DIRECT_IDS: ids outside [0, E) are skipped).  The slots of expert e are listed in ascending
+// flat index t*k + j, so the permutation is unique and can be compared bit for bit.
+#include <algorithm>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+constexpr int kRouteThreads = 1024;
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kMaxRouteExperts = 1024;  // shared-memory tables below
+
+// Exclusive block scan of one value per thread; returns the prefix, *total = sum.
+__device__ int block_excl_scan(int v, int* total, int* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kRouteWarps ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;  // inclusive prefix of warp sums
+  }
+  __syncthreads();
+  int warp_base = warp ? s_warp[warp - 1] : 0;
+  int t = s_warp[kRouteWarps - 1];
+  __syncthreads();
+  *total = t;
+  return warp_base + x - v;
+}
+
+// One CTA of 1024 threads routes the whole call.
+//   cnt[e], off[e] (off[E] = S), perm[S] = flat slot ids grouped by expert in ascending order,
+//   slot_of[f] = position of flat slot f or -1, tiles = {expert, first position, count} for
+//   every run of up to `tile_slots` consecutive positions of one expert; ctrl[1] = tile count,
+//   ctrl[2] = S.
+__global__ void __launch_bounds__(kRouteThreads)
+route_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile_slots, int max_tiles,
+             int32_t* __restrict__ cnt, int32_t* __restrict__ off, int32_t* __restrict__ perm,
+             int32_t* __restrict__ slot_of, int4* __restrict__ tiles, int32_t* __restrict__ ctrl) {
+  __shared__ int s_cnt[kMaxRouteExperts];
+  __shared__ int s_base[kMaxRouteExperts];
+  __shared__ int s_wc[kRouteWarps][kMaxRouteExperts / 4];  // per-warp counts, 8 bits each
+  __shared__ int s_warp[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  if (tid == 0) ctrl[0] = 0;  // error word of this call
+  for (int e = tid; e < E; e += kRouteThreads) s_cnt[e] = 0;
+  for (int i = tid; i < kRouteWarps * (kMaxRouteExperts / 4); i += kRouteThreads)
+    (&s_wc[0][0])[i] = 0;
+  __syncthreads();
+  for (int f = tid; f < Mk; f += kRouteThreads) {
+    int e = ids[f];
+    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+
+  // prefix over experts: thread t owns experts [t*per, t*per + per)
+  const int per = (E + kRouteThreads - 1) / kRouteThreads;
+  int local = 0, ltiles = 0;
+  for (int i = 0; i < per; ++i) {
+    int e = tid * per + i;
+    if (e < E) {
+      local += s_cnt[e];
+      ltiles += (s_cnt[e] + tile_slots - 1) / tile_slots;
+    }
+  }
+  int total;
+  int base = block_excl_scan(local, &total, s_warp);
+  int ttotal;
+  int tbase = block_excl_scan(ltiles, &ttotal, s_warp);
+  for (int i = 0; i < per; ++i) {
+    int e = tid * per + i;
+    if (e < E) {
+      int c = s_cnt[e];
+      cnt[e] = c;
+      off[e] = base;
+      s_base[e] = base;
+      for (int p = 0; p < c; p += tile_slots) {
+        if (tbase < max_tiles)
+          tiles[tbase] = make_int4(e, base + p, min(tile_slots, c - p), 0);
+        else
+          set_error(ctrl, kErrTileOverflow);
+        ++tbase;
+      }
+      base += c;
+    }
+  }
+  if (tid == 0) {
+    off[E] = total;
+    ctrl[1] = min(ttotal, max_tiles);
+    ctrl[2] = total;
+  }
+  __syncthreads();
+
+  // stable scatter, 1024 flat slots per round in order
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int r0 = 0; r0 < Mk; r0 += kRouteThreads) {
+    const int f = r0 + tid;
+    int e = f < Mk ? ids[f] : -1;
+    const bool valid = f < Mk && e >= 0 && e < E;
+    const int key = valid ? e : (E + lane);  // invalid slots never match a valid one
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const int rank = __popc(peers & lt_mask);
+    const int wcount = __popc(peers);
+    const bool leader = rank == 0;
+    // per-warp counts, 8 bits each (a warp has at most 32 slots of one expert)
+    if (valid && leader) atomicAdd(&s_wc[warp][e >> 2], wcount << ((e & 3) * 8));
+    __syncthreads();
+    int pos = -1;
+    if (valid) {
+      int before = 0;
+      for (int w = 0; w < warp; ++w) before += (s_wc[w][e >> 2] >> ((e & 3) * 8)) & 0xFF;
+      pos = s_base[e] + before + rank;
+    }
+    __syncthreads();
+    if (valid && leader) {
+      atomicAdd(&s_base[e], wcount);
+      atomicAnd(&s_wc[warp][e >> 2], ~(0xFF << ((e & 3) * 8)));
+    }
+    if (f < Mk) {
+      slot_of[f] = pos;
+      if (valid) {
+        if (pos >= 0 && pos < total) perm[pos] = f;
+        else set_error(ctrl, kErrRouteBounds);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// MXFP8 quantisation of x (W4A8): one thread per block of 32 elements.
+// Also clears the fp32 combine buffer (atomic mode) so that one launch prepares both.
+__global__ void __launch_bounds__(256)
+actq_kernel(const __nv_bfloat16* __restrict__ x, int M, int H, uint8_t* __restrict__ xq,
+            uint8_t* __restrict__ xs, float* __restrict__ acc, size_t acc_elems) {
+  const size_t nblk = (size_t)M * (H / 32);
+  const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t gsz = (size_t)gridDim.x * blockDim.x;
+  if (xq != nullptr) {
+    for (size_t b = gtid; b < nblk; b += gsz) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + b * 32);
+      float v[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 u = src[q];
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[q * 8 + 2 * i] = __uint_as_float(w[i] << 16);
+          v[q * 8 + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      const uint32_t s = mx_scale_byte(amax);
+      const float inv = e8m0_inv_f32(s);
+      uint32_t packed[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        packed[i] = f32_to_e4m3(v[4 * i] * inv) | (f32_to_e4m3(v[4 * i + 1] * inv) << 8) |
+                    (f32_to_e4m3(v[4 * i + 2] * inv) << 16) |
+                    (f32_to_e4m3(v[4 * i + 3] * inv) << 24);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(xq + b * 32);
+      dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      xs[b] = (uint8_t)s;
+    }
+  }
+  if (acc != nullptr) {
+    float4* a4 = reinterpret_cast<float4*>(acc);
+    for (size_t i = gtid; i < acc_elems / 4; i += gsz) a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int max_tiles,
+                         const RunPtrs& r, cudaStream_t st) {
+  route_kernel<<<1, kRouteThreads, 0, st>>>(ids, Mk, E, tile_slots, max_tiles, r.cnt, r.off,
+                                            r.perm, r.slot_of, r.tiles, r.ctrl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_actq(const void* x, int M, int H, const RunPtrs& r, bool quant_x,
+                        size_t acc_elems, cudaStream_t st) {
+  const size_t work = std::max<size_t>(quant_x ? (size_t)M * (H / 32) : 0, acc_elems / 4);
+  int blocks = (int)std::min<size_t>((work + 255) / 256, 152 * 8);
+  if (blocks < 1) blocks = 1;
+  actq_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), M, H,
+                                      quant_x ? r.xq : nullptr, quant_x ? r.xs : nullptr,
+                                      acc_elems ? r.acc : nullptr, acc_elems);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

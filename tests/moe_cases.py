@@ -1,0 +1,52 @@
+"""Shared helpers of the GPU tests: build a layer from a synth checkpoint, run it through the
+C ABI and compare with the oracle on the same seeded inputs."""
+import math
+
+import numpy as np
+
+from oracle import codecs as C
+from oracle import moe as O
+from synth import moe_inputs as S
+
+REL_L2_BOUND = 5e-3       # per-row relative L2 error
+MAX_ERR_BOUND = 2e-2      # per-row max |err| / rms(row)
+
+
+def to_device(x_bits, ids, w):
+    import torch
+    xt = torch.from_numpy(x_bits.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    it = torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int32)).cuda()
+    wt = torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32)).cuda()
+    return xt, it, wt
+
+
+def out_bits(out):
+    return out.view(dtype=__import__("torch").int16).cpu().numpy().view(np.uint16)
+
+
+def run_layer(layer, x_bits, ids, w):
+    xt, it, wt = to_device(x_bits, ids, w)
+    out = layer(xt, it, wt)
+    return out_bits(out)
+
+
+def check_rows(got_bits, ck, x_bits, ids, w, limit, rows=None, alpha=1.0, beta=0.0):
+    """Compare the given rows (all when None) with the oracle; returns (rel, mx) arrays."""
+    rows = np.arange(ids.shape[0]) if rows is None else np.asarray(rows)
+    _, f64 = O.moe_forward(ck, x_bits, ids, w, limit, alpha, beta, rows=rows, return_f64=True)
+    rel, mx = O.row_errors(got_bits[rows], f64[rows])
+    assert np.all(rel <= REL_L2_BOUND), (rows, rel)
+    assert np.all(mx <= MAX_ERR_BOUND), (rows, mx)
+    valid = ((ids >= 0) & (ids < ck.E)).any(axis=1)
+    for r in rows:
+        if not valid[r]:
+            assert np.all(got_bits[r] == 0), r
+    return rel, mx
+
+
+def small_cfg(quant, E=16, H=1280, I=192, topk=4, n_nvfp4=5):
+    base = {"mxfp4": S.CONFIGS["tiny_w4a8"], "nvfp4": S.CONFIGS["w4a16_nvfp4"],
+            "hybrid": S.CONFIGS["hybrid_nvfp4_nf3"]}[quant]
+    d = dict(base.__dict__)
+    d.update(E=E, H=H, I=I, topk=topk, n_nvfp4=min(n_nvfp4, E))
+    return S.MoEConfig(**d)

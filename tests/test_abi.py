@@ -1,0 +1,96 @@
+"""The C ABI library builds, loads and exports every function include/moe_gb300.h declares;
+host-only entry points (planning, sizing, argument checks) behave as documented.  No call here
+touches a GPU."""
+import ctypes
+import math
+
+import pytest
+
+from serving_route_count_gb300 import _lib, build
+import serving_route_count_gb300 as moe
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _lib.header_functions()
+    assert "moe_run" in names and "moe_plan" in names and "moe_prepare_weights" in names
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _lib.SIGNATURES, f"binding lacks a signature for {n}"
+
+
+def test_version_and_status_strings(lib):
+    assert "sm_103a" in moe.moe_version()
+    assert moe.moe_status_str(0) == "ok"
+    assert "capacity" in moe.moe_status_str(4)
+
+
+def test_plan_weights_shapes_and_sizes(lib):
+    E, H, I = 384, 7168, 576
+    wp = moe.moe_plan_weights(E, H, I, moe.MOE_W4A8_MXFP4)
+    n = moe.moe_prepared_bytes(wp)
+    codes = E * (2 * I * H // 2 + H * 640 // 2)
+    sf = E * (2 * 5 * (H // 128) * 512 + (H // 128) * 5 * 512)
+    assert codes + sf <= n <= codes + sf + 4096
+    moe.moe_destroy_weight_plan(wp)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_plan_weights(8, 200, 128, moe.MOE_W4A8_MXFP4)         # H % 128 != 0
+    assert ei.value.status == 2
+    with pytest.raises(moe.MoEError):
+        moe.moe_plan_weights(8, 256, 96, moe.MOE_W4A8_MXFP4)          # I % 64 != 0
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_plan_weights(8, 256, 128, moe.MOE_W4A16_HYBRID)       # hybrid needs a tier map
+    assert ei.value.status == 1
+    with pytest.raises(moe.MoEError):
+        moe.moe_plan_weights(4, 256, 128, moe.MOE_W4A16_HYBRID, tier_of_expert=[4, 3, 5, 3])
+    wp = moe.moe_plan_weights(4, 256, 128, moe.MOE_W4A16_HYBRID, tier_of_expert=[4, 3, 3, 4])
+    assert moe.moe_prepared_bytes(wp) > 0
+    moe.moe_destroy_weight_plan(wp)
+
+
+def test_plan_and_scratch_sizes(lib):
+    p_atomic = moe.moe_plan(384, 7168, 576, 6, 16, moe.MOE_W4A8_MXFP4, 7.0, 0)
+    p_det = moe.moe_plan(384, 7168, 576, 6, 16, moe.MOE_W4A8_MXFP4, 7.0, 1)
+    a, d = moe.moe_scratch_bytes(p_atomic), moe.moe_scratch_bytes(p_det)
+    assert a > 16 * 7168 * 4 and d > 96 * 7168 * 2
+    assert moe.moe_io_bytes(p_det) >= 2 * 16 * 7168 * 2 + 2 * 96 * 4
+    moe.moe_plan_set_swiglu_alpha_beta(p_det, 1.702, 1.0)
+    moe.moe_destroy_plan(p_atomic)
+    moe.moe_destroy_plan(p_det)
+    with pytest.raises(moe.MoEError):
+        moe.moe_plan(384, 7168, 576, 0, 16, moe.MOE_W4A8_MXFP4, 7.0, 0)       # top-k 0
+    with pytest.raises(moe.MoEError):
+        moe.moe_plan(384, 7168, 576, 6, 16, moe.MOE_W4A8_MXFP4, float("nan"), 0)
+    with pytest.raises(moe.MoEError):
+        moe.moe_plan(384, 7168, 576, 6, 16, 7, 7.0, 0)                        # bad quant mode
+    p = moe.moe_plan(8, 256, 128, 2, 4, moe.MOE_W4A8_MXFP4, math.inf, 0)
+    moe.moe_destroy_plan(p)
+
+
+def test_run_argument_checks_without_gpu(lib):
+    L = _lib.load()
+    p = moe.moe_plan(8, 256, 128, 2, 4, moe.MOE_W4A8_MXFP4, 7.0, 0)
+    wp = moe.moe_plan_weights(8, 256, 128, moe.MOE_W4A8_MXFP4)
+    # null plan / weights
+    assert L.moe_run(None, None, None, 0, None, None, None, None, 1, None) == 1
+    # M > max_m -> capacity, before any device work
+    fake = ctypes.c_void_p(1)
+    assert L.moe_run(ctypes.c_void_p(p), fake, None, 0, None, None, None, None, 5, None) == 4
+    # M == 0 is a no-op
+    assert L.moe_run(ctypes.c_void_p(p), fake, None, 0, None, None, None, None, 0, None) == 0
+    # negative M
+    assert L.moe_run(ctypes.c_void_p(p), fake, None, 0, None, None, None, None, -1, None) == 1
+    # null buffers with M > 0
+    assert L.moe_run(ctypes.c_void_p(p), fake, None, 0, None, None, None, None, 2, None) == 1
+    # prepare with a too small destination
+    ck = _lib.MoeCheckpoint()
+    out = ctypes.c_void_p()
+    assert L.moe_prepare_weights(ctypes.c_void_p(wp), ctypes.byref(ck), ctypes.c_void_p(256), 16,
+                                 None, ctypes.byref(out)) == 1
+    moe.moe_destroy_plan(p)
+    moe.moe_destroy_weight_plan(wp)

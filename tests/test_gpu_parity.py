@@ -1,0 +1,213 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle on the same seeded inputs.
+
+Bars: routing tables and MXFP8 activation codes / scales bit-exact; outputs per row within
+rel-L2 <= 5e-3 and max|err| <= 2e-2 * rms(row) of the oracle evaluated on the same quantised
+operands; deterministic mode bit-stable run to run and per token under token permutation."""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import codecs as C
+from oracle import moe as O
+from synth import moe_inputs as S
+from moe_cases import check_rows, run_layer, small_cfg, to_device, out_bits
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib_built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from serving_route_count_gb300 import build
+    build.build()
+
+
+def _layer(ck, topk, max_m, limit, det, **kw):
+    from serving_route_count_gb300 import MoELayer
+    return MoELayer(ck, topk, max_m, limit, det, **kw)
+
+
+# ---------------------------------------------------------------------------- tiny config
+
+@pytest.mark.parametrize("det", [0, 1])
+def test_tiny_w4a8_all_rows(det):
+    cfg = S.CONFIGS["tiny_w4a8"]
+    ck = S.make_checkpoint(cfg)
+    x, ids, w = S.make_inputs(cfg, 4)
+    layer = _layer(ck, cfg.topk, 4, cfg.swiglu_limit, det)
+    got = run_layer(layer, x, ids, w)
+    check_rows(got, ck, x, ids, w, cfg.swiglu_limit)
+    st, code = layer.device_error()
+    assert st == 0 and code == 0
+
+
+def test_tiny_routing_and_actq_bit_exact():
+    cfg = S.CONFIGS["tiny_w4a8"]
+    ck = S.make_checkpoint(cfg)
+    x, ids, w = S.make_inputs(cfg, 4)
+    layer = _layer(ck, cfg.topk, 4, cfg.swiglu_limit, 0)
+    run_layer(layer, x, ids, w)
+    torch.cuda.synchronize()
+    for a, b in zip(layer.routing(4), O.route(ids, cfg.E)):
+        assert np.array_equal(a, b)
+    xq, xs = layer.actq(4)
+    q, s = C.mxfp8_quantize(C.bf16_bits_to_f64(x))
+    assert np.array_equal(xq, q) and np.array_equal(xs, s)
+
+
+# ---------------------------------------------------------------------------- small, ragged
+
+@pytest.mark.parametrize("quant,det", [("mxfp4", 0), ("mxfp4", 1), ("nvfp4", 0), ("nvfp4", 1),
+                                       ("hybrid", 1), ("hybrid", 0)])
+def test_small_ragged_all_rows(quant, det):
+    """E=16, H=1280 (one full and one partial 1024-wide K chunk), I=192 (fc2 K padded to 256),
+    top-4, M=37 with padding rows and out-of-range ids: several tiles per expert and a tail."""
+    cfg = small_cfg(quant)
+    ck = S.make_checkpoint(cfg, seed=77, layout=S.W13_GATE_UP if det else S.W13_UP_GATE)
+    rng = np.random.default_rng(78)
+    M = 37
+    x = S.make_x(rng, M, cfg.H)
+    ids = S.zipf_topk(rng, M, cfg.E, cfg.topk, 1.2)
+    ids[-3:] = -1
+    ids[2, 1] = cfg.E
+    ids[5, 0] = -5
+    w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 2.5)
+    limit = 7.0 if quant == "mxfp4" else math.inf
+    layer = _layer(ck, cfg.topk, 40, limit, det)
+    got = run_layer(layer, x, ids, w)
+    check_rows(got, ck, x, ids, w, limit)
+    cnt, off, perm, slot_of = layer.routing(M)
+    for a, b in zip((cnt, off, perm, slot_of), O.route(ids, cfg.E)):
+        assert np.array_equal(a, b)
+    if quant == "mxfp4":
+        xq, xs = layer.actq(M)
+        q, s = C.mxfp8_quantize(C.bf16_bits_to_f64(x))
+        assert np.array_equal(xq, q) and np.array_equal(xs, s)
+
+
+def test_swiglu_alpha_beta_and_no_clamp():
+    cfg = small_cfg("mxfp4", E=8, H=256, I=128, topk=2)
+    ck = S.make_checkpoint(cfg, seed=5)
+    rng = np.random.default_rng(6)
+    M = 9
+    x = S.make_x(rng, M, cfg.H)
+    ids = S.uniform_topk(rng, M, cfg.E, cfg.topk)
+    w = S.router_weights(rng, M, cfg.topk, "softmax", 1.0)
+    layer = _layer(ck, cfg.topk, M, 3.0, 0, alpha=1.702, beta=1.0)
+    check_rows(run_layer(layer, x, ids, w), ck, x, ids, w, 3.0, alpha=1.702, beta=1.0)
+    layer = _layer(ck, cfg.topk, M, math.inf, 1)
+    check_rows(run_layer(layer, x, ids, w), ck, x, ids, w, math.inf)
+
+
+# ---------------------------------------------------------------------------- invariants
+
+def test_deterministic_bit_stable_and_permutation_invariant():
+    cfg = small_cfg("mxfp4")
+    ck = S.make_checkpoint(cfg, seed=9)
+    rng = np.random.default_rng(10)
+    M = 33
+    x = S.make_x(rng, M, cfg.H)
+    ids = S.uniform_topk(rng, M, cfg.E, cfg.topk)
+    w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 1.0)
+    layer = _layer(ck, cfg.topk, M, 7.0, 1)
+    a = run_layer(layer, x, ids, w)
+    b = run_layer(layer, x, ids, w)
+    assert np.array_equal(a, b)
+    p = rng.permutation(M)
+    c = run_layer(layer, x[p], ids[p], w[p])
+    assert np.array_equal(a[p], c)
+
+
+def test_edge_cases():
+    from serving_route_count_gb300 import MoEError
+    cfg = small_cfg("mxfp4", E=8, H=256, I=128, topk=2)
+    ck = S.make_checkpoint(cfg, seed=3)
+    rng = np.random.default_rng(4)
+    layer = _layer(ck, 2, 8, 7.0, 1)
+    # all ids invalid -> zero rows
+    x = S.make_x(rng, 3, cfg.H)
+    ids = np.array([[-1, 8], [-1, -1], [100, -7]], dtype=np.int32)
+    w = np.ones((3, 2), np.float32)
+    assert np.all(run_layer(layer, x, ids, w) == 0)
+    # M = 1
+    ids1 = np.array([[3, 5]], dtype=np.int32)
+    got = run_layer(layer, x[:1], ids1, w[:1])
+    check_rows(got, ck, x[:1], ids1, w[:1], 7.0)
+    # capacity
+    x9 = S.make_x(rng, 9, cfg.H)
+    xt, it, wt = to_device(x9, np.zeros((9, 2), np.int32), np.ones((9, 2), np.float32))
+    with pytest.raises(MoEError) as ei:
+        layer(xt, it, wt)
+    assert ei.value.status == 4
+    # every expert hit by every token (max tile load), M = max_m
+    ids8 = np.tile(np.array([[0, 1]], dtype=np.int32), (8, 1))
+    x8 = S.make_x(rng, 8, cfg.H)
+    got = run_layer(layer, x8, ids8, np.full((8, 2), 0.5, np.float32))
+    check_rows(got, ck, x8, ids8, np.full((8, 2), 0.5, np.float32), 7.0)
+
+
+def test_host_buffers_entry_point():
+    cfg = S.CONFIGS["tiny_w4a8"]
+    ck = S.make_checkpoint(cfg)
+    x, ids, w = S.make_inputs(cfg, 4)
+    layer = _layer(ck, cfg.topk, 4, cfg.swiglu_limit, 1)
+    xh = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    ih = torch.from_numpy(ids).pin_memory()
+    wh = torch.from_numpy(w).pin_memory()
+    oh = torch.empty((4, cfg.H), dtype=torch.bfloat16).pin_memory()
+    layer.run_host(xh, ih, wh, oh)
+    got = oh.view(torch.int16).numpy().view(np.uint16)
+    dev = run_layer(layer, x, ids, w)
+    assert np.array_equal(got, dev)
+
+
+# ---------------------------------------------------------------------------- full sizes
+
+@pytest.fixture(scope="module")
+def decode_layer():
+    cfg = S.CONFIGS["decode_w4a8"]
+    ck = S.make_checkpoint(cfg)
+    return cfg, ck
+
+
+@pytest.mark.parametrize("det", [0, 1])
+def test_decode_full_size_sampled(decode_layer, det):
+    """E=384, H=7168, I=576, top-6 at M=16 (last 4 rows padding): routing bit-exact for the
+    whole call, outputs of sampled rows against the oracle, padding rows exactly 0."""
+    cfg, ck = decode_layer
+    M = 16
+    x, ids, w = S.make_inputs(cfg, M)
+    layer = _layer(ck, cfg.topk, M, cfg.swiglu_limit, det)
+    got = run_layer(layer, x, ids, w)
+    for a, b in zip(layer.routing(M), O.route(ids, cfg.E)):
+        assert np.array_equal(a, b)
+    xq, xs = layer.actq(M)
+    q, s = C.mxfp8_quantize(C.bf16_bits_to_f64(x))
+    assert np.array_equal(xq, q) and np.array_equal(xs, s)
+    check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=[0, 7, 11, 12, 15])
+    layer.close()
+
+
+def test_nvfp4_full_size_sampled():
+    cfg = S.CONFIGS["w4a16_nvfp4"]
+    ck = S.make_checkpoint(cfg)
+    M = 64
+    x, ids, w = S.make_inputs(cfg, M)
+    layer = _layer(ck, cfg.topk, M, cfg.swiglu_limit, 0)
+    got = run_layer(layer, x, ids, w)
+    check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=[0, 31, 63])
+    layer.close()
+
+
+def test_hybrid_full_size_sampled():
+    cfg = S.CONFIGS["hybrid_nvfp4_nf3"]
+    ck = S.make_checkpoint(cfg)
+    M = 8
+    x, ids, w = S.make_inputs(cfg, M)
+    layer = _layer(ck, cfg.topk, M, cfg.swiglu_limit, 1)
+    got = run_layer(layer, x, ids, w)
+    check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=[0, 3, 7])
+    layer.close()
