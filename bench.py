@@ -1,0 +1,406 @@
+"""Benchmark of the routed-MoE layer on GB300.
+
+Default workload: the decode / verify slice E=384, H=7168, I=576, top-6, MXFP4 weights with
+MXFP8 activations, swiglu limit 7; one step = one layer call at each decode batch size
+M in {1,2,3,4,5,6,7,8,10,12,14,16} (last 25 % of rows are CUDA-graph padding, id -1).
+Metric: tokens/s (valid rows per second of layer time).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--det]
+
+Timing: every layer call is a CUDA graph replay bracketed by CUDA events on the launching
+stream; before each call (outside the events) a 512 MB buffer is written to flush L2, and the
+routing set rotates over 8 pre-generated sets per M.  The step time is the sum of its calls'
+event times.  The dominant kernel is timed by event-record nodes inside the same graphs.
+Under torchrun each rank runs the same workload on its own GPU (replicas; weak scaling);
+rank 0 prints one JSON line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synth import moe_inputs as S  # noqa: E402
+
+DECODE_CFG = "decode_w4a8"
+N_ROUTING_SETS = 8
+FLUSH_BYTES = 512 << 20
+EXPERT_BYTES_W13 = {"decode_w4a8": 2 * 576 * 7168 // 2 + 2 * 576 * 7168 // 32}   # codes + E8M0
+EXPERT_BYTES_W2 = {"decode_w4a8": 7168 * 576 // 2 + 7168 * 576 // 32}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--det", action="store_true", help="deterministic combine")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
+    p.add_argument("--sample-m", type=str, default="1,2", help=argparse.SUPPRESS)
+    return p.parse_args()
+
+
+def valid_rows(ids):
+    return int(((ids >= 0)).any(axis=1).sum())
+
+
+def distinct_experts(ids, E):
+    v = ids[(ids >= 0) & (ids < E)]
+    return int(np.unique(v).size)
+
+
+# ---------------------------------------------------------------------------------- oracle arm
+
+def oracle_sample(cfg, ck, m_list, sets):
+    """Time the fp64 oracle on one call per M in m_list; returns (tokens, seconds)."""
+    from oracle import moe as O
+    tok, sec = 0, 0.0
+    for i, M in enumerate(m_list):
+        x, ids, w = S.make_inputs(cfg, M, seed=cfg.seed_base + 100 * M + sets[i % len(sets)])
+        t0 = time.perf_counter()
+        O.moe_forward(ck, x, ids, w, cfg.swiglu_limit)
+        sec += time.perf_counter() - t0
+        tok += valid_rows(ids)
+    return tok, sec
+
+
+def cpu_baseline_worker(args):
+    cfg = S.CONFIGS[DECODE_CFG]
+    ck = S.make_checkpoint(cfg)
+    m_list = [int(v) for v in args.sample_m.split(",")]
+    tok, sec = oracle_sample(cfg, ck, m_list, [0])
+    print(json.dumps({"tokens": tok, "seconds": sec}))
+
+
+def run_cpu_baseline(m_list="1,2"):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-worker",
+                        "--sample-m", m_list], capture_output=True, text=True, env=env,
+                       timeout=900)
+    if r.returncode != 0:
+        return None
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["tokens"] / d["seconds"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"one layer call at each M in {{{m_list}}} of the decode workload "
+                      f"({d['tokens']} valid tokens, {d['seconds']:.1f} s; numpy fp64, BLAS "
+                      f"threads = 1)"}
+
+
+def reference_arm(args, rank, world):
+    """The oracle timed as the reference implementation (rank 0 only)."""
+    if rank != 0:
+        return
+    cfg = S.CONFIGS[DECODE_CFG]
+    ck = S.make_checkpoint(cfg)
+    tok_total, sec_total = 0, 0.0
+    for s in range(args.warmup + args.steps):
+        tok, sec = oracle_sample(cfg, ck, [1], [s % N_ROUTING_SETS])
+        if s >= args.warmup:
+            tok_total += tok
+            sec_total += sec
+    value = tok_total / sec_total
+    line = {
+        "impl": "reference", "metric": "decode MoE layer tokens/s", "value": value,
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sec_total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode_w4a8 sample: one call at M=1 per step (E=384, H=7168, "
+                               "I=576, top-6, MXFP4/MXFP8)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "one M=1 decode call per step, rotating routing sets"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r.split(",") for r in (self.out or "").strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx = float(r[1])
+                for n, v in zip(names, r[4:8]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------- our arm
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_traffic(kernel):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None when the kernel
+    source changed since the counters were taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = d.get(kernel)
+    if not ent:
+        return None
+    h = hashlib.sha256()
+    for src in ent["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != ent["sha256"]:
+        return None
+    return ent
+
+
+def our_arm(args, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    from serving_route_count_gb300 import MoELayer, build, moe_plan_set_profile_events
+    from serving_route_count_gb300 import moe_profile_stage_names
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    build.build()
+    cfg = S.CONFIGS[DECODE_CFG]
+    ck = S.make_checkpoint(cfg)
+    m_list = list(cfg.m_list)
+    max_m = max(m_list)
+    layer = MoELayer(ck, cfg.topk, max_m, cfg.swiglu_limit, args.det)
+    stages = moe_profile_stage_names(layer.plan)
+    dom = "fc1"
+    dom_i = stages.index(dom)
+
+    # inputs: per M, N_ROUTING_SETS routing sets (+ x), device resident; one graph per (M, set)
+    stream = torch.cuda.Stream()
+    calls = []   # (M, set, graph, x, ids, w, out, prof_events, tokens, distinct)
+    for M in m_list:
+        for s in range(N_ROUTING_SETS):
+            x, ids, w = S.make_inputs(cfg, M, seed=cfg.seed_base + 100 * M + s + 1000 * rank)
+            xt = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).cuda()
+            it = torch.from_numpy(ids).cuda()
+            wt = torch.from_numpy(w).cuda()
+            ot = torch.empty((M, cfg.H), dtype=torch.bfloat16, device="cuda")
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+            for ev in evs:   # torch creates the CUDA event on first record
+                ev.record()
+            calls.append(dict(M=M, set=s, x=xt, ids=it, w=wt, out=ot, ev=evs,
+                              tokens=valid_rows(ids), distinct=distinct_experts(ids, cfg.E),
+                              ids_np=ids, x_np=x, w_np=w))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for c in calls:   # eager warm-up of each shape
+            layer(c["x"], c["ids"], c["w"], c["out"])
+        stream.synchronize()
+        for c in calls:
+            moe_plan_set_profile_events(layer.plan, c["ev"])
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                layer(c["x"], c["ids"], c["w"], c["out"])
+            c["graph"] = g
+        moe_plan_set_profile_events(layer.plan, [])
+    torch.cuda.synchronize()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    per_step = len(m_list)
+
+    def step(si, record):
+        tot_ms, dom_ms, dom_bytes, toks = 0.0, 0.0, 0.0, 0
+        pairs = []
+        with torch.cuda.stream(stream):
+            for mi, M in enumerate(m_list):
+                c = calls[mi * N_ROUTING_SETS + (si % N_ROUTING_SETS)]
+                flush.fill_(si & 0xFF)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                c["graph"].replay()
+                b.record(stream)
+                pairs.append((a, b, c))
+        stream.synchronize()
+        for a, b, c in pairs:
+            tot_ms += a.elapsed_time(b)
+            dom_ms += c["ev"][dom_i].elapsed_time(c["ev"][dom_i + 1])
+            dom_bytes += c["distinct"] * EXPERT_BYTES_W13[DECODE_CFG] + c["M"] * cfg.H
+            toks += c["tokens"]
+        return tot_ms, dom_ms, dom_bytes, toks
+
+    for si in range(args.warmup):
+        step(si, False)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    tot_ms = dom_ms = dom_bytes = 0.0
+    toks = 0
+    with ClockSampler(local) as clk:
+        for si in range(args.steps):
+            a, b, c, d = step(args.warmup + si, True)
+            tot_ms += a
+            dom_ms += b
+            dom_bytes += c
+            toks += d
+    torch.cuda.synchronize()
+    if world > 1:
+        t = torch.tensor([tot_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+        dist.barrier()
+    clocks = clk.summary()
+
+    # end to end: host (pinned) buffers through moe_run_host, copies inside the timed region
+    e2e_ms, e2e_tok, h2d, d2h = 0.0, 0, 0, 0
+    host = []
+    for mi, M in enumerate(m_list):
+        c = calls[mi * N_ROUTING_SETS]
+        xh = torch.from_numpy(c["x_np"].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+        ih = torch.from_numpy(c["ids_np"]).pin_memory()
+        wh = torch.from_numpy(c["w_np"]).pin_memory()
+        oh = torch.empty((M, cfg.H), dtype=torch.bfloat16).pin_memory()
+        host.append((xh, ih, wh, oh, c["tokens"]))
+    for xh, ih, wh, oh, _ in host:   # warm-up
+        layer.run_host(xh, ih, wh, oh, stream=stream)
+    e2e_steps = max(3, args.steps // 2)
+    for _ in range(e2e_steps):
+        for xh, ih, wh, oh, tk in host:
+            flush.fill_(1)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            layer.run_host(xh, ih, wh, oh, stream=stream)
+            e2e_ms += 1e3 * (time.perf_counter() - t0)
+            e2e_tok += tk
+    h2d = sum(xh.numel() * 2 + ih.numel() * 4 + wh.numel() * 4 for xh, ih, wh, _, _ in host)
+    d2h = sum(oh.numel() * 2 for *_, oh, _ in host)
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = kernel_traffic("gemm_simt_kernel<false>")
+    n_launch_per_call = len(stages)
+    cpu = None if args.no_cpu_baseline else run_cpu_baseline()
+    line = {
+        "metric": "decode MoE layer tokens/s",
+        "value": toks * world / (tot_ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": tot_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "mxfp4 x mxfp8 (fp32 accumulate)",
+        "data": "synthetic",
+        "config": {
+            "workload": "decode_w4a8: E=384 H=7168 I=576 top-6, MXFP4 weights / MXFP8 "
+                        "activations, M ladder 1..16 (one call each per step), last 25% rows "
+                        "padding, swiglu limit 7",
+            "combine": "deterministic" if args.det else "atomic",
+            "tokens_per_step": toks // args.steps,
+            "timing": "CUDA graph per call, CUDA events around each replay; L2 flushed by a "
+                      "512 MB write before each call (outside the events); 8 routing sets "
+                      "rotated per M",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "kernel": dom,
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": None if traffic is None else traffic["bytes_per_launch"],
+            "algorithmic_bytes": "distinct touched experts x (w13 codes + E8M0 scales = "
+                                 f"{EXPERT_BYTES_W13[DECODE_CFG]} B) + x rows",
+            "kernel_ms_per_step": dom_ms / args.steps,
+        },
+        "stages": stages,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_tok / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "moe_run_host (pinned host buffers, H2D + run + D2H + sync)"},
+        "gpu_launches": n_launch_per_call * per_step * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.cpu_baseline_worker:
+        cpu_baseline_worker(args)
+        return
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            dist.init_process_group("nccl")
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+    our_arm(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

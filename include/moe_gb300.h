@@ -179,6 +179,16 @@ moe_status moe_debug_routing(const moe_plan_t* plan, void* scratch, int M, int32
 moe_status moe_debug_actq(const moe_plan_t* plan, void* scratch, int M, uint8_t* xq, uint8_t* xs,
                           void* stream);
 
+/* Profiling hook.  With n_events >= 1 set, every later moe_run with this plan records
+ * events[0] before its first kernel and events[i + 1] after stage i (up to n_events - 1 stages;
+ * events are cudaEvent_t handles created by the caller with timing enabled).  Inside stream
+ * capture the records become event-record nodes of the graph (cudaEventRecordExternal), so
+ * graph replays time each stage on the device.  n_events = 0 turns it off.
+ * moe_profile_stage_names returns the stage names of this plan's launch sequence, comma
+ * separated, e.g. "route,actq,fc1,act,fc2,finalize". */
+moe_status moe_plan_set_profile_events(moe_plan_t* plan, void* const* events, int n_events);
+const char* moe_profile_stage_names(const moe_plan_t* plan);
+
 void moe_destroy_weight_plan(moe_weight_plan* wp);
 void moe_destroy_prepared(moe_prepared* p);
 void moe_destroy_plan(moe_plan_t* plan);

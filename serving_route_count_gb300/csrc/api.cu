@@ -16,10 +16,9 @@ cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int 
 cudaError_t launch_actq(const void* x, int M, int H, const RunPtrs& r, bool quant_x,
                         size_t acc_elems, cudaStream_t st);
 // gemm_simt.cu
-struct SimtArgs;
-cudaError_t launch_simt_pipeline(const DevWeights& w, const RunPtrs& r, const PlanDims& d,
-                                 int max_tiles, const void* x, const float* topk_w, void* out,
-                                 int M, cudaStream_t st);
+cudaError_t launch_simt_stage(int stage, const DevWeights& w, const RunPtrs& r,
+                              const PlanDims& d, int max_tiles, const void* x,
+                              const float* topk_w, void* out, int M, cudaStream_t st);
 // prepare.cu
 cudaError_t launch_repack_rows(const void* src, void* dst, int E, int halves, int rows,
                                int src_cols, int dst_cols, int layout, int canon, cudaStream_t st);
@@ -48,6 +47,7 @@ struct moe_plan_s {
   PlanDims d;
   Scratch s;
   size_t io_x, io_ids, io_w, io_out, io_total;
+  std::vector<cudaEvent_t> prof;
 };
 
 namespace {
@@ -250,7 +250,7 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   s.hs = a8 ? take(Sm * d.Ip / 32) : 0;
   s.h16 = a8 ? 0 : take(Sm * d.Ip * 2);
   s.acc = d.deterministic ? 0 : take((size_t)max_m * H * 4);
-  s.rbuf = d.deterministic ? take(Sm * H * 2) : 0;
+  s.rbuf = d.deterministic ? take(Sm * H * 4) : 0;
   s.total = o;
   o = 0;
   p->io_x = take((size_t)max_m * H * 2);
@@ -299,8 +299,36 @@ static RunPtrs resolve(const moe_plan_t* plan, void* scratch) {
   r.hs = a8 ? b + s.hs : nullptr;
   r.h16 = a8 ? nullptr : reinterpret_cast<__nv_bfloat16*>(b + s.h16);
   r.acc = plan->d.deterministic ? nullptr : reinterpret_cast<float*>(b + s.acc);
-  r.rbuf = plan->d.deterministic ? reinterpret_cast<__nv_bfloat16*>(b + s.rbuf) : nullptr;
+  r.rbuf = plan->d.deterministic ? reinterpret_cast<float*>(b + s.rbuf) : nullptr;
   return r;
+}
+
+namespace {
+// Records profiling event i (if configured) on the stream of the call.
+struct ProfRec {
+  const std::vector<cudaEvent_t>* ev;
+  cudaStream_t st;
+  bool cap;
+  void operator()(size_t i) const {
+    if (i >= ev->size()) return;
+    if (cap)
+      cudaEventRecordWithFlags((*ev)[i], st, cudaEventRecordExternal);
+    else
+      cudaEventRecord((*ev)[i], st);
+  }
+};
+}  // namespace
+
+moe_status moe_plan_set_profile_events(moe_plan_t* plan, void* const* events, int n_events) {
+  if (plan == nullptr || n_events < 0 || (n_events > 0 && events == nullptr)) return MOE_ERR_ARG;
+  plan->prof.clear();
+  for (int i = 0; i < n_events; ++i) plan->prof.push_back(static_cast<cudaEvent_t>(events[i]));
+  return MOE_OK;
+}
+
+const char* moe_profile_stage_names(const moe_plan_t* plan) {
+  if (plan == nullptr) return "";
+  return "route,actq,fc1,act,fc2,finalize";
 }
 
 moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* scratch,
@@ -321,15 +349,24 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   if (w.E != d.E || w.H != d.H || w.I != d.I || w.quant != d.quant) return MOE_ERR_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const RunPtrs r = resolve(plan, scratch);
+  const ProfRec prof{&plan->prof, st, !plan->prof.empty() && capturing(st)};
+  prof(0);
   cudaError_t e = launch_route(topk_ids, M * d.topk, d.E, kSimtSlots, plan->s.max_tiles, r, st);
   if (e != cudaSuccess) return cuda_status(e);
+  prof(1);
   const bool a8 = d.quant == MOE_W4A8_MXFP4;
   if (a8 || !d.deterministic) {
     e = launch_actq(x, M, d.H, r, a8, d.deterministic ? 0 : (size_t)M * d.H, st);
     if (e != cudaSuccess) return cuda_status(e);
   }
-  e = launch_simt_pipeline(w, r, d, plan->s.max_tiles, x, topk_weights, out, M, st);
-  return cuda_status(e);
+  prof(2);
+  // fc1, SwiGLU + requant, fc2 + combine, finalize
+  for (int stage = 0; stage < 4; ++stage) {
+    e = launch_simt_stage(stage, w, r, d, plan->s.max_tiles, x, topk_weights, out, M, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    prof(3 + stage);
+  }
+  return MOE_OK;
 }
 
 moe_status moe_run_host(const moe_plan_t* plan, const moe_prepared* weights, void* scratch,

@@ -219,7 +219,7 @@ gemm_simt_kernel(SimtArgs a) {
     const int f = a.r.perm[p];
     const float wt = a.topk_w[f];
     if (a.deterministic) {
-      a.r.rbuf[(size_t)f * a.H + row] = __float2bfloat16_rn(wt * v);
+      a.r.rbuf[(size_t)f * a.H + row] = wt * v;
     } else {
       atomicAdd(&a.r.acc[(size_t)(f / a.topk) * a.H + row], wt * v);
     }
@@ -279,7 +279,7 @@ act_kernel(const float* __restrict__ g, const int32_t* __restrict__ ctrl, int I,
 // valid slots j = 0..k-1 of the route buffer (deterministic mode).  Eight columns per thread.
 __global__ void __launch_bounds__(256)
 finalize_kernel(int M, int H, int topk, int deterministic, const float* __restrict__ acc,
-                const __nv_bfloat16* __restrict__ rbuf, const int32_t* __restrict__ slot_of,
+                const float* __restrict__ rbuf, const int32_t* __restrict__ slot_of,
                 __nv_bfloat16* __restrict__ out) {
   const size_t total = (size_t)M * (H / 8);
   for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -298,13 +298,10 @@ finalize_kernel(int M, int H, int topk, int deterministic, const float* __restri
       for (int j = 0; j < topk; ++j) {
         const int f = t * topk + j;
         if (slot_of[f] < 0) continue;
-        const uint4 r = *reinterpret_cast<const uint4*>(rbuf + (size_t)f * H + c);
-        const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          v[2 * q] += __uint_as_float(rw[q] << 16);
-          v[2 * q + 1] += __uint_as_float(rw[q] & 0xFFFF0000u);
-        }
+        const float4* r4 = reinterpret_cast<const float4*>(rbuf + (size_t)f * H + c);
+        const float4 r0 = r4[0], r1 = r4[1];
+        v[0] += r0.x; v[1] += r0.y; v[2] += r0.z; v[3] += r0.w;
+        v[4] += r1.x; v[5] += r1.y; v[6] += r1.z; v[7] += r1.w;
       }
     }
     uint32_t o[4];
@@ -348,9 +345,10 @@ static cudaError_t launch_finalize(int M, int H, int topk, int det, const RunPtr
   return cudaGetLastError();
 }
 
-cudaError_t launch_simt_pipeline(const DevWeights& w, const RunPtrs& r, const PlanDims& d,
-                                 int max_tiles, const void* x, const float* topk_w, void* out,
-                                 int M, cudaStream_t st) {
+// stage 0: fc1, 1: SwiGLU + requant, 2: fc2 + combine, 3: finalize
+cudaError_t launch_simt_stage(int stage, const DevWeights& w, const RunPtrs& r,
+                              const PlanDims& d, int max_tiles, const void* x,
+                              const float* topk_w, void* out, int M, cudaStream_t st) {
   SimtArgs a;
   a.w = w;
   a.r = r;
@@ -360,12 +358,14 @@ cudaError_t launch_simt_pipeline(const DevWeights& w, const RunPtrs& r, const Pl
   a.quant = d.quant; a.deterministic = d.deterministic;
   const int Sm = M * d.topk;
   const int tiles = std::min(max_tiles, std::min(Sm, cdiv(Sm, kSimtSlots) + std::min(d.E, Sm)));
-  cudaError_t e = launch_simt_fc(false, a, tiles, st);
-  if (e == cudaSuccess)
-    e = launch_act(r, Sm, d.I, d.Ip, d.limit, d.alpha, d.beta, d.quant == kQuantW4A8 ? 1 : 0, st);
-  if (e == cudaSuccess) e = launch_simt_fc(true, a, tiles, st);
-  if (e == cudaSuccess) e = launch_finalize(M, d.H, d.topk, d.deterministic, r, out, st);
-  return e;
+  switch (stage) {
+    case 0: return launch_simt_fc(false, a, tiles, st);
+    case 1:
+      return launch_act(r, Sm, d.I, d.Ip, d.limit, d.alpha, d.beta,
+                        d.quant == kQuantW4A8 ? 1 : 0, st);
+    case 2: return launch_simt_fc(true, a, tiles, st);
+    default: return launch_finalize(M, d.H, d.topk, d.deterministic, r, out, st);
+  }
 }
 
 }  // namespace moe

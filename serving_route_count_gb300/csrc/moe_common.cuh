@@ -86,7 +86,7 @@ struct Scratch {
   size_t hq, hs;    // W4A8: u8 [Sm][Ip], u8 [Sm][Ip/32]
   size_t h16;       // W4A16: bf16 [Sm][Ip]
   size_t acc;       // fp32 [max_m][H]  (atomic combine)
-  size_t rbuf;      // bf16 [max_m*topk][H]  (deterministic combine)
+  size_t rbuf;      // fp32 [max_m*topk][H]  (deterministic combine: one row per slot)
   size_t total;
   int max_tiles;
 };
@@ -111,7 +111,7 @@ struct RunPtrs {
   uint8_t* hs;
   __nv_bfloat16* h16;
   float* acc;
-  __nv_bfloat16* rbuf;
+  float* rbuf;
 };
 
 // ----------------------------------------------------------------------------------------------

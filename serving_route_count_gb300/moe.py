@@ -163,6 +163,18 @@ def moe_debug_actq(plan, scratch, M, H, stream=None):
     return xq, xs
 
 
+def moe_plan_set_profile_events(plan, events):
+    """events: list of torch.cuda.Event(enable_timing=True) (or raw handles); [] turns it off."""
+    hs = [ev.cuda_event if hasattr(ev, "cuda_event") else int(ev) for ev in events]
+    arr = (ctypes.c_void_p * max(1, len(hs)))(*hs)
+    _check(_lib.load().moe_plan_set_profile_events(_handle(plan), arr, len(hs)),
+           "moe_plan_set_profile_events")
+
+
+def moe_profile_stage_names(plan):
+    return _lib.load().moe_profile_stage_names(_handle(plan)).decode().split(",")
+
+
 def moe_destroy_weight_plan(wp):
     _lib.load().moe_destroy_weight_plan(_handle(wp))
 
