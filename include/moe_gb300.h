@@ -137,6 +137,11 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
  * (B12xExperts `_swiglu_params`, SWIGLUOAI form). */
 moe_status moe_plan_set_swiglu_alpha_beta(moe_plan_t* plan, float alpha, float beta);
 
+/* Kernel family for later moe_run calls: 0 (default) = tcgen05 tensor-core GEMMs where the quant
+ * mode has them (W4A8), CUDA-core GEMMs otherwise; 1 = CUDA-core GEMMs for every mode (a
+ * slower, independent path, kept for cross-checks).  Errors: MOE_ERR_ARG. */
+moe_status moe_plan_set_backend(moe_plan_t* plan, int backend);
+
 /* Size in bytes of the device scratch buffer moe_run needs (routing tables, quantised
  * activations, the fc1 -> fc2 intermediate, the combine buffer). */
 moe_status moe_scratch_bytes(const moe_plan_t* plan, size_t* bytes);
@@ -173,7 +178,8 @@ moe_status moe_get_device_error(const moe_plan_t* plan, void* scratch, void* str
 
 /* Test hooks: after a moe_run on `stream`, copy routing tables / quantised activations of the
  * last call to host buffers (synchronises).  cnt [E], off [E+1], perm [S], slot_of [M*topk]
- * where S = off[E]; xq [M, H] E4M3 codes, xs [M, H/32] E8M0 bytes (W4A8 only). */
+ * where S = off[E]; xq [S, H] E4M3 codes, xs [S, H/32] E8M0 bytes (W4A8 only), row p holding
+ * the quantised row of token perm[p] / topk (buffers of M*topk rows suffice). */
 moe_status moe_debug_routing(const moe_plan_t* plan, void* scratch, int M, int32_t* cnt,
                              int32_t* off, int32_t* perm, int32_t* slot_of, void* stream);
 moe_status moe_debug_actq(const moe_plan_t* plan, void* scratch, int M, uint8_t* xq, uint8_t* xs,

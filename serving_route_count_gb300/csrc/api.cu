@@ -13,8 +13,14 @@ namespace moe {
 // route.cu
 cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int max_tiles,
                          const RunPtrs& r, cudaStream_t st);
-cudaError_t launch_actq(const void* x, int M, int H, const RunPtrs& r, bool quant_x,
-                        size_t acc_elems, cudaStream_t st);
+cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
+                        void* z0, size_t z0_words, void* z1, size_t z1_words, void* z2,
+                        size_t z2_words, cudaStream_t st);
+// gemm_tc.cu
+cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
+                            int bn, int tiles, int splits, const float* topk_w, int M,
+                            cudaStream_t st);
+int tc_pick_bn(int M, int topk);
 // gemm_simt.cu
 cudaError_t launch_simt_stage(int stage, const DevWeights& w, const RunPtrs& r,
                               const PlanDims& d, int max_tiles, const void* x,
@@ -229,7 +235,7 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   PlanDims& d = p->d;
   d.E = E; d.H = H; d.I = I; d.Ip = (int)align_up((size_t)I, 128); d.topk = topk; d.max_m = max_m;
   d.quant = quant_mode; d.deterministic = deterministic ? 1 : 0;
-  d.limit = swiglu_limit; d.alpha = 1.f; d.beta = 0.f;
+  d.limit = swiglu_limit; d.alpha = 1.f; d.beta = 0.f; d.backend = 0;
   const size_t Sm = (size_t)max_m * topk;
   Scratch& s = p->s;
   s.max_tiles = (int)std::min<size_t>(Sm, (Sm + kSimtSlots - 1) / kSimtSlots +
@@ -243,9 +249,10 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   s.perm = take(Sm * 4);
   s.slot_of = take(Sm * 4);
   s.tiles = take((size_t)s.max_tiles * 16);
-  s.xq = a8 ? take((size_t)max_m * H) : 0;
-  s.xs = a8 ? take((size_t)max_m * H / 32) : 0;
-  s.g = take(Sm * 2 * I * 4);
+  s.xq = a8 ? take(Sm * H) : 0;
+  s.xs = a8 ? take(Sm * H / 32) : 0;
+  s.g = take(Sm * 2 * d.Ip * 4);
+  s.tickets = take((size_t)s.max_tiles * cdiv(I, 128) * 4);
   s.hq = a8 ? take(Sm * d.Ip) : 0;
   s.hs = a8 ? take(Sm * d.Ip / 32) : 0;
   s.h16 = a8 ? 0 : take(Sm * d.Ip * 2);
@@ -295,6 +302,7 @@ static RunPtrs resolve(const moe_plan_t* plan, void* scratch) {
   r.xq = a8 ? b + s.xq : nullptr;
   r.xs = a8 ? b + s.xs : nullptr;
   r.g = reinterpret_cast<float*>(b + s.g);
+  r.tickets = reinterpret_cast<int32_t*>(b + s.tickets);
   r.hq = a8 ? b + s.hq : nullptr;
   r.hs = a8 ? b + s.hs : nullptr;
   r.h16 = a8 ? nullptr : reinterpret_cast<__nv_bfloat16*>(b + s.h16);
@@ -326,9 +334,17 @@ moe_status moe_plan_set_profile_events(moe_plan_t* plan, void* const* events, in
   return MOE_OK;
 }
 
+static bool use_tc(const PlanDims& d) { return d.backend == 0 && d.quant == MOE_W4A8_MXFP4; }
+
 const char* moe_profile_stage_names(const moe_plan_t* plan) {
   if (plan == nullptr) return "";
-  return "route,actq,fc1,act,fc2,finalize";
+  return use_tc(plan->d) ? "route,actq,fc1,fc2,finalize" : "route,actq,fc1,act,fc2,finalize";
+}
+
+moe_status moe_plan_set_backend(moe_plan_t* plan, int backend) {
+  if (plan == nullptr || backend < 0 || backend > 1) return MOE_ERR_ARG;
+  plan->d.backend = backend;
+  return MOE_OK;
 }
 
 moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* scratch,
@@ -350,16 +366,46 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const RunPtrs r = resolve(plan, scratch);
   const ProfRec prof{&plan->prof, st, !plan->prof.empty() && capturing(st)};
+  const bool a8 = d.quant == MOE_W4A8_MXFP4;
+  const bool tc = use_tc(d);
+  const int Sm = M * d.topk;
+  const int bn = tc ? tc_pick_bn(M, d.topk) : kSimtSlots;
+  // tiles of this call: at most one per slot, and at most ceil(S / bn) + (touched experts)
+  const int tiles = std::min(plan->s.max_tiles, std::min(Sm, cdiv(Sm, bn) + std::min(d.E, Sm)));
+  const int RT = cdiv(d.I, 128);
+  int splits = 1;
+  if (tc) {
+    // split K of fc1 so that small calls still put one CTA on most SMs
+    const int units = tiles * RT;
+    splits = std::max(1, std::min(std::min(152 / std::max(units, 1), d.H / 128 / 4), 16));
+  }
   prof(0);
-  cudaError_t e = launch_route(topk_ids, M * d.topk, d.E, kSimtSlots, plan->s.max_tiles, r, st);
+  cudaError_t e = launch_route(topk_ids, Sm, d.E, bn, plan->s.max_tiles, r, st);
   if (e != cudaSuccess) return cuda_status(e);
   prof(1);
-  const bool a8 = d.quant == MOE_W4A8_MXFP4;
-  if (a8 || !d.deterministic) {
-    e = launch_actq(x, M, d.H, r, a8, d.deterministic ? 0 : (size_t)M * d.H, st);
+  void* acc = d.deterministic ? nullptr : r.acc;
+  const size_t acc_words = d.deterministic ? 0 : (size_t)M * d.H;
+  void* g = (tc && splits > 1) ? r.g : nullptr;
+  const size_t g_words = g ? (size_t)Sm * 2 * d.Ip : 0;
+  void* tk = (tc && splits > 1) ? r.tickets : nullptr;
+  const size_t tk_words = tk ? align_up((size_t)tiles * RT, 4) : 0;
+  if (a8 || acc || g) {
+    e = launch_actq(x, M, d.H, d.topk, r, a8, acc, acc_words, g, g_words, tk, tk_words, st);
     if (e != cudaSuccess) return cuda_status(e);
   }
   prof(2);
+  if (tc) {
+    e = launch_tc_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    prof(3);
+    e = launch_tc_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    prof(4);
+    e = launch_simt_stage(3, w, r, d, plan->s.max_tiles, x, topk_weights, out, M, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    prof(5);
+    return MOE_OK;
+  }
   // fc1, SwiGLU + requant, fc2 + combine, finalize
   for (int stage = 0; stage < 4; ++stage) {
     e = launch_simt_stage(stage, w, r, d, plan->s.max_tiles, x, topk_weights, out, M, st);
@@ -444,9 +490,14 @@ moe_status moe_debug_actq(const moe_plan_t* plan, void* scratch, int M, uint8_t*
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const RunPtrs r = resolve(plan, scratch);
   cudaError_t e = cudaSuccess;
-  if (xq) e = cudaMemcpyAsync(xq, r.xq, (size_t)M * plan->d.H, cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess && xs)
-    e = cudaMemcpyAsync(xs, r.xs, (size_t)M * plan->d.H / 32, cudaMemcpyDeviceToHost, st);
+  int32_t S = 0;
+  e = cudaMemcpyAsync(&S, r.ctrl + 2, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (S < 0 || S > M * plan->d.topk) return MOE_ERR_DEVICE;
+  if (xq && S) e = cudaMemcpyAsync(xq, r.xq, (size_t)S * plan->d.H, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && xs && S)
+    e = cudaMemcpyAsync(xs, r.xs, (size_t)S * plan->d.H / 32, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   return cuda_status(e);
 }

@@ -95,13 +95,14 @@ template <bool FC2>
 __device__ __forceinline__ uint4 load_a8(const SimtArgs& a, int p, int k) {
   const bool a8 = a.quant == kQuantW4A8;
   if (!FC2) {
-    const int t = a.r.perm[p] / a.topk;
     if (!a8) {
+      const int t = a.r.perm[p] / a.topk;
       return *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.x) +
                                              (size_t)t * a.H + k);
     }
-    const uint2 q = *reinterpret_cast<const uint2*>(a.r.xq + (size_t)t * a.H + k);
-    const float sc = e8m0_to_f32(a.r.xs[(size_t)t * (a.H / 32) + k / 32]);
+    // quantised activations are stored in slot order
+    const uint2 q = *reinterpret_cast<const uint2*>(a.r.xq + (size_t)p * a.H + k);
+    const float sc = e8m0_to_f32(a.r.xs[(size_t)p * (a.H / 32) + k / 32]);
     uint32_t qq[2] = {q.x, q.y};
     uint32_t o[4];
 #pragma unroll

@@ -1,0 +1,522 @@
+// gemm_tc.cu - W4A8 grouped GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// fc1 and fc2 of the routed MoE (moe_b12x_next.py module docstring: MXFP4 weights, in-kernel
+// MXFP8 activations) as block-scaled MMAs of kind::mxf8f6f4: A = weights (E2M1, UE8M0 scale per
+// 32 along K), B = activations (E4M3, UE8M0 per 32), fp32 accumulators in TMEM.
+//
+// Orientation ("swap AB"): the 128 rows of an MMA are weight rows (output features) and the N
+// columns are the tile's tokens (slot positions of one expert), so decode calls with a handful
+// of tokens per expert still use full 128-row MMAs and stream each touched weight byte once.
+//
+// Per CTA: one tile (<= BN slot positions of one expert) x one 128-row block of weights x one
+// K range.  Warp roles in the main loop: warp 0 lane 0 issues TMA (weights and activations)
+// and bulk copies (weight scale atoms); warp 2 writes the activations' scale atoms; warp 1
+// lane 0 issues tcgen05.cp (scales -> TMEM) and tcgen05.mma.  All four warps run the
+// epilogue from TMEM (lane = weight row, column = token).
+//
+// fc1 epilogue: h = SwiGLU(gate, up) (clamped), requantised to MXFP8 per 32 intermediate
+// columns (the 32 rows of a warp), written as the fc2 activation operand.  With split K the
+// partial sums go to an fp32 buffer and the last CTA of the unit (atomic ticket, no waiting)
+// runs the epilogue.
+// fc2 epilogue: the combine (fp32 atomics into the token's row, or the weighted slot row of
+// the deterministic route buffer).
+#include <algorithm>
+
+#include "moe_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+using namespace tc;
+
+constexpr int kTcThreads = 128;
+constexpr int kTileBytesA = 128 * 128;   // 128 rows x 128 K of padded FP4 (1 byte / element)
+
+template <int BN>
+struct TcCfg {
+  static constexpr int kB = BN * 128;                         // activation tile bytes
+  static constexpr int kStage1 = (2 * kTileBytesA + kB + 3 * 512 + 1023) / 1024 * 1024;
+  static constexpr int kStage2 = (kTileBytesA + kB + 2 * 512 + 1023) / 1024 * 1024;
+  static constexpr int kStages1 = BN <= 32 ? 5 : (BN <= 64 ? 4 : 3);
+  static constexpr int kStages2 = BN <= 32 ? 5 : 4;
+  static constexpr int kCols1 = 2 * BN + 12 * kStages1;       // D_up, D_gate, scale ring
+  static constexpr int kCols2 = BN + 8 * kStages2;
+  static constexpr int pow2(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
+  static constexpr int kAlloc1 = pow2(kCols1);
+  static constexpr int kAlloc2 = pow2(kCols2);
+  static constexpr int kSmem1 = kStages1 * kStage1 + 1024;
+  static constexpr int kSmem2 = kStages2 * kStage2 + 1024;
+};
+
+struct TcFc1Params {
+  CUtensorMap tm_w13;        // packed FP4 [2E][I][H], box 128 x 128 x 1
+  CUtensorMap tm_x;          // E4M3 [Sm][H], box 128 x BN
+  const uint8_t* sf13;       // weight scale atoms [E][2][RT][KT][512]
+  const uint8_t* xs;         // activation scales [Sm][H/32]
+  const int4* tiles;
+  const int32_t* ctrl;
+  int32_t* err;
+  uint8_t* hq;               // [Sm][Ip]
+  uint8_t* hs;               // [Sm][Ip/32]
+  float* gacc;               // [Sm][2][Ip] split-K partial sums
+  int32_t* tickets;          // [max_tiles][RT]
+  int H, I, Ip, RT, KT, Sm, splits;
+  float limit, alpha, beta;
+};
+
+struct TcFc2Params {
+  CUtensorMap tm_w2;         // packed FP4 [E][H][Ip], box 128 x 128 x 1
+  CUtensorMap tm_h;          // E4M3 [Sm][Ip], box 128 x BN
+  const uint8_t* sf2;        // weight scale atoms [E][H/128][Ip/128][512]
+  const uint8_t* hs;         // [Sm][Ip/32]
+  const int4* tiles;
+  const int32_t* ctrl;
+  int32_t* err;
+  const int32_t* perm;
+  const float* topk_w;
+  float* acc;                // [M][H] atomic mode
+  float* rbuf;               // [M*k][H] deterministic mode
+  int H, Ip, KT, Sm, topk, deterministic;
+};
+
+// Scale atoms of BN activation rows for one 128-wide K tile: byte (n%32)*16 + (n/32)*4 + kb.
+template <int BN>
+__device__ __forceinline__ void write_act_sf(uint8_t* dst, const uint8_t* xs, int row0, int Sm,
+                                             int kblocks, int kt, int lane) {
+#pragma unroll
+  for (int n = lane; n < BN; n += 32) {
+    uint32_t v = 0;
+    if (row0 + n < Sm)
+      v = *reinterpret_cast<const uint32_t*>(xs + (size_t)(row0 + n) * kblocks + kt * 4);
+    *reinterpret_cast<uint32_t*>(dst + (n & 31) * 16 + (n >> 5) * 4) = v;
+  }
+}
+
+__device__ __forceinline__ float swiglu(float gate, float up, float limit, float alpha,
+                                        float beta) {
+  const float g = fminf(gate, limit);
+  const float u = fminf(fmaxf(up, -limit), limit);
+  return g / (1.0f + expf(-alpha * g)) * (u + beta);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// h of one token column for the 32 features of this warp -> MXFP8 code + scale.
+__device__ __forceinline__ void requant_store(float h, int lane, size_t row_base_q,
+                                              size_t row_base_s, int f, uint8_t* hq,
+                                              uint8_t* hs) {
+  const float amax = warp_max(fabsf(h));
+  const uint32_t s = mx_scale_byte(amax);
+  hq[row_base_q + f] = (uint8_t)f32_to_e4m3(h * e8m0_inv_f32(s));
+  if (lane == 0) hs[row_base_s + (f >> 5)] = (uint8_t)s;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kTcThreads, 1)
+fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
+  using Cfg = TcCfg<BN>;
+  constexpr int S = Cfg::kStages1;
+  const int tile = blockIdx.x;
+  if (tile >= p.ctrl[1]) return;
+  const int4 td = p.tiles[tile];
+  const int e = td.x, p0 = td.y, n = td.z;
+  const int fb = blockIdx.y, split = blockIdx.z;
+  const int kt0 = split * p.KT / p.splits, kt1 = (split + 1) * p.KT / p.splits;
+  const int nk = kt1 - kt0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full[S], empty[S], done;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_last;
+
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, Cfg::kAlloc1);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 2);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&done, 1);
+    fence_barrier_init();
+  }
+  if (tid == 64) prefetch_tmap(&p.tm_w13);
+  if (tid == 96) prefetch_tmap(&p.tm_x);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  bool ok = true;
+
+  auto stage = [&](int s) { return smem + s * Cfg::kStage1; };
+  // stage layout: A_up | A_gate | B | SFA_up | SFA_gate | SFB
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int i = 0; i < nk && ok; ++i) {
+        const int s = i % S;
+        if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
+        if (!ok) break;
+        uint8_t* st = stage(s);
+        const int kt = kt0 + i;
+        mbar_arrive_expect_tx(&full[s], 2 * kTileBytesA + Cfg::kB + 2 * 512);
+        tma_load_3d(st, &p.tm_w13, kt * 128, fb * 128, 2 * e + 0, &full[s]);
+        tma_load_3d(st + kTileBytesA, &p.tm_w13, kt * 128, fb * 128, 2 * e + 1, &full[s]);
+        tma_load_2d(st + 2 * kTileBytesA, &p.tm_x, kt * 128, p0, &full[s]);
+        const size_t a_up = ((size_t)(2 * e) * p.RT + fb) * p.KT + kt;
+        const size_t a_gt = ((size_t)(2 * e + 1) * p.RT + fb) * p.KT + kt;
+        bulk_load(st + 2 * kTileBytesA + Cfg::kB, p.sf13 + a_up * 512, 512, &full[s]);
+        bulk_load(st + 2 * kTileBytesA + Cfg::kB + 512, p.sf13 + a_gt * 512, 512, &full[s]);
+      }
+    }
+  } else if (warp == 2) {
+    for (int i = 0; i < nk && ok; ++i) {
+      const int s = i % S;
+      if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
+      if (!ok) break;
+      write_act_sf<BN>(stage(s) + 2 * kTileBytesA + Cfg::kB + 1024, p.xs, p0, p.Sm, p.H / 32,
+                       kt0 + i, lane);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[s]);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int i = 0; i < nk && ok; ++i) {
+        const int s = i % S;
+        ok = mbar_wait(&full[s], (i / S) & 1, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        uint8_t* st = stage(s);
+        const uint32_t sf = tmem + 2 * BN + 12 * s;
+        tc_cp_sf(sf + 0, desc_sf(st + 2 * kTileBytesA + Cfg::kB));
+        tc_cp_sf(sf + 4, desc_sf(st + 2 * kTileBytesA + Cfg::kB + 512));
+        tc_cp_sf(sf + 8, desc_sf(st + 2 * kTileBytesA + Cfg::kB + 1024));
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) {
+          const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, BN, kb);
+          const uint64_t bdesc = desc_sw128(st + 2 * kTileBytesA + 32 * kb);
+          const uint32_t acc = (i > 0 || kb > 0) ? 1u : 0u;
+          mma_mxf8f6f4(tmem, desc_sw128(st + 32 * kb), bdesc, idesc, sf + 0, sf + 8, acc);
+          mma_mxf8f6f4(tmem + BN, desc_sw128(st + kTileBytesA + 32 * kb), bdesc, idesc, sf + 4,
+                       sf + 8, acc);
+        }
+        tc_commit(&empty[s]);
+      }
+      tc_commit(&done);
+    }
+  }
+
+  // ---- epilogue: all four warps, thread = weight row (feature), columns = tokens
+  __syncwarp();
+  ok = mbar_wait(&done, 0, p.err) && ok;
+  tc_fence_after();
+  __syncwarp();
+  const int f = fb * 128 + warp * 32 + lane;          // intermediate feature of this lane
+  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  if (ok && nk > 0) {
+    if (p.splits == 1) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float up[16], gt[16];
+        tmem_ld16(trow + c0, up);
+        tmem_ld16(trow + BN + c0, gt);
+        if (c0 >= n) continue;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (c0 + j < n) {
+            const float h = f < p.I ? swiglu(gt[j], up[j], p.limit, p.alpha, p.beta) : 0.f;
+            const size_t row = (size_t)(p0 + c0 + j);
+            requant_store(h, lane, row * p.Ip, row * (p.Ip / 32), f, p.hq, p.hs);
+          }
+        }
+      }
+    } else {
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float up[16], gt[16];
+        tmem_ld16(trow + c0, up);
+        tmem_ld16(trow + BN + c0, gt);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (c0 + j < n) {
+            float* g = p.gacc + (size_t)(p0 + c0 + j) * 2 * p.Ip;
+            atomicAdd(g + f, up[j]);
+            atomicAdd(g + p.Ip + f, gt[j]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, Cfg::kAlloc1);
+  if (p.splits > 1) {
+    if (tid == 0) {
+      __threadfence();
+      const int t = atomicAdd(&p.tickets[tile * p.RT + fb], 1);
+      s_last = (t == p.splits - 1);
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      for (int c = 0; c < n; ++c) {
+        const float* g = p.gacc + (size_t)(p0 + c) * 2 * p.Ip;
+        const float up = __ldcg(g + f), gt = __ldcg(g + p.Ip + f);
+        const float h = f < p.I ? swiglu(gt, up, p.limit, p.alpha, p.beta) : 0.f;
+        const size_t row = (size_t)(p0 + c);
+        requant_store(h, lane, row * p.Ip, row * (p.Ip / 32), f, p.hq, p.hs);
+      }
+    }
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kTcThreads, 1)
+fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
+  using Cfg = TcCfg<BN>;
+  constexpr int S = Cfg::kStages2;
+  const int tile = blockIdx.x;
+  if (tile >= p.ctrl[1]) return;
+  const int4 td = p.tiles[tile];
+  const int e = td.x, p0 = td.y, n = td.z;
+  const int rt = blockIdx.y;
+  const int nk = p.KT;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full[S], empty[S], done;
+  __shared__ uint32_t s_tmem;
+
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, Cfg::kAlloc2);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 2);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&done, 1);
+    fence_barrier_init();
+  }
+  if (tid == 64) prefetch_tmap(&p.tm_w2);
+  if (tid == 96) prefetch_tmap(&p.tm_h);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  bool ok = true;
+  auto stage = [&](int s) { return smem + s * Cfg::kStage2; };
+  // stage layout: A | B | SFA | SFB
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int i = 0; i < nk && ok; ++i) {
+        const int s = i % S;
+        if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
+        if (!ok) break;
+        uint8_t* st = stage(s);
+        mbar_arrive_expect_tx(&full[s], kTileBytesA + Cfg::kB + 512);
+        tma_load_3d(st, &p.tm_w2, i * 128, rt * 128, e, &full[s]);
+        tma_load_2d(st + kTileBytesA, &p.tm_h, i * 128, p0, &full[s]);
+        const size_t a = ((size_t)e * (p.H / 128) + rt) * p.KT + i;
+        bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
+      }
+    }
+  } else if (warp == 2) {
+    for (int i = 0; i < nk && ok; ++i) {
+      const int s = i % S;
+      if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
+      if (!ok) break;
+      write_act_sf<BN>(stage(s) + kTileBytesA + Cfg::kB + 512, p.hs, p0, p.Sm, p.Ip / 32, i,
+                       lane);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[s]);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int i = 0; i < nk && ok; ++i) {
+        const int s = i % S;
+        ok = mbar_wait(&full[s], (i / S) & 1, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        uint8_t* st = stage(s);
+        const uint32_t sf = tmem + BN + 8 * s;
+        tc_cp_sf(sf + 0, desc_sf(st + kTileBytesA + Cfg::kB));
+        tc_cp_sf(sf + 4, desc_sf(st + kTileBytesA + Cfg::kB + 512));
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) {
+          const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, BN, kb);
+          mma_mxf8f6f4(tmem, desc_sw128(st + 32 * kb), desc_sw128(st + kTileBytesA + 32 * kb),
+                       idesc, sf + 0, sf + 4, (i > 0 || kb > 0) ? 1u : 0u);
+        }
+        tc_commit(&empty[s]);
+      }
+      tc_commit(&done);
+    }
+  }
+
+  __syncwarp();
+  ok = mbar_wait(&done, 0, p.err) && ok;
+  tc_fence_after();
+  __syncwarp();
+  const int h = rt * 128 + warp * 32 + lane;          // output column of this lane
+  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  if (ok) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      float y[16];
+      tmem_ld16(trow + c0, y);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (c0 + j < n) {
+          const int f = p.perm[p0 + c0 + j];
+          const float v = p.topk_w[f] * y[j];
+          if (p.deterministic)
+            p.rbuf[(size_t)f * p.H + h] = v;
+          else
+            atomicAdd(&p.acc[(size_t)(f / p.topk) * p.H + h], v);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, Cfg::kAlloc2);
+}
+
+// ---------------------------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// Packed FP4 weights [mats][rows][K] (K elements per row, 2 per byte) as a 3-D tensor map with
+// 128 x 128 boxes expanded to one byte per element in shared memory.
+static bool tmap_fp4(CUtensorMap* tm, const void* base, int K, int rows, int mats) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)mats};
+  cuuint64_t strides[2] = {(cuuint64_t)K / 2, (cuuint64_t)K / 2 * rows};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims, strides,
+             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Byte matrix [rows][K] (E4M3 activations), boxes of 128 x box_rows.
+static bool tmap_u8(CUtensorMap* tm, const void* base, int K, int rows, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct TcLaunch {
+  int bn;          // tokens per tile (16, 32, 64, 128)
+  int tiles;       // grid bound on the tile count of this call
+  int splits;      // fc1 split K
+};
+
+int tc_pick_bn(int M, int topk) {
+  (void)topk;
+  return M <= 16 ? 16 : (M <= 64 ? 32 : (M <= 512 ? 64 : 128));
+}
+
+template <int BN>
+static cudaError_t launch_fc1_bn(const TcFc1Params& p, int tiles, cudaStream_t st) {
+  using Cfg = TcCfg<BN>;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(fc1_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Cfg::kSmem1);
+    attr = true;
+  }
+  dim3 grid(tiles, p.RT, p.splits);
+  fc1_tc_kernel<BN><<<grid, kTcThreads, Cfg::kSmem1, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int BN>
+static cudaError_t launch_fc2_bn(const TcFc2Params& p, int tiles, cudaStream_t st) {
+  using Cfg = TcCfg<BN>;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(fc2_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Cfg::kSmem2);
+    attr = true;
+  }
+  dim3 grid(tiles, p.H / 128);
+  fc2_tc_kernel<BN><<<grid, kTcThreads, Cfg::kSmem2, st>>>(p);
+  return cudaGetLastError();
+}
+
+// fc1 (stage 0) or fc2 (stage 1) of the W4A8 tensor-core path.
+cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
+                            int bn, int tiles, int splits, const float* topk_w, int M,
+                            cudaStream_t st) {
+  const int Sm = M * d.topk;
+  const int RT = cdiv(d.I, 128);
+  if (stage == 0) {
+    TcFc1Params p;
+    if (!tmap_fp4(&p.tm_w13, w.w13, d.H, d.I, 2 * d.E)) return cudaErrorInvalidValue;
+    if (!tmap_u8(&p.tm_x, r.xq, d.H, Sm, bn)) return cudaErrorInvalidValue;
+    p.sf13 = w.s13; p.xs = r.xs; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
+    p.hq = r.hq; p.hs = r.hs; p.gacc = r.g; p.tickets = r.tickets;
+    p.H = d.H; p.I = d.I; p.Ip = d.Ip; p.RT = RT; p.KT = d.H / 128; p.Sm = Sm;
+    p.splits = splits; p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
+    switch (bn) {
+      case 16: return launch_fc1_bn<16>(p, tiles, st);
+      case 32: return launch_fc1_bn<32>(p, tiles, st);
+      case 64: return launch_fc1_bn<64>(p, tiles, st);
+      default: return launch_fc1_bn<128>(p, tiles, st);
+    }
+  }
+  TcFc2Params p;
+  if (!tmap_fp4(&p.tm_w2, w.w2, d.Ip, d.H, d.E)) return cudaErrorInvalidValue;
+  if (!tmap_u8(&p.tm_h, r.hq, d.Ip, Sm, bn)) return cudaErrorInvalidValue;
+  p.sf2 = w.s2; p.hs = r.hs; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
+  p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;
+  p.H = d.H; p.Ip = d.Ip; p.KT = d.Ip / 128; p.Sm = Sm; p.topk = d.topk;
+  p.deterministic = d.deterministic;
+  switch (bn) {
+    case 16: return launch_fc2_bn<16>(p, tiles, st);
+    case 32: return launch_fc2_bn<32>(p, tiles, st);
+    case 64: return launch_fc2_bn<64>(p, tiles, st);
+    default: return launch_fc2_bn<128>(p, tiles, st);
+  }
+}
+
+}  // namespace moe

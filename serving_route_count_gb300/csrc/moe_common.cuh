@@ -81,8 +81,9 @@ struct Scratch {
   size_t perm;      // int32[Sm]
   size_t slot_of;   // int32[Sm]
   size_t tiles;     // int4[max_tiles] {expert, first position, count, 0}
-  size_t xq, xs;    // W4A8: u8 [max_m][H], u8 [max_m][H/32]
-  size_t g;         // fp32 [Sm][2I]   fc1 output
+  size_t xq, xs;    // W4A8: u8 [Sm][H], u8 [Sm][H/32], one row per slot position
+  size_t g;         // fp32 [Sm][2][Ip]: fc1 output (CUDA-core path) / split-K partial sums
+  size_t tickets;   // int32 [max_tiles][ceil(I/128)] split-K completion tickets
   size_t hq, hs;    // W4A8: u8 [Sm][Ip], u8 [Sm][Ip/32]
   size_t h16;       // W4A16: bf16 [Sm][Ip]
   size_t acc;       // fp32 [max_m][H]  (atomic combine)
@@ -94,6 +95,7 @@ struct Scratch {
 struct PlanDims {
   int E, H, I, Ip, topk, max_m, quant, deterministic;
   float limit, alpha, beta;
+  int backend;      // 0: tensor cores where implemented, 1: CUDA-core path
 };
 
 // Pointers of one call, resolved from the scratch base.
@@ -107,6 +109,7 @@ struct RunPtrs {
   uint8_t* xq;
   uint8_t* xs;
   float* g;
+  int32_t* tickets;
   uint8_t* hq;
   uint8_t* hs;
   __nv_bfloat16* h16;

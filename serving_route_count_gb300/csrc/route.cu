@@ -143,49 +143,63 @@ route_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile_slots, int
   }
 }
 
-// MXFP8 quantisation of x (W4A8): one thread per block of 32 elements.
-// Also clears the fp32 combine buffer (atomic mode) so that one launch prepares both.
+// MXFP8 quantisation of x (W4A8) into slot order: one thread per block of 32 elements of the
+// row of the token that owns slot position p, so every GEMM tile reads contiguous rows.
+// The same launch clears the buffers that the later stages accumulate into.
+struct ZeroRegion {
+  void* ptr;
+  size_t words;   // 4-byte words, a multiple of 4
+};
+
 __global__ void __launch_bounds__(256)
-actq_kernel(const __nv_bfloat16* __restrict__ x, int M, int H, uint8_t* __restrict__ xq,
-            uint8_t* __restrict__ xs, float* __restrict__ acc, size_t acc_elems) {
-  const size_t nblk = (size_t)M * (H / 32);
+actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t* __restrict__ ctrl,
+            const int32_t* __restrict__ perm, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
+            ZeroRegion z0, ZeroRegion z1, ZeroRegion z2) {
   const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t gsz = (size_t)gridDim.x * blockDim.x;
   if (xq != nullptr) {
-    for (size_t b = gtid; b < nblk; b += gsz) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + b * 32);
+    const int nb = H / 32;
+    const size_t nblk = (size_t)ctrl[2] * nb;
+    for (size_t i = gtid; i < nblk; i += gsz) {
+      const size_t p = i / nb;
+      const int b = (int)(i % nb);
+      const int t = perm[p] / topk;
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H + b * 32);
       float v[32];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint4 u = src[q];
         uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          v[q * 8 + 2 * i] = __uint_as_float(w[i] << 16);
-          v[q * 8 + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        for (int j = 0; j < 4; ++j) {
+          v[q * 8 + 2 * j] = __uint_as_float(w[j] << 16);
+          v[q * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
         }
       }
       float amax = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
       const uint32_t s = mx_scale_byte(amax);
       const float inv = e8m0_inv_f32(s);
       uint32_t packed[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        packed[i] = f32_to_e4m3(v[4 * i] * inv) | (f32_to_e4m3(v[4 * i + 1] * inv) << 8) |
-                    (f32_to_e4m3(v[4 * i + 2] * inv) << 16) |
-                    (f32_to_e4m3(v[4 * i + 3] * inv) << 24);
+      for (int j = 0; j < 8; ++j) {
+        packed[j] = f32_to_e4m3(v[4 * j] * inv) | (f32_to_e4m3(v[4 * j + 1] * inv) << 8) |
+                    (f32_to_e4m3(v[4 * j + 2] * inv) << 16) |
+                    (f32_to_e4m3(v[4 * j + 3] * inv) << 24);
       }
-      uint4* dst = reinterpret_cast<uint4*>(xq + b * 32);
+      uint4* dst = reinterpret_cast<uint4*>(xq + p * H + b * 32);
       dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
       dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-      xs[b] = (uint8_t)s;
+      xs[p * nb + b] = (uint8_t)s;
     }
   }
-  if (acc != nullptr) {
-    float4* a4 = reinterpret_cast<float4*>(acc);
-    for (size_t i = gtid; i < acc_elems / 4; i += gsz) a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const ZeroRegion zs[3] = {z0, z1, z2};
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    if (zs[r].ptr == nullptr) continue;
+    uint4* a4 = reinterpret_cast<uint4*>(zs[r].ptr);
+    for (size_t i = gtid; i < zs[r].words / 4; i += gsz) a4[i] = make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -196,14 +210,18 @@ cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int 
   return cudaGetLastError();
 }
 
-cudaError_t launch_actq(const void* x, int M, int H, const RunPtrs& r, bool quant_x,
-                        size_t acc_elems, cudaStream_t st) {
-  const size_t work = std::max<size_t>(quant_x ? (size_t)M * (H / 32) : 0, acc_elems / 4);
+cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
+                        void* z0, size_t z0_words, void* z1, size_t z1_words, void* z2,
+                        size_t z2_words, cudaStream_t st) {
+  const size_t work = std::max(std::max(quant_x ? (size_t)M * topk * (H / 32) : (size_t)0,
+                                        z0_words / 4),
+                               std::max(z1_words / 4, z2_words / 4));
   int blocks = (int)std::min<size_t>((work + 255) / 256, 152 * 8);
   if (blocks < 1) blocks = 1;
-  actq_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), M, H,
-                                      quant_x ? r.xq : nullptr, quant_x ? r.xs : nullptr,
-                                      acc_elems ? r.acc : nullptr, acc_elems);
+  actq_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), H, topk, r.ctrl,
+                                      r.perm, quant_x ? r.xq : nullptr, quant_x ? r.xs : nullptr,
+                                      ZeroRegion{z0, z0_words}, ZeroRegion{z1, z1_words},
+                                      ZeroRegion{z2, z2_words});
   return cudaGetLastError();
 }
 

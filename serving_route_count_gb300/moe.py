@@ -105,6 +105,10 @@ def moe_plan_set_swiglu_alpha_beta(plan, alpha, beta):
            "moe_plan_set_swiglu_alpha_beta")
 
 
+def moe_plan_set_backend(plan, backend):
+    _check(_lib.load().moe_plan_set_backend(_handle(plan), int(backend)), "moe_plan_set_backend")
+
+
 def moe_scratch_bytes(plan) -> int:
     n = ctypes.c_size_t()
     _check(_lib.load().moe_scratch_bytes(_handle(plan), ctypes.byref(n)), "moe_scratch_bytes")
@@ -155,9 +159,10 @@ def moe_debug_routing(plan, scratch, M, E, topk, stream=None):
     return cnt, off, perm[: off[E]], slot_of[: M * topk]
 
 
-def moe_debug_actq(plan, scratch, M, H, stream=None):
-    xq = np.zeros((M, H), np.uint8)
-    xs = np.zeros((M, H // 32), np.uint8)
+def moe_debug_actq(plan, scratch, M, H, topk, stream=None):
+    """Quantised activations in slot order: row p is the MXFP8 row of token perm[p] // topk."""
+    xq = np.zeros((max(1, M * topk), H), np.uint8)
+    xs = np.zeros((max(1, M * topk), H // 32), np.uint8)
     _check(_lib.load().moe_debug_actq(_handle(plan), _ptr(scratch), int(M), _ptr(xq), _ptr(xs),
                                       _stream(stream)), "moe_debug_actq")
     return xq, xs
@@ -221,7 +226,7 @@ class MoELayer:
     """
 
     def __init__(self, ck, topk, max_m, swiglu_limit=float("inf"), deterministic=False,
-                 alpha=None, beta=None, device="cuda", keep_checkpoint=False):
+                 alpha=None, beta=None, device="cuda", keep_checkpoint=False, backend=0):
         self.E, self.H, self.I, self.topk, self.max_m = ck.E, ck.H, ck.I, topk, max_m
         self.quant = QUANT_OF[ck.quant]
         tier = ck.tier if ck.quant == "hybrid" else None
@@ -238,6 +243,8 @@ class MoELayer:
         if alpha is not None or beta is not None:
             moe_plan_set_swiglu_alpha_beta(self.plan, 1.0 if alpha is None else alpha,
                                            0.0 if beta is None else beta)
+        if backend:
+            moe_plan_set_backend(self.plan, backend)
         self.scratch = torch.empty(moe_scratch_bytes(self.plan), dtype=torch.uint8, device=device)
         self.device = device
         self._io = None
@@ -259,7 +266,10 @@ class MoELayer:
         return moe_debug_routing(self.plan, self.scratch, M, self.E, self.topk, stream)
 
     def actq(self, M, stream=None):
-        return moe_debug_actq(self.plan, self.scratch, M, self.H, stream)
+        """(xq, xs) of the last call in slot order, trimmed to the S valid slots."""
+        S = int(self.routing(M, stream)[1][-1])
+        xq, xs = moe_debug_actq(self.plan, self.scratch, M, self.H, self.topk, stream)
+        return xq[:S], xs[:S]
 
     def device_error(self, stream=None):
         return moe_get_device_error(self.plan, self.scratch, stream)

@@ -51,18 +51,21 @@ def test_tiny_routing_and_actq_bit_exact():
     layer = _layer(ck, cfg.topk, 4, cfg.swiglu_limit, 0)
     run_layer(layer, x, ids, w)
     torch.cuda.synchronize()
-    for a, b in zip(layer.routing(4), O.route(ids, cfg.E)):
+    route = O.route(ids, cfg.E)
+    for a, b in zip(layer.routing(4), route):
         assert np.array_equal(a, b)
     xq, xs = layer.actq(4)
     q, s = C.mxfp8_quantize(C.bf16_bits_to_f64(x))
-    assert np.array_equal(xq, q) and np.array_equal(xs, s)
+    tok = route[2] // cfg.topk
+    assert np.array_equal(xq, q[tok]) and np.array_equal(xs, s[tok])
 
 
 # ---------------------------------------------------------------------------- small, ragged
 
-@pytest.mark.parametrize("quant,det", [("mxfp4", 0), ("mxfp4", 1), ("nvfp4", 0), ("nvfp4", 1),
-                                       ("hybrid", 1), ("hybrid", 0)])
-def test_small_ragged_all_rows(quant, det):
+@pytest.mark.parametrize("quant,det,backend", [("mxfp4", 0, 0), ("mxfp4", 1, 0), ("mxfp4", 0, 1),
+                                               ("nvfp4", 0, 0), ("nvfp4", 1, 0), ("hybrid", 1, 0),
+                                               ("hybrid", 0, 0)])
+def test_small_ragged_all_rows(quant, det, backend):
     """E=16, H=1280 (one full and one partial 1024-wide K chunk), I=192 (fc2 K padded to 256),
     top-4, M=37 with padding rows and out-of-range ids: several tiles per expert and a tail."""
     cfg = small_cfg(quant)
@@ -76,7 +79,7 @@ def test_small_ragged_all_rows(quant, det):
     ids[5, 0] = -5
     w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 2.5)
     limit = 7.0 if quant == "mxfp4" else math.inf
-    layer = _layer(ck, cfg.topk, 40, limit, det)
+    layer = _layer(ck, cfg.topk, 40, limit, det, backend=backend)
     got = run_layer(layer, x, ids, w)
     check_rows(got, ck, x, ids, w, limit)
     cnt, off, perm, slot_of = layer.routing(M)
@@ -85,7 +88,8 @@ def test_small_ragged_all_rows(quant, det):
     if quant == "mxfp4":
         xq, xs = layer.actq(M)
         q, s = C.mxfp8_quantize(C.bf16_bits_to_f64(x))
-        assert np.array_equal(xq, q) and np.array_equal(xs, s)
+        tok = perm // cfg.topk
+        assert np.array_equal(xq, q[tok]) and np.array_equal(xs, s[tok])
 
 
 def test_swiglu_alpha_beta_and_no_clamp():
@@ -182,11 +186,13 @@ def test_decode_full_size_sampled(decode_layer, det):
     x, ids, w = S.make_inputs(cfg, M)
     layer = _layer(ck, cfg.topk, M, cfg.swiglu_limit, det)
     got = run_layer(layer, x, ids, w)
-    for a, b in zip(layer.routing(M), O.route(ids, cfg.E)):
+    route = O.route(ids, cfg.E)
+    for a, b in zip(layer.routing(M), route):
         assert np.array_equal(a, b)
     xq, xs = layer.actq(M)
     q, s = C.mxfp8_quantize(C.bf16_bits_to_f64(x))
-    assert np.array_equal(xq, q) and np.array_equal(xs, s)
+    tok = route[2] // cfg.topk
+    assert np.array_equal(xq, q[tok]) and np.array_equal(xs, s[tok])
     check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=[0, 7, 11, 12, 15])
     layer.close()
 
@@ -211,3 +217,34 @@ def test_hybrid_full_size_sampled():
     got = run_layer(layer, x, ids, w)
     check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=[0, 3, 7])
     layer.close()
+
+
+# ---------------------------------------------------------------------------- tensor-core path
+
+@pytest.mark.parametrize("M,det", [(5, 0), (16, 1), (37, 0), (200, 1), (600, 0)])
+def test_w4a8_tensor_core_tile_widths(M, det):
+    """W4A8 through the tcgen05 kernels at M covering every token-tile width (16, 32, 64, 128)
+    and both fc1 schedules (split K for small M, whole K otherwise); E=16, H=1280 (10 K tiles),
+    I=192 (two 128-row weight blocks, the second half empty), Zipf routing with dropped ids."""
+    cfg = small_cfg("mxfp4")
+    ck = S.make_checkpoint(cfg, seed=1000 + M)
+    rng = np.random.default_rng(2000 + M)
+    x = S.make_x(rng, M, cfg.H)
+    ids = S.zipf_topk(rng, M, cfg.E, cfg.topk, 1.1)
+    ids[rng.random(ids.shape) < 0.05] = -1
+    w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 2.5)
+    layer = _layer(ck, cfg.topk, M, 7.0, det)
+    got = run_layer(layer, x, ids, w)
+    st, code = layer.device_error()
+    assert st == 0 and code == 0, code
+    rows = None if M <= 64 else rng.choice(M, 24, replace=False)
+    check_rows(got, ck, x, ids, w, 7.0, rows=rows)
+    xq, xs = layer.actq(M)
+    _, _, perm, _ = layer.routing(M)
+    q, s = C.mxfp8_quantize(C.bf16_bits_to_f64(x))
+    assert np.array_equal(xq, q[perm // cfg.topk]) and np.array_equal(xs, s[perm // cfg.topk])
+    # the CUDA-core backend computes the same call independently
+    simt = _layer(ck, cfg.topk, M, 7.0, det, backend=1)
+    other = run_layer(simt, x, ids, w)
+    a, b = C.bf16_bits_to_f64(got), C.bf16_bits_to_f64(other)
+    assert np.allclose(a, b, rtol=2e-2, atol=2e-2 * np.sqrt((b ** 2).mean()))
