@@ -206,6 +206,20 @@ def kernel_traffic(kernel):
     return ent
 
 
+def reduce_over_ranks(step_ms: float, tokens: int, world: int, device=None):
+    """Whole-job numbers of a replicated run: the slowest rank's time and the tokens of all
+    ranks (each rank processes its own batches; there is no data-path collective)."""
+    if world <= 1:
+        return step_ms, tokens
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([step_ms], dtype=torch.float64, device=device)
+    n = torch.tensor([tokens], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
 def our_arm(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -293,10 +307,8 @@ def our_arm(args, rank, world):
             dom_bytes += c
             toks += d
     torch.cuda.synchronize()
+    tot_ms, all_toks = reduce_over_ranks(tot_ms, toks, world, device="cuda")
     if world > 1:
-        t = torch.tensor([tot_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
         dist.barrier()
     clocks = clk.summary()
 
@@ -333,7 +345,7 @@ def our_arm(args, rank, world):
     cpu = None if args.no_cpu_baseline else run_cpu_baseline()
     line = {
         "metric": "decode MoE layer tokens/s",
-        "value": toks * world / (tot_ms * 1e-3),
+        "value": all_toks / (tot_ms * 1e-3),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,

@@ -31,6 +31,9 @@ using namespace tc;
 
 constexpr int kTcThreads = 128;
 constexpr int kTileBytesA = 128 * 128;   // 128 rows x 128 K of padded FP4 (1 byte / element)
+// The packed-FP4 TMA format counts the bytes it reads from global memory (two elements per
+// byte) as the transaction size, not the expanded shared-memory footprint.
+constexpr int kTxBytesA = 128 * 128 / 2;
 
 template <int BN>
 struct TcCfg {
@@ -167,7 +170,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
         if (!ok) break;
         uint8_t* st = stage(s);
         const int kt = kt0 + i;
-        mbar_arrive_expect_tx(&full[s], 2 * kTileBytesA + Cfg::kB + 2 * 512);
+        mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512);
         tma_load_3d(st, &p.tm_w13, kt * 128, fb * 128, 2 * e + 0, &full[s]);
         tma_load_3d(st + kTileBytesA, &p.tm_w13, kt * 128, fb * 128, 2 * e + 1, &full[s]);
         tma_load_2d(st + 2 * kTileBytesA, &p.tm_x, kt * 128, p0, &full[s]);
@@ -327,7 +330,7 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
         if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
         if (!ok) break;
         uint8_t* st = stage(s);
-        mbar_arrive_expect_tx(&full[s], kTileBytesA + Cfg::kB + 512);
+        mbar_arrive_expect_tx(&full[s], kTxBytesA + Cfg::kB + 512);
         tma_load_3d(st, &p.tm_w2, i * 128, rt * 128, e, &full[s]);
         tma_load_2d(st + kTileBytesA, &p.tm_h, i * 128, p0, &full[s]);
         const size_t a = ((size_t)e * (p.H / 128) + rt) * p.KT + i;
