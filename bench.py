@@ -47,6 +47,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--det", action="store_true", help="deterministic combine")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile", type=int, default=0, metavar="M",
+                   help="profiling case: eager layer calls at decode size M (no timing)")
+    p.add_argument("--profile-calls", type=int, default=4)
     p.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--sample-m", type=str, default="1,2", help=argparse.SUPPRESS)
     return p.parse_args()
@@ -218,6 +221,27 @@ def reduce_over_ranks(step_ms: float, tokens: int, world: int, device=None):
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     dist.all_reduce(n, op=dist.ReduceOp.SUM)
     return float(t.item()), int(n.item())
+
+
+def profile_case(args):
+    """A small case for ncu: the decode layer (E=384, H=7168, I=576, top-6) called eagerly
+    `--profile-calls` times at M = `--profile`, each call on its own routing set."""
+    import torch
+
+    from serving_route_count_gb300 import MoELayer, build
+    build.build()
+    cfg = S.CONFIGS[DECODE_CFG]
+    ck = S.make_checkpoint(cfg)
+    M = args.profile
+    layer = MoELayer(ck, cfg.topk, M, cfg.swiglu_limit, args.det)
+    del ck
+    for c in range(args.profile_calls):
+        x, ids, w = S.make_inputs(cfg, M, seed=cfg.seed_base + 100 * M + c)
+        xt = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).cuda()
+        layer(xt, torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    st, code = layer.device_error()
+    print(json.dumps({"profile_case": M, "calls": args.profile_calls, "device_error": code}))
 
 
 def our_arm(args, rank, world):
@@ -395,6 +419,9 @@ def main():
     args = parse()
     if args.cpu_baseline_worker:
         cpu_baseline_worker(args)
+        return
+    if args.profile:
+        profile_case(args)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

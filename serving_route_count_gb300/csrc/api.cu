@@ -252,7 +252,7 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   s.xq = a8 ? take(Sm * H) : 0;
   s.xs = a8 ? take(Sm * H / 32) : 0;
   s.g = take(Sm * 2 * d.Ip * 4);
-  s.tickets = take((size_t)s.max_tiles * cdiv(I, 128) * 4);
+  s.tickets = take(align_up((size_t)s.max_tiles * cdiv(I, 128), 4) * 4);
   s.hq = a8 ? take(Sm * d.Ip) : 0;
   s.hs = a8 ? take(Sm * d.Ip / 32) : 0;
   s.h16 = a8 ? 0 : take(Sm * d.Ip * 2);

@@ -259,6 +259,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
       }
     }
   }
+  if (p.splits > 1) __threadfence();   // partial sums visible device-wide before the ticket
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, Cfg::kAlloc1);

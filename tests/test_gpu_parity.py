@@ -237,14 +237,19 @@ def test_w4a8_tensor_core_tile_widths(M, det):
     got = run_layer(layer, x, ids, w)
     st, code = layer.device_error()
     assert st == 0 and code == 0, code
-    rows = None if M <= 64 else rng.choice(M, 24, replace=False)
-    check_rows(got, ck, x, ids, w, 7.0, rows=rows)
+    _, f64 = O.moe_forward(ck, x, ids, w, 7.0, return_f64=True)
+    rel, mx = O.row_errors(got, f64)
+    bad = np.nonzero((rel > 5e-3) | (mx > 2e-2))[0]
+    # the CUDA-core backend computes the same call independently
+    simt = _layer(ck, cfg.topk, M, 7.0, det, backend=1)
+    other = run_layer(simt, x, ids, w)
+    rel2, mx2 = O.row_errors(other, f64)
+    bad2 = np.nonzero((rel2 > 5e-3) | (mx2 > 2e-2))[0]
+    assert bad.size == 0 and bad2.size == 0, (
+        f"tensor-core rows failing: {bad[:20]} rel {rel[bad[:5]]}; "
+        f"CUDA-core rows failing: {bad2[:20]} rel {rel2[bad2[:5]]}; ids of first: "
+        f"{ids[bad[:3]] if bad.size else ids[bad2[:3]]}")
     xq, xs = layer.actq(M)
     _, _, perm, _ = layer.routing(M)
     q, s = C.mxfp8_quantize(C.bf16_bits_to_f64(x))
     assert np.array_equal(xq, q[perm // cfg.topk]) and np.array_equal(xs, s[perm // cfg.topk])
-    # the CUDA-core backend computes the same call independently
-    simt = _layer(ck, cfg.topk, M, 7.0, det, backend=1)
-    other = run_layer(simt, x, ids, w)
-    a, b = C.bf16_bits_to_f64(got), C.bf16_bits_to_f64(other)
-    assert np.allclose(a, b, rtol=2e-2, atol=2e-2 * np.sqrt((b ** 2).mean()))
