@@ -195,6 +195,13 @@ moe_status moe_debug_actq(const moe_plan_t* plan, void* scratch, int M, uint8_t*
 moe_status moe_plan_set_profile_events(moe_plan_t* plan, void* const* events, int n_events);
 const char* moe_profile_stage_names(const moe_plan_t* plan);
 
+/* Test hook: the fc2 activation operand of the last call in slot order (synchronises).
+ * W4A8: hq [S, Ip] E4M3 codes and hs [S, Ip/32] E8M0 bytes (Ip = I rounded up to 128; columns
+ * >= I are zero).  W4A16 / hybrid: hq receives [S, Ip] bf16 values, hs is not written.
+ * Buffers of M*topk rows suffice. */
+moe_status moe_debug_h(const moe_plan_t* plan, void* scratch, int M, void* hq, uint8_t* hs,
+                       void* stream);
+
 void moe_destroy_weight_plan(moe_weight_plan* wp);
 void moe_destroy_prepared(moe_prepared* p);
 void moe_destroy_plan(moe_plan_t* plan);

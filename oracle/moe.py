@@ -188,6 +188,26 @@ def moe_forward(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.
     return bits
 
 
+def slot_intermediate(ck, x_bits, topk_ids, limit=math.inf, alpha=1.0, beta=0.0):
+    """The SwiGLU output h (fp64, before the fc2 quantisation) of every valid slot, in routing
+    order (row p belongs to flat slot perm[p]); shape [S, I]."""
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    M, k = ids.shape
+    a8 = activation_a8(ck)
+    _, _, xhat = quantize_x(np.asarray(x_bits), a8)
+    _, off, perm, _ = route(ids, ck.E)
+    out = np.zeros((perm.shape[0], ck.I))
+    for e in range(ck.E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi == lo:
+            continue
+        W13, _, _ = expert_weights(ck, e)
+        G = xhat[perm[lo:hi] // k] @ W13.T
+        gate, up = split_w13(G, ck.I, ck.layout)
+        out[lo:hi] = swiglu(gate, up, limit, alpha, beta)
+    return out
+
+
 def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.0):
     """Token by token, slot by slot, element by element (pure Python loops; tiny inputs only).
     Dequantises each weight element from its own code and scale with scalar decoders."""

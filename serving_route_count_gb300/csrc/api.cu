@@ -502,6 +502,28 @@ moe_status moe_debug_actq(const moe_plan_t* plan, void* scratch, int M, uint8_t*
   return cuda_status(e);
 }
 
+moe_status moe_debug_h(const moe_plan_t* plan, void* scratch, int M, void* hq, uint8_t* hs,
+                       void* stream) {
+  if (plan == nullptr || scratch == nullptr || M < 0 || M > plan->d.max_m) return MOE_ERR_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const RunPtrs r = resolve(plan, scratch);
+  int32_t S = 0;
+  cudaError_t e = cudaMemcpyAsync(&S, r.ctrl + 2, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (S < 0 || S > M * plan->d.topk) return MOE_ERR_DEVICE;
+  const size_t Ip = plan->d.Ip;
+  if (plan->d.quant == MOE_W4A8_MXFP4) {
+    if (hq && S) e = cudaMemcpyAsync(hq, r.hq, (size_t)S * Ip, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && hs && S)
+      e = cudaMemcpyAsync(hs, r.hs, (size_t)S * Ip / 32, cudaMemcpyDeviceToHost, st);
+  } else if (hq && S) {
+    e = cudaMemcpyAsync(hq, r.h16, (size_t)S * Ip * 2, cudaMemcpyDeviceToHost, st);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return cuda_status(e);
+}
+
 void moe_destroy_weight_plan(moe_weight_plan* wp) { delete wp; }
 void moe_destroy_prepared(moe_prepared* p) { delete p; }
 void moe_destroy_plan(moe_plan_t* plan) { delete plan; }

@@ -35,6 +35,8 @@ constexpr int kTileBytesA = 128 * 128;   // 128 rows x 128 K of padded FP4 (1 by
 // byte) as the transaction size, not the expanded shared-memory footprint.
 constexpr int kTxBytesA = 128 * 128 / 2;
 
+constexpr int kSfChunk = 32;   // K tiles of activation scales staged per batch
+
 template <int BN>
 struct TcCfg {
   static constexpr int kB = BN * 128;                         // activation tile bytes
@@ -47,8 +49,9 @@ struct TcCfg {
   static constexpr int pow2(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
   static constexpr int kAlloc1 = pow2(kCols1);
   static constexpr int kAlloc2 = pow2(kCols2);
-  static constexpr int kSmem1 = kStages1 * kStage1 + 1024;
-  static constexpr int kSmem2 = kStages2 * kStage2 + 1024;
+  static constexpr int kSfStage = BN * kSfChunk * 4;            // staged activation scales
+  static constexpr int kSmem1 = kStages1 * kStage1 + kSfStage + 1024;
+  static constexpr int kSmem2 = kStages2 * kStage2 + kSfStage + 1024;
 };
 
 struct TcFc1Params {
@@ -82,17 +85,30 @@ struct TcFc2Params {
   int H, Ip, KT, Sm, topk, deterministic;
 };
 
-// Scale atoms of BN activation rows for one 128-wide K tile: byte (n%32)*16 + (n/32)*4 + kb.
+// Activation scales of a CTA's BN rows for up to kSfChunk K tiles, staged in shared memory with
+// one batch of independent loads (row n, K tile j -> 4 bytes at stage[n * kSfChunk + j]), so the
+// per-stage scale atoms are built without a global-memory round trip on the critical path.
+
 template <int BN>
-__device__ __forceinline__ void write_act_sf(uint8_t* dst, const uint8_t* xs, int row0, int Sm,
-                                             int kblocks, int kt, int lane) {
-#pragma unroll
-  for (int n = lane; n < BN; n += 32) {
+__device__ __forceinline__ void stage_act_sf(uint32_t* stage, const uint8_t* xs, int row0,
+                                             int Sm, int kblocks, int kt0, int nkt, int lane) {
+  for (int idx = lane; idx < BN * nkt; idx += 32) {
+    const int n = idx / nkt, j = idx - n * nkt;
     uint32_t v = 0;
     if (row0 + n < Sm)
-      v = *reinterpret_cast<const uint32_t*>(xs + (size_t)(row0 + n) * kblocks + kt * 4);
-    *reinterpret_cast<uint32_t*>(dst + (n & 31) * 16 + (n >> 5) * 4) = v;
+      v = __ldg(reinterpret_cast<const uint32_t*>(xs + (size_t)(row0 + n) * kblocks +
+                                                  (kt0 + j) * 4));
+    stage[n * kSfChunk + j] = v;
   }
+}
+
+// Scale atom of BN activation rows for one 128-wide K tile: byte (n%32)*16 + (n/32)*4 + kb.
+template <int BN>
+__device__ __forceinline__ void write_act_sf(uint8_t* dst, const uint32_t* stage, int j,
+                                             int lane) {
+#pragma unroll
+  for (int n = lane; n < BN; n += 32)
+    *reinterpret_cast<uint32_t*>(dst + (n & 31) * 16 + (n >> 5) * 4) = stage[n * kSfChunk + j];
 }
 
 __device__ __forceinline__ float swiglu(float gate, float up, float limit, float alpha,
@@ -181,12 +197,16 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
       }
     }
   } else if (warp == 2) {
+    uint32_t* sfst = reinterpret_cast<uint32_t*>(smem + S * Cfg::kStage1);
     for (int i = 0; i < nk && ok; ++i) {
       const int s = i % S;
+      if (i % kSfChunk == 0) {
+        stage_act_sf<BN>(sfst, p.xs, p0, p.Sm, p.H / 32, kt0 + i, min(kSfChunk, nk - i), lane);
+        __syncwarp();
+      }
       if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
       if (!ok) break;
-      write_act_sf<BN>(stage(s) + 2 * kTileBytesA + Cfg::kB + 1024, p.xs, p0, p.Sm, p.H / 32,
-                       kt0 + i, lane);
+      write_act_sf<BN>(stage(s) + 2 * kTileBytesA + Cfg::kB + 1024, sfst, i % kSfChunk, lane);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[s]);
@@ -339,12 +359,16 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
       }
     }
   } else if (warp == 2) {
+    uint32_t* sfst = reinterpret_cast<uint32_t*>(smem + S * Cfg::kStage2);
     for (int i = 0; i < nk && ok; ++i) {
       const int s = i % S;
+      if (i % kSfChunk == 0) {
+        stage_act_sf<BN>(sfst, p.hs, p0, p.Sm, p.Ip / 32, i, min(kSfChunk, nk - i), lane);
+        __syncwarp();
+      }
       if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
       if (!ok) break;
-      write_act_sf<BN>(stage(s) + kTileBytesA + Cfg::kB + 512, p.hs, p0, p.Sm, p.Ip / 32, i,
-                       lane);
+      write_act_sf<BN>(stage(s) + kTileBytesA + Cfg::kB + 512, sfst, i % kSfChunk, lane);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[s]);

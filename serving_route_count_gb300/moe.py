@@ -168,6 +168,21 @@ def moe_debug_actq(plan, scratch, M, H, topk, stream=None):
     return xq, xs
 
 
+def moe_debug_h(plan, scratch, M, Ip, topk, a8, stream=None):
+    """fc2 activation operand of the last call in slot order: (codes, scales) for W4A8,
+    (bf16 bits, None) otherwise."""
+    rows = max(1, M * topk)
+    if a8:
+        hq = np.zeros((rows, Ip), np.uint8)
+        hs = np.zeros((rows, Ip // 32), np.uint8)
+    else:
+        hq = np.zeros((rows, Ip), np.uint16)
+        hs = None
+    _check(_lib.load().moe_debug_h(_handle(plan), _ptr(scratch), int(M), _ptr(hq), _ptr(hs),
+                                   _stream(stream)), "moe_debug_h")
+    return hq, hs
+
+
 def moe_plan_set_profile_events(plan, events):
     """events: list of torch.cuda.Event(enable_timing=True) (or raw handles); [] turns it off."""
     hs = [ev.cuda_event if hasattr(ev, "cuda_event") else int(ev) for ev in events]
@@ -270,6 +285,14 @@ class MoELayer:
         S = int(self.routing(M, stream)[1][-1])
         xq, xs = moe_debug_actq(self.plan, self.scratch, M, self.H, self.topk, stream)
         return xq[:S], xs[:S]
+
+    def intermediate(self, M, stream=None):
+        """fc2 activation operand of the last call, trimmed to the S valid slots."""
+        S = int(self.routing(M, stream)[1][-1])
+        Ip = (self.I + 127) // 128 * 128
+        hq, hs = moe_debug_h(self.plan, self.scratch, M, Ip, self.topk,
+                             self.quant == MOE_W4A8_MXFP4, stream)
+        return hq[:S], (hs[:S] if hs is not None else None)
 
     def device_error(self, stream=None):
         return moe_get_device_error(self.plan, self.scratch, stream)

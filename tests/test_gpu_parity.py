@@ -253,3 +253,34 @@ def test_w4a8_tensor_core_tile_widths(M, det):
     _, _, perm, _ = layer.routing(M)
     q, s = C.mxfp8_quantize(C.bf16_bits_to_f64(x))
     assert np.array_equal(xq, q[perm // cfg.topk]) and np.array_equal(xs, s[perm // cfg.topk])
+
+
+@pytest.mark.parametrize("backend", [0, 1])
+def test_w4a8_intermediate_requant(backend):
+    """The fc2 operand h -> MXFP8 against the oracle's quantisation of the exact SwiGLU output:
+    codes may differ only where the fp32 h sits within rounding noise of an E4M3 midpoint, so
+    mismatches must be rare and each within one E4M3 step of the exact value."""
+    cfg = small_cfg("mxfp4")
+    M = 600
+    ck = S.make_checkpoint(cfg, seed=1000 + M)
+    rng = np.random.default_rng(2000 + M)
+    x = S.make_x(rng, M, cfg.H)
+    ids = S.zipf_topk(rng, M, cfg.E, cfg.topk, 1.1)
+    w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 2.5)
+    layer = _layer(ck, cfg.topk, M, 7.0, 0, backend=backend)
+    run_layer(layer, x, ids, w)
+    hq, hs = layer.intermediate(M)
+    h = O.slot_intermediate(ck, x, ids, 7.0)
+    q, s = C.mxfp8_quantize(h)
+    I = cfg.I
+    got = C.mxfp8_dequantize(hq[:, :I], hs[:, : I // 32])
+    want = C.mxfp8_dequantize(q, s)
+    mism = got != want
+    rate = float(mism.mean())
+    step = np.repeat(C.e8m0_value(s), 32, axis=1) * 2.0 ** np.floor(
+        np.log2(np.maximum(np.abs(h) / np.repeat(C.e8m0_value(s), 32, axis=1), 2.0 ** -6))) / 8
+    print(f"\nbackend {backend}: requant mismatches {int(mism.sum())} of {mism.size} "
+          f"({rate:.2e}); rows with any: {int(mism.any(axis=1).sum())} of {mism.shape[0]}")
+    assert np.all(np.abs(got - h)[mism] <= 1.0001 * step[mism])
+    assert rate < 2e-3
+    assert np.all(hq[:, I:] == 0)

@@ -263,3 +263,23 @@ def test_synth_recipes():
     cfg = S.CONFIGS["hybrid_nvfp4_nf3"]
     ck = S.make_checkpoint(cfg, E=16, H=64, I=32)
     assert (ck.tier == S.TIER_NVFP4).sum() == 16 or ck.nv.E + ck.nf.E == 16
+
+
+def test_slot_intermediate_matches_direct_dot_products():
+    ck, x, ids, w = _small_case()
+    h = O.slot_intermediate(ck, x, ids, 7.0)
+    _, _, perm, _ = O.route(ids, ck.E)
+    xq, xs = C.mxfp8_quantize(C.bf16_bits_to_f64(x))
+    xhat = C.mxfp8_dequantize(xq, xs)
+    k = ids.shape[1]
+    for p in (0, 5, len(perm) - 1):
+        t, j = divmod(int(perm[p]), k)
+        e = int(ids[t, j])
+        codes = C.unpack_fp4(ck.w13[e])
+        scale = np.repeat(C.e8m0_value(ck.s13[e]), 32, axis=1)
+        rows = C.E2M1_TABLE[codes] * scale
+        up = sum(rows[i] @ xhat[t] for i in [0])          # row 0 of the up half
+        gate = rows[ck.I] @ xhat[t]                         # row 0 of the gate half
+        g = min(gate, 7.0)
+        u = max(-7.0, min(up, 7.0))
+        assert h[p, 0] == pytest.approx(g / (1 + math.exp(-g)) * u, rel=1e-12, abs=1e-12)
