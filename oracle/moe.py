@@ -208,6 +208,41 @@ def slot_intermediate(ck, x_bits, topk_ids, limit=math.inf, alpha=1.0, beta=0.0)
     return out
 
 
+def requant_alternatives(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.0,
+                         rel=1e-4, rows=None):
+    """Legitimate alternatives of the fc2 operand's rounding (reading: where floating point
+    decides a quantised code, arithmetic exact to a relative error `rel` may land on either
+    neighbour of a near-midpoint value).  For every output row (or the given rows) returns a list
+    of fp64 vectors d, one per ambiguous intermediate element of that row's slots, such that
+    rounding that element the other way changes the row's unrounded output by exactly d."""
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    w = np.asarray(topk_w, dtype=np.float64)
+    M, k = ids.shape
+    a8 = activation_a8(ck)
+    h = slot_intermediate(ck, x_bits, ids, limit, alpha, beta)
+    if a8:
+        mask, alt = C.mxfp8_alternates(h, rel)
+        q, s = C.mxfp8_quantize(h)
+        near = C.mxfp8_dequantize(q, s)
+    else:
+        mask, alt = C.bf16_alternates(h, rel)
+        near = C.bf16_round(h)
+    _, _, perm, _ = route(ids, ck.E)
+    want = set(range(M)) if rows is None else set(int(r) for r in rows)
+    out = {r: [] for r in want}
+    cache = {}
+    for p, i in zip(*np.nonzero(mask)):
+        f = int(perm[p])
+        t, j = divmod(f, k)
+        if t not in want:
+            continue
+        e = int(ids[t, j])
+        if e not in cache:
+            cache[e] = expert_weights(ck, e)[1]
+        out[t].append(w[t, j] * (alt[p, i] - near[p, i]) * cache[e][:, i])
+    return out
+
+
 def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.0):
     """Token by token, slot by slot, element by element (pure Python loops; tiny inputs only).
     Dequantises each weight element from its own code and scale with scalar decoders."""

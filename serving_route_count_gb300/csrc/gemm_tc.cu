@@ -92,14 +92,16 @@ struct TcFc2Params {
 template <int BN>
 __device__ __forceinline__ void stage_act_sf(uint32_t* stage, const uint8_t* xs, int row0,
                                              int Sm, int kblocks, int kt0, int nkt, int lane) {
+  // all copies are issued before one wait: a single memory latency per chunk
   for (int idx = lane; idx < BN * nkt; idx += 32) {
     const int n = idx / nkt, j = idx - n * nkt;
-    uint32_t v = 0;
+    uint32_t* dst = stage + n * kSfChunk + j;
     if (row0 + n < Sm)
-      v = __ldg(reinterpret_cast<const uint32_t*>(xs + (size_t)(row0 + n) * kblocks +
-                                                  (kt0 + j) * 4));
-    stage[n * kSfChunk + j] = v;
+      cp_async4(dst, xs + (size_t)(row0 + n) * kblocks + (kt0 + j) * 4);
+    else
+      *dst = 0;
   }
+  cp_async_wait_all();
 }
 
 // Scale atom of BN activation rows for one 128-wide K tile: byte (n%32)*16 + (n/32)*4 + kb.

@@ -62,6 +62,13 @@ TC_DEV bool mbar_wait(uint64_t* b, uint32_t parity, int32_t* err) {
   }
 }
 
+// 4-byte asynchronous global -> shared copy (both addresses 4-byte aligned).
+TC_DEV void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+TC_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 TC_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

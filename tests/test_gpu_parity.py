@@ -237,18 +237,10 @@ def test_w4a8_tensor_core_tile_widths(M, det):
     got = run_layer(layer, x, ids, w)
     st, code = layer.device_error()
     assert st == 0 and code == 0, code
-    _, f64 = O.moe_forward(ck, x, ids, w, 7.0, return_f64=True)
-    rel, mx = O.row_errors(got, f64)
-    bad = np.nonzero((rel > 5e-3) | (mx > 2e-2))[0]
+    check_rows(got, ck, x, ids, w, 7.0)
     # the CUDA-core backend computes the same call independently
     simt = _layer(ck, cfg.topk, M, 7.0, det, backend=1)
-    other = run_layer(simt, x, ids, w)
-    rel2, mx2 = O.row_errors(other, f64)
-    bad2 = np.nonzero((rel2 > 5e-3) | (mx2 > 2e-2))[0]
-    assert bad.size == 0 and bad2.size == 0, (
-        f"tensor-core rows failing: {bad[:20]} rel {rel[bad[:5]]}; "
-        f"CUDA-core rows failing: {bad2[:20]} rel {rel2[bad2[:5]]}; ids of first: "
-        f"{ids[bad[:3]] if bad.size else ids[bad2[:3]]}")
+    check_rows(run_layer(simt, x, ids, w), ck, x, ids, w, 7.0)
     xq, xs = layer.actq(M)
     _, _, perm, _ = layer.routing(M)
     q, s = C.mxfp8_quantize(C.bf16_bits_to_f64(x))
@@ -281,6 +273,8 @@ def test_w4a8_intermediate_requant(backend):
         np.log2(np.maximum(np.abs(h) / np.repeat(C.e8m0_value(s), 32, axis=1), 2.0 ** -6))) / 8
     print(f"\nbackend {backend}: requant mismatches {int(mism.sum())} of {mism.size} "
           f"({rate:.2e}); rows with any: {int(mism.any(axis=1).sum())} of {mism.shape[0]}")
-    assert np.all(np.abs(got - h)[mism] <= 1.0001 * step[mism])
+    amb, alt = C.mxfp8_alternates(h, 1e-4)
+    assert np.all(amb[mism]), "a code differs where the rounding is not decided by fp32 noise"
+    assert np.all(got[mism] == alt[mism])
     assert rate < 2e-3
     assert np.all(hq[:, I:] == 0)

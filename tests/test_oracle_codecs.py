@@ -189,3 +189,21 @@ def test_nf3_dequant_definition():
     want0 = round(m * 256) / 256 * 2 ** e
     assert np.all(d[0, :32] == want0)
     assert np.all(d[0, 32:] == -1.0)
+
+
+def test_rounding_alternates():
+    # scaled block: amax 256 -> scale byte 127 (scale 1); 1.0625 is the midpoint of 1.0 and 1.125
+    v = np.zeros((1, 32))
+    v[0, 0] = 256.0
+    v[0, 1] = 1.0625 * (1 + 1e-6)      # just above the midpoint: nearest is 1.125
+    v[0, 2] = 1.0625 * (1 - 1e-6)      # just below: nearest is 1.0
+    v[0, 3] = 1.03                      # far from a midpoint
+    mask, alt = C.mxfp8_alternates(v, 1e-4)
+    assert mask[0, 1:3].tolist() == [True, True] and not mask[0, 3] and not mask[0, 0]
+    assert alt[0, 1] == 1.0 and alt[0, 2] == 1.125
+    assert alt[0, 3] == C.mxfp8_dequantize(*C.mxfp8_quantize(v))[0, 3]
+    # bf16: 1 + 2^-8 is the midpoint of 1 and 1 + 2^-7
+    b = np.array([1 + 2 ** -8 + 1e-9, 1 + 2 ** -8 - 1e-9, 1.3])
+    mask, alt = C.bf16_alternates(b, 1e-6)
+    assert mask.tolist() == [True, True, False]
+    assert alt[0] == 1.0 and alt[1] == 1 + 2 ** -7 and alt[2] == C.bf16_round(1.3)
