@@ -14,8 +14,8 @@ namespace moe {
 cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int max_tiles,
                          const RunPtrs& r, cudaStream_t st);
 cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
-                        void* z0, size_t z0_words, void* z1, size_t z1_words, void* z2,
-                        size_t z2_words, cudaStream_t st);
+                        bool to_f16, void* z0, size_t z0_words, void* z1, size_t z1_words,
+                        void* z2, size_t z2_words, cudaStream_t st);
 // gemm_tc.cu
 cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                             int bn, int tiles, int splits, const float* topk_w, int M,
@@ -33,6 +33,12 @@ cudaError_t launch_repack_sf_atoms(const void* src, void* dst, int E, int halves
                                    cudaStream_t st);
 cudaError_t launch_repack_nf3(const void* src, void* dst, int E, int halves, int rows, int src_k,
                               int dst_k, int layout, cudaStream_t st);
+cudaError_t launch_repack_nf3_scales(const void* src, void* dst, int E, int halves, int rows,
+                                     int src_k, int dst_k, int layout, cudaStream_t st);
+// gemm_tc16.cu
+cudaError_t launch_tc16_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
+                              int bn, int tiles, int splits, const float* topk_w, int M,
+                              cudaStream_t st);
 }  // namespace moe
 
 using namespace moe;
@@ -146,9 +152,9 @@ moe_status moe_plan_weights(int E, int H, int I, int quant_mode, int w13_layout,
     wp->g2 = take(E4 * 4);
   }
   wp->nf_w13 = take(E3 * 2 * I_ * 3 * H_ / 8);
-  wp->nf_s13 = take(E3 * 2 * I_ * H_ / 32);
+  wp->nf_s13 = take(E3 * 2 * I_ * (size_t)cdiv(H, 256) * 16);
   wp->nf_w2 = take(E3 * H_ * 3 * Ip / 8);
-  wp->nf_s2 = take(E3 * H_ * Ip / 32);
+  wp->nf_s2 = take(E3 * H_ * (size_t)cdiv((int)Ip, 256) * 16);
   wp->tmap = take((size_t)E * 4);
   wp->total = o;
   *out = wp;
@@ -199,8 +205,8 @@ moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* 
   if (nf3) {
     chk(launch_repack_nf3(src->nf_w13, base + wp->nf_w13, E3, 2, I, H, H, L, st));
     chk(launch_repack_nf3(src->nf_w2, base + wp->nf_w2, E3, 1, H, I, Ip, L, st));
-    chk(launch_repack_rows(src->nf_s13, base + wp->nf_s13, E3, 2, I, H / 32, H / 32, L, 0, st));
-    chk(launch_repack_rows(src->nf_s2, base + wp->nf_s2, E3, 1, H, I / 32, Ip / 32, L, 0, st));
+    chk(launch_repack_nf3_scales(src->nf_s13, base + wp->nf_s13, E3, 2, I, H, H, L, st));
+    chk(launch_repack_nf3_scales(src->nf_s2, base + wp->nf_s2, E3, 1, H, I, Ip, L, st));
   }
   if (!wp->tier_map.empty())
     chk(cudaMemcpyAsync(base + wp->tmap, wp->tier_map.data(), wp->tier_map.size() * 4,
@@ -256,6 +262,7 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   s.hq = a8 ? take(Sm * d.Ip) : 0;
   s.hs = a8 ? take(Sm * d.Ip / 32) : 0;
   s.h16 = a8 ? 0 : take(Sm * d.Ip * 2);
+  s.x16 = a8 ? 0 : take(Sm * H * 2);
   s.acc = d.deterministic ? 0 : take((size_t)max_m * H * 4);
   s.rbuf = d.deterministic ? take(Sm * H * 4) : 0;
   s.total = o;
@@ -306,6 +313,7 @@ static RunPtrs resolve(const moe_plan_t* plan, void* scratch) {
   r.hq = a8 ? b + s.hq : nullptr;
   r.hs = a8 ? b + s.hs : nullptr;
   r.h16 = a8 ? nullptr : reinterpret_cast<__nv_bfloat16*>(b + s.h16);
+  r.x16 = a8 ? nullptr : reinterpret_cast<uint16_t*>(b + s.x16);
   r.acc = plan->d.deterministic ? nullptr : reinterpret_cast<float*>(b + s.acc);
   r.rbuf = plan->d.deterministic ? reinterpret_cast<float*>(b + s.rbuf) : nullptr;
   return r;
@@ -335,10 +343,16 @@ moe_status moe_plan_set_profile_events(moe_plan_t* plan, void* const* events, in
 }
 
 static bool use_tc(const PlanDims& d) { return d.backend == 0 && d.quant == MOE_W4A8_MXFP4; }
+// W4A16 / hybrid on tensor cores: the NVFP4 scale rows of fc2 (Ip/16 bytes) must be whole
+// 16-byte units for the tensor maps.
+static bool use_tc16(const PlanDims& d) {
+  return d.backend == 0 && d.quant != MOE_W4A8_MXFP4 && d.Ip % 256 == 0;
+}
 
 const char* moe_profile_stage_names(const moe_plan_t* plan) {
   if (plan == nullptr) return "";
-  return use_tc(plan->d) ? "route,actq,fc1,fc2,finalize" : "route,actq,fc1,act,fc2,finalize";
+  return (use_tc(plan->d) || use_tc16(plan->d)) ? "route,actq,fc1,fc2,finalize"
+                                                 : "route,actq,fc1,act,fc2,finalize";
 }
 
 moe_status moe_plan_set_backend(moe_plan_t* plan, int backend) {
@@ -367,7 +381,8 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   const RunPtrs r = resolve(plan, scratch);
   const ProfRec prof{&plan->prof, st, !plan->prof.empty() && capturing(st)};
   const bool a8 = d.quant == MOE_W4A8_MXFP4;
-  const bool tc = use_tc(d);
+  const bool tc8 = use_tc(d), t16 = use_tc16(d);
+  const bool tc = tc8 || t16;
   const int Sm = M * d.topk;
   const int bn = tc ? tc_pick_bn(M, d.topk) : kSimtSlots;
   // tiles of this call: at most one per slot, and at most ceil(S / bn) + (touched experts)
@@ -389,16 +404,18 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   const size_t g_words = g ? (size_t)Sm * 2 * d.Ip : 0;
   void* tk = (tc && splits > 1) ? r.tickets : nullptr;
   const size_t tk_words = tk ? align_up((size_t)tiles * RT, 4) : 0;
-  if (a8 || acc || g) {
-    e = launch_actq(x, M, d.H, d.topk, r, a8, acc, acc_words, g, g_words, tk, tk_words, st);
+  if (a8 || acc || g || t16) {
+    e = launch_actq(x, M, d.H, d.topk, r, a8, t16, acc, acc_words, g, g_words, tk, tk_words, st);
     if (e != cudaSuccess) return cuda_status(e);
   }
   prof(2);
   if (tc) {
-    e = launch_tc_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st);
+    e = tc8 ? launch_tc_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st)
+            : launch_tc16_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(3);
-    e = launch_tc_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st);
+    e = tc8 ? launch_tc_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st)
+            : launch_tc16_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(4);
     e = launch_simt_stage(3, w, r, d, plan->s.max_tiles, x, topk_weights, out, M, st);

@@ -61,7 +61,8 @@ __device__ __forceinline__ void load_w8(const DevWeights& w, int kind, int le, i
     const uint8_t* base = (FC2 ? w.nf_w2 : w.nf_w13) + rowb * (size_t)(3 * K / 8);
     const uint32_t lo = *reinterpret_cast<const uint16_t*>(base + k / 4);
     const uint32_t hi = base[K / 4 + k / 8];
-    const float sc = e4m3_to_f32((FC2 ? w.nf_s2 : w.nf_s13)[rowb * (K / 32) + k / 32]);
+    const float sc = e4m3_to_f32((FC2 ? w.nf_s2 : w.nf_s13)[rowb * (cdiv(K, 256) * 16) +
+                                                           nf3_scale_byte(k)]);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t c = ((lo >> (2 * i)) & 3u) | (((hi >> i) & 1u) << 2);

@@ -1,0 +1,527 @@
+// gemm_tc16.cu - W4A16 grouped GEMMs (NVFP4 and NF3 weights, 16-bit activations) on the
+// 5th-generation tensor cores.
+//
+// The NVFP4 kept tier and the NF3 tier of the hybrid layer (hybrid_loader.py: NVFP4 =
+// E2M1 x E4M3 scale per 16 x per-expert fp32 global; NF3 = 8-entry LUT x E4M3 scale per 32,
+// `_unpack_nf3`) run with bf16 activations.  There is no block-scaled MMA kind for a 16-bit
+// operand, so the weights are expanded in shared memory ahead of the MMA (tcgen05 kind::f16):
+//   NVFP4: E2M1 x E4M3 has at most 6 significant bits and lies in [2^-10, 2688]: exact in f16;
+//   NF3:   bf16(fp32(LUT[c]) x fp32(scale)) (the page's unpack) is exact in f16 for E4M3 scales;
+//   activations: bf16 values are exact in f16 when |x| <= 65504 (larger values set an error
+//   bit; values below 2^-14 lose low bits as f16 subnormals).
+// So the MMA runs on f16 A and B (both operands must have the same type) with fp32 accumulation,
+// and the per-expert NVFP4 global scale is applied in the fp32 epilogue.
+//
+// Same orientation and work split as the W4A8 kernels (gemm_tc.cu): weight rows are the
+// 128-row MMA operand, the tile's tokens the N columns.  Roles (192 threads):
+//   warp 0 lane 0  TMA: raw packed weights + scales (256-wide K stages), activation tiles
+//                  (64-wide K sub-tiles, 128-byte swizzle);
+//   warp 1 lane 0  tcgen05.mma (4 MMAs of K = 16 per sub-tile and matrix) and commits;
+//   warps 2..5     converters (thread = weight row) writing f16 sub-tiles in the 128-byte
+//                  swizzled K-major layout, then the epilogue from TMEM.
+#include <algorithm>
+#include <cstring>
+
+#include "moe_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+using namespace tc;
+
+constexpr int k16Threads = 192;
+constexpr int k16RawK = 256;              // K elements per raw stage
+constexpr int k16SubK = 64;               // K elements per converted f16 sub-tile (128 B rows)
+constexpr int k16ATile = 128 * 128;       // one converted f16 sub-tile: 128 rows x 128 B
+constexpr int k16RawCodes = 128 * 128;    // raw codes region per matrix (NVFP4: 128 x 128 B)
+constexpr int k16RawScales = 128 * 16;    // raw scales region per matrix (128 rows x 16 B)
+
+__constant__ float c_nf3_lut16[8] = {-1.0f, -0.6047f, -0.3563f, -0.1275f,
+                                     0.1275f, 0.3563f,  0.6047f,  1.0f};
+
+template <int BN, bool FC2>
+struct Tc16Cfg {
+  static constexpr int kMats = FC2 ? 1 : 2;
+  static constexpr int kRaw = kMats * (k16RawCodes + k16RawScales);     // per raw stage
+  static constexpr int kA = kMats * k16ATile;                           // per A slot
+  static constexpr int kB = BN * 128;                                   // per B slot
+  static constexpr int kSr = FC2 ? 4 : (BN <= 32 ? 3 : 2);
+  static constexpr int kSa = FC2 ? 3 : 2;
+  static constexpr int kSb = BN <= 32 ? 8 : (BN <= 64 ? 6 : 4);
+  static constexpr int kSmem = kSr * kRaw + kSa * kA + kSb * kB + 1024;
+  static constexpr int kCols = kMats * BN;
+  static constexpr int kAlloc = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : 256;
+};
+
+struct Tc16Params {
+  // fp4 (NVFP4) tier: codes [mats][rows][K/2] (SW128 boxes of 128 B x 128 rows), scales
+  // [mats][rows][K/16] (boxes of 16 B x 128 rows)
+  CUtensorMap tm_nv_codes, tm_nv_scales;
+  // NF3 tier: per row a 2-bit plane then a 1-bit plane (boxes of 32 B x 128 rows); scales padded
+  // to 16 B per 256-wide K tile (boxes of 16 B x 128 rows)
+  CUtensorMap tm_nf_codes, tm_nf_scales;
+  CUtensorMap tm_act;         // f16 [Sm][K] activations, boxes 64 x BN, 128-byte swizzle
+  const int32_t* tier_map;    // hybrid: (tier << 24) | local; nullptr: every expert NVFP4
+  const float* gscale;        // NVFP4 per-expert global of this matrix ([E4])
+  const int4* tiles;
+  const int32_t* ctrl;
+  int32_t* err;
+  // fc1 outputs
+  uint16_t* h16;              // f16 [Sm][Ip] (bf16-rounded SwiGLU output)
+  float* gacc;                // [Sm][2][Ip] split-K partial sums
+  int32_t* tickets;
+  // fc2 outputs
+  const int32_t* perm;
+  const float* topk_w;
+  float* acc;
+  float* rbuf;
+  int K, R, I, Ip, RB, KT, Sm, splits, topk, deterministic, H, nf3_row_bytes;
+  float limit, alpha, beta;
+};
+
+__device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
+  uint32_t out;
+  asm("{\n .reg .b8 b;\n cvt.u8.u32 b, %1;\n cvt.rn.f16x2.e2m1x2 %0, b;\n}"
+      : "=r"(out)
+      : "r"(byte));
+  return out;
+}
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two_bytes) {
+  uint32_t out;
+  asm("{\n .reg .b16 h;\n cvt.u16.u32 h, %1;\n cvt.rn.f16x2.e4m3x2 %0, h;\n}"
+      : "=r"(out)
+      : "r"(two_bytes));
+  return out;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t f16x2_bcast(uint32_t f16bits) {
+  return (f16bits & 0xFFFFu) | (f16bits << 16);
+}
+
+// NVFP4 row r, K sub-tile q (64 elements) -> 8 chunks of 8 f16 in the 128-byte swizzled row.
+__device__ __forceinline__ void convert_nvfp4_row(const uint8_t* codes, const uint8_t* scales,
+                                                  uint8_t* dst, int r, int q) {
+  const int sw = r & 7;
+  const uint4 c0 = *reinterpret_cast<const uint4*>(codes + r * 128 + (((2 * q) ^ sw) << 4));
+  const uint4 c1 = *reinterpret_cast<const uint4*>(codes + r * 128 + (((2 * q + 1) ^ sw) << 4));
+  const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(scales + r * 16 + q * 4);
+  const uint32_t s01 = cvt_e4m3x2_f16x2(sc4 & 0xFFFF);
+  const uint32_t s23 = cvt_e4m3x2_f16x2(sc4 >> 16);
+  const uint32_t sc[4] = {f16x2_bcast(s01), f16x2_bcast(s01 >> 16), f16x2_bcast(s23),
+                          f16x2_bcast(s23 >> 16)};
+  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t w = words[j];
+    const uint32_t s = sc[j >> 1];
+    uint4 o;
+    o.x = hmul2(cvt_e2m1x2_f16x2(w & 0xFF), s);
+    o.y = hmul2(cvt_e2m1x2_f16x2((w >> 8) & 0xFF), s);
+    o.z = hmul2(cvt_e2m1x2_f16x2((w >> 16) & 0xFF), s);
+    o.w = hmul2(cvt_e2m1x2_f16x2(w >> 24), s);
+    *reinterpret_cast<uint4*>(dst + r * 128 + ((j ^ sw) << 4)) = o;
+  }
+}
+
+// f16 of bf16(fp32(LUT[c]) * scale) for the 8 codes, packed as 4 f16x2 words (codes 2i, 2i+1).
+__device__ __forceinline__ void nf3_table(float scale, uint32_t* t) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a = __bfloat162float(__float2bfloat16_rn(c_nf3_lut16[2 * i] * scale));
+    const float b = __bfloat162float(__float2bfloat16_rn(c_nf3_lut16[2 * i + 1] * scale));
+    t[i] = (uint32_t)__half_as_ushort(__float2half_rn(a)) |
+           ((uint32_t)__half_as_ushort(__float2half_rn(b)) << 16);
+  }
+}
+
+// Two NF3 codes -> f16x2 from the 8-entry table (codes 0..3 in t[0..1], 4..7 in t[2..3]).
+__device__ __forceinline__ uint32_t nf3_pick2(const uint32_t* t, uint32_t c0, uint32_t c1) {
+  const uint32_t l0 = c0 & 3, l1 = c1 & 3;
+  const uint32_t sel = (2 * l0) | ((2 * l0 + 1) << 4) | ((2 * l1) << 8) | ((2 * l1 + 1) << 12);
+  const uint32_t lo = __byte_perm(t[0], t[1], sel);
+  const uint32_t hi = __byte_perm(t[2], t[3], sel);
+  const uint32_t m = ((c0 & 4) ? 0x0000FFFFu : 0u) | ((c1 & 4) ? 0xFFFF0000u : 0u);
+  return (lo & ~m) | (hi & m);
+}
+
+// NF3 row r, K sub-tile q (64 codes) -> 8 chunks of 8 f16.  Raw smem: box0 / box1 = the two
+// 32-byte halves of the 2-bit plane of the 256-wide stage, box2 = its 1-bit plane (32 B).
+__device__ __forceinline__ void convert_nf3_row(const uint8_t* codes, const uint8_t* scales,
+                                                uint8_t* dst, int r, int q) {
+  const int sw = r & 7;
+  const uint4 lo = *reinterpret_cast<const uint4*>(codes + (q >> 1) * 4096 + r * 32 +
+                                                   (q & 1) * 16);
+  const uint2 hi = *reinterpret_cast<const uint2*>(codes + 8192 + r * 32 + q * 8);
+  const uint8_t s0 = scales[r * 16 + q * 2], s1 = scales[r * 16 + q * 2 + 1];
+  uint32_t t0[4], t1[4];
+  nf3_table(e4m3_to_f32(s0), t0);
+  nf3_table(e4m3_to_f32(s1), t1);
+  const uint32_t low[4] = {lo.x, lo.y, lo.z, lo.w};
+  const uint32_t high[2] = {hi.x, hi.y};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t l16 = (low[j >> 1] >> ((j & 1) * 16)) & 0xFFFF;
+    const uint32_t h8 = (high[j >> 2] >> ((j & 3) * 8)) & 0xFF;
+    const uint32_t* t = j < 4 ? t0 : t1;
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t c0 = ((l16 >> (4 * e)) & 3) | (((h8 >> (2 * e)) & 1) << 2);
+      const uint32_t c1 = ((l16 >> (4 * e + 2)) & 3) | (((h8 >> (2 * e + 1)) & 1) << 2);
+      o[e] = nf3_pick2(t, c0, c1);
+    }
+    *reinterpret_cast<uint4*>(dst + r * 128 + ((j ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+__device__ __forceinline__ float swiglu16(float gate, float up, float limit, float alpha,
+                                          float beta) {
+  const float g = fminf(gate, limit);
+  const float u = fminf(fmaxf(up, -limit), limit);
+  return g / (1.0f + expf(-alpha * g)) * (u + beta);
+}
+
+// h (fp32) -> bf16 rounding (the method's intermediate) -> f16 bits for the next MMA.
+__device__ __forceinline__ uint16_t h_to_f16(float h, int32_t* err) {
+  const float hb = __bfloat162float(__float2bfloat16_rn(h));
+  if (fabsf(hb) > 65504.f) atomicOr(err, kErrRange);
+  return __half_as_ushort(__float2half_rn(hb));
+}
+
+template <int BN, bool FC2>
+__global__ void __launch_bounds__(k16Threads, 1)
+gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
+  using Cfg = Tc16Cfg<BN, FC2>;
+  constexpr int kMats = Cfg::kMats;
+  const int tile = blockIdx.x;
+  if (tile >= p.ctrl[1]) return;
+  const int4 td = p.tiles[tile];
+  const int e = td.x, p0 = td.y, n = td.z;
+  const int rb = blockIdx.y, split = blockIdx.z;
+  const int kt0 = split * p.KT / p.splits, kt1 = (split + 1) * p.KT / p.splits;
+  const int nraw = kt1 - kt0;               // raw stages (256-wide K)
+  const int nsub = nraw * 4;                // 64-wide sub-tiles
+  int le = e;
+  bool nf3 = false;
+  if (p.tier_map != nullptr) {
+    const int m = p.tier_map[e];
+    nf3 = (m >> 24) == kTierNF3;
+    le = m & 0xFFFFFF;
+  }
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* raw_base = smem;
+  uint8_t* a_base = raw_base + Cfg::kSr * Cfg::kRaw;
+  uint8_t* b_base = a_base + Cfg::kSa * Cfg::kA;
+  __shared__ __align__(8) uint64_t raw_full[Cfg::kSr], raw_empty[Cfg::kSr];
+  __shared__ __align__(8) uint64_t a_full[Cfg::kSa], a_empty[Cfg::kSa];
+  __shared__ __align__(8) uint64_t b_full[Cfg::kSb], b_empty[Cfg::kSb];
+  __shared__ __align__(8) uint64_t done;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_last;
+
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, Cfg::kAlloc);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int s = 0; s < Cfg::kSr; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], 4);
+    }
+    for (int s = 0; s < Cfg::kSa; ++s) {
+      mbar_init(&a_full[s], 4);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < Cfg::kSb; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
+    }
+    mbar_init(&done, 1);
+    fence_barrier_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  bool ok = true;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int g = 0;   // next activation sub-tile to load
+      for (int i = 0; i < nraw && ok; ++i) {
+        const int s = i % Cfg::kSr;
+        if (i >= Cfg::kSr) ok = mbar_wait(&raw_empty[s], ((i / Cfg::kSr) - 1) & 1, p.err);
+        if (!ok) break;
+        uint8_t* st = raw_base + s * Cfg::kRaw;
+        const int kt = kt0 + i;
+        if (!nf3) {
+          mbar_arrive_expect_tx(&raw_full[s], kMats * (k16RawCodes + k16RawScales));
+          for (int m = 0; m < kMats; ++m) {
+            const int mat = FC2 ? le : 2 * le + m;
+            tma_load_3d(st + m * k16RawCodes, &p.tm_nv_codes, kt * 128, rb * 128, mat,
+                        &raw_full[s]);
+            tma_load_3d(st + kMats * k16RawCodes + m * k16RawScales, &p.tm_nv_scales, kt * 16,
+                        rb * 128, mat, &raw_full[s]);
+          }
+        } else {
+          mbar_arrive_expect_tx(&raw_full[s], kMats * (3 * 4096 + k16RawScales));
+          for (int m = 0; m < kMats; ++m) {
+            const int mat = FC2 ? le : 2 * le + m;
+            uint8_t* c = st + m * k16RawCodes;
+            tma_load_3d(c, &p.tm_nf_codes, kt * 64, rb * 128, mat, &raw_full[s]);
+            tma_load_3d(c + 4096, &p.tm_nf_codes, kt * 64 + 32, rb * 128, mat, &raw_full[s]);
+            tma_load_3d(c + 8192, &p.tm_nf_codes, p.K / 4 + kt * 32, rb * 128, mat,
+                        &raw_full[s]);
+            tma_load_3d(st + kMats * k16RawCodes + m * k16RawScales, &p.tm_nf_scales, kt * 16,
+                        rb * 128, mat, &raw_full[s]);
+          }
+        }
+        // the four activation sub-tiles of this raw stage
+        for (int q = 0; q < 4 && ok; ++q, ++g) {
+          const int sb = g % Cfg::kSb;
+          if (g >= Cfg::kSb) ok = mbar_wait(&b_empty[sb], ((g / Cfg::kSb) - 1) & 1, p.err);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&b_full[sb], Cfg::kB);
+          tma_load_2d(b_base + sb * Cfg::kB, &p.tm_act, kt * k16RawK + q * k16SubK, p0,
+                      &b_full[sb]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((128u >> 4) << 24);
+      for (int g = 0; g < nsub && ok; ++g) {
+        const int sa = g % Cfg::kSa, sb = g % Cfg::kSb;
+        ok = mbar_wait(&a_full[sa], (g / Cfg::kSa) & 1, p.err) &&
+             mbar_wait(&b_full[sb], (g / Cfg::kSb) & 1, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint8_t* A = a_base + sa * Cfg::kA;
+        const uint8_t* B = b_base + sb * Cfg::kB;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bd = desc_sw128(B + 32 * kk);
+          const uint32_t acc = (g > 0 || kk > 0) ? 1u : 0u;
+#pragma unroll
+          for (int m = 0; m < kMats; ++m)
+            mma_f16(tmem + m * BN, desc_sw128(A + m * k16ATile + 32 * kk), bd, idesc, acc);
+        }
+        tc_commit(&a_empty[sa]);
+        tc_commit(&b_empty[sb]);
+      }
+      tc_commit(&done);
+    }
+  } else {
+    // converters: thread = row of the 128-row weight block
+    const int r = tid - 64;
+    int g = 0;
+    for (int i = 0; i < nraw && ok; ++i) {
+      const int s = i % Cfg::kSr;
+      ok = mbar_wait(&raw_full[s], (i / Cfg::kSr) & 1, p.err);
+      if (!ok) break;
+      const uint8_t* st = raw_base + s * Cfg::kRaw;
+      for (int q = 0; q < 4 && ok; ++q, ++g) {
+        const int sa = g % Cfg::kSa;
+        if (g >= Cfg::kSa) ok = mbar_wait(&a_empty[sa], ((g / Cfg::kSa) - 1) & 1, p.err);
+        if (!ok) break;
+        uint8_t* A = a_base + sa * Cfg::kA;
+#pragma unroll
+        for (int m = 0; m < kMats; ++m) {
+          const uint8_t* c = st + m * k16RawCodes;
+          const uint8_t* sc = st + kMats * k16RawCodes + m * k16RawScales;
+          if (nf3)
+            convert_nf3_row(c, sc, A + m * k16ATile, r, q);
+          else
+            convert_nvfp4_row(c, sc, A + m * k16ATile, r, q);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[sa]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&raw_empty[s]);
+    }
+  }
+
+  // ---- epilogue (warps 2..5): TMEM lane quadrant = warp % 4
+  if (warp >= 2) {
+    ok = mbar_wait(&done, 0, p.err) && ok;
+    tc_fence_after();
+    __syncwarp();
+    const int quad = warp & 3;
+    const int row = rb * 128 + quad * 32 + lane;           // weight row of this lane
+    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+    const float gs = (!nf3 && p.gscale != nullptr) ? p.gscale[le] : 1.f;
+    if (ok && nsub > 0) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v0[16], v1[16];
+        tmem_ld16(trow + c0, v0);
+        if (!FC2) tmem_ld16(trow + BN + c0, v1);
+        if (c0 >= n) continue;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int c = c0 + j;
+          if (c >= n) break;
+          const int pos = p0 + c;
+          if (!FC2) {
+            if (p.splits == 1) {
+              const float h = row < p.I ? swiglu16(v1[j] * gs, v0[j] * gs, p.limit, p.alpha,
+                                                   p.beta)
+                                        : 0.f;
+              p.h16[(size_t)pos * p.Ip + row] = h_to_f16(h, p.err);
+            } else {
+              float* gg = p.gacc + (size_t)pos * 2 * p.Ip;
+              atomicAdd(gg + row, v0[j]);
+              atomicAdd(gg + p.Ip + row, v1[j]);
+            }
+          } else {
+            const int f = p.perm[pos];
+            const float v = p.topk_w[f] * (v0[j] * gs);
+            if (p.deterministic)
+              p.rbuf[(size_t)f * p.H + row] = v;
+            else
+              atomicAdd(&p.acc[(size_t)(f / p.topk) * p.H + row], v);
+          }
+        }
+      }
+    }
+  }
+  if (!FC2 && p.splits > 1) __threadfence();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, Cfg::kAlloc);
+  if (!FC2 && p.splits > 1) {
+    if (tid == 0) {
+      __threadfence();
+      const int t = atomicAdd(&p.tickets[tile * p.RB + rb], 1);
+      s_last = (t == p.splits - 1);
+    }
+    __syncthreads();
+    if (s_last && warp >= 2) {
+      __threadfence();
+      const int quad = warp & 3;
+      const int row = rb * 128 + quad * 32 + lane;
+      const float gs = (!nf3 && p.gscale != nullptr) ? p.gscale[le] : 1.f;
+      for (int c = 0; c < n; ++c) {
+        const float* gg = p.gacc + (size_t)(p0 + c) * 2 * p.Ip;
+        const float up = __ldcg(gg + row), gt = __ldcg(gg + p.Ip + row);
+        const float h = row < p.I ? swiglu16(gt * gs, up * gs, p.limit, p.alpha, p.beta) : 0.f;
+        p.h16[(size_t)(p0 + c) * p.Ip + row] = h_to_f16(h, p.err);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn16)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn16 encode16() {
+  static EncodeTiledFn16 fn = nullptr;
+  if (fn == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn16>(f);
+  }
+  return fn;
+}
+
+// 3-D byte tensor [mats][rows][row_bytes] with boxes box_x bytes x 128 rows x 1.
+static bool tmap_bytes3(CUtensorMap* tm, const void* base, int row_bytes, int rows, int mats,
+                        int box_x, bool swizzle) {
+  EncodeTiledFn16 enc = encode16();
+  if (!enc || mats <= 0) return enc != nullptr;
+  cuuint64_t dims[3] = {(cuuint64_t)row_bytes, (cuuint64_t)rows, (cuuint64_t)mats};
+  cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)row_bytes * rows};
+  cuuint32_t box[3] = {(cuuint32_t)box_x, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// f16 activations [rows][K] with boxes 64 x box_rows and 128-byte swizzle.
+static bool tmap_f16(CUtensorMap* tm, const void* base, int K, int rows, int box_rows) {
+  EncodeTiledFn16 enc = encode16();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool FC2>
+static cudaError_t launch16(const Tc16Params& p, int tiles, cudaStream_t st) {
+  using Cfg = Tc16Cfg<BN, FC2>;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(gemm_tc16_kernel<BN, FC2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Cfg::kSmem);
+    attr = true;
+  }
+  dim3 grid(tiles, p.RB, FC2 ? 1 : p.splits);
+  gemm_tc16_kernel<BN, FC2><<<grid, k16Threads, Cfg::kSmem, st>>>(p);
+  return cudaGetLastError();
+}
+
+// stage 0: fc1 (+ SwiGLU, h -> bf16 -> f16), stage 1: fc2 (+ combine).
+cudaError_t launch_tc16_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
+                              int bn, int tiles, int splits, const float* topk_w, int M,
+                              cudaStream_t st) {
+  const int Sm = M * d.topk;
+  Tc16Params p;
+  memset(&p, 0, sizeof(p));
+  const bool fc2 = stage == 1;
+  const int K = fc2 ? d.Ip : d.H;
+  const int rows = fc2 ? d.H : d.I;
+  const int mats4 = fc2 ? w.E4 : 2 * w.E4;
+  const int mats3 = fc2 ? w.E3 : 2 * w.E3;
+  const int KT = (K + k16RawK - 1) / k16RawK;
+  if (!tmap_bytes3(&p.tm_nv_codes, fc2 ? w.w2 : w.w13, K / 2, rows, mats4, 128, true) ||
+      !tmap_bytes3(&p.tm_nv_scales, fc2 ? w.s2 : w.s13, K / 16, rows, mats4, 16, false) ||
+      !tmap_bytes3(&p.tm_nf_codes, fc2 ? w.nf_w2 : w.nf_w13, 3 * K / 8, rows, mats3, 32, false) ||
+      !tmap_bytes3(&p.tm_nf_scales, fc2 ? w.nf_s2 : w.nf_s13, KT * 16, rows, mats3, 16, false))
+    return cudaErrorInvalidValue;
+  if (!tmap_f16(&p.tm_act, fc2 ? (const void*)r.h16 : (const void*)r.x16, K, Sm, bn))
+    return cudaErrorInvalidValue;
+  p.tier_map = w.tier_map;
+  p.gscale = fc2 ? w.g2 : w.g13;
+  p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
+  p.h16 = reinterpret_cast<uint16_t*>(r.h16); p.gacc = r.g; p.tickets = r.tickets;
+  p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;
+  p.K = K; p.R = rows; p.I = d.I; p.Ip = d.Ip; p.RB = fc2 ? d.H / 128 : cdiv(d.I, 128);
+  p.KT = KT; p.Sm = Sm; p.splits = fc2 ? 1 : splits; p.topk = d.topk;
+  p.deterministic = d.deterministic; p.H = d.H; p.nf3_row_bytes = 3 * K / 8;
+  p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
+  switch (bn * 2 + (fc2 ? 1 : 0)) {
+    case 32: return launch16<16, false>(p, tiles, st);
+    case 33: return launch16<16, true>(p, tiles, st);
+    case 64: return launch16<32, false>(p, tiles, st);
+    case 65: return launch16<32, true>(p, tiles, st);
+    case 128: return launch16<64, false>(p, tiles, st);
+    case 129: return launch16<64, true>(p, tiles, st);
+    case 256: return launch16<128, false>(p, tiles, st);
+    default: return launch16<128, true>(p, tiles, st);
+  }
+}
+
+}  // namespace moe

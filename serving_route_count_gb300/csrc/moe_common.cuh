@@ -22,9 +22,12 @@ constexpr int kTierNF3 = 3;
 constexpr int kErrRouteBounds = 1;   // a routing index fell outside its table
 constexpr int kErrTimeout = 2;       // a bounded wait gave up
 constexpr int kErrTileOverflow = 4;  // more GEMM tiles than the plan reserved
+constexpr int kErrRange = 8;         // a bf16 value outside the f16 range of the W4A16 MMA
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+// byte offset of the NF3 scale of element k within a row's padded scale groups
+__host__ __device__ inline int nf3_scale_byte(int k) { return (k >> 8) * 16 + ((k & 255) >> 5); }
 
 // ----------------------------------------------------------------------------------------------
 // Prepared (device) weight layout.
@@ -40,7 +43,9 @@ __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 //   atoms ordered [expert][half][row tile][k tile]  (fc1)  /  [expert][row tile][k tile]  (fc2).
 // NVFP4 E4M3 scales: row-major [row][K/16].  NF3: per row a 2-bit plane (K/4 bytes, code c's low
 //   two bits at bits 2*(c%4) of byte c/4) followed by a 1-bit plane (K/8 bytes, bit 2 of code c
-//   at bit c%8 of byte c/8); E4M3 scales row-major [row][K/32].
+//   at bit c%8 of byte c/8); E4M3 scales per row in 16-byte groups, one per 256-wide K tile
+//   (byte kt*16 + g = scale of K group 8*kt + g; bytes 8..15 zero) so that tensor-map boxes of
+//   16 bytes fetch one tile's scales.
 // ----------------------------------------------------------------------------------------------
 struct DevWeights {
   int quant = 0;
@@ -55,9 +60,9 @@ struct DevWeights {
   const float* g2 = nullptr;
   // NF3 tier
   const uint8_t* nf_w13 = nullptr;    // [E3][2][I][3H/8] planes
-  const uint8_t* nf_s13 = nullptr;    // [E3][2][I][H/32]
+  const uint8_t* nf_s13 = nullptr;    // [E3][2][I][ceil(H/256)][16]
   const uint8_t* nf_w2 = nullptr;     // [E3][H][3Ip/8] planes
-  const uint8_t* nf_s2 = nullptr;     // [E3][H][Ip/32]
+  const uint8_t* nf_s2 = nullptr;     // [E3][H][ceil(Ip/256)][16]
   const int32_t* tier_map = nullptr;  // [E]: (tier << 24) | local index
 };
 
@@ -85,7 +90,8 @@ struct Scratch {
   size_t g;         // fp32 [Sm][2][Ip]: fc1 output (CUDA-core path) / split-K partial sums
   size_t tickets;   // int32 [max_tiles][ceil(I/128)] split-K completion tickets
   size_t hq, hs;    // W4A8: u8 [Sm][Ip], u8 [Sm][Ip/32]
-  size_t h16;       // W4A16: bf16 [Sm][Ip]
+  size_t h16;       // W4A16: bf16 [Sm][Ip] (CUDA-core path) or f16 (tensor-core path)
+  size_t x16;       // W4A16 tensor-core path: f16 activations [Sm][H] in slot order
   size_t acc;       // fp32 [max_m][H]  (atomic combine)
   size_t rbuf;      // fp32 [max_m*topk][H]  (deterministic combine: one row per slot)
   size_t total;
@@ -113,6 +119,7 @@ struct RunPtrs {
   uint8_t* hq;
   uint8_t* hs;
   __nv_bfloat16* h16;
+  uint16_t* x16;
   float* acc;
   float* rbuf;
 };

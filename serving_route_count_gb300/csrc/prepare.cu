@@ -109,6 +109,29 @@ __global__ void repack_nf3_kernel(const uint8_t* __restrict__ src, uint8_t* __re
   }
 }
 
+// NF3 E4M3 scales [E][halves*rows][src_k/32] -> [E][halves][rows][ceil(dst_k/256)][16]
+__global__ void repack_nf3_scales_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                         int E, int halves, int rows, int src_k, int dst_k,
+                                         int layout) {
+  const int kt = (dst_k + 255) / 256;
+  const size_t n = (size_t)E * halves * rows * kt * 16;
+  GRID_STRIDE(idx, n) {
+    const int b = (int)(idx % (kt * 16));
+    const size_t rowid = idx / (kt * 16);
+    const int i = (int)(rowid % rows);
+    const size_t mh = rowid / rows;
+    const int half = (int)(mh % halves);
+    const size_t e = mh / halves;
+    const int g = (b >> 4) * 8 + (b & 15);       // K group of 32 elements
+    uint8_t v = 0;
+    if ((b & 15) < 8 && g < src_k / 32) {
+      const int sr = halves == 2 ? src_row_fc1(half, i, rows, layout) : i;
+      v = src[(e * (size_t)(halves * rows) + sr) * (src_k / 32) + g];
+    }
+    dst[idx] = v;
+  }
+}
+
 static int grid_for(size_t n) {
   size_t b = (n + 255) / 256;
   if (b > 152 * 32) b = 152 * 32;
@@ -141,6 +164,15 @@ cudaError_t launch_repack_nf3(const void* src, void* dst, int E, int halves, int
   if (n == 0) return cudaSuccess;
   repack_nf3_kernel<<<grid_for(n), 256, 0, st>>>((const uint8_t*)src, (uint8_t*)dst, E, halves,
                                                  rows, src_k, dst_k, layout);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack_nf3_scales(const void* src, void* dst, int E, int halves, int rows,
+                                     int src_k, int dst_k, int layout, cudaStream_t st) {
+  const size_t n = (size_t)E * halves * rows * ((dst_k + 255) / 256) * 16;
+  if (n == 0) return cudaSuccess;
+  repack_nf3_scales_kernel<<<grid_for(n), 256, 0, st>>>((const uint8_t*)src, (uint8_t*)dst, E,
+                                                        halves, rows, src_k, dst_k, layout);
   return cudaGetLastError();
 }
 

@@ -154,7 +154,8 @@ struct ZeroRegion {
 __global__ void __launch_bounds__(256)
 actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t* __restrict__ ctrl,
             const int32_t* __restrict__ perm, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
-            ZeroRegion z0, ZeroRegion z1, ZeroRegion z2) {
+            uint16_t* __restrict__ x16, int32_t* __restrict__ err, ZeroRegion z0, ZeroRegion z1,
+            ZeroRegion z2) {
   const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t gsz = (size_t)gridDim.x * blockDim.x;
   if (xq != nullptr) {
@@ -194,6 +195,29 @@ actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t*
       xs[p * nb + b] = (uint8_t)s;
     }
   }
+  if (x16 != nullptr) {
+    // bf16 -> f16 copy in slot order for the 16-bit tensor-core path (exact within f16 range)
+    const int nc = H / 8;
+    const size_t nchunk = (size_t)ctrl[2] * nc;
+    bool range_ok = true;
+    for (size_t i = gtid; i < nchunk; i += gsz) {
+      const size_t p = i / nc;
+      const int c = (int)(i % nc);
+      const int t = perm[p] / topk;
+      const uint4 u = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c * 8);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xFFFF0000u);
+        range_ok &= fabsf(a) <= 65504.f && fabsf(b) <= 65504.f;
+        o[j] = (uint32_t)__half_as_ushort(__float2half_rn(a)) |
+               ((uint32_t)__half_as_ushort(__float2half_rn(b)) << 16);
+      }
+      *reinterpret_cast<uint4*>(x16 + p * H + c * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (!range_ok) atomicOr(err, kErrRange);
+  }
   const ZeroRegion zs[3] = {z0, z1, z2};
 #pragma unroll
   for (int r = 0; r < 3; ++r) {
@@ -211,15 +235,17 @@ cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int 
 }
 
 cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
-                        void* z0, size_t z0_words, void* z1, size_t z1_words, void* z2,
-                        size_t z2_words, cudaStream_t st) {
-  const size_t work = std::max(std::max(quant_x ? (size_t)M * topk * (H / 32) : (size_t)0,
-                                        z0_words / 4),
-                               std::max(z1_words / 4, z2_words / 4));
+                        bool to_f16, void* z0, size_t z0_words, void* z1, size_t z1_words,
+                        void* z2, size_t z2_words, cudaStream_t st) {
+  const size_t work = std::max(
+      std::max(quant_x ? (size_t)M * topk * (H / 32) : (size_t)0,
+               to_f16 ? (size_t)M * topk * (H / 8) : (size_t)0),
+      std::max(z0_words / 4, std::max(z1_words / 4, z2_words / 4)));
   int blocks = (int)std::min<size_t>((work + 255) / 256, 152 * 8);
   if (blocks < 1) blocks = 1;
   actq_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), H, topk, r.ctrl,
                                       r.perm, quant_x ? r.xq : nullptr, quant_x ? r.xs : nullptr,
+                                      to_f16 ? r.x16 : nullptr, r.ctrl,
                                       ZeroRegion{z0, z0_words}, ZeroRegion{z1, z1_words},
                                       ZeroRegion{z2, z2_words});
   return cudaGetLastError();

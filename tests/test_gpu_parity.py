@@ -278,3 +278,33 @@ def test_w4a8_intermediate_requant(backend):
     assert np.all(got[mism] == alt[mism])
     assert rate < 2e-3
     assert np.all(hq[:, I:] == 0)
+
+
+@pytest.mark.parametrize("quant,M,det", [("nvfp4", 5, 0), ("hybrid", 16, 1), ("nvfp4", 37, 1),
+                                         ("hybrid", 200, 0), ("hybrid", 600, 1)])
+def test_w4a16_tensor_core_tile_widths(quant, M, det):
+    """NVFP4 and the NVFP4 + NF3 hybrid through the 16-bit tcgen05 kernels (weights expanded to
+    f16 in shared memory) at every token-tile width, against the oracle on every row; the
+    CUDA-core backend must agree too.  E=16 (5 NVFP4 experts), H=1280, I=256."""
+    cfg = small_cfg(quant, I=256)
+    ck = S.make_checkpoint(cfg, seed=3000 + M)
+    rng = np.random.default_rng(4000 + M)
+    x = S.make_x(rng, M, cfg.H)
+    ids = S.zipf_topk(rng, M, cfg.E, cfg.topk, 0.8)
+    ids[rng.random(ids.shape) < 0.05] = -1
+    w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 1.0)
+    layer = _layer(ck, cfg.topk, M, math.inf, det)
+    got = run_layer(layer, x, ids, w)
+    st, code = layer.device_error()
+    assert st == 0 and code == 0, code
+    check_rows(got, ck, x, ids, w, math.inf)
+    # intermediate h: bf16 rounding of the SwiGLU output, carried as f16
+    hq, _ = layer.intermediate(M)
+    h = O.slot_intermediate(ck, x, ids, math.inf)
+    got_h = hq[:, : cfg.I].view(np.float16).astype(np.float64)
+    want_h = C.bf16_round(h)
+    amb, alt = C.bf16_alternates(h, 1e-4)
+    mism = got_h != want_h
+    assert np.all(amb[mism]) and np.all(got_h[mism] == alt[mism]), int(mism.sum())
+    simt = _layer(ck, cfg.topk, M, math.inf, det, backend=1)
+    check_rows(run_layer(simt, x, ids, w), ck, x, ids, w, math.inf)
