@@ -28,6 +28,8 @@ cudaError_t launch_simt_stage(int stage, const DevWeights& w, const RunPtrs& r,
 // prepare.cu
 cudaError_t launch_repack_rows(const void* src, void* dst, int E, int halves, int rows,
                                int src_cols, int dst_cols, int layout, int canon, cudaStream_t st);
+cudaError_t launch_repack_fp4_tiled(const void* src, void* dst, int E, int halves, int rows,
+                                    int src_cols, int dst_cols, int layout, cudaStream_t st);
 cudaError_t launch_repack_sf_atoms(const void* src, void* dst, int E, int halves, int rows,
                                    int kblocks, int row_tiles, int k_tiles, int layout,
                                    cudaStream_t st);
@@ -188,8 +190,13 @@ moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* 
   cudaError_t e = cudaSuccess;
   auto chk = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
   if (fp4) {
-    chk(launch_repack_rows(src->w13, base + wp->w13, E4, 2, I, H / 2, H / 2, L, 1, st));
-    chk(launch_repack_rows(src->w2, base + wp->w2, E4, 1, H, I / 2, Ip / 2, L, 1, st));
+    if (wp->quant == MOE_W4A8_MXFP4) {
+      chk(launch_repack_fp4_tiled(src->w13, base + wp->w13, E4, 2, I, H / 2, H / 2, L, st));
+      chk(launch_repack_fp4_tiled(src->w2, base + wp->w2, E4, 1, H, I / 2, Ip / 2, L, st));
+    } else {
+      chk(launch_repack_rows(src->w13, base + wp->w13, E4, 2, I, H / 2, H / 2, L, 1, st));
+      chk(launch_repack_rows(src->w2, base + wp->w2, E4, 1, H, I / 2, Ip / 2, L, 1, st));
+    }
     if (wp->quant == MOE_W4A8_MXFP4) {
       chk(launch_repack_sf_atoms(src->s13, base + wp->s13, E4, 2, I, H / 32, cdiv(I, 128),
                                  H / 128, L, st));
@@ -216,6 +223,7 @@ moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* 
   if (p == nullptr) return MOE_ERR_ARG;
   DevWeights& w = p->w;
   w.quant = wp->quant; w.E = wp->E; w.H = H; w.I = I; w.Ip = Ip; w.E4 = E4; w.E3 = E3;
+  w.fp4_tiled = wp->quant == MOE_W4A8_MXFP4 ? 1 : 0;
   w.w13 = base + wp->w13; w.s13 = base + wp->s13; w.w2 = base + wp->w2; w.s2 = base + wp->s2;
   if (wp->quant != MOE_W4A8_MXFP4) {
     w.g13 = reinterpret_cast<const float*>(base + wp->g13);

@@ -71,8 +71,18 @@ __device__ __forceinline__ void load_w8(const DevWeights& w, int kind, int le, i
     return;
   }
   const size_t rowb = (size_t)le * R + row;
-  const uint32_t codes = *reinterpret_cast<const uint32_t*>((FC2 ? w.w2 : w.w13) +
-                                                           rowb * (size_t)(K / 2) + k / 2);
+  size_t cbyte;
+  if (w.fp4_tiled) {
+    if (FC2) {
+      cbyte = fp4_tiled_byte((size_t)w.E4, w.H, K, (size_t)le, row, k);
+    } else {
+      const int half = row / w.I;
+      cbyte = fp4_tiled_byte((size_t)w.E4 * 2, w.I, K, (size_t)le * 2 + half, row - half * w.I, k);
+    }
+  } else {
+    cbyte = rowb * (size_t)(K / 2) + k / 2;
+  }
+  const uint32_t codes = *reinterpret_cast<const uint32_t*>((FC2 ? w.w2 : w.w13) + cbyte);
   float sc;
   if (kind == kKindMXFP4) {
     size_t byte;

@@ -21,6 +21,7 @@
 // fc2 epilogue: the combine (fp32 atomics into the token's row, or the weighted slot row of
 // the deterministic route buffer).
 #include <algorithm>
+#include <cstring>
 
 #include "moe_common.cuh"
 #include "tc_ptx.cuh"
@@ -55,7 +56,8 @@ struct TcCfg {
 };
 
 struct TcFc1Params {
-  CUtensorMap tm_w13;        // packed FP4 [2E][I][H], box 128 x 128 x 1
+  CUtensorMap tm_w13;        // packed FP4 full 128-row tiles [2E*RTf*KT][128][128], box 128x128x1
+  CUtensorMap tm_w13_tail;   // partial last row tile [2E*KT][I%128][128], box 128 x (I%128) x 1
   CUtensorMap tm_x;          // E4M3 [Sm][H], box 128 x BN
   const uint8_t* sf13;       // weight scale atoms [E][2][RT][KT][512]
   const uint8_t* xs;         // activation scales [Sm][H/32]
@@ -67,11 +69,12 @@ struct TcFc1Params {
   float* gacc;               // [Sm][2][Ip] split-K partial sums
   int32_t* tickets;          // [max_tiles][RT]
   int H, I, Ip, RT, KT, Sm, splits;
+  int RTf, rem;              // full 128-row weight tiles per half, rows of the partial tile
   float limit, alpha, beta;
 };
 
 struct TcFc2Params {
-  CUtensorMap tm_w2;         // packed FP4 [E][H][Ip], box 128 x 128 x 1
+  CUtensorMap tm_w2;         // packed FP4 tiles [E*(H/128)*KT][128][128], box 128 x 128 x 1
   CUtensorMap tm_h;          // E4M3 [Sm][Ip], box 128 x BN
   const uint8_t* sf2;        // weight scale atoms [E][H/128][Ip/128][512]
   const uint8_t* hs;         // [Sm][Ip/32]
@@ -188,9 +191,18 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
         if (!ok) break;
         uint8_t* st = stage(s);
         const int kt = kt0 + i;
-        mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512);
-        tma_load_3d(st, &p.tm_w13, kt * 128, fb * 128, 2 * e + 0, &full[s]);
-        tma_load_3d(st + kTileBytesA, &p.tm_w13, kt * 128, fb * 128, 2 * e + 1, &full[s]);
+        if (fb < p.RTf) {
+          mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512);
+          tma_load_3d(st, &p.tm_w13, 0, 0, ((2 * e) * p.RTf + fb) * p.KT + kt, &full[s]);
+          tma_load_3d(st + kTileBytesA, &p.tm_w13, 0, 0, ((2 * e + 1) * p.RTf + fb) * p.KT + kt,
+                      &full[s]);
+        } else {
+          // partial row tile: rows >= I % 128 of the smem tile keep stale (finite) codes; their
+          // accumulator rows are never read
+          mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + Cfg::kB + 2 * 512);
+          tma_load_3d(st, &p.tm_w13_tail, 0, 0, (2 * e) * p.KT + kt, &full[s]);
+          tma_load_3d(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * e + 1) * p.KT + kt, &full[s]);
+        }
         tma_load_2d(st + 2 * kTileBytesA, &p.tm_x, kt * 128, p0, &full[s]);
         const size_t a_up = ((size_t)(2 * e) * p.RT + fb) * p.KT + kt;
         const size_t a_gt = ((size_t)(2 * e + 1) * p.RT + fb) * p.KT + kt;
@@ -354,7 +366,7 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
         if (!ok) break;
         uint8_t* st = stage(s);
         mbar_arrive_expect_tx(&full[s], kTxBytesA + Cfg::kB + 512);
-        tma_load_3d(st, &p.tm_w2, i * 128, rt * 128, e, &full[s]);
+        tma_load_3d(st, &p.tm_w2, 0, 0, ((size_t)e * (p.H / 128) + rt) * p.KT + i, &full[s]);
         tma_load_2d(st + kTileBytesA, &p.tm_h, i * 128, p0, &full[s]);
         const size_t a = ((size_t)e * (p.H / 128) + rt) * p.KT + i;
         bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
@@ -447,14 +459,16 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Packed FP4 weights [mats][rows][K] (K elements per row, 2 per byte) as a 3-D tensor map with
-// 128 x 128 boxes expanded to one byte per element in shared memory.
-static bool tmap_fp4(CUtensorMap* tm, const void* base, int K, int rows, int mats) {
+// Tile-contiguous packed FP4 weights: `tiles` runs of rows x 128 elements (64 B per row) as a 3-D
+// tensor map whose boxes (128 elements x rows x 1) are whole tiles, expanded to one byte per
+// element in shared memory.
+static bool tmap_fp4(CUtensorMap* tm, const void* base, int rows, long long tiles) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)mats};
-  cuuint64_t strides[2] = {(cuuint64_t)K / 2, (cuuint64_t)K / 2 * rows};
-  cuuint32_t box[3] = {128, 128, 1};
+  if (tiles <= 0 || rows <= 0) return true;
+  cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)tiles};
+  cuuint64_t strides[2] = {64, (cuuint64_t)64 * rows};
+  cuuint32_t box[3] = {128, (cuuint32_t)rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(tm, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims, strides,
              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -521,7 +535,13 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
   const int RT = cdiv(d.I, 128);
   if (stage == 0) {
     TcFc1Params p;
-    if (!tmap_fp4(&p.tm_w13, w.w13, d.H, d.I, 2 * d.E)) return cudaErrorInvalidValue;
+    memset(&p.tm_w13_tail, 0, sizeof(p.tm_w13_tail));
+    p.RTf = d.I / 128;
+    p.rem = d.I % 128;
+    const long long kt = d.H / 128;
+    if (!tmap_fp4(&p.tm_w13, w.w13, 128, 2LL * d.E * p.RTf * kt) ||
+        !tmap_fp4(&p.tm_w13_tail, w.w13 + (size_t)2 * d.E * p.RTf * kt * 8192, p.rem, 2LL * d.E * kt))
+      return cudaErrorInvalidValue;
     if (!tmap_u8(&p.tm_x, r.xq, d.H, Sm, bn)) return cudaErrorInvalidValue;
     p.sf13 = w.s13; p.xs = r.xs; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
     p.hq = r.hq; p.hs = r.hs; p.gacc = r.g; p.tickets = r.tickets;
@@ -535,7 +555,8 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
     }
   }
   TcFc2Params p;
-  if (!tmap_fp4(&p.tm_w2, w.w2, d.Ip, d.H, d.E)) return cudaErrorInvalidValue;
+  if (!tmap_fp4(&p.tm_w2, w.w2, 128, (long long)d.E * (d.H / 128) * (d.Ip / 128)))
+    return cudaErrorInvalidValue;
   if (!tmap_u8(&p.tm_h, r.hq, d.Ip, Sm, bn)) return cudaErrorInvalidValue;
   p.sf2 = w.s2; p.hs = r.hs; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
   p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;

@@ -37,7 +37,10 @@ __host__ __device__ inline int nf3_scale_byte(int k) { return (k >> 8) * 16 + ((
 // (zero codes beyond I), because the packed-FP4 TMA format needs a row length that is a
 // multiple of 128 elements.
 //
-// FP4 codes: rows of K/2 bytes, element 2j in the low nibble of byte j (checkpoint order).
+// FP4 codes: element 2j in the low nibble of byte j (checkpoint order).  NVFP4: rows of K/2
+//   bytes.  MXFP4: tile-contiguous (fp4_tiled_byte): every 128-row x 128-K block is one 8 KB run
+//   ([mats][rows/128][K/128][128][64 B]), the partial last row block of rows % 128 rows follows
+//   all full blocks ([mats][K/128][rows % 128][64 B]), so each TMA box streams contiguous bytes.
 // MXFP4 E8M0 scales ("SF atoms"): for each 128-row tile and each 128-wide K tile, 512 bytes
 //   byte(r, kb) = (r % 32) * 16 + (r / 32) * 4 + kb     (r < 128 in the tile, kb < 4 blocks of 32)
 //   atoms ordered [expert][half][row tile][k tile]  (fc1)  /  [expert][row tile][k tile]  (fc2).
@@ -51,6 +54,7 @@ struct DevWeights {
   int quant = 0;
   int E = 0, H = 0, I = 0, Ip = 0;
   int E4 = 0, E3 = 0;                 // experts in the fp4 tier / the NF3 tier
+  int fp4_tiled = 0;                  // MXFP4 codes in the tile-contiguous layout
   // fp4 tier (MXFP4 or NVFP4)
   const uint8_t* w13 = nullptr;       // [E4][2][I][H/2]
   const uint8_t* s13 = nullptr;       // MXFP4 atoms / NVFP4 [E4][2][I][H/16]
@@ -65,6 +69,14 @@ struct DevWeights {
   const uint8_t* nf_s2 = nullptr;     // [E3][H][ceil(Ip/256)][16]
   const int32_t* tier_map = nullptr;  // [E]: (tier << 24) | local index
 };
+
+__host__ __device__ inline size_t fp4_tiled_byte(size_t n_mats, int rows, int K, size_t mat,
+                                                 int r, int k) {
+  const int rtf = rows >> 7, rem = rows & 127, kt_n = K >> 7;
+  const int rt = r >> 7, rr = r & 127, kt = k >> 7, kb = (k & 127) >> 1;
+  if (rt < rtf) return ((((mat * rtf + rt) * kt_n + kt) << 7) + rr) * 64 + kb;
+  return n_mats * rtf * kt_n * 8192 + (((mat * kt_n + kt) * rem) + rr) * 64 + kb;
+}
 
 __host__ __device__ inline size_t sf_atom_byte(int row_tiles, int k_tiles, size_t mat, int r,
                                                int kb) {

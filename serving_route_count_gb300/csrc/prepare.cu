@@ -48,6 +48,30 @@ __global__ void repack_rows_kernel(const uint8_t* __restrict__ src, uint8_t* __r
   }
 }
 
+// Packed FP4 rows -> the tile-contiguous layout (fp4_tiled_byte), zero padding of the row tail
+// (src_cols .. dst_cols) and -0 -> +0.  src [E][halves*rows][src_cols], dst for
+// mats = E*halves matrices of rows x (2*dst_cols) elements.
+__global__ void repack_fp4_tiled_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                        int E, int halves, int rows, int src_cols, int dst_cols,
+                                        int layout) {
+  const size_t n = (size_t)E * halves * rows * dst_cols;
+  const size_t n_mats = (size_t)E * halves;
+  GRID_STRIDE(idx, n) {
+    const int c = (int)(idx % dst_cols);
+    const size_t rowid = idx / dst_cols;
+    const int i = (int)(rowid % rows);
+    const size_t mh = rowid / rows;
+    const int half = (int)(mh % halves);
+    const size_t e = mh / halves;
+    uint8_t v = 0;
+    if (c < src_cols) {
+      const int sr = halves == 2 ? src_row_fc1(half, i, rows, layout) : i;
+      v = canon_fp4_byte(src[(e * (size_t)(halves * rows) + sr) * src_cols + c]);
+    }
+    dst[fp4_tiled_byte(n_mats, rows, 2 * dst_cols, mh, i, 2 * c)] = v;
+  }
+}
+
 // MXFP4 E8M0 scales -> SF atoms.  src [E][halves*rows][kblocks] (checkpoint stacking),
 // dst atoms [E][halves][row_tiles][k_tiles][512]; padded rows / k-blocks get byte 0.
 __global__ void repack_sf_atoms_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
@@ -144,6 +168,15 @@ cudaError_t launch_repack_rows(const void* src, void* dst, int E, int halves, in
   if (n == 0) return cudaSuccess;
   repack_rows_kernel<<<grid_for(n), 256, 0, st>>>((const uint8_t*)src, (uint8_t*)dst, E, halves,
                                                   rows, src_cols, dst_cols, layout, canon);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack_fp4_tiled(const void* src, void* dst, int E, int halves, int rows,
+                                    int src_cols, int dst_cols, int layout, cudaStream_t st) {
+  const size_t n = (size_t)E * halves * rows * dst_cols;
+  if (n == 0) return cudaSuccess;
+  repack_fp4_tiled_kernel<<<grid_for(n), 256, 0, st>>>((const uint8_t*)src, (uint8_t*)dst, E,
+                                                       halves, rows, src_cols, dst_cols, layout);
   return cudaGetLastError();
 }
 
