@@ -161,6 +161,25 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
                    size_t scratch_bytes, const void* x, const int32_t* topk_ids,
                    const float* topk_weights, void* out, int M, void* stream);
 
+/* moe_run without a caller-provided scratch buffer (the pages have no counterpart of this entry
+ * point).  It is for callers that cannot allocate device memory: code running under another
+ * framework's memory pool with no allocator exposed to plug-ins, sandboxed or embedded runtimes
+ * where cudaMalloc is unavailable after start-up, and paths that must never allocate.  The
+ * scratch is a 16 MiB array compiled into the library (a file-scope __device__ variable): every
+ * GPU that loads the library holds it until the process exits.  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library call.
+ *   Arguments as moe_run, without scratch.  Plans whose moe_scratch_bytes exceeds 16 MiB are
+ *   rejected with MOE_ERR_CAPACITY (e.g. decode batches of the E=384, H=7168, I=576, top-6 layer
+ *   fit: 1.7 MiB atomic / 4 MiB deterministic at max_m = 16).
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
+ *   that device current) and caches it; make that first call before any stream capture.
+ *   All calls on a device share the array and it keeps the last call's contents; calls whose
+ *   executions overlap on the GPU (other streams, other host threads) race on it and must be
+ *   serialised by the caller.  Errors: as moe_run, plus MOE_ERR_CAPACITY as above. */
+moe_status moe_run_static_scratch(const moe_plan_t* plan, const moe_prepared* weights,
+                                  const void* x, const int32_t* topk_ids,
+                                  const float* topk_weights, void* out, int M, void* stream);
+
 /* Size of the device staging buffer moe_run_host needs (x, ids, weights and out of max_m rows). */
 moe_status moe_io_bytes(const moe_plan_t* plan, size_t* bytes);
 

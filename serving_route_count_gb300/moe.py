@@ -131,6 +131,16 @@ def moe_run(plan, prepared, scratch: torch.Tensor, x, topk_ids, topk_weights, ou
                                _ptr(topk_weights), _ptr(out), int(M), _stream(stream)), "moe_run")
 
 
+def moe_run_static_scratch(plan, prepared, x, topk_ids, topk_weights, out, M=None, stream=None):
+    """moe_run with the scratch in the library's fixed 16 MiB device array, for callers that
+    cannot allocate device memory (see include/moe_gb300.h).  Calls on one device share that
+    array: overlapping calls must be serialised by the caller."""
+    M = x.shape[0] if M is None else M
+    _check(_lib.load().moe_run_static_scratch(_handle(plan), _handle(prepared), _ptr(x),
+                                              _ptr(topk_ids), _ptr(topk_weights), _ptr(out),
+                                              int(M), _stream(stream)), "moe_run_static_scratch")
+
+
 def moe_run_host(plan, prepared, scratch, io, x_host, ids_host, w_host, out_host, M=None,
                  stream=None):
     M = x_host.shape[0] if M is None else M
