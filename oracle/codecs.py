@@ -167,12 +167,14 @@ def mxfp8_quantize(v: np.ndarray):
     return codes, s.astype(np.uint8)
 
 
-def mxfp8_alternates(v: np.ndarray, rel: float):
+def mxfp8_alternates(v: np.ndarray, rel: float, atol=0.0):
     """Elements whose MXFP8 rounding is decided by noise: the exact value lies within
-    rel * |value| of the midpoint between its two E4M3 neighbours (under the block scale the
-    quantiser picks), so arithmetic that is exact only to that relative error may return either
-    neighbour.  Returns (mask, alternate dequantised value) with the same shape as v; where
-    mask is False the alternate equals the nearest value."""
+    rel * |value| + atol of the midpoint between its two E4M3 neighbours (under the block scale
+    the quantiser picks), so arithmetic that is exact only to that error may return either
+    neighbour.  `atol` (a scalar or an array broadcasting against v) covers sums that cancel:
+    their rounding error follows the size of the terms, not of the result.  Returns (mask,
+    alternate dequantised value) with the same shape as v; where mask is False the alternate
+    equals the nearest value."""
     v = np.asarray(v, dtype=np.float64)
     q, s = mxfp8_quantize(v)
     K = v.shape[-1]
@@ -182,23 +184,25 @@ def mxfp8_alternates(v: np.ndarray, rel: float):
     lo = np.clip(np.searchsorted(_E4M3_POS, np.minimum(a, E4M3_MAX), side="right") - 1, 0, 126)
     hi = np.minimum(lo + 1, 126)
     mid = (_E4M3_POS[lo] + _E4M3_POS[hi]) / 2
-    mask = (np.abs(a - mid) <= rel * a) & (hi != lo) & (a < E4M3_MAX)
+    tol = rel * a + np.broadcast_to(np.asarray(atol, dtype=np.float64), v.shape) / sc
+    mask = (np.abs(a - mid) <= tol) & (hi != lo) & (a < E4M3_MAX)
     other_mag = np.where(np.isclose(np.abs(near) / sc, _E4M3_POS[lo], rtol=0, atol=0),
                          _E4M3_POS[hi], _E4M3_POS[lo])
     alt = np.where(mask, np.copysign(other_mag * sc, v), near)
     return mask, alt
 
 
-def bf16_alternates(v: np.ndarray, rel: float):
-    """As mxfp8_alternates for rounding to bf16: elements within rel * |value| of the midpoint
-    of their two bf16 neighbours, and the neighbour the nearest rounding did not pick."""
+def bf16_alternates(v: np.ndarray, rel: float, atol=0.0):
+    """As mxfp8_alternates for rounding to bf16: elements within rel * |value| + atol of the
+    midpoint of their two bf16 neighbours, and the neighbour the nearest rounding did not
+    pick."""
     v = np.asarray(v, dtype=np.float64)
     near = bf16_round(v)
     _, ex = np.frexp(np.where(v == 0, 1.0, v))
     ulp = np.ldexp(1.0, np.maximum(ex.astype(np.int64) - 1, -126) - 7)
     other = np.where(np.abs(v) >= np.abs(near), near + np.sign(v) * ulp, near - np.sign(v) * ulp)
     mid = (near + other) / 2
-    mask = (np.abs(v - mid) <= rel * np.abs(v)) & (v != 0)
+    mask = (np.abs(v - mid) <= rel * np.abs(v) + atol) & (v != 0)
     return mask, np.where(mask, other, near)
 
 

@@ -207,3 +207,16 @@ def test_rounding_alternates():
     mask, alt = C.bf16_alternates(b, 1e-6)
     assert mask.tolist() == [True, True, False]
     assert alt[0] == 1.0 and alt[1] == 1 + 2 ** -7 and alt[2] == C.bf16_round(1.3)
+    # the absolute part: 2^-20 * (1 + 2^-8) + 1e-9 is the midpoint of two tiny bf16 values plus
+    # an offset far beyond 1e-6 of its size, but inside an absolute window of 2e-9
+    t = np.array([2.0 ** -20 * (1 + 2 ** -8) + 1e-9, 0.5 + 1e-9])
+    assert C.bf16_alternates(t, 1e-6)[0].tolist() == [False, False]
+    mask, alt = C.bf16_alternates(t, 1e-6, atol=2e-9)
+    assert mask.tolist() == [True, False] and alt[0] == 2.0 ** -20
+    # MXFP8 with a per-element window: 1.0625 + 1e-3 is ambiguous only under atol 2e-3
+    v[0, 1] = 1.0625 + 1e-3
+    assert not C.mxfp8_alternates(v, 1e-4)[0][0, 1]
+    atol = np.zeros_like(v)
+    atol[0, 1] = 2e-3
+    mask, alt = C.mxfp8_alternates(v, 1e-4, atol)
+    assert mask[0, 1] and alt[0, 1] == 1.0 and not mask[0, 3]
