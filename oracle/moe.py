@@ -314,15 +314,29 @@ def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1
 
 # ---------------------------------------------------------------------------- bounds
 
+def _bf16_half_ulp(v):
+    """Half the spacing of bf16 values in the binade of v (8 significant bits)."""
+    _, ex = np.frexp(np.where(v == 0, 1.0, v))          # |v| in [2^(ex-1), 2^ex)
+    return np.ldexp(1.0, np.maximum(ex.astype(np.int64) - 1, -126) - 8)
+
+
 def row_errors(got_bits, ref_f64):
-    """Per-row relative L2 error and max|err| / rms(row) of bf16 output against the fp64 sum."""
+    """Per-row relative L2 error, and the largest error beyond the output's own rounding as a
+    fraction of the row's rms, of bf16 output against the fp64 sum.
+
+    The output is bf16, so even the exact result rounded once misses by up to half a bf16 ulp
+    of each element; an element far above the row's rms (an outlier) would make that unavoidable
+    rounding alone exceed a bound on max|err| / rms.  So the second figure measures
+    max(|err| - half_ulp(ref), 0) / rms: it is 0 for the correctly rounded result and grows
+    with any error of the computation.  A row whose reference is zero must be exactly zero."""
     got = C.bf16_bits_to_f64(got_bits)
     ref = np.asarray(ref_f64, dtype=np.float64)
     diff = got - ref
     nref = np.sqrt((ref ** 2).sum(axis=1))
     rms = np.sqrt((ref ** 2).mean(axis=1))
     rel = np.sqrt((diff ** 2).sum(axis=1)) / np.where(nref > 0, nref, 1.0)
-    mx = np.abs(diff).max(axis=1) / np.where(rms > 0, rms, 1.0)
+    excess = np.maximum(np.abs(diff) - _bf16_half_ulp(ref), 0.0)
+    mx = excess.max(axis=1) / np.where(rms > 0, rms, 1.0)
     zero_rows = nref == 0
     rel[zero_rows] = np.where(np.abs(got[zero_rows]).max(axis=1) == 0, 0.0, np.inf) \
         if zero_rows.any() else rel[zero_rows]

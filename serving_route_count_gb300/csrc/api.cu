@@ -21,6 +21,15 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
                             int bn, int tiles, int splits, const float* topk_w, int M,
                             cudaStream_t st);
 int tc_pick_bn(int M, int topk);
+// gemm_tc_persist.cu
+bool fc1_stream_supported(int bn);
+size_t fc1_stream_part_bytes();
+cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanDims& d, int bn,
+                              int M, float* part, int32_t* tickets, cudaStream_t st);
+bool fc2_persist_supported(int bn);
+cudaError_t launch_fc2_persist(const DevWeights& w, const RunPtrs& r, const PlanDims& d, int bn,
+                               int M, const float* topk_w, int32_t* tickets, void* out,
+                               cudaStream_t st);
 // gemm_simt.cu
 cudaError_t launch_simt_stage(int stage, const DevWeights& w, const RunPtrs& r,
                               const PlanDims& d, int max_tiles, const void* x,
@@ -79,6 +88,19 @@ moe_status cuda_status(cudaError_t e) {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Tiles of a call of M tokens at tile width bn: at most one per slot, and at most
+// ceil(S / bn) + (touched experts).
+int call_tiles(const PlanDims& d, int max_tiles, int M, int bn) {
+  const int Sm = M * d.topk;
+  return std::min(max_tiles, std::min(Sm, cdiv(Sm, bn) + std::min(d.E, Sm)));
+}
+
+// K splits of the tensor-core fc1 so that small calls still put one CTA on most SMs.
+int fc1_splits(const PlanDims& d, int tiles) {
+  const int units = tiles * cdiv(d.I, 128);
+  return std::max(1, std::min(std::min(152 / std::max(units, 1), d.H / 128 / 4), 16));
+}
 
 moe_status check_geometry(int E, int H, int I, int quant) {
   if (E < 1 || E > 1024) return MOE_ERR_SHAPE;
@@ -265,8 +287,17 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   s.tiles = take((size_t)s.max_tiles * 16);
   s.xq = a8 ? take(Sm * H) : 0;
   s.xs = a8 ? take(Sm * H / 32) : 0;
-  s.g = take(Sm * 2 * d.Ip * 4);
-  s.tickets = take(align_up((size_t)s.max_tiles * cdiv(I, 128), 4) * 4);
+  // fc1 output of the CUDA-core path, or the per-split partial sums of the tensor-core path
+  // ([split][slot][2][Ip], one slice per split, summed in split order)
+  size_t g_rows = Sm;
+  for (int m = 1; m <= max_m; ++m) {
+    const int sp = fc1_splits(d, call_tiles(d, s.max_tiles, m, tc_pick_bn(m, topk)));
+    if (sp > 1) g_rows = std::max(g_rows, (size_t)sp * m * topk);
+  }
+  s.g = take(g_rows * 2 * d.Ip * 4);
+  // fc1 tickets [max_tiles][RT], then the persistent fc2's row-block tickets [H / 128]
+  s.tickets = take((align_up((size_t)s.max_tiles * cdiv(I, 128), 4) + align_up(H / 128, 4)) * 4);
+  s.part = a8 ? take(fc1_stream_part_bytes()) : 0;
   s.hq = a8 ? take(Sm * d.Ip) : 0;
   s.hs = a8 ? take(Sm * d.Ip / 32) : 0;
   s.h16 = a8 ? 0 : take(Sm * d.Ip * 2);
@@ -318,6 +349,7 @@ static RunPtrs resolve(const moe_plan_t* plan, void* scratch) {
   r.xs = a8 ? b + s.xs : nullptr;
   r.g = reinterpret_cast<float*>(b + s.g);
   r.tickets = reinterpret_cast<int32_t*>(b + s.tickets);
+  r.part = a8 ? reinterpret_cast<float*>(b + s.part) : nullptr;
   r.hq = a8 ? b + s.hq : nullptr;
   r.hs = a8 ? b + s.hs : nullptr;
   r.h16 = a8 ? nullptr : reinterpret_cast<__nv_bfloat16*>(b + s.h16);
@@ -393,41 +425,48 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   const bool tc = tc8 || t16;
   const int Sm = M * d.topk;
   const int bn = tc ? tc_pick_bn(M, d.topk) : kSimtSlots;
-  // tiles of this call: at most one per slot, and at most ceil(S / bn) + (touched experts)
-  const int tiles = std::min(plan->s.max_tiles, std::min(Sm, cdiv(Sm, bn) + std::min(d.E, Sm)));
+  const int tiles = call_tiles(d, plan->s.max_tiles, M, bn);
   const int RT = cdiv(d.I, 128);
-  int splits = 1;
-  if (tc) {
-    // split K of fc1 so that small calls still put one CTA on most SMs
-    const int units = tiles * RT;
-    splits = std::max(1, std::min(std::min(152 / std::max(units, 1), d.H / 128 / 4), 16));
-  }
+  // decode widths: persistent stream-K fc1, persistent fc2 with the finalize fused in
+  const bool streamk = tc8 && fc1_stream_supported(bn);
+  const bool fc2p = tc8 && fc2_persist_supported(bn);
+  const int splits = (tc && !streamk) ? fc1_splits(d, tiles) : 1;
+  const size_t tk2 = align_up((size_t)plan->s.max_tiles * RT, 4);   // fc2 tickets offset
   prof(0);
   cudaError_t e = launch_route(topk_ids, Sm, d.E, bn, plan->s.max_tiles, r, st);
   if (e != cudaSuccess) return cuda_status(e);
   prof(1);
   void* acc = d.deterministic ? nullptr : r.acc;
   const size_t acc_words = d.deterministic ? 0 : (size_t)M * d.H;
-  void* g = (tc && splits > 1) ? r.g : nullptr;
-  const size_t g_words = g ? (size_t)Sm * 2 * d.Ip : 0;
-  void* tk = (tc && splits > 1) ? r.tickets : nullptr;
-  const size_t tk_words = tk ? align_up((size_t)tiles * RT, 4) : 0;
+  void* g = nullptr;            // split partials are fully written before they are read
+  const size_t g_words = 0;
+  void* tk = (tc && (splits > 1 || streamk || fc2p)) ? r.tickets : nullptr;
+  const size_t tk_words = !tk ? 0 : fc2p ? tk2 + align_up(d.H / 128, 4)
+                                         : align_up((size_t)tiles * RT, 4);
   if (a8 || acc || g || t16) {
     e = launch_actq(x, M, d.H, d.topk, r, a8, t16, acc, acc_words, g, g_words, tk, tk_words, st);
     if (e != cudaSuccess) return cuda_status(e);
   }
   prof(2);
   if (tc) {
-    e = tc8 ? launch_tc_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st)
-            : launch_tc16_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st);
+    if (streamk)
+      e = launch_fc1_stream(w, r, d, bn, M, r.part, r.tickets, st);
+    else
+      e = tc8 ? launch_tc_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st)
+              : launch_tc16_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(3);
-    e = tc8 ? launch_tc_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st)
-            : launch_tc16_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st);
+    if (fc2p)
+      e = launch_fc2_persist(w, r, d, bn, M, topk_weights, r.tickets + tk2, out, st);
+    else
+      e = tc8 ? launch_tc_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st)
+              : launch_tc16_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(4);
-    e = launch_simt_stage(3, w, r, d, plan->s.max_tiles, x, topk_weights, out, M, st);
-    if (e != cudaSuccess) return cuda_status(e);
+    if (!fc2p) {
+      e = launch_simt_stage(3, w, r, d, plan->s.max_tiles, x, topk_weights, out, M, st);
+      if (e != cudaSuccess) return cuda_status(e);
+    }
     prof(5);
     return MOE_OK;
   }

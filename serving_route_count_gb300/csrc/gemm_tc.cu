@@ -15,8 +15,9 @@
 // epilogue from TMEM (lane = weight row, column = token).
 //
 // fc1 epilogue: h = SwiGLU(gate, up) (clamped), requantised to MXFP8 per 32 intermediate
-// columns (the 32 rows of a warp), written as the fc2 activation operand.  With split K the
-// partial sums go to an fp32 buffer and the last CTA of the unit (atomic ticket, no waiting)
+// columns (the 32 rows of a warp), written as the fc2 activation operand.  With split K each
+// split stores its partial sums in its own slice of an fp32 buffer, and the last CTA of the unit
+// (atomic ticket, no waiting) adds the slices in split order - the same sum on every run - and
 // runs the epilogue.
 // fc2 epilogue: the combine (fp32 atomics into the token's row, or the weighted slot row of
 // the deterministic route buffer).
@@ -25,26 +26,25 @@
 
 #include "moe_common.cuh"
 #include "tc_ptx.cuh"
+#include "tc_tile.cuh"
 
 namespace moe {
 
 using namespace tc;
 
-constexpr int kTcThreads = 128;
-constexpr int kTileBytesA = 128 * 128;   // 128 rows x 128 K of padded FP4 (1 byte / element)
-// The packed-FP4 TMA format counts the bytes it reads from global memory (two elements per
-// byte) as the transaction size, not the expanded shared-memory footprint.
-constexpr int kTxBytesA = 128 * 128 / 2;
-
-constexpr int kSfChunk = 32;   // K tiles of activation scales staged per batch
+// K tiles of weights a CTA requests into L2 ahead of its TMA loads: more bytes in flight than the
+// shared-memory ring holds (the padded FP4 format takes 2 bytes of it per weight byte).
+constexpr int kPrefetchTiles = 8;
 
 template <int BN>
 struct TcCfg {
   static constexpr int kB = BN * 128;                         // activation tile bytes
   static constexpr int kStage1 = (2 * kTileBytesA + kB + 3 * 512 + 1023) / 1024 * 1024;
   static constexpr int kStage2 = (kTileBytesA + kB + 2 * 512 + 1023) / 1024 * 1024;
-  static constexpr int kStages1 = BN <= 32 ? 5 : (BN <= 64 ? 4 : 3);
-  static constexpr int kStages2 = BN <= 32 ? 5 : 4;
+  // short pipelines, two resident CTAs per SM at the decode widths: measured faster than deep
+  // pipelines at one CTA per SM
+  static constexpr int kStages1 = BN <= 16 ? 3 : (BN <= 64 ? 4 : 3);
+  static constexpr int kStages2 = BN <= 32 ? 2 : 4;
   static constexpr int kCols1 = 2 * BN + 12 * kStages1;       // D_up, D_gate, scale ring
   static constexpr int kCols2 = BN + 8 * kStages2;
   static constexpr int pow2(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
@@ -66,7 +66,9 @@ struct TcFc1Params {
   int32_t* err;
   uint8_t* hq;               // [Sm][Ip]
   uint8_t* hs;               // [Sm][Ip/32]
-  float* gacc;               // [Sm][2][Ip] split-K partial sums
+  const uint8_t* w13;        // raw weight tiles (L2 prefetch): the full ones, then the partial
+  const uint8_t* w13_tail;
+  float* gacc;               // [splits][Sm][2][Ip] split-K partial sums, one slice per split
   int32_t* tickets;          // [max_tiles][RT]
   int H, I, Ip, RT, KT, Sm, splits;
   int RTf, rem;              // full 128-row weight tiles per half, rows of the partial tile
@@ -85,62 +87,12 @@ struct TcFc2Params {
   const float* topk_w;
   float* acc;                // [M][H] atomic mode
   float* rbuf;               // [M*k][H] deterministic mode
+  const uint8_t* w2;         // raw weight tiles (L2 prefetch)
   int H, Ip, KT, Sm, topk, deterministic;
 };
 
-// Activation scales of a CTA's BN rows for up to kSfChunk K tiles, staged in shared memory with
-// one batch of independent loads (row n, K tile j -> 4 bytes at stage[n * kSfChunk + j]), so the
-// per-stage scale atoms are built without a global-memory round trip on the critical path.
-
 template <int BN>
-__device__ __forceinline__ void stage_act_sf(uint32_t* stage, const uint8_t* xs, int row0,
-                                             int Sm, int kblocks, int kt0, int nkt, int lane) {
-  // all copies are issued before one wait: a single memory latency per chunk
-  for (int idx = lane; idx < BN * nkt; idx += 32) {
-    const int n = idx / nkt, j = idx - n * nkt;
-    uint32_t* dst = stage + n * kSfChunk + j;
-    if (row0 + n < Sm)
-      cp_async4(dst, xs + (size_t)(row0 + n) * kblocks + (kt0 + j) * 4);
-    else
-      *dst = 0;
-  }
-  cp_async_wait_all();
-}
-
-// Scale atom of BN activation rows for one 128-wide K tile: byte (n%32)*16 + (n/32)*4 + kb.
-template <int BN>
-__device__ __forceinline__ void write_act_sf(uint8_t* dst, const uint32_t* stage, int j,
-                                             int lane) {
-#pragma unroll
-  for (int n = lane; n < BN; n += 32)
-    *reinterpret_cast<uint32_t*>(dst + (n & 31) * 16 + (n >> 5) * 4) = stage[n * kSfChunk + j];
-}
-
-__device__ __forceinline__ float swiglu(float gate, float up, float limit, float alpha,
-                                        float beta) {
-  const float g = fminf(gate, limit);
-  const float u = fminf(fmaxf(up, -limit), limit);
-  return g / (1.0f + expf(-alpha * g)) * (u + beta);
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-// h of one token column for the 32 features of this warp -> MXFP8 code + scale.
-__device__ __forceinline__ void requant_store(float h, int lane, size_t row_base_q,
-                                              size_t row_base_s, int f, uint8_t* hq,
-                                              uint8_t* hs) {
-  const float amax = warp_max(fabsf(h));
-  const uint32_t s = mx_scale_byte(amax);
-  hq[row_base_q + f] = (uint8_t)f32_to_e4m3(h * e8m0_inv_f32(s));
-  if (lane == 0) hs[row_base_s + (f >> 5)] = (uint8_t)s;
-}
-
-template <int BN>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads)
 fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::kStages1;
@@ -158,7 +110,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
                                              ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[S], empty[S], done;
   __shared__ uint32_t s_tmem;
-  __shared__ int s_last;
+  __shared__ int s_last, s_fail;
 
   if (warp == 0) {
     tmem_alloc(&s_tmem, Cfg::kAlloc1);
@@ -170,6 +122,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
       mbar_init(&empty[s], 1);
     }
     mbar_init(&done, 1);
+    s_fail = 0;
     fence_barrier_init();
   }
   if (tid == 64) prefetch_tmap(&p.tm_w13);
@@ -179,14 +132,32 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   bool ok = true;
-
+  int issued = 0;                                   // stages filled by the TMA producer
   auto stage = [&](int s) { return smem + s * Cfg::kStage1; };
   // stage layout: A_up | A_gate | B | SFA_up | SFA_gate | SFB
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int i = 0; i < nk && ok; ++i) {
+      // L2 prefetch of the weight tiles and scale atoms of K tile kt
+      auto prefetch = [&](int kt) {
+        if (fb < p.RTf) {
+          bulk_prefetch_l2(p.w13 + ((size_t)((2 * e) * p.RTf + fb) * p.KT + kt) * kTxBytesA,
+                           kTxBytesA);
+          bulk_prefetch_l2(p.w13 + ((size_t)((2 * e + 1) * p.RTf + fb) * p.KT + kt) * kTxBytesA,
+                           kTxBytesA);
+        } else {
+          bulk_prefetch_l2(p.w13_tail + ((size_t)(2 * e) * p.KT + kt) * p.rem * 64, p.rem * 64);
+          bulk_prefetch_l2(p.w13_tail + ((size_t)(2 * e + 1) * p.KT + kt) * p.rem * 64,
+                           p.rem * 64);
+        }
+        bulk_prefetch_l2(p.sf13 + (((size_t)(2 * e) * p.RT + fb) * p.KT + kt) * 512, 512);
+        bulk_prefetch_l2(p.sf13 + (((size_t)(2 * e + 1) * p.RT + fb) * p.KT + kt) * 512, 512);
+      };
+      int ip = 0;                                   // next K tile (of this split) to prefetch
+      int i = 0;
+      for (; i < nk && ok; ++i) {
         const int s = i % S;
+        for (const int lim = min(i + kPrefetchTiles, nk); ip < lim; ++ip) prefetch(kt0 + ip);
         if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
         if (!ok) break;
         uint8_t* st = stage(s);
@@ -209,6 +180,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
         bulk_load(st + 2 * kTileBytesA + Cfg::kB, p.sf13 + a_up * 512, 512, &full[s]);
         bulk_load(st + 2 * kTileBytesA + Cfg::kB + 512, p.sf13 + a_gt * 512, 512, &full[s]);
       }
+      issued = i;
     }
   } else if (warp == 2) {
     uint32_t* sfst = reinterpret_cast<uint32_t*>(smem + S * Cfg::kStage1);
@@ -285,17 +257,21 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           if (c0 + j < n) {
-            float* g = p.gacc + (size_t)(p0 + c0 + j) * 2 * p.Ip;
-            atomicAdd(g + f, up[j]);
-            atomicAdd(g + p.Ip + f, gt[j]);
+            float* g = p.gacc + ((size_t)split * p.Sm + p0 + c0 + j) * 2 * p.Ip;
+            g[f] = up[j];
+            g[p.Ip + f] = gt[j];
           }
         }
       }
     }
   }
   if (p.splits > 1) __threadfence();   // partial sums visible device-wide before the ticket
+  if (!ok) s_fail = 1;
   tc_fence_before();
   __syncthreads();
+  // a wait gave up: let this CTA's copies land before its shared memory is released (its MMAs
+  // completed or timed out at the wait on `done`)
+  if (s_fail && warp == 0 && lane == 0) drain_stage_loads<S>(full, issued, p.err);
   if (warp == 0) tmem_dealloc(tmem, Cfg::kAlloc1);
   if (p.splits > 1) {
     if (tid == 0) {
@@ -307,8 +283,13 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
     if (s_last) {
       __threadfence();
       for (int c = 0; c < n; ++c) {
-        const float* g = p.gacc + (size_t)(p0 + c) * 2 * p.Ip;
-        const float up = __ldcg(g + f), gt = __ldcg(g + p.Ip + f);
+        // partial sums added in split order: the same result on every run
+        float up = 0.f, gt = 0.f;
+        for (int sp = 0; sp < p.splits; ++sp) {
+          const float* g = p.gacc + ((size_t)sp * p.Sm + p0 + c) * 2 * p.Ip;
+          up += __ldcg(g + f);
+          gt += __ldcg(g + p.Ip + f);
+        }
         const float h = f < p.I ? swiglu(gt, up, p.limit, p.alpha, p.beta) : 0.f;
         const size_t row = (size_t)(p0 + c);
         requant_store(h, lane, row * p.Ip, row * (p.Ip / 32), f, p.hq, p.hs);
@@ -318,7 +299,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
 }
 
 template <int BN>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads)
 fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::kStages2;
@@ -335,6 +316,7 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
                                              ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[S], empty[S], done;
   __shared__ uint32_t s_tmem;
+  __shared__ int s_fail;
 
   if (warp == 0) {
     tmem_alloc(&s_tmem, Cfg::kAlloc2);
@@ -346,6 +328,7 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
       mbar_init(&empty[s], 1);
     }
     mbar_init(&done, 1);
+    s_fail = 0;
     fence_barrier_init();
   }
   if (tid == 64) prefetch_tmap(&p.tm_w2);
@@ -355,13 +338,21 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   bool ok = true;
+  int issued = 0;                                   // stages filled by the TMA producer
   auto stage = [&](int s) { return smem + s * Cfg::kStage2; };
   // stage layout: A | B | SFA | SFB
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int i = 0; i < nk && ok; ++i) {
+      const size_t a0 = ((size_t)e * (p.H / 128) + rt) * p.KT;   // first tile of this unit
+      int ip = 0;                                   // next K tile to prefetch into L2
+      int i = 0;
+      for (; i < nk && ok; ++i) {
         const int s = i % S;
+        for (const int lim = min(i + 2 * kPrefetchTiles, nk); ip < lim; ++ip) {
+          bulk_prefetch_l2(p.w2 + (a0 + ip) * kTxBytesA, kTxBytesA);
+          bulk_prefetch_l2(p.sf2 + (a0 + ip) * 512, 512);
+        }
         if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
         if (!ok) break;
         uint8_t* st = stage(s);
@@ -371,6 +362,7 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
         const size_t a = ((size_t)e * (p.H / 128) + rt) * p.KT + i;
         bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
       }
+      issued = i;
     }
   } else if (warp == 2) {
     uint32_t* sfst = reinterpret_cast<uint32_t*>(smem + S * Cfg::kStage2);
@@ -434,19 +426,18 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
       }
     }
   }
+  if (!ok) s_fail = 1;
   tc_fence_before();
   __syncthreads();
+  // a wait gave up: let this CTA's copies land before its shared memory is released (its MMAs
+  // completed or timed out at the wait on `done`)
+  if (s_fail && warp == 0 && lane == 0) drain_stage_loads<S>(full, issued, p.err);
   if (warp == 0) tmem_dealloc(tmem, Cfg::kAlloc2);
 }
 
 // ---------------------------------------------------------------------------------- host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
+EncodeTiledFn tc_encode_fn() {
   static EncodeTiledFn fn = nullptr;
   if (fn == nullptr) {
     void* p = nullptr;
@@ -459,11 +450,8 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Tile-contiguous packed FP4 weights: `tiles` runs of rows x 128 elements (64 B per row) as a 3-D
-// tensor map whose boxes (128 elements x rows x 1) are whole tiles, expanded to one byte per
-// element in shared memory.
-static bool tmap_fp4(CUtensorMap* tm, const void* base, int rows, long long tiles) {
-  EncodeTiledFn enc = encode_fn();
+bool tmap_fp4(CUtensorMap* tm, const void* base, int rows, long long tiles) {
+  EncodeTiledFn enc = tc_encode_fn();
   if (!enc) return false;
   if (tiles <= 0 || rows <= 0) return true;
   cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)tiles};
@@ -475,9 +463,8 @@ static bool tmap_fp4(CUtensorMap* tm, const void* base, int rows, long long tile
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Byte matrix [rows][K] (E4M3 activations), boxes of 128 x box_rows.
-static bool tmap_u8(CUtensorMap* tm, const void* base, int K, int rows, int box_rows) {
-  EncodeTiledFn enc = encode_fn();
+bool tmap_u8(CUtensorMap* tm, const void* base, int K, int rows, int box_rows) {
+  EncodeTiledFn enc = tc_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)K};
@@ -487,12 +474,6 @@ static bool tmap_u8(CUtensorMap* tm, const void* base, int K, int rows, int box_
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-struct TcLaunch {
-  int bn;          // tokens per tile (16, 32, 64, 128)
-  int tiles;       // grid bound on the tile count of this call
-  int splits;      // fc1 split K
-};
 
 int tc_pick_bn(int M, int topk) {
   (void)topk;
@@ -545,6 +526,8 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
     if (!tmap_u8(&p.tm_x, r.xq, d.H, Sm, bn)) return cudaErrorInvalidValue;
     p.sf13 = w.s13; p.xs = r.xs; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
     p.hq = r.hq; p.hs = r.hs; p.gacc = r.g; p.tickets = r.tickets;
+    p.w13 = w.w13;
+    p.w13_tail = w.w13 + (size_t)2 * d.E * p.RTf * kt * 8192;
     p.H = d.H; p.I = d.I; p.Ip = d.Ip; p.RT = RT; p.KT = d.H / 128; p.Sm = Sm;
     p.splits = splits; p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
     switch (bn) {
@@ -559,7 +542,7 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
     return cudaErrorInvalidValue;
   if (!tmap_u8(&p.tm_h, r.hq, d.Ip, Sm, bn)) return cudaErrorInvalidValue;
   p.sf2 = w.s2; p.hs = r.hs; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
-  p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;
+  p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf; p.w2 = w.w2;
   p.H = d.H; p.Ip = d.Ip; p.KT = d.Ip / 128; p.Sm = Sm; p.topk = d.topk;
   p.deterministic = d.deterministic;
   switch (bn) {

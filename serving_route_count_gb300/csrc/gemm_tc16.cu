@@ -68,7 +68,7 @@ struct Tc16Params {
   int32_t* err;
   // fc1 outputs
   uint16_t* h16;              // f16 [Sm][Ip] (bf16-rounded SwiGLU output)
-  float* gacc;                // [Sm][2][Ip] split-K partial sums
+  float* gacc;                // [splits][Sm][2][Ip] split-K partial sums, one slice per split
   int32_t* tickets;
   // fc2 outputs
   const int32_t* perm;
@@ -225,7 +225,7 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   __shared__ __align__(8) uint64_t b_full[Cfg::kSb], b_empty[Cfg::kSb];
   __shared__ __align__(8) uint64_t done;
   __shared__ uint32_t s_tmem;
-  __shared__ int s_last;
+  __shared__ int s_last, s_fail;
 
   if (warp == 0) {
     tmem_alloc(&s_tmem, Cfg::kAlloc);
@@ -245,6 +245,7 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
       mbar_init(&b_empty[s], 1);
     }
     mbar_init(&done, 1);
+    s_fail = 0;
     fence_barrier_init();
   }
   tc_fence_before();
@@ -252,11 +253,12 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   bool ok = true;
+  int issued = 0, g = 0;   // raw stages filled, next activation sub-tile to load
 
   if (warp == 0) {
     if (lane == 0) {
-      int g = 0;   // next activation sub-tile to load
-      for (int i = 0; i < nraw && ok; ++i) {
+      int i = 0;
+      for (; i < nraw && ok; ++i) {
         const int s = i % Cfg::kSr;
         if (i >= Cfg::kSr) ok = mbar_wait(&raw_empty[s], ((i / Cfg::kSr) - 1) & 1, p.err);
         if (!ok) break;
@@ -294,6 +296,7 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
                       &b_full[sb]);
         }
       }
+      issued = i;
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -379,9 +382,9 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
                                         : 0.f;
               p.h16[(size_t)pos * p.Ip + row] = h_to_f16(h, p.err);
             } else {
-              float* gg = p.gacc + (size_t)pos * 2 * p.Ip;
-              atomicAdd(gg + row, v0[j]);
-              atomicAdd(gg + p.Ip + row, v1[j]);
+              float* gg = p.gacc + ((size_t)split * p.Sm + pos) * 2 * p.Ip;
+              gg[row] = v0[j];
+              gg[p.Ip + row] = v1[j];
             }
           } else {
             const int f = p.perm[pos];
@@ -396,8 +399,15 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
     }
   }
   if (!FC2 && p.splits > 1) __threadfence();
+  if (!ok) s_fail = 1;
   tc_fence_before();
   __syncthreads();
+  // a wait gave up: let this CTA's copies land before its shared memory is released (its MMAs
+  // completed or timed out at the wait on `done`)
+  if (s_fail && warp == 0 && lane == 0) {
+    drain_stage_loads<Cfg::kSr>(raw_full, issued, p.err);
+    drain_stage_loads<Cfg::kSb>(b_full, g, p.err);
+  }
   if (warp == 0) tmem_dealloc(tmem, Cfg::kAlloc);
   if (!FC2 && p.splits > 1) {
     if (tid == 0) {
@@ -412,8 +422,13 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
       const int row = rb * 128 + quad * 32 + lane;
       const float gs = (!nf3 && p.gscale != nullptr) ? p.gscale[le] : 1.f;
       for (int c = 0; c < n; ++c) {
-        const float* gg = p.gacc + (size_t)(p0 + c) * 2 * p.Ip;
-        const float up = __ldcg(gg + row), gt = __ldcg(gg + p.Ip + row);
+        // partial sums added in split order: the same result on every run
+        float up = 0.f, gt = 0.f;
+        for (int sp = 0; sp < p.splits; ++sp) {
+          const float* gg = p.gacc + ((size_t)sp * p.Sm + p0 + c) * 2 * p.Ip;
+          up += __ldcg(gg + row);
+          gt += __ldcg(gg + p.Ip + row);
+        }
         const float h = row < p.I ? swiglu16(gt * gs, up * gs, p.limit, p.alpha, p.beta) : 0.f;
         p.h16[(size_t)(p0 + c) * p.Ip + row] = h_to_f16(h, p.err);
       }

@@ -62,6 +62,16 @@ TC_DEV bool mbar_wait(uint64_t* b, uint32_t parity, int32_t* err) {
   }
 }
 
+// After a wait gave up: waits (each wait bounded) for the stages this thread filled last - the
+// loads of fill numbers max(0, issued - S) .. issued - 1, stage j % S, phase j / S - so that no
+// copy still targets the CTA's shared memory when it exits.  A phase that cannot complete (its
+// other arrivals never came) ends at the time limit.
+template <int S>
+TC_DEV void drain_stage_loads(uint64_t* full, int issued, int32_t* err) {
+  for (int j = issued > S ? issued - S : 0; j < issued; ++j)
+    mbar_wait(&full[j % S], (uint32_t)(j / S) & 1u, err);
+}
+
 // 4-byte asynchronous global -> shared copy (both addresses 4-byte aligned).
 TC_DEV void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
@@ -94,6 +104,11 @@ TC_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+// L2 prefetch hint for `bytes` at src (16-byte aligned, size a multiple of 16): no completion,
+// no shared memory; a later load of the same bytes finds them in L2.
+TC_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 TC_DEV void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");

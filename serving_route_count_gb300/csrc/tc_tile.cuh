@@ -1,0 +1,87 @@
+// tc_tile.cuh - pieces shared by the W4A8 tensor-core kernels: tile geometry, activation scale
+// atoms, the SwiGLU + MXFP8 requantisation of an accumulator column, tensor maps.
+#pragma once
+
+#include <cuda.h>
+
+#include "moe_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+using namespace tc;
+
+constexpr int kTcThreads = 128;
+constexpr int kTileBytesA = 128 * 128;   // 128 rows x 128 K of padded FP4 (1 byte / element)
+// The packed-FP4 TMA format counts the bytes it reads from global memory (two elements per
+// byte) as the transaction size, not the expanded shared-memory footprint.
+constexpr int kTxBytesA = 128 * 128 / 2;
+
+constexpr int kSfChunk = 32;   // K tiles of activation scales staged per batch
+
+// Activation scales of a CTA's BN rows for up to kSfChunk K tiles, staged in shared memory with
+// one batch of independent loads (row n, K tile j -> 4 bytes at stage[n * kSfChunk + j]), so the
+// per-stage scale atoms are built without a global-memory round trip on the critical path.
+template <int BN>
+static __device__ __forceinline__ void stage_act_sf(uint32_t* stage, const uint8_t* xs, int row0,
+                                                    int Sm, int kblocks, int kt0, int nkt,
+                                                    int lane) {
+  // all copies are issued before one wait: a single memory latency per chunk
+  for (int idx = lane; idx < BN * nkt; idx += 32) {
+    const int n = idx / nkt, j = idx - n * nkt;
+    uint32_t* dst = stage + n * kSfChunk + j;
+    if (row0 + n < Sm)
+      cp_async4(dst, xs + (size_t)(row0 + n) * kblocks + (kt0 + j) * 4);
+    else
+      *dst = 0;
+  }
+  cp_async_wait_all();
+}
+
+// Scale atom of BN activation rows for one 128-wide K tile: byte (n%32)*16 + (n/32)*4 + kb.
+template <int BN>
+static __device__ __forceinline__ void write_act_sf(uint8_t* dst, const uint32_t* stage, int j,
+                                                    int lane) {
+#pragma unroll
+  for (int n = lane; n < BN; n += 32)
+    *reinterpret_cast<uint32_t*>(dst + (n & 31) * 16 + (n >> 5) * 4) = stage[n * kSfChunk + j];
+}
+
+static __device__ __forceinline__ float swiglu(float gate, float up, float limit, float alpha,
+                                               float beta) {
+  const float g = fminf(gate, limit);
+  const float u = fminf(fmaxf(up, -limit), limit);
+  return g / (1.0f + expf(-alpha * g)) * (u + beta);
+}
+
+static __device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// h of one token column for the 32 features of this warp -> MXFP8 code + scale.
+static __device__ __forceinline__ void requant_store(float h, int lane, size_t row_base_q,
+                                                     size_t row_base_s, int f, uint8_t* hq,
+                                                     uint8_t* hs) {
+  const float amax = warp_max(fabsf(h));
+  const uint32_t s = mx_scale_byte(amax);
+  hq[row_base_q + f] = (uint8_t)f32_to_e4m3(h * e8m0_inv_f32(s));
+  if (lane == 0) hs[row_base_s + (f >> 5)] = (uint8_t)s;
+}
+
+// ---------------------------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tc_encode_fn();
+// Tile-contiguous packed FP4 weights: `tiles` runs of rows x 128 elements (64 B per row) as a 3-D
+// tensor map whose boxes (128 elements x rows x 1) are whole tiles, expanded to one byte per
+// element in shared memory.  rows or tiles of 0 leave the map unset (never used).
+bool tmap_fp4(CUtensorMap* tm, const void* base, int rows, long long tiles);
+// Byte matrix [rows][K] (E4M3 activations), boxes of 128 x box_rows.
+bool tmap_u8(CUtensorMap* tm, const void* base, int K, int rows, int box_rows);
+
+}  // namespace moe

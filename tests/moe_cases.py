@@ -31,6 +31,10 @@ def run_layer(layer, x_bits, ids, w):
 
 
 REQUANT_REL = 1e-4       # relative window of a rounding decision taken in fp32 arithmetic
+# absolute part of the intermediate's ambiguity window, as a fraction of the slot's rms: a gate
+# or up sum that cancels keeps the absolute fp32 error of its terms (about 2^-24 * sqrt(K) of
+# their size), so an element far smaller than the slot's rms can sit that close to a midpoint
+H_CANCEL_ATOL = 2.0 ** -16
 
 
 def _row_ok(got_row_bits, ref_row):

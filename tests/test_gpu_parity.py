@@ -11,7 +11,7 @@ import pytest
 from oracle import codecs as C
 from oracle import moe as O
 from synth import moe_inputs as S
-from moe_cases import check_rows, run_layer, small_cfg, to_device, out_bits
+from moe_cases import H_CANCEL_ATOL, check_rows, run_layer, small_cfg, to_device, out_bits
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -298,13 +298,29 @@ def test_w4a16_tensor_core_tile_widths(quant, M, det):
     st, code = layer.device_error()
     assert st == 0 and code == 0, code
     check_rows(got, ck, x, ids, w, math.inf)
-    # intermediate h: bf16 rounding of the SwiGLU output, carried as f16
+    # intermediate h: bf16 rounding of the SwiGLU output, carried as f16.  bf16 values are exact
+    # in f16 down to 2^-16 (f16 subnormal step 2^-24); below that the f16 subnormal rounding
+    # applies, an absolute error under 2^-24 that no output can see.
     hq, _ = layer.intermediate(M)
     h = O.slot_intermediate(ck, x, ids, math.inf)
     got_h = hq[:, : cfg.I].view(np.float16).astype(np.float64)
     want_h = C.bf16_round(h)
-    amb, alt = C.bf16_alternates(h, 1e-4)
-    mism = got_h != want_h
-    assert np.all(amb[mism]) and np.all(got_h[mism] == alt[mism]), int(mism.sum())
+    # ambiguity window: 1e-4 of the value, plus H_CANCEL_ATOL of the slot's rms for elements
+    # whose gate or up projection cancels (fp32 sums err by the size of their terms)
+    rms = np.sqrt(np.mean(h * h, axis=1, keepdims=True))
+    amb, alt = C.bf16_alternates(h, 1e-4, H_CANCEL_ATOL * rms)
+    big = np.abs(h) >= 2.0 ** -16
+    mism = (got_h != want_h) & big
+    # a mismatch is the other rounding of a near-midpoint value, or (a cancelled sum, whose
+    # error exceeds an ulp of its small result) within the absolute window of the exact value
+    near_exact = np.abs(got_h - h) <= np.abs(want_h - h) + H_CANCEL_ATOL * rms
+    bad = mism & ~(amb & (got_h == alt)) & ~near_exact
+    if bad.any():
+        i = np.argwhere(bad)[:5]
+        print("unexplained h mismatches:", int(bad.sum()),
+              [(float(h[a, b]), float(want_h[a, b]), float(got_h[a, b]), float(rms[a, 0]))
+               for a, b in i])
+    assert not bad.any(), int(bad.sum())
+    assert np.all(np.abs(got_h - want_h)[~big] <= 2.0 ** -24)
     simt = _layer(ck, cfg.topk, M, math.inf, det, backend=1)
     check_rows(run_layer(simt, x, ids, w), ck, x, ids, w, math.inf)

@@ -249,6 +249,23 @@ def test_row_errors_bound_helper():
     bad = C.f64_to_bf16_bits(ref + np.array([[0.0, 0.0, 0.5], [0.0, 1.0, 0.0]]))
     rel, mx = O.row_errors(bad, ref)
     assert rel[0] > 0.1 and np.isinf(rel[1])
+    # an outlier row: 1001.75 rounds to 1000 (bf16 spacing 4 there); its rounding error 1.75
+    # alone is above 2e-2 of the row's rms, yet the correctly rounded output has no error beyond
+    # its own rounding
+    row = np.array([[1001.75] + [1.0] * 255])
+    rms = np.sqrt((row ** 2).mean())
+    rel, mx = O.row_errors(C.f64_to_bf16_bits(row), row)
+    assert mx[0] == 0.0 and 0 < rel[0] < 2e-3 and 1.75 / rms > 0.02
+    # the other neighbour (1004): the error 2.25 exceeds the half step 2 by 0.25
+    off = C.f64_to_bf16_bits(row).copy()
+    off[0, 0] = C.f64_to_bf16_bits(np.array([1004.0]))[0]
+    _, mx = O.row_errors(off, row)
+    assert mx[0] == 0.25 / rms
+    # below the binade of 1.0 the half step is 2^-9: 0.5 + 2^-8 (one step up) is 2^-9 beyond
+    small = np.array([[0.5, 0.5]])
+    up = C.f64_to_bf16_bits(np.array([[0.5 + 2 ** -8, 0.5]]))
+    _, mx = O.row_errors(up, small)
+    assert mx[0] == 2 ** -9 / 0.5
 
 
 def test_synth_recipes():
