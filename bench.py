@@ -37,12 +37,14 @@ N_ROUTING_SETS = 8
 FLUSH_BYTES = 512 << 20
 EXPERT_BYTES_W13 = {"decode_w4a8": 2 * 576 * 7168 // 2 + 2 * 576 * 7168 // 32}   # codes + E8M0
 EXPERT_BYTES_W2 = {"decode_w4a8": 7168 * 576 // 2 + 7168 * 576 // 32}
+# the dominant kernel of the decode ladder (every call has M <= 16: 16-token tiles)
+FC1_KERNEL = "fc1_stream_kernel<16>"
 
 
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--det", action="store_true", help="deterministic combine")
@@ -132,13 +134,16 @@ def reference_arm(args, rank, world):
 # ---------------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 200 ms from before the warm-up to after the timed region; the
+    summary keeps the samples whose timestamps fall inside the marked timed region."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
@@ -149,6 +154,12 @@ class ClockSampler:
         except OSError:
             self.proc = None
         return self
+
+    def start(self):
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
 
     def __exit__(self, *a):
         self.out = ""
@@ -161,20 +172,25 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate()
 
     def summary(self):
+        import datetime
         rows = [r.split(",") for r in (self.out or "").strip().splitlines() if r.strip()]
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             try:
-                sm.append(float(r[0]))
-                mx = float(r[1])
-                for n, v in zip(names, r[4:8]):
+                ts = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                mx = float(r[2])
+                if self.t0 is not None and not (self.t0 <= ts <= self.t1):
+                    continue
+                sm.append(float(r[1]))
+                for n, v in zip(names, r[5:9]):
                     if v.strip().lower() == "active":
                         reasons.add(n)
             except (ValueError, IndexError):
                 continue
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window_s": None if self.t0 is None else round(self.t1 - self.t0, 3)}
 
 
 # ---------------------------------------------------------------------------------- our arm
@@ -249,7 +265,7 @@ def our_arm(args, rank, world):
     import torch.distributed as dist
 
     from serving_route_count_gb300 import MoELayer, build, moe_plan_set_profile_events
-    from serving_route_count_gb300 import moe_profile_stage_names
+    from serving_route_count_gb300 import moe_call_launches, moe_profile_stage_names
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
@@ -293,7 +309,6 @@ def our_arm(args, rank, world):
         moe_plan_set_profile_events(layer.plan, [])
     torch.cuda.synchronize()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    per_step = len(m_list)
 
     def step(si, record):
         tot_ms, dom_ms, dom_bytes, toks = 0.0, 0.0, 0.0, 0
@@ -316,21 +331,23 @@ def our_arm(args, rank, world):
             toks += c["tokens"]
         return tot_ms, dom_ms, dom_bytes, toks
 
-    for si in range(args.warmup):
-        step(si, False)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
     tot_ms = dom_ms = dom_bytes = 0.0
     toks = 0
     with ClockSampler(local) as clk:
+        for si in range(args.warmup):
+            step(si, False)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clk.start()
         for si in range(args.steps):
             a, b, c, d = step(args.warmup + si, True)
             tot_ms += a
             dom_ms += b
             dom_bytes += c
             toks += d
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        clk.stop()
     tot_ms, all_toks = reduce_over_ranks(tot_ms, toks, world, device="cuda")
     if world > 1:
         dist.barrier()
@@ -364,8 +381,8 @@ def our_arm(args, rank, world):
         return
     peak, peak_kind = measured_peaks()
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    traffic = kernel_traffic("gemm_simt_kernel<false>")
-    n_launch_per_call = len(stages)
+    traffic = kernel_traffic(FC1_KERNEL)
+    launches_per_step = sum(moe_call_launches(layer.plan, M) for M in m_list)
     cpu = None if args.no_cpu_baseline else run_cpu_baseline()
     line = {
         "metric": "decode MoE layer tokens/s",
@@ -409,7 +426,7 @@ def our_arm(args, rank, world):
         "e2e": {"value": e2e_tok / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": "moe_run_host (pinned host buffers, H2D + run + D2H + sync)"},
-        "gpu_launches": n_launch_per_call * per_step * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line))

@@ -214,6 +214,12 @@ moe_status moe_debug_actq(const moe_plan_t* plan, void* scratch, int M, uint8_t*
 moe_status moe_plan_set_profile_events(moe_plan_t* plan, void* const* events, int n_events);
 const char* moe_profile_stage_names(const moe_plan_t* plan);
 
+/* Number of kernel launches moe_run makes for a call of M tokens with this plan and backend
+ * (route, activation quantisation, fc1, fc2, and a separate finalize except where the
+ * persistent fc2 of the 16/32-token W4A8 widths writes the output itself).  0 for M = 0.
+ * Errors: MOE_ERR_ARG, MOE_ERR_CAPACITY (M > max_m). */
+moe_status moe_call_launches(const moe_plan_t* plan, int M, int* launches);
+
 /* Test hook: the fc2 activation operand of the last call in slot order (synchronises).
  * W4A8: hq [S, Ip] E4M3 codes and hs [S, Ip/32] E8M0 bytes (Ip = I rounded up to 128; columns
  * >= I are zero).  W4A16 / hybrid: hq receives [S, Ip] bf16 values, hs is not written.

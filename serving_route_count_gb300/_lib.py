@@ -53,6 +53,7 @@ SIGNATURES = {
     "moe_debug_h": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_plan_set_profile_events": (c_int, [c_void_p, ctypes.POINTER(c_void_p), c_int]),
     "moe_profile_stage_names": (ctypes.c_char_p, [c_void_p]),
+    "moe_call_launches": (c_int, [c_void_p, c_int, ctypes.POINTER(c_int)]),
     "moe_destroy_weight_plan": (None, [c_void_p]),
     "moe_destroy_prepared": (None, [c_void_p]),
     "moe_destroy_plan": (None, [c_void_p]),

@@ -401,6 +401,27 @@ moe_status moe_plan_set_backend(moe_plan_t* plan, int backend) {
   return MOE_OK;
 }
 
+moe_status moe_call_launches(const moe_plan_t* plan, int M, int* launches) {
+  if (plan == nullptr || launches == nullptr || M < 0) return MOE_ERR_ARG;
+  if (M > plan->d.max_m) return MOE_ERR_CAPACITY;
+  const PlanDims& d = plan->d;
+  if (M == 0) {
+    *launches = 0;
+    return MOE_OK;
+  }
+  const bool tc8 = use_tc(d), t16 = use_tc16(d);
+  if (tc8 || t16) {
+    // route, actq, fc1, fc2 (+ finalize unless the persistent fc2 writes the output)
+    const bool fc2p = tc8 && fc2_persist_supported(tc_pick_bn(M, d.topk));
+    *launches = fc2p ? 4 : 5;
+    return MOE_OK;
+  }
+  // route, actq (when something needs it), fc1, act, fc2, finalize
+  const bool actq = d.quant == MOE_W4A8_MXFP4 || !d.deterministic;
+  *launches = 5 + (actq ? 1 : 0);
+  return MOE_OK;
+}
+
 moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* scratch,
                    size_t scratch_bytes, const void* x, const int32_t* topk_ids,
                    const float* topk_weights, void* out, int M, void* stream) {

@@ -18,10 +18,11 @@
 // Units are (tile, 128-row block of H) pairs, tile-major; the fixed grid splits them into equal
 // contiguous ranges (fc2's K = I is short, so a unit is never split).  Accumulators alternate
 // between two TMEM buffers so the combine of one unit overlaps the MMAs of the next.  The
-// combine is that of fc2_tc_kernel (fp32 atomics, or the weighted slot row of the route buffer);
-// then the unit bumps its row block's ticket, and the CTA that completes a row block (all tiles
-// done) writes that block of every token's output row in bf16 - the work of the separate
-// finalize launch, with the same arithmetic (the fp32 sum, or the fixed-order top-k sum).
+// combine is that of fc2_tc_kernel (fp32 atomics, or the weighted slot row of the route buffer).
+// When a CTA has combined all its units it fences once and bumps the ticket of each unit's row
+// block; the CTA that completes a row block (all tiles done) writes that block of every token's
+// output row in bf16 - the work of the separate finalize launch, with the same arithmetic (the
+// fp32 sum, or the fixed-order top-k sum).
 //
 // Both kernels request the weight tiles of the next kPrefetchTiles K tiles into L2 ahead of
 // their TMA loads, so more bytes are in flight than the shared-memory ring holds.
@@ -422,7 +423,7 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
                                              ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[S], empty[S], acc_full[2], acc_empty[2], drain;
   __shared__ uint32_t s_tmem;
-  __shared__ int s_last, s_fail;
+  __shared__ int s_fail, s_nfin, s_fin[128];
 
   if (warp == 0) {
     tmem_alloc(&s_tmem, Cfg::kAlloc);
@@ -573,15 +574,26 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[b]);
-      // the last unit of row block rb (over all tiles) writes that block of the output
-      __threadfence();
+    }
+    // One fence for all of this CTA's combines, then a ticket per unit; the CTA holding the
+    // last ticket of row block rb (over all tiles) writes that block of the output.  Units go
+    // 128 at a time, one per epilogue thread.
+    __threadfence();
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    for (int u0 = u_begin; u0 < u_end; u0 += 128) {
+      if (row == 0) s_nfin = 0;
       asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (warp == 4 && lane == 0) s_last = atomicAdd(&p.tickets[rb], 1) == ntiles - 1;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (s_last && ok) {
-        __threadfence();
-        finalize_block(p, rb, row);
+      const int u = u0 + row;
+      if (u < u_end) {
+        const int rb = u % p.RB;
+        if (atomicAdd(&p.tickets[rb], 1) == ntiles - 1) s_fin[atomicAdd(&s_nfin, 1)] = rb;
       }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (ok) {
+        __threadfence();
+        for (int q = 0; q < s_nfin; ++q) finalize_block(p, s_fin[q], row);
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
     }
   }
   if (!ok) s_fail = 1;

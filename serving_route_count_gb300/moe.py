@@ -201,6 +201,14 @@ def moe_plan_set_profile_events(plan, events):
            "moe_plan_set_profile_events")
 
 
+def moe_call_launches(plan, M) -> int:
+    """Kernel launches moe_run makes for a call of M tokens."""
+    n = ctypes.c_int(0)
+    _check(_lib.load().moe_call_launches(_handle(plan), int(M), ctypes.byref(n)),
+           "moe_call_launches")
+    return n.value
+
+
 def moe_profile_stage_names(plan):
     return _lib.load().moe_profile_stage_names(_handle(plan)).decode().split(",")
 

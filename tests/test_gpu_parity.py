@@ -321,6 +321,8 @@ def test_w4a16_tensor_core_tile_widths(quant, M, det):
               [(float(h[a, b]), float(want_h[a, b]), float(got_h[a, b]), float(rms[a, 0]))
                for a, b in i])
     assert not bad.any(), int(bad.sum())
-    assert np.all(np.abs(got_h - want_h)[~big] <= 2.0 ** -24)
+    # tiny elements: f16 subnormal rounding (under 2^-24) on top of the same absolute window
+    tiny_ok = np.abs(got_h - h) <= np.abs(want_h - h) + 2.0 ** -24 + H_CANCEL_ATOL * rms
+    assert np.all(tiny_ok[~big])
     simt = _layer(ck, cfg.topk, M, math.inf, det, backend=1)
     check_rows(run_layer(simt, x, ids, w), ck, x, ids, w, math.inf)
