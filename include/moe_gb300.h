@@ -170,7 +170,8 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
  * cudaMalloc, cudaFree or allocating library call.
  *   Arguments as moe_run, without scratch.  Plans whose moe_scratch_bytes exceeds 16 MiB are
  *   rejected with MOE_ERR_CAPACITY (e.g. decode batches of the E=384, H=7168, I=576, top-6 layer
- *   fit: 1.7 MiB atomic / 4 MiB deterministic at max_m = 16).
+ *   fit: 11.7 MiB atomic / 13.8 MiB deterministic at max_m = 16, 10 MiB of it the fixed
+ *   partial-sum slots of the persistent W4A8 fc1).
  *   The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
  *   that device current) and caches it; make that first call before any stream capture.
  *   All calls on a device share the array and it keeps the last call's contents; calls whose
@@ -215,8 +216,8 @@ moe_status moe_plan_set_profile_events(moe_plan_t* plan, void* const* events, in
 const char* moe_profile_stage_names(const moe_plan_t* plan);
 
 /* Number of kernel launches moe_run makes for a call of M tokens with this plan and backend
- * (route, activation quantisation, fc1, fc2, and a separate finalize except where the
- * persistent fc2 of the 16/32-token W4A8 widths writes the output itself).  0 for M = 0.
+ * (route, activation quantisation when needed, fc1, [SwiGLU on the CUDA-core path], fc2,
+ * finalize).  0 for M = 0.
  * Errors: MOE_ERR_ARG, MOE_ERR_CAPACITY (M > max_m). */
 moe_status moe_call_launches(const moe_plan_t* plan, int M, int* launches);
 

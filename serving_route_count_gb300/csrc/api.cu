@@ -22,14 +22,10 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
                             cudaStream_t st);
 int tc_pick_bn(int M, int topk);
 // gemm_tc_persist.cu
-bool fc1_stream_supported(int bn);
+bool fc1_stream_preferred(int bn, int units);
 size_t fc1_stream_part_bytes();
 cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanDims& d, int bn,
                               int M, float* part, int32_t* tickets, cudaStream_t st);
-bool fc2_persist_supported(int bn);
-cudaError_t launch_fc2_persist(const DevWeights& w, const RunPtrs& r, const PlanDims& d, int bn,
-                               int M, const float* topk_w, int32_t* tickets, void* out,
-                               cudaStream_t st);
 // gemm_simt.cu
 cudaError_t launch_simt_stage(int stage, const DevWeights& w, const RunPtrs& r,
                               const PlanDims& d, int max_tiles, const void* x,
@@ -295,8 +291,7 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
     if (sp > 1) g_rows = std::max(g_rows, (size_t)sp * m * topk);
   }
   s.g = take(g_rows * 2 * d.Ip * 4);
-  // fc1 tickets [max_tiles][RT], then the persistent fc2's row-block tickets [H / 128]
-  s.tickets = take((align_up((size_t)s.max_tiles * cdiv(I, 128), 4) + align_up(H / 128, 4)) * 4);
+  s.tickets = take(align_up((size_t)s.max_tiles * cdiv(I, 128), 4) * 4);
   s.part = a8 ? take(fc1_stream_part_bytes()) : 0;
   s.hq = a8 ? take(Sm * d.Ip) : 0;
   s.hs = a8 ? take(Sm * d.Ip / 32) : 0;
@@ -411,9 +406,7 @@ moe_status moe_call_launches(const moe_plan_t* plan, int M, int* launches) {
   }
   const bool tc8 = use_tc(d), t16 = use_tc16(d);
   if (tc8 || t16) {
-    // route, actq, fc1, fc2 (+ finalize unless the persistent fc2 writes the output)
-    const bool fc2p = tc8 && fc2_persist_supported(tc_pick_bn(M, d.topk));
-    *launches = fc2p ? 4 : 5;
+    *launches = 5;   // route, actq, fc1, fc2, finalize
     return MOE_OK;
   }
   // route, actq (when something needs it), fc1, act, fc2, finalize
@@ -448,11 +441,9 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   const int bn = tc ? tc_pick_bn(M, d.topk) : kSimtSlots;
   const int tiles = call_tiles(d, plan->s.max_tiles, M, bn);
   const int RT = cdiv(d.I, 128);
-  // decode widths: persistent stream-K fc1, persistent fc2 with the finalize fused in
-  const bool streamk = tc8 && fc1_stream_supported(bn);
-  const bool fc2p = tc8 && fc2_persist_supported(bn);
+  // decode widths with more units than one wave of CTAs: the persistent stream-K fc1
+  const bool streamk = tc8 && fc1_stream_preferred(bn, tiles * RT);
   const int splits = (tc && !streamk) ? fc1_splits(d, tiles) : 1;
-  const size_t tk2 = align_up((size_t)plan->s.max_tiles * RT, 4);   // fc2 tickets offset
   prof(0);
   cudaError_t e = launch_route(topk_ids, Sm, d.E, bn, plan->s.max_tiles, r, st);
   if (e != cudaSuccess) return cuda_status(e);
@@ -461,9 +452,8 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   const size_t acc_words = d.deterministic ? 0 : (size_t)M * d.H;
   void* g = nullptr;            // split partials are fully written before they are read
   const size_t g_words = 0;
-  void* tk = (tc && (splits > 1 || streamk || fc2p)) ? r.tickets : nullptr;
-  const size_t tk_words = !tk ? 0 : fc2p ? tk2 + align_up(d.H / 128, 4)
-                                         : align_up((size_t)tiles * RT, 4);
+  void* tk = (tc && (splits > 1 || streamk)) ? r.tickets : nullptr;
+  const size_t tk_words = tk ? align_up((size_t)tiles * RT, 4) : 0;
   if (a8 || acc || g || t16) {
     e = launch_actq(x, M, d.H, d.topk, r, a8, t16, acc, acc_words, g, g_words, tk, tk_words, st);
     if (e != cudaSuccess) return cuda_status(e);
@@ -477,17 +467,12 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
               : launch_tc16_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(3);
-    if (fc2p)
-      e = launch_fc2_persist(w, r, d, bn, M, topk_weights, r.tickets + tk2, out, st);
-    else
-      e = tc8 ? launch_tc_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st)
-              : launch_tc16_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st);
+    e = tc8 ? launch_tc_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st)
+            : launch_tc16_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(4);
-    if (!fc2p) {
-      e = launch_simt_stage(3, w, r, d, plan->s.max_tiles, x, topk_weights, out, M, st);
-      if (e != cudaSuccess) return cuda_status(e);
-    }
+    e = launch_simt_stage(3, w, r, d, plan->s.max_tiles, x, topk_weights, out, M, st);
+    if (e != cudaSuccess) return cuda_status(e);
     prof(5);
     return MOE_OK;
   }

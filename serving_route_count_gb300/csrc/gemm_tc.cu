@@ -41,8 +41,9 @@ struct TcCfg {
   static constexpr int kB = BN * 128;                         // activation tile bytes
   static constexpr int kStage1 = (2 * kTileBytesA + kB + 3 * 512 + 1023) / 1024 * 1024;
   static constexpr int kStage2 = (kTileBytesA + kB + 2 * 512 + 1023) / 1024 * 1024;
-  // short pipelines, two resident CTAs per SM at the decode widths: measured faster than deep
-  // pipelines at one CTA per SM
+  // short rings, several CTAs per SM: a CTA keeps only a few stages in flight behind its one
+  // producer thread, so more CTAs per SM stream more bytes at once (measured: fc2 at 2 stages
+  // and 5 CTAs per SM runs 3x faster than at 6 stages and 1 CTA per SM)
   static constexpr int kStages1 = BN <= 16 ? 3 : (BN <= 64 ? 4 : 3);
   static constexpr int kStages2 = BN <= 32 ? 2 : 4;
   static constexpr int kCols1 = 2 * BN + 12 * kStages1;       // D_up, D_gate, scale ring
@@ -282,17 +283,35 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
     __syncthreads();
     if (s_last) {
       __threadfence();
-      for (int c = 0; c < n; ++c) {
-        // partial sums added in split order: the same result on every run
-        float up = 0.f, gt = 0.f;
+      // partial sums added in split order (the same result on every run), 16 columns at a time
+      // with each split's 32 loads issued together: one memory latency per split and chunk
+      for (int c0 = 0; c0 < n; c0 += 16) {
+        float up[16], gt[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) up[j] = gt[j] = 0.f;
         for (int sp = 0; sp < p.splits; ++sp) {
-          const float* g = p.gacc + ((size_t)sp * p.Sm + p0 + c) * 2 * p.Ip;
-          up += __ldcg(g + f);
-          gt += __ldcg(g + p.Ip + f);
+          const float* g = p.gacc + ((size_t)sp * p.Sm + p0 + c0) * 2 * p.Ip + f;
+          float a[16], b[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const bool in = c0 + j < n;
+            a[j] = in ? __ldcg(g + (size_t)j * 2 * p.Ip) : 0.f;
+            b[j] = in ? __ldcg(g + (size_t)j * 2 * p.Ip + p.Ip) : 0.f;
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            up[j] += a[j];
+            gt[j] += b[j];
+          }
         }
-        const float h = f < p.I ? swiglu(gt, up, p.limit, p.alpha, p.beta) : 0.f;
-        const size_t row = (size_t)(p0 + c);
-        requant_store(h, lane, row * p.Ip, row * (p.Ip / 32), f, p.hq, p.hs);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (c0 + j < n) {
+            const float h = f < p.I ? swiglu(gt[j], up[j], p.limit, p.alpha, p.beta) : 0.f;
+            const size_t row = (size_t)(p0 + c0 + j);
+            requant_store(h, lane, row * p.Ip, row * (p.Ip / 32), f, p.hq, p.hs);
+          }
+        }
       }
     }
   }
@@ -317,6 +336,8 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
   __shared__ __align__(8) uint64_t full[S], empty[S], done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_fail;
+  __shared__ int s_f[BN];          // flat slot index of each tile column
+  __shared__ float s_w[BN];        // its router weight
 
   if (warp == 0) {
     tmem_alloc(&s_tmem, Cfg::kAlloc2);
@@ -400,9 +421,16 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
       }
       tc_commit(&done);
     }
+  } else {
+    // warp 3: the combine's slot indices and router weights, loaded while the GEMM runs
+    for (int c = lane; c < n; c += 32) {
+      const int f = p.perm[p0 + c];
+      s_f[c] = f;
+      s_w[c] = p.topk_w[f];
+    }
   }
 
-  __syncwarp();
+  __syncthreads();                                    // s_f / s_w written
   ok = mbar_wait(&done, 0, p.err) && ok;
   tc_fence_after();
   __syncwarp();
@@ -416,8 +444,8 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         if (c0 + j < n) {
-          const int f = p.perm[p0 + c0 + j];
-          const float v = p.topk_w[f] * y[j];
+          const int f = s_f[c0 + j];
+          const float v = s_w[c0 + j] * y[j];
           if (p.deterministic)
             p.rbuf[(size_t)f * p.H + h] = v;
           else
@@ -487,6 +515,9 @@ static cudaError_t launch_fc1_bn(const TcFc1Params& p, int tiles, cudaStream_t s
   if (!attr) {
     cudaFuncSetAttribute(fc1_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          Cfg::kSmem1);
+    // all of the unified L1 / shared storage as shared memory
+    cudaFuncSetAttribute(fc1_tc_kernel<BN>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
     attr = true;
   }
   dim3 grid(tiles, p.RT, p.splits);
@@ -501,6 +532,9 @@ static cudaError_t launch_fc2_bn(const TcFc2Params& p, int tiles, cudaStream_t s
   if (!attr) {
     cudaFuncSetAttribute(fc2_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          Cfg::kSmem2);
+    // all of the unified L1 / shared storage as shared memory
+    cudaFuncSetAttribute(fc2_tc_kernel<BN>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
     attr = true;
   }
   dim3 grid(tiles, p.H / 128);

@@ -226,6 +226,8 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   __shared__ __align__(8) uint64_t done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_last, s_fail;
+  __shared__ int s_f[BN];          // fc2: flat slot index of each tile column
+  __shared__ float s_w[BN];        // fc2: its router weight
 
   if (warp == 0) {
     tmem_alloc(&s_tmem, Cfg::kAlloc);
@@ -325,6 +327,12 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   } else {
     // converters: thread = row of the 128-row weight block
     const int r = tid - 64;
+    if (FC2 && r < n) {
+      // the combine's slot indices and router weights, read by these threads' epilogue
+      const int f = p.perm[p0 + r];
+      s_f[r] = f;
+      s_w[r] = p.topk_w[f];
+    }
     int g = 0;
     for (int i = 0; i < nraw && ok; ++i) {
       const int s = i % Cfg::kSr;
@@ -356,6 +364,7 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
 
   // ---- epilogue (warps 2..5): TMEM lane quadrant = warp % 4
   if (warp >= 2) {
+    asm volatile("bar.sync 1, 128;" ::: "memory");         // s_f / s_w written (warps 2..5)
     ok = mbar_wait(&done, 0, p.err) && ok;
     tc_fence_after();
     __syncwarp();
@@ -387,8 +396,8 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
               gg[p.Ip + row] = v1[j];
             }
           } else {
-            const int f = p.perm[pos];
-            const float v = p.topk_w[f] * (v0[j] * gs);
+            const int f = s_f[c];
+            const float v = s_w[c] * (v0[j] * gs);
             if (p.deterministic)
               p.rbuf[(size_t)f * p.H + row] = v;
             else
@@ -421,16 +430,35 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
       const int quad = warp & 3;
       const int row = rb * 128 + quad * 32 + lane;
       const float gs = (!nf3 && p.gscale != nullptr) ? p.gscale[le] : 1.f;
-      for (int c = 0; c < n; ++c) {
-        // partial sums added in split order: the same result on every run
-        float up = 0.f, gt = 0.f;
+      // partial sums added in split order (the same result on every run), 16 columns at a
+      // time with each split's 32 loads issued together
+      for (int c0 = 0; c0 < n; c0 += 16) {
+        float up[16], gt[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) up[j] = gt[j] = 0.f;
         for (int sp = 0; sp < p.splits; ++sp) {
-          const float* gg = p.gacc + ((size_t)sp * p.Sm + p0 + c) * 2 * p.Ip;
-          up += __ldcg(gg + row);
-          gt += __ldcg(gg + p.Ip + row);
+          const float* gg = p.gacc + ((size_t)sp * p.Sm + p0 + c0) * 2 * p.Ip + row;
+          float a[16], b[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const bool in = c0 + j < n;
+            a[j] = in ? __ldcg(gg + (size_t)j * 2 * p.Ip) : 0.f;
+            b[j] = in ? __ldcg(gg + (size_t)j * 2 * p.Ip + p.Ip) : 0.f;
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            up[j] += a[j];
+            gt[j] += b[j];
+          }
         }
-        const float h = row < p.I ? swiglu16(gt * gs, up * gs, p.limit, p.alpha, p.beta) : 0.f;
-        p.h16[(size_t)(p0 + c) * p.Ip + row] = h_to_f16(h, p.err);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (c0 + j < n) {
+            const float h = row < p.I ? swiglu16(gt[j] * gs, up[j] * gs, p.limit, p.alpha, p.beta)
+                                      : 0.f;
+            p.h16[(size_t)(p0 + c0 + j) * p.Ip + row] = h_to_f16(h, p.err);
+          }
+        }
       }
     }
   }
@@ -491,6 +519,9 @@ static cudaError_t launch16(const Tc16Params& p, int tiles, cudaStream_t st) {
   if (!attr) {
     cudaFuncSetAttribute(gemm_tc16_kernel<BN, FC2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          Cfg::kSmem);
+    // all of the unified L1 / shared storage as shared memory
+    cudaFuncSetAttribute(gemm_tc16_kernel<BN, FC2>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
     attr = true;
   }
   dim3 grid(tiles, p.RB, FC2 ? 1 : p.splits);

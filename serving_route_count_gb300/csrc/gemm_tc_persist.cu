@@ -1,7 +1,5 @@
-// gemm_tc_persist.cu - persistent W4A8 kernels for decode-size calls: a stream-K fc1 and an fc2
-// that also finalises the output.
+// gemm_tc_persist.cu - persistent, stream-K W4A8 fc1 for decode-size calls.
 //
-// fc1 ---------------------------------------------------------------------------------------
 // Decode calls touch few experts (M = 16, top-6: ~66 experts x 5 weight blocks = ~330 units of
 // 56 K tiles each), so one CTA per unit leaves a tail wave that runs a fraction of the SMs.
 // Here a fixed grid of G CTAs (every SM times its resident CTAs) splits the flattened
@@ -14,20 +12,10 @@
 //     K order - the same order on every run - and runs SwiGLU + requantisation.
 // Block-scaled MMA, layouts and operand staging are those of fc1_tc_kernel (gemm_tc.cu).
 //
-// fc2 ---------------------------------------------------------------------------------------
-// Units are (tile, 128-row block of H) pairs, tile-major; the fixed grid splits them into equal
-// contiguous ranges (fc2's K = I is short, so a unit is never split).  Accumulators alternate
-// between two TMEM buffers so the combine of one unit overlaps the MMAs of the next.  The
-// combine is that of fc2_tc_kernel (fp32 atomics, or the weighted slot row of the route buffer).
-// When a CTA has combined all its units it fences once and bumps the ticket of each unit's row
-// block; the CTA that completes a row block (all tiles done) writes that block of every token's
-// output row in bf16 - the work of the separate finalize launch, with the same arithmetic (the
-// fp32 sum, or the fixed-order top-k sum).
+// The producer requests the weight tiles of the next kPrefetchTiles K tiles into L2 ahead of its
+// TMA loads, so more bytes are in flight than the shared-memory ring holds.
 //
-// Both kernels request the weight tiles of the next kPrefetchTiles K tiles into L2 ahead of
-// their TMA loads, so more bytes are in flight than the shared-memory ring holds.
-//
-// Warps (256 threads, both kernels): 0 TMA producer (lane 0), 1 MMA issuer (lane 0),
+// Warps (256 threads): 0 TMA producer (lane 0), 1 MMA issuer (lane 0),
 // 2 activation-scale atoms, 3 idle, 4..7 epilogue (TMEM lane quadrant = warp % 4).
 #include <algorithm>
 #include <cstring>
@@ -144,11 +132,17 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
 
   if (warp == 0) {
     if (lane == 0) {
-      // L2 prefetch of the weight tiles and scale atoms of flat index y
+      // L2 prefetch of the weight tiles and scale atoms of flat index y; the expert of a tile
+      // is looked up once per tile (a dependent global load per stage would pace the producer)
+      int pf_tile = -1, pf_e = 0;
       auto prefetch = [&](long long y) {
         const int u = (int)(y / p.KT), kt = (int)(y % p.KT);
         const int tile = u / p.RT, fb = u - tile * p.RT;
-        const int e = p.tiles[tile].x;
+        if (tile != pf_tile) {
+          pf_tile = tile;
+          pf_e = p.tiles[tile].x;
+        }
+        const int e = pf_e;
         if (fb < p.RTf) {
           bulk_prefetch_l2(p.w13 + ((size_t)((2 * e) * p.RTf + fb) * p.KT + kt) * kTxBytesA,
                            kTxBytesA);
@@ -316,18 +310,36 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
           // the unit's pieces in K order: CTAs cta_of(u*KT) .. cta_of(u*KT + KT - 1)
           const int c_first = cta_of((long long)u * p.KT, G, W);
           const int c_last = cta_of((long long)u * p.KT + p.KT - 1, G, W);
-          for (int cc = 0; cc < n; ++cc) {
-            float up = 0.f, gt = 0.f;
+          // 16 columns at a time, each piece's 32 loads issued together
+          for (int c0 = 0; c0 < n; c0 += 16) {
+            float up[16], gt[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) up[jj] = gt[jj] = 0.f;
             for (int q = c_first; q <= c_last; ++q) {
               // CTAs with empty ranges (grids larger than the K-tile count) hold no piece
               if (range_begin(q + 1, G, W) == range_begin(q, G, W)) continue;
-              const float* pp = p.part + (size_t)part_slot(q, u, G, W, p.KT) * Cfg::kPartFloats;
-              up += __ldcg(pp + cc * 128 + row);
-              gt += __ldcg(pp + (BN + cc) * 128 + row);
+              const float* pp = p.part + (size_t)part_slot(q, u, G, W, p.KT) * Cfg::kPartFloats +
+                                c0 * 128 + row;
+              float a[16], b[16];
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) {
+                a[jj] = __ldcg(pp + jj * 128);
+                b[jj] = __ldcg(pp + (BN + jj) * 128);
+              }
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) {
+                up[jj] += a[jj];
+                gt[jj] += b[jj];
+              }
             }
-            const float h = f < p.I ? swiglu(gt, up, p.limit, p.alpha, p.beta) : 0.f;
-            const size_t r = (size_t)(p0 + cc);
-            requant_store(h, lane, r * p.Ip, r * (p.Ip / 32), f, p.hq, p.hs);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              if (c0 + jj < n) {
+                const float h = f < p.I ? swiglu(gt[jj], up[jj], p.limit, p.alpha, p.beta) : 0.f;
+                const size_t r = (size_t)(p0 + c0 + jj);
+                requant_store(h, lane, r * p.Ip, r * (p.Ip / 32), f, p.hq, p.hs);
+              }
+            }
           }
         }
       }
@@ -350,286 +362,49 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   if (warp == 0) tmem_dealloc(tmem, Cfg::kAlloc);
 }
 
-template <int BN>
-struct PersistFc2Cfg {
-  static constexpr int kB = BN * 128;
-  static constexpr int kStage = (kTileBytesA + kB + 2 * 512 + 1023) / 1024 * 1024;
-  static constexpr int kStages = 4;                      // two CTAs per SM
-  static constexpr int kSfStage = BN * kSfChunk * 4;
-  static constexpr int kSmem = kStages * kStage + kSfStage + 1024;
-  static constexpr int kCols = 2 * BN + 8 * kStages;     // two accumulators, scale ring
-  static constexpr int kAlloc = kCols <= 64 ? 64 : kCols <= 128 ? 128 : 256;
-};
-
-struct PersistFc2Params {
-  CUtensorMap tm_w2;         // packed FP4 tiles [E*RB*KT][128][128], box 128 x 128 x 1
-  CUtensorMap tm_h;          // E4M3 [Sm][Ip], boxes 128 x BN
-  const uint8_t* w2;         // raw weight tiles (L2 prefetch), 8192 B each
-  const uint8_t* sf2;        // weight scale atoms [E][RB][KT][512]
-  const uint8_t* hs;         // [Sm][Ip/32]
-  const int4* tiles;
-  const int32_t* ctrl;
-  int32_t* err;
-  const int32_t* perm;
-  const int32_t* slot_of;
-  const float* topk_w;
-  float* acc;                // [M][H] atomic mode
-  float* rbuf;               // [M*k][H] deterministic mode
-  int32_t* tickets;          // [RB] units of each row block completed
-  __nv_bfloat16* out;        // [M][H]
-  int M, H, Ip, KT, RB, Sm, topk, deterministic;
-};
-
-// Row block rb of every token's output: column h = rb * 128 + row for row = 0..127 (one per
-// thread of the calling 128 threads), the arithmetic of the separate finalize launch.
-__device__ __forceinline__ void finalize_block(const PersistFc2Params& p, int rb, int row) {
-  const int h = rb * 128 + row;
-  for (int t = 0; t < p.M; ++t) {
-    float v = 0.f;
-    if (!p.deterministic) {
-      v = __ldcg(p.acc + (size_t)t * p.H + h);
-    } else {
-      for (int j = 0; j < p.topk; ++j) {
-        const int f = t * p.topk + j;
-        if (p.slot_of[f] < 0) continue;
-        v += __ldcg(p.rbuf + (size_t)f * p.H + h);
-      }
-    }
-    p.out[(size_t)t * p.H + h] = __float2bfloat16_rn(v);
-  }
-}
-
-template <int BN>
-__global__ void __launch_bounds__(kStreamThreads)
-fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
-  using Cfg = PersistFc2Cfg<BN>;
-  constexpr int S = Cfg::kStages;
-  const int G = gridDim.x, c = blockIdx.x;
-  const int ntiles = p.ctrl[1];
-  const int units = ntiles * p.RB;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (units == 0) {
-    // no valid slot in the call: every output row is zero, written here
-    if (tid < 128)
-      for (int rb = c; rb < p.RB; rb += G) finalize_block(p, rb, tid);
-    return;
-  }
-  const int u_begin = (int)((long long)c * units / G);
-  const int u_end = (int)((long long)(c + 1) * units / G);
-  if (u_begin >= u_end) return;
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[S], empty[S], acc_full[2], acc_empty[2], drain;
-  __shared__ uint32_t s_tmem;
-  __shared__ int s_fail, s_nfin, s_fin[128];
-
-  if (warp == 0) {
-    tmem_alloc(&s_tmem, Cfg::kAlloc);
-    tmem_relinquish();
-  }
-  if (tid == 32) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 2);
-      mbar_init(&empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
-    }
-    mbar_init(&drain, 1);
-    s_fail = 0;
-    fence_barrier_init();
-  }
-  if (tid == 64) prefetch_tmap(&p.tm_w2);
-  if (tid == 96) prefetch_tmap(&p.tm_h);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = s_tmem;
-  bool ok = true;
-  int issued = 0;                                   // stages filled by the TMA producer
-  auto stage = [&](int s) { return smem + s * Cfg::kStage; };
-  // stage layout: A | B | SFA | SFB
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // L2 prefetch of the weight tile and scale atom of flat index y = unit * KT + kt
-      auto prefetch = [&](long long y) {
-        const int u = (int)(y / p.KT), kt = (int)(y % p.KT);
-        const int tile = u / p.RB, rb = u - tile * p.RB;
-        const size_t a = ((size_t)p.tiles[tile].x * p.RB + rb) * p.KT + kt;
-        bulk_prefetch_l2(p.w2 + a * kTxBytesA, kTxBytesA);
-        bulk_prefetch_l2(p.sf2 + a * 512, 512);
-      };
-      const long long y_end = (long long)u_end * p.KT;
-      long long yp = (long long)u_begin * p.KT;       // next flat index to prefetch
-      int i = 0;
-      for (int u = u_begin; u < u_end && ok; ++u) {
-        const int tile = u / p.RB, rb = u - tile * p.RB;
-        const int4 td = p.tiles[tile];
-        const int e = td.x, p0 = td.y;
-        for (int kt = 0; kt < p.KT && ok; ++kt, ++i) {
-          const int s = i % S;
-          for (const long long lim = std::min((long long)u * p.KT + kt + 2 * kPrefetchTiles,
-                                              y_end);
-               yp < lim; ++yp)
-            prefetch(yp);
-          if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
-          if (!ok) break;
-          uint8_t* st = stage(s);
-          const size_t a = ((size_t)e * p.RB + rb) * p.KT + kt;
-          mbar_arrive_expect_tx(&full[s], kTxBytesA + Cfg::kB + 512);
-          tma_load_3d(st, &p.tm_w2, 0, 0, (int)a, &full[s]);
-          tma_load_2d(st + kTileBytesA, &p.tm_h, kt * 128, p0, &full[s]);
-          bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
-        }
-      }
-      issued = i;
-    }
-  } else if (warp == 2) {
-    uint32_t* sfst = reinterpret_cast<uint32_t*>(smem + S * Cfg::kStage);
-    int i = 0, staged_tile = -1;
-    for (int u = u_begin; u < u_end && ok; ++u) {
-      const int tile = u / p.RB;
-      const int p0 = p.tiles[tile].y;
-      for (int kt = 0; kt < p.KT && ok; ++kt, ++i) {
-        const int s = i % S;
-        // the staged scales cover all of K when it fits one chunk: restage on a new tile only
-        if (kt % kSfChunk == 0 && (p.KT > kSfChunk || tile != staged_tile)) {
-          __syncwarp();
-          stage_act_sf<BN>(sfst, p.hs, p0, p.Sm, p.Ip / 32, kt, min(kSfChunk, p.KT - kt), lane);
-          __syncwarp();
-          staged_tile = tile;
-        }
-        if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
-        if (!ok) break;
-        write_act_sf<BN>(stage(s) + kTileBytesA + Cfg::kB + 512, sfst, kt % kSfChunk, lane);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[s]);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      int i = 0, j = 0;
-      for (int u = u_begin; u < u_end && ok; ++u, ++j) {
-        const int b = j & 1;
-        if (j >= 2) ok = mbar_wait(&acc_empty[b], ((j >> 1) - 1) & 1, p.err);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t d = tmem + b * BN;
-        for (int kt = 0; kt < p.KT && ok; ++kt, ++i) {
-          const int s = i % S;
-          ok = mbar_wait(&full[s], (i / S) & 1, p.err);
-          if (!ok) break;
-          tc_fence_after();
-          uint8_t* st = stage(s);
-          const uint32_t sf = tmem + 2 * BN + 8 * s;
-          tc_cp_sf(sf + 0, desc_sf(st + kTileBytesA + Cfg::kB));
-          tc_cp_sf(sf + 4, desc_sf(st + kTileBytesA + Cfg::kB + 512));
-#pragma unroll
-          for (int kb = 0; kb < 4; ++kb) {
-            const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, BN, kb);
-            mma_mxf8f6f4(d, desc_sw128(st + 32 * kb), desc_sw128(st + kTileBytesA + 32 * kb),
-                         idesc, sf + 0, sf + 4, (kt > 0 || kb > 0) ? 1u : 0u);
-          }
-          tc_commit(&empty[s]);
-        }
-        tc_commit(&acc_full[b]);
-      }
-    }
-  } else if (warp >= 4) {
-    const int quad = warp & 3;
-    const int row = quad * 32 + lane;                          // row of the 128-row block
-    int j = 0;
-    for (int u = u_begin; u < u_end; ++u, ++j) {
-      const int tile = u / p.RB, rb = u - tile * p.RB;
-      const int4 td = p.tiles[tile];
-      const int p0 = td.y, n = td.z;
-      const int h = rb * 128 + row;
-      const int b = j & 1;
-      ok = ok && mbar_wait(&acc_full[b], (j >> 1) & 1, p.err);
-      tc_fence_after();
-      __syncwarp();
-      const uint32_t trow = tmem + b * BN + ((uint32_t)(quad * 32) << 16);
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        float y[16];
-        tmem_ld16(trow + c0, y);
-        if (!ok || c0 >= n) continue;
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          if (c0 + jj < n) {
-            const int f = p.perm[p0 + c0 + jj];
-            const float v = p.topk_w[f] * y[jj];
-            if (p.deterministic)
-              p.rbuf[(size_t)f * p.H + h] = v;
-            else
-              atomicAdd(&p.acc[(size_t)(f / p.topk) * p.H + h], v);
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[b]);
-    }
-    // One fence for all of this CTA's combines, then a ticket per unit; the CTA holding the
-    // last ticket of row block rb (over all tiles) writes that block of the output.  Units go
-    // 128 at a time, one per epilogue thread.
-    __threadfence();
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    for (int u0 = u_begin; u0 < u_end; u0 += 128) {
-      if (row == 0) s_nfin = 0;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      const int u = u0 + row;
-      if (u < u_end) {
-        const int rb = u % p.RB;
-        if (atomicAdd(&p.tickets[rb], 1) == ntiles - 1) s_fin[atomicAdd(&s_nfin, 1)] = rb;
-      }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (ok) {
-        __threadfence();
-        for (int q = 0; q < s_nfin; ++q) finalize_block(p, s_fin[q], row);
-      }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-    }
-  }
-  if (!ok) s_fail = 1;
-  tc_fence_before();
-  __syncthreads();
-  if (s_fail) {
-    // a wait gave up: let this CTA's copies and MMAs land before its memory is released
-    if (warp == 0 && lane == 0) drain_stage_loads<S>(full, issued, p.err);
-    if (warp == 1 && lane == 0) {
-      tc_commit(&drain);
-      mbar_wait(&drain, 0, p.err);
-    }
-    tc_fence_before();
-    __syncthreads();
-  }
-  if (warp == 0) tmem_dealloc(tmem, Cfg::kAlloc);
-}
-
 // ---------------------------------------------------------------------------------- host side
 
 constexpr int kStreamMaxCtas = 320;   // partial slots are reserved for this many CTAs
 
-// Resident CTAs (at most two per SM) of a persistent kernel with `smem` bytes of dynamic shared
-// memory, capped at `cap`.
+// Resident CTAs of a persistent kernel: as many per SM as shared memory and tensor memory hold
+// (`smem` dynamic bytes and `tmem_cols` columns per CTA), capped at `per_sm_cap` per SM and at
+// `cap` in all.  (The occupancy query of the runtime reports one CTA per SM for any kernel that
+// allocates tensor memory, although several are co-scheduled when both memories allow it.)
 template <typename K>
-static int persistent_grid(K kernel, int smem, int cap) {
-  int per_sm = 0, sms = 0, dev = 0;
+static int persistent_grid(K kernel, int smem, int tmem_cols, int per_sm_cap, int cap) {
+  int sms = 0, dev = 0, sm_smem = 0, reserved = 0;
   cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // all of the unified L1 / shared storage as shared memory
+  cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       (int)cudaSharedmemCarveoutMaxShared);
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kStreamThreads, smem);
-  return std::min(cap, std::max(1, std::min(per_sm, 2)) * std::max(sms, 1));
+  cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) fa.sharedSizeBytes = 0;
+  const int per_cta = smem + (int)fa.sharedSizeBytes + reserved;
+  int per_sm = std::min(sm_smem / std::max(per_cta, 1), 512 / std::max(tmem_cols, 32));
+  per_sm = std::max(1, std::min(per_sm, per_sm_cap));
+  (void)cudaGetLastError();
+  return std::min(cap, per_sm * std::max(sms, 1));
 }
 
-// The stream-K fc1 serves the 16-token tiles of decode-size calls.
-bool fc1_stream_supported(int bn) { return bn == 16; }
+// The stream-K fc1 serves the 16-token tiles of decode-size calls whose (tile, row block) units
+// outnumber the CTAs that fit on the GPU at once: there the one-unit-per-CTA kernel would run a
+// second, mostly empty wave.
+bool fc1_stream_preferred(int bn, int units) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      (void)cudaGetLastError();
+      sms = 1;
+    }
+  }
+  return bn == 16 && units > 2 * sms;
+}
 // Scratch of its partial slots: 2 per CTA, each [2][16][128] fp32.
 size_t fc1_stream_part_bytes() { return (size_t)2 * kStreamMaxCtas * 2 * 16 * 128 * 4; }
 
@@ -653,40 +428,8 @@ cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanD
   p.H = d.H; p.I = d.I; p.Ip = d.Ip; p.RT = cdiv(d.I, 128); p.KT = d.H / 128; p.Sm = Sm;
   p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
   static const int G = persistent_grid(fc1_stream_kernel<16>, StreamCfg<16>::kSmem,
-                                       kStreamMaxCtas);
+                                       StreamCfg<16>::kAlloc, 2, kStreamMaxCtas);
   fc1_stream_kernel<16><<<G, kStreamThreads, StreamCfg<16>::kSmem, st>>>(p);
-  return cudaGetLastError();
-}
-
-// The persistent fc2 serves the 16- and 32-token tiles of decode-size calls.
-bool fc2_persist_supported(int bn) { return bn == 16 || bn == 32; }
-
-cudaError_t launch_fc2_persist(const DevWeights& w, const RunPtrs& r, const PlanDims& d, int bn,
-                               int M, const float* topk_w, int32_t* tickets, void* out,
-                               cudaStream_t st) {
-  PersistFc2Params p;
-  memset(&p, 0, sizeof(p));
-  const int Sm = M * d.topk;
-  p.RB = d.H / 128;
-  p.KT = d.Ip / 128;
-  if (!tmap_fp4(&p.tm_w2, w.w2, 128, (long long)d.E * p.RB * p.KT) ||
-      !tmap_u8(&p.tm_h, r.hq, d.Ip, Sm, bn))
-    return cudaErrorInvalidValue;
-  p.w2 = w.w2;
-  p.sf2 = w.s2; p.hs = r.hs; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
-  p.perm = r.perm; p.slot_of = r.slot_of; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;
-  p.tickets = tickets; p.out = reinterpret_cast<__nv_bfloat16*>(out);
-  p.M = M; p.H = d.H; p.Ip = d.Ip; p.Sm = Sm; p.topk = d.topk;
-  p.deterministic = d.deterministic;
-  if (bn == 16) {
-    static const int G = persistent_grid(fc2_persist_kernel<16>, PersistFc2Cfg<16>::kSmem, 1 << 20);
-    fc2_persist_kernel<16><<<G, kStreamThreads, PersistFc2Cfg<16>::kSmem, st>>>(p);
-  } else if (bn == 32) {
-    static const int G = persistent_grid(fc2_persist_kernel<32>, PersistFc2Cfg<32>::kSmem, 1 << 20);
-    fc2_persist_kernel<32><<<G, kStreamThreads, PersistFc2Cfg<32>::kSmem, st>>>(p);
-  } else {
-    return cudaErrorInvalidValue;
-  }
   return cudaGetLastError();
 }
 

@@ -101,8 +101,7 @@ struct Scratch {
   size_t xq, xs;    // W4A8: u8 [Sm][H], u8 [Sm][H/32], one row per slot position
   size_t g;         // fp32 fc1 output [Sm][2][Ip] (CUDA-core path) / split-K partial sums
                     // [splits][Sm][2][Ip] (tensor-core paths)
-  size_t tickets;   // int32 [max_tiles][ceil(I/128)] fc1 completion tickets, then [H/128]
-                    // row-block tickets of the persistent fc2
+  size_t tickets;   // int32 [max_tiles][ceil(I/128)] fc1 completion tickets
   size_t part;      // W4A8: fp32 partial sums of the stream-K fc1 (fixed-size slots)
   size_t hq, hs;    // W4A8: u8 [Sm][Ip], u8 [Sm][Ip/32]
   size_t h16;       // W4A16: bf16 [Sm][Ip] (CUDA-core path) or f16 (tensor-core path)
