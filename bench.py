@@ -209,7 +209,7 @@ def kernel_traffic(kernel):
     source changed since the counters were taken."""
     import hashlib
     try:
-        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
@@ -417,6 +417,10 @@ def our_arm(args, rank, world):
             "unit": "GB/s",
             "frac": achieved / peak,
             "traffic": None if traffic is None else traffic["bytes_per_launch"],
+            "traffic_kernel": FC1_KERNEL,
+            "traffic_workload": None if traffic is None else traffic["workload"],
+            "traffic_algorithmic_bytes": None if traffic is None
+            else traffic["algorithmic_bytes_per_launch"],
             "algorithmic_bytes": "distinct touched experts x (w13 codes + E8M0 scales = "
                                  f"{EXPERT_BYTES_W13[DECODE_CFG]} B) + x rows",
             "kernel_ms_per_step": dom_ms / args.steps,
