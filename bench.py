@@ -300,17 +300,25 @@ def our_arm(args, rank, world):
         for c in calls:   # eager warm-up of each shape
             layer(c["x"], c["ids"], c["w"], c["out"])
         stream.synchronize()
+        # two graphs per call: the timed one, whose kernels launch as a chain, and one with an
+        # event record between stages (which breaks the chain) for the per-kernel durations
         for c in calls:
-            moe_plan_set_profile_events(layer.plan, c["ev"])
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 layer(c["x"], c["ids"], c["w"], c["out"])
             c["graph"] = g
-        moe_plan_set_profile_events(layer.plan, [])
+            moe_plan_set_profile_events(layer.plan, c["ev"])
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                layer(c["x"], c["ids"], c["w"], c["out"])
+            c["graph_ev"] = g
+            moe_plan_set_profile_events(layer.plan, [])
     torch.cuda.synchronize()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
-    def step(si, record):
+    def step(si, stage_events=False):
+        """One ladder pass; with stage_events the instrumented graphs run and the fc1 stage
+        durations are returned instead of whole-call times."""
         tot_ms, dom_ms, dom_bytes, toks = 0.0, 0.0, 0.0, 0
         pairs = []
         with torch.cuda.stream(stream):
@@ -320,14 +328,15 @@ def our_arm(args, rank, world):
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                c["graph"].replay()
+                (c["graph_ev"] if stage_events else c["graph"]).replay()
                 b.record(stream)
                 pairs.append((a, b, c))
         stream.synchronize()
         for a, b, c in pairs:
             tot_ms += a.elapsed_time(b)
-            dom_ms += c["ev"][dom_i].elapsed_time(c["ev"][dom_i + 1])
-            dom_bytes += c["distinct"] * EXPERT_BYTES_W13[DECODE_CFG] + c["M"] * cfg.H
+            if stage_events:
+                dom_ms += c["ev"][dom_i].elapsed_time(c["ev"][dom_i + 1])
+                dom_bytes += c["distinct"] * EXPERT_BYTES_W13[DECODE_CFG] + c["M"] * cfg.H
             toks += c["tokens"]
         return tot_ms, dom_ms, dom_bytes, toks
 
@@ -335,19 +344,22 @@ def our_arm(args, rank, world):
     toks = 0
     with ClockSampler(local) as clk:
         for si in range(args.warmup):
-            step(si, False)
+            step(si)
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         clk.start()
         for si in range(args.steps):
-            a, b, c, d = step(args.warmup + si, True)
+            a, _, _, d = step(args.warmup + si)
             tot_ms += a
-            dom_ms += b
-            dom_bytes += c
             toks += d
         torch.cuda.synchronize()
         clk.stop()
+        # fc1 durations: the same calls again through the stage-instrumented graphs
+        for si in range(max(3, args.steps // 4)):
+            _, b, c, _ = step(args.warmup + si, stage_events=True)
+            dom_ms += b
+            dom_bytes += c
     tot_ms, all_toks = reduce_over_ranks(tot_ms, toks, world, device="cuda")
     if world > 1:
         dist.barrier()
@@ -423,7 +435,9 @@ def our_arm(args, rank, world):
             else traffic["algorithmic_bytes_per_launch"],
             "algorithmic_bytes": "distinct touched experts x (w13 codes + E8M0 scales = "
                                  f"{EXPERT_BYTES_W13[DECODE_CFG]} B) + x rows",
-            "kernel_ms_per_step": dom_ms / args.steps,
+            "kernel_ms_per_ladder_pass": dom_ms / max(3, args.steps // 4),
+            "kernel_timing": "CUDA events around fc1 inside graphs of the same calls (separate "
+                             "replays: an event between kernels breaks the launch chain)",
         },
         "stages": stages,
         "cpu_baseline": cpu,

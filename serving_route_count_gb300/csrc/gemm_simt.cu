@@ -148,6 +148,8 @@ __device__ __forceinline__ uint4 load_a8(const SimtArgs& a, int p, int k) {
 template <bool FC2>
 __global__ void __launch_bounds__(kSimtThreads)
 gemm_simt_kernel(SimtArgs a) {
+  pdl_wait_prev();     // previous kernel of the call complete, its writes visible
+  pdl_launch_next();
   const int tile = blockIdx.x;
   if (tile >= a.r.ctrl[1]) return;
   const int4 td = a.r.tiles[tile];
@@ -243,6 +245,8 @@ __global__ void __launch_bounds__(256)
 act_kernel(const float* __restrict__ g, const int32_t* __restrict__ ctrl, int I, int Ip,
            float limit, float alpha, float beta, int a8, uint8_t* __restrict__ hq,
            uint8_t* __restrict__ hs, __nv_bfloat16* __restrict__ h16) {
+  pdl_wait_prev();     // previous kernel of the call complete, its writes visible
+  pdl_launch_next();
   const int S = ctrl[2];
   const int nb = Ip / 32;
   const size_t total = (size_t)S * nb;
@@ -293,6 +297,8 @@ __global__ void __launch_bounds__(256)
 finalize_kernel(int M, int H, int topk, int deterministic, const float* __restrict__ acc,
                 const float* __restrict__ rbuf, const int32_t* __restrict__ slot_of,
                 __nv_bfloat16* __restrict__ out) {
+  pdl_wait_prev();     // previous kernel of the call complete, its writes visible
+  pdl_launch_next();
   const size_t total = (size_t)M * (H / 8);
   for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (size_t)gridDim.x * blockDim.x) {
@@ -330,11 +336,8 @@ finalize_kernel(int M, int H, int topk, int deterministic, const float* __restri
 static cudaError_t launch_simt_fc(bool fc2, const SimtArgs& a, int max_tiles, cudaStream_t st) {
   const int R = fc2 ? a.H : 2 * a.I;
   dim3 grid(max_tiles, cdiv(R, kSimtRowsPerCta));
-  if (fc2)
-    gemm_simt_kernel<true><<<grid, kSimtThreads, 0, st>>>(a);
-  else
-    gemm_simt_kernel<false><<<grid, kSimtThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return fc2 ? launch_kernel(gemm_simt_kernel<true>, grid, dim3(kSimtThreads), 0, st, true, a)
+             : launch_kernel(gemm_simt_kernel<false>, grid, dim3(kSimtThreads), 0, st, true, a);
 }
 
 static cudaError_t launch_act(const RunPtrs& r, int Sm, int I, int Ip, float limit, float alpha,
@@ -342,9 +345,9 @@ static cudaError_t launch_act(const RunPtrs& r, int Sm, int I, int Ip, float lim
   const size_t total = (size_t)Sm * (Ip / 32);
   int blocks = (int)std::min<size_t>((total + 255) / 256, 152 * 16);
   if (blocks < 1) blocks = 1;
-  act_kernel<<<blocks, 256, 0, st>>>(r.g, r.ctrl, I, Ip, limit, alpha, beta, a8, r.hq, r.hs,
-                                     r.h16);
-  return cudaGetLastError();
+  return launch_kernel(act_kernel, dim3(blocks), dim3(256), 0, st, true,
+                       static_cast<const float*>(r.g), static_cast<const int32_t*>(r.ctrl), I, Ip,
+                       limit, alpha, beta, a8, r.hq, r.hs, r.h16);
 }
 
 static cudaError_t launch_finalize(int M, int H, int topk, int det, const RunPtrs& r, void* out,
@@ -352,9 +355,10 @@ static cudaError_t launch_finalize(int M, int H, int topk, int det, const RunPtr
   const size_t total = (size_t)M * (H / 8);
   int blocks = (int)std::min<size_t>((total + 255) / 256, 152 * 16);
   if (blocks < 1) blocks = 1;
-  finalize_kernel<<<blocks, 256, 0, st>>>(M, H, topk, det, r.acc, r.rbuf, r.slot_of,
-                                          reinterpret_cast<__nv_bfloat16*>(out));
-  return cudaGetLastError();
+  return launch_kernel(finalize_kernel, dim3(blocks), dim3(256), 0, st, true, M, H, topk, det,
+                       static_cast<const float*>(r.acc), static_cast<const float*>(r.rbuf),
+                       static_cast<const int32_t*>(r.slot_of),
+                       reinterpret_cast<__nv_bfloat16*>(out));
 }
 
 // stage 0: fc1, 1: SwiGLU + requant, 2: fc2 + combine, 3: finalize

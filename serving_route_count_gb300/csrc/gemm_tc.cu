@@ -97,6 +97,8 @@ __global__ void __launch_bounds__(kTcThreads)
 fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::kStages1;
+  pdl_wait_prev();     // previous kernel of the call complete, its writes visible
+  pdl_launch_next();
   const int tile = blockIdx.x;
   if (tile >= p.ctrl[1]) return;
   const int4 td = p.tiles[tile];
@@ -322,6 +324,8 @@ __global__ void __launch_bounds__(kTcThreads)
 fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::kStages2;
+  pdl_wait_prev();     // previous kernel of the call complete, its writes visible
+  pdl_launch_next();
   const int tile = blockIdx.x;
   if (tile >= p.ctrl[1]) return;
   const int4 td = p.tiles[tile];
@@ -521,8 +525,7 @@ static cudaError_t launch_fc1_bn(const TcFc1Params& p, int tiles, cudaStream_t s
     attr = true;
   }
   dim3 grid(tiles, p.RT, p.splits);
-  fc1_tc_kernel<BN><<<grid, kTcThreads, Cfg::kSmem1, st>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(fc1_tc_kernel<BN>, grid, dim3(kTcThreads), Cfg::kSmem1, st, true, p);
 }
 
 template <int BN>
@@ -538,8 +541,7 @@ static cudaError_t launch_fc2_bn(const TcFc2Params& p, int tiles, cudaStream_t s
     attr = true;
   }
   dim3 grid(tiles, p.H / 128);
-  fc2_tc_kernel<BN><<<grid, kTcThreads, Cfg::kSmem2, st>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(fc2_tc_kernel<BN>, grid, dim3(kTcThreads), Cfg::kSmem2, st, true, p);
 }
 
 // fc1 (stage 0) or fc2 (stage 1) of the W4A8 tensor-core path.

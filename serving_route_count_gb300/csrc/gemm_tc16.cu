@@ -197,6 +197,8 @@ __global__ void __launch_bounds__(k16Threads, 1)
 gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   using Cfg = Tc16Cfg<BN, FC2>;
   constexpr int kMats = Cfg::kMats;
+  pdl_wait_prev();     // previous kernel of the call complete, its writes visible
+  pdl_launch_next();
   const int tile = blockIdx.x;
   if (tile >= p.ctrl[1]) return;
   const int4 td = p.tiles[tile];
@@ -525,8 +527,7 @@ static cudaError_t launch16(const Tc16Params& p, int tiles, cudaStream_t st) {
     attr = true;
   }
   dim3 grid(tiles, p.RB, FC2 ? 1 : p.splits);
-  gemm_tc16_kernel<BN, FC2><<<grid, k16Threads, Cfg::kSmem, st>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(gemm_tc16_kernel<BN, FC2>, grid, dim3(k16Threads), Cfg::kSmem, st, true, p);
 }
 
 // stage 0: fc1 (+ SwiGLU, h -> bf16 -> f16), stage 1: fc2 (+ combine).

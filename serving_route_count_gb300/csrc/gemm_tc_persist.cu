@@ -89,6 +89,8 @@ __global__ void __launch_bounds__(kStreamThreads)
 fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   using Cfg = StreamCfg<BN>;
   constexpr int S = Cfg::kStages;
+  pdl_wait_prev();     // previous kernel of the call complete, its writes visible
+  pdl_launch_next();
   const int G = gridDim.x, c = blockIdx.x;
   const int units = p.ctrl[1] * p.RT;
   const long long W = (long long)units * p.KT;
@@ -429,8 +431,8 @@ cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanD
   p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
   static const int G = persistent_grid(fc1_stream_kernel<16>, StreamCfg<16>::kSmem,
                                        StreamCfg<16>::kAlloc, 2, kStreamMaxCtas);
-  fc1_stream_kernel<16><<<G, kStreamThreads, StreamCfg<16>::kSmem, st>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(fc1_stream_kernel<16>, dim3(G), dim3(kStreamThreads), StreamCfg<16>::kSmem,
+                       st, true, p);
 }
 
 }  // namespace moe

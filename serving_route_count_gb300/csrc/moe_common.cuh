@@ -183,4 +183,36 @@ __device__ __forceinline__ uint32_t f32_to_e4m3(float a) {
 
 __device__ __forceinline__ void set_error(int32_t* ctrl, int bit) { atomicOr(ctrl, bit); }
 
+// ----------------------------------------------------------------------------------------------
+// Chained launches (programmatic dependent launch)
+// ----------------------------------------------------------------------------------------------
+// The kernels of one call are launched as a chain: each lets the next one launch once all of its
+// own CTAs are running (pdl_launch_next), and each waits for the previous one to complete and
+// its memory to be visible (pdl_wait_prev) before touching any buffer of the call.  A kernel that
+// was launched without the chaining attribute returns from the wait at once.
+__device__ __forceinline__ void pdl_wait_prev() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_next() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launches kernel<<<grid, block, smem, st>>>(args...); `chained` lets it start (up to its
+// pdl_wait_prev) while the previous kernel of the stream is still running.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, bool chained, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = chained ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace moe

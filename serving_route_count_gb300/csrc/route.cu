@@ -57,6 +57,8 @@ route_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile_slots, int
   __shared__ int s_wc[kRouteWarps][kMaxRouteExperts / 4];  // per-warp counts, 8 bits each
   __shared__ int s_warp[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait_prev();     // previous kernel of the call complete, its writes visible
+  pdl_launch_next();
 
   if (tid == 0) ctrl[0] = 0;  // error word of this call
   for (int e = tid; e < E; e += kRouteThreads) s_cnt[e] = 0;
@@ -156,6 +158,8 @@ actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t*
             const int32_t* __restrict__ perm, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
             uint16_t* __restrict__ x16, int32_t* __restrict__ err, ZeroRegion z0, ZeroRegion z1,
             ZeroRegion z2) {
+  pdl_wait_prev();
+  pdl_launch_next();
   const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t gsz = (size_t)gridDim.x * blockDim.x;
   if (xq != nullptr) {
@@ -229,9 +233,9 @@ actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t*
 
 cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int max_tiles,
                          const RunPtrs& r, cudaStream_t st) {
-  route_kernel<<<1, kRouteThreads, 0, st>>>(ids, Mk, E, tile_slots, max_tiles, r.cnt, r.off,
-                                            r.perm, r.slot_of, r.tiles, r.ctrl);
-  return cudaGetLastError();
+  // first kernel of a call: an ordinary launch (the previous call may still read the tables)
+  return launch_kernel(route_kernel, dim3(1), dim3(kRouteThreads), 0, st, false, ids, Mk, E,
+                       tile_slots, max_tiles, r.cnt, r.off, r.perm, r.slot_of, r.tiles, r.ctrl);
 }
 
 cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
@@ -243,12 +247,12 @@ cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r,
       std::max(z0_words / 4, std::max(z1_words / 4, z2_words / 4)));
   int blocks = (int)std::min<size_t>((work + 255) / 256, 152 * 8);
   if (blocks < 1) blocks = 1;
-  actq_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), H, topk, r.ctrl,
-                                      r.perm, quant_x ? r.xq : nullptr, quant_x ? r.xs : nullptr,
-                                      to_f16 ? r.x16 : nullptr, r.ctrl,
-                                      ZeroRegion{z0, z0_words}, ZeroRegion{z1, z1_words},
-                                      ZeroRegion{z2, z2_words});
-  return cudaGetLastError();
+  return launch_kernel(actq_kernel, dim3(blocks), dim3(256), 0, st, true,
+                       reinterpret_cast<const __nv_bfloat16*>(x), H, topk,
+                       static_cast<const int32_t*>(r.ctrl), static_cast<const int32_t*>(r.perm),
+                       quant_x ? r.xq : nullptr, quant_x ? r.xs : nullptr,
+                       to_f16 ? r.x16 : nullptr, r.ctrl, ZeroRegion{z0, z0_words},
+                       ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words});
 }
 
 }  // namespace moe
