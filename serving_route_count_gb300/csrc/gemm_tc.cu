@@ -285,36 +285,16 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
     __syncthreads();
     if (s_last) {
       __threadfence();
-      // partial sums added in split order (the same result on every run), 16 columns at a time
-      // with each split's 32 loads issued together: one memory latency per split and chunk
-      for (int c0 = 0; c0 < n; c0 += 16) {
-        float up[16], gt[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) up[j] = gt[j] = 0.f;
-        for (int sp = 0; sp < p.splits; ++sp) {
-          const float* g = p.gacc + ((size_t)sp * p.Sm + p0 + c0) * 2 * p.Ip + f;
-          float a[16], b[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const bool in = c0 + j < n;
-            a[j] = in ? __ldcg(g + (size_t)j * 2 * p.Ip) : 0.f;
-            b[j] = in ? __ldcg(g + (size_t)j * 2 * p.Ip + p.Ip) : 0.f;
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            up[j] += a[j];
-            gt[j] += b[j];
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (c0 + j < n) {
-            const float h = f < p.I ? swiglu(gt[j], up[j], p.limit, p.alpha, p.beta) : 0.f;
-            const size_t row = (size_t)(p0 + c0 + j);
+      // partial sums added in split order: the same result on every run
+      reduce_pieces(
+          p.splits, n, (size_t)p.Ip,
+          [&](int sp, int c) { return p.gacc + ((size_t)sp * p.Sm + p0 + c) * 2 * p.Ip + f; },
+          [](int) { return false; },
+          [&](int c, float up, float gt) {
+            const float h = f < p.I ? swiglu(gt, up, p.limit, p.alpha, p.beta) : 0.f;
+            const size_t row = (size_t)(p0 + c);
             requant_store(h, lane, row * p.Ip, row * (p.Ip / 32), f, p.hq, p.hs);
-          }
-        }
-      }
+          });
     }
   }
 }

@@ -312,37 +312,22 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
           // the unit's pieces in K order: CTAs cta_of(u*KT) .. cta_of(u*KT + KT - 1)
           const int c_first = cta_of((long long)u * p.KT, G, W);
           const int c_last = cta_of((long long)u * p.KT + p.KT - 1, G, W);
-          // 16 columns at a time, each piece's 32 loads issued together
-          for (int c0 = 0; c0 < n; c0 += 16) {
-            float up[16], gt[16];
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) up[jj] = gt[jj] = 0.f;
-            for (int q = c_first; q <= c_last; ++q) {
-              // CTAs with empty ranges (grids larger than the K-tile count) hold no piece
-              if (range_begin(q + 1, G, W) == range_begin(q, G, W)) continue;
-              const float* pp = p.part + (size_t)part_slot(q, u, G, W, p.KT) * Cfg::kPartFloats +
-                                c0 * 128 + row;
-              float a[16], b[16];
-#pragma unroll
-              for (int jj = 0; jj < 16; ++jj) {
-                a[jj] = __ldcg(pp + jj * 128);
-                b[jj] = __ldcg(pp + (BN + jj) * 128);
-              }
-#pragma unroll
-              for (int jj = 0; jj < 16; ++jj) {
-                up[jj] += a[jj];
-                gt[jj] += b[jj];
-              }
-            }
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              if (c0 + jj < n) {
-                const float h = f < p.I ? swiglu(gt[jj], up[jj], p.limit, p.alpha, p.beta) : 0.f;
-                const size_t r = (size_t)(p0 + c0 + jj);
+          // pieces of the CTAs c_first.. in K order; CTAs with empty ranges (grids larger
+          // than the K-tile count) hold none
+          reduce_pieces(
+              c_last - c_first + 1, n, (size_t)BN * 128,
+              [&](int q, int cc) {
+                return p.part + (size_t)part_slot(c_first + q, u, G, W, p.KT) * Cfg::kPartFloats +
+                       cc * 128 + row;
+              },
+              [&](int q) {
+                return range_begin(c_first + q + 1, G, W) == range_begin(c_first + q, G, W);
+              },
+              [&](int cc, float up, float gt) {
+                const float h = f < p.I ? swiglu(gt, up, p.limit, p.alpha, p.beta) : 0.f;
+                const size_t r = (size_t)(p0 + cc);
                 requant_store(h, lane, r * p.Ip, r * (p.Ip / 32), f, p.hq, p.hs);
-              }
-            }
-          }
+              });
         }
       }
       x += k1 - k0;

@@ -70,6 +70,70 @@ static __device__ __forceinline__ void requant_store(float h, int lane, size_t r
   if (lane == 0) hs[row_base_s + (f >> 5)] = (uint8_t)s;
 }
 
+// Adds `np` partial sums of this thread's accumulator row, in piece order 0..np-1, for the tile
+// columns 0..n-1 and hands each column's (up, gate) total to emit(c, up, gate).  ptr(q, c) is
+// the address of piece q's up value of column c (gate at + gate_off); skip(q) marks a piece that
+// holds nothing (it adds nothing: its loads are predicated off and +0 leaves a sum unchanged).
+// The loads are issued 32 at a time - 4 pieces x 4 columns while n <= 4, 16 columns of one piece
+// otherwise - so a reduction costs a few memory latencies, not one per piece.  n and np are
+// uniform across the warp (emit may use warp shuffles).
+template <typename Ptr, typename Skip, typename Emit>
+static __device__ __forceinline__ void reduce_pieces(int np, int n, size_t gate_off, Ptr ptr,
+                                                     Skip skip, Emit emit) {
+  if (n <= 4) {
+    float up[4] = {0.f, 0.f, 0.f, 0.f}, gt[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int q0 = 0; q0 < np; q0 += 4) {
+      float a[4][4], b[4][4];
+#pragma unroll
+      for (int jq = 0; jq < 4; ++jq) {
+        const bool live = q0 + jq < np && !skip(q0 + jq);
+#pragma unroll
+        for (int jc = 0; jc < 4; ++jc) {
+          const bool in = live && jc < n;
+          const float* pp = in ? ptr(q0 + jq, jc) : nullptr;
+          a[jq][jc] = in ? __ldcg(pp) : 0.f;
+          b[jq][jc] = in ? __ldcg(pp + gate_off) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int jq = 0; jq < 4; ++jq)
+#pragma unroll
+        for (int jc = 0; jc < 4; ++jc) {
+          up[jc] += a[jq][jc];
+          gt[jc] += b[jq][jc];
+        }
+    }
+#pragma unroll
+    for (int jc = 0; jc < 4; ++jc)
+      if (jc < n) emit(jc, up[jc], gt[jc]);
+    return;
+  }
+  for (int c0 = 0; c0 < n; c0 += 16) {
+    float up[16], gt[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) up[j] = gt[j] = 0.f;
+    for (int q = 0; q < np; ++q) {
+      if (skip(q)) continue;
+      float a[16], b[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const bool in = c0 + j < n;
+        const float* pp = in ? ptr(q, c0 + j) : nullptr;
+        a[j] = in ? __ldcg(pp) : 0.f;
+        b[j] = in ? __ldcg(pp + gate_off) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        up[j] += a[j];
+        gt[j] += b[j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (c0 + j < n) emit(c0 + j, up[j], gt[j]);
+  }
+}
+
 // ---------------------------------------------------------------------------------- host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
