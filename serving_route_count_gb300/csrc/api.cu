@@ -16,6 +16,11 @@ cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int 
 cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
                         bool to_f16, void* z0, size_t z0_words, void* z1, size_t z1_words,
                         void* z2, size_t z2_words, cudaStream_t st);
+bool route_actq_small_supported(int Mk, int E);
+cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int tile_slots,
+                                    int max_tiles, const void* x, int H, int topk,
+                                    const RunPtrs& r, void* z0, size_t z0_words, void* z1,
+                                    size_t z1_words, void* z2, size_t z2_words, cudaStream_t st);
 // gemm_tc.cu
 cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                             int bn, int tiles, int splits, const float* topk_w, int M,
@@ -406,7 +411,9 @@ moe_status moe_call_launches(const moe_plan_t* plan, int M, int* launches) {
   }
   const bool tc8 = use_tc(d), t16 = use_tc16(d);
   if (tc8 || t16) {
-    *launches = 5;   // route, actq, fc1, fc2, finalize
+    // route and actq (one launch for small W4A8 calls), fc1, fc2, finalize
+    const bool small = tc8 && route_actq_small_supported(M * d.topk, d.E);
+    *launches = (small ? 1 : 2) + 3;
     return MOE_OK;
   }
   // route, actq (when something needs it), fc1, act, fc2, finalize
@@ -444,19 +451,30 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   // decode widths with more units than one wave of CTAs: the persistent stream-K fc1
   const bool streamk = tc8 && fc1_stream_preferred(bn, tiles * RT);
   const int splits = (tc && !streamk) ? fc1_splits(d, tiles) : 1;
-  prof(0);
-  cudaError_t e = launch_route(topk_ids, Sm, d.E, bn, plan->s.max_tiles, r, st);
-  if (e != cudaSuccess) return cuda_status(e);
-  prof(1);
+  // small W4A8 calls route and quantise in one launch
+  const bool small = tc8 && route_actq_small_supported(Sm, d.E);
   void* acc = d.deterministic ? nullptr : r.acc;
   const size_t acc_words = d.deterministic ? 0 : (size_t)M * d.H;
   void* g = nullptr;            // split partials are fully written before they are read
   const size_t g_words = 0;
   void* tk = (tc && (splits > 1 || streamk)) ? r.tickets : nullptr;
   const size_t tk_words = tk ? align_up((size_t)tiles * RT, 4) : 0;
-  if (a8 || acc || g || t16) {
-    e = launch_actq(x, M, d.H, d.topk, r, a8, t16, acc, acc_words, g, g_words, tk, tk_words, st);
+  prof(0);
+  cudaError_t e;
+  if (small) {
+    e = launch_route_actq_small(topk_ids, Sm, d.E, bn, plan->s.max_tiles, x, d.H, d.topk, r, acc,
+                                acc_words, g, g_words, tk, tk_words, st);
     if (e != cudaSuccess) return cuda_status(e);
+    prof(1);
+  } else {
+    e = launch_route(topk_ids, Sm, d.E, bn, plan->s.max_tiles, r, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    prof(1);
+    if (a8 || acc || g || t16) {
+      e = launch_actq(x, M, d.H, d.topk, r, a8, t16, acc, acc_words, g, g_words, tk, tk_words,
+                      st);
+      if (e != cudaSuccess) return cuda_status(e);
+    }
   }
   prof(2);
   if (tc) {

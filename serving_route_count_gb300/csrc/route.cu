@@ -15,6 +15,35 @@ constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kMaxRouteExperts = 1024;  // shared-memory tables below
 
+// Exclusive block scan of one value per thread over NW warps; returns the prefix, *total = sum.
+template <int NW>
+__device__ int block_excl_scan_n(int v, int* total, int* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < NW ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;  // inclusive prefix of warp sums
+  }
+  __syncthreads();
+  int warp_base = warp ? s_warp[warp - 1] : 0;
+  int t = s_warp[NW - 1];
+  __syncthreads();
+  *total = t;
+  return warp_base + x - v;
+}
+
 // Exclusive block scan of one value per thread; returns the prefix, *total = sum.
 __device__ int block_excl_scan(int v, int* total, int* s_warp) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -148,6 +177,39 @@ route_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile_slots, int
 // MXFP8 quantisation of x (W4A8) into slot order: one thread per block of 32 elements of the
 // row of the token that owns slot position p, so every GEMM tile reads contiguous rows.
 // The same launch clears the buffers that the later stages accumulate into.
+// One block of 32 bf16 activations -> 32 E4M3 codes + the E8M0 scale byte (OCP MX rule:
+// scale = 2^(floor(log2 amax) - 8), codes round to nearest even with saturation).
+__device__ __forceinline__ void quantize_block32(const __nv_bfloat16* __restrict__ src_bf16,
+                                                 uint8_t* __restrict__ q, uint8_t* __restrict__ s8) {
+  const uint4* src = reinterpret_cast<const uint4*>(src_bf16);
+  float v[32];
+#pragma unroll
+  for (int qq = 0; qq < 4; ++qq) {
+    uint4 u = src[qq];
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[qq * 8 + 2 * j] = __uint_as_float(w[j] << 16);
+      v[qq * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  const uint32_t s = mx_scale_byte(amax);
+  const float inv = e8m0_inv_f32(s);
+  uint32_t packed[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    packed[j] = f32_to_e4m3(v[4 * j] * inv) | (f32_to_e4m3(v[4 * j + 1] * inv) << 8) |
+                (f32_to_e4m3(v[4 * j + 2] * inv) << 16) | (f32_to_e4m3(v[4 * j + 3] * inv) << 24);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(q);
+  dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  *s8 = (uint8_t)s;
+}
+
 struct ZeroRegion {
   void* ptr;
   size_t words;   // 4-byte words, a multiple of 4
@@ -169,34 +231,7 @@ actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t*
       const size_t p = i / nb;
       const int b = (int)(i % nb);
       const int t = perm[p] / topk;
-      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H + b * 32);
-      float v[32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 u = src[q];
-        uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          v[q * 8 + 2 * j] = __uint_as_float(w[j] << 16);
-          v[q * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-        }
-      }
-      float amax = 0.f;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
-      const uint32_t s = mx_scale_byte(amax);
-      const float inv = e8m0_inv_f32(s);
-      uint32_t packed[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        packed[j] = f32_to_e4m3(v[4 * j] * inv) | (f32_to_e4m3(v[4 * j + 1] * inv) << 8) |
-                    (f32_to_e4m3(v[4 * j + 2] * inv) << 16) |
-                    (f32_to_e4m3(v[4 * j + 3] * inv) << 24);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(xq + p * H + b * 32);
-      dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-      dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-      xs[p * nb + b] = (uint8_t)s;
+      quantize_block32(x + (size_t)t * H + b * 32, xq + p * H + b * 32, xs + p * nb + b);
     }
   }
   if (x16 != nullptr) {
@@ -229,6 +264,137 @@ actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t*
     uint4* a4 = reinterpret_cast<uint4*>(zs[r].ptr);
     for (size_t i = gtid; i < zs[r].words / 4; i += gsz) a4[i] = make_uint4(0, 0, 0, 0);
   }
+}
+
+// Small W4A8 calls (at most kSmallRouteSlots flat slots): routing and MXFP8 quantisation in one
+// launch.  Every CTA routes the call in shared memory (the same tables as route_kernel: stable
+// order, tiles of up to tile_slots positions), CTA 0 writes them out, and all CTAs quantise
+// their share of the slot-ordered activation blocks and clear the accumulation buffers.
+constexpr int kSmallRouteSlots = 256;
+constexpr int kSmallRouteThreads = 256;
+
+__global__ void __launch_bounds__(kSmallRouteThreads)
+route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile_slots,
+                        int max_tiles, const __nv_bfloat16* __restrict__ x, int H, int topk,
+                        int32_t* __restrict__ cnt, int32_t* __restrict__ off,
+                        int32_t* __restrict__ perm, int32_t* __restrict__ slot_of,
+                        int4* __restrict__ tiles, int32_t* __restrict__ ctrl,
+                        uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, ZeroRegion z0,
+                        ZeroRegion z1, ZeroRegion z2) {
+  constexpr int NW = kSmallRouteThreads / 32;
+  __shared__ int s_ids[kSmallRouteSlots];
+  __shared__ int s_perm[kSmallRouteSlots];
+  __shared__ int s_cnt[kMaxRouteExperts];
+  __shared__ int s_warp[32];
+  const int tid = threadIdx.x;
+  const bool writer = blockIdx.x == 0;
+  pdl_wait_prev();
+  pdl_launch_next();
+
+  if (writer && tid == 0) ctrl[0] = 0;  // error word of this call
+  for (int e = tid; e < E; e += kSmallRouteThreads) s_cnt[e] = 0;
+  for (int f = tid; f < kSmallRouteSlots; f += kSmallRouteThreads) {
+    const int e = f < Mk ? ids[f] : -1;
+    s_ids[f] = (e >= 0 && e < E) ? e : -1;
+  }
+  __syncthreads();
+  for (int f = tid; f < Mk; f += kSmallRouteThreads)
+    if (s_ids[f] >= 0) atomicAdd(&s_cnt[s_ids[f]], 1);
+  __syncthreads();
+
+  // prefix over experts (thread t owns experts [t*per, t*per + per)), and over their tiles
+  const int per = (E + kSmallRouteThreads - 1) / kSmallRouteThreads;
+  int local = 0, ltiles = 0;
+  for (int i = 0; i < per; ++i) {
+    const int e = tid * per + i;
+    if (e < E) {
+      local += s_cnt[e];
+      ltiles += (s_cnt[e] + tile_slots - 1) / tile_slots;
+    }
+  }
+  int total, ttotal;
+  int base = block_excl_scan_n<NW>(local, &total, s_warp);
+  int tbase = block_excl_scan_n<NW>(ltiles, &ttotal, s_warp);
+  for (int i = 0; i < per; ++i) {
+    const int e = tid * per + i;
+    if (e < E) {
+      const int c = s_cnt[e];
+      if (writer) {
+        cnt[e] = c;
+        off[e] = base;
+        for (int p = 0; p < c; p += tile_slots) {
+          if (tbase < max_tiles)
+            tiles[tbase] = make_int4(e, base + p, min(tile_slots, c - p), 0);
+          else
+            set_error(ctrl, kErrTileOverflow);
+          ++tbase;
+        }
+      }
+      s_cnt[e] = base;   // now the expert's first position
+      base += c;
+    }
+  }
+  if (writer && tid == 0) {
+    off[E] = total;
+    ctrl[1] = min(ttotal, max_tiles);
+    ctrl[2] = total;
+  }
+  __syncthreads();
+  // stable positions: earlier flat slots of the same expert come first
+  for (int f = tid; f < Mk; f += kSmallRouteThreads) {
+    const int e = s_ids[f];
+    int pos = -1;
+    if (e >= 0) {
+      int rank = 0;
+      for (int g = 0; g < f; ++g) rank += s_ids[g] == e;
+      pos = s_cnt[e] + rank;
+      s_perm[pos] = f;
+      if (writer) perm[pos] = f;
+    }
+    if (writer) slot_of[f] = pos;
+  }
+  __syncthreads();
+
+  // MXFP8 quantisation of the slot-ordered rows (as actq_kernel)
+  const size_t gtid = (size_t)blockIdx.x * blockDim.x + tid;
+  const size_t gsz = (size_t)gridDim.x * blockDim.x;
+  const int nb = H / 32;
+  const size_t nblk = (size_t)total * nb;
+  for (size_t i = gtid; i < nblk; i += gsz) {
+    const size_t p = i / nb;
+    const int b = (int)(i % nb);
+    const int t = s_perm[p] / topk;
+    quantize_block32(x + (size_t)t * H + b * 32, xq + p * H + b * 32, xs + p * nb + b);
+  }
+  const ZeroRegion zs[3] = {z0, z1, z2};
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    if (zs[r].ptr == nullptr) continue;
+    uint4* a4 = reinterpret_cast<uint4*>(zs[r].ptr);
+    for (size_t i = gtid; i < zs[r].words / 4; i += gsz) a4[i] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+bool route_actq_small_supported(int Mk, int E) {
+  return Mk <= kSmallRouteSlots && E <= kMaxRouteExperts;
+}
+
+cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int tile_slots,
+                                    int max_tiles, const void* x, int H, int topk,
+                                    const RunPtrs& r, void* z0, size_t z0_words, void* z1,
+                                    size_t z1_words, void* z2, size_t z2_words, cudaStream_t st) {
+  if (!route_actq_small_supported(Mk, E)) return cudaErrorInvalidValue;
+  const size_t work = std::max((size_t)Mk * (H / 32),
+                               std::max(z0_words / 4, std::max(z1_words / 4, z2_words / 4)));
+  int blocks = (int)std::min<size_t>((work + kSmallRouteThreads - 1) / kSmallRouteThreads,
+                                     152 * 4);
+  if (blocks < 1) blocks = 1;
+  // first kernel of a call: an ordinary launch (the previous call may still read the tables)
+  return launch_kernel(route_actq_small_kernel, dim3(blocks), dim3(kSmallRouteThreads), 0, st,
+                       false, ids, Mk, E, tile_slots, max_tiles,
+                       reinterpret_cast<const __nv_bfloat16*>(x), H, topk, r.cnt, r.off, r.perm,
+                       r.slot_of, r.tiles, r.ctrl, r.xq, r.xs, ZeroRegion{z0, z0_words},
+                       ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words});
 }
 
 cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int max_tiles,
