@@ -138,9 +138,19 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
 moe_status moe_plan_set_swiglu_alpha_beta(moe_plan_t* plan, float alpha, float beta);
 
 /* Kernel family for later moe_run calls: 0 (default) = tcgen05 tensor-core GEMMs where the quant
- * mode has them (W4A8), CUDA-core GEMMs otherwise; 1 = CUDA-core GEMMs for every mode (a
- * slower, independent path, kept for cross-checks).  Errors: MOE_ERR_ARG. */
+ * mode and shape have them (W4A8; W4A16 NVFP4 / hybrid when I rounded up to 128 is a multiple
+ * of 256), CUDA-core GEMMs otherwise; 1 = CUDA-core GEMMs for every mode (a slower, independent
+ * path, kept for cross-checks).  Errors: MOE_ERR_ARG. */
 moe_status moe_plan_set_backend(moe_plan_t* plan, int backend);
+
+/* fc1 kernel of the W4A8 tensor-core path at the 16-token tile width (calls with M <= 16):
+ *   0 (default) automatic: one (tile, row block) unit per CTA, split along K for small calls,
+ *     while the units fit one wave of CTAs; the persistent stream-K kernel beyond;
+ *   1 always the unit-per-CTA kernel;  2 always the stream-K kernel.
+ * Both give results within the same tolerance of the method (in deterministic mode each is
+ * bit-stable on its own; the two differ in the rounding order of fc1's K sum).
+ * Errors: MOE_ERR_ARG. */
+moe_status moe_plan_set_fc1_kernel(moe_plan_t* plan, int choice);
 
 /* Size in bytes of the device scratch buffer moe_run needs (routing tables, quantised
  * activations, the fc1 -> fc2 intermediate, the combine buffer). */

@@ -272,7 +272,7 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   PlanDims& d = p->d;
   d.E = E; d.H = H; d.I = I; d.Ip = (int)align_up((size_t)I, 128); d.topk = topk; d.max_m = max_m;
   d.quant = quant_mode; d.deterministic = deterministic ? 1 : 0;
-  d.limit = swiglu_limit; d.alpha = 1.f; d.beta = 0.f; d.backend = 0;
+  d.limit = swiglu_limit; d.alpha = 1.f; d.beta = 0.f; d.backend = 0; d.fc1_kernel = 0;
   const size_t Sm = (size_t)max_m * topk;
   Scratch& s = p->s;
   s.max_tiles = (int)std::min<size_t>(Sm, (Sm + kSimtSlots - 1) / kSimtSlots +
@@ -395,6 +395,12 @@ const char* moe_profile_stage_names(const moe_plan_t* plan) {
                                                  : "route,actq,fc1,act,fc2,finalize";
 }
 
+moe_status moe_plan_set_fc1_kernel(moe_plan_t* plan, int choice) {
+  if (plan == nullptr || choice < 0 || choice > 2) return MOE_ERR_ARG;
+  plan->d.fc1_kernel = choice;
+  return MOE_OK;
+}
+
 moe_status moe_plan_set_backend(moe_plan_t* plan, int backend) {
   if (plan == nullptr || backend < 0 || backend > 1) return MOE_ERR_ARG;
   plan->d.backend = backend;
@@ -449,7 +455,8 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   const int tiles = call_tiles(d, plan->s.max_tiles, M, bn);
   const int RT = cdiv(d.I, 128);
   // decode widths with more units than one wave of CTAs: the persistent stream-K fc1
-  const bool streamk = tc8 && fc1_stream_preferred(bn, tiles * RT);
+  const bool streamk = tc8 && bn == 16 &&
+                       (d.fc1_kernel == 0 ? fc1_stream_preferred(bn, tiles * RT) : d.fc1_kernel == 2);
   const int splits = (tc && !streamk) ? fc1_splits(d, tiles) : 1;
   // small W4A8 calls route and quantise in one launch
   const bool small = tc8 && route_actq_small_supported(Sm, d.E);

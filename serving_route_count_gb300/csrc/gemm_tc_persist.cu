@@ -29,6 +29,7 @@ namespace moe {
 using namespace tc;
 
 constexpr int kStreamThreads = 256;
+constexpr int kSfSteps = 16;          // flat K steps of activation scales staged per chunk
 // K tiles of weights each CTA requests into L2 ahead of its TMA loads: more bytes in flight than
 // the shared-memory ring holds (the padded FP4 format takes 2 bytes of it per weight byte).
 constexpr int kPrefetchTiles = 8;
@@ -38,7 +39,7 @@ struct StreamCfg {
   static constexpr int kB = BN * 128;
   static constexpr int kStage = (2 * kTileBytesA + kB + 3 * 512 + 1023) / 1024 * 1024;
   static constexpr int kStages = 3;                      // two CTAs per SM
-  static constexpr int kSfStage = BN * kSfChunk * 4;
+  static constexpr int kSfStage = 2 * kSfSteps * BN * 4;  // double-buffered scale chunks
   static constexpr int kSmem = kStages * kStage + kSfStage + 1024;
   static constexpr int kAcc = 2 * BN;                    // one accumulator buffer: up | gate
   static constexpr int kCols = 2 * kAcc + 12 * kStages;
@@ -196,29 +197,55 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
       issued = i;
     }
   } else if (warp == 2) {
-    uint32_t* sfst = reinterpret_cast<uint32_t*>(smem + S * Cfg::kStage);
-    int i = 0;
-    for (long long x = x_begin; x < x_end && ok;) {
-      const int u = (int)(x / p.KT), k0 = (int)(x % p.KT);
-      const int k1 = (int)std::min<long long>(p.KT, k0 + (x_end - x));
-      const int p0 = p.tiles[u / p.RT].y;
-      for (int kt = k0; kt < k1 && ok; ++kt, ++i) {
-        const int s = i % S;
-        if ((kt - k0) % kSfChunk == 0) {
-          __syncwarp();
-          stage_act_sf<BN>(sfst, p.xs, p0, p.Sm, p.H / 32, kt, min(kSfChunk, k1 - kt), lane);
-          __syncwarp();
+    // Activation scale atoms.  The scales of kSfSteps consecutive flat K steps are staged per
+    // chunk with one batch of cp.async, double-buffered: the next chunk is in flight while the
+    // current one's atoms are written, so neither a new unit nor a new chunk stalls the ring.
+    uint32_t* sfbuf = reinterpret_cast<uint32_t*>(smem + S * Cfg::kStage);   // [2][steps][BN]
+    int cached_tile = -1, cached_p0 = 0;
+    auto stage_chunk = [&](long long c) {
+      uint32_t* dst = sfbuf + (c & 1) * kSfSteps * BN;
+      for (int idx = lane; idx < kSfSteps * BN; idx += 32) {
+        const int j = idx / BN, n = idx - j * BN;
+        const long long y = x_begin + c * kSfSteps + j;
+        if (y >= x_end) continue;
+        const int u = (int)(y / p.KT), kt = (int)(y % p.KT);
+        const int tile = u / p.RT;
+        if (tile != cached_tile) {
+          cached_tile = tile;
+          cached_p0 = p.tiles[tile].y;
         }
-        if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
-        if (!ok) break;
-        write_act_sf<BN>(stage(s) + 2 * kTileBytesA + Cfg::kB + 1024, sfst, (kt - k0) % kSfChunk,
-                         lane);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[s]);
+        if (cached_p0 + n < p.Sm)
+          cp_async4(dst + idx, p.xs + (size_t)(cached_p0 + n) * (p.H / 32) + kt * 4);
+        else
+          dst[idx] = 0;
       }
-      x += k1 - k0;
+      cp_async_commit();
+    };
+    const long long nflat = x_end - x_begin;
+    const long long nchunks = (nflat + kSfSteps - 1) / kSfSteps;
+    stage_chunk(0);
+    for (long long y = 0; y < nflat && ok; ++y) {
+      const int s = (int)(y % S);
+      const long long c = y / kSfSteps;
+      const int j = (int)(y % kSfSteps);
+      if (j == 0) {
+        if (c + 1 < nchunks) {
+          stage_chunk(c + 1);
+          cp_async_wait_group<1>();     // chunk c landed, chunk c + 1 may still fly
+        } else {
+          cp_async_wait_group<0>();
+        }
+        __syncwarp();
+      }
+      if (y >= S) ok = mbar_wait(&empty[s], ((y / S) - 1) & 1, p.err);
+      if (!ok) break;
+      write_act_sf_rows<BN>(stage(s) + 2 * kTileBytesA + Cfg::kB + 1024,
+                            sfbuf + (c & 1) * kSfSteps * BN + j * BN, lane);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[s]);
     }
+    cp_async_wait_group<0>();
   } else if (warp == 1) {
     if (lane == 0) {
       int i = 0, j = 0;

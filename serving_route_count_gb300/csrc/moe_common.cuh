@@ -116,6 +116,7 @@ struct PlanDims {
   int E, H, I, Ip, topk, max_m, quant, deterministic;
   float limit, alpha, beta;
   int backend;      // 0: tensor cores where implemented, 1: CUDA-core path
+  int fc1_kernel;   // W4A8 fc1 at 16-token tiles: 0 automatic, 1 unit per CTA, 2 stream-K
 };
 
 // Pointers of one call, resolved from the scratch base.

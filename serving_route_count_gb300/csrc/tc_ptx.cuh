@@ -78,6 +78,12 @@ TC_DEV void cp_async4(void* dst, const void* src) {
                : "memory");
 }
 TC_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+TC_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's committed cp.async groups are still in flight.
+template <int N>
+TC_DEV void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 TC_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -47,6 +47,16 @@ static __device__ __forceinline__ void write_act_sf(uint8_t* dst, const uint32_t
     *reinterpret_cast<uint32_t*>(dst + (n & 31) * 16 + (n >> 5) * 4) = stage[n * kSfChunk + j];
 }
 
+// Scale atom of BN activation rows for one K tile from a [j][BN] staging buffer (4 bytes per row:
+// the row's four E8M0 bytes of that K tile): byte (n%32)*16 + (n/32)*4 + kb.
+template <int BN>
+static __device__ __forceinline__ void write_act_sf_rows(uint8_t* dst, const uint32_t* rows,
+                                                         int lane) {
+#pragma unroll
+  for (int n = lane; n < BN; n += 32)
+    *reinterpret_cast<uint32_t*>(dst + (n & 31) * 16 + (n >> 5) * 4) = rows[n];
+}
+
 static __device__ __forceinline__ float swiglu(float gate, float up, float limit, float alpha,
                                                float beta) {
   const float g = fminf(gate, limit);

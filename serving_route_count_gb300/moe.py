@@ -109,6 +109,11 @@ def moe_plan_set_backend(plan, backend):
     _check(_lib.load().moe_plan_set_backend(_handle(plan), int(backend)), "moe_plan_set_backend")
 
 
+def moe_plan_set_fc1_kernel(plan, choice):
+    _check(_lib.load().moe_plan_set_fc1_kernel(_handle(plan), int(choice)),
+           "moe_plan_set_fc1_kernel")
+
+
 def moe_scratch_bytes(plan) -> int:
     n = ctypes.c_size_t()
     _check(_lib.load().moe_scratch_bytes(_handle(plan), ctypes.byref(n)), "moe_scratch_bytes")
@@ -259,7 +264,8 @@ class MoELayer:
     """
 
     def __init__(self, ck, topk, max_m, swiglu_limit=float("inf"), deterministic=False,
-                 alpha=None, beta=None, device="cuda", keep_checkpoint=False, backend=0):
+                 alpha=None, beta=None, device="cuda", keep_checkpoint=False, backend=0,
+                 fc1_kernel=0):
         self.E, self.H, self.I, self.topk, self.max_m = ck.E, ck.H, ck.I, topk, max_m
         self.quant = QUANT_OF[ck.quant]
         tier = ck.tier if ck.quant == "hybrid" else None
@@ -278,6 +284,8 @@ class MoELayer:
                                            0.0 if beta is None else beta)
         if backend:
             moe_plan_set_backend(self.plan, backend)
+        if fc1_kernel:
+            moe_plan_set_fc1_kernel(self.plan, fc1_kernel)
         self.scratch = torch.empty(moe_scratch_bytes(self.plan), dtype=torch.uint8, device=device)
         self.device = device
         self._io = None

@@ -177,14 +177,15 @@ def decode_layer():
     return cfg, ck
 
 
-@pytest.mark.parametrize("det", [0, 1])
-def test_decode_full_size_sampled(decode_layer, det):
+@pytest.mark.parametrize("det,fc1_kernel", [(0, 0), (1, 0), (0, 1), (1, 2)])
+def test_decode_full_size_sampled(decode_layer, det, fc1_kernel):
     """E=384, H=7168, I=576, top-6 at M=16 (last 4 rows padding): routing bit-exact for the
-    whole call, outputs of sampled rows against the oracle, padding rows exactly 0."""
+    whole call, outputs of sampled rows against the oracle, padding rows exactly 0; with the
+    automatic fc1 choice (stream-K here) and each fc1 kernel forced."""
     cfg, ck = decode_layer
     M = 16
     x, ids, w = S.make_inputs(cfg, M)
-    layer = _layer(ck, cfg.topk, M, cfg.swiglu_limit, det)
+    layer = _layer(ck, cfg.topk, M, cfg.swiglu_limit, det, fc1_kernel=fc1_kernel)
     got = run_layer(layer, x, ids, w)
     route = O.route(ids, cfg.E)
     for a, b in zip(layer.routing(M), route):
@@ -245,6 +246,36 @@ def test_w4a8_tensor_core_tile_widths(M, det):
     _, _, perm, _ = layer.routing(M)
     q, s = C.mxfp8_quantize(C.bf16_bits_to_f64(x))
     assert np.array_equal(xq, q[perm // cfg.topk]) and np.array_equal(xs, s[perm // cfg.topk])
+
+
+@pytest.mark.parametrize("M,det", [(1, 1), (3, 0), (9, 1), (16, 0)])
+def test_w4a8_stream_k_fc1(M, det):
+    """The persistent stream-K fc1 forced on small layers (E=16, H=1280: 10 K tiles per unit,
+    far fewer than the grid's CTAs, so units split into many pieces and most CTAs hold none):
+    every row against the oracle, the fc2 operand's codes against the oracle's requantisation
+    within the near-midpoint reading, and (deterministic mode) bit-identical repeats."""
+    cfg = small_cfg("mxfp4")
+    ck = S.make_checkpoint(cfg, seed=5000 + M)
+    rng = np.random.default_rng(6000 + M)
+    x = S.make_x(rng, M, cfg.H)
+    ids = S.zipf_topk(rng, M, cfg.E, cfg.topk, 1.1)
+    ids[rng.random(ids.shape) < 0.05] = -1
+    w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 2.5)
+    layer = _layer(ck, cfg.topk, M, 7.0, det, fc1_kernel=2)
+    got = run_layer(layer, x, ids, w)
+    st, code = layer.device_error()
+    assert st == 0 and code == 0, code
+    check_rows(got, ck, x, ids, w, 7.0)
+    if det:
+        assert np.array_equal(run_layer(layer, x, ids, w), got)
+    hq, hs = layer.intermediate(M)
+    h = O.slot_intermediate(ck, x, ids, 7.0)
+    q, s8 = C.mxfp8_quantize(h)
+    got_h = C.mxfp8_dequantize(hq[:, : cfg.I], hs[:, : cfg.I // 32])
+    want_h = C.mxfp8_dequantize(q, s8)
+    amb, alt = C.mxfp8_alternates(h, 1e-4)
+    mism = got_h != want_h
+    assert np.all(amb[mism] & (got_h[mism] == alt[mism])), int(mism.sum())
 
 
 @pytest.mark.parametrize("backend", [0, 1])
