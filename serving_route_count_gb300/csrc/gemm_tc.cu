@@ -32,10 +32,6 @@ namespace moe {
 
 using namespace tc;
 
-// K tiles of weights a CTA requests into L2 ahead of its TMA loads: more bytes in flight than the
-// shared-memory ring holds (the padded FP4 format takes 2 bytes of it per weight byte).
-constexpr int kPrefetchTiles = 8;
-
 template <int BN>
 struct TcCfg {
   static constexpr int kB = BN * 128;                         // activation tile bytes
@@ -67,8 +63,6 @@ struct TcFc1Params {
   int32_t* err;
   uint8_t* hq;               // [Sm][Ip]
   uint8_t* hs;               // [Sm][Ip/32]
-  const uint8_t* w13;        // raw weight tiles (L2 prefetch): the full ones, then the partial
-  const uint8_t* w13_tail;
   float* gacc;               // [splits][Sm][2][Ip] split-K partial sums, one slice per split
   int32_t* tickets;          // [max_tiles][RT]
   int H, I, Ip, RT, KT, Sm, splits;
@@ -88,7 +82,6 @@ struct TcFc2Params {
   const float* topk_w;
   float* acc;                // [M][H] atomic mode
   float* rbuf;               // [M*k][H] deterministic mode
-  const uint8_t* w2;         // raw weight tiles (L2 prefetch)
   int H, Ip, KT, Sm, topk, deterministic;
 };
 
@@ -141,26 +134,9 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
 
   if (warp == 0) {
     if (lane == 0) {
-      // L2 prefetch of the weight tiles and scale atoms of K tile kt
-      auto prefetch = [&](int kt) {
-        if (fb < p.RTf) {
-          bulk_prefetch_l2(p.w13 + ((size_t)((2 * e) * p.RTf + fb) * p.KT + kt) * kTxBytesA,
-                           kTxBytesA);
-          bulk_prefetch_l2(p.w13 + ((size_t)((2 * e + 1) * p.RTf + fb) * p.KT + kt) * kTxBytesA,
-                           kTxBytesA);
-        } else {
-          bulk_prefetch_l2(p.w13_tail + ((size_t)(2 * e) * p.KT + kt) * p.rem * 64, p.rem * 64);
-          bulk_prefetch_l2(p.w13_tail + ((size_t)(2 * e + 1) * p.KT + kt) * p.rem * 64,
-                           p.rem * 64);
-        }
-        bulk_prefetch_l2(p.sf13 + (((size_t)(2 * e) * p.RT + fb) * p.KT + kt) * 512, 512);
-        bulk_prefetch_l2(p.sf13 + (((size_t)(2 * e + 1) * p.RT + fb) * p.KT + kt) * 512, 512);
-      };
-      int ip = 0;                                   // next K tile (of this split) to prefetch
       int i = 0;
       for (; i < nk && ok; ++i) {
         const int s = i % S;
-        for (const int lim = min(i + kPrefetchTiles, nk); ip < lim; ++ip) prefetch(kt0 + ip);
         if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
         if (!ok) break;
         uint8_t* st = stage(s);
@@ -349,15 +325,9 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
 
   if (warp == 0) {
     if (lane == 0) {
-      const size_t a0 = ((size_t)e * (p.H / 128) + rt) * p.KT;   // first tile of this unit
-      int ip = 0;                                   // next K tile to prefetch into L2
       int i = 0;
       for (; i < nk && ok; ++i) {
         const int s = i % S;
-        for (const int lim = min(i + 2 * kPrefetchTiles, nk); ip < lim; ++ip) {
-          bulk_prefetch_l2(p.w2 + (a0 + ip) * kTxBytesA, kTxBytesA);
-          bulk_prefetch_l2(p.sf2 + (a0 + ip) * 512, 512);
-        }
         if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
         if (!ok) break;
         uint8_t* st = stage(s);
@@ -542,8 +512,6 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
     if (!tmap_u8(&p.tm_x, r.xq, d.H, Sm, bn)) return cudaErrorInvalidValue;
     p.sf13 = w.s13; p.xs = r.xs; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
     p.hq = r.hq; p.hs = r.hs; p.gacc = r.g; p.tickets = r.tickets;
-    p.w13 = w.w13;
-    p.w13_tail = w.w13 + (size_t)2 * d.E * p.RTf * kt * 8192;
     p.H = d.H; p.I = d.I; p.Ip = d.Ip; p.RT = RT; p.KT = d.H / 128; p.Sm = Sm;
     p.splits = splits; p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
     switch (bn) {
@@ -558,7 +526,7 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
     return cudaErrorInvalidValue;
   if (!tmap_u8(&p.tm_h, r.hq, d.Ip, Sm, bn)) return cudaErrorInvalidValue;
   p.sf2 = w.s2; p.hs = r.hs; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
-  p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf; p.w2 = w.w2;
+  p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;
   p.H = d.H; p.Ip = d.Ip; p.KT = d.Ip / 128; p.Sm = Sm; p.topk = d.topk;
   p.deterministic = d.deterministic;
   switch (bn) {

@@ -2,18 +2,17 @@
 //
 // Decode calls touch few experts (M = 16, top-6: ~66 experts x 5 weight blocks = ~330 units of
 // 56 K tiles each), so one CTA per unit leaves a tail wave that runs a fraction of the SMs.
-// Here a fixed grid of G CTAs (every SM times its resident CTAs) splits the flattened
-// (unit, K tile) space into G equal ranges; a CTA streams its range through one TMA pipeline,
-// crossing unit boundaries.  Each unit-piece ("segment") accumulates in one of two TMEM
-// buffers, so the epilogue warps drain segment j while the MMA fills segment j + 1:
+// Here a fixed grid of G CTAs (every SM times its resident CTAs) takes the units in full waves
+// (whole units, data-parallel) and splits the K tiles of the remaining units evenly over all
+// CTAs (stream-K).  A CTA streams its piece(s) first and then its whole units through one TMA
+// pipeline; each segment (a run of one unit's K tiles) accumulates in one of two TMEM buffers,
+// so the epilogue warps drain segment j while the MMA fills segment j + 1:
 //   - a segment that covers its whole unit goes straight to SwiGLU + MXFP8 requantisation;
-//   - otherwise it is stored as an fp32 partial in a slot of its CTA, and the CTA that
-//     completes the unit (ticket counting K tiles, no waiting) adds the unit's partials in
-//     K order - the same order on every run - and runs SwiGLU + requantisation.
+//   - a piece is stored as fp32 partial sums (the tile's token columns only) in a slot of its
+//     CTA, and the CTA that completes the unit (ticket counting K tiles, no waiting) adds the
+//     unit's pieces in K order - the same order on every run - and runs SwiGLU +
+//     requantisation.
 // Block-scaled MMA, layouts and operand staging are those of fc1_tc_kernel (gemm_tc.cu).
-//
-// The producer requests the weight tiles of the next kPrefetchTiles K tiles into L2 ahead of its
-// TMA loads, so more bytes are in flight than the shared-memory ring holds.
 //
 // Warps (256 threads): 0 TMA producer (lane 0), 1 MMA issuer (lane 0),
 // 2 activation-scale atoms, 3 idle, 4..7 epilogue (TMEM lane quadrant = warp % 4).
@@ -30,9 +29,6 @@ using namespace tc;
 
 constexpr int kStreamThreads = 256;
 constexpr int kSfSteps = 16;          // flat K steps of activation scales staged per chunk
-// K tiles of weights each CTA requests into L2 ahead of its TMA loads: more bytes in flight than
-// the shared-memory ring holds (the padded FP4 format takes 2 bytes of it per weight byte).
-constexpr int kPrefetchTiles = 8;
 
 template <int BN>
 struct StreamCfg {
@@ -51,8 +47,6 @@ struct StreamFc1Params {
   CUtensorMap tm_w13;        // full 128-row weight tiles
   CUtensorMap tm_w13_tail;   // partial last row tile
   CUtensorMap tm_x;          // E4M3 activations [Sm][H], boxes 128 x BN
-  const uint8_t* w13;        // raw weight tiles (L2 prefetch): the full ones (8192 B each)
-  const uint8_t* w13_tail;   // and the partial ones (rem * 64 B each)
   const uint8_t* sf13;
   const uint8_t* xs;
   const int4* tiles;
@@ -66,24 +60,63 @@ struct StreamFc1Params {
   float limit, alpha, beta;
 };
 
-// First K-flat index of CTA c's range.
-__device__ __forceinline__ long long range_begin(int c, int G, long long W) {
-  return (long long)c * W / G;
-}
-// CTA whose range contains flat index x (0 <= x < W); ranges may be empty when G > W, and the
-// one returned is the CTA whose non-empty range holds x.
-__device__ __forceinline__ int cta_of(long long x, int G, long long W) {
-  int c = (int)((x * G) / W);
-  while (c + 1 < G && range_begin(c + 1, G, W) <= x) ++c;
-  while (c > 0 && range_begin(c, G, W) > x) --c;
-  return c;
-}
-// Partial slot of CTA c's segment of unit u: 2c for the segment its range starts in, 2c + 1 for
-// the one it ends in (at most these two segments of a range can be partial).
-__device__ __forceinline__ int part_slot(int c, int u, int G, long long W, int KT) {
-  const int first_unit = (int)(range_begin(c, G, W) / KT);
-  return 2 * c + (u == first_unit ? 0 : 1);
-}
+// Work of one CTA (G CTAs, U units of KT K steps).  With D = floor(U / G) full waves, the units
+// D*G .. U-1 ("stream units") are split over all CTAs by K steps: CTA c gets the flat range
+// [c*W/G, (c+1)*W/G) of their W = (U - D*G) * KT steps.  CTA c first streams that range, then
+// its whole units c, c + G, ..., c + (D-1)*G, so the pieces' hand-over to the reducing CTA
+// overlaps the whole units' streaming.  The CTA's steps are numbered q = 0 .. nsteps-1.
+struct StreamWork {
+  int KT, G, c, D, first_stream_unit;   // first_stream_unit = D * G
+  long long W, x0, x1;                  // stream steps of all CTAs; this CTA's range
+  int n_sk, nsteps;                     // this CTA's stream steps; all its steps
+
+  __device__ __forceinline__ void init(int units, int kt, int g, int cta) {
+    KT = kt; G = g; c = cta;
+    D = units / g;
+    first_stream_unit = D * g;
+    W = (long long)(units - first_stream_unit) * kt;
+    x0 = begin_of(cta);
+    x1 = begin_of(cta + 1);
+    n_sk = (int)(x1 - x0);
+    nsteps = n_sk + D * kt;
+  }
+  __device__ __forceinline__ long long begin_of(int cta) const { return (long long)cta * W / G; }
+  // unit and K tile of step q
+  __device__ __forceinline__ void step(int q, int& u, int& kt) const {
+    if (q < n_sk) {
+      const long long x = x0 + q;
+      u = first_stream_unit + (int)(x / KT);
+      kt = (int)(x % KT);
+    } else {
+      const int r = q - n_sk;
+      u = c + (r / KT) * G;
+      kt = r % KT;
+    }
+  }
+  // does step q start / end a segment (a run of one unit's K tiles)?
+  __device__ __forceinline__ bool seg_start(int q) const {
+    if (q == 0 || q == n_sk) return true;
+    int u, kt;
+    step(q, u, kt);
+    return kt == 0;
+  }
+  __device__ __forceinline__ bool seg_end(int q) const {
+    return q + 1 == nsteps || seg_start(q + 1);
+  }
+  // stream steps: CTA holding flat stream step x (ranges may be empty when G > W)
+  __device__ __forceinline__ int cta_of(long long x) const {
+    int cc = (int)((x * G) / W);
+    while (cc + 1 < G && begin_of(cc + 1) <= x) ++cc;
+    while (cc > 0 && begin_of(cc) > x) --cc;
+    return cc;
+  }
+  // partial slot of CTA cc's piece of stream unit u: 2cc for the unit its range starts in,
+  // 2cc + 1 for the one it ends in (no other piece of a range can be partial)
+  __device__ __forceinline__ int part_slot(int cc, int u) const {
+    const int first = first_stream_unit + (int)(begin_of(cc) / KT);
+    return 2 * cc + (u == first ? 0 : 1);
+  }
+};
 
 template <int BN>
 __global__ void __launch_bounds__(kStreamThreads)
@@ -92,11 +125,9 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   constexpr int S = Cfg::kStages;
   pdl_wait_prev();     // previous kernel of the call complete, its writes visible
   pdl_launch_next();
-  const int G = gridDim.x, c = blockIdx.x;
-  const int units = p.ctrl[1] * p.RT;
-  const long long W = (long long)units * p.KT;
-  const long long x_begin = range_begin(c, G, W), x_end = range_begin(c + 1, G, W);
-  if (x_begin >= x_end) return;
+  StreamWork wk;
+  wk.init(p.ctrl[1] * p.RT, p.KT, gridDim.x, blockIdx.x);
+  if (wk.nsteps <= 0) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   extern __shared__ uint8_t smem_raw[];
@@ -135,80 +166,53 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
 
   if (warp == 0) {
     if (lane == 0) {
-      // L2 prefetch of the weight tiles and scale atoms of flat index y; the expert of a tile
-      // is looked up once per tile (a dependent global load per stage would pace the producer)
-      int pf_tile = -1, pf_e = 0;
-      auto prefetch = [&](long long y) {
-        const int u = (int)(y / p.KT), kt = (int)(y % p.KT);
+      int i = 0, cur_tile = -1, e = 0, p0 = 0;
+      for (; i < wk.nsteps && ok; ++i) {
+        int u, kt;
+        wk.step(i, u, kt);
         const int tile = u / p.RT, fb = u - tile * p.RT;
-        if (tile != pf_tile) {
-          pf_tile = tile;
-          pf_e = p.tiles[tile].x;
+        if (tile != cur_tile) {
+          cur_tile = tile;
+          const int4 td = p.tiles[tile];
+          e = td.x;
+          p0 = td.y;
         }
-        const int e = pf_e;
+        const int s = i % S;
+        if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
+        if (!ok) break;
+        uint8_t* st = stage(s);
         if (fb < p.RTf) {
-          bulk_prefetch_l2(p.w13 + ((size_t)((2 * e) * p.RTf + fb) * p.KT + kt) * kTxBytesA,
-                           kTxBytesA);
-          bulk_prefetch_l2(p.w13 + ((size_t)((2 * e + 1) * p.RTf + fb) * p.KT + kt) * kTxBytesA,
-                           kTxBytesA);
+          mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512);
+          tma_load_3d(st, &p.tm_w13, 0, 0, ((2 * e) * p.RTf + fb) * p.KT + kt, &full[s]);
+          tma_load_3d(st + kTileBytesA, &p.tm_w13, 0, 0, ((2 * e + 1) * p.RTf + fb) * p.KT + kt,
+                      &full[s]);
         } else {
-          bulk_prefetch_l2(p.w13_tail + ((size_t)(2 * e) * p.KT + kt) * p.rem * 64, p.rem * 64);
-          bulk_prefetch_l2(p.w13_tail + ((size_t)(2 * e + 1) * p.KT + kt) * p.rem * 64,
-                           p.rem * 64);
+          mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + Cfg::kB + 2 * 512);
+          tma_load_3d(st, &p.tm_w13_tail, 0, 0, (2 * e) * p.KT + kt, &full[s]);
+          tma_load_3d(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * e + 1) * p.KT + kt, &full[s]);
         }
-        bulk_prefetch_l2(p.sf13 + (((size_t)(2 * e) * p.RT + fb) * p.KT + kt) * 512, 512);
-        bulk_prefetch_l2(p.sf13 + (((size_t)(2 * e + 1) * p.RT + fb) * p.KT + kt) * 512, 512);
-      };
-      long long xp = x_begin;                       // next flat index to prefetch
-      int i = 0;
-      for (long long x = x_begin; x < x_end && ok;) {
-        const int u = (int)(x / p.KT), k0 = (int)(x % p.KT);
-        const int k1 = (int)std::min<long long>(p.KT, k0 + (x_end - x));
-        const int tile = u / p.RT, fb = u - tile * p.RT;
-        const int4 td = p.tiles[tile];
-        const int e = td.x, p0 = td.y;
-        for (int kt = k0; kt < k1 && ok; ++kt, ++i) {
-          const int s = i % S;
-          for (const long long lim = std::min(x + (kt - k0) + kPrefetchTiles, x_end); xp < lim;
-               ++xp)
-            prefetch(xp);
-          if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
-          if (!ok) break;
-          uint8_t* st = stage(s);
-          if (fb < p.RTf) {
-            mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512);
-            tma_load_3d(st, &p.tm_w13, 0, 0, ((2 * e) * p.RTf + fb) * p.KT + kt, &full[s]);
-            tma_load_3d(st + kTileBytesA, &p.tm_w13, 0, 0,
-                        ((2 * e + 1) * p.RTf + fb) * p.KT + kt, &full[s]);
-          } else {
-            mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + Cfg::kB + 2 * 512);
-            tma_load_3d(st, &p.tm_w13_tail, 0, 0, (2 * e) * p.KT + kt, &full[s]);
-            tma_load_3d(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * e + 1) * p.KT + kt,
-                        &full[s]);
-          }
-          tma_load_2d(st + 2 * kTileBytesA, &p.tm_x, kt * 128, p0, &full[s]);
-          const size_t a_up = ((size_t)(2 * e) * p.RT + fb) * p.KT + kt;
-          const size_t a_gt = ((size_t)(2 * e + 1) * p.RT + fb) * p.KT + kt;
-          bulk_load(st + 2 * kTileBytesA + Cfg::kB, p.sf13 + a_up * 512, 512, &full[s]);
-          bulk_load(st + 2 * kTileBytesA + Cfg::kB + 512, p.sf13 + a_gt * 512, 512, &full[s]);
-        }
-        x += k1 - k0;
+        tma_load_2d(st + 2 * kTileBytesA, &p.tm_x, kt * 128, p0, &full[s]);
+        const size_t a_up = ((size_t)(2 * e) * p.RT + fb) * p.KT + kt;
+        const size_t a_gt = ((size_t)(2 * e + 1) * p.RT + fb) * p.KT + kt;
+        bulk_load(st + 2 * kTileBytesA + Cfg::kB, p.sf13 + a_up * 512, 512, &full[s]);
+        bulk_load(st + 2 * kTileBytesA + Cfg::kB + 512, p.sf13 + a_gt * 512, 512, &full[s]);
       }
       issued = i;
     }
   } else if (warp == 2) {
-    // Activation scale atoms.  The scales of kSfSteps consecutive flat K steps are staged per
-    // chunk with one batch of cp.async, double-buffered: the next chunk is in flight while the
-    // current one's atoms are written, so neither a new unit nor a new chunk stalls the ring.
+    // Activation scale atoms.  The scales of kSfSteps consecutive steps are staged per chunk
+    // with one batch of cp.async, double-buffered: the next chunk is in flight while the current
+    // one's atoms are written, so neither a new unit nor a new chunk stalls the ring.
     uint32_t* sfbuf = reinterpret_cast<uint32_t*>(smem + S * Cfg::kStage);   // [2][steps][BN]
     int cached_tile = -1, cached_p0 = 0;
-    auto stage_chunk = [&](long long c) {
+    auto stage_chunk = [&](int c) {
       uint32_t* dst = sfbuf + (c & 1) * kSfSteps * BN;
       for (int idx = lane; idx < kSfSteps * BN; idx += 32) {
         const int j = idx / BN, n = idx - j * BN;
-        const long long y = x_begin + c * kSfSteps + j;
-        if (y >= x_end) continue;
-        const int u = (int)(y / p.KT), kt = (int)(y % p.KT);
+        const int q = c * kSfSteps + j;
+        if (q >= wk.nsteps) continue;
+        int u, kt;
+        wk.step(q, u, kt);
         const int tile = u / p.RT;
         if (tile != cached_tile) {
           cached_tile = tile;
@@ -221,13 +225,11 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
       }
       cp_async_commit();
     };
-    const long long nflat = x_end - x_begin;
-    const long long nchunks = (nflat + kSfSteps - 1) / kSfSteps;
+    const int nchunks = (wk.nsteps + kSfSteps - 1) / kSfSteps;
     stage_chunk(0);
-    for (long long y = 0; y < nflat && ok; ++y) {
-      const int s = (int)(y % S);
-      const long long c = y / kSfSteps;
-      const int j = (int)(y % kSfSteps);
+    for (int q = 0; q < wk.nsteps && ok; ++q) {
+      const int s = q % S;
+      const int c = q / kSfSteps, j = q % kSfSteps;
       if (j == 0) {
         if (c + 1 < nchunks) {
           stage_chunk(c + 1);
@@ -237,7 +239,7 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
         }
         __syncwarp();
       }
-      if (y >= S) ok = mbar_wait(&empty[s], ((y / S) - 1) & 1, p.err);
+      if (q >= S) ok = mbar_wait(&empty[s], ((q / S) - 1) & 1, p.err);
       if (!ok) break;
       write_act_sf_rows<BN>(stage(s) + 2 * kTileBytesA + Cfg::kB + 1024,
                             sfbuf + (c & 1) * kSfSteps * BN + j * BN, lane);
@@ -248,47 +250,51 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
     cp_async_wait_group<0>();
   } else if (warp == 1) {
     if (lane == 0) {
-      int i = 0, j = 0;
-      for (long long x = x_begin; x < x_end && ok; ++j) {
-        const int k0 = (int)(x % p.KT);
-        const int k1 = (int)std::min<long long>(p.KT, k0 + (x_end - x));
-        const int b = j & 1;
-        if (j >= 2) ok = mbar_wait(&acc_empty[b], ((j >> 1) - 1) & 1, p.err);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t d_up = tmem + b * Cfg::kAcc, d_gt = d_up + BN;
-        for (int kt = k0; kt < k1 && ok; ++kt, ++i) {
-          const int s = i % S;
-          ok = mbar_wait(&full[s], (i / S) & 1, p.err);
+      int j = -1, b = 0;
+      uint32_t d_up = 0, d_gt = 0;
+      for (int i = 0; i < wk.nsteps && ok; ++i) {
+        const bool first = wk.seg_start(i);
+        if (first) {
+          ++j;
+          b = j & 1;
+          if (j >= 2) ok = mbar_wait(&acc_empty[b], ((j >> 1) - 1) & 1, p.err);
           if (!ok) break;
           tc_fence_after();
-          uint8_t* st = stage(s);
-          const uint32_t sf = tmem + 2 * Cfg::kAcc + 12 * s;
-          tc_cp_sf(sf + 0, desc_sf(st + 2 * kTileBytesA + Cfg::kB));
-          tc_cp_sf(sf + 4, desc_sf(st + 2 * kTileBytesA + Cfg::kB + 512));
-          tc_cp_sf(sf + 8, desc_sf(st + 2 * kTileBytesA + Cfg::kB + 1024));
-#pragma unroll
-          for (int kb = 0; kb < 4; ++kb) {
-            const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, BN, kb);
-            const uint64_t bdesc = desc_sw128(st + 2 * kTileBytesA + 32 * kb);
-            const uint32_t acc = (kt > k0 || kb > 0) ? 1u : 0u;
-            mma_mxf8f6f4(d_up, desc_sw128(st + 32 * kb), bdesc, idesc, sf + 0, sf + 8, acc);
-            mma_mxf8f6f4(d_gt, desc_sw128(st + kTileBytesA + 32 * kb), bdesc, idesc, sf + 4,
-                         sf + 8, acc);
-          }
-          tc_commit(&empty[s]);
+          d_up = tmem + b * Cfg::kAcc;
+          d_gt = d_up + BN;
         }
-        tc_commit(&acc_full[b]);
-        x += k1 - k0;
+        const int s = i % S;
+        ok = mbar_wait(&full[s], (i / S) & 1, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        uint8_t* st = stage(s);
+        const uint32_t sf = tmem + 2 * Cfg::kAcc + 12 * s;
+        tc_cp_sf(sf + 0, desc_sf(st + 2 * kTileBytesA + Cfg::kB));
+        tc_cp_sf(sf + 4, desc_sf(st + 2 * kTileBytesA + Cfg::kB + 512));
+        tc_cp_sf(sf + 8, desc_sf(st + 2 * kTileBytesA + Cfg::kB + 1024));
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) {
+          const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, BN, kb);
+          const uint64_t bdesc = desc_sw128(st + 2 * kTileBytesA + 32 * kb);
+          const uint32_t acc = (!first || kb > 0) ? 1u : 0u;
+          mma_mxf8f6f4(d_up, desc_sw128(st + 32 * kb), bdesc, idesc, sf + 0, sf + 8, acc);
+          mma_mxf8f6f4(d_gt, desc_sw128(st + kTileBytesA + 32 * kb), bdesc, idesc, sf + 4,
+                       sf + 8, acc);
+        }
+        tc_commit(&empty[s]);
+        if (wk.seg_end(i)) tc_commit(&acc_full[b]);
       }
     }
   } else if (warp >= 4) {
     const int quad = warp & 3;
     const int row = quad * 32 + lane;                         // weight row within the block
     int j = 0;
-    for (long long x = x_begin; x < x_end; ++j) {
-      const int u = (int)(x / p.KT), k0 = (int)(x % p.KT);
-      const int k1 = (int)std::min<long long>(p.KT, k0 + (x_end - x));
+    for (int q = 0; q < wk.nsteps; ++j) {
+      int u, k0;
+      wk.step(q, u, k0);
+      int len = 1;
+      while (q + len < wk.nsteps && !wk.seg_start(q + len)) ++len;
+      const int k1 = k0 + len;
       const int tile = u / p.RT, fb = u - tile * p.RT;
       const int4 td = p.tiles[tile];
       const int p0 = td.y, n = td.z;
@@ -299,7 +305,8 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
       __syncwarp();
       const uint32_t trow = tmem + b * Cfg::kAcc + ((uint32_t)(quad * 32) << 16);
       const bool whole = k0 == 0 && k1 == p.KT;
-      float* part = p.part + (size_t)part_slot(c, u, G, W, p.KT) * Cfg::kPartFloats;
+      float* part = whole ? nullptr
+                          : p.part + (size_t)wk.part_slot(wk.c, u) * Cfg::kPartFloats;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float up[16], gt[16];
@@ -316,10 +323,13 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
             }
           }
         } else {
+          // only the tile's n token columns are kept
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
-            part[(c0 + jj) * 128 + row] = up[jj];
-            part[(BN + c0 + jj) * 128 + row] = gt[jj];
+            if (c0 + jj < n) {
+              part[(c0 + jj) * 128 + row] = up[jj];
+              part[(BN + c0 + jj) * 128 + row] = gt[jj];
+            }
           }
         }
       }
@@ -330,26 +340,23 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
         __threadfence();
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (warp == 4 && lane == 0) {
-          const int t = atomicAdd(&p.tickets[u], k1 - k0);
-          s_last = (t + (k1 - k0) == p.KT);
+          const int t = atomicAdd(&p.tickets[u], len);
+          s_last = (t + len == p.KT);
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (s_last && ok) {
           __threadfence();
-          // the unit's pieces in K order: CTAs cta_of(u*KT) .. cta_of(u*KT + KT - 1)
-          const int c_first = cta_of((long long)u * p.KT, G, W);
-          const int c_last = cta_of((long long)u * p.KT + p.KT - 1, G, W);
-          // pieces of the CTAs c_first.. in K order; CTAs with empty ranges (grids larger
-          // than the K-tile count) hold none
+          // the unit's pieces in K order: CTAs holding its first .. last stream step; CTAs
+          // with empty ranges (grids larger than the step count) hold none
+          const long long xf = (long long)(u - wk.first_stream_unit) * p.KT;
+          const int c_first = wk.cta_of(xf), c_last = wk.cta_of(xf + p.KT - 1);
           reduce_pieces(
               c_last - c_first + 1, n, (size_t)BN * 128,
-              [&](int q, int cc) {
-                return p.part + (size_t)part_slot(c_first + q, u, G, W, p.KT) * Cfg::kPartFloats +
+              [&](int qq, int cc) {
+                return p.part + (size_t)wk.part_slot(c_first + qq, u) * Cfg::kPartFloats +
                        cc * 128 + row;
               },
-              [&](int q) {
-                return range_begin(c_first + q + 1, G, W) == range_begin(c_first + q, G, W);
-              },
+              [&](int qq) { return wk.begin_of(c_first + qq + 1) == wk.begin_of(c_first + qq); },
               [&](int cc, float up, float gt) {
                 const float h = f < p.I ? swiglu(gt, up, p.limit, p.alpha, p.beta) : 0.f;
                 const size_t r = (size_t)(p0 + cc);
@@ -357,7 +364,7 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
               });
         }
       }
-      x += k1 - k0;
+      q += len;
     }
   }
   if (!ok) s_fail = 1;
@@ -431,10 +438,9 @@ cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanD
   p.rem = d.I % 128;
   const long long kt = d.H / 128;
   const int Sm = M * d.topk;
-  p.w13 = w.w13;
-  p.w13_tail = w.w13 + (size_t)2 * d.E * p.RTf * kt * 8192;
-  if (!tmap_fp4(&p.tm_w13, p.w13, 128, 2LL * d.E * p.RTf * kt) ||
-      !tmap_fp4(&p.tm_w13_tail, p.w13_tail, p.rem, 2LL * d.E * kt) ||
+  if (!tmap_fp4(&p.tm_w13, w.w13, 128, 2LL * d.E * p.RTf * kt) ||
+      !tmap_fp4(&p.tm_w13_tail, w.w13 + (size_t)2 * d.E * p.RTf * kt * 8192, p.rem,
+                2LL * d.E * kt) ||
       !tmap_u8(&p.tm_x, r.xq, d.H, Sm, bn))
     return cudaErrorInvalidValue;
   p.sf13 = w.s13; p.xs = r.xs; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;

@@ -111,11 +111,6 @@ TC_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
       ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
-// L2 prefetch hint for `bytes` at src (16-byte aligned, size a multiple of 16): no completion,
-// no shared memory; a later load of the same bytes finds them in L2.
-TC_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 TC_DEV void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
 }
