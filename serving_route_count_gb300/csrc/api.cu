@@ -90,6 +90,8 @@ moe_status cuda_status(cudaError_t e) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+constexpr int kFc1CtasPerSm = 2;
+
 // Tiles of a call of M tokens at tile width bn: at most one per slot, and at most
 // ceil(S / bn) + (touched experts).
 int call_tiles(const PlanDims& d, int max_tiles, int M, int bn) {
@@ -98,9 +100,28 @@ int call_tiles(const PlanDims& d, int max_tiles, int M, int bn) {
 }
 
 // K splits of the tensor-core fc1 so that small calls still put one CTA on most SMs.
+// SMs of the current device (152 when there is none, e.g. when plans are sized on a host
+// without a GPU), looked up once.
+int device_sms() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      sms = n;
+    else
+      sms = 152;
+    (void)cudaGetLastError();
+  }
+  return sms;
+}
+
+// K splits of the unit-per-CTA fc1 so that small calls still fill the CTA slots (two CTAs of
+// the decode tile width fit an SM), with at least 4 K tiles per split.
 int fc1_splits(const PlanDims& d, int tiles) {
   const int units = tiles * cdiv(d.I, 128);
-  return std::max(1, std::min(std::min(152 / std::max(units, 1), d.H / 128 / 4), 16));
+  const int slots = kFc1CtasPerSm * device_sms();
+  return std::max(1, std::min(std::min(slots / std::max(units, 1), d.H / 128 / 4), 16));
 }
 
 moe_status check_geometry(int E, int H, int I, int quant) {
