@@ -14,13 +14,14 @@ namespace moe {
 cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int max_tiles,
                          const RunPtrs& r, cudaStream_t st);
 cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
-                        bool to_f16, void* z0, size_t z0_words, void* z1, size_t z1_words,
-                        void* z2, size_t z2_words, cudaStream_t st);
+                        bool atoms, bool to_f16, void* z0, size_t z0_words, void* z1,
+                        size_t z1_words, void* z2, size_t z2_words, cudaStream_t st);
 bool route_actq_small_supported(int Mk, int E);
 cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int tile_slots,
                                     int max_tiles, const void* x, int H, int topk,
-                                    const RunPtrs& r, void* z0, size_t z0_words, void* z1,
-                                    size_t z1_words, void* z2, size_t z2_words, cudaStream_t st);
+                                    const RunPtrs& r, bool atoms, void* z0, size_t z0_words,
+                                    void* z1, size_t z1_words, void* z2, size_t z2_words,
+                                    cudaStream_t st);
 // gemm_tc.cu
 cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                             int bn, int tiles, int splits, const float* topk_w, int M,
@@ -309,6 +310,10 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   s.tiles = take((size_t)s.max_tiles * 16);
   s.xq = a8 ? take(Sm * H) : 0;
   s.xs = a8 ? take(Sm * H / 32) : 0;
+  // scale atoms of the 16/32-token tiles (calls of up to 64 tokens)
+  s.r16 = (int)std::min<size_t>(Sm, (size_t)64 * topk) + 32;
+  s.xs16 = a8 ? take((size_t)(H / 128) * s.r16 * 16) : 0;
+  s.hs16 = a8 ? take((size_t)(d.Ip / 128) * s.r16 * 16) : 0;
   // fc1 output of the CUDA-core path, or the per-split partial sums of the tensor-core path
   // ([split][slot][2][Ip], one slice per split, summed in split order)
   size_t g_rows = Sm;
@@ -368,6 +373,9 @@ static RunPtrs resolve(const moe_plan_t* plan, void* scratch) {
   r.tiles = reinterpret_cast<int4*>(b + s.tiles);
   r.xq = a8 ? b + s.xq : nullptr;
   r.xs = a8 ? b + s.xs : nullptr;
+  r.xs16 = a8 ? b + s.xs16 : nullptr;
+  r.hs16 = a8 ? b + s.hs16 : nullptr;
+  r.r16 = s.r16;
   r.g = reinterpret_cast<float*>(b + s.g);
   r.tickets = reinterpret_cast<int32_t*>(b + s.tickets);
   r.part = a8 ? reinterpret_cast<float*>(b + s.part) : nullptr;
@@ -481,6 +489,8 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   const int splits = (tc && !streamk) ? fc1_splits(d, tiles) : 1;
   // small W4A8 calls route and quantise in one launch
   const bool small = tc8 && route_actq_small_supported(Sm, d.E);
+  // 16/32-token tiles read their activation-scale atoms from prepared rows
+  const bool atoms = tc8 && bn <= 32;
   void* acc = d.deterministic ? nullptr : r.acc;
   const size_t acc_words = d.deterministic ? 0 : (size_t)M * d.H;
   void* g = nullptr;            // split partials are fully written before they are read
@@ -490,8 +500,8 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   prof(0);
   cudaError_t e;
   if (small) {
-    e = launch_route_actq_small(topk_ids, Sm, d.E, bn, plan->s.max_tiles, x, d.H, d.topk, r, acc,
-                                acc_words, g, g_words, tk, tk_words, st);
+    e = launch_route_actq_small(topk_ids, Sm, d.E, bn, plan->s.max_tiles, x, d.H, d.topk, r,
+                                atoms, acc, acc_words, g, g_words, tk, tk_words, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
   } else {
@@ -499,8 +509,8 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
     if (a8 || acc || g || t16) {
-      e = launch_actq(x, M, d.H, d.topk, r, a8, t16, acc, acc_words, g, g_words, tk, tk_words,
-                      st);
+      e = launch_actq(x, M, d.H, d.topk, r, a8, atoms, t16, acc, acc_words, g, g_words, tk,
+                      tk_words, st);
       if (e != cudaSuccess) return cuda_status(e);
     }
   }

@@ -47,7 +47,10 @@ struct TcCfg {
   static constexpr int pow2(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
   static constexpr int kAlloc1 = pow2(kCols1);
   static constexpr int kAlloc2 = pow2(kCols2);
-  static constexpr int kSfStage = BN * kSfChunk * 4;            // staged activation scales
+  // activation-scale atoms: one bulk copy of the prepared atom rows per stage for BN <= 32,
+  // else built by warp 2 from scales it stages in shared memory
+  static constexpr bool kSfbCopy = BN <= 32;
+  static constexpr int kSfStage = kSfbCopy ? 0 : BN * kSfChunk * 4;
   static constexpr int kSmem1 = kStages1 * kStage1 + kSfStage + 1024;
   static constexpr int kSmem2 = kStages2 * kStage2 + kSfStage + 1024;
 };
@@ -58,6 +61,9 @@ struct TcFc1Params {
   CUtensorMap tm_x;          // E4M3 [Sm][H], box 128 x BN
   const uint8_t* sf13;       // weight scale atoms [E][2][RT][KT][512]
   const uint8_t* xs;         // activation scales [Sm][H/32]
+  const uint8_t* xs16;       // the same in the atom layout [H/128][r16][16] (BN <= 32)
+  uint8_t* hs16;             // h scales in the atom layout [Ip/128][r16][16] (BN <= 32)
+  int r16;
   const int4* tiles;
   const int32_t* ctrl;
   int32_t* err;
@@ -75,6 +81,8 @@ struct TcFc2Params {
   CUtensorMap tm_h;          // E4M3 [Sm][Ip], box 128 x BN
   const uint8_t* sf2;        // weight scale atoms [E][H/128][Ip/128][512]
   const uint8_t* hs;         // [Sm][Ip/32]
+  const uint8_t* hs16;       // the same in the atom layout [Ip/128][r16][16] (BN <= 32)
+  int r16;
   const int4* tiles;
   const int32_t* ctrl;
   int32_t* err;
@@ -114,7 +122,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   }
   if (tid == 32) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 2);
+      mbar_init(&full[s], Cfg::kSfbCopy ? 1 : 2);
       mbar_init(&empty[s], 1);
     }
     mbar_init(&done, 1);
@@ -142,14 +150,16 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
         uint8_t* st = stage(s);
         const int kt = kt0 + i;
         if (fb < p.RTf) {
-          mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512);
+          mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512 +
+                                              (Cfg::kSfbCopy ? BN * 16 : 0));
           tma_load_3d(st, &p.tm_w13, 0, 0, ((2 * e) * p.RTf + fb) * p.KT + kt, &full[s]);
           tma_load_3d(st + kTileBytesA, &p.tm_w13, 0, 0, ((2 * e + 1) * p.RTf + fb) * p.KT + kt,
                       &full[s]);
         } else {
           // partial row tile: rows >= I % 128 of the smem tile keep stale (finite) codes; their
           // accumulator rows are never read
-          mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + Cfg::kB + 2 * 512);
+          mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + Cfg::kB + 2 * 512 +
+                                              (Cfg::kSfbCopy ? BN * 16 : 0));
           tma_load_3d(st, &p.tm_w13_tail, 0, 0, (2 * e) * p.KT + kt, &full[s]);
           tma_load_3d(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * e + 1) * p.KT + kt, &full[s]);
         }
@@ -158,10 +168,13 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
         const size_t a_gt = ((size_t)(2 * e + 1) * p.RT + fb) * p.KT + kt;
         bulk_load(st + 2 * kTileBytesA + Cfg::kB, p.sf13 + a_up * 512, 512, &full[s]);
         bulk_load(st + 2 * kTileBytesA + Cfg::kB + 512, p.sf13 + a_gt * 512, 512, &full[s]);
+        if (Cfg::kSfbCopy)
+          bulk_load(st + 2 * kTileBytesA + Cfg::kB + 1024,
+                    p.xs16 + ((size_t)kt * p.r16 + p0) * 16, BN * 16, &full[s]);
       }
       issued = i;
     }
-  } else if (warp == 2) {
+  } else if (warp == 2 && !Cfg::kSfbCopy) {
     uint32_t* sfst = reinterpret_cast<uint32_t*>(smem + S * Cfg::kStage1);
     for (int i = 0; i < nk && ok; ++i) {
       const int s = i % S;
@@ -223,7 +236,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
           if (c0 + j < n) {
             const float h = f < p.I ? swiglu(gt[j], up[j], p.limit, p.alpha, p.beta) : 0.f;
             const size_t row = (size_t)(p0 + c0 + j);
-            requant_store(h, lane, row * p.Ip, row * (p.Ip / 32), f, p.hq, p.hs);
+            requant_store(h, lane, row, p.Ip, f, p.hq, p.hs, p.hs16, p.r16);
           }
         }
       }
@@ -269,7 +282,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
           [&](int c, float up, float gt) {
             const float h = f < p.I ? swiglu(gt, up, p.limit, p.alpha, p.beta) : 0.f;
             const size_t row = (size_t)(p0 + c);
-            requant_store(h, lane, row * p.Ip, row * (p.Ip / 32), f, p.hq, p.hs);
+            requant_store(h, lane, row, p.Ip, f, p.hq, p.hs, p.hs16, p.r16);
           });
     }
   }
@@ -305,7 +318,7 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
   }
   if (tid == 32) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 2);
+      mbar_init(&full[s], Cfg::kSfbCopy ? 1 : 2);
       mbar_init(&empty[s], 1);
     }
     mbar_init(&done, 1);
@@ -331,15 +344,19 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
         if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
         if (!ok) break;
         uint8_t* st = stage(s);
-        mbar_arrive_expect_tx(&full[s], kTxBytesA + Cfg::kB + 512);
+        mbar_arrive_expect_tx(&full[s], kTxBytesA + Cfg::kB + 512 +
+                                            (Cfg::kSfbCopy ? BN * 16 : 0));
         tma_load_3d(st, &p.tm_w2, 0, 0, ((size_t)e * (p.H / 128) + rt) * p.KT + i, &full[s]);
         tma_load_2d(st + kTileBytesA, &p.tm_h, i * 128, p0, &full[s]);
         const size_t a = ((size_t)e * (p.H / 128) + rt) * p.KT + i;
         bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
+        if (Cfg::kSfbCopy)
+          bulk_load(st + kTileBytesA + Cfg::kB + 512, p.hs16 + ((size_t)i * p.r16 + p0) * 16,
+                    BN * 16, &full[s]);
       }
       issued = i;
     }
-  } else if (warp == 2) {
+  } else if (warp == 2 && !Cfg::kSfbCopy) {
     uint32_t* sfst = reinterpret_cast<uint32_t*>(smem + S * Cfg::kStage2);
     for (int i = 0; i < nk && ok; ++i) {
       const int s = i % S;
@@ -375,7 +392,7 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
       }
       tc_commit(&done);
     }
-  } else {
+  } else if (warp == 3) {
     // warp 3: the combine's slot indices and router weights, loaded while the GEMM runs
     for (int c = lane; c < n; c += 32) {
       const int f = p.perm[p0 + c];
@@ -512,6 +529,7 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
     if (!tmap_u8(&p.tm_x, r.xq, d.H, Sm, bn)) return cudaErrorInvalidValue;
     p.sf13 = w.s13; p.xs = r.xs; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
     p.hq = r.hq; p.hs = r.hs; p.gacc = r.g; p.tickets = r.tickets;
+    p.xs16 = r.xs16; p.hs16 = bn <= 32 ? r.hs16 : nullptr; p.r16 = r.r16;
     p.H = d.H; p.I = d.I; p.Ip = d.Ip; p.RT = RT; p.KT = d.H / 128; p.Sm = Sm;
     p.splits = splits; p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
     switch (bn) {
@@ -526,6 +544,7 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
     return cudaErrorInvalidValue;
   if (!tmap_u8(&p.tm_h, r.hq, d.Ip, Sm, bn)) return cudaErrorInvalidValue;
   p.sf2 = w.s2; p.hs = r.hs; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
+  p.hs16 = r.hs16; p.r16 = r.r16;
   p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;
   p.H = d.H; p.Ip = d.Ip; p.KT = d.Ip / 128; p.Sm = Sm; p.topk = d.topk;
   p.deterministic = d.deterministic;

@@ -14,8 +14,8 @@
 //     requantisation.
 // Block-scaled MMA, layouts and operand staging are those of fc1_tc_kernel (gemm_tc.cu).
 //
-// Warps (256 threads): 0 TMA producer (lane 0), 1 MMA issuer (lane 0),
-// 2 activation-scale atoms, 3 idle, 4..7 epilogue (TMEM lane quadrant = warp % 4).
+// Warps (256 threads): 0 TMA producer (lane 0), 1 MMA issuer (lane 0), 2..3 idle,
+// 4..7 epilogue (TMEM lane quadrant = warp % 4).
 #include <algorithm>
 #include <cstring>
 
@@ -28,14 +28,13 @@ namespace moe {
 using namespace tc;
 
 constexpr int kStreamThreads = 256;
-constexpr int kSfSteps = 16;          // flat K steps of activation scales staged per chunk
 
 template <int BN>
 struct StreamCfg {
   static constexpr int kB = BN * 128;
   static constexpr int kStage = (2 * kTileBytesA + kB + 3 * 512 + 1023) / 1024 * 1024;
   static constexpr int kStages = 3;                      // two CTAs per SM
-  static constexpr int kSfStage = 2 * kSfSteps * BN * 4;  // double-buffered scale chunks
+  static constexpr int kSfStage = 0;                     // scale atoms arrive by bulk copy
   static constexpr int kSmem = kStages * kStage + kSfStage + 1024;
   static constexpr int kAcc = 2 * BN;                    // one accumulator buffer: up | gate
   static constexpr int kCols = 2 * kAcc + 12 * kStages;
@@ -48,12 +47,14 @@ struct StreamFc1Params {
   CUtensorMap tm_w13_tail;   // partial last row tile
   CUtensorMap tm_x;          // E4M3 activations [Sm][H], boxes 128 x BN
   const uint8_t* sf13;
-  const uint8_t* xs;
+  const uint8_t* xs16;       // activation-scale atom rows [H/128][r16][16]
   const int4* tiles;
   const int32_t* ctrl;
   int32_t* err;
   uint8_t* hq;
   uint8_t* hs;
+  uint8_t* hs16;             // h scales in the atom layout [Ip/128][r16][16]
+  int r16;
   float* part;               // [2 * G][2][BN][128] partial accumulators
   int32_t* tickets;          // [units] K tiles completed
   int H, I, Ip, RT, KT, Sm, RTf, rem;
@@ -143,7 +144,7 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   }
   if (tid == 32) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 2);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -182,12 +183,12 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
         if (!ok) break;
         uint8_t* st = stage(s);
         if (fb < p.RTf) {
-          mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512);
+          mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512 + BN * 16);
           tma_load_3d(st, &p.tm_w13, 0, 0, ((2 * e) * p.RTf + fb) * p.KT + kt, &full[s]);
           tma_load_3d(st + kTileBytesA, &p.tm_w13, 0, 0, ((2 * e + 1) * p.RTf + fb) * p.KT + kt,
                       &full[s]);
         } else {
-          mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + Cfg::kB + 2 * 512);
+          mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + Cfg::kB + 2 * 512 + BN * 16);
           tma_load_3d(st, &p.tm_w13_tail, 0, 0, (2 * e) * p.KT + kt, &full[s]);
           tma_load_3d(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * e + 1) * p.KT + kt, &full[s]);
         }
@@ -196,58 +197,12 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
         const size_t a_gt = ((size_t)(2 * e + 1) * p.RT + fb) * p.KT + kt;
         bulk_load(st + 2 * kTileBytesA + Cfg::kB, p.sf13 + a_up * 512, 512, &full[s]);
         bulk_load(st + 2 * kTileBytesA + Cfg::kB + 512, p.sf13 + a_gt * 512, 512, &full[s]);
+        // activation-scale atom: the tile's prepared atom rows, one bulk copy
+        bulk_load(st + 2 * kTileBytesA + Cfg::kB + 1024, p.xs16 + ((size_t)kt * p.r16 + p0) * 16,
+                  BN * 16, &full[s]);
       }
       issued = i;
     }
-  } else if (warp == 2) {
-    // Activation scale atoms.  The scales of kSfSteps consecutive steps are staged per chunk
-    // with one batch of cp.async, double-buffered: the next chunk is in flight while the current
-    // one's atoms are written, so neither a new unit nor a new chunk stalls the ring.
-    uint32_t* sfbuf = reinterpret_cast<uint32_t*>(smem + S * Cfg::kStage);   // [2][steps][BN]
-    int cached_tile = -1, cached_p0 = 0;
-    auto stage_chunk = [&](int c) {
-      uint32_t* dst = sfbuf + (c & 1) * kSfSteps * BN;
-      for (int idx = lane; idx < kSfSteps * BN; idx += 32) {
-        const int j = idx / BN, n = idx - j * BN;
-        const int q = c * kSfSteps + j;
-        if (q >= wk.nsteps) continue;
-        int u, kt;
-        wk.step(q, u, kt);
-        const int tile = u / p.RT;
-        if (tile != cached_tile) {
-          cached_tile = tile;
-          cached_p0 = p.tiles[tile].y;
-        }
-        if (cached_p0 + n < p.Sm)
-          cp_async4(dst + idx, p.xs + (size_t)(cached_p0 + n) * (p.H / 32) + kt * 4);
-        else
-          dst[idx] = 0;
-      }
-      cp_async_commit();
-    };
-    const int nchunks = (wk.nsteps + kSfSteps - 1) / kSfSteps;
-    stage_chunk(0);
-    for (int q = 0; q < wk.nsteps && ok; ++q) {
-      const int s = q % S;
-      const int c = q / kSfSteps, j = q % kSfSteps;
-      if (j == 0) {
-        if (c + 1 < nchunks) {
-          stage_chunk(c + 1);
-          cp_async_wait_group<1>();     // chunk c landed, chunk c + 1 may still fly
-        } else {
-          cp_async_wait_group<0>();
-        }
-        __syncwarp();
-      }
-      if (q >= S) ok = mbar_wait(&empty[s], ((q / S) - 1) & 1, p.err);
-      if (!ok) break;
-      write_act_sf_rows<BN>(stage(s) + 2 * kTileBytesA + Cfg::kB + 1024,
-                            sfbuf + (c & 1) * kSfSteps * BN + j * BN, lane);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full[s]);
-    }
-    cp_async_wait_group<0>();
   } else if (warp == 1) {
     if (lane == 0) {
       int j = -1, b = 0;
@@ -319,7 +274,7 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
             if (c0 + jj < n) {
               const float h = f < p.I ? swiglu(gt[jj], up[jj], p.limit, p.alpha, p.beta) : 0.f;
               const size_t r = (size_t)(p0 + c0 + jj);
-              requant_store(h, lane, r * p.Ip, r * (p.Ip / 32), f, p.hq, p.hs);
+              requant_store(h, lane, r, p.Ip, f, p.hq, p.hs, p.hs16, p.r16);
             }
           }
         } else {
@@ -360,7 +315,7 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
               [&](int cc, float up, float gt) {
                 const float h = f < p.I ? swiglu(gt, up, p.limit, p.alpha, p.beta) : 0.f;
                 const size_t r = (size_t)(p0 + cc);
-                requant_store(h, lane, r * p.Ip, r * (p.Ip / 32), f, p.hq, p.hs);
+                requant_store(h, lane, r, p.Ip, f, p.hq, p.hs, p.hs16, p.r16);
               });
         }
       }
@@ -443,7 +398,8 @@ cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanD
                 2LL * d.E * kt) ||
       !tmap_u8(&p.tm_x, r.xq, d.H, Sm, bn))
     return cudaErrorInvalidValue;
-  p.sf13 = w.s13; p.xs = r.xs; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
+  p.sf13 = w.s13; p.xs16 = r.xs16; p.hs16 = r.hs16; p.r16 = r.r16;
+  p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
   p.hq = r.hq; p.hs = r.hs; p.part = part; p.tickets = tickets;
   p.H = d.H; p.I = d.I; p.Ip = d.Ip; p.RT = cdiv(d.I, 128); p.KT = d.H / 128; p.Sm = Sm;
   p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;

@@ -99,6 +99,11 @@ struct Scratch {
   size_t slot_of;   // int32[Sm]
   size_t tiles;     // int4[max_tiles] {expert, first position, count, 0}
   size_t xq, xs;    // W4A8: u8 [Sm][H], u8 [Sm][H/32], one row per slot position
+  // W4A8 calls with 16/32-token tiles: the E8M0 scales of x and of h again, laid out as the
+  // tensor cores' scale atoms want them - per 128-wide K tile, one 16-byte row per slot position
+  // (bytes 0..3 = the position's four scales of that K tile) - so a tile's atom is one bulk copy
+  size_t xs16, hs16;  // u8 [H/128][r16][16], u8 [Ip/128][r16][16]
+  int r16;            // rows per K tile: the positions of a 64-token call + 32 of padding
   size_t g;         // fp32 fc1 output [Sm][2][Ip] (CUDA-core path) / split-K partial sums
                     // [splits][Sm][2][Ip] (tensor-core paths)
   size_t tickets;   // int32 [max_tiles][ceil(I/128)] fc1 completion tickets
@@ -129,6 +134,9 @@ struct RunPtrs {
   int4* tiles;
   uint8_t* xq;
   uint8_t* xs;
+  uint8_t* xs16;
+  uint8_t* hs16;
+  int r16;
   float* g;
   int32_t* tickets;
   float* part;

@@ -179,8 +179,9 @@ route_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile_slots, int
 // The same launch clears the buffers that the later stages accumulate into.
 // One block of 32 bf16 activations -> 32 E4M3 codes + the E8M0 scale byte (OCP MX rule:
 // scale = 2^(floor(log2 amax) - 8), codes round to nearest even with saturation).
-__device__ __forceinline__ void quantize_block32(const __nv_bfloat16* __restrict__ src_bf16,
-                                                 uint8_t* __restrict__ q, uint8_t* __restrict__ s8) {
+__device__ __forceinline__ uint32_t quantize_block32(const __nv_bfloat16* __restrict__ src_bf16,
+                                                     uint8_t* __restrict__ q,
+                                                     uint8_t* __restrict__ s8) {
   const uint4* src = reinterpret_cast<const uint4*>(src_bf16);
   float v[32];
 #pragma unroll
@@ -208,6 +209,7 @@ __device__ __forceinline__ void quantize_block32(const __nv_bfloat16* __restrict
   dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
   dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
   *s8 = (uint8_t)s;
+  return s;
 }
 
 struct ZeroRegion {
@@ -218,8 +220,8 @@ struct ZeroRegion {
 __global__ void __launch_bounds__(256)
 actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t* __restrict__ ctrl,
             const int32_t* __restrict__ perm, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
-            uint16_t* __restrict__ x16, int32_t* __restrict__ err, ZeroRegion z0, ZeroRegion z1,
-            ZeroRegion z2) {
+            uint8_t* __restrict__ xs16, int r16, uint16_t* __restrict__ x16,
+            int32_t* __restrict__ err, ZeroRegion z0, ZeroRegion z1, ZeroRegion z2) {
   pdl_wait_prev();
   pdl_launch_next();
   const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -231,7 +233,9 @@ actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t*
       const size_t p = i / nb;
       const int b = (int)(i % nb);
       const int t = perm[p] / topk;
-      quantize_block32(x + (size_t)t * H + b * 32, xq + p * H + b * 32, xs + p * nb + b);
+      const uint32_t sb =
+          quantize_block32(x + (size_t)t * H + b * 32, xq + p * H + b * 32, xs + p * nb + b);
+      if (xs16 != nullptr) xs16[((size_t)(b >> 2) * r16 + p) * 16 + (b & 3)] = (uint8_t)sb;
     }
   }
   if (x16 != nullptr) {
@@ -279,8 +283,9 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
                         int32_t* __restrict__ cnt, int32_t* __restrict__ off,
                         int32_t* __restrict__ perm, int32_t* __restrict__ slot_of,
                         int4* __restrict__ tiles, int32_t* __restrict__ ctrl,
-                        uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, ZeroRegion z0,
-                        ZeroRegion z1, ZeroRegion z2) {
+                        uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
+                        uint8_t* __restrict__ xs16, int r16, ZeroRegion z0, ZeroRegion z1,
+                        ZeroRegion z2) {
   constexpr int NW = kSmallRouteThreads / 32;
   __shared__ int s_ids[kSmallRouteSlots];
   __shared__ int s_perm[kSmallRouteSlots];
@@ -364,7 +369,9 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
     const size_t p = i / nb;
     const int b = (int)(i % nb);
     const int t = s_perm[p] / topk;
-    quantize_block32(x + (size_t)t * H + b * 32, xq + p * H + b * 32, xs + p * nb + b);
+    const uint32_t sb =
+        quantize_block32(x + (size_t)t * H + b * 32, xq + p * H + b * 32, xs + p * nb + b);
+    if (xs16 != nullptr) xs16[((size_t)(b >> 2) * r16 + p) * 16 + (b & 3)] = (uint8_t)sb;
   }
   const ZeroRegion zs[3] = {z0, z1, z2};
 #pragma unroll
@@ -381,8 +388,9 @@ bool route_actq_small_supported(int Mk, int E) {
 
 cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int tile_slots,
                                     int max_tiles, const void* x, int H, int topk,
-                                    const RunPtrs& r, void* z0, size_t z0_words, void* z1,
-                                    size_t z1_words, void* z2, size_t z2_words, cudaStream_t st) {
+                                    const RunPtrs& r, bool atoms, void* z0, size_t z0_words,
+                                    void* z1, size_t z1_words, void* z2, size_t z2_words,
+                                    cudaStream_t st) {
   if (!route_actq_small_supported(Mk, E)) return cudaErrorInvalidValue;
   const size_t work = std::max((size_t)Mk * (H / 32),
                                std::max(z0_words / 4, std::max(z1_words / 4, z2_words / 4)));
@@ -393,8 +401,9 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int tile_
   return launch_kernel(route_actq_small_kernel, dim3(blocks), dim3(kSmallRouteThreads), 0, st,
                        false, ids, Mk, E, tile_slots, max_tiles,
                        reinterpret_cast<const __nv_bfloat16*>(x), H, topk, r.cnt, r.off, r.perm,
-                       r.slot_of, r.tiles, r.ctrl, r.xq, r.xs, ZeroRegion{z0, z0_words},
-                       ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words});
+                       r.slot_of, r.tiles, r.ctrl, r.xq, r.xs, atoms ? r.xs16 : nullptr, r.r16,
+                       ZeroRegion{z0, z0_words}, ZeroRegion{z1, z1_words},
+                       ZeroRegion{z2, z2_words});
 }
 
 cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int max_tiles,
@@ -405,8 +414,8 @@ cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int 
 }
 
 cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
-                        bool to_f16, void* z0, size_t z0_words, void* z1, size_t z1_words,
-                        void* z2, size_t z2_words, cudaStream_t st) {
+                        bool atoms, bool to_f16, void* z0, size_t z0_words, void* z1,
+                        size_t z1_words, void* z2, size_t z2_words, cudaStream_t st) {
   const size_t work = std::max(
       std::max(quant_x ? (size_t)M * topk * (H / 32) : (size_t)0,
                to_f16 ? (size_t)M * topk * (H / 8) : (size_t)0),
@@ -417,6 +426,7 @@ cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r,
                        reinterpret_cast<const __nv_bfloat16*>(x), H, topk,
                        static_cast<const int32_t*>(r.ctrl), static_cast<const int32_t*>(r.perm),
                        quant_x ? r.xq : nullptr, quant_x ? r.xs : nullptr,
+                       (quant_x && atoms) ? r.xs16 : nullptr, r.r16,
                        to_f16 ? r.x16 : nullptr, r.ctrl, ZeroRegion{z0, z0_words},
                        ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words});
 }

@@ -70,14 +70,18 @@ static __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// h of one token column for the 32 features of this warp -> MXFP8 code + scale.
-static __device__ __forceinline__ void requant_store(float h, int lane, size_t row_base_q,
-                                                     size_t row_base_s, int f, uint8_t* hq,
-                                                     uint8_t* hs) {
+// h of one token column for the 32 features of this warp -> MXFP8 code + scale (row-major
+// [rows][Ip/32], and, when hs16 is given, in the atom layout [Ip/128][r16][16]).
+static __device__ __forceinline__ void requant_store(float h, int lane, size_t row, int Ip, int f,
+                                                     uint8_t* hq, uint8_t* hs, uint8_t* hs16,
+                                                     int r16) {
   const float amax = warp_max(fabsf(h));
   const uint32_t s = mx_scale_byte(amax);
-  hq[row_base_q + f] = (uint8_t)f32_to_e4m3(h * e8m0_inv_f32(s));
-  if (lane == 0) hs[row_base_s + (f >> 5)] = (uint8_t)s;
+  hq[row * Ip + f] = (uint8_t)f32_to_e4m3(h * e8m0_inv_f32(s));
+  if (lane == 0) {
+    hs[row * (Ip / 32) + (f >> 5)] = (uint8_t)s;
+    if (hs16 != nullptr) hs16[((size_t)(f >> 7) * r16 + row) * 16 + ((f >> 5) & 3)] = (uint8_t)s;
+  }
 }
 
 // Adds `np` partial sums of this thread's accumulator row, in piece order 0..np-1, for the tile
