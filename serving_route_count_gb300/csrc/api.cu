@@ -32,6 +32,9 @@ bool fc1_stream_preferred(int bn, int units);
 size_t fc1_stream_part_bytes();
 cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanDims& d, int bn,
                               int M, float* part, int32_t* tickets, cudaStream_t st);
+bool fc2_persist_preferred(int bn, int units);
+cudaError_t launch_fc2_persist(const DevWeights& w, const RunPtrs& r, const PlanDims& d, int bn,
+                               int M, const float* topk_w, cudaStream_t st);
 // gemm_simt.cu
 cudaError_t launch_simt_stage(int stage, const DevWeights& w, const RunPtrs& r,
                               const PlanDims& d, int max_tiles, const void* x,
@@ -523,8 +526,11 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
               : launch_tc16_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(3);
-    e = tc8 ? launch_tc_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st)
-            : launch_tc16_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st);
+    if (tc8 && fc2_persist_preferred(bn, tiles * (d.H / 128)))
+      e = launch_fc2_persist(w, r, d, bn, M, topk_weights, st);
+    else
+      e = tc8 ? launch_tc_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st)
+              : launch_tc16_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(4);
     e = launch_simt_stage(3, w, r, d, plan->s.max_tiles, x, topk_weights, out, M, st);

@@ -338,6 +338,210 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   if (warp == 0) tmem_dealloc(tmem, Cfg::kAlloc);
 }
 
+// ------------------------------------------------------------------------------------ fc2
+// Persistent fc2 for the 16/32-token tiles: units are (tile, 128-row block of H) pairs,
+// tile-major; the G CTAs take equal contiguous ranges (fc2's K = Ip is a few tiles, so units
+// are never split).  The accumulators alternate between two TMEM buffers, so the combine of
+// one unit overlaps the loads and MMAs of the next instead of ending the CTA.  The combine is
+// that of fc2_tc_kernel (fp32 atomics into the token's row, or the weighted slot row of the
+// route buffer); a separate finalize launch writes the output.
+
+template <int BN>
+struct PersistFc2Cfg {
+  static constexpr int kB = BN * 128;
+  static constexpr int kStage = (kTileBytesA + kB + 512 + BN * 16 + 1023) / 1024 * 1024;
+  static constexpr int kStages = 3;                      // three CTAs per SM
+  static constexpr int kSmem = kStages * kStage + 1024;
+  static constexpr int kCols = 2 * BN + 8 * kStages;     // two accumulators, scale ring
+  static constexpr int kAlloc = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : 256;
+};
+
+struct PersistFc2Params {
+  CUtensorMap tm_w2;         // packed FP4 tiles [E*RB*KT][128][128], box 128 x 128 x 1
+  CUtensorMap tm_h;          // E4M3 [Sm][Ip], boxes 128 x BN
+  const uint8_t* sf2;        // weight scale atoms [E][RB][KT][512]
+  const uint8_t* hs16;       // h scale atom rows [Ip/128][r16][16]
+  const int4* tiles;
+  const int32_t* ctrl;
+  int32_t* err;
+  const int32_t* perm;
+  const float* topk_w;
+  float* acc;                // [M][H] atomic mode
+  float* rbuf;               // [M*k][H] deterministic mode
+  int H, KT, RB, Sm, topk, deterministic, r16;
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kStreamThreads)
+fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
+  using Cfg = PersistFc2Cfg<BN>;
+  constexpr int S = Cfg::kStages;
+  pdl_wait_prev();     // previous kernel of the call complete, its writes visible
+  pdl_launch_next();
+  const int G = gridDim.x, c = blockIdx.x;
+  const int units = p.ctrl[1] * p.RB;
+  const int u_begin = (int)((long long)c * units / G);
+  const int u_end = (int)((long long)(c + 1) * units / G);
+  if (u_begin >= u_end) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full[S], empty[S], acc_full[2], acc_empty[2], drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_fail;
+  __shared__ int s_f[BN];          // flat slot index of each column of the current tile
+  __shared__ float s_w[BN];        // its router weight
+
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, Cfg::kAlloc);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(&drain, 1);
+    s_fail = 0;
+    fence_barrier_init();
+  }
+  if (tid == 64) prefetch_tmap(&p.tm_w2);
+  if (tid == 96) prefetch_tmap(&p.tm_h);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  bool ok = true;
+  int issued = 0;                                   // stages filled by the TMA producer
+  auto stage = [&](int s) { return smem + s * Cfg::kStage; };
+  // stage layout: A | B | SFA | SFB
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int i = 0, cur_tile = -1, e = 0, p0 = 0;
+      for (int u = u_begin; u < u_end && ok; ++u) {
+        const int tile = u / p.RB, rb = u - tile * p.RB;
+        if (tile != cur_tile) {
+          cur_tile = tile;
+          const int4 td = p.tiles[tile];
+          e = td.x;
+          p0 = td.y;
+        }
+        for (int kt = 0; kt < p.KT && ok; ++kt, ++i) {
+          const int s = i % S;
+          if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
+          if (!ok) break;
+          uint8_t* st = stage(s);
+          const size_t a = ((size_t)e * p.RB + rb) * p.KT + kt;
+          mbar_arrive_expect_tx(&full[s], kTxBytesA + Cfg::kB + 512 + BN * 16);
+          tma_load_3d(st, &p.tm_w2, 0, 0, (int)a, &full[s]);
+          tma_load_2d(st + kTileBytesA, &p.tm_h, kt * 128, p0, &full[s]);
+          bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
+          bulk_load(st + kTileBytesA + Cfg::kB + 512, p.hs16 + ((size_t)kt * p.r16 + p0) * 16,
+                    BN * 16, &full[s]);
+        }
+      }
+      issued = i;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int i = 0, j = 0;
+      for (int u = u_begin; u < u_end && ok; ++u, ++j) {
+        const int b = j & 1;
+        if (j >= 2) ok = mbar_wait(&acc_empty[b], ((j >> 1) - 1) & 1, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem + b * BN;
+        for (int kt = 0; kt < p.KT && ok; ++kt, ++i) {
+          const int s = i % S;
+          ok = mbar_wait(&full[s], (i / S) & 1, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          uint8_t* st = stage(s);
+          const uint32_t sf = tmem + 2 * BN + 8 * s;
+          tc_cp_sf(sf + 0, desc_sf(st + kTileBytesA + Cfg::kB));
+          tc_cp_sf(sf + 4, desc_sf(st + kTileBytesA + Cfg::kB + 512));
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb) {
+            const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, BN, kb);
+            mma_mxf8f6f4(d, desc_sw128(st + 32 * kb), desc_sw128(st + kTileBytesA + 32 * kb),
+                         idesc, sf + 0, sf + 4, (kt > 0 || kb > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);
+        }
+        tc_commit(&acc_full[b]);
+      }
+    }
+  } else if (warp >= 4) {
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;                          // row of the 128-row block
+    int j = 0, cur_tile = -1, n = 0;
+    for (int u = u_begin; u < u_end; ++u, ++j) {
+      const int tile = u / p.RB, rb = u - tile * p.RB;
+      if (tile != cur_tile) {
+        // the combine's slot indices and router weights of the new tile, loaded before its
+        // accumulators are waited for (consecutive units of a range share their tile)
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        const int4 td = p.tiles[tile];
+        n = td.z;
+        if (row < n) {
+          const int f = p.perm[td.y + row];
+          s_f[row] = f;
+          s_w[row] = p.topk_w[f];
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        cur_tile = tile;
+      }
+      const int h = rb * 128 + row;
+      const int b = j & 1;
+      ok = ok && mbar_wait(&acc_full[b], (j >> 1) & 1, p.err);
+      tc_fence_after();
+      __syncwarp();
+      const uint32_t trow = tmem + b * BN + ((uint32_t)(quad * 32) << 16);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float y[16];
+        tmem_ld16(trow + c0, y);
+        if (!ok || c0 >= n) continue;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          if (c0 + jj < n) {
+            const int f = s_f[c0 + jj];
+            const float v = s_w[c0 + jj] * y[jj];
+            if (p.deterministic)
+              p.rbuf[(size_t)f * p.H + h] = v;
+            else
+              atomicAdd(&p.acc[(size_t)(f / p.topk) * p.H + h], v);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+    }
+  }
+  if (!ok) s_fail = 1;
+  tc_fence_before();
+  __syncthreads();
+  if (s_fail) {
+    // a wait gave up: let this CTA's copies and MMAs land before its memory is released
+    if (warp == 0 && lane == 0) drain_stage_loads<S>(full, issued, p.err);
+    if (warp == 1 && lane == 0) {
+      tc_commit(&drain);
+      mbar_wait(&drain, 0, p.err);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+  if (warp == 0) tmem_dealloc(tmem, Cfg::kAlloc);
+}
+
 // ---------------------------------------------------------------------------------- host side
 
 constexpr int kStreamMaxCtas = 320;   // partial slots are reserved for this many CTAs
@@ -407,6 +611,50 @@ cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanD
                                        StreamCfg<16>::kAlloc, 2, kStreamMaxCtas);
   return launch_kernel(fc1_stream_kernel<16>, dim3(G), dim3(kStreamThreads), StreamCfg<16>::kSmem,
                        st, true, p);
+}
+
+// The persistent fc2 serves the 16- and 32-token tiles (calls of up to 64 tokens) when the
+// unit-per-CTA fc2 would run many waves (measured: 39 -> 36 us at 3,750 units; slower than the
+// unit-per-CTA kernel below ~2.5 waves).
+bool fc2_persist_preferred(int bn, int units) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      (void)cudaGetLastError();
+      sms = 152;
+    }
+  }
+  return (bn == 16 || bn == 32) && units > 20 * sms;
+}
+
+template <int BN>
+static cudaError_t launch_fc2_persist_bn(const PersistFc2Params& p, cudaStream_t st) {
+  using Cfg = PersistFc2Cfg<BN>;
+  static const int G = persistent_grid(fc2_persist_kernel<BN>, Cfg::kSmem, Cfg::kAlloc, 4,
+                                       1 << 20);
+  return launch_kernel(fc2_persist_kernel<BN>, dim3(G), dim3(kStreamThreads), Cfg::kSmem, st,
+                       true, p);
+}
+
+cudaError_t launch_fc2_persist(const DevWeights& w, const RunPtrs& r, const PlanDims& d, int bn,
+                               int M, const float* topk_w, cudaStream_t st) {
+  PersistFc2Params p;
+  memset(&p, 0, sizeof(p));
+  const int Sm = M * d.topk;
+  p.RB = d.H / 128;
+  p.KT = d.Ip / 128;
+  if (!tmap_fp4(&p.tm_w2, w.w2, 128, (long long)d.E * p.RB * p.KT) ||
+      !tmap_u8(&p.tm_h, r.hq, d.Ip, Sm, bn))
+    return cudaErrorInvalidValue;
+  p.sf2 = w.s2; p.hs16 = r.hs16; p.r16 = r.r16;
+  p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
+  p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;
+  p.H = d.H; p.Sm = Sm; p.topk = d.topk; p.deterministic = d.deterministic;
+  if (bn == 16) return launch_fc2_persist_bn<16>(p, st);
+  if (bn == 32) return launch_fc2_persist_bn<32>(p, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace moe
