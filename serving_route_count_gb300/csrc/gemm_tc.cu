@@ -35,24 +35,22 @@ using namespace tc;
 template <int BN>
 struct TcCfg {
   static constexpr int kB = BN * 128;                         // activation tile bytes
-  static constexpr int kStage1 = (2 * kTileBytesA + kB + 3 * 512 + 1023) / 1024 * 1024;
-  static constexpr int kStage2 = (kTileBytesA + kB + 2 * 512 + 1023) / 1024 * 1024;
+  // stage: weight tile(s) | activation tile | weight scale atom(s) | activation scale atom
+  static constexpr int kStage1 = (2 * kTileBytesA + kB + 2 * 512 + BN * 16 + 1023) / 1024 * 1024;
+  static constexpr int kStage2 = (kTileBytesA + kB + 512 + BN * 16 + 1023) / 1024 * 1024;
   // short rings, several CTAs per SM: a CTA keeps only a few stages in flight behind its one
   // producer thread, so more CTAs per SM stream more bytes at once (measured: fc2 at 2 stages
   // and 5 CTAs per SM runs 3x faster than at 6 stages and 1 CTA per SM)
-  static constexpr int kStages1 = BN <= 16 ? 3 : (BN <= 64 ? 4 : 3);
-  static constexpr int kStages2 = BN <= 32 ? 2 : 4;
+  static constexpr int kStages1 = BN <= 16 ? 3 : 2;   // two CTAs per SM
+  static constexpr int kStages2 = 2;
   static constexpr int kCols1 = 2 * BN + 12 * kStages1;       // D_up, D_gate, scale ring
   static constexpr int kCols2 = BN + 8 * kStages2;
   static constexpr int pow2(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
   static constexpr int kAlloc1 = pow2(kCols1);
   static constexpr int kAlloc2 = pow2(kCols2);
-  // activation-scale atoms: one bulk copy of the prepared atom rows per stage for BN <= 32,
-  // else built by warp 2 from scales it stages in shared memory
-  static constexpr bool kSfbCopy = BN <= 32;
-  static constexpr int kSfStage = kSfbCopy ? 0 : BN * kSfChunk * 4;
-  static constexpr int kSmem1 = kStages1 * kStage1 + kSfStage + 1024;
-  static constexpr int kSmem2 = kStages2 * kStage2 + kSfStage + 1024;
+  static_assert(BN == 16 || BN == 32, "the W4A8 kernels use 16- and 32-token tiles");
+  static constexpr int kSmem1 = kStages1 * kStage1 + 1024;
+  static constexpr int kSmem2 = kStages2 * kStage2 + 1024;
 };
 
 struct TcFc1Params {
@@ -60,9 +58,8 @@ struct TcFc1Params {
   CUtensorMap tm_w13_tail;   // partial last row tile [2E*KT][I%128][128], box 128 x (I%128) x 1
   CUtensorMap tm_x;          // E4M3 [Sm][H], box 128 x BN
   const uint8_t* sf13;       // weight scale atoms [E][2][RT][KT][512]
-  const uint8_t* xs;         // activation scales [Sm][H/32]
-  const uint8_t* xs16;       // the same in the atom layout [H/128][r16][16] (BN <= 32)
-  uint8_t* hs16;             // h scales in the atom layout [Ip/128][r16][16] (BN <= 32)
+  const uint8_t* xs16;       // activation scales in the atom layout [H/128][r16][16]
+  uint8_t* hs16;             // h scales in the atom layout [Ip/128][r16][16]
   int r16;
   const int4* tiles;
   const int32_t* ctrl;
@@ -80,8 +77,7 @@ struct TcFc2Params {
   CUtensorMap tm_w2;         // packed FP4 tiles [E*(H/128)*KT][128][128], box 128 x 128 x 1
   CUtensorMap tm_h;          // E4M3 [Sm][Ip], box 128 x BN
   const uint8_t* sf2;        // weight scale atoms [E][H/128][Ip/128][512]
-  const uint8_t* hs;         // [Sm][Ip/32]
-  const uint8_t* hs16;       // the same in the atom layout [Ip/128][r16][16] (BN <= 32)
+  const uint8_t* hs16;       // h scales in the atom layout [Ip/128][r16][16]
   int r16;
   const int4* tiles;
   const int32_t* ctrl;
@@ -122,7 +118,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   }
   if (tid == 32) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], Cfg::kSfbCopy ? 1 : 2);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(&done, 1);
@@ -150,16 +146,14 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
         uint8_t* st = stage(s);
         const int kt = kt0 + i;
         if (fb < p.RTf) {
-          mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512 +
-                                              (Cfg::kSfbCopy ? BN * 16 : 0));
+          mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512 + BN * 16);
           tma_load_3d(st, &p.tm_w13, 0, 0, ((2 * e) * p.RTf + fb) * p.KT + kt, &full[s]);
           tma_load_3d(st + kTileBytesA, &p.tm_w13, 0, 0, ((2 * e + 1) * p.RTf + fb) * p.KT + kt,
                       &full[s]);
         } else {
           // partial row tile: rows >= I % 128 of the smem tile keep stale (finite) codes; their
           // accumulator rows are never read
-          mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + Cfg::kB + 2 * 512 +
-                                              (Cfg::kSfbCopy ? BN * 16 : 0));
+          mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + Cfg::kB + 2 * 512 + BN * 16);
           tma_load_3d(st, &p.tm_w13_tail, 0, 0, (2 * e) * p.KT + kt, &full[s]);
           tma_load_3d(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * e + 1) * p.KT + kt, &full[s]);
         }
@@ -168,26 +162,11 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
         const size_t a_gt = ((size_t)(2 * e + 1) * p.RT + fb) * p.KT + kt;
         bulk_load(st + 2 * kTileBytesA + Cfg::kB, p.sf13 + a_up * 512, 512, &full[s]);
         bulk_load(st + 2 * kTileBytesA + Cfg::kB + 512, p.sf13 + a_gt * 512, 512, &full[s]);
-        if (Cfg::kSfbCopy)
-          bulk_load(st + 2 * kTileBytesA + Cfg::kB + 1024,
-                    p.xs16 + ((size_t)kt * p.r16 + p0) * 16, BN * 16, &full[s]);
+        // activation-scale atom: the tile's prepared atom rows
+        bulk_load(st + 2 * kTileBytesA + Cfg::kB + 1024, p.xs16 + ((size_t)kt * p.r16 + p0) * 16,
+                  BN * 16, &full[s]);
       }
       issued = i;
-    }
-  } else if (warp == 2 && !Cfg::kSfbCopy) {
-    uint32_t* sfst = reinterpret_cast<uint32_t*>(smem + S * Cfg::kStage1);
-    for (int i = 0; i < nk && ok; ++i) {
-      const int s = i % S;
-      if (i % kSfChunk == 0) {
-        stage_act_sf<BN>(sfst, p.xs, p0, p.Sm, p.H / 32, kt0 + i, min(kSfChunk, nk - i), lane);
-        __syncwarp();
-      }
-      if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
-      if (!ok) break;
-      write_act_sf<BN>(stage(s) + 2 * kTileBytesA + Cfg::kB + 1024, sfst, i % kSfChunk, lane);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full[s]);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -318,7 +297,7 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
   }
   if (tid == 32) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], Cfg::kSfbCopy ? 1 : 2);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(&done, 1);
@@ -344,32 +323,15 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
         if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
         if (!ok) break;
         uint8_t* st = stage(s);
-        mbar_arrive_expect_tx(&full[s], kTxBytesA + Cfg::kB + 512 +
-                                            (Cfg::kSfbCopy ? BN * 16 : 0));
+        mbar_arrive_expect_tx(&full[s], kTxBytesA + Cfg::kB + 512 + BN * 16);
         tma_load_3d(st, &p.tm_w2, 0, 0, ((size_t)e * (p.H / 128) + rt) * p.KT + i, &full[s]);
         tma_load_2d(st + kTileBytesA, &p.tm_h, i * 128, p0, &full[s]);
         const size_t a = ((size_t)e * (p.H / 128) + rt) * p.KT + i;
         bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
-        if (Cfg::kSfbCopy)
-          bulk_load(st + kTileBytesA + Cfg::kB + 512, p.hs16 + ((size_t)i * p.r16 + p0) * 16,
-                    BN * 16, &full[s]);
+        bulk_load(st + kTileBytesA + Cfg::kB + 512, p.hs16 + ((size_t)i * p.r16 + p0) * 16,
+                  BN * 16, &full[s]);
       }
       issued = i;
-    }
-  } else if (warp == 2 && !Cfg::kSfbCopy) {
-    uint32_t* sfst = reinterpret_cast<uint32_t*>(smem + S * Cfg::kStage2);
-    for (int i = 0; i < nk && ok; ++i) {
-      const int s = i % S;
-      if (i % kSfChunk == 0) {
-        stage_act_sf<BN>(sfst, p.hs, p0, p.Sm, p.Ip / 32, i, min(kSfChunk, nk - i), lane);
-        __syncwarp();
-      }
-      if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
-      if (!ok) break;
-      write_act_sf<BN>(stage(s) + kTileBytesA + Cfg::kB + 512, sfst, i % kSfChunk, lane);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full[s]);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -474,8 +436,14 @@ bool tmap_u8(CUtensorMap* tm, const void* base, int K, int rows, int box_rows) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int tc_pick_bn(int M, int topk) {
+// Token-tile width of the tensor-core kernels.  W4A8 uses 32-token tiles beyond 16 tokens at
+// every size: measured faster than 64/128 from M = 128 to 4096, uniform and Zipf routing
+// (M = 1024: 784 vs 1183 / 2214 us per call; the wide-tile kernels run one CTA per SM and
+// their epilogues do not overlap the next unit), although experts with many slots then read
+// their weights once per tile.  The 16-bit path keeps wider tiles.
+int tc_pick_bn(int M, int topk, bool w4a8) {
   (void)topk;
+  if (w4a8) return M <= 16 ? 16 : 32;
   return M <= 16 ? 16 : (M <= 64 ? 32 : (M <= 512 ? 64 : 128));
 }
 
@@ -527,23 +495,22 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
         !tmap_fp4(&p.tm_w13_tail, w.w13 + (size_t)2 * d.E * p.RTf * kt * 8192, p.rem, 2LL * d.E * kt))
       return cudaErrorInvalidValue;
     if (!tmap_u8(&p.tm_x, r.xq, d.H, Sm, bn)) return cudaErrorInvalidValue;
-    p.sf13 = w.s13; p.xs = r.xs; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
+    p.sf13 = w.s13; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
     p.hq = r.hq; p.hs = r.hs; p.gacc = r.g; p.tickets = r.tickets;
-    p.xs16 = r.xs16; p.hs16 = bn <= 32 ? r.hs16 : nullptr; p.r16 = r.r16;
+    p.xs16 = r.xs16; p.hs16 = r.hs16; p.r16 = r.r16;
     p.H = d.H; p.I = d.I; p.Ip = d.Ip; p.RT = RT; p.KT = d.H / 128; p.Sm = Sm;
     p.splits = splits; p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
     switch (bn) {
       case 16: return launch_fc1_bn<16>(p, tiles, st);
       case 32: return launch_fc1_bn<32>(p, tiles, st);
-      case 64: return launch_fc1_bn<64>(p, tiles, st);
-      default: return launch_fc1_bn<128>(p, tiles, st);
+      default: return cudaErrorInvalidValue;
     }
   }
   TcFc2Params p;
   if (!tmap_fp4(&p.tm_w2, w.w2, 128, (long long)d.E * (d.H / 128) * (d.Ip / 128)))
     return cudaErrorInvalidValue;
   if (!tmap_u8(&p.tm_h, r.hq, d.Ip, Sm, bn)) return cudaErrorInvalidValue;
-  p.sf2 = w.s2; p.hs = r.hs; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
+  p.sf2 = w.s2; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
   p.hs16 = r.hs16; p.r16 = r.r16;
   p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;
   p.H = d.H; p.Ip = d.Ip; p.KT = d.Ip / 128; p.Sm = Sm; p.topk = d.topk;
@@ -551,8 +518,7 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
   switch (bn) {
     case 16: return launch_fc2_bn<16>(p, tiles, st);
     case 32: return launch_fc2_bn<32>(p, tiles, st);
-    case 64: return launch_fc2_bn<64>(p, tiles, st);
-    default: return launch_fc2_bn<128>(p, tiles, st);
+    default: return cudaErrorInvalidValue;
   }
 }
 

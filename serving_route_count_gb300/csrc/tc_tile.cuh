@@ -17,36 +17,6 @@ constexpr int kTileBytesA = 128 * 128;   // 128 rows x 128 K of padded FP4 (1 by
 // byte) as the transaction size, not the expanded shared-memory footprint.
 constexpr int kTxBytesA = 128 * 128 / 2;
 
-constexpr int kSfChunk = 32;   // K tiles of activation scales staged per batch
-
-// Activation scales of a CTA's BN rows for up to kSfChunk K tiles, staged in shared memory with
-// one batch of independent loads (row n, K tile j -> 4 bytes at stage[n * kSfChunk + j]), so the
-// per-stage scale atoms are built without a global-memory round trip on the critical path.
-template <int BN>
-static __device__ __forceinline__ void stage_act_sf(uint32_t* stage, const uint8_t* xs, int row0,
-                                                    int Sm, int kblocks, int kt0, int nkt,
-                                                    int lane) {
-  // all copies are issued before one wait: a single memory latency per chunk
-  for (int idx = lane; idx < BN * nkt; idx += 32) {
-    const int n = idx / nkt, j = idx - n * nkt;
-    uint32_t* dst = stage + n * kSfChunk + j;
-    if (row0 + n < Sm)
-      cp_async4(dst, xs + (size_t)(row0 + n) * kblocks + (kt0 + j) * 4);
-    else
-      *dst = 0;
-  }
-  cp_async_wait_all();
-}
-
-// Scale atom of BN activation rows for one 128-wide K tile: byte (n%32)*16 + (n/32)*4 + kb.
-template <int BN>
-static __device__ __forceinline__ void write_act_sf(uint8_t* dst, const uint32_t* stage, int j,
-                                                    int lane) {
-#pragma unroll
-  for (int n = lane; n < BN; n += 32)
-    *reinterpret_cast<uint32_t*>(dst + (n & 31) * 16 + (n >> 5) * 4) = stage[n * kSfChunk + j];
-}
-
 // Scale atom of BN activation rows for one K tile from a [j][BN] staging buffer (4 bytes per row:
 // the row's four E8M0 bytes of that K tile): byte (n%32)*16 + (n/32)*4 + kb.
 template <int BN>

@@ -224,9 +224,10 @@ def test_hybrid_full_size_sampled():
 
 @pytest.mark.parametrize("M,det", [(5, 0), (16, 1), (37, 0), (200, 1), (600, 0)])
 def test_w4a8_tensor_core_tile_widths(M, det):
-    """W4A8 through the tcgen05 kernels at M covering every token-tile width (16, 32, 64, 128)
-    and both fc1 schedules (split K for small M, whole K otherwise); E=16, H=1280 (10 K tiles),
-    I=192 (two 128-row weight blocks, the second half empty), Zipf routing with dropped ids."""
+    """W4A8 through the tcgen05 kernels at M covering both token-tile widths (16 up to 16
+    tokens, 32 beyond), experts with many tiles, and both fc1 schedules (split K for small M,
+    whole K otherwise); E=16, H=1280 (10 K tiles), I=192 (two 128-row weight blocks, the
+    second half empty), Zipf routing with dropped ids."""
     cfg = small_cfg("mxfp4")
     ck = S.make_checkpoint(cfg, seed=1000 + M)
     rng = np.random.default_rng(2000 + M)
