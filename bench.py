@@ -49,6 +49,7 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--det", action="store_true", help="deterministic combine")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefill", action="store_true", help="skip the prefill ladder report")
     p.add_argument("--profile", type=int, default=0, metavar="M",
                    help="profiling case: eager layer calls at decode size M (no timing)")
     p.add_argument("--profile-calls", type=int, default=4)
@@ -260,6 +261,68 @@ def profile_case(args):
     print(json.dumps({"profile_case": M, "calls": args.profile_calls, "device_error": code}))
 
 
+PREFILL_CFG = "prefill_w4a8"
+PREFILL_M = (128, 512, 2048, 4096)
+EXPERT_BYTES = 2 * 576 * 7168 // 2 + 2 * 576 * 7168 // 32 + 7168 * 576 // 2 + 7168 * 576 // 32
+
+
+def prefill_report(stream, flush, hbm_peak):
+    """Secondary report: whole-call times of the prefill ladder (E=384, H=7168, I=576, top-6,
+    uniform routing, atomic combine), each call a CUDA graph replayed after an L2 flush, with the
+    fraction of the HBM roofline (touched expert bytes) and of the dense FP8 tensor peak."""
+    import torch
+    from serving_route_count_gb300 import MoELayer
+    cfg = S.CONFIGS[PREFILL_CFG]
+    ck = S.make_checkpoint(cfg)
+    layer = MoELayer(ck, cfg.topk, max(PREFILL_M), cfg.swiglu_limit, 0)
+    del ck
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    # dense FP8 (kind::mxf8f6f4) peak: the measured bf16 GEMM rate x the nominal FP8/bf16 ratio 2
+    fp8_peak = 2.0 * float(peaks.get("bf16_tflops", 1900.0))
+    out = {}
+    for M in PREFILL_M:
+        x, ids, w = S.make_inputs(cfg, M)
+        xt = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).cuda()
+        it = torch.from_numpy(ids).cuda()
+        wt = torch.from_numpy(w).cuda()
+        ot = torch.empty((M, cfg.H), dtype=torch.bfloat16, device="cuda")
+        with torch.cuda.stream(stream):
+            layer(xt, it, wt, ot)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                layer(xt, it, wt, ot)
+        ts = []
+        for c in range(7):
+            with torch.cuda.stream(stream):
+                flush.fill_(c)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+            stream.synchronize()
+            if c >= 2:
+                ts.append(a.elapsed_time(b) * 1e-3)
+        sec = float(np.median(ts))
+        distinct = distinct_experts(ids, cfg.E)
+        slots = int(((ids >= 0) & (ids < cfg.E)).sum())
+        flops = 2.0 * slots * (2 * cfg.I * cfg.H + cfg.H * cfg.I)
+        out[str(M)] = {"us": round(sec * 1e6, 1), "tokens_per_s": round(M / sec),
+                       "hbm_frac": round(distinct * EXPERT_BYTES / sec / 1e9 / hbm_peak, 3),
+                       "tflops": round(flops / sec / 1e12, 1),
+                       "fp8_dense_frac": round(flops / sec / 1e12 / fp8_peak, 3)}
+    layer.close()
+    return {"workload": "prefill_w4a8: E=384 H=7168 I=576 top-6, MXFP4 x MXFP8, uniform "
+                        "routing, atomic combine; one graph replay per M after an L2 flush",
+            "fp8_dense_peak_tflops": fp8_peak, "calls": out}
+
+
 def our_arm(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -446,6 +509,7 @@ def our_arm(args, rank, world):
                 "api": "moe_run_host (pinned host buffers, H2D + run + D2H + sync)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
+        "prefill": None if args.no_prefill else prefill_report(stream, flush, peak),
     }
     print(json.dumps(line))
 
