@@ -255,9 +255,10 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
       __threadfence();
       // partial sums added in split order: the same result on every run
       reduce_pieces(
-          p.splits, n, (size_t)p.Ip,
-          [&](int sp, int c) { return p.gacc + ((size_t)sp * p.Sm + p0 + c) * 2 * p.Ip + f; },
-          [](int) { return false; },
+          p.splits, n, (size_t)2 * p.Ip, (size_t)p.Ip,
+          [&](int sp) -> const float* {
+            return p.gacc + ((size_t)sp * p.Sm + p0) * 2 * p.Ip + f;
+          },
           [&](int c, float up, float gt) {
             const float h = f < p.I ? swiglu(gt, up, p.limit, p.alpha, p.beta) : 0.f;
             const size_t row = (size_t)(p0 + c);

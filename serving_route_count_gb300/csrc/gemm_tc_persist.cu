@@ -65,7 +65,7 @@ struct StreamFc1Params {
 // D*G .. U-1 ("stream units") are split over all CTAs by K steps: CTA c gets the flat range
 // [c*W/G, (c+1)*W/G) of their W = (U - D*G) * KT steps.  CTA c first streams that range, then
 // its whole units c, c + G, ..., c + (D-1)*G, so the pieces' hand-over to the reducing CTA
-// overlaps the whole units' streaming.  The CTA's steps are numbered q = 0 .. nsteps-1.
+// overlaps the whole units' streaming.
 struct StreamWork {
   int KT, G, c, D, first_stream_unit;   // first_stream_unit = D * G
   long long W, x0, x1;                  // stream steps of all CTAs; this CTA's range
@@ -82,28 +82,31 @@ struct StreamWork {
     nsteps = n_sk + D * kt;
   }
   __device__ __forceinline__ long long begin_of(int cta) const { return (long long)cta * W / G; }
-  // unit and K tile of step q
-  __device__ __forceinline__ void step(int q, int& u, int& kt) const {
-    if (q < n_sk) {
-      const long long x = x0 + q;
-      u = first_stream_unit + (int)(x / KT);
-      kt = (int)(x % KT);
-    } else {
-      const int r = q - n_sk;
-      u = c + (r / KT) * G;
-      kt = r % KT;
+  // Segments of this CTA in order, without a division per K step: its stream range (split at
+  // unit boundaries), then its whole units.  next() returns false after the last one.
+  struct Segs {
+    const StreamWork* w;
+    long long x;    // next flat stream step
+    int dp;         // whole units handed out
+    __device__ __forceinline__ bool next(int& u, int& k0, int& len) {
+      if (x < w->x1) {
+        u = w->first_stream_unit + (int)(x / w->KT);
+        k0 = (int)(x % w->KT);
+        len = (int)min((long long)(w->KT - k0), w->x1 - x);
+        x += len;
+        return true;
+      }
+      if (dp < w->D) {
+        u = w->c + dp * w->G;
+        k0 = 0;
+        len = w->KT;
+        ++dp;
+        return true;
+      }
+      return false;
     }
-  }
-  // does step q start / end a segment (a run of one unit's K tiles)?
-  __device__ __forceinline__ bool seg_start(int q) const {
-    if (q == 0 || q == n_sk) return true;
-    int u, kt;
-    step(q, u, kt);
-    return kt == 0;
-  }
-  __device__ __forceinline__ bool seg_end(int q) const {
-    return q + 1 == nsteps || seg_start(q + 1);
-  }
+  };
+  __device__ __forceinline__ Segs segs() const { return Segs{this, x0, 0}; }
   // stream steps: CTA holding flat stream step x (ranges may be empty when G > W)
   __device__ __forceinline__ int cta_of(long long x) const {
     int cc = (int)((x * G) / W);
@@ -168,9 +171,9 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   if (warp == 0) {
     if (lane == 0) {
       int i = 0, cur_tile = -1, e = 0, p0 = 0;
-      for (; i < wk.nsteps && ok; ++i) {
-        int u, kt;
-        wk.step(i, u, kt);
+      auto sg = wk.segs();
+      int u, k0, len;
+      while (ok && sg.next(u, k0, len)) {
         const int tile = u / p.RT, fb = u - tile * p.RT;
         if (tile != cur_tile) {
           cur_tile = tile;
@@ -178,77 +181,77 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
           e = td.x;
           p0 = td.y;
         }
-        const int s = i % S;
-        if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
-        if (!ok) break;
-        uint8_t* st = stage(s);
-        if (fb < p.RTf) {
-          mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512 + BN * 16);
-          tma_load_3d(st, &p.tm_w13, 0, 0, ((2 * e) * p.RTf + fb) * p.KT + kt, &full[s]);
-          tma_load_3d(st + kTileBytesA, &p.tm_w13, 0, 0, ((2 * e + 1) * p.RTf + fb) * p.KT + kt,
-                      &full[s]);
-        } else {
-          mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + Cfg::kB + 2 * 512 + BN * 16);
-          tma_load_3d(st, &p.tm_w13_tail, 0, 0, (2 * e) * p.KT + kt, &full[s]);
-          tma_load_3d(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * e + 1) * p.KT + kt, &full[s]);
+        for (int kt = k0; kt < k0 + len && ok; ++kt, ++i) {
+          const int s = i % S;
+          if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
+          if (!ok) break;
+          uint8_t* st = stage(s);
+          if (fb < p.RTf) {
+            mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512 + BN * 16);
+            tma_load_3d(st, &p.tm_w13, 0, 0, ((2 * e) * p.RTf + fb) * p.KT + kt, &full[s]);
+            tma_load_3d(st + kTileBytesA, &p.tm_w13, 0, 0,
+                        ((2 * e + 1) * p.RTf + fb) * p.KT + kt, &full[s]);
+          } else {
+            mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + Cfg::kB + 2 * 512 + BN * 16);
+            tma_load_3d(st, &p.tm_w13_tail, 0, 0, (2 * e) * p.KT + kt, &full[s]);
+            tma_load_3d(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * e + 1) * p.KT + kt,
+                        &full[s]);
+          }
+          tma_load_2d(st + 2 * kTileBytesA, &p.tm_x, kt * 128, p0, &full[s]);
+          const size_t a_up = ((size_t)(2 * e) * p.RT + fb) * p.KT + kt;
+          const size_t a_gt = ((size_t)(2 * e + 1) * p.RT + fb) * p.KT + kt;
+          bulk_load(st + 2 * kTileBytesA + Cfg::kB, p.sf13 + a_up * 512, 512, &full[s]);
+          bulk_load(st + 2 * kTileBytesA + Cfg::kB + 512, p.sf13 + a_gt * 512, 512, &full[s]);
+          // activation-scale atom: the tile's prepared atom rows, one bulk copy
+          bulk_load(st + 2 * kTileBytesA + Cfg::kB + 1024,
+                    p.xs16 + ((size_t)kt * p.r16 + p0) * 16, BN * 16, &full[s]);
         }
-        tma_load_2d(st + 2 * kTileBytesA, &p.tm_x, kt * 128, p0, &full[s]);
-        const size_t a_up = ((size_t)(2 * e) * p.RT + fb) * p.KT + kt;
-        const size_t a_gt = ((size_t)(2 * e + 1) * p.RT + fb) * p.KT + kt;
-        bulk_load(st + 2 * kTileBytesA + Cfg::kB, p.sf13 + a_up * 512, 512, &full[s]);
-        bulk_load(st + 2 * kTileBytesA + Cfg::kB + 512, p.sf13 + a_gt * 512, 512, &full[s]);
-        // activation-scale atom: the tile's prepared atom rows, one bulk copy
-        bulk_load(st + 2 * kTileBytesA + Cfg::kB + 1024, p.xs16 + ((size_t)kt * p.r16 + p0) * 16,
-                  BN * 16, &full[s]);
       }
       issued = i;
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      int j = -1, b = 0;
-      uint32_t d_up = 0, d_gt = 0;
-      for (int i = 0; i < wk.nsteps && ok; ++i) {
-        const bool first = wk.seg_start(i);
-        if (first) {
-          ++j;
-          b = j & 1;
-          if (j >= 2) ok = mbar_wait(&acc_empty[b], ((j >> 1) - 1) & 1, p.err);
-          if (!ok) break;
-          tc_fence_after();
-          d_up = tmem + b * Cfg::kAcc;
-          d_gt = d_up + BN;
-        }
-        const int s = i % S;
-        ok = mbar_wait(&full[s], (i / S) & 1, p.err);
+      int i = 0, j = 0;
+      auto sg = wk.segs();
+      int u, k0, len;
+      while (ok && sg.next(u, k0, len)) {
+        const int b = j & 1;
+        if (j >= 2) ok = mbar_wait(&acc_empty[b], ((j >> 1) - 1) & 1, p.err);
         if (!ok) break;
         tc_fence_after();
-        uint8_t* st = stage(s);
-        const uint32_t sf = tmem + 2 * Cfg::kAcc + 12 * s;
-        tc_cp_sf(sf + 0, desc_sf(st + 2 * kTileBytesA + Cfg::kB));
-        tc_cp_sf(sf + 4, desc_sf(st + 2 * kTileBytesA + Cfg::kB + 512));
-        tc_cp_sf(sf + 8, desc_sf(st + 2 * kTileBytesA + Cfg::kB + 1024));
+        const uint32_t d_up = tmem + b * Cfg::kAcc, d_gt = d_up + BN;
+        for (int kt = 0; kt < len && ok; ++kt, ++i) {
+          const int s = i % S;
+          ok = mbar_wait(&full[s], (i / S) & 1, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          uint8_t* st = stage(s);
+          const uint32_t sf = tmem + 2 * Cfg::kAcc + 12 * s;
+          tc_cp_sf(sf + 0, desc_sf(st + 2 * kTileBytesA + Cfg::kB));
+          tc_cp_sf(sf + 4, desc_sf(st + 2 * kTileBytesA + Cfg::kB + 512));
+          tc_cp_sf(sf + 8, desc_sf(st + 2 * kTileBytesA + Cfg::kB + 1024));
 #pragma unroll
-        for (int kb = 0; kb < 4; ++kb) {
-          const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, BN, kb);
-          const uint64_t bdesc = desc_sw128(st + 2 * kTileBytesA + 32 * kb);
-          const uint32_t acc = (!first || kb > 0) ? 1u : 0u;
-          mma_mxf8f6f4(d_up, desc_sw128(st + 32 * kb), bdesc, idesc, sf + 0, sf + 8, acc);
-          mma_mxf8f6f4(d_gt, desc_sw128(st + kTileBytesA + 32 * kb), bdesc, idesc, sf + 4,
-                       sf + 8, acc);
+          for (int kb = 0; kb < 4; ++kb) {
+            const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, BN, kb);
+            const uint64_t bdesc = desc_sw128(st + 2 * kTileBytesA + 32 * kb);
+            const uint32_t acc = (kt > 0 || kb > 0) ? 1u : 0u;
+            mma_mxf8f6f4(d_up, desc_sw128(st + 32 * kb), bdesc, idesc, sf + 0, sf + 8, acc);
+            mma_mxf8f6f4(d_gt, desc_sw128(st + kTileBytesA + 32 * kb), bdesc, idesc, sf + 4,
+                         sf + 8, acc);
+          }
+          tc_commit(&empty[s]);
         }
-        tc_commit(&empty[s]);
-        if (wk.seg_end(i)) tc_commit(&acc_full[b]);
+        tc_commit(&acc_full[b]);
+        ++j;
       }
     }
   } else if (warp >= 4) {
     const int quad = warp & 3;
     const int row = quad * 32 + lane;                         // weight row within the block
     int j = 0;
-    for (int q = 0; q < wk.nsteps; ++j) {
-      int u, k0;
-      wk.step(q, u, k0);
-      int len = 1;
-      while (q + len < wk.nsteps && !wk.seg_start(q + len)) ++len;
+    auto sg = wk.segs();
+    int u, k0, len;
+    for (; sg.next(u, k0, len); ++j) {
       const int k1 = k0 + len;
       const int tile = u / p.RT, fb = u - tile * p.RT;
       const int4 td = p.tiles[tile];
@@ -306,12 +309,12 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
           const long long xf = (long long)(u - wk.first_stream_unit) * p.KT;
           const int c_first = wk.cta_of(xf), c_last = wk.cta_of(xf + p.KT - 1);
           reduce_pieces(
-              c_last - c_first + 1, n, (size_t)BN * 128,
-              [&](int qq, int cc) {
-                return p.part + (size_t)wk.part_slot(c_first + qq, u) * Cfg::kPartFloats +
-                       cc * 128 + row;
+              c_last - c_first + 1, n, (size_t)128, (size_t)BN * 128,
+              [&](int qq) -> const float* {
+                const int cc = c_first + qq;
+                if (wk.begin_of(cc + 1) == wk.begin_of(cc)) return nullptr;   // empty range
+                return p.part + (size_t)wk.part_slot(cc, u) * Cfg::kPartFloats + row;
               },
-              [&](int qq) { return wk.begin_of(c_first + qq + 1) == wk.begin_of(c_first + qq); },
               [&](int cc, float up, float gt) {
                 const float h = f < p.I ? swiglu(gt, up, p.limit, p.alpha, p.beta) : 0.f;
                 const size_t r = (size_t)(p0 + cc);
@@ -319,7 +322,6 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
               });
         }
       }
-      q += len;
     }
   }
   if (!ok) s_fail = 1;

@@ -55,26 +55,29 @@ static __device__ __forceinline__ void requant_store(float h, int lane, size_t r
 }
 
 // Adds `np` partial sums of this thread's accumulator row, in piece order 0..np-1, for the tile
-// columns 0..n-1 and hands each column's (up, gate) total to emit(c, up, gate).  ptr(q, c) is
-// the address of piece q's up value of column c (gate at + gate_off); skip(q) marks a piece that
-// holds nothing (it adds nothing: its loads are predicated off and +0 leaves a sum unchanged).
-// The loads are issued 32 at a time - 4 pieces x 4 columns while n <= 4, 16 columns of one piece
-// otherwise - so a reduction costs a few memory latencies, not one per piece.  n and np are
-// uniform across the warp (emit may use warp shuffles).
-template <typename Ptr, typename Skip, typename Emit>
-static __device__ __forceinline__ void reduce_pieces(int np, int n, size_t gate_off, Ptr ptr,
-                                                     Skip skip, Emit emit) {
+// columns 0..n-1 and hands each column's (up, gate) total to emit(c, up, gate).  base(q) is the
+// address of piece q's up value of column 0, or null for a piece that holds nothing (it adds
+// nothing: +0 leaves a sum unchanged); column c is at + c * col_stride, gate at + gate_off.
+// The piece addresses are computed once per piece and the loads issued 32 at a time - 4 pieces
+// x 4 columns while n <= 4, 16 columns of one piece otherwise - so a reduction costs a few
+// memory latencies, not one per piece.  n and np are uniform across the warp (emit may use warp
+// shuffles).
+template <typename Base, typename Emit>
+static __device__ __forceinline__ void reduce_pieces(int np, int n, size_t col_stride,
+                                                     size_t gate_off, Base base, Emit emit) {
   if (n <= 4) {
     float up[4] = {0.f, 0.f, 0.f, 0.f}, gt[4] = {0.f, 0.f, 0.f, 0.f};
     for (int q0 = 0; q0 < np; q0 += 4) {
+      const float* bq[4];
+#pragma unroll
+      for (int jq = 0; jq < 4; ++jq) bq[jq] = q0 + jq < np ? base(q0 + jq) : nullptr;
       float a[4][4], b[4][4];
 #pragma unroll
       for (int jq = 0; jq < 4; ++jq) {
-        const bool live = q0 + jq < np && !skip(q0 + jq);
 #pragma unroll
         for (int jc = 0; jc < 4; ++jc) {
-          const bool in = live && jc < n;
-          const float* pp = in ? ptr(q0 + jq, jc) : nullptr;
+          const bool in = bq[jq] != nullptr && jc < n;
+          const float* pp = in ? bq[jq] + (size_t)jc * col_stride : nullptr;
           a[jq][jc] = in ? __ldcg(pp) : 0.f;
           b[jq][jc] = in ? __ldcg(pp + gate_off) : 0.f;
         }
@@ -97,12 +100,13 @@ static __device__ __forceinline__ void reduce_pieces(int np, int n, size_t gate_
 #pragma unroll
     for (int j = 0; j < 16; ++j) up[j] = gt[j] = 0.f;
     for (int q = 0; q < np; ++q) {
-      if (skip(q)) continue;
+      const float* bq = base(q);
+      if (bq == nullptr) continue;
       float a[16], b[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const bool in = c0 + j < n;
-        const float* pp = in ? ptr(q, c0 + j) : nullptr;
+        const float* pp = in ? bq + (size_t)(c0 + j) * col_stride : nullptr;
         a[j] = in ? __ldcg(pp) : 0.f;
         b[j] = in ? __ldcg(pp + gate_off) : 0.f;
       }
