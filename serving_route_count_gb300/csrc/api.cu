@@ -26,7 +26,7 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int tile_
 cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                             int bn, int tiles, int splits, const float* topk_w, int M,
                             cudaStream_t st);
-int tc_pick_bn(int M, int topk, bool w4a8);
+int tc_pick_bn(int M, int topk, int E, bool w4a8);
 // gemm_tc_persist.cu
 bool fc1_stream_preferred(int bn, int units);
 size_t fc1_stream_part_bytes();
@@ -313,8 +313,9 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   s.tiles = take((size_t)s.max_tiles * 16);
   s.xq = a8 ? take(Sm * H) : 0;
   s.xs = a8 ? take(Sm * H / 32) : 0;
-  // scale atoms of the 16/32-token tiles (every W4A8 tensor-core call)
-  s.r16 = (int)Sm + 32;
+  // scale atom rows of the W4A8 tensor-core calls, padded for the widest tile (96 tokens) that
+  // starts at the last slot position
+  s.r16 = (int)Sm + 96;
   s.xs16 = a8 ? take((size_t)(H / 128) * s.r16 * 16) : 0;
   s.hs16 = a8 ? take((size_t)(d.Ip / 128) * s.r16 * 16) : 0;
   // fc1 output of the CUDA-core path, or the per-split partial sums of the tensor-core path
@@ -322,7 +323,7 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   size_t g_rows = Sm;
   for (int m = 1; m <= max_m; ++m) {
     const int sp = fc1_splits(
-        d, call_tiles(d, s.max_tiles, m, tc_pick_bn(m, topk, quant_mode == MOE_W4A8_MXFP4)));
+        d, call_tiles(d, s.max_tiles, m, tc_pick_bn(m, topk, E, quant_mode == MOE_W4A8_MXFP4)));
     if (sp > 1) g_rows = std::max(g_rows, (size_t)sp * m * topk);
   }
   s.g = take(g_rows * 2 * d.Ip * 4);
@@ -484,7 +485,7 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   const bool tc8 = use_tc(d), t16 = use_tc16(d);
   const bool tc = tc8 || t16;
   const int Sm = M * d.topk;
-  const int bn = tc ? tc_pick_bn(M, d.topk, tc8) : kSimtSlots;
+  const int bn = tc ? tc_pick_bn(M, d.topk, d.E, tc8) : kSimtSlots;
   const int tiles = call_tiles(d, plan->s.max_tiles, M, bn);
   const int RT = cdiv(d.I, 128);
   // decode widths with more units than one wave of CTAs: the persistent stream-K fc1

@@ -43,12 +43,17 @@ struct TcCfg {
   // and 5 CTAs per SM runs 3x faster than at 6 stages and 1 CTA per SM)
   static constexpr int kStages1 = BN <= 16 ? 3 : 2;   // two CTAs per SM
   static constexpr int kStages2 = 2;
-  static constexpr int kCols1 = 2 * BN + 12 * kStages1;       // D_up, D_gate, scale ring
-  static constexpr int kCols2 = BN + 8 * kStages2;
+  static constexpr int kChunks = NChunks<BN>::kCount;
+  static constexpr int kSf1 = 8 + 4 * kChunks;                // SFA_up, SFA_gate, SFB chunks
+  static constexpr int kSf2 = 4 + 4 * kChunks;                // SFA, SFB chunks
+  static constexpr int kCols1 = 2 * BN + kSf1 * kStages1;     // D_up, D_gate, scale ring
+  static constexpr int kCols2 = BN + kSf2 * kStages2;
   static constexpr int pow2(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
   static constexpr int kAlloc1 = pow2(kCols1);
   static constexpr int kAlloc2 = pow2(kCols2);
-  static_assert(BN == 16 || BN == 32, "the W4A8 kernels use 16- and 32-token tiles");
+  static_assert(BN == 16 || BN == 32 || BN == 64 || BN == 96, "W4A8 token tile widths");
+  // two CTAs per SM: tensor memory of at most 256 columns each
+  static_assert(pow2(kCols1) <= 256, "fc1 tensor memory");
   static constexpr int kSmem1 = kStages1 * kStage1 + 1024;
   static constexpr int kSmem2 = kStages2 * kStage2 + 1024;
 };
@@ -100,6 +105,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   if (tile >= p.ctrl[1]) return;
   const int4 td = p.tiles[tile];
   const int e = td.x, p0 = td.y, n = td.z;
+  const TileLoad<BN> tl(n);
   const int fb = blockIdx.y, split = blockIdx.z;
   const int kt0 = split * p.KT / p.splits, kt1 = (split + 1) * p.KT / p.splits;
   const int nk = kt1 - kt0;
@@ -146,25 +152,25 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
         uint8_t* st = stage(s);
         const int kt = kt0 + i;
         if (fb < p.RTf) {
-          mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512 + BN * 16);
+          mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + tl.b_bytes + 2 * 512 + tl.sf_bytes);
           tma_load_3d(st, &p.tm_w13, 0, 0, ((2 * e) * p.RTf + fb) * p.KT + kt, &full[s]);
           tma_load_3d(st + kTileBytesA, &p.tm_w13, 0, 0, ((2 * e + 1) * p.RTf + fb) * p.KT + kt,
                       &full[s]);
         } else {
           // partial row tile: rows >= I % 128 of the smem tile keep stale (finite) codes; their
           // accumulator rows are never read
-          mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + Cfg::kB + 2 * 512 + BN * 16);
+          mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + tl.b_bytes + 2 * 512 + tl.sf_bytes);
           tma_load_3d(st, &p.tm_w13_tail, 0, 0, (2 * e) * p.KT + kt, &full[s]);
           tma_load_3d(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * e + 1) * p.KT + kt, &full[s]);
         }
-        tma_load_2d(st + 2 * kTileBytesA, &p.tm_x, kt * 128, p0, &full[s]);
+        tl.load_b(st + 2 * kTileBytesA, &p.tm_x, kt * 128, p0, &full[s]);
         const size_t a_up = ((size_t)(2 * e) * p.RT + fb) * p.KT + kt;
         const size_t a_gt = ((size_t)(2 * e + 1) * p.RT + fb) * p.KT + kt;
         bulk_load(st + 2 * kTileBytesA + Cfg::kB, p.sf13 + a_up * 512, 512, &full[s]);
         bulk_load(st + 2 * kTileBytesA + Cfg::kB + 512, p.sf13 + a_gt * 512, 512, &full[s]);
         // activation-scale atom: the tile's prepared atom rows
         bulk_load(st + 2 * kTileBytesA + Cfg::kB + 1024, p.xs16 + ((size_t)kt * p.r16 + p0) * 16,
-                  BN * 16, &full[s]);
+                  tl.sf_bytes, &full[s]);
       }
       issued = i;
     }
@@ -176,18 +182,27 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
         if (!ok) break;
         tc_fence_after();
         uint8_t* st = stage(s);
-        const uint32_t sf = tmem + 2 * BN + 12 * s;
+        const uint32_t sf = tmem + 2 * BN + Cfg::kSf1 * s;
         tc_cp_sf(sf + 0, desc_sf(st + 2 * kTileBytesA + Cfg::kB));
         tc_cp_sf(sf + 4, desc_sf(st + 2 * kTileBytesA + Cfg::kB + 512));
-        tc_cp_sf(sf + 8, desc_sf(st + 2 * kTileBytesA + Cfg::kB + 1024));
+#pragma unroll
+        for (int j = 0; j < Cfg::kChunks; ++j)
+          if (j < tl.nch)
+            tc_cp_sf(sf + 8 + 4 * j, desc_sf(st + 2 * kTileBytesA + Cfg::kB + 1024 + 512 * j));
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) {
-          const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, BN, kb);
-          const uint64_t bdesc = desc_sw128(st + 2 * kTileBytesA + 32 * kb);
+          const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, NChunks<BN>::kWidth, kb);
           const uint32_t acc = (i > 0 || kb > 0) ? 1u : 0u;
-          mma_mxf8f6f4(tmem, desc_sw128(st + 32 * kb), bdesc, idesc, sf + 0, sf + 8, acc);
-          mma_mxf8f6f4(tmem + BN, desc_sw128(st + kTileBytesA + 32 * kb), bdesc, idesc, sf + 4,
-                       sf + 8, acc);
+#pragma unroll
+          for (int j = 0; j < Cfg::kChunks; ++j) {
+            if (j >= tl.nch) break;
+            // columns 32j.. of the tile: B rows 32j.. (4 KB into the 128-byte-row tile)
+            const uint64_t bdesc = desc_sw128(st + 2 * kTileBytesA + 4096 * j + 32 * kb);
+            mma_mxf8f6f4(tmem + 32 * j, desc_sw128(st + 32 * kb), bdesc, idesc, sf + 0,
+                         sf + 8 + 4 * j, acc);
+            mma_mxf8f6f4(tmem + BN + 32 * j, desc_sw128(st + kTileBytesA + 32 * kb), bdesc, idesc,
+                         sf + 4, sf + 8 + 4 * j, acc);
+          }
         }
         tc_commit(&empty[s]);
       }
@@ -279,6 +294,7 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
   if (tile >= p.ctrl[1]) return;
   const int4 td = p.tiles[tile];
   const int e = td.x, p0 = td.y, n = td.z;
+  const TileLoad<BN> tl(n);
   const int rt = blockIdx.y;
   const int nk = p.KT;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -324,13 +340,13 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
         if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
         if (!ok) break;
         uint8_t* st = stage(s);
-        mbar_arrive_expect_tx(&full[s], kTxBytesA + Cfg::kB + 512 + BN * 16);
+        mbar_arrive_expect_tx(&full[s], kTxBytesA + tl.b_bytes + 512 + tl.sf_bytes);
         tma_load_3d(st, &p.tm_w2, 0, 0, ((size_t)e * (p.H / 128) + rt) * p.KT + i, &full[s]);
-        tma_load_2d(st + kTileBytesA, &p.tm_h, i * 128, p0, &full[s]);
+        tl.load_b(st + kTileBytesA, &p.tm_h, i * 128, p0, &full[s]);
         const size_t a = ((size_t)e * (p.H / 128) + rt) * p.KT + i;
         bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
         bulk_load(st + kTileBytesA + Cfg::kB + 512, p.hs16 + ((size_t)i * p.r16 + p0) * 16,
-                  BN * 16, &full[s]);
+                  tl.sf_bytes, &full[s]);
       }
       issued = i;
     }
@@ -342,14 +358,21 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
         if (!ok) break;
         tc_fence_after();
         uint8_t* st = stage(s);
-        const uint32_t sf = tmem + BN + 8 * s;
+        const uint32_t sf = tmem + BN + Cfg::kSf2 * s;
         tc_cp_sf(sf + 0, desc_sf(st + kTileBytesA + Cfg::kB));
-        tc_cp_sf(sf + 4, desc_sf(st + kTileBytesA + Cfg::kB + 512));
+#pragma unroll
+        for (int j = 0; j < Cfg::kChunks; ++j)
+          if (j < tl.nch)
+            tc_cp_sf(sf + 4 + 4 * j, desc_sf(st + kTileBytesA + Cfg::kB + 512 + 512 * j));
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) {
-          const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, BN, kb);
-          mma_mxf8f6f4(tmem, desc_sw128(st + 32 * kb), desc_sw128(st + kTileBytesA + 32 * kb),
-                       idesc, sf + 0, sf + 4, (i > 0 || kb > 0) ? 1u : 0u);
+          const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, NChunks<BN>::kWidth, kb);
+#pragma unroll
+          for (int j = 0; j < Cfg::kChunks; ++j)
+            if (j < tl.nch)
+              mma_mxf8f6f4(tmem + 32 * j, desc_sw128(st + 32 * kb),
+                         desc_sw128(st + kTileBytesA + 4096 * j + 32 * kb), idesc, sf + 0,
+                         sf + 4 + 4 * j, (i > 0 || kb > 0) ? 1u : 0u);
         }
         tc_commit(&empty[s]);
       }
@@ -437,14 +460,19 @@ bool tmap_u8(CUtensorMap* tm, const void* base, int K, int rows, int box_rows) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Token-tile width of the tensor-core kernels.  W4A8 uses 32-token tiles beyond 16 tokens at
-// every size: measured faster than 64/128 from M = 128 to 4096, uniform and Zipf routing
-// (M = 1024: 784 vs 1183 / 2214 us per call; the wide-tile kernels run one CTA per SM and
-// their epilogues do not overlap the next unit), although experts with many slots then read
-// their weights once per tile.  The 16-bit path keeps wider tiles.
-int tc_pick_bn(int M, int topk, bool w4a8) {
-  (void)topk;
-  if (w4a8) return M <= 16 ? 16 : 32;
+// Token-tile width of the tensor-core kernels.  W4A8: 16-token tiles for decode calls (M <= 16);
+// beyond, the width follows the expected slots per expert (M * topk / E under uniform routing),
+// so that an expert's weights stream through the SMs about once per call: 32 up to 16 slots per
+// expert, 64 up to 40, 96 beyond (2 CTAs per SM at every width: 2-stage rings, <= 256 tensor
+// memory columns).  The 16-bit path keeps its M-based widths.
+int tc_pick_bn(int M, int topk, int E, bool w4a8) {
+  if (w4a8) {
+    if (M <= 16) return 16;
+    const long long slots = (long long)M * topk;
+    if (slots <= 16LL * E) return 32;
+    if (slots <= 40LL * E) return 64;
+    return 96;
+  }
   return M <= 16 ? 16 : (M <= 64 ? 32 : (M <= 512 ? 64 : 128));
 }
 
@@ -495,7 +523,7 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
     if (!tmap_fp4(&p.tm_w13, w.w13, 128, 2LL * d.E * p.RTf * kt) ||
         !tmap_fp4(&p.tm_w13_tail, w.w13 + (size_t)2 * d.E * p.RTf * kt * 8192, p.rem, 2LL * d.E * kt))
       return cudaErrorInvalidValue;
-    if (!tmap_u8(&p.tm_x, r.xq, d.H, Sm, bn)) return cudaErrorInvalidValue;
+    if (!tmap_u8(&p.tm_x, r.xq, d.H, Sm, act_box_rows(bn))) return cudaErrorInvalidValue;
     p.sf13 = w.s13; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
     p.hq = r.hq; p.hs = r.hs; p.gacc = r.g; p.tickets = r.tickets;
     p.xs16 = r.xs16; p.hs16 = r.hs16; p.r16 = r.r16;
@@ -504,13 +532,15 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
     switch (bn) {
       case 16: return launch_fc1_bn<16>(p, tiles, st);
       case 32: return launch_fc1_bn<32>(p, tiles, st);
+      case 64: return launch_fc1_bn<64>(p, tiles, st);
+      case 96: return launch_fc1_bn<96>(p, tiles, st);
       default: return cudaErrorInvalidValue;
     }
   }
   TcFc2Params p;
   if (!tmap_fp4(&p.tm_w2, w.w2, 128, (long long)d.E * (d.H / 128) * (d.Ip / 128)))
     return cudaErrorInvalidValue;
-  if (!tmap_u8(&p.tm_h, r.hq, d.Ip, Sm, bn)) return cudaErrorInvalidValue;
+  if (!tmap_u8(&p.tm_h, r.hq, d.Ip, Sm, act_box_rows(bn))) return cudaErrorInvalidValue;
   p.sf2 = w.s2; p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
   p.hs16 = r.hs16; p.r16 = r.r16;
   p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;
@@ -519,6 +549,8 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
   switch (bn) {
     case 16: return launch_fc2_bn<16>(p, tiles, st);
     case 32: return launch_fc2_bn<32>(p, tiles, st);
+    case 64: return launch_fc2_bn<64>(p, tiles, st);
+    case 96: return launch_fc2_bn<96>(p, tiles, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -354,8 +354,11 @@ struct PersistFc2Cfg {
   static constexpr int kStage = (kTileBytesA + kB + 512 + BN * 16 + 1023) / 1024 * 1024;
   static constexpr int kStages = 3;                      // three CTAs per SM
   static constexpr int kSmem = kStages * kStage + 1024;
-  static constexpr int kCols = 2 * BN + 8 * kStages;     // two accumulators, scale ring
+  static constexpr int kChunks = NChunks<BN>::kCount;
+  static constexpr int kSf = 4 + 4 * kChunks;           // SFA, SFB chunks
+  static constexpr int kCols = 2 * BN + kSf * kStages;  // two accumulators, scale ring
   static constexpr int kAlloc = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : 256;
+  static_assert(kCols <= 256, "fc2 tensor memory");
 };
 
 struct PersistFc2Params {
@@ -395,6 +398,8 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
   __shared__ int s_fail;
   __shared__ int s_f[BN];          // flat slot index of each column of the current tile
   __shared__ float s_w[BN];        // its router weight
+  // per epilogue warp: 16 token columns x its 32 output features, read back transposed
+  __shared__ __align__(16) float s_y[4][16][32];
 
   if (warp == 0) {
     tmem_alloc(&s_tmem, Cfg::kAlloc);
@@ -427,6 +432,7 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
   if (warp == 0) {
     if (lane == 0) {
       int i = 0, cur_tile = -1, e = 0, p0 = 0;
+      TileLoad<BN> tl(BN);
       for (int u = u_begin; u < u_end && ok; ++u) {
         const int tile = u / p.RB, rb = u - tile * p.RB;
         if (tile != cur_tile) {
@@ -434,6 +440,7 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
           const int4 td = p.tiles[tile];
           e = td.x;
           p0 = td.y;
+          tl = TileLoad<BN>(td.z);
         }
         for (int kt = 0; kt < p.KT && ok; ++kt, ++i) {
           const int s = i % S;
@@ -441,20 +448,26 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
           if (!ok) break;
           uint8_t* st = stage(s);
           const size_t a = ((size_t)e * p.RB + rb) * p.KT + kt;
-          mbar_arrive_expect_tx(&full[s], kTxBytesA + Cfg::kB + 512 + BN * 16);
+          mbar_arrive_expect_tx(&full[s], kTxBytesA + tl.b_bytes + 512 + tl.sf_bytes);
           tma_load_3d(st, &p.tm_w2, 0, 0, (int)a, &full[s]);
-          tma_load_2d(st + kTileBytesA, &p.tm_h, kt * 128, p0, &full[s]);
+          tl.load_b(st + kTileBytesA, &p.tm_h, kt * 128, p0, &full[s]);
           bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
           bulk_load(st + kTileBytesA + Cfg::kB + 512, p.hs16 + ((size_t)kt * p.r16 + p0) * 16,
-                    BN * 16, &full[s]);
+                    tl.sf_bytes, &full[s]);
         }
       }
       issued = i;
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      int i = 0, j = 0;
+      int i = 0, j = 0, cur_tile = -1;
+      TileLoad<BN> tl(BN);
       for (int u = u_begin; u < u_end && ok; ++u, ++j) {
+        const int tile = u / p.RB;
+        if (tile != cur_tile) {
+          cur_tile = tile;
+          tl = TileLoad<BN>(p.tiles[tile].z);
+        }
         const int b = j & 1;
         if (j >= 2) ok = mbar_wait(&acc_empty[b], ((j >> 1) - 1) & 1, p.err);
         if (!ok) break;
@@ -466,14 +479,21 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
           if (!ok) break;
           tc_fence_after();
           uint8_t* st = stage(s);
-          const uint32_t sf = tmem + 2 * BN + 8 * s;
+          const uint32_t sf = tmem + 2 * BN + Cfg::kSf * s;
           tc_cp_sf(sf + 0, desc_sf(st + kTileBytesA + Cfg::kB));
-          tc_cp_sf(sf + 4, desc_sf(st + kTileBytesA + Cfg::kB + 512));
+#pragma unroll
+          for (int jc = 0; jc < Cfg::kChunks; ++jc)
+            if (jc < tl.nch)
+              tc_cp_sf(sf + 4 + 4 * jc, desc_sf(st + kTileBytesA + Cfg::kB + 512 + 512 * jc));
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb) {
-            const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, BN, kb);
-            mma_mxf8f6f4(d, desc_sw128(st + 32 * kb), desc_sw128(st + kTileBytesA + 32 * kb),
-                         idesc, sf + 0, sf + 4, (kt > 0 || kb > 0) ? 1u : 0u);
+            const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, NChunks<BN>::kWidth, kb);
+#pragma unroll
+            for (int jc = 0; jc < Cfg::kChunks; ++jc)
+              if (jc < tl.nch)
+                mma_mxf8f6f4(d + 32 * jc, desc_sw128(st + 32 * kb),
+                           desc_sw128(st + kTileBytesA + 4096 * jc + 32 * kb), idesc, sf + 0,
+                           sf + 4 + 4 * jc, (kt > 0 || kb > 0) ? 1u : 0u);
           }
           tc_commit(&empty[s]);
         }
@@ -500,28 +520,38 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
         asm volatile("bar.sync 1, 128;" ::: "memory");
         cur_tile = tile;
       }
-      const int h = rb * 128 + row;
+      // after the transpose a lane holds four consecutive output features of one token
+      const int h4 = rb * 128 + quad * 32 + 4 * (lane & 7);
       const int b = j & 1;
       ok = ok && mbar_wait(&acc_full[b], (j >> 1) & 1, p.err);
       tc_fence_after();
       __syncwarp();
       const uint32_t trow = tmem + b * BN + ((uint32_t)(quad * 32) << 16);
+      float(*sy)[32] = s_y[quad];
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float y[16];
         tmem_ld16(trow + c0, y);
         if (!ok || c0 >= n) continue;
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          if (c0 + jj < n) {
-            const int f = s_f[c0 + jj];
-            const float v = s_w[c0 + jj] * y[jj];
+        for (int jj = 0; jj < 16; ++jj) sy[jj][lane] = y[jj];
+        __syncwarp();
+        // one 16-byte combine per (token, 4 features): a quarter of the scalar atomics
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int cc = 4 * r + (lane >> 3);
+          if (c0 + cc < n) {
+            const float4 v = *reinterpret_cast<const float4*>(&sy[cc][4 * (lane & 7)]);
+            const int f = s_f[c0 + cc];
+            const float wt = s_w[c0 + cc];
+            const float4 o = make_float4(wt * v.x, wt * v.y, wt * v.z, wt * v.w);
             if (p.deterministic)
-              p.rbuf[(size_t)f * p.H + h] = v;
+              *reinterpret_cast<float4*>(p.rbuf + (size_t)f * p.H + h4) = o;
             else
-              atomicAdd(&p.acc[(size_t)(f / p.topk) * p.H + h], v);
+              atomicAdd(reinterpret_cast<float4*>(p.acc + (size_t)(f / p.topk) * p.H + h4), o);
           }
         }
+        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();
@@ -615,9 +645,9 @@ cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanD
                        st, true, p);
 }
 
-// The persistent fc2 serves the 16- and 32-token tiles (calls of up to 64 tokens) when the
-// unit-per-CTA fc2 would run many waves (measured: 39 -> 36 us at 3,750 units; slower than the
-// unit-per-CTA kernel below ~2.5 waves).
+// The persistent fc2 serves every W4A8 tile width when the unit-per-CTA fc2 would run many
+// waves (measured: 39 -> 36 us at 3,750 units; slower than the unit-per-CTA kernel below ~2.5
+// waves).
 bool fc2_persist_preferred(int bn, int units) {
   static int sms = 0;
   if (sms == 0) {
@@ -628,7 +658,7 @@ bool fc2_persist_preferred(int bn, int units) {
       sms = 152;
     }
   }
-  return (bn == 16 || bn == 32) && units > 20 * sms;
+  return (bn == 16 || bn == 32 || bn == 64 || bn == 96) && units > 20 * sms;
 }
 
 template <int BN>
@@ -648,7 +678,7 @@ cudaError_t launch_fc2_persist(const DevWeights& w, const RunPtrs& r, const Plan
   p.RB = d.H / 128;
   p.KT = d.Ip / 128;
   if (!tmap_fp4(&p.tm_w2, w.w2, 128, (long long)d.E * p.RB * p.KT) ||
-      !tmap_u8(&p.tm_h, r.hq, d.Ip, Sm, bn))
+      !tmap_u8(&p.tm_h, r.hq, d.Ip, Sm, act_box_rows(bn)))
     return cudaErrorInvalidValue;
   p.sf2 = w.s2; p.hs16 = r.hs16; p.r16 = r.r16;
   p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
@@ -656,6 +686,8 @@ cudaError_t launch_fc2_persist(const DevWeights& w, const RunPtrs& r, const Plan
   p.H = d.H; p.Sm = Sm; p.topk = d.topk; p.deterministic = d.deterministic;
   if (bn == 16) return launch_fc2_persist_bn<16>(p, st);
   if (bn == 32) return launch_fc2_persist_bn<32>(p, st);
+  if (bn == 64) return launch_fc2_persist_bn<64>(p, st);
+  if (bn == 96) return launch_fc2_persist_bn<96>(p, st);
   return cudaErrorInvalidValue;
 }
 

@@ -17,6 +17,50 @@ constexpr int kTileBytesA = 128 * 128;   // 128 rows x 128 K of padded FP4 (1 by
 // byte) as the transaction size, not the expanded shared-memory footprint.
 constexpr int kTxBytesA = 128 * 128 / 2;
 
+// Token columns of one block-scaled MMA.  A tile of BN tokens runs as ceil(BN / 32) MMAs of
+// up to 32 columns each: the activation scales of a tile are BN consecutive 16-byte atom rows
+// (bytes 0..3 = a token's four scales of the K tile), and each 32-row run of them is exactly the
+// scale atom of a 32-column MMA, copied to tensor memory as is.
+template <int BN>
+struct NChunks {
+  static constexpr int kCount = (BN + 31) / 32;
+  static constexpr int kWidth = BN < 32 ? BN : 32;
+  static_assert(BN % 16 == 0 && BN <= 96 && (BN <= 32 || BN % 32 == 0), "token tile width");
+};
+
+// What a tile of n tokens at tile width BN loads per K tile: up to 32 tokens the whole BN-row
+// box; beyond, only the 32-row chunks that hold tokens (one 32-column MMA each), so that a
+// wide tile of a cold expert costs no more than a narrow one.
+template <int BN>
+struct TileLoad {
+  int nch;              // 32-column MMAs of the tile (1 up to 32 tokens)
+  uint32_t b_bytes;     // activation codes
+  uint32_t sf_bytes;    // activation scale atom rows
+  __device__ __forceinline__ explicit TileLoad(int n) {
+    if (BN <= 32) {
+      nch = 1;
+      b_bytes = BN * 128;
+      sf_bytes = BN * 16;
+    } else {
+      nch = min(NChunks<BN>::kCount, (n + 31) >> 5);
+      b_bytes = (uint32_t)nch * 4096;
+      sf_bytes = (uint32_t)nch * 512;
+    }
+  }
+  // activation codes of K offset k, slot positions p0.. (the map's boxes are BN rows up to
+  // 32, else 32 rows)
+  __device__ __forceinline__ void load_b(uint8_t* dst, const CUtensorMap* tm, int k, int p0,
+                                         uint64_t* bar) const {
+    if (BN <= 32) {
+      tma_load_2d(dst, tm, k, p0, bar);
+    } else {
+      for (int j = 0; j < nch; ++j) tma_load_2d(dst + 4096 * j, tm, k, p0 + 32 * j, bar);
+    }
+  }
+};
+// Rows of the activation tensor map's box at tile width BN.
+inline int act_box_rows(int bn) { return bn < 32 ? bn : 32; }
+
 // Scale atom of BN activation rows for one K tile from a [j][BN] staging buffer (4 bytes per row:
 // the row's four E8M0 bytes of that K tile): byte (n%32)*16 + (n/32)*4 + kb.
 template <int BN>

@@ -198,6 +198,34 @@ def test_decode_full_size_sampled(decode_layer, det, fc1_kernel):
     layer.close()
 
 
+@pytest.mark.parametrize("cfg_name,M,det", [("prefill_w4a8", 1024, 1), ("prefill_w4a8", 2048, 0),
+                                             ("prefill_w4a8_zipf", 4096, 1)])
+def test_prefill_full_size_sampled(decode_layer, cfg_name, M, det):
+    """E=384, H=7168, I=576, top-6 prefill calls (the decode layer's weights, the prefill
+    routing recipe) at the three wide token-tile widths (32, 64 and 96 tokens at 16, 32 and 64
+    expected slots per expert) with the persistent fc2: routing and activation codes
+    bit-exact for the whole call, outputs of sampled rows against the oracle, and
+    (deterministic mode) bit-identical repeats."""
+    cfg, ck = decode_layer
+    pcfg = S.CONFIGS[cfg_name]
+    x, ids, w = S.make_inputs(pcfg, M)
+    layer = _layer(ck, cfg.topk, M, cfg.swiglu_limit, det)
+    got = run_layer(layer, x, ids, w)
+    st, code = layer.device_error()
+    assert st == 0 and code == 0, code
+    route = O.route(ids, cfg.E)
+    for a, b in zip(layer.routing(M), route):
+        assert np.array_equal(a, b)
+    xq, xs = layer.actq(M)
+    q, s = C.mxfp8_quantize(C.bf16_bits_to_f64(x))
+    tok = route[2] // cfg.topk
+    assert np.array_equal(xq, q[tok]) and np.array_equal(xs, s[tok])
+    check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=[0, 1, M // 2, M - 1])
+    if det:
+        assert np.array_equal(run_layer(layer, x, ids, w), got)
+    layer.close()
+
+
 def test_nvfp4_full_size_sampled():
     cfg = S.CONFIGS["w4a16_nvfp4"]
     ck = S.make_checkpoint(cfg)
@@ -222,12 +250,13 @@ def test_hybrid_full_size_sampled():
 
 # ---------------------------------------------------------------------------- tensor-core path
 
-@pytest.mark.parametrize("M,det", [(5, 0), (16, 1), (37, 0), (200, 1), (600, 0)])
+@pytest.mark.parametrize("M,det", [(5, 0), (16, 1), (37, 0), (100, 1), (200, 1), (600, 0)])
 def test_w4a8_tensor_core_tile_widths(M, det):
-    """W4A8 through the tcgen05 kernels at M covering both token-tile widths (16 up to 16
-    tokens, 32 beyond), experts with many tiles, and both fc1 schedules (split K for small M,
-    whole K otherwise); E=16, H=1280 (10 K tiles), I=192 (two 128-row weight blocks, the
-    second half empty), Zipf routing with dropped ids."""
+    """W4A8 through the tcgen05 kernels at M covering every token-tile width (16 up to 16
+    tokens; then 32, 64 and 96 by expected slots per expert: M = 37, 100, 200 / 600 here),
+    experts with many tiles, and both fc1 schedules (split K for small M, whole K otherwise);
+    E=16, H=1280 (10 K tiles), I=192 (two 128-row weight blocks, the second half empty), Zipf
+    routing with dropped ids."""
     cfg = small_cfg("mxfp4")
     ck = S.make_checkpoint(cfg, seed=1000 + M)
     rng = np.random.default_rng(2000 + M)
