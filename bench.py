@@ -241,8 +241,9 @@ def reduce_over_ranks(step_ms: float, tokens: int, world: int, device=None):
 
 
 def profile_case(args):
-    """A small case for ncu: the decode layer (E=384, H=7168, I=576, top-6) called eagerly
-    `--profile-calls` times at M = `--profile`, each call on its own routing set."""
+    """A case for ncu: the decode / prefill layer (E=384, H=7168, I=576, top-6) called eagerly
+    `--profile-calls` times at M = `--profile`, each call on its own routing set (the decode
+    recipe up to M = 16, the uniform prefill recipe beyond)."""
     import torch
 
     from serving_route_count_gb300 import MoELayer, build
@@ -250,10 +251,11 @@ def profile_case(args):
     cfg = S.CONFIGS[DECODE_CFG]
     ck = S.make_checkpoint(cfg)
     M = args.profile
+    icfg = cfg if M <= 16 else S.CONFIGS[PREFILL_CFG]
     layer = MoELayer(ck, cfg.topk, M, cfg.swiglu_limit, args.det)
     del ck
     for c in range(args.profile_calls):
-        x, ids, w = S.make_inputs(cfg, M, seed=cfg.seed_base + 100 * M + c)
+        x, ids, w = S.make_inputs(icfg, M, seed=icfg.seed_base + 100 * M + c)
         xt = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).cuda()
         layer(xt, torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda())
     torch.cuda.synchronize()

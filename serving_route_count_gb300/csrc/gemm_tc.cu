@@ -75,6 +75,7 @@ struct TcFc1Params {
   int32_t* tickets;          // [max_tiles][RT]
   int H, I, Ip, RT, KT, Sm, splits;
   int RTf, rem;              // full 128-row weight tiles per half, rows of the partial tile
+  int fb_in_x;               // grid (RT, tiles, splits) instead of (tiles, RT, splits)
   float limit, alpha, beta;
 };
 
@@ -101,12 +102,14 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   constexpr int S = Cfg::kStages1;
   pdl_wait_prev();     // previous kernel of the call complete, its writes visible
   pdl_launch_next();
-  const int tile = blockIdx.x;
+  // the row blocks of a tile are adjacent in launch order (while the tiles fit the grid's y),
+  // so the CTAs that read the same activation tile run together and share it through L2
+  const int tile = p.fb_in_x ? blockIdx.y : blockIdx.x;
+  const int fb = p.fb_in_x ? blockIdx.x : blockIdx.y, split = blockIdx.z;
   if (tile >= p.ctrl[1]) return;
   const int4 td = p.tiles[tile];
   const int e = td.x, p0 = td.y, n = td.z;
   const TileLoad<BN> tl(n);
-  const int fb = blockIdx.y, split = blockIdx.z;
   const int kt0 = split * p.KT / p.splits, kt1 = (split + 1) * p.KT / p.splits;
   const int nk = kt1 - kt0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -144,6 +147,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
 
   if (warp == 0) {
     if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
       int i = 0;
       for (; i < nk && ok; ++i) {
         const int s = i % S;
@@ -153,15 +157,18 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
         const int kt = kt0 + i;
         if (fb < p.RTf) {
           mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + tl.b_bytes + 2 * 512 + tl.sf_bytes);
-          tma_load_3d(st, &p.tm_w13, 0, 0, ((2 * e) * p.RTf + fb) * p.KT + kt, &full[s]);
-          tma_load_3d(st + kTileBytesA, &p.tm_w13, 0, 0, ((2 * e + 1) * p.RTf + fb) * p.KT + kt,
-                      &full[s]);
+          tma_load_3d_hint(st, &p.tm_w13, 0, 0, ((2 * e) * p.RTf + fb) * p.KT + kt, &full[s],
+                           pol);
+          tma_load_3d_hint(st + kTileBytesA, &p.tm_w13, 0, 0,
+                           ((2 * e + 1) * p.RTf + fb) * p.KT + kt,
+                      &full[s], pol);
         } else {
           // partial row tile: rows >= I % 128 of the smem tile keep stale (finite) codes; their
           // accumulator rows are never read
           mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + tl.b_bytes + 2 * 512 + tl.sf_bytes);
-          tma_load_3d(st, &p.tm_w13_tail, 0, 0, (2 * e) * p.KT + kt, &full[s]);
-          tma_load_3d(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * e + 1) * p.KT + kt, &full[s]);
+          tma_load_3d_hint(st, &p.tm_w13_tail, 0, 0, (2 * e) * p.KT + kt, &full[s], pol);
+          tma_load_3d_hint(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * e + 1) * p.KT + kt,
+                           &full[s], pol);
         }
         tl.load_b(st + 2 * kTileBytesA, &p.tm_x, kt * 128, p0, &full[s]);
         const size_t a_up = ((size_t)(2 * e) * p.RT + fb) * p.KT + kt;
@@ -334,6 +341,7 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
 
   if (warp == 0) {
     if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
       int i = 0;
       for (; i < nk && ok; ++i) {
         const int s = i % S;
@@ -341,7 +349,8 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
         if (!ok) break;
         uint8_t* st = stage(s);
         mbar_arrive_expect_tx(&full[s], kTxBytesA + tl.b_bytes + 512 + tl.sf_bytes);
-        tma_load_3d(st, &p.tm_w2, 0, 0, ((size_t)e * (p.H / 128) + rt) * p.KT + i, &full[s]);
+        tma_load_3d_hint(st, &p.tm_w2, 0, 0, (int)(((size_t)e * (p.H / 128) + rt) * p.KT + i),
+                         &full[s], pol);
         tl.load_b(st + kTileBytesA, &p.tm_h, i * 128, p0, &full[s]);
         const size_t a = ((size_t)e * (p.H / 128) + rt) * p.KT + i;
         bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
@@ -488,8 +497,10 @@ static cudaError_t launch_fc1_bn(const TcFc1Params& p, int tiles, cudaStream_t s
                          (int)cudaSharedmemCarveoutMaxShared);
     attr = true;
   }
-  dim3 grid(tiles, p.RT, p.splits);
-  return launch_kernel(fc1_tc_kernel<BN>, grid, dim3(kTcThreads), Cfg::kSmem1, st, true, p);
+  TcFc1Params q = p;
+  q.fb_in_x = tiles <= 65535 ? 1 : 0;
+  const dim3 grid = q.fb_in_x ? dim3(p.RT, tiles, p.splits) : dim3(tiles, p.RT, p.splits);
+  return launch_kernel(fc1_tc_kernel<BN>, grid, dim3(kTcThreads), Cfg::kSmem1, st, true, q);
 }
 
 template <int BN>

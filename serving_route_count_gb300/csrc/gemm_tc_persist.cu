@@ -170,6 +170,7 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
 
   if (warp == 0) {
     if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
       int i = 0, cur_tile = -1, e = 0, p0 = 0;
       auto sg = wk.segs();
       int u, k0, len;
@@ -188,14 +189,15 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
           uint8_t* st = stage(s);
           if (fb < p.RTf) {
             mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512 + BN * 16);
-            tma_load_3d(st, &p.tm_w13, 0, 0, ((2 * e) * p.RTf + fb) * p.KT + kt, &full[s]);
-            tma_load_3d(st + kTileBytesA, &p.tm_w13, 0, 0,
-                        ((2 * e + 1) * p.RTf + fb) * p.KT + kt, &full[s]);
+            tma_load_3d_hint(st, &p.tm_w13, 0, 0, ((2 * e) * p.RTf + fb) * p.KT + kt, &full[s],
+                             pol);
+            tma_load_3d_hint(st + kTileBytesA, &p.tm_w13, 0, 0,
+                        ((2 * e + 1) * p.RTf + fb) * p.KT + kt, &full[s], pol);
           } else {
             mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + Cfg::kB + 2 * 512 + BN * 16);
-            tma_load_3d(st, &p.tm_w13_tail, 0, 0, (2 * e) * p.KT + kt, &full[s]);
-            tma_load_3d(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * e + 1) * p.KT + kt,
-                        &full[s]);
+            tma_load_3d_hint(st, &p.tm_w13_tail, 0, 0, (2 * e) * p.KT + kt, &full[s], pol);
+            tma_load_3d_hint(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * e + 1) * p.KT + kt,
+                        &full[s], pol);
           }
           tma_load_2d(st + 2 * kTileBytesA, &p.tm_x, kt * 128, p0, &full[s]);
           const size_t a_up = ((size_t)(2 * e) * p.RT + fb) * p.KT + kt;
@@ -431,6 +433,7 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
 
   if (warp == 0) {
     if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
       int i = 0, cur_tile = -1, e = 0, p0 = 0;
       TileLoad<BN> tl(BN);
       for (int u = u_begin; u < u_end && ok; ++u) {
@@ -449,7 +452,7 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
           uint8_t* st = stage(s);
           const size_t a = ((size_t)e * p.RB + rb) * p.KT + kt;
           mbar_arrive_expect_tx(&full[s], kTxBytesA + tl.b_bytes + 512 + tl.sf_bytes);
-          tma_load_3d(st, &p.tm_w2, 0, 0, (int)a, &full[s]);
+          tma_load_3d_hint(st, &p.tm_w2, 0, 0, (int)a, &full[s], pol);
           tl.load_b(st + kTileBytesA, &p.tm_h, kt * 128, p0, &full[s]);
           bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
           bulk_load(st + kTileBytesA + Cfg::kB + 512, p.hs16 + ((size_t)kt * p.r16 + p0) * 16,
