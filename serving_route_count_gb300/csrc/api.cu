@@ -17,6 +17,14 @@ cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r,
                         bool atoms, bool to_f16, void* z0, size_t z0_words, void* z1,
                         size_t z1_words, void* z2, size_t z2_words, cudaStream_t st);
 bool route_actq_small_supported(int Mk, int E);
+int route_chunks(int Mk);
+cudaError_t launch_route_count(const int32_t* ids, int Mk, int E, const RunPtrs& r,
+                               cudaStream_t st);
+cudaError_t launch_route_scatter(const int32_t* ids, int Mk, int E, int tile_slots,
+                                 int max_tiles, const RunPtrs& r, cudaStream_t st);
+cudaError_t launch_actq_rows(const void* x, int M, int H, int topk, const RunPtrs& r, void* z0,
+                             size_t z0_words, void* z1, size_t z1_words, void* z2,
+                             size_t z2_words, cudaStream_t st);
 cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int tile_slots,
                                     int max_tiles, const void* x, int H, int topk,
                                     const RunPtrs& r, bool atoms, void* z0, size_t z0_words,
@@ -329,6 +337,7 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   s.g = take(g_rows * 2 * d.Ip * 4);
   s.tickets = take(align_up((size_t)s.max_tiles * cdiv(I, 128), 4) * 4);
   s.part = a8 ? take(fc1_stream_part_bytes()) : 0;
+  s.rcc = a8 ? take((size_t)route_chunks((int)Sm) * E * 4) : 0;
   s.hq = a8 ? take(Sm * d.Ip) : 0;
   s.hs = a8 ? take(Sm * d.Ip / 32) : 0;
   s.h16 = a8 ? 0 : take(Sm * d.Ip * 2);
@@ -384,6 +393,7 @@ static RunPtrs resolve(const moe_plan_t* plan, void* scratch) {
   r.g = reinterpret_cast<float*>(b + s.g);
   r.tickets = reinterpret_cast<int32_t*>(b + s.tickets);
   r.part = a8 ? reinterpret_cast<float*>(b + s.part) : nullptr;
+  r.rcc = a8 ? reinterpret_cast<int32_t*>(b + s.rcc) : nullptr;
   r.hq = a8 ? b + s.hq : nullptr;
   r.hs = a8 ? b + s.hs : nullptr;
   r.h16 = a8 ? nullptr : reinterpret_cast<__nv_bfloat16*>(b + s.h16);
@@ -451,9 +461,10 @@ moe_status moe_call_launches(const moe_plan_t* plan, int M, int* launches) {
   }
   const bool tc8 = use_tc(d), t16 = use_tc16(d);
   if (tc8 || t16) {
-    // route and actq (one launch for small W4A8 calls), fc1, fc2, finalize
+    // routing and quantisation (one launch for small W4A8 calls, three - counts, scatter,
+    // quantisation - for larger ones, two for the 16-bit path), fc1, fc2, finalize
     const bool small = tc8 && route_actq_small_supported(M * d.topk, d.E);
-    *launches = (small ? 1 : 2) + 3;
+    *launches = (small ? 1 : (tc8 ? 3 : 2)) + 3;
     return MOE_OK;
   }
   // route, actq (when something needs it), fc1, act, fc2, finalize
@@ -510,6 +521,15 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
                                 atoms, acc, acc_words, g, g_words, tk, tk_words, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
+  } else if (tc8) {
+    // larger W4A8 calls: routing over many CTAs, quantisation straight into slot order
+    e = launch_route_count(topk_ids, Sm, d.E, r, st);
+    if (e == cudaSuccess)
+      e = launch_route_scatter(topk_ids, Sm, d.E, bn, plan->s.max_tiles, r, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    prof(1);
+    e = launch_actq_rows(x, M, d.H, d.topk, r, acc, acc_words, g, g_words, tk, tk_words, st);
+    if (e != cudaSuccess) return cuda_status(e);
   } else {
     e = launch_route(topk_ids, Sm, d.E, bn, plan->s.max_tiles, r, st);
     if (e != cudaSuccess) return cuda_status(e);

@@ -108,6 +108,7 @@ struct Scratch {
                     // [splits][Sm][2][Ip] (tensor-core paths)
   size_t tickets;   // int32 [max_tiles][ceil(I/128)] fc1 completion tickets
   size_t part;      // W4A8: fp32 partial sums of the stream-K fc1 (fixed-size slots)
+  size_t rcc;       // W4A8: int32 [ceil(Sm / 1024)][E] chunked-routing counts + 1 ticket
   size_t hq, hs;    // W4A8: u8 [Sm][Ip], u8 [Sm][Ip/32]
   size_t h16;       // W4A16: bf16 [Sm][Ip] (CUDA-core path) or f16 (tensor-core path)
   size_t x16;       // W4A16 tensor-core path: f16 activations [Sm][H] in slot order
@@ -146,6 +147,7 @@ struct RunPtrs {
   uint16_t* x16;
   float* acc;
   float* rbuf;
+  int32_t* rcc;     // chunked routing: per-chunk expert counts / bases, then a ticket
 };
 
 // ----------------------------------------------------------------------------------------------

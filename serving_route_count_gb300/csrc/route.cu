@@ -382,6 +382,233 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Larger W4A8 calls: routing spread over CTAs of kChunkSlots flat slots each, then the MXFP8
+// quantisation of the slot-ordered rows, in three launches.
+//   route_count_kernel: per-chunk expert counts cc[c][e].
+//   route_scatter_kernel: one CTA per chunk adds up the chunk counts into the expert totals and
+//     its chunk's bases base[e] = off[e] + (slots of e in earlier chunks) and ranks the chunk's
+//     slots (stable: by flat index within each expert, the same ranking as route_kernel's
+//     rounds) into perm / slot_of; CTA 0 writes cnt / off / tiles / ctrl.
+//   actq_rows_kernel: one warp per slot position quantises its token's row.
+// Same tables and codes, bit for bit, as route_kernel + actq_kernel.
+constexpr int kChunkSlots = 1024;
+
+__global__ void __launch_bounds__(kRouteThreads)
+route_count_kernel(const int32_t* __restrict__ ids, int Mk, int E, int32_t* __restrict__ ctrl,
+                   int32_t* __restrict__ cc) {
+  __shared__ int s_cnt[kMaxRouteExperts];
+  const int tid = threadIdx.x, c = blockIdx.x;
+  pdl_wait_prev();     // previous kernel of the call complete, its writes visible
+  pdl_launch_next();
+  if (c == 0 && tid == 0) ctrl[0] = 0;  // error word of this call
+  for (int e = tid; e < E; e += kRouteThreads) s_cnt[e] = 0;
+  __syncthreads();
+  const int f = c * kChunkSlots + tid;
+  if (f < Mk) {
+    const int e = ids[f];
+    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kRouteThreads) cc[(size_t)c * E + e] = s_cnt[e];
+}
+
+__global__ void __launch_bounds__(kRouteThreads)
+route_scatter_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile_slots,
+                     int max_tiles, const int32_t* __restrict__ cc, int32_t* __restrict__ cnt,
+                     int32_t* __restrict__ off, int32_t* __restrict__ perm,
+                     int32_t* __restrict__ slot_of, int4* __restrict__ tiles,
+                     int32_t* __restrict__ ctrl) {
+  __shared__ int s_base[kMaxRouteExperts];
+  __shared__ int s_wc[kRouteWarps][kMaxRouteExperts / 4];  // per-warp counts, 8 bits each
+  __shared__ int s_warp[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nch = gridDim.x, c = blockIdx.x;
+  const bool writer = c == 0;
+  pdl_wait_prev();     // chunk counts written
+  pdl_launch_next();
+  for (int i = tid; i < kRouteWarps * (kMaxRouteExperts / 4); i += kRouteThreads)
+    (&s_wc[0][0])[i] = 0;
+
+  // expert totals and this chunk's bases: thread t owns expert t (E <= kRouteThreads)
+  int tot = 0, mine = 0;
+  if (tid < E) {
+    for (int q = 0; q < nch; ++q) {
+      const int v = cc[(size_t)q * E + tid];
+      mine += q < c ? v : 0;
+      tot += v;
+    }
+  }
+  int total, ttotal;
+  const int base = block_excl_scan(tot, &total, s_warp);
+  int tbase = block_excl_scan((tot + tile_slots - 1) / tile_slots, &ttotal, s_warp);
+  if (tid < E) {
+    s_base[tid] = base + mine;
+    if (writer) {
+      cnt[tid] = tot;
+      off[tid] = base;
+      for (int p = 0; p < tot; p += tile_slots, ++tbase) {
+        if (tbase < max_tiles)
+          tiles[tbase] = make_int4(tid, base + p, min(tile_slots, tot - p), 0);
+        else
+          set_error(ctrl, kErrTileOverflow);
+      }
+    }
+  }
+  if (writer && tid == 0) {
+    off[E] = total;
+    ctrl[1] = min(ttotal, max_tiles);
+    ctrl[2] = total;
+  }
+  __syncthreads();
+
+  const int f = c * kChunkSlots + tid;
+  const int e = f < Mk ? ids[f] : -1;
+  const bool valid = f < Mk && e >= 0 && e < E;
+  const int key = valid ? e : (E + lane);  // invalid slots never match a valid one
+  const unsigned peers = __match_any_sync(0xffffffffu, key);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (valid && rank == 0) atomicAdd(&s_wc[warp][e >> 2], __popc(peers) << ((e & 3) * 8));
+  __syncthreads();
+  if (f < Mk) {
+    int pos = -1;
+    if (valid) {
+      int before = 0;
+      for (int w = 0; w < warp; ++w) before += (s_wc[w][e >> 2] >> ((e & 3) * 8)) & 0xFF;
+      pos = s_base[e] + before + rank;
+      if (pos < total) {
+        perm[pos] = f;
+      } else {
+        set_error(ctrl, kErrRouteBounds);
+        pos = -1;
+      }
+    }
+    slot_of[f] = pos;
+  }
+}
+
+// MXFP8 quantisation of x into slot order, token by token: a token's row is read and quantised
+// once and its codes stored at the slot position of each of its valid slots (slot_of).  Work
+// items of one warp: 1024 consecutive elements of one token row (four segments of 256).  A lane
+// loads one 16-byte chunk (8 elements) per segment - all four loads issued before any is used -
+// four lanes share a block of 32 and its scale (amax over the group by shuffles), and the 16
+// lanes of a 128-element K tile hand their four scales to one lane, which writes the tile's
+// scale atom row (4 scale bytes, 12 zero bytes) with one 16-byte store.  Codes and scales are
+// those of quantize_block32.  The same launch clears the buffers that the later stages
+// accumulate into.
+constexpr int kActqSegs = 4;
+
+__global__ void __launch_bounds__(256)
+actq_rows_kernel(const __nv_bfloat16* __restrict__ x, int M, int H, int topk,
+                 const int32_t* __restrict__ slot_of, uint8_t* __restrict__ xq,
+                 uint8_t* __restrict__ xs, uint8_t* __restrict__ xs16, int r16, ZeroRegion z0,
+                 ZeroRegion z1, ZeroRegion z2) {
+  pdl_wait_prev();
+  pdl_launch_next();
+  const int lane = threadIdx.x & 31;
+  const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t gsz = (size_t)gridDim.x * blockDim.x;
+  const int nb = H / 32, nc = H / 8;           // blocks, 16-byte chunks per row (nc % 16 == 0)
+  const int per_row = (nc + 32 * kActqSegs - 1) / (32 * kActqSegs);   // work items per row
+  const size_t items = (size_t)M * per_row;
+  for (size_t it = gtid >> 5; it < items; it += gsz >> 5) {
+    const size_t t = it / per_row;
+    const int c0 = (int)(it - t * per_row) * 32 * kActqSegs;
+    // slot positions of the token's top-k slots (-1: dropped), lane j holding slot j
+    const int mypos = lane < topk ? slot_of[t * topk + lane] : -1;
+    if (!__any_sync(0xffffffffu, mypos >= 0)) continue;   // padding row
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
+    uint4 u[kActqSegs];
+#pragma unroll
+    for (int k = 0; k < kActqSegs; ++k) {
+      const int c = c0 + 32 * k + lane;
+      u[k] = c < nc ? src[c] : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < kActqSegs; ++k) {
+      const int c = c0 + 32 * k + lane;
+      const bool in = c < nc;                  // uniform per 16-lane half
+      const uint32_t w[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[2 * j] = __uint_as_float(w[j] << 16);
+        v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      const uint32_t sc = mx_scale_byte(amax);
+      const float inv = e8m0_inv_f32(sc);
+      uint32_t q[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        q[h] = f32_to_e4m3(v[4 * h] * inv) | (f32_to_e4m3(v[4 * h + 1] * inv) << 8) |
+               (f32_to_e4m3(v[4 * h + 2] * inv) << 16) | (f32_to_e4m3(v[4 * h + 3] * inv) << 24);
+      const int g = lane & ~15;                // first lane of this K tile's 16
+      const uint32_t atom = __shfl_sync(0xffffffffu, sc, g) |
+                            (__shfl_sync(0xffffffffu, sc, g + 4) << 8) |
+                            (__shfl_sync(0xffffffffu, sc, g + 8) << 16) |
+                            (__shfl_sync(0xffffffffu, sc, g + 12) << 24);
+      for (int j = 0; j < topk; ++j) {
+        const int p = __shfl_sync(0xffffffffu, mypos, j);
+        if (p < 0 || !in) continue;
+        reinterpret_cast<uint2*>(xq + (size_t)p * H)[c] = make_uint2(q[0], q[1]);
+        if ((c & 3) == 0) xs[(size_t)p * nb + (c >> 2)] = (uint8_t)sc;
+        if ((c & 15) == 0)
+          *reinterpret_cast<uint4*>(xs16 + ((size_t)(c >> 4) * r16 + p) * 16) =
+              make_uint4(atom, 0u, 0u, 0u);
+      }
+    }
+  }
+  const ZeroRegion zs[3] = {z0, z1, z2};
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    if (zs[r].ptr == nullptr) continue;
+    uint4* a4 = reinterpret_cast<uint4*>(zs[r].ptr);
+    for (size_t i = gtid; i < zs[r].words / 4; i += gsz) a4[i] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+int route_chunks(int Mk) { return (Mk + kChunkSlots - 1) / kChunkSlots; }
+
+cudaError_t launch_route_count(const int32_t* ids, int Mk, int E, const RunPtrs& r,
+                               cudaStream_t st) {
+  static_assert(kMaxRouteExperts <= kRouteThreads, "one expert per thread");
+  if (E > kMaxRouteExperts || Mk < 1) return cudaErrorInvalidValue;
+  // first kernel of a call: an ordinary launch (the previous call may still read the tables)
+  return launch_kernel(route_count_kernel, dim3(route_chunks(Mk)), dim3(kRouteThreads), 0, st,
+                       false, ids, Mk, E, r.ctrl, r.rcc);
+}
+
+cudaError_t launch_route_scatter(const int32_t* ids, int Mk, int E, int tile_slots,
+                                 int max_tiles, const RunPtrs& r, cudaStream_t st) {
+  if (E > kMaxRouteExperts || Mk < 1) return cudaErrorInvalidValue;
+  return launch_kernel(route_scatter_kernel, dim3(route_chunks(Mk)), dim3(kRouteThreads), 0, st,
+                       true, ids, Mk, E, tile_slots, max_tiles,
+                       static_cast<const int32_t*>(r.rcc), r.cnt, r.off, r.perm, r.slot_of,
+                       r.tiles, r.ctrl);
+}
+
+cudaError_t launch_actq_rows(const void* x, int M, int H, int topk, const RunPtrs& r, void* z0,
+                             size_t z0_words, void* z1, size_t z1_words, void* z2,
+                             size_t z2_words, cudaStream_t st) {
+  if (H % 128 != 0) return cudaErrorInvalidValue;
+  // a warp per 1024 elements of a token row; zeroing in 16-byte words
+  if (topk > 32) return cudaErrorInvalidValue;
+  const size_t items = (size_t)M * ((H / 8 + 32 * kActqSegs - 1) / (32 * kActqSegs));
+  const size_t work = std::max(items * 32,
+                               std::max(z0_words / 4, std::max(z1_words / 4, z2_words / 4)));
+  const int blocks = (int)std::max<size_t>(1, std::min<size_t>((work + 255) / 256, 152 * 8));
+  return launch_kernel(actq_rows_kernel, dim3(blocks), dim3(256), 0, st, true,
+                       reinterpret_cast<const __nv_bfloat16*>(x), M, H, topk,
+                       static_cast<const int32_t*>(r.slot_of), r.xq, r.xs, r.xs16, r.r16,
+                       ZeroRegion{z0, z0_words},
+                       ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words});
+}
+
 bool route_actq_small_supported(int Mk, int E) {
   return Mk <= kSmallRouteSlots && E <= kMaxRouteExperts;
 }
