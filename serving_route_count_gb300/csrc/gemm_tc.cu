@@ -295,11 +295,16 @@ __global__ void __launch_bounds__(kTcThreads)
 fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::kStages2;
-  pdl_wait_prev();     // previous kernel of the call complete, its writes visible
   pdl_launch_next();
+  // The routing tables were complete before fc1 let this kernel launch (fc1 waits for the
+  // routing launch first), so the tile and the weights of the first stages are read before
+  // waiting for fc1's output (L2 reads: nothing of them is in this SM's L1).
   const int tile = blockIdx.x;
-  if (tile >= p.ctrl[1]) return;
-  const int4 td = p.tiles[tile];
+  if (tile >= __ldcg(&p.ctrl[1])) {
+    pdl_wait_prev();
+    return;
+  }
+  const int4 td = __ldcg(&p.tiles[tile]);
   const int e = td.x, p0 = td.y, n = td.z;
   const TileLoad<BN> tl(n);
   const int rt = blockIdx.y;
@@ -339,27 +344,41 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
   auto stage = [&](int s) { return smem + s * Cfg::kStage2; };
   // stage layout: A | B | SFA | SFB
 
-  if (warp == 0) {
-    if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
-      int i = 0;
-      for (; i < nk && ok; ++i) {
-        const int s = i % S;
-        if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
-        if (!ok) break;
-        uint8_t* st = stage(s);
-        mbar_arrive_expect_tx(&full[s], kTxBytesA + tl.b_bytes + 512 + tl.sf_bytes);
-        tma_load_3d_hint(st, &p.tm_w2, 0, 0, (int)(((size_t)e * (p.H / 128) + rt) * p.KT + i),
-                         &full[s], pol);
-        tl.load_b(st + kTileBytesA, &p.tm_h, i * 128, p0, &full[s]);
-        const size_t a = ((size_t)e * (p.H / 128) + rt) * p.KT + i;
-        bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
-        bulk_load(st + kTileBytesA + Cfg::kB + 512, p.hs16 + ((size_t)i * p.r16 + p0) * 16,
-                  tl.sf_bytes, &full[s]);
-      }
-      issued = i;
+  if (warp == 0 && lane == 0) {
+    const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
+    const int pre = nk < S ? nk : S;
+    // weights of the first stages, before fc1 completes: the stage's barrier expects their
+    // bytes now and is arrived on once the activation part is issued too
+    for (int i = 0; i < pre; ++i) {
+      const size_t a = ((size_t)e * (p.H / 128) + rt) * p.KT + i;
+      mbar_expect_tx(&full[i], kTxBytesA + 512);
+      tma_load_3d_hint(stage(i), &p.tm_w2, 0, 0, (int)a, &full[i], pol);
+      bulk_load(stage(i) + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[i]);
     }
-  } else if (warp == 1) {
+    pdl_wait_prev();     // fc1 complete, h visible
+    int i = 0;
+    for (; i < nk && ok; ++i) {
+      const int s = i % S;
+      if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
+      if (!ok) break;
+      uint8_t* st = stage(s);
+      if (i < pre) {
+        mbar_arrive_expect_tx(&full[s], tl.b_bytes + tl.sf_bytes);
+      } else {
+        const size_t a = ((size_t)e * (p.H / 128) + rt) * p.KT + i;
+        mbar_arrive_expect_tx(&full[s], kTxBytesA + tl.b_bytes + 512 + tl.sf_bytes);
+        tma_load_3d_hint(st, &p.tm_w2, 0, 0, (int)a, &full[s], pol);
+        bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
+      }
+      tl.load_b(st + kTileBytesA, &p.tm_h, i * 128, p0, &full[s]);
+      bulk_load(st + kTileBytesA + Cfg::kB + 512, p.hs16 + ((size_t)i * p.r16 + p0) * 16,
+                tl.sf_bytes, &full[s]);
+    }
+    issued = i;
+  } else {
+    pdl_wait_prev();     // previous kernels of the call complete
+  }
+  if (warp == 1) {
     if (lane == 0) {
       for (int i = 0; i < nk && ok; ++i) {
         const int s = i % S;

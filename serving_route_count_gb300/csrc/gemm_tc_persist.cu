@@ -383,13 +383,18 @@ __global__ void __launch_bounds__(kStreamThreads)
 fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
   using Cfg = PersistFc2Cfg<BN>;
   constexpr int S = Cfg::kStages;
-  pdl_wait_prev();     // previous kernel of the call complete, its writes visible
   pdl_launch_next();
+  // The routing tables were complete before fc1 let this kernel launch (fc1 waits for the
+  // routing launch first): the unit range and the weights of the first stages are read before
+  // waiting for fc1's output (L2 reads: nothing of them is in this SM's L1).
   const int G = gridDim.x, c = blockIdx.x;
-  const int units = p.ctrl[1] * p.RB;
+  const int units = __ldcg(&p.ctrl[1]) * p.RB;
   const int u_begin = (int)((long long)c * units / G);
   const int u_end = (int)((long long)(c + 1) * units / G);
-  if (u_begin >= u_end) return;
+  if (u_begin >= u_end) {
+    pdl_wait_prev();
+    return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   extern __shared__ uint8_t smem_raw[];
@@ -431,37 +436,56 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
   auto stage = [&](int s) { return smem + s * Cfg::kStage; };
   // stage layout: A | B | SFA | SFB
 
-  if (warp == 0) {
-    if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
-      int i = 0, cur_tile = -1, e = 0, p0 = 0;
-      TileLoad<BN> tl(BN);
-      for (int u = u_begin; u < u_end && ok; ++u) {
-        const int tile = u / p.RB, rb = u - tile * p.RB;
-        if (tile != cur_tile) {
-          cur_tile = tile;
-          const int4 td = p.tiles[tile];
-          e = td.x;
-          p0 = td.y;
-          tl = TileLoad<BN>(td.z);
-        }
-        for (int kt = 0; kt < p.KT && ok; ++kt, ++i) {
-          const int s = i % S;
-          if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
-          if (!ok) break;
-          uint8_t* st = stage(s);
+  if (warp == 0 && lane == 0) {
+    const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
+    const int fills = (u_end - u_begin) * p.KT;
+    const int pre = fills < S ? fills : S;
+    // weights of the first stages, before fc1 completes: the stage's barrier expects their
+    // bytes now and is arrived on once the activation part is issued too
+    for (int i = 0; i < pre; ++i) {
+      const int u = u_begin + i / p.KT, kt = i % p.KT;
+      const int tile = u / p.RB, rb = u - tile * p.RB;
+      const int e = __ldcg(reinterpret_cast<const int*>(p.tiles + tile));
+      const size_t a = ((size_t)e * p.RB + rb) * p.KT + kt;
+      mbar_expect_tx(&full[i], kTxBytesA + 512);
+      tma_load_3d_hint(stage(i), &p.tm_w2, 0, 0, (int)a, &full[i], pol);
+      bulk_load(stage(i) + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[i]);
+    }
+    pdl_wait_prev();     // fc1 complete, h visible
+    int i = 0, cur_tile = -1, e = 0, p0 = 0;
+    TileLoad<BN> tl(BN);
+    for (int u = u_begin; u < u_end && ok; ++u) {
+      const int tile = u / p.RB, rb = u - tile * p.RB;
+      if (tile != cur_tile) {
+        cur_tile = tile;
+        const int4 td = p.tiles[tile];
+        e = td.x;
+        p0 = td.y;
+        tl = TileLoad<BN>(td.z);
+      }
+      for (int kt = 0; kt < p.KT && ok; ++kt, ++i) {
+        const int s = i % S;
+        if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
+        if (!ok) break;
+        uint8_t* st = stage(s);
+        if (i < pre) {
+          mbar_arrive_expect_tx(&full[s], tl.b_bytes + tl.sf_bytes);
+        } else {
           const size_t a = ((size_t)e * p.RB + rb) * p.KT + kt;
           mbar_arrive_expect_tx(&full[s], kTxBytesA + tl.b_bytes + 512 + tl.sf_bytes);
           tma_load_3d_hint(st, &p.tm_w2, 0, 0, (int)a, &full[s], pol);
-          tl.load_b(st + kTileBytesA, &p.tm_h, kt * 128, p0, &full[s]);
           bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
-          bulk_load(st + kTileBytesA + Cfg::kB + 512, p.hs16 + ((size_t)kt * p.r16 + p0) * 16,
-                    tl.sf_bytes, &full[s]);
         }
+        tl.load_b(st + kTileBytesA, &p.tm_h, kt * 128, p0, &full[s]);
+        bulk_load(st + kTileBytesA + Cfg::kB + 512, p.hs16 + ((size_t)kt * p.r16 + p0) * 16,
+                  tl.sf_bytes, &full[s]);
       }
-      issued = i;
     }
-  } else if (warp == 1) {
+    issued = i;
+  } else {
+    pdl_wait_prev();     // previous kernels of the call complete
+  }
+  if (warp == 1) {
     if (lane == 0) {
       int i = 0, j = 0, cur_tile = -1;
       TileLoad<BN> tl(BN);
