@@ -33,13 +33,14 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int tile_
 // gemm_tc.cu
 cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                             int bn, int tiles, int splits, const float* topk_w, int M,
-                            cudaStream_t st);
+                            const int32_t* ids, int max_tiles, cudaStream_t st);
 int tc_pick_bn(int M, int topk, int E, bool w4a8);
 // gemm_tc_persist.cu
 bool fc1_stream_preferred(int bn, int units);
 size_t fc1_stream_part_bytes();
 cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanDims& d, int bn,
-                              int M, float* part, int32_t* tickets, cudaStream_t st);
+                              int M, float* part, int32_t* tickets, const int32_t* ids,
+                              int max_tiles, cudaStream_t st);
 bool fc2_persist_preferred(int bn, int units);
 cudaError_t launch_fc2_persist(const DevWeights& w, const RunPtrs& r, const PlanDims& d, int bn,
                                int M, const float* topk_w, cudaStream_t st);
@@ -543,16 +544,17 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   prof(2);
   if (tc) {
     if (streamk)
-      e = launch_fc1_stream(w, r, d, bn, M, r.part, r.tickets, st);
+      e = launch_fc1_stream(w, r, d, bn, M, r.part, r.tickets, topk_ids, plan->s.max_tiles, st);
     else
-      e = tc8 ? launch_tc_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st)
+      e = tc8 ? launch_tc_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, topk_ids,
+                                plan->s.max_tiles, st)
               : launch_tc16_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(3);
     if (tc8 && fc2_persist_preferred(bn, tiles * (d.H / 128)))
       e = launch_fc2_persist(w, r, d, bn, M, topk_weights, st);
     else
-      e = tc8 ? launch_tc_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st)
+      e = tc8 ? launch_tc_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, nullptr, 0, st)
               : launch_tc16_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(4);

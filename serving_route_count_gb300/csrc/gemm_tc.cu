@@ -77,6 +77,10 @@ struct TcFc1Params {
   int RTf, rem;              // full 128-row weight tiles per half, rows of the partial tile
   int fb_in_x;               // grid (RT, tiles, splits) instead of (tiles, RT, splits)
   float limit, alpha, beta;
+  // small calls (Mk <= kPreRouteSlots): the router ids, to route in shared memory ahead of the
+  // routing launch (null: wait for its tables)
+  const int32_t* ids;
+  int Mk, E, max_tiles;
 };
 
 struct TcFc2Params {
@@ -100,16 +104,11 @@ __global__ void __launch_bounds__(kTcThreads)
 fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::kStages1;
-  pdl_wait_prev();     // previous kernel of the call complete, its writes visible
   pdl_launch_next();
   // the row blocks of a tile are adjacent in launch order (while the tiles fit the grid's y),
   // so the CTAs that read the same activation tile run together and share it through L2
   const int tile = p.fb_in_x ? blockIdx.y : blockIdx.x;
   const int fb = p.fb_in_x ? blockIdx.x : blockIdx.y, split = blockIdx.z;
-  if (tile >= p.ctrl[1]) return;
-  const int4 td = p.tiles[tile];
-  const int e = td.x, p0 = td.y, n = td.z;
-  const TileLoad<BN> tl(n);
   const int kt0 = split * p.KT / p.splits, kt1 = (split + 1) * p.KT / p.splits;
   const int nk = kt1 - kt0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -120,6 +119,23 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   __shared__ __align__(8) uint64_t full[S], empty[S], done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_last, s_fail;
+
+  // Small calls route in shared memory (scratch in the last stage, before any copy lands
+  // there), so the weights of the first stages are requested while the routing launch still
+  // runs; larger calls wait for its tables.
+  int e_pre = -1;
+  if (p.ids != nullptr) {
+    int* scratch = reinterpret_cast<int*>(smem + (S - 1) * Cfg::kStage1);
+    const int nt = min(pre_route_tiles<kTcThreads>(p.ids, p.Mk, p.E, BN, scratch), p.max_tiles);
+    if (tile >= nt) {
+      pdl_wait_prev();
+      return;
+    }
+    if (tile < kPreRouteTiles) e_pre = scratch[p.E + tile];
+  } else {
+    pdl_wait_prev();     // routing tables complete
+    if (tile >= p.ctrl[1]) return;
+  }
 
   if (warp == 0) {
     tmem_alloc(&s_tmem, Cfg::kAlloc1);
@@ -144,6 +160,39 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   int issued = 0;                                   // stages filled by the TMA producer
   auto stage = [&](int s) { return smem + s * Cfg::kStage1; };
   // stage layout: A_up | A_gate | B | SFA_up | SFA_gate | SFB
+  const uint32_t a_bytes = fb < p.RTf ? 2 * kTxBytesA : 2 * p.rem * 64;
+  // the weight part of a stage: both halves' codes and scale atoms of K tile kt of expert ex
+  auto load_a = [&](uint8_t* st, int ex, int kt, uint64_t* bar, uint64_t pol) {
+    if (fb < p.RTf) {
+      tma_load_3d_hint(st, &p.tm_w13, 0, 0, ((2 * ex) * p.RTf + fb) * p.KT + kt, bar, pol);
+      tma_load_3d_hint(st + kTileBytesA, &p.tm_w13, 0, 0,
+                       ((2 * ex + 1) * p.RTf + fb) * p.KT + kt, bar, pol);
+    } else {
+      // partial row tile: rows >= I % 128 of the smem tile keep stale (finite) codes; their
+      // accumulator rows are never read
+      tma_load_3d_hint(st, &p.tm_w13_tail, 0, 0, (2 * ex) * p.KT + kt, bar, pol);
+      tma_load_3d_hint(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * ex + 1) * p.KT + kt, bar,
+                       pol);
+    }
+    const size_t a_up = ((size_t)(2 * ex) * p.RT + fb) * p.KT + kt;
+    const size_t a_gt = ((size_t)(2 * ex + 1) * p.RT + fb) * p.KT + kt;
+    bulk_load(st + 2 * kTileBytesA + Cfg::kB, p.sf13 + a_up * 512, 512, bar);
+    bulk_load(st + 2 * kTileBytesA + Cfg::kB + 512, p.sf13 + a_gt * 512, 512, bar);
+  };
+  int pre = 0;                 // stages whose weights were requested before the wait
+  if (warp == 0 && lane == 0 && e_pre >= 0) {
+    const uint64_t pol = l2_evict_first_policy();
+    pre = nk < S ? nk : S;
+    for (int i = 0; i < pre; ++i) {
+      mbar_expect_tx(&full[i], a_bytes + 2 * 512);
+      load_a(stage(i), e_pre, kt0 + i, &full[i], pol);
+    }
+  }
+  pdl_wait_prev();             // routing tables and activations complete
+  const int4 td = p.tiles[tile];
+  const int e = td.x, p0 = td.y, n = td.z;
+  const TileLoad<BN> tl(n);
+  if (pre > 0 && e != e_pre) set_error(p.err, kErrRouteBounds);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -155,26 +204,13 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
         if (!ok) break;
         uint8_t* st = stage(s);
         const int kt = kt0 + i;
-        if (fb < p.RTf) {
-          mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + tl.b_bytes + 2 * 512 + tl.sf_bytes);
-          tma_load_3d_hint(st, &p.tm_w13, 0, 0, ((2 * e) * p.RTf + fb) * p.KT + kt, &full[s],
-                           pol);
-          tma_load_3d_hint(st + kTileBytesA, &p.tm_w13, 0, 0,
-                           ((2 * e + 1) * p.RTf + fb) * p.KT + kt,
-                      &full[s], pol);
+        if (i < pre) {
+          mbar_arrive_expect_tx(&full[s], tl.b_bytes + tl.sf_bytes);
         } else {
-          // partial row tile: rows >= I % 128 of the smem tile keep stale (finite) codes; their
-          // accumulator rows are never read
-          mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + tl.b_bytes + 2 * 512 + tl.sf_bytes);
-          tma_load_3d_hint(st, &p.tm_w13_tail, 0, 0, (2 * e) * p.KT + kt, &full[s], pol);
-          tma_load_3d_hint(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * e + 1) * p.KT + kt,
-                           &full[s], pol);
+          mbar_arrive_expect_tx(&full[s], a_bytes + tl.b_bytes + 2 * 512 + tl.sf_bytes);
+          load_a(st, e, kt, &full[s], pol);
         }
         tl.load_b(st + 2 * kTileBytesA, &p.tm_x, kt * 128, p0, &full[s]);
-        const size_t a_up = ((size_t)(2 * e) * p.RT + fb) * p.KT + kt;
-        const size_t a_gt = ((size_t)(2 * e + 1) * p.RT + fb) * p.KT + kt;
-        bulk_load(st + 2 * kTileBytesA + Cfg::kB, p.sf13 + a_up * 512, 512, &full[s]);
-        bulk_load(st + 2 * kTileBytesA + Cfg::kB + 512, p.sf13 + a_gt * 512, 512, &full[s]);
         // activation-scale atom: the tile's prepared atom rows
         bulk_load(st + 2 * kTileBytesA + Cfg::kB + 1024, p.xs16 + ((size_t)kt * p.r16 + p0) * 16,
                   tl.sf_bytes, &full[s]);
@@ -541,7 +577,7 @@ static cudaError_t launch_fc2_bn(const TcFc2Params& p, int tiles, cudaStream_t s
 // fc1 (stage 0) or fc2 (stage 1) of the W4A8 tensor-core path.
 cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                             int bn, int tiles, int splits, const float* topk_w, int M,
-                            cudaStream_t st) {
+                            const int32_t* ids, int max_tiles, cudaStream_t st) {
   const int Sm = M * d.topk;
   const int RT = cdiv(d.I, 128);
   if (stage == 0) {
@@ -559,6 +595,8 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
     p.xs16 = r.xs16; p.hs16 = r.hs16; p.r16 = r.r16;
     p.H = d.H; p.I = d.I; p.Ip = d.Ip; p.RT = RT; p.KT = d.H / 128; p.Sm = Sm;
     p.splits = splits; p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
+    p.ids = (ids != nullptr && Sm <= kPreRouteSlots) ? ids : nullptr;
+    p.Mk = Sm; p.E = d.E; p.max_tiles = max_tiles;
     switch (bn) {
       case 16: return launch_fc1_bn<16>(p, tiles, st);
       case 32: return launch_fc1_bn<32>(p, tiles, st);

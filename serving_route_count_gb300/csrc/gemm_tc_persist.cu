@@ -59,6 +59,10 @@ struct StreamFc1Params {
   int32_t* tickets;          // [units] K tiles completed
   int H, I, Ip, RT, KT, Sm, RTf, rem;
   float limit, alpha, beta;
+  // small calls (Mk <= kPreRouteSlots): the router ids, to route in shared memory ahead of the
+  // routing launch (null: wait for its tables)
+  const int32_t* ids;
+  int Mk, E, max_tiles;
 };
 
 // Work of one CTA (G CTAs, U units of KT K steps).  With D = floor(U / G) full waves, the units
@@ -127,19 +131,44 @@ __global__ void __launch_bounds__(kStreamThreads)
 fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   using Cfg = StreamCfg<BN>;
   constexpr int S = Cfg::kStages;
-  pdl_wait_prev();     // previous kernel of the call complete, its writes visible
   pdl_launch_next();
-  StreamWork wk;
-  wk.init(p.ctrl[1] * p.RT, p.KT, gridDim.x, blockIdx.x);
-  if (wk.nsteps <= 0) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[S], empty[S], acc_full[2], acc_empty[2], drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_last, s_fail;
+
+  // Small calls route in shared memory (scratch in the last stage, before any copy lands
+  // there), so the weights of the first stages are requested while the routing launch still
+  // runs; larger calls wait for its tables.
+  int* scratch = reinterpret_cast<int*>(smem + (S - 1) * Cfg::kStage);
+  int n_tiles;
+  if (p.ids != nullptr) {
+    n_tiles = min(pre_route_tiles<kStreamThreads>(p.ids, p.Mk, p.E, BN, scratch), p.max_tiles);
+  } else {
+    pdl_wait_prev();     // routing tables complete
+    n_tiles = p.ctrl[1];
+  }
+  StreamWork wk;
+  wk.init(n_tiles * p.RT, p.KT, gridDim.x, blockIdx.x);
+  if (wk.nsteps <= 0) {
+    pdl_wait_prev();
+    return;
+  }
+  // experts of the first stages' units (read before the producer's copies reach the scratch)
+  int pre_e[S];
+  int pre = 0;
+  if (p.ids != nullptr && warp == 0 && lane == 0) {
+    auto sg = wk.segs();
+    int u, k0, len;
+    while (pre < S && sg.next(u, k0, len)) {
+      const int tile = u / p.RT;
+      const int ex = tile < kPreRouteTiles ? scratch[p.E + tile] : -1;
+      for (int kt = k0; kt < k0 + len && pre < S; ++kt) pre_e[pre++] = ex;
+    }
+  }
 
   if (warp == 0) {
     tmem_alloc(&s_tmem, Cfg::kAlloc);
@@ -168,6 +197,46 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   int issued = 0;                                   // stages filled by the TMA producer
   auto stage = [&](int s) { return smem + s * Cfg::kStage; };
 
+  // the weight part of a stage: both halves' codes and scale atoms of K tile kt, row block fb
+  // of expert ex; returns its byte count
+  auto load_a = [&](uint8_t* st, int ex, int fb, int kt, uint64_t* bar, uint64_t pol,
+                    bool expect_only) -> uint32_t {
+    const uint32_t bytes = (fb < p.RTf ? 2 * kTxBytesA : 2 * p.rem * 64) + 2 * 512;
+    if (expect_only) mbar_expect_tx(bar, bytes);
+    if (fb < p.RTf) {
+      tma_load_3d_hint(st, &p.tm_w13, 0, 0, ((2 * ex) * p.RTf + fb) * p.KT + kt, bar, pol);
+      tma_load_3d_hint(st + kTileBytesA, &p.tm_w13, 0, 0,
+                       ((2 * ex + 1) * p.RTf + fb) * p.KT + kt, bar, pol);
+    } else {
+      tma_load_3d_hint(st, &p.tm_w13_tail, 0, 0, (2 * ex) * p.KT + kt, bar, pol);
+      tma_load_3d_hint(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * ex + 1) * p.KT + kt, bar,
+                       pol);
+    }
+    const size_t a_up = ((size_t)(2 * ex) * p.RT + fb) * p.KT + kt;
+    const size_t a_gt = ((size_t)(2 * ex + 1) * p.RT + fb) * p.KT + kt;
+    bulk_load(st + 2 * kTileBytesA + Cfg::kB, p.sf13 + a_up * 512, 512, bar);
+    bulk_load(st + 2 * kTileBytesA + Cfg::kB + 512, p.sf13 + a_gt * 512, 512, bar);
+    return bytes;
+  };
+  if (warp == 0 && lane == 0 && pre > 0) {
+    // weights of the first stages, before the routing launch completes; the stage barriers
+    // expect their bytes now and are arrived on once the activation part is issued too
+    const uint64_t pol = l2_evict_first_policy();
+    auto sg = wk.segs();
+    int u, k0, len, i = 0;
+    while (i < pre && sg.next(u, k0, len)) {
+      const int fb = u % p.RT;
+      for (int kt = k0; kt < k0 + len && i < pre; ++kt, ++i) {
+        if (pre_e[i] < 0) {   // tile beyond the shared-memory table: no early request
+          pre = i;
+          break;
+        }
+        load_a(stage(i), pre_e[i], fb, kt, &full[i], pol, true);
+      }
+    }
+  }
+  pdl_wait_prev();     // routing tables and activations complete
+
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
@@ -187,23 +256,16 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
           if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
           if (!ok) break;
           uint8_t* st = stage(s);
-          if (fb < p.RTf) {
-            mbar_arrive_expect_tx(&full[s], 2 * kTxBytesA + Cfg::kB + 2 * 512 + BN * 16);
-            tma_load_3d_hint(st, &p.tm_w13, 0, 0, ((2 * e) * p.RTf + fb) * p.KT + kt, &full[s],
-                             pol);
-            tma_load_3d_hint(st + kTileBytesA, &p.tm_w13, 0, 0,
-                        ((2 * e + 1) * p.RTf + fb) * p.KT + kt, &full[s], pol);
+          if (i < pre) {
+            if (pre_e[i] != e) set_error(p.err, kErrRouteBounds);
+            mbar_arrive_expect_tx(&full[s], Cfg::kB + BN * 16);
           } else {
-            mbar_arrive_expect_tx(&full[s], 2 * p.rem * 64 + Cfg::kB + 2 * 512 + BN * 16);
-            tma_load_3d_hint(st, &p.tm_w13_tail, 0, 0, (2 * e) * p.KT + kt, &full[s], pol);
-            tma_load_3d_hint(st + kTileBytesA, &p.tm_w13_tail, 0, 0, (2 * e + 1) * p.KT + kt,
-                        &full[s], pol);
+            const uint32_t ab =
+                (fb < p.RTf ? 2 * kTxBytesA : 2 * p.rem * 64) + 2 * 512;
+            mbar_arrive_expect_tx(&full[s], ab + Cfg::kB + BN * 16);
+            load_a(st, e, fb, kt, &full[s], pol, false);
           }
           tma_load_2d(st + 2 * kTileBytesA, &p.tm_x, kt * 128, p0, &full[s]);
-          const size_t a_up = ((size_t)(2 * e) * p.RT + fb) * p.KT + kt;
-          const size_t a_gt = ((size_t)(2 * e + 1) * p.RT + fb) * p.KT + kt;
-          bulk_load(st + 2 * kTileBytesA + Cfg::kB, p.sf13 + a_up * 512, 512, &full[s]);
-          bulk_load(st + 2 * kTileBytesA + Cfg::kB + 512, p.sf13 + a_gt * 512, 512, &full[s]);
           // activation-scale atom: the tile's prepared atom rows, one bulk copy
           bulk_load(st + 2 * kTileBytesA + Cfg::kB + 1024,
                     p.xs16 + ((size_t)kt * p.r16 + p0) * 16, BN * 16, &full[s]);
@@ -648,7 +710,8 @@ bool fc1_stream_preferred(int bn, int units) {
 size_t fc1_stream_part_bytes() { return (size_t)2 * kStreamMaxCtas * 2 * 16 * 128 * 4; }
 
 cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanDims& d, int bn,
-                              int M, float* part, int32_t* tickets, cudaStream_t st) {
+                              int M, float* part, int32_t* tickets, const int32_t* ids,
+                              int max_tiles, cudaStream_t st) {
   if (bn != 16) return cudaErrorInvalidValue;
   StreamFc1Params p;
   memset(&p, 0, sizeof(p));
@@ -666,6 +729,8 @@ cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanD
   p.hq = r.hq; p.hs = r.hs; p.part = part; p.tickets = tickets;
   p.H = d.H; p.I = d.I; p.Ip = d.Ip; p.RT = cdiv(d.I, 128); p.KT = d.H / 128; p.Sm = Sm;
   p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
+  p.ids = (ids != nullptr && Sm <= kPreRouteSlots) ? ids : nullptr;
+  p.Mk = Sm; p.E = d.E; p.max_tiles = max_tiles;
   static const int G = persistent_grid(fc1_stream_kernel<16>, StreamCfg<16>::kSmem,
                                        StreamCfg<16>::kAlloc, 2, kStreamMaxCtas);
   return launch_kernel(fc1_stream_kernel<16>, dim3(G), dim3(kStreamThreads), StreamCfg<16>::kSmem,

@@ -71,6 +71,63 @@ static __device__ __forceinline__ void write_act_sf_rows(uint8_t* dst, const uin
     *reinterpret_cast<uint32_t*>(dst + (n & 31) * 16 + (n >> 5) * 4) = rows[n];
 }
 
+// Routing of a small call in shared memory, ahead of the routing launch's tables: the experts
+// of the GEMM tile list, built as the routing launch builds it (experts in ascending order,
+// ceil(count / tile_slots) tiles each; ids outside [0, E) dropped), from the router ids alone.
+// A kernel chained behind the routing launch may read the ids before waiting for it (the ids
+// were complete when the routing launch passed its own wait), so it can request weights early.
+// scratch: (E + kPreRouteTiles + 32) ints of shared memory; on return scratch[E + t] is the
+// expert of tile t for t < min(tiles, kPreRouteTiles).  Every thread of the CTA (NT threads)
+// calls it; returns the tile count.
+constexpr int kPreRouteSlots = 256;   // calls of at most this many flat slots
+constexpr int kPreRouteTiles = 256;
+template <int NT>
+static __device__ int pre_route_tiles(const int32_t* ids, int Mk, int E, int tile_slots,
+                                      int* scratch) {
+  int* s_cnt = scratch;
+  int* s_tile_e = scratch + E;
+  int* s_red = scratch + E + kPreRouteTiles;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += NT) s_cnt[e] = 0;
+  __syncthreads();
+  for (int f = tid; f < Mk; f += NT) {
+    const int e = __ldcg(ids + f);
+    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  const int per = (E + NT - 1) / NT;        // thread t: experts [t*per, t*per + per)
+  int lt = 0;
+  for (int i = 0; i < per; ++i) {
+    const int e = tid * per + i;
+    if (e < E) lt += (s_cnt[e] + tile_slots - 1) / tile_slots;
+  }
+  // exclusive scan of the per-thread tile counts
+  int incl = lt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_red[warp] = incl;
+  __syncthreads();
+  int before = 0, total = 0;
+  for (int w = 0; w < NT / 32; ++w) {
+    before += w < warp ? s_red[w] : 0;
+    total += s_red[w];
+  }
+  int t = before + incl - lt;
+  for (int i = 0; i < per; ++i) {
+    const int e = tid * per + i;
+    if (e >= E) break;
+    for (int c = s_cnt[e]; c > 0; c -= tile_slots, ++t)
+      if (t < kPreRouteTiles) s_tile_e[t] = e;
+  }
+  // the scratch lies in a pipeline stage that TMA writes next
+  fence_proxy_async_smem();
+  __syncthreads();
+  return total;
+}
+
 static __device__ __forceinline__ float swiglu(float gate, float up, float limit, float alpha,
                                                float beta) {
   const float g = fminf(gate, limit);
