@@ -226,6 +226,26 @@ def test_prefill_full_size_sampled(decode_layer, cfg_name, M, det):
     layer.close()
 
 
+@pytest.mark.parametrize("M,det", [(16, 0), (512, 1)])
+def test_prefill_ep_i1152_sampled(M, det):
+    """The expert-parallel slice of the prefill config: E=192 local experts of 384, H=7168,
+    I=1152 (nine full 128-row weight blocks per half), ids drawn over 384 experts with the
+    foreign ones masked (weight 0, local id): routing bit-exact, sampled rows against the
+    oracle."""
+    cfg = S.CONFIGS["prefill_w4a8_ep_i1152"]
+    ck = S.make_checkpoint(cfg)
+    x, ids, w = S.make_inputs(cfg, M)
+    layer = _layer(ck, cfg.topk, M, cfg.swiglu_limit, det)
+    got = run_layer(layer, x, ids, w)
+    st, code = layer.device_error()
+    assert st == 0 and code == 0, code
+    route = O.route(ids, cfg.E)
+    for a, b in zip(layer.routing(M), route):
+        assert np.array_equal(a, b)
+    check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=[0, M // 3, M - 1])
+    layer.close()
+
+
 def test_nvfp4_full_size_sampled():
     cfg = S.CONFIGS["w4a16_nvfp4"]
     ck = S.make_checkpoint(cfg)
