@@ -53,6 +53,8 @@ def parse():
     p.add_argument("--profile", type=int, default=0, metavar="M",
                    help="profiling case: eager layer calls at decode size M (no timing)")
     p.add_argument("--profile-calls", type=int, default=4)
+    p.add_argument("--profile-cfg", default="",
+                   help="profiling case of another synthetic config (e.g. w4a16_nvfp4)")
     p.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--sample-m", type=str, default="1,2", help=argparse.SUPPRESS)
     return p.parse_args()
@@ -248,10 +250,10 @@ def profile_case(args):
 
     from serving_route_count_gb300 import MoELayer, build
     build.build()
-    cfg = S.CONFIGS[DECODE_CFG]
+    cfg = S.CONFIGS[args.profile_cfg or DECODE_CFG]
     ck = S.make_checkpoint(cfg)
     M = args.profile
-    icfg = cfg if M <= 16 else S.CONFIGS[PREFILL_CFG]
+    icfg = cfg if (M <= 16 or args.profile_cfg) else S.CONFIGS[PREFILL_CFG]
     layer = MoELayer(ck, cfg.topk, M, cfg.swiglu_limit, args.det)
     del ck
     for c in range(args.profile_calls):

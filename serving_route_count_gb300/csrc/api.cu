@@ -49,17 +49,14 @@ cudaError_t launch_simt_stage(int stage, const DevWeights& w, const RunPtrs& r,
                               const PlanDims& d, int max_tiles, const void* x,
                               const float* topk_w, void* out, int M, cudaStream_t st);
 // prepare.cu
-cudaError_t launch_repack_rows(const void* src, void* dst, int E, int halves, int rows,
-                               int src_cols, int dst_cols, int layout, int canon, cudaStream_t st);
 cudaError_t launch_repack_fp4_tiled(const void* src, void* dst, int E, int halves, int rows,
                                     int src_cols, int dst_cols, int layout, cudaStream_t st);
 cudaError_t launch_repack_sf_atoms(const void* src, void* dst, int E, int halves, int rows,
                                    int kblocks, int row_tiles, int k_tiles, int layout,
                                    cudaStream_t st);
-cudaError_t launch_repack_nf3(const void* src, void* dst, int E, int halves, int rows, int src_k,
-                              int dst_k, int layout, cudaStream_t st);
-cudaError_t launch_repack_nf3_scales(const void* src, void* dst, int E, int halves, int rows,
-                                     int src_k, int dst_k, int layout, cudaStream_t st);
+// kind: 0 NVFP4 codes, 1 NVFP4 scales, 2 NF3 codes, 3 NF3 scales
+cudaError_t launch_repack_w16_tiled(int kind, const void* src, void* dst, int E, int halves,
+                                    int rows, int src_k, int K, int layout, cudaStream_t st);
 // gemm_tc16.cu
 cudaError_t launch_tc16_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                               int bn, int tiles, int splits, const float* topk_w, int M,
@@ -129,12 +126,17 @@ int device_sms() {
   return sms;
 }
 
-// K splits of the unit-per-CTA fc1 so that small calls still fill the CTA slots (two CTAs of
-// the decode tile width fit an SM), with at least 4 K tiles per split.
+// K splits of the unit-per-CTA fc1 so that small calls still fill the CTA slots: the most
+// splits that keep the grid within one wave.  W4A8: two CTAs of the decode tile width per SM,
+// at least 4 K tiles of 128 per split.  W4A16: one CTA per SM (its rings of raw and expanded
+// weight stages), at least 2 raw stages of 256 per split (measured: splitting calls with more
+// units than SMs into several waves was slower).
 int fc1_splits(const PlanDims& d, int tiles) {
-  const int units = tiles * cdiv(d.I, 128);
-  const int slots = kFc1CtasPerSm * device_sms();
-  return std::max(1, std::min(std::min(slots / std::max(units, 1), d.H / 128 / 4), 16));
+  const int units = std::max(1, tiles * cdiv(d.I, 128));
+  const bool a8 = d.quant == MOE_W4A8_MXFP4;
+  const int slots = (a8 ? kFc1CtasPerSm : 1) * device_sms();
+  const int smax = a8 ? d.H / 128 / 4 : cdiv(d.H, 256) / 2;
+  return std::max(1, std::min(std::min(slots / units, smax), 16));
 }
 
 moe_status check_geometry(int E, int H, int I, int quant) {
@@ -198,22 +200,27 @@ moe_status moe_plan_weights(int E, int H, int I, int quant_mode, int w13_layout,
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
   const size_t E4 = wp->E4, E3 = wp->E3;
-  wp->w13 = take(E4 * 2 * I_ * H_ / 2);
-  wp->w2 = take(E4 * H_ * Ip / 2);
+  // W4A16 tiles of 128 rows x 256 K per matrix (fc1: I x H, fc2: H x Ip)
+  const size_t t13 = (size_t)2 * cdiv(I, 128) * cdiv(H, 256);
+  const size_t t2 = (size_t)(H / 128) * cdiv((int)Ip, 256);
   if (quant_mode == MOE_W4A8_MXFP4) {
+    wp->w13 = take(E4 * 2 * I_ * H_ / 2);
+    wp->w2 = take(E4 * H_ * Ip / 2);
     wp->s13 = take(E4 * 2 * (size_t)cdiv(I, 128) * (H_ / 128) * 512);
     wp->s2 = take(E4 * (H_ / 128) * (Ip / 128) * 512);
     wp->g13 = wp->g2 = 0;
   } else {
-    wp->s13 = take(E4 * 2 * I_ * H_ / 16);
-    wp->s2 = take(E4 * H_ * Ip / 16);
+    wp->w13 = take(E4 * t13 * kNvCodeTile);
+    wp->w2 = take(E4 * t2 * kNvCodeTile);
+    wp->s13 = take(E4 * t13 * kW16ScaleTile);
+    wp->s2 = take(E4 * t2 * kW16ScaleTile);
     wp->g13 = take(E4 * 4);
     wp->g2 = take(E4 * 4);
   }
-  wp->nf_w13 = take(E3 * 2 * I_ * 3 * H_ / 8);
-  wp->nf_s13 = take(E3 * 2 * I_ * (size_t)cdiv(H, 256) * 16);
-  wp->nf_w2 = take(E3 * H_ * 3 * Ip / 8);
-  wp->nf_s2 = take(E3 * H_ * (size_t)cdiv((int)Ip, 256) * 16);
+  wp->nf_w13 = take(E3 * t13 * kNfCodeTile);
+  wp->nf_s13 = take(E3 * t13 * kW16ScaleTile);
+  wp->nf_w2 = take(E3 * t2 * kNfCodeTile);
+  wp->nf_s2 = take(E3 * t2 * kW16ScaleTile);
   wp->tmap = take((size_t)E * 4);
   wp->total = o;
   *out = wp;
@@ -251,8 +258,8 @@ moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* 
       chk(launch_repack_fp4_tiled(src->w13, base + wp->w13, E4, 2, I, H / 2, H / 2, L, st));
       chk(launch_repack_fp4_tiled(src->w2, base + wp->w2, E4, 1, H, I / 2, Ip / 2, L, st));
     } else {
-      chk(launch_repack_rows(src->w13, base + wp->w13, E4, 2, I, H / 2, H / 2, L, 1, st));
-      chk(launch_repack_rows(src->w2, base + wp->w2, E4, 1, H, I / 2, Ip / 2, L, 1, st));
+      chk(launch_repack_w16_tiled(0, src->w13, base + wp->w13, E4, 2, I, H, H, L, st));
+      chk(launch_repack_w16_tiled(0, src->w2, base + wp->w2, E4, 1, H, I, Ip, L, st));
     }
     if (wp->quant == MOE_W4A8_MXFP4) {
       chk(launch_repack_sf_atoms(src->s13, base + wp->s13, E4, 2, I, H / 32, cdiv(I, 128),
@@ -260,17 +267,17 @@ moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* 
       chk(launch_repack_sf_atoms(src->s2, base + wp->s2, E4, 1, H, I / 32, H / 128, Ip / 128, L,
                                  st));
     } else {
-      chk(launch_repack_rows(src->s13, base + wp->s13, E4, 2, I, H / 16, H / 16, L, 0, st));
-      chk(launch_repack_rows(src->s2, base + wp->s2, E4, 1, H, I / 16, Ip / 16, L, 0, st));
+      chk(launch_repack_w16_tiled(1, src->s13, base + wp->s13, E4, 2, I, H, H, L, st));
+      chk(launch_repack_w16_tiled(1, src->s2, base + wp->s2, E4, 1, H, I, Ip, L, st));
       chk(cudaMemcpyAsync(base + wp->g13, src->g13, (size_t)E4 * 4, cudaMemcpyDeviceToDevice, st));
       chk(cudaMemcpyAsync(base + wp->g2, src->g2, (size_t)E4 * 4, cudaMemcpyDeviceToDevice, st));
     }
   }
   if (nf3) {
-    chk(launch_repack_nf3(src->nf_w13, base + wp->nf_w13, E3, 2, I, H, H, L, st));
-    chk(launch_repack_nf3(src->nf_w2, base + wp->nf_w2, E3, 1, H, I, Ip, L, st));
-    chk(launch_repack_nf3_scales(src->nf_s13, base + wp->nf_s13, E3, 2, I, H, H, L, st));
-    chk(launch_repack_nf3_scales(src->nf_s2, base + wp->nf_s2, E3, 1, H, I, Ip, L, st));
+    chk(launch_repack_w16_tiled(2, src->nf_w13, base + wp->nf_w13, E3, 2, I, H, H, L, st));
+    chk(launch_repack_w16_tiled(2, src->nf_w2, base + wp->nf_w2, E3, 1, H, I, Ip, L, st));
+    chk(launch_repack_w16_tiled(3, src->nf_s13, base + wp->nf_s13, E3, 2, I, H, H, L, st));
+    chk(launch_repack_w16_tiled(3, src->nf_s2, base + wp->nf_s2, E3, 1, H, I, Ip, L, st));
   }
   if (!wp->tier_map.empty())
     chk(cudaMemcpyAsync(base + wp->tmap, wp->tier_map.data(), wp->tier_map.size() * 4,

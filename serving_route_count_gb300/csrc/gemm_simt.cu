@@ -56,13 +56,16 @@ __device__ __forceinline__ void load_w8(const DevWeights& w, int kind, int le, i
                                         float* out) {
   const int K = FC2 ? w.Ip : w.H;
   const int R = FC2 ? w.H : 2 * w.I;
+  // W4A16 tiles: matrix and row within it, tiles per matrix
+  const int half = FC2 ? 0 : row / w.I;
+  const size_t mat = FC2 ? (size_t)le : (size_t)le * 2 + half;
+  const int mr = FC2 ? row : row - half * w.I;
+  const int rbs = cdiv(FC2 ? w.H : w.I, 128), kts = cdiv(K, 256);
   if (kind == kKindNF3) {
-    const size_t rowb = (size_t)le * R + row;
-    const uint8_t* base = (FC2 ? w.nf_w2 : w.nf_w13) + rowb * (size_t)(3 * K / 8);
-    const uint32_t lo = *reinterpret_cast<const uint16_t*>(base + k / 4);
-    const uint32_t hi = base[K / 4 + k / 8];
-    const float sc = e4m3_to_f32((FC2 ? w.nf_s2 : w.nf_s13)[rowb * (cdiv(K, 256) * 16) +
-                                                           nf3_scale_byte(k)]);
+    const uint8_t* codes = FC2 ? w.nf_w2 : w.nf_w13;
+    const uint32_t lo = *reinterpret_cast<const uint16_t*>(codes + nf_lo_byte(mat, mr, k, rbs, kts));
+    const uint32_t hi = codes[nf_hi_byte(mat, mr, k, rbs, kts)];
+    const float sc = e4m3_to_f32((FC2 ? w.nf_s2 : w.nf_s13)[nf_scale_byte(mat, mr, k, rbs, kts)]);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t c = ((lo >> (2 * i)) & 3u) | (((hi >> i) & 1u) << 2);
@@ -70,9 +73,10 @@ __device__ __forceinline__ void load_w8(const DevWeights& w, int kind, int le, i
     }
     return;
   }
-  const size_t rowb = (size_t)le * R + row;
   size_t cbyte;
-  if (w.fp4_tiled) {
+  if (kind == kKindNVFP4) {
+    cbyte = nv_code_byte(mat, mr, k, rbs, kts);
+  } else if (w.fp4_tiled) {
     if (FC2) {
       cbyte = fp4_tiled_byte((size_t)w.E4, w.H, K, (size_t)le, row, k);
     } else {
@@ -80,7 +84,7 @@ __device__ __forceinline__ void load_w8(const DevWeights& w, int kind, int le, i
       cbyte = fp4_tiled_byte((size_t)w.E4 * 2, w.I, K, (size_t)le * 2 + half, row - half * w.I, k);
     }
   } else {
-    cbyte = rowb * (size_t)(K / 2) + k / 2;
+    cbyte = ((size_t)le * R + row) * (size_t)(K / 2) + k / 2;
   }
   const uint32_t codes = *reinterpret_cast<const uint32_t*>((FC2 ? w.w2 : w.w13) + cbyte);
   float sc;
@@ -94,7 +98,7 @@ __device__ __forceinline__ void load_w8(const DevWeights& w, int kind, int le, i
     }
     sc = e8m0_to_f32((FC2 ? w.s2 : w.s13)[byte]);
   } else {
-    sc = e4m3_to_f32((FC2 ? w.s2 : w.s13)[rowb * (K / 16) + k / 16]);
+    sc = e4m3_to_f32((FC2 ? w.s2 : w.s13)[nv_scale_byte(mat, mr, k, rbs, kts)]);
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) out[i] = e2m1_to_f32((codes >> (4 * i)) & 0xFu) * sc;

@@ -13,12 +13,13 @@
 // and the per-expert NVFP4 global scale is applied in the fp32 epilogue.
 //
 // Same orientation and work split as the W4A8 kernels (gemm_tc.cu): weight rows are the
-// 128-row MMA operand, the tile's tokens the N columns.  Roles (192 threads):
-//   warp 0 lane 0  TMA: raw packed weights + scales (256-wide K stages), activation tiles
-//                  (64-wide K sub-tiles, 128-byte swizzle);
-//   warp 1 lane 0  tcgen05.mma (4 MMAs of K = 16 per sub-tile and matrix) and commits;
-//   warps 2..5     converters (thread = weight row) writing f16 sub-tiles in the 128-byte
-//                  swizzled K-major layout, then the epilogue from TMEM.
+// 128-row MMA operand, the tile's tokens the N columns.  Roles (320 threads):
+//   warp 0 lane 0   bulk copies of the raw weight tiles (codes + scales, 256-wide K stages)
+//                   and TMA of the activation sub-tiles (64-wide K, 128-byte swizzle);
+//   warp 1 lane 0   tcgen05.mma (4 MMAs of K = 16 per sub-tile and matrix) and commits;
+//   warps 2..9      converters (two threads per weight row, one half of each sub-tile each)
+//                   writing f16 sub-tiles in the 128-byte swizzled K-major layout; warps 2..5
+//                   then run the epilogue from TMEM.
 #include <algorithm>
 #include <cstring>
 
@@ -29,7 +30,7 @@ namespace moe {
 
 using namespace tc;
 
-constexpr int k16Threads = 192;
+constexpr int k16Threads = 320;           // producer, MMA issuer, 8 converter warps
 constexpr int k16RawK = 256;              // K elements per raw stage
 constexpr int k16SubK = 64;               // K elements per converted f16 sub-tile (128 B rows)
 constexpr int k16ATile = 128 * 128;       // one converted f16 sub-tile: 128 rows x 128 B
@@ -45,22 +46,27 @@ struct Tc16Cfg {
   static constexpr int kRaw = kMats * (k16RawCodes + k16RawScales);     // per raw stage
   static constexpr int kA = kMats * k16ATile;                           // per A slot
   static constexpr int kB = BN * 128;                                   // per B slot
-  static constexpr int kSr = FC2 ? 4 : (BN <= 32 ? 3 : 2);
-  static constexpr int kSa = FC2 ? 3 : 2;
-  static constexpr int kSb = BN <= 32 ? 8 : (BN <= 64 ? 6 : 4);
+  // fc2's K (the intermediate size) is a couple of raw stages: short rings, so that two CTAs
+  // fit an SM.  fc1 (one CTA per SM): two raw stages and as many expanded sub-tiles as fit -
+  // the expanded ring decouples the converters from the MMA (with two slots the conversion and
+  // the MMA of consecutive sub-tiles ran in series)
+  static constexpr int kSr = 2;
+  static constexpr int kSa = FC2 ? 2 : (BN <= 32 ? 4 : (BN <= 64 ? 3 : 2));
+  static constexpr int kSb = FC2 ? (BN <= 32 ? 8 : 4)
+                                 : (BN <= 16 ? 8 : (BN <= 32 ? 4 : (BN <= 64 ? 6 : 4)));
   static constexpr int kSmem = kSr * kRaw + kSa * kA + kSb * kB + 1024;
+  static_assert(kSmem <= 227 * 1024, "shared memory");
   static constexpr int kCols = kMats * BN;
   static constexpr int kAlloc = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : 256;
 };
 
 struct Tc16Params {
-  // fp4 (NVFP4) tier: codes [mats][rows][K/2] (SW128 boxes of 128 B x 128 rows), scales
-  // [mats][rows][K/16] (boxes of 16 B x 128 rows)
-  CUtensorMap tm_nv_codes, tm_nv_scales;
-  // NF3 tier: per row a 2-bit plane then a 1-bit plane (boxes of 32 B x 128 rows); scales padded
-  // to 16 B per 256-wide K tile (boxes of 16 B x 128 rows)
-  CUtensorMap tm_nf_codes, tm_nf_scales;
   CUtensorMap tm_act;         // f16 [Sm][K] activations, boxes 64 x BN, 128-byte swizzle
+  // weight tiles of 128 rows x 256 K per matrix (moe_common.cuh): one bulk copy each
+  const uint8_t* nv_codes;    // NVFP4 codes, 16 KB tiles (128-byte swizzled rows)
+  const uint8_t* nv_scales;   // NVFP4 scales, 2 KB tiles
+  const uint8_t* nf_codes;    // NF3 planes, 12 KB tiles
+  const uint8_t* nf_scales;   // NF3 scales, 2 KB tiles
   const int32_t* tier_map;    // hybrid: (tier << 24) | local; nullptr: every expert NVFP4
   const float* gscale;        // NVFP4 per-expert global of this matrix ([E4])
   const int4* tiles;
@@ -102,28 +108,26 @@ __device__ __forceinline__ uint32_t f16x2_bcast(uint32_t f16bits) {
   return (f16bits & 0xFFFFu) | (f16bits << 16);
 }
 
-// NVFP4 row r, K sub-tile q (64 elements) -> 8 chunks of 8 f16 in the 128-byte swizzled row.
-__device__ __forceinline__ void convert_nvfp4_row(const uint8_t* codes, const uint8_t* scales,
-                                                  uint8_t* dst, int r, int q) {
+// NVFP4 row r, K sub-tile q (64 elements), half h (elements 32h..32h+31) -> 4 chunks of 8 f16
+// (E2M1 x E4M3 scale, exact in f16) at chunks 4h..4h+3 of the 128-byte swizzled f16 row.
+__device__ __forceinline__ void convert_nvfp4_half(const uint8_t* codes, const uint8_t* scales,
+                                                   uint8_t* dst, int r, int q, int h) {
   const int sw = r & 7;
-  const uint4 c0 = *reinterpret_cast<const uint4*>(codes + r * 128 + (((2 * q) ^ sw) << 4));
-  const uint4 c1 = *reinterpret_cast<const uint4*>(codes + r * 128 + (((2 * q + 1) ^ sw) << 4));
+  const uint4 c = *reinterpret_cast<const uint4*>(codes + r * 128 + (((2 * q + h) ^ sw) << 4));
   const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(scales + r * 16 + q * 4);
-  const uint32_t s01 = cvt_e4m3x2_f16x2(sc4 & 0xFFFF);
-  const uint32_t s23 = cvt_e4m3x2_f16x2(sc4 >> 16);
-  const uint32_t sc[4] = {f16x2_bcast(s01), f16x2_bcast(s01 >> 16), f16x2_bcast(s23),
-                          f16x2_bcast(s23 >> 16)};
-  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const uint32_t s2 = cvt_e4m3x2_f16x2((sc4 >> (16 * h)) & 0xFFFF);
+  const uint32_t sc[2] = {f16x2_bcast(s2), f16x2_bcast(s2 >> 16)};
+  const uint32_t words[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t w = words[j];
-    const uint32_t s = sc[j >> 1];
+  for (int jj = 0; jj < 4; ++jj) {
+    const uint32_t w = words[jj];
+    const uint32_t s = sc[jj >> 1];
     uint4 o;
     o.x = hmul2(cvt_e2m1x2_f16x2(w & 0xFF), s);
     o.y = hmul2(cvt_e2m1x2_f16x2((w >> 8) & 0xFF), s);
     o.z = hmul2(cvt_e2m1x2_f16x2((w >> 16) & 0xFF), s);
     o.w = hmul2(cvt_e2m1x2_f16x2(w >> 24), s);
-    *reinterpret_cast<uint4*>(dst + r * 128 + ((j ^ sw) << 4)) = o;
+    *reinterpret_cast<uint4*>(dst + r * 128 + (((4 * h + jj) ^ sw) << 4)) = o;
   }
 }
 
@@ -148,25 +152,22 @@ __device__ __forceinline__ uint32_t nf3_pick2(const uint32_t* t, uint32_t c0, ui
   return (lo & ~m) | (hi & m);
 }
 
-// NF3 row r, K sub-tile q (64 codes) -> 8 chunks of 8 f16.  Raw smem: box0 / box1 = the two
-// 32-byte halves of the 2-bit plane of the 256-wide stage, box2 = its 1-bit plane (32 B).
-__device__ __forceinline__ void convert_nf3_row(const uint8_t* codes, const uint8_t* scales,
-                                                uint8_t* dst, int r, int q) {
+// NF3 row r, K sub-tile q (64 codes), half h (codes 32h..32h+31: one scale group) -> 4 chunks of
+// 8 f16 at chunks 4h..4h+3 of the swizzled f16 row.  Raw smem: 32-byte rows of the tile's 2-bit
+// plane halves (bytes 0..31 at +0, 32..63 at +4096) and of its 1-bit plane (+8192).
+__device__ __forceinline__ void convert_nf3_half(const uint8_t* codes, const uint8_t* scales,
+                                                 uint8_t* dst, int r, int q, int h) {
   const int sw = r & 7;
-  const uint4 lo = *reinterpret_cast<const uint4*>(codes + (q >> 1) * 4096 + r * 32 +
-                                                   (q & 1) * 16);
-  const uint2 hi = *reinterpret_cast<const uint2*>(codes + 8192 + r * 32 + q * 8);
-  const uint8_t s0 = scales[r * 16 + q * 2], s1 = scales[r * 16 + q * 2 + 1];
-  uint32_t t0[4], t1[4];
-  nf3_table(e4m3_to_f32(s0), t0);
-  nf3_table(e4m3_to_f32(s1), t1);
-  const uint32_t low[4] = {lo.x, lo.y, lo.z, lo.w};
-  const uint32_t high[2] = {hi.x, hi.y};
+  const uint2 lo = *reinterpret_cast<const uint2*>(codes + (q >> 1) * 4096 + r * 32 +
+                                                   (q & 1) * 16 + 8 * h);
+  const uint32_t hi = *reinterpret_cast<const uint32_t*>(codes + 8192 + r * 32 + q * 8 + 4 * h);
+  uint32_t t[4];
+  nf3_table(e4m3_to_f32(scales[r * 16 + q * 2 + h]), t);
+  const uint32_t low[2] = {lo.x, lo.y};
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t l16 = (low[j >> 1] >> ((j & 1) * 16)) & 0xFFFF;
-    const uint32_t h8 = (high[j >> 2] >> ((j & 3) * 8)) & 0xFF;
-    const uint32_t* t = j < 4 ? t0 : t1;
+  for (int jj = 0; jj < 4; ++jj) {
+    const uint32_t l16 = (low[jj >> 1] >> ((jj & 1) * 16)) & 0xFFFF;
+    const uint32_t h8 = (hi >> (jj * 8)) & 0xFF;
     uint32_t o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -174,7 +175,8 @@ __device__ __forceinline__ void convert_nf3_row(const uint8_t* codes, const uint
       const uint32_t c1 = ((l16 >> (4 * e + 2)) & 3) | (((h8 >> (2 * e + 1)) & 1) << 2);
       o[e] = nf3_pick2(t, c0, c1);
     }
-    *reinterpret_cast<uint4*>(dst + r * 128 + ((j ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(dst + r * 128 + (((4 * h + jj) ^ sw) << 4)) =
+        make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -238,10 +240,10 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   if (tid == 32) {
     for (int s = 0; s < Cfg::kSr; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], 4);
+      mbar_init(&raw_empty[s], 8);
     }
     for (int s = 0; s < Cfg::kSa; ++s) {
-      mbar_init(&a_full[s], 4);
+      mbar_init(&a_full[s], 8);
       mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < Cfg::kSb; ++s) {
@@ -261,6 +263,7 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
 
   if (warp == 0) {
     if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
       int i = 0;
       for (; i < nraw && ok; ++i) {
         const int s = i % Cfg::kSr;
@@ -268,27 +271,15 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
         if (!ok) break;
         uint8_t* st = raw_base + s * Cfg::kRaw;
         const int kt = kt0 + i;
-        if (!nf3) {
-          mbar_arrive_expect_tx(&raw_full[s], kMats * (k16RawCodes + k16RawScales));
-          for (int m = 0; m < kMats; ++m) {
-            const int mat = FC2 ? le : 2 * le + m;
-            tma_load_3d(st + m * k16RawCodes, &p.tm_nv_codes, kt * 128, rb * 128, mat,
-                        &raw_full[s]);
-            tma_load_3d(st + kMats * k16RawCodes + m * k16RawScales, &p.tm_nv_scales, kt * 16,
-                        rb * 128, mat, &raw_full[s]);
-          }
-        } else {
-          mbar_arrive_expect_tx(&raw_full[s], kMats * (3 * 4096 + k16RawScales));
-          for (int m = 0; m < kMats; ++m) {
-            const int mat = FC2 ? le : 2 * le + m;
-            uint8_t* c = st + m * k16RawCodes;
-            tma_load_3d(c, &p.tm_nf_codes, kt * 64, rb * 128, mat, &raw_full[s]);
-            tma_load_3d(c + 4096, &p.tm_nf_codes, kt * 64 + 32, rb * 128, mat, &raw_full[s]);
-            tma_load_3d(c + 8192, &p.tm_nf_codes, p.K / 4 + kt * 32, rb * 128, mat,
-                        &raw_full[s]);
-            tma_load_3d(st + kMats * k16RawCodes + m * k16RawScales, &p.tm_nf_scales, kt * 16,
-                        rb * 128, mat, &raw_full[s]);
-          }
+        const uint32_t code_bytes = nf3 ? kNfCodeTile : kNvCodeTile;
+        mbar_arrive_expect_tx(&raw_full[s], kMats * (code_bytes + kW16ScaleTile));
+        for (int m = 0; m < kMats; ++m) {
+          const size_t tile = w16_tile(FC2 ? le : 2 * le + m, rb, kt, p.RB, p.KT);
+          bulk_load_hint(st + m * k16RawCodes, (nf3 ? p.nf_codes : p.nv_codes) +
+                         tile * code_bytes, code_bytes, &raw_full[s], pol);
+          bulk_load_hint(st + kMats * k16RawCodes + m * k16RawScales,
+                         (nf3 ? p.nf_scales : p.nv_scales) + tile * kW16ScaleTile, kW16ScaleTile,
+                         &raw_full[s], pol);
         }
         // the four activation sub-tiles of this raw stage
         for (int q = 0; q < 4 && ok; ++q, ++g) {
@@ -327,9 +318,10 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
       tc_commit(&done);
     }
   } else {
-    // converters: thread = row of the 128-row weight block
-    const int r = tid - 64;
-    if (FC2 && r < n) {
+    // converters: two threads per row of the 128-row weight block, each expanding one half of
+    // every 64-wide sub-tile (warps 2..5 the first half, 6..9 the second)
+    const int r = (tid - 64) & 127, half = (tid - 64) >> 7;
+    if (FC2 && half == 0 && r < n) {
       // the combine's slot indices and router weights, read by these threads' epilogue
       const int f = p.perm[p0 + r];
       s_f[r] = f;
@@ -351,9 +343,9 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
           const uint8_t* c = st + m * k16RawCodes;
           const uint8_t* sc = st + kMats * k16RawCodes + m * k16RawScales;
           if (nf3)
-            convert_nf3_row(c, sc, A + m * k16ATile, r, q);
+            convert_nf3_half(c, sc, A + m * k16ATile, r, q, half);
           else
-            convert_nvfp4_row(c, sc, A + m * k16ATile, r, q);
+            convert_nvfp4_half(c, sc, A + m * k16ATile, r, q, half);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -365,7 +357,7 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   }
 
   // ---- epilogue (warps 2..5): TMEM lane quadrant = warp % 4
-  if (warp >= 2) {
+  if (warp >= 2 && warp < 6) {
     asm volatile("bar.sync 1, 128;" ::: "memory");         // s_f / s_w written (warps 2..5)
     ok = mbar_wait(&done, 0, p.err) && ok;
     tc_fence_after();
@@ -427,7 +419,7 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
       s_last = (t == p.splits - 1);
     }
     __syncthreads();
-    if (s_last && warp >= 2) {
+    if (s_last && warp >= 2 && warp < 6) {
       __threadfence();
       const int quad = warp & 3;
       const int row = rb * 128 + quad * 32 + lane;
@@ -486,21 +478,6 @@ static EncodeTiledFn16 encode16() {
   return fn;
 }
 
-// 3-D byte tensor [mats][rows][row_bytes] with boxes box_x bytes x 128 rows x 1.
-static bool tmap_bytes3(CUtensorMap* tm, const void* base, int row_bytes, int rows, int mats,
-                        int box_x, bool swizzle) {
-  EncodeTiledFn16 enc = encode16();
-  if (!enc || mats <= 0) return enc != nullptr;
-  cuuint64_t dims[3] = {(cuuint64_t)row_bytes, (cuuint64_t)rows, (cuuint64_t)mats};
-  cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)row_bytes * rows};
-  cuuint32_t box[3] = {(cuuint32_t)box_x, 128, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // f16 activations [rows][K] with boxes 64 x box_rows and 128-byte swizzle.
 static bool tmap_f16(CUtensorMap* tm, const void* base, int K, int rows, int box_rows) {
   EncodeTiledFn16 enc = encode16();
@@ -539,15 +516,11 @@ cudaError_t launch_tc16_stage(int stage, const DevWeights& w, const RunPtrs& r, 
   memset(&p, 0, sizeof(p));
   const bool fc2 = stage == 1;
   const int K = fc2 ? d.Ip : d.H;
-  const int rows = fc2 ? d.H : d.I;
-  const int mats4 = fc2 ? w.E4 : 2 * w.E4;
-  const int mats3 = fc2 ? w.E3 : 2 * w.E3;
   const int KT = (K + k16RawK - 1) / k16RawK;
-  if (!tmap_bytes3(&p.tm_nv_codes, fc2 ? w.w2 : w.w13, K / 2, rows, mats4, 128, true) ||
-      !tmap_bytes3(&p.tm_nv_scales, fc2 ? w.s2 : w.s13, K / 16, rows, mats4, 16, false) ||
-      !tmap_bytes3(&p.tm_nf_codes, fc2 ? w.nf_w2 : w.nf_w13, 3 * K / 8, rows, mats3, 32, false) ||
-      !tmap_bytes3(&p.tm_nf_scales, fc2 ? w.nf_s2 : w.nf_s13, KT * 16, rows, mats3, 16, false))
-    return cudaErrorInvalidValue;
+  p.nv_codes = fc2 ? w.w2 : w.w13;
+  p.nv_scales = fc2 ? w.s2 : w.s13;
+  p.nf_codes = fc2 ? w.nf_w2 : w.nf_w13;
+  p.nf_scales = fc2 ? w.nf_s2 : w.nf_s13;
   if (!tmap_f16(&p.tm_act, fc2 ? (const void*)r.h16 : (const void*)r.x16, K, Sm, bn))
     return cudaErrorInvalidValue;
   p.tier_map = w.tier_map;
@@ -555,7 +528,7 @@ cudaError_t launch_tc16_stage(int stage, const DevWeights& w, const RunPtrs& r, 
   p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
   p.h16 = reinterpret_cast<uint16_t*>(r.h16); p.gacc = r.g; p.tickets = r.tickets;
   p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;
-  p.K = K; p.R = rows; p.I = d.I; p.Ip = d.Ip; p.RB = fc2 ? d.H / 128 : cdiv(d.I, 128);
+  p.K = K; p.R = fc2 ? d.H : d.I; p.I = d.I; p.Ip = d.Ip; p.RB = fc2 ? d.H / 128 : cdiv(d.I, 128);
   p.KT = KT; p.Sm = Sm; p.splits = fc2 ? 1 : splits; p.topk = d.topk;
   p.deterministic = d.deterministic; p.H = d.H; p.nf3_row_bytes = 3 * K / 8;
   p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;

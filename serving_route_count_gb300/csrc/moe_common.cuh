@@ -26,8 +26,6 @@ constexpr int kErrRange = 8;         // a bf16 value outside the f16 range of th
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
-// byte offset of the NF3 scale of element k within a row's padded scale groups
-__host__ __device__ inline int nf3_scale_byte(int k) { return (k >> 8) * 16 + ((k & 255) >> 5); }
 
 // ----------------------------------------------------------------------------------------------
 // Prepared (device) weight layout.
@@ -37,18 +35,22 @@ __host__ __device__ inline int nf3_scale_byte(int k) { return (k >> 8) * 16 + ((
 // (zero codes beyond I), because the packed-FP4 TMA format needs a row length that is a
 // multiple of 128 elements.
 //
-// FP4 codes: element 2j in the low nibble of byte j (checkpoint order).  NVFP4: rows of K/2
-//   bytes.  MXFP4: tile-contiguous (fp4_tiled_byte): every 128-row x 128-K block is one 8 KB run
+// FP4 codes: element 2j in the low nibble of byte j (checkpoint order).  MXFP4: tile-contiguous (fp4_tiled_byte): every 128-row x 128-K block is one 8 KB run
 //   ([mats][rows/128][K/128][128][64 B]), the partial last row block of rows % 128 rows follows
 //   all full blocks ([mats][K/128][rows % 128][64 B]), so each TMA box streams contiguous bytes.
 // MXFP4 E8M0 scales ("SF atoms"): for each 128-row tile and each 128-wide K tile, 512 bytes
 //   byte(r, kb) = (r % 32) * 16 + (r / 32) * 4 + kb     (r < 128 in the tile, kb < 4 blocks of 32)
 //   atoms ordered [expert][half][row tile][k tile]  (fc1)  /  [expert][row tile][k tile]  (fc2).
-// NVFP4 E4M3 scales: row-major [row][K/16].  NF3: per row a 2-bit plane (K/4 bytes, code c's low
-//   two bits at bits 2*(c%4) of byte c/4) followed by a 1-bit plane (K/8 bytes, bit 2 of code c
-//   at bit c%8 of byte c/8); E4M3 scales per row in 16-byte groups, one per 256-wide K tile
-//   (byte kt*16 + g = scale of K group 8*kt + g; bytes 8..15 zero) so that tensor-map boxes of
-//   16 bytes fetch one tile's scales.
+// W4A16 tiers (NVFP4, NF3): tile-contiguous too, in tiles of 128 rows x 256 K of one matrix
+//   ([mats][ceil(rows/128)][ceil(K/256)] tiles; rows and K beyond the matrix are zero), so that
+//   a pipeline stage of a matrix is one bulk copy of codes and one of scales:
+//   NVFP4 codes: 16 KB per tile, row r at r*128, its 16-byte chunk j (elements 32j..32j+31) at
+//     chunk j ^ (r % 8) - the 128-byte swizzle the expanding warps read;
+//   NVFP4 scales: 2 KB per tile, row r at r*16 (the E4M3 scales of its 16 groups of 16);
+//   NF3 codes: 12 KB per tile, [3][128][32 B]: the row's 2-bit plane bytes 0..31 and 32..63 of
+//     the tile (code c's low two bits at bits 2*(c%4) of byte c/4), then its 1-bit plane bytes
+//     0..31 (bit 2 of code c at bit c%8 of byte c/8);
+//   NF3 scales: 2 KB per tile, row r at r*16: the E4M3 scales of its 8 groups of 32, 8 zero.
 // ----------------------------------------------------------------------------------------------
 struct DevWeights {
   int quant = 0;
@@ -56,17 +58,17 @@ struct DevWeights {
   int E4 = 0, E3 = 0;                 // experts in the fp4 tier / the NF3 tier
   int fp4_tiled = 0;                  // MXFP4 codes in the tile-contiguous layout
   // fp4 tier (MXFP4 or NVFP4)
-  const uint8_t* w13 = nullptr;       // [E4][2][I][H/2]
-  const uint8_t* s13 = nullptr;       // MXFP4 atoms / NVFP4 [E4][2][I][H/16]
+  const uint8_t* w13 = nullptr;       // [E4][2][I][H/2] codes (tiled, see above)
+  const uint8_t* s13 = nullptr;       // MXFP4 atoms / NVFP4 scale tiles
   const uint8_t* w2 = nullptr;        // [E4][H][Ip/2]
   const uint8_t* s2 = nullptr;        // MXFP4 atoms / NVFP4 [E4][H][Ip/16]
   const float* g13 = nullptr;         // [E4] NVFP4 global scales
   const float* g2 = nullptr;
   // NF3 tier
-  const uint8_t* nf_w13 = nullptr;    // [E3][2][I][3H/8] planes
-  const uint8_t* nf_s13 = nullptr;    // [E3][2][I][ceil(H/256)][16]
+  const uint8_t* nf_w13 = nullptr;    // NF3 code tiles of [E3][2] matrices I x H
+  const uint8_t* nf_s13 = nullptr;    // NF3 scale tiles
   const uint8_t* nf_w2 = nullptr;     // [E3][H][3Ip/8] planes
-  const uint8_t* nf_s2 = nullptr;     // [E3][H][ceil(Ip/256)][16]
+  const uint8_t* nf_s2 = nullptr;     // NF3 scale tiles of [E3] matrices H x Ip
   const int32_t* tier_map = nullptr;  // [E]: (tier << 24) | local index
 };
 
@@ -76,6 +78,39 @@ __host__ __device__ inline size_t fp4_tiled_byte(size_t n_mats, int rows, int K,
   const int rt = r >> 7, rr = r & 127, kt = k >> 7, kb = (k & 127) >> 1;
   if (rt < rtf) return ((((mat * rtf + rt) * kt_n + kt) << 7) + rr) * 64 + kb;
   return n_mats * rtf * kt_n * 8192 + (((mat * kt_n + kt) * rem) + rr) * 64 + kb;
+}
+
+// W4A16 tiles (see above): tile of matrix `mat`, row block rb, K tile kt.
+__host__ __device__ inline size_t w16_tile(size_t mat, int rb, int kt, int rbs, int kts) {
+  return (mat * (size_t)rbs + rb) * (size_t)kts + kt;
+}
+constexpr int kNvCodeTile = 16384, kNfCodeTile = 12288, kW16ScaleTile = 2048;
+// NVFP4 code byte of elements k, k+1 (k even) of row r of matrix mat (rbs x kts tiles)
+__host__ __device__ inline size_t nv_code_byte(size_t mat, int r, int k, int rbs, int kts) {
+  const int rr = r & 127, kk = k & 255;
+  return w16_tile(mat, r >> 7, k >> 8, rbs, kts) * kNvCodeTile + (size_t)rr * 128 +
+         ((((kk >> 5) ^ (rr & 7))) << 4) + ((kk & 31) >> 1);
+}
+// NVFP4 scale byte of element k of row r
+__host__ __device__ inline size_t nv_scale_byte(size_t mat, int r, int k, int rbs, int kts) {
+  return w16_tile(mat, r >> 7, k >> 8, rbs, kts) * kW16ScaleTile + (size_t)(r & 127) * 16 +
+         ((k & 255) >> 4);
+}
+// NF3 2-bit plane byte of codes k..k+3 (k % 4 == 0) and 1-bit plane byte of codes k..k+7
+// (k % 8 == 0) of row r
+__host__ __device__ inline size_t nf_lo_byte(size_t mat, int r, int k, int rbs, int kts) {
+  const int kk = k & 255;
+  return w16_tile(mat, r >> 7, k >> 8, rbs, kts) * kNfCodeTile + (size_t)(kk >> 7) * 4096 +
+         (size_t)(r & 127) * 32 + ((kk >> 2) & 31);
+}
+__host__ __device__ inline size_t nf_hi_byte(size_t mat, int r, int k, int rbs, int kts) {
+  return w16_tile(mat, r >> 7, k >> 8, rbs, kts) * kNfCodeTile + 8192 + (size_t)(r & 127) * 32 +
+         ((k & 255) >> 3);
+}
+// NF3 scale byte of element k of row r
+__host__ __device__ inline size_t nf_scale_byte(size_t mat, int r, int k, int rbs, int kts) {
+  return w16_tile(mat, r >> 7, k >> 8, rbs, kts) * kW16ScaleTile + (size_t)(r & 127) * 16 +
+         ((k & 255) >> 5);
 }
 
 __host__ __device__ inline size_t sf_atom_byte(int row_tiles, int k_tiles, size_t mat, int r,

@@ -25,29 +25,6 @@ __device__ __forceinline__ uint8_t canon_fp4_byte(uint8_t b) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)(n); \
        i += (size_t)gridDim.x * blockDim.x)
 
-// Row-wise copy with a per-row source mapping and zero padding of the row tail.
-//   dst [mats][rows][dst_cols] <- src [mats][rows][src_cols]; fc1 mats interleave halves.
-__global__ void repack_rows_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
-                                   int E, int halves, int rows, int src_cols, int dst_cols,
-                                   int layout, int canon_fp4) {
-  const size_t n = (size_t)E * halves * rows * dst_cols;
-  GRID_STRIDE(idx, n) {
-    const int c = (int)(idx % dst_cols);
-    const size_t rowid = idx / dst_cols;
-    const int i = (int)(rowid % rows);
-    const size_t mh = rowid / rows;
-    const int half = (int)(mh % halves);
-    const size_t e = mh / halves;
-    uint8_t v = 0;
-    if (c < src_cols) {
-      const int sr = halves == 2 ? src_row_fc1(half, i, rows, layout) : i;
-      v = src[(e * (size_t)(halves * rows) + sr) * src_cols + c];
-      if (canon_fp4) v = canon_fp4_byte(v);
-    }
-    dst[idx] = v;
-  }
-}
-
 // Packed FP4 rows -> the tile-contiguous layout (fp4_tiled_byte), zero padding of the row tail
 // (src_cols .. dst_cols) and -0 -> +0.  src [E][halves*rows][src_cols], dst for
 // mats = E*halves matrices of rows x (2*dst_cols) elements.
@@ -99,60 +76,105 @@ __global__ void repack_sf_atoms_kernel(const uint8_t* __restrict__ src, uint8_t*
   }
 }
 
-// NF3: 3-byte groups of 8 codes -> per-row 2-bit plane + 1-bit plane (row tails padded with
-// code 0 in both planes; their scale is 0, so the padded weights are exactly 0).
-//   src [E][halves*rows][3*src_k/8], dst [E][halves][rows][3*dst_k/8]
-__global__ void repack_nf3_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
-                                  int E, int halves, int rows, int src_k, int dst_k, int layout) {
-  const int groups = dst_k / 8;
-  const size_t n = (size_t)E * halves * rows * groups;
+// W4A16 tiles (moe_common.cuh): every kernel below walks the destination bytes of
+// mats = E*halves matrices of `rows` rows and K elements in tiles of 128 x 256, and reads the
+// checkpoint row (fc1 halves in the checkpoint's stacking order) or writes 0 beyond it.
+
+// NVFP4 codes (16 KB tiles, 128-byte swizzle), -0 -> +0.  src [E][halves*rows][src_k/2].
+__global__ void repack_nv_codes_tiled_kernel(const uint8_t* __restrict__ src,
+                                             uint8_t* __restrict__ dst, int E, int halves,
+                                             int rows, int src_k, int K, int layout) {
+  const int rbs = (rows + 127) / 128, kts = (K + 255) / 256;
+  const size_t n = (size_t)E * halves * rbs * kts * kNvCodeTile;
   GRID_STRIDE(idx, n) {
-    const int gi = (int)(idx % groups);
-    const size_t rowid = idx / groups;
-    const int i = (int)(rowid % rows);
-    const size_t mh = rowid / rows;
-    const int half = (int)(mh % halves);
-    const size_t e = mh / halves;
-    uint32_t w24 = 0;
-    if (gi < src_k / 8) {
-      const int sr = halves == 2 ? src_row_fc1(half, i, rows, layout) : i;
-      const uint8_t* s = src + (e * (size_t)(halves * rows) + sr) * (size_t)(3 * src_k / 8) + 3 * gi;
-      w24 = (uint32_t)s[0] | ((uint32_t)s[1] << 8) | ((uint32_t)s[2] << 16);
+    const int off = (int)(idx % kNvCodeTile);
+    size_t t = idx / kNvCodeTile;
+    const int kt = (int)(t % kts);
+    t /= kts;
+    const int rb = (int)(t % rbs);
+    const size_t mat = t / rbs;
+    const int rr = off >> 7, j = ((off >> 4) & 7) ^ (rr & 7), b = off & 15;
+    const int r = rb * 128 + rr;
+    const int cbyte = kt * 128 + j * 16 + b;          // packed byte within the row
+    uint8_t v = 0;
+    if (r < rows && 2 * cbyte < src_k) {
+      const int half = (int)(mat % halves);
+      const size_t e = mat / halves;
+      const int sr = halves == 2 ? src_row_fc1(half, r, rows, layout) : r;
+      v = canon_fp4_byte(src[(e * (size_t)(halves * rows) + sr) * (size_t)(src_k / 2) + cbyte]);
     }
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t code = (w24 >> (3 * c)) & 7u;
-      lo |= (code & 3u) << (2 * c);
-      hi |= (code >> 2) << c;
-    }
-    uint8_t* d = dst + rowid * (size_t)(3 * dst_k / 8);
-    d[2 * gi] = (uint8_t)(lo & 0xFF);
-    d[2 * gi + 1] = (uint8_t)(lo >> 8);
-    d[dst_k / 4 + gi] = (uint8_t)hi;
+    dst[idx] = v;
   }
 }
 
-// NF3 E4M3 scales [E][halves*rows][src_k/32] -> [E][halves][rows][ceil(dst_k/256)][16]
-__global__ void repack_nf3_scales_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
-                                         int E, int halves, int rows, int src_k, int dst_k,
-                                         int layout) {
-  const int kt = (dst_k + 255) / 256;
-  const size_t n = (size_t)E * halves * rows * kt * 16;
+// Scales of 16 bytes per row and tile: NVFP4 (`group` = 16 elements, 16 per tile) or NF3
+// (`group` = 32 elements, 8 per tile, bytes 8..15 zero).  src [E][halves*rows][src_k/group].
+__global__ void repack_w16_scales_tiled_kernel(const uint8_t* __restrict__ src,
+                                               uint8_t* __restrict__ dst, int E, int halves,
+                                               int rows, int src_k, int K, int group, int layout) {
+  const int rbs = (rows + 127) / 128, kts = (K + 255) / 256;
+  const int per_tile = 256 / group;
+  const size_t n = (size_t)E * halves * rbs * kts * kW16ScaleTile;
   GRID_STRIDE(idx, n) {
-    const int b = (int)(idx % (kt * 16));
-    const size_t rowid = idx / (kt * 16);
-    const int i = (int)(rowid % rows);
-    const size_t mh = rowid / rows;
-    const int half = (int)(mh % halves);
-    const size_t e = mh / halves;
-    const int g = (b >> 4) * 8 + (b & 15);       // K group of 32 elements
+    const int off = (int)(idx % kW16ScaleTile);
+    size_t t = idx / kW16ScaleTile;
+    const int kt = (int)(t % kts);
+    t /= kts;
+    const int rb = (int)(t % rbs);
+    const size_t mat = t / rbs;
+    const int rr = off >> 4, b = off & 15;
+    const int r = rb * 128 + rr;
+    const int g = kt * per_tile + b;
     uint8_t v = 0;
-    if ((b & 15) < 8 && g < src_k / 32) {
-      const int sr = halves == 2 ? src_row_fc1(half, i, rows, layout) : i;
-      v = src[(e * (size_t)(halves * rows) + sr) * (src_k / 32) + g];
+    if (b < per_tile && r < rows && g < src_k / group) {
+      const int half = (int)(mat % halves);
+      const size_t e = mat / halves;
+      const int sr = halves == 2 ? src_row_fc1(half, r, rows, layout) : r;
+      v = src[(e * (size_t)(halves * rows) + sr) * (size_t)(src_k / group) + g];
     }
     dst[idx] = v;
+  }
+}
+
+// NF3 code c of checkpoint row `sr` (3-byte groups of 8 codes), 0 beyond src_k.
+__device__ __forceinline__ uint32_t nf3_code(const uint8_t* src, size_t row_base, int c,
+                                             int src_k) {
+  if (c >= src_k) return 0;
+  const uint8_t* s = src + row_base + 3 * (c >> 3);
+  const uint32_t w24 = (uint32_t)s[0] | ((uint32_t)s[1] << 8) | ((uint32_t)s[2] << 16);
+  return (w24 >> (3 * (c & 7))) & 7u;
+}
+
+// NF3 codes -> 12 KB tiles of 2-bit and 1-bit planes.  src [E][halves*rows][3*src_k/8].
+__global__ void repack_nf3_tiled_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                        int E, int halves, int rows, int src_k, int K,
+                                        int layout) {
+  const int rbs = (rows + 127) / 128, kts = (K + 255) / 256;
+  const size_t n = (size_t)E * halves * rbs * kts * kNfCodeTile;
+  GRID_STRIDE(idx, n) {
+    const int off = (int)(idx % kNfCodeTile);
+    size_t t = idx / kNfCodeTile;
+    const int kt = (int)(t % kts);
+    t /= kts;
+    const int rb = (int)(t % rbs);
+    const size_t mat = t / rbs;
+    const int box = off >> 12, rr = (off >> 5) & 127, bb = off & 31;
+    const int r = rb * 128 + rr;
+    uint32_t v = 0;
+    if (r < rows) {
+      const int half = (int)(mat % halves);
+      const size_t e = mat / halves;
+      const int sr = halves == 2 ? src_row_fc1(half, r, rows, layout) : r;
+      const size_t row_base = (e * (size_t)(halves * rows) + sr) * (size_t)(3 * src_k / 8);
+      if (box < 2) {            // 2-bit plane byte: codes c0..c0+3, low two bits each
+        const int c0 = kt * 256 + (box * 32 + bb) * 4;
+        for (int i = 0; i < 4; ++i) v |= (nf3_code(src, row_base, c0 + i, src_k) & 3u) << (2 * i);
+      } else {                  // 1-bit plane byte: codes c0..c0+7, bit 2 each
+        const int c0 = kt * 256 + bb * 8;
+        for (int i = 0; i < 8; ++i) v |= (nf3_code(src, row_base, c0 + i, src_k) >> 2) << i;
+      }
+    }
+    dst[idx] = (uint8_t)v;
   }
 }
 
@@ -160,15 +182,6 @@ static int grid_for(size_t n) {
   size_t b = (n + 255) / 256;
   if (b > 152 * 32) b = 152 * 32;
   return b < 1 ? 1 : (int)b;
-}
-
-cudaError_t launch_repack_rows(const void* src, void* dst, int E, int halves, int rows,
-                               int src_cols, int dst_cols, int layout, int canon, cudaStream_t st) {
-  const size_t n = (size_t)E * halves * rows * dst_cols;
-  if (n == 0) return cudaSuccess;
-  repack_rows_kernel<<<grid_for(n), 256, 0, st>>>((const uint8_t*)src, (uint8_t*)dst, E, halves,
-                                                  rows, src_cols, dst_cols, layout, canon);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_repack_fp4_tiled(const void* src, void* dst, int E, int halves, int rows,
@@ -191,21 +204,32 @@ cudaError_t launch_repack_sf_atoms(const void* src, void* dst, int E, int halves
   return cudaGetLastError();
 }
 
-cudaError_t launch_repack_nf3(const void* src, void* dst, int E, int halves, int rows, int src_k,
-                              int dst_k, int layout, cudaStream_t st) {
-  const size_t n = (size_t)E * halves * rows * (dst_k / 8);
-  if (n == 0) return cudaSuccess;
-  repack_nf3_kernel<<<grid_for(n), 256, 0, st>>>((const uint8_t*)src, (uint8_t*)dst, E, halves,
-                                                 rows, src_k, dst_k, layout);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_repack_nf3_scales(const void* src, void* dst, int E, int halves, int rows,
-                                     int src_k, int dst_k, int layout, cudaStream_t st) {
-  const size_t n = (size_t)E * halves * rows * ((dst_k + 255) / 256) * 16;
-  if (n == 0) return cudaSuccess;
-  repack_nf3_scales_kernel<<<grid_for(n), 256, 0, st>>>((const uint8_t*)src, (uint8_t*)dst, E,
-                                                        halves, rows, src_k, dst_k, layout);
+cudaError_t launch_repack_w16_tiled(int kind, const void* src, void* dst, int E, int halves,
+                                    int rows, int src_k, int K, int layout, cudaStream_t st) {
+  const size_t tiles = (size_t)E * halves * ((rows + 127) / 128) * ((K + 255) / 256);
+  if (tiles == 0) return cudaSuccess;
+  const uint8_t* s8 = static_cast<const uint8_t*>(src);
+  uint8_t* d8 = static_cast<uint8_t*>(dst);
+  switch (kind) {
+    case 0:   // NVFP4 codes
+      repack_nv_codes_tiled_kernel<<<grid_for(tiles * kNvCodeTile), 256, 0, st>>>(
+          s8, d8, E, halves, rows, src_k, K, layout);
+      break;
+    case 1:   // NVFP4 scales
+      repack_w16_scales_tiled_kernel<<<grid_for(tiles * kW16ScaleTile), 256, 0, st>>>(
+          s8, d8, E, halves, rows, src_k, K, 16, layout);
+      break;
+    case 2:   // NF3 codes
+      repack_nf3_tiled_kernel<<<grid_for(tiles * kNfCodeTile), 256, 0, st>>>(
+          s8, d8, E, halves, rows, src_k, K, layout);
+      break;
+    case 3:   // NF3 scales
+      repack_w16_scales_tiled_kernel<<<grid_for(tiles * kW16ScaleTile), 256, 0, st>>>(
+          s8, d8, E, halves, rows, src_k, K, 32, layout);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

@@ -133,6 +133,15 @@ TC_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
       ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// bulk_load with an L2 cache policy.
+TC_DEV void bulk_load_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                           uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 TC_DEV void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
 }
