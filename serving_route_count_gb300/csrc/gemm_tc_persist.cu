@@ -651,9 +651,9 @@ cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanD
                        st, true, p);
 }
 
-// The persistent fc2 serves every W4A8 tile width when the unit-per-CTA fc2 would run many
-// waves (measured: 39 -> 36 us at 3,750 units; slower than the unit-per-CTA kernel below ~2.5
-// waves).
+// The persistent fc2 serves every W4A8 tile width when the unit-per-CTA fc2 would run more
+// than 5 waves of one unit per SM (measured: 39 -> 36 us at 3,750 units, 2-3 % faster calls at
+// 1,000-2,000 units; slower than the unit-per-CTA kernel below ~2.5 waves).
 bool fc2_persist_preferred(int bn, int units) {
   static int sms = 0;
   if (sms == 0) {
@@ -664,7 +664,7 @@ bool fc2_persist_preferred(int bn, int units) {
       sms = 152;
     }
   }
-  return (bn == 16 || bn == 32 || bn == 64 || bn == 96) && units > 20 * sms;
+  return (bn == 16 || bn == 32 || bn == 64 || bn == 96) && units > 5 * sms;
 }
 
 template <int BN>
