@@ -317,13 +317,30 @@ finalize_kernel(int M, int H, int topk, int deterministic, const float* __restri
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = 0.f;
-      for (int j = 0; j < topk; ++j) {
-        const int f = t * topk + j;
-        if (slot_of[f] < 0) continue;
-        const float4* r4 = reinterpret_cast<const float4*>(rbuf + (size_t)f * H + c);
-        const float4 r0 = r4[0], r1 = r4[1];
-        v[0] += r0.x; v[1] += r0.y; v[2] += r0.z; v[3] += r0.w;
-        v[4] += r1.x; v[5] += r1.y; v[6] += r1.z; v[7] += r1.w;
+      // slots in groups of 8: their indices, then their rows, all loads of a group in flight
+      // together, added in slot order (the same sum on every run)
+      for (int j0 = 0; j0 < topk; j0 += 8) {
+        int so[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) so[j] = j0 + j < topk ? slot_of[t * topk + j0 + j] : -1;
+        float4 r[8][2];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (so[j] >= 0) {
+            const float4* r4 =
+                reinterpret_cast<const float4*>(rbuf + (size_t)(t * topk + j0 + j) * H + c);
+            r[j][0] = r4[0];
+            r[j][1] = r4[1];
+          } else {
+            r[j][0] = r[j][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (so[j] < 0) continue;
+          v[0] += r[j][0].x; v[1] += r[j][0].y; v[2] += r[j][0].z; v[3] += r[j][0].w;
+          v[4] += r[j][1].x; v[5] += r[j][1].y; v[6] += r[j][1].z; v[7] += r[j][1].w;
+        }
       }
     }
     uint32_t o[4];
