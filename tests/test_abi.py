@@ -94,3 +94,41 @@ def test_run_argument_checks_without_gpu(lib):
                                  None, ctypes.byref(out)) == 1
     moe.moe_destroy_plan(p)
     moe.moe_destroy_weight_plan(wp)
+
+
+def test_w4a16_tiled_weight_sizes(lib):
+    """NVFP4 and NF3 tiers are stored in tiles of 128 rows x 256 K per matrix: no padding at the
+    config's shapes (I = 512, H = 6144), zero padding up to whole tiles otherwise."""
+    E, H, I = 8, 6144, 512
+    wp = moe.moe_plan_weights(E, H, I, moe.MOE_W4A16_NVFP4)
+    codes = E * (2 * I * H // 2 + H * I // 2)
+    scales = E * (2 * I * H // 16 + H * I // 16)
+    assert codes + scales <= moe.moe_prepared_bytes(wp) <= codes + scales + 8 * 256 + 2 * E * 4
+    moe.moe_destroy_weight_plan(wp)
+    # I = 192: the fc1 row blocks (2 of 128 per half) and fc2's K (Ip = 256: one tile) padded
+    wp = moe.moe_plan_weights(E, 1280, 192, moe.MOE_W4A16_NVFP4)
+    tiles = E * (2 * 2 * 5 + 10 * 1)
+    assert moe.moe_prepared_bytes(wp) >= tiles * (16384 + 2048)
+    moe.moe_destroy_weight_plan(wp)
+
+
+def test_launch_counts(lib):
+    """Launches per call: W4A8 calls of at most 256 flat slots route and quantise in one launch,
+    larger ones in three (chunk counts, stable scatter, quantisation); then fc1, fc2, finalize.
+    The 16-bit path routes and converts in two; the CUDA-core backend adds the SwiGLU launch."""
+    p = moe.moe_plan(384, 7168, 576, 6, 4096, moe.MOE_W4A8_MXFP4, 7.0, 0)
+    assert moe.moe_call_launches(p, 0) == 0
+    assert moe.moe_call_launches(p, 16) == 4            # 96 slots
+    assert moe.moe_call_launches(p, 42) == 4            # 252 slots
+    assert moe.moe_call_launches(p, 43) == 6            # 258 slots
+    assert moe.moe_call_launches(p, 4096) == 6
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_call_launches(p, 4097)
+    assert ei.value.status == 4
+    moe.moe_destroy_plan(p)
+    p = moe.moe_plan(256, 6144, 512, 8, 64, moe.MOE_W4A16_NVFP4, float("inf"), 0)
+    assert moe.moe_call_launches(p, 8) == 5
+    moe.moe_plan_set_backend(p, 1)
+    assert moe.moe_call_launches(p, 8) == 6             # route, convert, fc1, act, fc2, finalize
+    moe.moe_destroy_plan(p)
+
