@@ -33,7 +33,6 @@ using namespace tc;
 constexpr int k16Threads = 320;           // producer, MMA issuer, 8 converter warps
 constexpr int k16RawK = 256;              // K elements per raw stage
 constexpr int k16SubK = 64;               // K elements per converted f16 sub-tile (128 B rows)
-constexpr int k16ATile = 128 * 128;       // one converted f16 sub-tile: 128 rows x 128 B
 constexpr int k16RawCodes = 128 * 128;    // raw codes region per matrix (NVFP4: 128 x 128 B)
 constexpr int k16RawScales = 128 * 16;    // raw scales region per matrix (128 rows x 16 B)
 
@@ -44,20 +43,26 @@ template <int BN, bool FC2>
 struct Tc16Cfg {
   static constexpr int kMats = FC2 ? 1 : 2;
   static constexpr int kRaw = kMats * (k16RawCodes + k16RawScales);     // per raw stage
-  static constexpr int kA = kMats * k16ATile;                           // per A slot
   static constexpr int kB = BN * 128;                                   // per B slot
-  // fc2's K (the intermediate size) is a couple of raw stages: short rings, so that two CTAs
-  // fit an SM.  fc1 (one CTA per SM): two raw stages and as many expanded sub-tiles as fit -
-  // the expanded ring decouples the converters from the MMA (with two slots the conversion and
-  // the MMA of consecutive sub-tiles ran in series)
-  static constexpr int kSr = 2;
-  static constexpr int kSa = FC2 ? 2 : (BN <= 32 ? 4 : (BN <= 64 ? 3 : 2));
+  // The expanded f16 weights go to tensor memory (the MMA's A operand), not shared memory:
+  // shared memory holds the raw stages and the activation sub-tiles only.  fc1 (one CTA per SM
+  // by its tensor memory): 4 raw stages; fc2 (K = the intermediate size, a couple of raw
+  // stages): 2, so that two CTAs fit an SM.
+  static constexpr int kSr = FC2 ? 2 : 4;
+  static constexpr int kSa = 4;                                         // expanded sub-tiles
   static constexpr int kSb = FC2 ? (BN <= 32 ? 8 : 4)
-                                 : (BN <= 16 ? 8 : (BN <= 32 ? 4 : (BN <= 64 ? 6 : 4)));
-  static constexpr int kSmem = kSr * kRaw + kSa * kA + kSb * kB + 1024;
+                                 : (BN <= 32 ? 8 : (BN <= 64 ? 6 : 4));
+  static constexpr int kSmem = kSr * kRaw + kSb * kB + 1024;
   static_assert(kSmem <= 227 * 1024, "shared memory");
-  static constexpr int kCols = kMats * BN;
-  static constexpr int kAlloc = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : 256;
+  // tensor memory: D (kMats x BN columns), then the expanded-A ring (kMats x 32 columns per
+  // 64-wide sub-tile: two f16 per column)
+  static constexpr int kColsD = kMats * BN;
+  static constexpr int kA0 = (kColsD + 31) / 32 * 32;
+  static constexpr int kASlot = kMats * 32;
+  static constexpr int kCols = kA0 + kSa * kASlot;
+  static constexpr int kAlloc = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128
+                                : kCols <= 256 ? 256 : 512;
+  static_assert(kCols <= 512, "tensor memory");
 };
 
 struct Tc16Params {
@@ -108,10 +113,11 @@ __device__ __forceinline__ uint32_t f16x2_bcast(uint32_t f16bits) {
   return (f16bits & 0xFFFFu) | (f16bits << 16);
 }
 
-// NVFP4 row r, K sub-tile q (64 elements), half h (elements 32h..32h+31) -> 4 chunks of 8 f16
-// (E2M1 x E4M3 scale, exact in f16) at chunks 4h..4h+3 of the 128-byte swizzled f16 row.
+// NVFP4 row r, K sub-tile q (64 elements), half h (elements 32h..32h+31) -> 16 f16x2 words in
+// K order (E2M1 x E4M3 scale, exact in f16).  Raw smem: the tile's 128-byte swizzled code rows
+// (16-byte chunk j at j ^ (r % 8)) and 16-byte scale rows.
 __device__ __forceinline__ void convert_nvfp4_half(const uint8_t* codes, const uint8_t* scales,
-                                                   uint8_t* dst, int r, int q, int h) {
+                                                   int r, int q, int h, uint32_t* out) {
   const int sw = r & 7;
   const uint4 c = *reinterpret_cast<const uint4*>(codes + r * 128 + (((2 * q + h) ^ sw) << 4));
   const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(scales + r * 16 + q * 4);
@@ -122,12 +128,10 @@ __device__ __forceinline__ void convert_nvfp4_half(const uint8_t* codes, const u
   for (int jj = 0; jj < 4; ++jj) {
     const uint32_t w = words[jj];
     const uint32_t s = sc[jj >> 1];
-    uint4 o;
-    o.x = hmul2(cvt_e2m1x2_f16x2(w & 0xFF), s);
-    o.y = hmul2(cvt_e2m1x2_f16x2((w >> 8) & 0xFF), s);
-    o.z = hmul2(cvt_e2m1x2_f16x2((w >> 16) & 0xFF), s);
-    o.w = hmul2(cvt_e2m1x2_f16x2(w >> 24), s);
-    *reinterpret_cast<uint4*>(dst + r * 128 + (((4 * h + jj) ^ sw) << 4)) = o;
+    out[4 * jj + 0] = hmul2(cvt_e2m1x2_f16x2(w & 0xFF), s);
+    out[4 * jj + 1] = hmul2(cvt_e2m1x2_f16x2((w >> 8) & 0xFF), s);
+    out[4 * jj + 2] = hmul2(cvt_e2m1x2_f16x2((w >> 16) & 0xFF), s);
+    out[4 * jj + 3] = hmul2(cvt_e2m1x2_f16x2(w >> 24), s);
   }
 }
 
@@ -152,12 +156,11 @@ __device__ __forceinline__ uint32_t nf3_pick2(const uint32_t* t, uint32_t c0, ui
   return (lo & ~m) | (hi & m);
 }
 
-// NF3 row r, K sub-tile q (64 codes), half h (codes 32h..32h+31: one scale group) -> 4 chunks of
-// 8 f16 at chunks 4h..4h+3 of the swizzled f16 row.  Raw smem: 32-byte rows of the tile's 2-bit
-// plane halves (bytes 0..31 at +0, 32..63 at +4096) and of its 1-bit plane (+8192).
+// NF3 row r, K sub-tile q (64 codes), half h (codes 32h..32h+31: one scale group) -> 16 f16x2
+// words in K order.  Raw smem: 32-byte rows of the tile's 2-bit plane halves (bytes 0..31 at +0,
+// 32..63 at +4096) and of its 1-bit plane (+8192).
 __device__ __forceinline__ void convert_nf3_half(const uint8_t* codes, const uint8_t* scales,
-                                                 uint8_t* dst, int r, int q, int h) {
-  const int sw = r & 7;
+                                                 int r, int q, int h, uint32_t* out) {
   const uint2 lo = *reinterpret_cast<const uint2*>(codes + (q >> 1) * 4096 + r * 32 +
                                                    (q & 1) * 16 + 8 * h);
   const uint32_t hi = *reinterpret_cast<const uint32_t*>(codes + 8192 + r * 32 + q * 8 + 4 * h);
@@ -168,15 +171,12 @@ __device__ __forceinline__ void convert_nf3_half(const uint8_t* codes, const uin
   for (int jj = 0; jj < 4; ++jj) {
     const uint32_t l16 = (low[jj >> 1] >> ((jj & 1) * 16)) & 0xFFFF;
     const uint32_t h8 = (hi >> (jj * 8)) & 0xFF;
-    uint32_t o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const uint32_t c0 = ((l16 >> (4 * e)) & 3) | (((h8 >> (2 * e)) & 1) << 2);
       const uint32_t c1 = ((l16 >> (4 * e + 2)) & 3) | (((h8 >> (2 * e + 1)) & 1) << 2);
-      o[e] = nf3_pick2(t, c0, c1);
+      out[4 * jj + e] = nf3_pick2(t, c0, c1);
     }
-    *reinterpret_cast<uint4*>(dst + r * 128 + (((4 * h + jj) ^ sw) << 4)) =
-        make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -200,7 +200,6 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   using Cfg = Tc16Cfg<BN, FC2>;
   constexpr int kMats = Cfg::kMats;
   pdl_wait_prev();     // previous kernel of the call complete, its writes visible
-  pdl_launch_next();
   const int tile = blockIdx.x;
   if (tile >= p.ctrl[1]) return;
   const int4 td = p.tiles[tile];
@@ -222,8 +221,7 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* raw_base = smem;
-  uint8_t* a_base = raw_base + Cfg::kSr * Cfg::kRaw;
-  uint8_t* b_base = a_base + Cfg::kSa * Cfg::kA;
+  uint8_t* b_base = raw_base + Cfg::kSr * Cfg::kRaw;
   __shared__ __align__(8) uint64_t raw_full[Cfg::kSr], raw_empty[Cfg::kSr];
   __shared__ __align__(8) uint64_t a_full[Cfg::kSa], a_empty[Cfg::kSa];
   __shared__ __align__(8) uint64_t b_full[Cfg::kSb], b_empty[Cfg::kSb];
@@ -257,6 +255,10 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the next kernel may launch only once every CTA of this one holds its tensor memory (fc1
+  // takes all of an SM's columns: a CTA of the next kernel allocating first would make it wait
+  // for columns that are freed only after this kernel completes)
+  pdl_launch_next();
   const uint32_t tmem = s_tmem;
   bool ok = true;
   int issued = 0, g = 0;   // raw stages filled, next activation sub-tile to load
@@ -302,7 +304,7 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
              mbar_wait(&b_full[sb], (g / Cfg::kSb) & 1, p.err);
         if (!ok) break;
         tc_fence_after();
-        const uint8_t* A = a_base + sa * Cfg::kA;
+        const uint32_t A = tmem + Cfg::kA0 + sa * Cfg::kASlot;
         const uint8_t* B = b_base + sb * Cfg::kB;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
@@ -310,7 +312,7 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
           const uint32_t acc = (g > 0 || kk > 0) ? 1u : 0u;
 #pragma unroll
           for (int m = 0; m < kMats; ++m)
-            mma_f16(tmem + m * BN, desc_sw128(A + m * k16ATile + 32 * kk), bd, idesc, acc);
+            mma_f16_ta(tmem + m * BN, A + m * 32 + 8 * kk, bd, idesc, acc);
         }
         tc_commit(&a_empty[sa]);
         tc_commit(&b_empty[sb]);
@@ -319,8 +321,10 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
     }
   } else {
     // converters: two threads per row of the 128-row weight block, each expanding one half of
-    // every 64-wide sub-tile (warps 2..5 the first half, 6..9 the second)
-    const int r = (tid - 64) & 127, half = (tid - 64) >> 7;
+    // every 64-wide sub-tile into tensor memory (warps 2..5 the first half, 6..9 the second; a
+    // warp handles the rows of its tensor-memory lane quadrant)
+    const int r = 32 * (warp & 3) + lane, half = (warp - 2) >> 2;
+    const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     if (FC2 && half == 0 && r < n) {
       // the combine's slot indices and router weights, read by these threads' epilogue
       const int f = p.perm[p0 + r];
@@ -337,17 +341,20 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
         const int sa = g % Cfg::kSa;
         if (g >= Cfg::kSa) ok = mbar_wait(&a_empty[sa], ((g / Cfg::kSa) - 1) & 1, p.err);
         if (!ok) break;
-        uint8_t* A = a_base + sa * Cfg::kA;
+        tc_fence_after();
 #pragma unroll
         for (int m = 0; m < kMats; ++m) {
           const uint8_t* c = st + m * k16RawCodes;
           const uint8_t* sc = st + kMats * k16RawCodes + m * k16RawScales;
+          uint32_t words[16];
           if (nf3)
-            convert_nf3_half(c, sc, A + m * k16ATile, r, q, half);
+            convert_nf3_half(c, sc, r, q, half, words);
           else
-            convert_nvfp4_half(c, sc, A + m * k16ATile, r, q, half);
+            convert_nvfp4_half(c, sc, r, q, half, words);
+          tmem_st16(trow + Cfg::kA0 + sa * Cfg::kASlot + m * 32 + 16 * half, words);
         }
-        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[sa]);
       }

@@ -201,6 +201,28 @@ TC_DEV void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] x B[smem]^T, f16 / bf16 operands, fp32 accumulation; A is M rows over
+// the 128 lanes, two 16-bit elements along K per 32-bit column (the even one in the low half).
+TC_DEV void mma_f16_ta(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns from registers; the warp writes its own quadrant.
+TC_DEV void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+// Waits until this thread's tcgen05.st stores have completed.
+TC_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // Arrive on `bar` once all tcgen05 operations issued so far by this thread have completed.
 TC_DEV void tc_commit(uint64_t* bar) {
   asm volatile(
