@@ -58,6 +58,7 @@ cudaError_t launch_repack_sf_atoms(const void* src, void* dst, int E, int halves
 cudaError_t launch_repack_w16_tiled(int kind, const void* src, void* dst, int E, int halves,
                                     int rows, int src_k, int K, int layout, cudaStream_t st);
 // gemm_tc16.cu
+bool tc16_fc1_pair(int bn, int quant);
 cudaError_t launch_tc16_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                               int bn, int tiles, int splits, const float* topk_w, int M,
                               cudaStream_t st);
@@ -128,13 +129,13 @@ int device_sms() {
 
 // K splits of the unit-per-CTA fc1 so that small calls still fill the CTA slots: the most
 // splits that keep the grid within one wave.  W4A8: two CTAs of the decode tile width per SM,
-// at least 4 K tiles of 128 per split.  W4A16: one CTA per SM (its rings of raw and expanded
-// weight stages), at least 2 raw stages of 256 per split (measured: splitting calls with more
-// units than SMs into several waves was slower).
-int fc1_splits(const PlanDims& d, int tiles) {
+// at least 4 K tiles of 128 per split.  W4A16: one or two CTAs per SM (tc16_fc1_pair), at least
+// 2 raw stages of 256 per split (measured: splitting calls with more units than SMs into
+// several waves was slower).
+int fc1_splits(const PlanDims& d, int tiles, int bn) {
   const int units = std::max(1, tiles * cdiv(d.I, 128));
   const bool a8 = d.quant == MOE_W4A8_MXFP4;
-  const int slots = (a8 ? kFc1CtasPerSm : 1) * device_sms();
+  const int slots = (a8 ? kFc1CtasPerSm : (tc16_fc1_pair(bn, d.quant) ? 2 : 1)) * device_sms();
   const int smax = a8 ? d.H / 128 / 4 : cdiv(d.H, 256) / 2;
   return std::max(1, std::min(std::min(slots / units, smax), 16));
 }
@@ -338,8 +339,8 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   // ([split][slot][2][Ip], one slice per split, summed in split order)
   size_t g_rows = Sm;
   for (int m = 1; m <= max_m; ++m) {
-    const int sp = fc1_splits(
-        d, call_tiles(d, s.max_tiles, m, tc_pick_bn(m, topk, E, quant_mode == MOE_W4A8_MXFP4)));
+    const int bn_m = tc_pick_bn(m, topk, E, quant_mode == MOE_W4A8_MXFP4);
+    const int sp = fc1_splits(d, call_tiles(d, s.max_tiles, m, bn_m), bn_m);
     if (sp > 1) g_rows = std::max(g_rows, (size_t)sp * m * topk);
   }
   s.g = take(g_rows * 2 * d.Ip * 4);
@@ -510,7 +511,7 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   // decode widths with more units than one wave of CTAs: the persistent stream-K fc1
   const bool streamk = tc8 && bn == 16 &&
                        (d.fc1_kernel == 0 ? fc1_stream_preferred(bn, tiles * RT) : d.fc1_kernel == 2);
-  const int splits = (tc && !streamk) ? fc1_splits(d, tiles) : 1;
+  const int splits = (tc && !streamk) ? fc1_splits(d, tiles, bn) : 1;
   // small W4A8 calls route and quantise in one launch
   const bool small = tc8 && route_actq_small_supported(Sm, d.E);
   // the W4A8 tensor-core kernels (16/32-token tiles) read activation-scale atoms from prepared

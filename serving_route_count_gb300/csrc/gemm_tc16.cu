@@ -39,7 +39,9 @@ constexpr int k16RawScales = 128 * 16;    // raw scales region per matrix (128 r
 __constant__ float c_nf3_lut16[8] = {-1.0f, -0.6047f, -0.3563f, -0.1275f,
                                      0.1275f, 0.3563f,  0.6047f,  1.0f};
 
-template <int BN, bool FC2>
+// PAIR: fc1 at two CTAs per SM (short rings; NVFP4-only layers at tile widths <= 32 - the NF3
+// expansion is heavier and runs better one CTA per SM)
+template <int BN, bool FC2, bool PAIR = false>
 struct Tc16Cfg {
   static constexpr int kMats = FC2 ? 1 : 2;
   static constexpr int kRaw = kMats * (k16RawCodes + k16RawScales);     // per raw stage
@@ -48,8 +50,8 @@ struct Tc16Cfg {
   // shared memory holds the raw stages and the activation sub-tiles only.  fc1 (one CTA per SM
   // by its tensor memory): 4 raw stages; fc2 (K = the intermediate size, a couple of raw
   // stages): 2, so that two CTAs fit an SM.
-  static constexpr int kSr = FC2 ? 2 : 4;
-  static constexpr int kSa = 4;                                         // expanded sub-tiles
+  static constexpr int kSr = (FC2 || PAIR) ? 2 : 4;
+  static constexpr int kSa = PAIR ? 3 : 4;                              // expanded sub-tiles
   static constexpr int kSb = FC2 ? (BN <= 32 ? 8 : 4)
                                  : (BN <= 32 ? 8 : (BN <= 64 ? 6 : 4));
   static constexpr int kSmem = kSr * kRaw + kSb * kB + 1024;
@@ -194,10 +196,10 @@ __device__ __forceinline__ uint16_t h_to_f16(float h, int32_t* err) {
   return __half_as_ushort(__float2half_rn(hb));
 }
 
-template <int BN, bool FC2>
+template <int BN, bool FC2, bool PAIR>
 __global__ void __launch_bounds__(k16Threads, 1)
 gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
-  using Cfg = Tc16Cfg<BN, FC2>;
+  using Cfg = Tc16Cfg<BN, FC2, PAIR>;
   constexpr int kMats = Cfg::kMats;
   pdl_wait_prev();     // previous kernel of the call complete, its writes visible
   const int tile = blockIdx.x;
@@ -498,21 +500,24 @@ static bool tmap_f16(CUtensorMap* tm, const void* base, int K, int rows, int box
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool FC2>
+template <int BN, bool FC2, bool PAIR = false>
 static cudaError_t launch16(const Tc16Params& p, int tiles, cudaStream_t st) {
-  using Cfg = Tc16Cfg<BN, FC2>;
+  using Cfg = Tc16Cfg<BN, FC2, PAIR>;
+  auto kernel = gemm_tc16_kernel<BN, FC2, PAIR>;
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(gemm_tc16_kernel<BN, FC2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         Cfg::kSmem);
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     // all of the unified L1 / shared storage as shared memory
-    cudaFuncSetAttribute(gemm_tc16_kernel<BN, FC2>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                          (int)cudaSharedmemCarveoutMaxShared);
     attr = true;
   }
   dim3 grid(tiles, p.RB, FC2 ? 1 : p.splits);
-  return launch_kernel(gemm_tc16_kernel<BN, FC2>, grid, dim3(k16Threads), Cfg::kSmem, st, true, p);
+  return launch_kernel(kernel, grid, dim3(k16Threads), Cfg::kSmem, st, true, p);
 }
+
+// fc1 of the W4A16 path at two CTAs per SM (NVFP4-only layers, token tiles of at most 32)
+bool tc16_fc1_pair(int bn, int quant) { return bn <= 32 && quant == kQuantNVFP4; }
 
 // stage 0: fc1 (+ SwiGLU, h -> bf16 -> f16), stage 1: fc2 (+ combine).
 cudaError_t launch_tc16_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
@@ -539,10 +544,13 @@ cudaError_t launch_tc16_stage(int stage, const DevWeights& w, const RunPtrs& r, 
   p.KT = KT; p.Sm = Sm; p.splits = fc2 ? 1 : splits; p.topk = d.topk;
   p.deterministic = d.deterministic; p.H = d.H; p.nf3_row_bytes = 3 * K / 8;
   p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
+  const bool pair = !fc2 && tc16_fc1_pair(bn, d.quant);
   switch (bn * 2 + (fc2 ? 1 : 0)) {
-    case 32: return launch16<16, false>(p, tiles, st);
+    case 32: return pair ? launch16<16, false, true>(p, tiles, st)
+                         : launch16<16, false>(p, tiles, st);
     case 33: return launch16<16, true>(p, tiles, st);
-    case 64: return launch16<32, false>(p, tiles, st);
+    case 64: return pair ? launch16<32, false, true>(p, tiles, st)
+                         : launch16<32, false>(p, tiles, st);
     case 65: return launch16<32, true>(p, tiles, st);
     case 128: return launch16<64, false>(p, tiles, st);
     case 129: return launch16<64, true>(p, tiles, st);
