@@ -226,8 +226,9 @@ moe_status moe_plan_set_profile_events(moe_plan_t* plan, void* const* events, in
 const char* moe_profile_stage_names(const moe_plan_t* plan);
 
 /* Number of kernel launches moe_run makes for a call of M tokens with this plan and backend
- * (routing and activation quantisation - one launch for W4A8 calls of at most 256 slots, three
- * for larger ones -, fc1, [SwiGLU on the CUDA-core path], fc2, finalize).  0 for M = 0.
+ * (routing and activation quantisation or conversion - one launch for tensor-core calls of at
+ * most 256 slots, three for larger W4A8 calls, two otherwise -, fc1, [SwiGLU on the CUDA-core
+ * path], fc2, finalize).  0 for M = 0.
  * Errors: MOE_ERR_ARG, MOE_ERR_CAPACITY (M > max_m). */
 moe_status moe_call_launches(const moe_plan_t* plan, int M, int* launches);
 

@@ -27,9 +27,9 @@ cudaError_t launch_actq_rows(const void* x, int M, int H, int topk, const RunPtr
                              size_t z2_words, cudaStream_t st);
 cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int tile_slots,
                                     int max_tiles, const void* x, int H, int topk,
-                                    const RunPtrs& r, bool atoms, void* z0, size_t z0_words,
-                                    void* z1, size_t z1_words, void* z2, size_t z2_words,
-                                    cudaStream_t st);
+                                    const RunPtrs& r, bool atoms, bool to_f16, void* z0,
+                                    size_t z0_words, void* z1, size_t z1_words, void* z2,
+                                    size_t z2_words, cudaStream_t st);
 // gemm_tc.cu
 cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                             int bn, int tiles, int splits, const float* topk_w, int M,
@@ -470,9 +470,10 @@ moe_status moe_call_launches(const moe_plan_t* plan, int M, int* launches) {
   }
   const bool tc8 = use_tc(d), t16 = use_tc16(d);
   if (tc8 || t16) {
-    // routing and quantisation (one launch for small W4A8 calls, three - counts, scatter,
-    // quantisation - for larger ones, two for the 16-bit path), fc1, fc2, finalize
-    const bool small = tc8 && route_actq_small_supported(M * d.topk, d.E);
+    // routing and quantisation / conversion (one launch for calls of at most 256 flat slots;
+    // beyond, three - counts, scatter, quantisation - for W4A8, two for the 16-bit path), fc1,
+    // fc2, finalize
+    const bool small = route_actq_small_supported(M * d.topk, d.E);
     *launches = (small ? 1 : (tc8 ? 3 : 2)) + 3;
     return MOE_OK;
   }
@@ -512,8 +513,8 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   const bool streamk = tc8 && bn == 16 &&
                        (d.fc1_kernel == 0 ? fc1_stream_preferred(bn, tiles * RT) : d.fc1_kernel == 2);
   const int splits = (tc && !streamk) ? fc1_splits(d, tiles, bn) : 1;
-  // small W4A8 calls route and quantise in one launch
-  const bool small = tc8 && route_actq_small_supported(Sm, d.E);
+  // small tensor-core calls route and quantise (W4A8) or convert (16-bit path) in one launch
+  const bool small = tc && route_actq_small_supported(Sm, d.E);
   // the W4A8 tensor-core kernels (16/32-token tiles) read activation-scale atoms from prepared
   // rows
   const bool atoms = tc8;
@@ -527,7 +528,7 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   cudaError_t e;
   if (small) {
     e = launch_route_actq_small(topk_ids, Sm, d.E, bn, plan->s.max_tiles, x, d.H, d.topk, r,
-                                atoms, acc, acc_words, g, g_words, tk, tk_words, st);
+                                atoms, t16, acc, acc_words, g, g_words, tk, tk_words, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
   } else if (tc8) {

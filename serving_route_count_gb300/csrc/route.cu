@@ -217,6 +217,20 @@ struct ZeroRegion {
   size_t words;   // 4-byte words, a multiple of 4
 };
 
+// Eight bf16 values -> f16 (exact within the f16 range; `ok` cleared when one lies outside it).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 u, bool& ok) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xFFFF0000u);
+    ok &= fabsf(a) <= 65504.f && fabsf(b) <= 65504.f;
+    o[j] = (uint32_t)__half_as_ushort(__float2half_rn(a)) |
+           ((uint32_t)__half_as_ushort(__float2half_rn(b)) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __global__ void __launch_bounds__(256)
 actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t* __restrict__ ctrl,
             const int32_t* __restrict__ perm, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
@@ -248,16 +262,7 @@ actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t*
       const int c = (int)(i % nc);
       const int t = perm[p] / topk;
       const uint4 u = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c * 8);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xFFFF0000u);
-        range_ok &= fabsf(a) <= 65504.f && fabsf(b) <= 65504.f;
-        o[j] = (uint32_t)__half_as_ushort(__float2half_rn(a)) |
-               ((uint32_t)__half_as_ushort(__float2half_rn(b)) << 16);
-      }
-      *reinterpret_cast<uint4*>(x16 + p * H + c * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(x16 + p * H + c * 8) = bf16x8_to_f16x8(u, range_ok);
     }
     if (!range_ok) atomicOr(err, kErrRange);
   }
@@ -284,8 +289,8 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
                         int32_t* __restrict__ perm, int32_t* __restrict__ slot_of,
                         int4* __restrict__ tiles, int32_t* __restrict__ ctrl,
                         uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
-                        uint8_t* __restrict__ xs16, int r16, ZeroRegion z0, ZeroRegion z1,
-                        ZeroRegion z2) {
+                        uint8_t* __restrict__ xs16, int r16, uint16_t* __restrict__ x16,
+                        ZeroRegion z0, ZeroRegion z1, ZeroRegion z2) {
   constexpr int NW = kSmallRouteThreads / 32;
   __shared__ int s_ids[kSmallRouteSlots];
   __shared__ int s_perm[kSmallRouteSlots];
@@ -360,18 +365,34 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
   }
   __syncthreads();
 
-  // MXFP8 quantisation of the slot-ordered rows (as actq_kernel)
+  // MXFP8 quantisation (W4A8) or the f16 copy (16-bit tensor-core path) of the slot-ordered
+  // rows, as actq_kernel does
   const size_t gtid = (size_t)blockIdx.x * blockDim.x + tid;
   const size_t gsz = (size_t)gridDim.x * blockDim.x;
-  const int nb = H / 32;
-  const size_t nblk = (size_t)total * nb;
-  for (size_t i = gtid; i < nblk; i += gsz) {
-    const size_t p = i / nb;
-    const int b = (int)(i % nb);
-    const int t = s_perm[p] / topk;
-    const uint32_t sb =
-        quantize_block32(x + (size_t)t * H + b * 32, xq + p * H + b * 32, xs + p * nb + b);
-    if (xs16 != nullptr) xs16[((size_t)(b >> 2) * r16 + p) * 16 + (b & 3)] = (uint8_t)sb;
+  if (xq != nullptr) {
+    const int nb = H / 32;
+    const size_t nblk = (size_t)total * nb;
+    for (size_t i = gtid; i < nblk; i += gsz) {
+      const size_t p = i / nb;
+      const int b = (int)(i % nb);
+      const int t = s_perm[p] / topk;
+      const uint32_t sb =
+          quantize_block32(x + (size_t)t * H + b * 32, xq + p * H + b * 32, xs + p * nb + b);
+      if (xs16 != nullptr) xs16[((size_t)(b >> 2) * r16 + p) * 16 + (b & 3)] = (uint8_t)sb;
+    }
+  }
+  if (x16 != nullptr) {
+    const int nc = H / 8;
+    const size_t nchunk = (size_t)total * nc;
+    bool range_ok = true;
+    for (size_t i = gtid; i < nchunk; i += gsz) {
+      const size_t p = i / nc;
+      const int c = (int)(i % nc);
+      const int t = s_perm[p] / topk;
+      const uint4 u = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c * 8);
+      *reinterpret_cast<uint4*>(x16 + p * H + c * 8) = bf16x8_to_f16x8(u, range_ok);
+    }
+    if (!range_ok) atomicOr(ctrl, kErrRange);
   }
   const ZeroRegion zs[3] = {z0, z1, z2};
 #pragma unroll
@@ -615,11 +636,11 @@ bool route_actq_small_supported(int Mk, int E) {
 
 cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int tile_slots,
                                     int max_tiles, const void* x, int H, int topk,
-                                    const RunPtrs& r, bool atoms, void* z0, size_t z0_words,
-                                    void* z1, size_t z1_words, void* z2, size_t z2_words,
-                                    cudaStream_t st) {
+                                    const RunPtrs& r, bool atoms, bool to_f16, void* z0,
+                                    size_t z0_words, void* z1, size_t z1_words, void* z2,
+                                    size_t z2_words, cudaStream_t st) {
   if (!route_actq_small_supported(Mk, E)) return cudaErrorInvalidValue;
-  const size_t work = std::max((size_t)Mk * (H / 32),
+  const size_t work = std::max((size_t)Mk * (to_f16 ? H / 8 : H / 32),
                                std::max(z0_words / 4, std::max(z1_words / 4, z2_words / 4)));
   int blocks = (int)std::min<size_t>((work + kSmallRouteThreads - 1) / kSmallRouteThreads,
                                      152 * 4);
@@ -628,9 +649,10 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int tile_
   return launch_kernel(route_actq_small_kernel, dim3(blocks), dim3(kSmallRouteThreads), 0, st,
                        false, ids, Mk, E, tile_slots, max_tiles,
                        reinterpret_cast<const __nv_bfloat16*>(x), H, topk, r.cnt, r.off, r.perm,
-                       r.slot_of, r.tiles, r.ctrl, r.xq, r.xs, atoms ? r.xs16 : nullptr, r.r16,
-                       ZeroRegion{z0, z0_words}, ZeroRegion{z1, z1_words},
-                       ZeroRegion{z2, z2_words});
+                       r.slot_of, r.tiles, r.ctrl, to_f16 ? nullptr : r.xq,
+                       to_f16 ? nullptr : r.xs, (atoms && !to_f16) ? r.xs16 : nullptr, r.r16,
+                       to_f16 ? r.x16 : nullptr, ZeroRegion{z0, z0_words},
+                       ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words});
 }
 
 cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int max_tiles,
