@@ -152,6 +152,15 @@ moe_status moe_plan_set_backend(moe_plan_t* plan, int backend);
  * Errors: MOE_ERR_ARG. */
 moe_status moe_plan_set_fc1_kernel(moe_plan_t* plan, int choice);
 
+/* Expert parallelism (moe_b12x_next.py `ep_remap` / `ep_remap_reference`): this plan's E
+ * experts are the global experts [first_expert, first_expert + E).  topk_ids then hold global
+ * ids; routing maps each to its local id (id - first_expert) on the device, and ids of other
+ * ranks' experts (and padding) contribute nothing to out.  The adapter's remap gives such slots
+ * weight 0 and some local expert; a weight-0 term adds an exact 0 to every output sum, so
+ * dropping the slot gives the same out and skips its GEMM rows.  Default 0 (ids are local).
+ * Errors: MOE_ERR_ARG (plan NULL, first_expert < 0 or first_expert + E > INT32_MAX). */
+moe_status moe_plan_set_expert_offset(moe_plan_t* plan, int first_expert);
+
 /* Size in bytes of the device scratch buffer moe_run needs (routing tables, quantised
  * activations, the fc1 -> fc2 intermediate, the combine buffer). */
 moe_status moe_scratch_bytes(const moe_plan_t* plan, size_t* bytes);
@@ -170,6 +179,16 @@ moe_status moe_scratch_bytes(const moe_plan_t* plan, size_t* bytes);
 moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* scratch,
                    size_t scratch_bytes, const void* x, const int32_t* topk_ids,
                    const float* topk_weights, void* out, int M, void* stream);
+
+/* moe_run for any M >= 0 (moe_b12x_next.py `_Geometry.forward`: the host loop over row chunks of
+ * the largest capacity).  Rows [s, s + max_m) run as one moe_run each, in order, on the same
+ * scratch and stream; every row's result is the one a single call of its chunk gives (so in
+ * deterministic mode bit-identical to those calls).  Pointers, alignment and errors as moe_run;
+ * the first failing chunk's status is returned and later chunks are not launched.  Graph
+ * capture works as for moe_run. */
+moe_status moe_run_chunked(const moe_plan_t* plan, const moe_prepared* weights, void* scratch,
+                           size_t scratch_bytes, const void* x, const int32_t* topk_ids,
+                           const float* topk_weights, void* out, int M, void* stream);
 
 /* moe_run without a caller-provided scratch buffer (the pages have no counterpart of this entry
  * point).  It is for callers that cannot allocate device memory: code running under another

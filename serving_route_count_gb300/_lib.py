@@ -40,8 +40,11 @@ SIGNATURES = {
     "moe_scratch_bytes": (c_int, [c_void_p, c_size_t_p]),
     "moe_plan_set_backend": (c_int, [c_void_p, c_int]),
     "moe_plan_set_fc1_kernel": (c_int, [c_void_p, c_int]),
+    "moe_plan_set_expert_offset": (c_int, [c_void_p, c_int]),
     "moe_run": (c_int, [c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p, c_void_p,
                         c_void_p, c_int, c_void_p]),
+    "moe_run_chunked": (c_int, [c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p,
+                                c_void_p, c_void_p, c_int, c_void_p]),
     "moe_run_static_scratch": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                        c_void_p, c_int, c_void_p]),
     "moe_io_bytes": (c_int, [c_void_p, c_size_t_p]),

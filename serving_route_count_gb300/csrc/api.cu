@@ -11,22 +11,22 @@
 
 namespace moe {
 // route.cu
-cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int max_tiles,
-                         const RunPtrs& r, cudaStream_t st);
+cudaError_t launch_route(const int32_t* ids, int Mk, int E, int ep_first, int tile_slots,
+                         int max_tiles, const RunPtrs& r, cudaStream_t st);
 cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
                         bool atoms, bool to_f16, void* z0, size_t z0_words, void* z1,
                         size_t z1_words, void* z2, size_t z2_words, cudaStream_t st);
 bool route_actq_small_supported(int Mk, int E);
 int route_chunks(int Mk);
-cudaError_t launch_route_count(const int32_t* ids, int Mk, int E, const RunPtrs& r,
-                               cudaStream_t st);
-cudaError_t launch_route_scatter(const int32_t* ids, int Mk, int E, int tile_slots,
+cudaError_t launch_route_count(const int32_t* ids, int Mk, int E, int ep_first,
+                               const RunPtrs& r, cudaStream_t st);
+cudaError_t launch_route_scatter(const int32_t* ids, int Mk, int E, int ep_first, int tile_slots,
                                  int max_tiles, const RunPtrs& r, cudaStream_t st);
 cudaError_t launch_actq_rows(const void* x, int M, int H, int topk, const RunPtrs& r, void* z0,
                              size_t z0_words, void* z1, size_t z1_words, void* z2,
                              size_t z2_words, cudaStream_t st);
-cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int tile_slots,
-                                    int max_tiles, const void* x, int H, int topk,
+cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_first,
+                                    int tile_slots, int max_tiles, const void* x, int H, int topk,
                                     const RunPtrs& r, bool atoms, bool to_f16, void* z0,
                                     size_t z0_words, void* z1, size_t z1_words, void* z2,
                                     size_t z2_words, cudaStream_t st);
@@ -315,6 +315,7 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   d.E = E; d.H = H; d.I = I; d.Ip = (int)align_up((size_t)I, 128); d.topk = topk; d.max_m = max_m;
   d.quant = quant_mode; d.deterministic = deterministic ? 1 : 0;
   d.limit = swiglu_limit; d.alpha = 1.f; d.beta = 0.f; d.backend = 0; d.fc1_kernel = 0;
+  d.ep_first = 0;
   const size_t Sm = (size_t)max_m * topk;
   Scratch& s = p->s;
   s.max_tiles = (int)std::min<size_t>(Sm, (Sm + kSimtSlots - 1) / kSimtSlots +
@@ -454,6 +455,13 @@ moe_status moe_plan_set_fc1_kernel(moe_plan_t* plan, int choice) {
   return MOE_OK;
 }
 
+moe_status moe_plan_set_expert_offset(moe_plan_t* plan, int first_expert) {
+  if (plan == nullptr || first_expert < 0 || first_expert > INT32_MAX - plan->d.E)
+    return MOE_ERR_ARG;
+  plan->d.ep_first = first_expert;
+  return MOE_OK;
+}
+
 moe_status moe_plan_set_backend(moe_plan_t* plan, int backend) {
   if (plan == nullptr || backend < 0 || backend > 1) return MOE_ERR_ARG;
   plan->d.backend = backend;
@@ -527,21 +535,22 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   prof(0);
   cudaError_t e;
   if (small) {
-    e = launch_route_actq_small(topk_ids, Sm, d.E, bn, plan->s.max_tiles, x, d.H, d.topk, r,
-                                atoms, t16, acc, acc_words, g, g_words, tk, tk_words, st);
+    e = launch_route_actq_small(topk_ids, Sm, d.E, d.ep_first, bn, plan->s.max_tiles, x, d.H,
+                                d.topk, r, atoms, t16, acc, acc_words, g, g_words, tk, tk_words,
+                                st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
   } else if (tc8) {
     // larger W4A8 calls: routing over many CTAs, quantisation straight into slot order
-    e = launch_route_count(topk_ids, Sm, d.E, r, st);
+    e = launch_route_count(topk_ids, Sm, d.E, d.ep_first, r, st);
     if (e == cudaSuccess)
-      e = launch_route_scatter(topk_ids, Sm, d.E, bn, plan->s.max_tiles, r, st);
+      e = launch_route_scatter(topk_ids, Sm, d.E, d.ep_first, bn, plan->s.max_tiles, r, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
     e = launch_actq_rows(x, M, d.H, d.topk, r, acc, acc_words, g, g_words, tk, tk_words, st);
     if (e != cudaSuccess) return cuda_status(e);
   } else {
-    e = launch_route(topk_ids, Sm, d.E, bn, plan->s.max_tiles, r, st);
+    e = launch_route(topk_ids, Sm, d.E, d.ep_first, bn, plan->s.max_tiles, r, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
     if (a8 || acc || g || t16) {
@@ -577,6 +586,23 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
     e = launch_simt_stage(stage, w, r, d, plan->s.max_tiles, x, topk_weights, out, M, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(3 + stage);
+  }
+  return MOE_OK;
+}
+
+moe_status moe_run_chunked(const moe_plan_t* plan, const moe_prepared* weights, void* scratch,
+                           size_t scratch_bytes, const void* x, const int32_t* topk_ids,
+                           const float* topk_weights, void* out, int M, void* stream) {
+  if (plan == nullptr || M < 0) return MOE_ERR_ARG;
+  if (M > 0 && (x == nullptr || topk_ids == nullptr || topk_weights == nullptr || out == nullptr))
+    return MOE_ERR_ARG;
+  const int cap = plan->d.max_m, H = plan->d.H, k = plan->d.topk;
+  for (int s = 0; s < M; s += cap) {
+    const moe_status rc = moe_run(
+        plan, weights, scratch, scratch_bytes, static_cast<const uint16_t*>(x) + (size_t)s * H,
+        topk_ids + (size_t)s * k, topk_weights + (size_t)s * k,
+        static_cast<uint16_t*>(out) + (size_t)s * H, std::min(cap, M - s), stream);
+    if (rc != MOE_OK) return rc;
   }
   return MOE_OK;
 }

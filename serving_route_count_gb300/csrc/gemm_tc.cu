@@ -80,7 +80,7 @@ struct TcFc1Params {
   // small calls (Mk <= kPreRouteSlots): the router ids, to route in shared memory ahead of the
   // routing launch (null: wait for its tables)
   const int32_t* ids;
-  int Mk, E, max_tiles;
+  int Mk, E, max_tiles, ep_first;
 };
 
 struct TcFc2Params {
@@ -104,7 +104,6 @@ __global__ void __launch_bounds__(kTcThreads)
 fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::kStages1;
-  pdl_launch_next();
   // the row blocks of a tile are adjacent in launch order (while the tiles fit the grid's y),
   // so the CTAs that read the same activation tile run together and share it through L2
   const int tile = p.fb_in_x ? blockIdx.y : blockIdx.x;
@@ -126,7 +125,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   int e_pre = -1;
   if (p.ids != nullptr) {
     int* scratch = reinterpret_cast<int*>(smem + (S - 1) * Cfg::kStage1);
-    const int nt = min(pre_route_tiles<kTcThreads>(p.ids, p.Mk, p.E, BN, scratch), p.max_tiles);
+    const int nt = min(pre_route_tiles<kTcThreads>(p.ids, p.Mk, p.E, p.ep_first, BN, scratch), p.max_tiles);
     if (tile >= nt) {
       pdl_wait_prev();
       return;
@@ -189,6 +188,9 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
     }
   }
   pdl_wait_prev();             // routing tables and activations complete
+  // fc2 reads the routing tables before its own wait: it may launch only once every CTA of
+  // this kernel has seen them complete
+  pdl_launch_next();
   const int4 td = p.tiles[tile];
   const int e = td.x, p0 = td.y, n = td.z;
   const TileLoad<BN> tl(n);
@@ -596,7 +598,7 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
     p.H = d.H; p.I = d.I; p.Ip = d.Ip; p.RT = RT; p.KT = d.H / 128; p.Sm = Sm;
     p.splits = splits; p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
     p.ids = (ids != nullptr && Sm <= kPreRouteSlots) ? ids : nullptr;
-    p.Mk = Sm; p.E = d.E; p.max_tiles = max_tiles;
+    p.Mk = Sm; p.E = d.E; p.max_tiles = max_tiles; p.ep_first = d.ep_first;
     switch (bn) {
       case 16: return launch_fc1_bn<16>(p, tiles, st);
       case 32: return launch_fc1_bn<32>(p, tiles, st);

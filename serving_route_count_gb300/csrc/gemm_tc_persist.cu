@@ -63,7 +63,7 @@ struct StreamFc1Params {
   // small calls (Mk <= kPreRouteSlots): the router ids, to route in shared memory ahead of the
   // routing launch (null: wait for its tables)
   const int32_t* ids;
-  int Mk, E, max_tiles;
+  int Mk, E, max_tiles, ep_first;
 };
 
 template <int BN>
@@ -71,7 +71,6 @@ __global__ void __launch_bounds__(kStreamThreads)
 fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   using Cfg = StreamCfg<BN>;
   constexpr int S = Cfg::kStages;
-  pdl_launch_next();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -86,7 +85,7 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   int* scratch = reinterpret_cast<int*>(smem + (S - 1) * Cfg::kStage);
   int n_tiles;
   if (p.ids != nullptr) {
-    n_tiles = min(pre_route_tiles<kStreamThreads>(p.ids, p.Mk, p.E, BN, scratch), p.max_tiles);
+    n_tiles = min(pre_route_tiles<kStreamThreads>(p.ids, p.Mk, p.E, p.ep_first, BN, scratch), p.max_tiles);
   } else {
     pdl_wait_prev();     // routing tables complete
     n_tiles = p.ctrl[1];
@@ -176,6 +175,9 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
     }
   }
   pdl_wait_prev();     // routing tables and activations complete
+  // fc2 reads the routing tables before its own wait: it may launch only once every CTA of
+  // this kernel has seen them complete
+  pdl_launch_next();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -644,7 +646,7 @@ cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanD
   p.H = d.H; p.I = d.I; p.Ip = d.Ip; p.RT = cdiv(d.I, 128); p.KT = d.H / 128; p.Sm = Sm;
   p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
   p.ids = (ids != nullptr && Sm <= kPreRouteSlots) ? ids : nullptr;
-  p.Mk = Sm; p.E = d.E; p.max_tiles = max_tiles;
+  p.Mk = Sm; p.E = d.E; p.max_tiles = max_tiles; p.ep_first = d.ep_first;
   static const int G = persistent_grid(fc1_stream_kernel<16>, StreamCfg<16>::kSmem,
                                        StreamCfg<16>::kAlloc, 2, kStreamMaxCtas);
   return launch_kernel(fc1_stream_kernel<16>, dim3(G), dim3(kStreamThreads), StreamCfg<16>::kSmem,

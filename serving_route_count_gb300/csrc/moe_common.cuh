@@ -158,7 +158,17 @@ struct PlanDims {
   float limit, alpha, beta;
   int backend;      // 0: tensor cores where implemented, 1: CUDA-core path
   int fc1_kernel;   // W4A8 fc1 at 16-token tiles: 0 automatic, 1 unit per CTA, 2 stream-K
+  int ep_first;     // global id of local expert 0; router ids outside [ep_first, ep_first + E)
+                    // belong to other ranks and are dropped
 };
+
+// Local id of router id `id` on a plan that owns the global experts [first, first + E): id -
+// first, or -1 for another rank's expert or padding.  Unsigned arithmetic, so no id overflows
+// (first + E <= INT_MAX, checked when the offset is set).
+__device__ __forceinline__ int local_expert(int id, int first, int E) {
+  const unsigned u = static_cast<unsigned>(id) - static_cast<unsigned>(first);
+  return u < static_cast<unsigned>(E) ? static_cast<int>(u) : -1;
+}
 
 // Pointers of one call, resolved from the scratch base.
 struct RunPtrs {

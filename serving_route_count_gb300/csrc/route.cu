@@ -80,7 +80,8 @@ __device__ int block_excl_scan(int v, int* total, int* s_warp) {
 __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile_slots, int max_tiles,
              int32_t* __restrict__ cnt, int32_t* __restrict__ off, int32_t* __restrict__ perm,
-             int32_t* __restrict__ slot_of, int4* __restrict__ tiles, int32_t* __restrict__ ctrl) {
+             int32_t* __restrict__ slot_of, int4* __restrict__ tiles, int32_t* __restrict__ ctrl,
+             int ep_first) {
   __shared__ int s_cnt[kMaxRouteExperts];
   __shared__ int s_base[kMaxRouteExperts];
   __shared__ int s_wc[kRouteWarps][kMaxRouteExperts / 4];  // per-warp counts, 8 bits each
@@ -95,7 +96,7 @@ route_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile_slots, int
     (&s_wc[0][0])[i] = 0;
   __syncthreads();
   for (int f = tid; f < Mk; f += kRouteThreads) {
-    int e = ids[f];
+    int e = local_expert(ids[f], ep_first, E);
     if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
   }
   __syncthreads();
@@ -142,7 +143,7 @@ route_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile_slots, int
   const unsigned lt_mask = (1u << lane) - 1u;
   for (int r0 = 0; r0 < Mk; r0 += kRouteThreads) {
     const int f = r0 + tid;
-    int e = f < Mk ? ids[f] : -1;
+    int e = f < Mk ? local_expert(ids[f], ep_first, E) : -1;
     const bool valid = f < Mk && e >= 0 && e < E;
     const int key = valid ? e : (E + lane);  // invalid slots never match a valid one
     const unsigned peers = __match_any_sync(0xffffffffu, key);
@@ -290,7 +291,7 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
                         int4* __restrict__ tiles, int32_t* __restrict__ ctrl,
                         uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
                         uint8_t* __restrict__ xs16, int r16, uint16_t* __restrict__ x16,
-                        ZeroRegion z0, ZeroRegion z1, ZeroRegion z2) {
+                        ZeroRegion z0, ZeroRegion z1, ZeroRegion z2, int ep_first) {
   constexpr int NW = kSmallRouteThreads / 32;
   __shared__ int s_ids[kSmallRouteSlots];
   __shared__ int s_perm[kSmallRouteSlots];
@@ -304,7 +305,7 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
   if (writer && tid == 0) ctrl[0] = 0;  // error word of this call
   for (int e = tid; e < E; e += kSmallRouteThreads) s_cnt[e] = 0;
   for (int f = tid; f < kSmallRouteSlots; f += kSmallRouteThreads) {
-    const int e = f < Mk ? ids[f] : -1;
+    const int e = f < Mk ? local_expert(ids[f], ep_first, E) : -1;
     s_ids[f] = (e >= 0 && e < E) ? e : -1;
   }
   __syncthreads();
@@ -417,7 +418,7 @@ constexpr int kChunkSlots = 1024;
 
 __global__ void __launch_bounds__(kRouteThreads)
 route_count_kernel(const int32_t* __restrict__ ids, int Mk, int E, int32_t* __restrict__ ctrl,
-                   int32_t* __restrict__ cc) {
+                   int32_t* __restrict__ cc, int ep_first) {
   __shared__ int s_cnt[kMaxRouteExperts];
   const int tid = threadIdx.x, c = blockIdx.x;
   pdl_wait_prev();     // previous kernel of the call complete, its writes visible
@@ -427,7 +428,7 @@ route_count_kernel(const int32_t* __restrict__ ids, int Mk, int E, int32_t* __re
   __syncthreads();
   const int f = c * kChunkSlots + tid;
   if (f < Mk) {
-    const int e = ids[f];
+    const int e = local_expert(ids[f], ep_first, E);
     if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
   }
   __syncthreads();
@@ -439,7 +440,7 @@ route_scatter_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile_sl
                      int max_tiles, const int32_t* __restrict__ cc, int32_t* __restrict__ cnt,
                      int32_t* __restrict__ off, int32_t* __restrict__ perm,
                      int32_t* __restrict__ slot_of, int4* __restrict__ tiles,
-                     int32_t* __restrict__ ctrl) {
+                     int32_t* __restrict__ ctrl, int ep_first) {
   __shared__ int s_base[kMaxRouteExperts];
   __shared__ int s_wc[kRouteWarps][kMaxRouteExperts / 4];  // per-warp counts, 8 bits each
   __shared__ int s_warp[32];
@@ -484,7 +485,7 @@ route_scatter_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile_sl
   __syncthreads();
 
   const int f = c * kChunkSlots + tid;
-  const int e = f < Mk ? ids[f] : -1;
+  const int e = f < Mk ? local_expert(ids[f], ep_first, E) : -1;
   const bool valid = f < Mk && e >= 0 && e < E;
   const int key = valid ? e : (E + lane);  // invalid slots never match a valid one
   const unsigned peers = __match_any_sync(0xffffffffu, key);
@@ -595,22 +596,22 @@ actq_rows_kernel(const __nv_bfloat16* __restrict__ x, int M, int H, int topk,
 
 int route_chunks(int Mk) { return (Mk + kChunkSlots - 1) / kChunkSlots; }
 
-cudaError_t launch_route_count(const int32_t* ids, int Mk, int E, const RunPtrs& r,
-                               cudaStream_t st) {
+cudaError_t launch_route_count(const int32_t* ids, int Mk, int E, int ep_first,
+                               const RunPtrs& r, cudaStream_t st) {
   static_assert(kMaxRouteExperts <= kRouteThreads, "one expert per thread");
   if (E > kMaxRouteExperts || Mk < 1) return cudaErrorInvalidValue;
   // first kernel of a call: an ordinary launch (the previous call may still read the tables)
   return launch_kernel(route_count_kernel, dim3(route_chunks(Mk)), dim3(kRouteThreads), 0, st,
-                       false, ids, Mk, E, r.ctrl, r.rcc);
+                       false, ids, Mk, E, r.ctrl, r.rcc, ep_first);
 }
 
-cudaError_t launch_route_scatter(const int32_t* ids, int Mk, int E, int tile_slots,
+cudaError_t launch_route_scatter(const int32_t* ids, int Mk, int E, int ep_first, int tile_slots,
                                  int max_tiles, const RunPtrs& r, cudaStream_t st) {
   if (E > kMaxRouteExperts || Mk < 1) return cudaErrorInvalidValue;
   return launch_kernel(route_scatter_kernel, dim3(route_chunks(Mk)), dim3(kRouteThreads), 0, st,
                        true, ids, Mk, E, tile_slots, max_tiles,
                        static_cast<const int32_t*>(r.rcc), r.cnt, r.off, r.perm, r.slot_of,
-                       r.tiles, r.ctrl);
+                       r.tiles, r.ctrl, ep_first);
 }
 
 cudaError_t launch_actq_rows(const void* x, int M, int H, int topk, const RunPtrs& r, void* z0,
@@ -634,9 +635,9 @@ bool route_actq_small_supported(int Mk, int E) {
   return Mk <= kSmallRouteSlots && E <= kMaxRouteExperts;
 }
 
-cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int tile_slots,
-                                    int max_tiles, const void* x, int H, int topk,
-                                    const RunPtrs& r, bool atoms, bool to_f16, void* z0,
+cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_first,
+                                    int tile_slots, int max_tiles, const void* x, int H,
+                                    int topk, const RunPtrs& r, bool atoms, bool to_f16, void* z0,
                                     size_t z0_words, void* z1, size_t z1_words, void* z2,
                                     size_t z2_words, cudaStream_t st) {
   if (!route_actq_small_supported(Mk, E)) return cudaErrorInvalidValue;
@@ -652,14 +653,15 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int tile_
                        r.slot_of, r.tiles, r.ctrl, to_f16 ? nullptr : r.xq,
                        to_f16 ? nullptr : r.xs, (atoms && !to_f16) ? r.xs16 : nullptr, r.r16,
                        to_f16 ? r.x16 : nullptr, ZeroRegion{z0, z0_words},
-                       ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words});
+                       ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words}, ep_first);
 }
 
-cudaError_t launch_route(const int32_t* ids, int Mk, int E, int tile_slots, int max_tiles,
-                         const RunPtrs& r, cudaStream_t st) {
+cudaError_t launch_route(const int32_t* ids, int Mk, int E, int ep_first, int tile_slots,
+                         int max_tiles, const RunPtrs& r, cudaStream_t st) {
   // first kernel of a call: an ordinary launch (the previous call may still read the tables)
   return launch_kernel(route_kernel, dim3(1), dim3(kRouteThreads), 0, st, false, ids, Mk, E,
-                       tile_slots, max_tiles, r.cnt, r.off, r.perm, r.slot_of, r.tiles, r.ctrl);
+                       tile_slots, max_tiles, r.cnt, r.off, r.perm, r.slot_of, r.tiles, r.ctrl,
+                       ep_first);
 }
 
 cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,

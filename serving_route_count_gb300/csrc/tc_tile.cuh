@@ -73,7 +73,8 @@ static __device__ __forceinline__ void write_act_sf_rows(uint8_t* dst, const uin
 
 // Routing of a small call in shared memory, ahead of the routing launch's tables: the experts
 // of the GEMM tile list, built as the routing launch builds it (experts in ascending order,
-// ceil(count / tile_slots) tiles each; ids outside [0, E) dropped), from the router ids alone.
+// ceil(count / tile_slots) tiles each; ids outside [ep_first, ep_first + E) dropped), from the
+// router ids alone.
 // A kernel chained behind the routing launch may read the ids before waiting for it (the ids
 // were complete when the routing launch passed its own wait), so it can request weights early.
 // scratch: (E + kPreRouteTiles + 32) ints of shared memory; on return scratch[E + t] is the
@@ -82,8 +83,8 @@ static __device__ __forceinline__ void write_act_sf_rows(uint8_t* dst, const uin
 constexpr int kPreRouteSlots = 256;   // calls of at most this many flat slots
 constexpr int kPreRouteTiles = 256;
 template <int NT>
-static __device__ int pre_route_tiles(const int32_t* ids, int Mk, int E, int tile_slots,
-                                      int* scratch) {
+static __device__ int pre_route_tiles(const int32_t* ids, int Mk, int E, int ep_first,
+                                      int tile_slots, int* scratch) {
   int* s_cnt = scratch;
   int* s_tile_e = scratch + E;
   int* s_red = scratch + E + kPreRouteTiles;
@@ -91,7 +92,7 @@ static __device__ int pre_route_tiles(const int32_t* ids, int Mk, int E, int til
   for (int e = tid; e < E; e += NT) s_cnt[e] = 0;
   __syncthreads();
   for (int f = tid; f < Mk; f += NT) {
-    const int e = __ldcg(ids + f);
+    const int e = local_expert(__ldcg(ids + f), ep_first, E);
     if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
   }
   __syncthreads();

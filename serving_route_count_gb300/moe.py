@@ -114,6 +114,11 @@ def moe_plan_set_fc1_kernel(plan, choice):
            "moe_plan_set_fc1_kernel")
 
 
+def moe_plan_set_expert_offset(plan, first_expert):
+    _check(_lib.load().moe_plan_set_expert_offset(_handle(plan), int(first_expert)),
+           "moe_plan_set_expert_offset")
+
+
 def moe_scratch_bytes(plan) -> int:
     n = ctypes.c_size_t()
     _check(_lib.load().moe_scratch_bytes(_handle(plan), ctypes.byref(n)), "moe_scratch_bytes")
@@ -134,6 +139,16 @@ def moe_run(plan, prepared, scratch: torch.Tensor, x, topk_ids, topk_weights, ou
     _check(_lib.load().moe_run(_handle(plan), _handle(prepared), _ptr(scratch),
                                scratch.numel() * scratch.element_size(), _ptr(x), _ptr(topk_ids),
                                _ptr(topk_weights), _ptr(out), int(M), _stream(stream)), "moe_run")
+
+
+def moe_run_chunked(plan, prepared, scratch: torch.Tensor, x, topk_ids, topk_weights, out,
+                    M=None, stream=None):
+    """moe_run for any number of rows: chunks of the plan's capacity, run in order."""
+    M = x.shape[0] if M is None else M
+    _check(_lib.load().moe_run_chunked(_handle(plan), _handle(prepared), _ptr(scratch),
+                                       scratch.numel() * scratch.element_size(), _ptr(x),
+                                       _ptr(topk_ids), _ptr(topk_weights), _ptr(out), int(M),
+                                       _stream(stream)), "moe_run_chunked")
 
 
 def moe_run_static_scratch(plan, prepared, x, topk_ids, topk_weights, out, M=None, stream=None):
@@ -265,7 +280,7 @@ class MoELayer:
 
     def __init__(self, ck, topk, max_m, swiglu_limit=float("inf"), deterministic=False,
                  alpha=None, beta=None, device="cuda", keep_checkpoint=False, backend=0,
-                 fc1_kernel=0):
+                 fc1_kernel=0, first_expert=0):
         self.E, self.H, self.I, self.topk, self.max_m = ck.E, ck.H, ck.I, topk, max_m
         self.quant = QUANT_OF[ck.quant]
         tier = ck.tier if ck.quant == "hybrid" else None
@@ -286,6 +301,8 @@ class MoELayer:
             moe_plan_set_backend(self.plan, backend)
         if fc1_kernel:
             moe_plan_set_fc1_kernel(self.plan, fc1_kernel)
+        if first_expert:
+            moe_plan_set_expert_offset(self.plan, first_expert)
         self.scratch = torch.empty(moe_scratch_bytes(self.plan), dtype=torch.uint8, device=device)
         self.device = device
         self._io = None

@@ -134,3 +134,17 @@ def test_launch_counts(lib):
     assert moe.moe_call_launches(p, 8) == 6             # route, convert, fc1, act, fc2, finalize
     moe.moe_destroy_plan(p)
 
+
+
+def test_expert_offset_arguments(lib):
+    """The expert offset of an expert-parallel plan: any first id with first + E within int32;
+    negative or overflowing offsets are argument errors."""
+    p = moe.moe_plan(192, 7168, 1152, 6, 512, moe.MOE_W4A8_MXFP4, 7.0, 0)
+    moe.moe_plan_set_expert_offset(p, 0)
+    moe.moe_plan_set_expert_offset(p, 192)
+    moe.moe_plan_set_expert_offset(p, 2**31 - 1 - 192)
+    for bad in (-1, 2**31 - 192):
+        with pytest.raises(moe.MoEError) as ei:
+            moe.moe_plan_set_expert_offset(p, bad)
+        assert ei.value.status == 1
+    moe.moe_destroy_plan(p)

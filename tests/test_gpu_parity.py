@@ -246,6 +246,74 @@ def test_prefill_ep_i1152_sampled(M, det):
     layer.close()
 
 
+@pytest.mark.parametrize("quant,M,backend,fc1_kernel", [
+    ("mxfp4", 5, 0, 0),       # one-launch routing + quantisation, fc1 tile list from the ids
+    ("mxfp4", 16, 0, 2),      # stream-K fc1 with its own tile list from the ids
+    ("mxfp4", 300, 0, 0),     # chunked routing over two 1024-slot chunks
+    ("mxfp4", 40, 1, 0),      # CUDA-core backend: single-CTA routing kernel
+    ("nvfp4", 8, 0, 0),       # one-launch routing + f16 conversion
+    ("nvfp4", 100, 0, 0),     # single-CTA routing, then conversion
+])
+def test_expert_offset_on_device(quant, M, backend, fc1_kernel):
+    """Expert parallelism on the device: a plan owning global experts [16, 32) of 48 takes
+    global router ids (plus -1 padding).  Routing tables must equal the oracle's for the local
+    ids with foreign ones dropped, and every row must match the oracle run on the adapter's
+    own remap of the same inputs (foreign slots: weight 0, some local expert), which the
+    dropped slots must reproduce."""
+    cfg = small_cfg(quant)
+    first, n_global = 16, 48
+    ck = S.make_checkpoint(cfg, seed=3000 + M)
+    rng = np.random.default_rng(4000 + M)
+    x = S.make_x(rng, M, cfg.H)
+    ids_g = S.zipf_topk(rng, M, n_global, cfg.topk, 0.6)
+    ids_g[rng.random(ids_g.shape) < 0.05] = -1
+    w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 2.5)
+    layer = _layer(ck, cfg.topk, M, 7.0, 1, backend=backend, fc1_kernel=fc1_kernel,
+                   first_expert=first)
+    got = run_layer(layer, x, ids_g, w)
+    st, code = layer.device_error()
+    assert st == 0 and code == 0, code
+    lid = ids_g.astype(np.int64) - first
+    local = np.where((lid >= 0) & (lid < cfg.E), lid, -1).astype(np.int32)
+    assert (local >= 0).any() and (local < 0).any()
+    for a, b in zip(layer.routing(M), O.route(local, cfg.E)):
+        assert np.array_equal(a, b)
+    ids_r, w_r = S.ep_mask_foreign(ids_g, w, first, cfg.E)
+    check_rows(got, ck, x, ids_r, w_r, 7.0)
+    # a row whose slots are all foreign gives 0 (the remap's weight-0 slots add exact zeros)
+    none = ~(local >= 0).any(axis=1)
+    assert np.all(got[none] == 0)
+    layer.close()
+
+
+@pytest.mark.parametrize("quant", ["mxfp4", "nvfp4"])
+def test_run_chunked_above_capacity(quant):
+    """M = 70 rows on a capacity-32 plan through the chunked entry point: three chunks (32, 32,
+    6) in order on one scratch.  Deterministic mode: bit-identical to three separate calls, and
+    every row within the bound of the oracle."""
+    from serving_route_count_gb300 import moe_run_chunked
+    cfg = small_cfg(quant)
+    ck = S.make_checkpoint(cfg, seed=5000)
+    rng = np.random.default_rng(5001)
+    M, cap = 70, 32
+    x = S.make_x(rng, M, cfg.H)
+    ids = S.uniform_topk(rng, M, cfg.E, cfg.topk)
+    ids[rng.random(ids.shape) < 0.05] = -1
+    w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 2.5)
+    layer = _layer(ck, cfg.topk, cap, 7.0, 1)
+    xt, it, wt = to_device(x, ids, w)
+    out = torch.empty((M, cfg.H), dtype=torch.bfloat16, device="cuda")
+    moe_run_chunked(layer.plan, layer.prep, layer.scratch, xt, it, wt, out)
+    got = out_bits(out)
+    st, code = layer.device_error()
+    assert st == 0 and code == 0, code
+    sep = np.concatenate([run_layer(layer, x[s:s + cap], ids[s:s + cap], w[s:s + cap])
+                          for s in range(0, M, cap)])
+    assert np.array_equal(got, sep)
+    check_rows(got, ck, x, ids, w, 7.0)
+    layer.close()
+
+
 def test_nvfp4_full_size_sampled():
     cfg = S.CONFIGS["w4a16_nvfp4"]
     ck = S.make_checkpoint(cfg)
