@@ -57,7 +57,15 @@ typedef enum {
   /* Per-expert tier map: NVFP4 (tier 4) or NF3 (tier 3, 8-entry LUT x E4M3 per 32), bf16
    * activations, both tiers summed by one top-k sum (hybrid_loader.py, class docstring and
    * the union-staging path of `_apply_b12x_nf3`). */
-  MOE_W4A16_HYBRID = 2
+  MOE_W4A16_HYBRID = 2,
+  /* The same tier map with the kept tier in MXFP4 (E2M1 + UE8M0 per 32, no global scale) and
+   * bf16 activations: hybrid_loader.py "v3" kept format `mxfp4_e8m0k32` (`create_weights`,
+   * `_build_kept_mxfp4`, A16 default).  Prepare turns each UE8M0 scale 2^(b-127) into an f16
+   * multiplier 2^(b - b_max + 13) with b_max the largest scale byte of the expert's matrix and
+   * moves 2^(b_max - 140) into a per-matrix fp32 factor, so E2M1 x multiplier is exact in f16
+   * for every group within 36 binades of the matrix's largest scale (groups further below are
+   * flushed to zero: their terms are < 2^-34 of the matrix's largest weights). */
+  MOE_W4A16_HYBRID_MX = 3
 } moe_quant_mode;
 
 typedef enum {
@@ -75,7 +83,8 @@ typedef struct moe_plan_s moe_plan_t;
 /* Checkpoint-layout expert tensors (device pointers, contiguous), as listed by
  * moe_b12x_next.py `_convert_layer` (MXFP4) and hybrid_loader.py `create_weights` (NVFP4 / NF3).
  * For MOE_W4A16_HYBRID the fp4 fields hold the NVFP4 tier compacted over its experts (in
- * ascending expert id) and the nf3 fields the NF3 tier likewise.
+ * ascending expert id) and the nf3 fields the NF3 tier likewise; for MOE_W4A16_HYBRID_MX the
+ * fp4 fields hold the kept tier in the MXFP4 layout below (compacted the same way).
  *   MXFP4: w13 [E, 2I, H/2] u8 (element 2j = low nibble of byte j), s13 [E, 2I, H/32] u8 E8M0,
  *          w2 [E, H, I/2] u8, s2 [E, H, I/32] u8 E8M0; g13 = g2 = NULL.
  *   NVFP4: w13 [E4, 2I, H/2], s13 [E4, 2I, H/16] u8 E4M3, g13 [E4] f32,
@@ -99,7 +108,8 @@ typedef struct {
  * `_Geometry.__init__` -> fm.plan_weights; B12xExperts `_prepare_experts`).
  *   E, H, I   experts, hidden size, intermediate size (per rank).  Requires H % 128 == 0,
  *             I % 64 == 0 (moe_b12x_next.py `create_weights` checks), E >= 1.
- *   tier_of_expert  host [E] int8 of MOE_TIER_NVFP4 / MOE_TIER_NF3 for MOE_W4A16_HYBRID,
+ *   tier_of_expert  host [E] int8 of MOE_TIER_NVFP4 (the kept 4-bit tier: NVFP4, or MXFP4
+ *             for MOE_W4A16_HYBRID_MX) / MOE_TIER_NF3 for MOE_W4A16_HYBRID(_MX),
  *             NULL otherwise.  Copied; the caller keeps ownership.
  * Errors: MOE_ERR_ARG (null out), MOE_ERR_SHAPE, MOE_ERR_UNSUPPORTED. */
 moe_status moe_plan_weights(int E, int H, int I, int quant_mode, int w13_layout,

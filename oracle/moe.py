@@ -13,6 +13,8 @@ Readings where the pages are silent (each one is listed with its reason in the d
     L = +inf means no clamp, which is the plain silu(g) * u of ``_apply_ref``.
   * W4A8: x is quantised to MXFP8 before fc1, h is quantised to MXFP8 before fc2 (from the
     unrounded SwiGLU output).  W4A16: x enters as bf16, h is rounded to bf16 before fc2.
+  * Hybrid layers: the kept tier is NVFP4, or MXFP4 for hybrid_loader.py's "v3" kept format
+    (``_build_kept_mxfp4``, A16 default); either way with bf16 activations.
   * The result is accumulated in fp64 over the top-k slots and rounded to bf16 once.
   * Routing order: the slots of expert e are listed in ascending (t, j) order (stable
     counting sort).

@@ -55,6 +55,9 @@ cudaError_t launch_repack_sf_atoms(const void* src, void* dst, int E, int halves
                                    int kblocks, int row_tiles, int k_tiles, int layout,
                                    cudaStream_t st);
 // kind: 0 NVFP4 codes, 1 NVFP4 scales, 2 NF3 codes, 3 NF3 scales
+cudaError_t launch_repack_mx16_scales(const void* src, void* dst, int32_t* kmax, float* g, int E,
+                                      int halves, int rows, int src_k, int K, int layout,
+                                      cudaStream_t st);
 cudaError_t launch_repack_w16_tiled(int kind, const void* src, void* dst, int E, int halves,
                                     int rows, int src_k, int K, int layout, cudaStream_t st);
 // gemm_tc16.cu
@@ -71,7 +74,7 @@ struct moe_weight_plan {
   int E4, E3;
   std::vector<int32_t> tier_map;  // (tier << 24) | local
   // section offsets in the prepared buffer
-  size_t w13, s13, w2, s2, g13, g2, nf_w13, nf_s13, nf_w2, nf_s2, tmap, total;
+  size_t w13, s13, w2, s2, g13, g2, mxk13, mxk2, nf_w13, nf_s13, nf_w2, nf_s2, tmap, total;
 };
 
 struct moe_prepared {
@@ -145,7 +148,7 @@ moe_status check_geometry(int E, int H, int I, int quant) {
   if (H < 128 || H % 128 != 0) return MOE_ERR_SHAPE;
   if (I < 64 || I % 64 != 0) return MOE_ERR_SHAPE;
   if ((long long)H * H > (1LL << 40) || (long long)I > (1 << 20)) return MOE_ERR_SHAPE;
-  if (quant < 0 || quant > 2) return MOE_ERR_UNSUPPORTED;
+  if (quant < 0 || quant > 3) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -177,13 +180,14 @@ moe_status moe_plan_weights(int E, int H, int I, int quant_mode, int w13_layout,
   moe_status st = check_geometry(E, H, I, quant_mode);
   if (st != MOE_OK) return st;
   if (w13_layout != MOE_W13_UP_GATE && w13_layout != MOE_W13_GATE_UP) return MOE_ERR_ARG;
-  if ((quant_mode == MOE_W4A16_HYBRID) != (tier_of_expert != nullptr)) return MOE_ERR_ARG;
+  const bool hybrid = quant_mode == MOE_W4A16_HYBRID || quant_mode == MOE_W4A16_HYBRID_MX;
+  if (hybrid != (tier_of_expert != nullptr)) return MOE_ERR_ARG;
   moe_weight_plan* wp = new (std::nothrow) moe_weight_plan();
   if (wp == nullptr) return MOE_ERR_ARG;
   wp->E = E; wp->H = H; wp->I = I; wp->Ip = (int)align_up((size_t)I, 128);
   wp->quant = quant_mode; wp->layout = w13_layout;
   wp->E4 = E; wp->E3 = 0;
-  if (quant_mode == MOE_W4A16_HYBRID) {
+  if (hybrid) {
     wp->E4 = wp->E3 = 0;
     wp->tier_map.resize(E);
     for (int e = 0; e < E; ++e) {
@@ -209,7 +213,7 @@ moe_status moe_plan_weights(int E, int H, int I, int quant_mode, int w13_layout,
     wp->w2 = take(E4 * H_ * Ip / 2);
     wp->s13 = take(E4 * 2 * (size_t)cdiv(I, 128) * (H_ / 128) * 512);
     wp->s2 = take(E4 * (H_ / 128) * (Ip / 128) * 512);
-    wp->g13 = wp->g2 = 0;
+    wp->g13 = wp->g2 = wp->mxk13 = wp->mxk2 = 0;
   } else {
     wp->w13 = take(E4 * t13 * kNvCodeTile);
     wp->w2 = take(E4 * t2 * kNvCodeTile);
@@ -217,6 +221,9 @@ moe_status moe_plan_weights(int E, int H, int I, int quant_mode, int w13_layout,
     wp->s2 = take(E4 * t2 * kW16ScaleTile);
     wp->g13 = take(E4 * 4);
     wp->g2 = take(E4 * 4);
+    const bool mx = quant_mode == MOE_W4A16_HYBRID_MX;
+    wp->mxk13 = mx ? take(E4 * 4) : 0;
+    wp->mxk2 = mx ? take(E4 * 4) : 0;
   }
   wp->nf_w13 = take(E3 * t13 * kNfCodeTile);
   wp->nf_s13 = take(E3 * t13 * kW16ScaleTile);
@@ -245,7 +252,8 @@ moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* 
   if (fp4 && (src->w13 == nullptr || src->s13 == nullptr || src->w2 == nullptr ||
               src->s2 == nullptr))
     return MOE_ERR_ARG;
-  if (fp4 && wp->quant != MOE_W4A8_MXFP4 && (src->g13 == nullptr || src->g2 == nullptr))
+  const bool mx16 = wp->quant == MOE_W4A16_HYBRID_MX;
+  if (fp4 && wp->quant != MOE_W4A8_MXFP4 && !mx16 && (src->g13 == nullptr || src->g2 == nullptr))
     return MOE_ERR_ARG;
   if (nf3 && (src->nf_w13 == nullptr || src->nf_s13 == nullptr || src->nf_w2 == nullptr ||
               src->nf_s2 == nullptr))
@@ -267,6 +275,16 @@ moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* 
                                  H / 128, L, st));
       chk(launch_repack_sf_atoms(src->s2, base + wp->s2, E4, 1, H, I / 32, H / 128, Ip / 128, L,
                                  st));
+    } else if (mx16) {
+      // UE8M0 per 32 -> f16 multipliers + per-expert factors (in the NVFP4 global's place)
+      chk(launch_repack_mx16_scales(src->s13, base + wp->s13,
+                                    reinterpret_cast<int32_t*>(base + wp->mxk13),
+                                    reinterpret_cast<float*>(base + wp->g13), E4, 2, I, H, H, L,
+                                    st));
+      chk(launch_repack_mx16_scales(src->s2, base + wp->s2,
+                                    reinterpret_cast<int32_t*>(base + wp->mxk2),
+                                    reinterpret_cast<float*>(base + wp->g2), E4, 1, H, I, Ip, L,
+                                    st));
     } else {
       chk(launch_repack_w16_tiled(1, src->s13, base + wp->s13, E4, 2, I, H, H, L, st));
       chk(launch_repack_w16_tiled(1, src->s2, base + wp->s2, E4, 1, H, I, Ip, L, st));
@@ -289,6 +307,7 @@ moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* 
   DevWeights& w = p->w;
   w.quant = wp->quant; w.E = wp->E; w.H = H; w.I = I; w.Ip = Ip; w.E4 = E4; w.E3 = E3;
   w.fp4_tiled = wp->quant == MOE_W4A8_MXFP4 ? 1 : 0;
+  w.mx_kept = mx16 ? 1 : 0;
   w.w13 = base + wp->w13; w.s13 = base + wp->s13; w.w2 = base + wp->w2; w.s2 = base + wp->s2;
   if (wp->quant != MOE_W4A8_MXFP4) {
     w.g13 = reinterpret_cast<const float*>(base + wp->g13);

@@ -97,6 +97,10 @@ __device__ __forceinline__ void load_w8(const DevWeights& w, int kind, int le, i
       byte = sf_atom_byte(cdiv(w.I, 128), w.H / 128, (size_t)le * 2 + half, i, k / 32);
     }
     sc = e8m0_to_f32((FC2 ? w.s2 : w.s13)[byte]);
+  } else if (w.mx_kept) {
+    // MXFP4 kept tier of the 16-bit path: the group's prepared f16 multiplier
+    sc = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(
+        (FC2 ? w.s2 : w.s13) + mx16_scale_off(mat, mr, k, rbs, kts))));
   } else {
     sc = e4m3_to_f32((FC2 ? w.s2 : w.s13)[nv_scale_byte(mat, mr, k, rbs, kts)]);
   }

@@ -3,9 +3,11 @@
 //
 // The NVFP4 kept tier and the NF3 tier of the hybrid layer (hybrid_loader.py: NVFP4 =
 // E2M1 x E4M3 scale per 16 x per-expert fp32 global; NF3 = 8-entry LUT x E4M3 scale per 32,
-// `_unpack_nf3`) run with bf16 activations.  There is no block-scaled MMA kind for a 16-bit
+// `_unpack_nf3`; "v3" MXFP4 kept tier = E2M1 x 2^(b-127) per 32, prepared as an f16 multiplier
+// per group and a per-matrix power-of-two factor) run with bf16 activations.  There is no block-scaled MMA kind for a 16-bit
 // operand, so the weights are expanded in shared memory ahead of the MMA (tcgen05 kind::f16):
 //   NVFP4: E2M1 x E4M3 has at most 6 significant bits and lies in [2^-10, 2688]: exact in f16;
+//   MXFP4: E2M1 x 2^j for j in [-23, 13] (the prepared multipliers): exact in f16;
 //   NF3:   bf16(fp32(LUT[c]) x fp32(scale)) (the page's unpack) is exact in f16 for E4M3 scales;
 //   activations: bf16 values are exact in f16 when |x| <= 65504 (larger values set an error
 //   bit; values below 2^-14 lose low bits as f16 subnormals).
@@ -75,7 +77,9 @@ struct Tc16Params {
   const uint8_t* nf_codes;    // NF3 planes, 12 KB tiles
   const uint8_t* nf_scales;   // NF3 scales, 2 KB tiles
   const int32_t* tier_map;    // hybrid: (tier << 24) | local; nullptr: every expert NVFP4
-  const float* gscale;        // NVFP4 per-expert global of this matrix ([E4])
+  const float* gscale;        // NVFP4 per-expert global of this matrix ([E4]); MXFP4 kept
+                              // tier: the matrix's power-of-two factor
+  int mx;                     // kept tier MXFP4 (f16 multiplier per group of 32)
   const int4* tiles;
   const int32_t* ctrl;
   int32_t* err;
@@ -117,14 +121,23 @@ __device__ __forceinline__ uint32_t f16x2_bcast(uint32_t f16bits) {
 
 // NVFP4 row r, K sub-tile q (64 elements), half h (elements 32h..32h+31) -> 16 f16x2 words in
 // K order (E2M1 x E4M3 scale, exact in f16).  Raw smem: the tile's 128-byte swizzled code rows
-// (16-byte chunk j at j ^ (r % 8)) and 16-byte scale rows.
+// (16-byte chunk j at j ^ (r % 8)) and 16-byte scale rows.  `mx`: the kept tier is MXFP4 and
+// the scale row holds one f16 multiplier per group of 32 (the half's two bytes) instead of two
+// E4M3 scales per half.
 __device__ __forceinline__ void convert_nvfp4_half(const uint8_t* codes, const uint8_t* scales,
-                                                   int r, int q, int h, uint32_t* out) {
+                                                   int r, int q, int h, bool mx, uint32_t* out) {
   const int sw = r & 7;
   const uint4 c = *reinterpret_cast<const uint4*>(codes + r * 128 + (((2 * q + h) ^ sw) << 4));
   const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(scales + r * 16 + q * 4);
-  const uint32_t s2 = cvt_e4m3x2_f16x2((sc4 >> (16 * h)) & 0xFFFF);
-  const uint32_t sc[2] = {f16x2_bcast(s2), f16x2_bcast(s2 >> 16)};
+  const uint32_t raw = (sc4 >> (16 * h)) & 0xFFFF;
+  uint32_t sc[2];
+  if (mx) {
+    sc[0] = sc[1] = f16x2_bcast(raw);
+  } else {
+    const uint32_t s2 = cvt_e4m3x2_f16x2(raw);
+    sc[0] = f16x2_bcast(s2);
+    sc[1] = f16x2_bcast(s2 >> 16);
+  }
   const uint32_t words[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
@@ -352,7 +365,7 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
           if (nf3)
             convert_nf3_half(c, sc, r, q, half, words);
           else
-            convert_nvfp4_half(c, sc, r, q, half, words);
+            convert_nvfp4_half(c, sc, r, q, half, p.mx != 0, words);
           tmem_st16(trow + Cfg::kA0 + sa * Cfg::kASlot + m * 32 + 16 * half, words);
         }
         tmem_wait_st();
@@ -537,6 +550,7 @@ cudaError_t launch_tc16_stage(int stage, const DevWeights& w, const RunPtrs& r, 
     return cudaErrorInvalidValue;
   p.tier_map = w.tier_map;
   p.gscale = fc2 ? w.g2 : w.g13;
+  p.mx = w.mx_kept;
   p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
   p.h16 = reinterpret_cast<uint16_t*>(r.h16); p.gacc = r.g; p.tickets = r.tickets;
   p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;

@@ -15,6 +15,7 @@ namespace moe {
 constexpr int kQuantW4A8 = 0;
 constexpr int kQuantNVFP4 = 1;
 constexpr int kQuantHybrid = 2;
+constexpr int kQuantHybridMx = 3;   // hybrid with the kept tier in MXFP4
 constexpr int kTierNVFP4 = 4;
 constexpr int kTierNF3 = 3;
 
@@ -51,6 +52,10 @@ __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 //     the tile (code c's low two bits at bits 2*(c%4) of byte c/4), then its 1-bit plane bytes
 //     0..31 (bit 2 of code c at bit c%8 of byte c/8);
 //   NF3 scales: 2 KB per tile, row r at r*16: the E4M3 scales of its 8 groups of 32, 8 zero.
+//   MXFP4 kept tier of the 16-bit path: codes as NVFP4; scales 2 KB per tile, row r at r*16:
+//     the f16 multipliers 2^(b - b_max + 13) of its 8 groups of 32 (b the UE8M0 byte, b_max
+//     the largest of the expert's matrix, kept per expert with the fp32 factor 2^(b_max - 140)
+//     in place of the NVFP4 global scale).
 // ----------------------------------------------------------------------------------------------
 struct DevWeights {
   int quant = 0;
@@ -62,8 +67,9 @@ struct DevWeights {
   const uint8_t* s13 = nullptr;       // MXFP4 atoms / NVFP4 scale tiles
   const uint8_t* w2 = nullptr;        // [E4][H][Ip/2]
   const uint8_t* s2 = nullptr;        // MXFP4 atoms / NVFP4 [E4][H][Ip/16]
-  const float* g13 = nullptr;         // [E4] NVFP4 global scales
+  const float* g13 = nullptr;         // [E4] NVFP4 global scales (MXFP4 kept tier: 2^shift)
   const float* g2 = nullptr;
+  int mx_kept = 0;                    // kept tier MXFP4: scale tiles hold f16 multipliers
   // NF3 tier
   const uint8_t* nf_w13 = nullptr;    // NF3 code tiles of [E3][2] matrices I x H
   const uint8_t* nf_s13 = nullptr;    // NF3 scale tiles
@@ -95,6 +101,11 @@ __host__ __device__ inline size_t nv_code_byte(size_t mat, int r, int k, int rbs
 __host__ __device__ inline size_t nv_scale_byte(size_t mat, int r, int k, int rbs, int kts) {
   return w16_tile(mat, r >> 7, k >> 8, rbs, kts) * kW16ScaleTile + (size_t)(r & 127) * 16 +
          ((k & 255) >> 4);
+}
+// MXFP4 kept tier: byte offset of the f16 multiplier of element k of row r
+__host__ __device__ inline size_t mx16_scale_off(size_t mat, int r, int k, int rbs, int kts) {
+  return w16_tile(mat, r >> 7, k >> 8, rbs, kts) * kW16ScaleTile + (size_t)(r & 127) * 16 +
+         ((k & 255) >> 5) * 2;
 }
 // NF3 2-bit plane byte of codes k..k+3 (k % 4 == 0) and 1-bit plane byte of codes k..k+7
 // (k % 8 == 0) of row r

@@ -136,6 +136,68 @@ __global__ void repack_w16_scales_tiled_kernel(const uint8_t* __restrict__ src,
   }
 }
 
+// MXFP4 kept tier of the 16-bit path, step 1: per expert, the largest UE8M0 scale byte of the
+// matrix (0xFF, NaN, left out) -> kmax[e], and the matrix's fp32 factor 2^(kmax - 140) -> g[e]
+// (built from its bits: normal down to 2^-126, subnormal below).  One CTA per expert.
+__global__ void mx_scale_max_kernel(const uint8_t* __restrict__ src, size_t per_expert,
+                                    int32_t* __restrict__ kmax, float* __restrict__ g) {
+  __shared__ int s_max[32];
+  const size_t e = blockIdx.x;
+  int m = -1;
+  for (size_t i = threadIdx.x; i < per_expert; i += blockDim.x) {
+    const int b = src[e * per_expert + i];
+    if (b != 0xFF && b > m) m = b;
+  }
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = max(m, s_max[w]);
+    if (m < 0) m = 140;                       // no finite scale: factor 1
+    const int x = m - 140;                    // factor exponent, -140 .. 114
+    const uint32_t bits = x >= -126 ? (uint32_t)(x + 127) << 23 : 1u << (x + 149);
+    kmax[e] = m;
+    g[e] = __uint_as_float(bits);
+  }
+}
+
+// Step 2: the scale tiles, each group's f16 multiplier 2^(b - kmax + 13): exponent j in
+// [-23, 13] (normal from 2^-14, subnormal below); groups below 2^-23 flushed to 0, NaN kept.
+__device__ __forceinline__ uint16_t mx_multiplier_f16(int b, int kmax) {
+  if (b == 0xFF) return 0x7E00;
+  const int j = b - kmax + 13;
+  if (j < -23) return 0;
+  return j >= -14 ? (uint16_t)((j + 15) << 10) : (uint16_t)(1u << (j + 24));
+}
+
+__global__ void repack_mx16_scales_tiled_kernel(const uint8_t* __restrict__ src,
+                                                const int32_t* __restrict__ kmax,
+                                                uint16_t* __restrict__ dst, int E, int halves,
+                                                int rows, int src_k, int K, int layout) {
+  const int rbs = (rows + 127) / 128, kts = (K + 255) / 256;
+  const size_t n = (size_t)E * halves * rbs * kts * (kW16ScaleTile / 2);
+  GRID_STRIDE(idx, n) {
+    const int off = (int)(idx % (kW16ScaleTile / 2));
+    size_t t = idx / (kW16ScaleTile / 2);
+    const int kt = (int)(t % kts);
+    t /= kts;
+    const int rb = (int)(t % rbs);
+    const size_t mat = t / rbs;
+    const int rr = off >> 3, b = off & 7;
+    const int r = rb * 128 + rr;
+    const int grp = kt * 8 + b;
+    uint16_t v = 0;
+    if (r < rows && grp < src_k / 32) {
+      const int half = (int)(mat % halves);
+      const size_t e = mat / halves;
+      const int sr = halves == 2 ? src_row_fc1(half, r, rows, layout) : r;
+      v = mx_multiplier_f16(src[(e * (size_t)(halves * rows) + sr) * (size_t)(src_k / 32) + grp],
+                            kmax[e]);
+    }
+    dst[idx] = v;
+  }
+}
+
 // NF3 code c of checkpoint row `sr` (3-byte groups of 8 codes), 0 beyond src_k.
 __device__ __forceinline__ uint32_t nf3_code(const uint8_t* src, size_t row_base, int c,
                                              int src_k) {
@@ -201,6 +263,21 @@ cudaError_t launch_repack_sf_atoms(const void* src, void* dst, int E, int halves
   repack_sf_atoms_kernel<<<grid_for(n), 256, 0, st>>>((const uint8_t*)src, (uint8_t*)dst, E,
                                                       halves, rows, kblocks, row_tiles, k_tiles,
                                                       layout);
+  return cudaGetLastError();
+}
+
+// MXFP4 kept tier scales: src [E][halves*rows][src_k/32] UE8M0 -> per-expert kmax / factor g,
+// then the f16 multiplier tiles.
+cudaError_t launch_repack_mx16_scales(const void* src, void* dst, int32_t* kmax, float* g, int E,
+                                      int halves, int rows, int src_k, int K, int layout,
+                                      cudaStream_t st) {
+  if (E == 0) return cudaSuccess;
+  const uint8_t* s8 = static_cast<const uint8_t*>(src);
+  mx_scale_max_kernel<<<E, 256, 0, st>>>(s8, (size_t)halves * rows * (src_k / 32), kmax, g);
+  const size_t n = (size_t)E * halves * ((rows + 127) / 128) * ((K + 255) / 256) *
+                   (kW16ScaleTile / 2);
+  repack_mx16_scales_tiled_kernel<<<grid_for(n), 256, 0, st>>>(
+      s8, kmax, static_cast<uint16_t*>(dst), E, halves, rows, src_k, K, layout);
   return cudaGetLastError();
 }
 

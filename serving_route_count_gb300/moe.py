@@ -16,6 +16,7 @@ from . import _lib
 MOE_W4A8_MXFP4 = 0
 MOE_W4A16_NVFP4 = 1
 MOE_W4A16_HYBRID = 2
+MOE_W4A16_HYBRID_MX = 3
 MOE_W13_UP_GATE = 0
 MOE_W13_GATE_UP = 1
 MOE_TIER_NVFP4 = 4
@@ -258,6 +259,14 @@ def moe_version() -> str:
 QUANT_OF = {"mxfp4": MOE_W4A8_MXFP4, "nvfp4": MOE_W4A16_NVFP4, "hybrid": MOE_W4A16_HYBRID}
 
 
+def quant_mode_of(ck) -> int:
+    """Library quant mode of a host checkpoint: a hybrid layer whose kept tier is MXFP4 is the
+    MXFP4-kept hybrid mode."""
+    if ck.quant == "hybrid" and ck.nv is not None and ck.nv.quant == "mxfp4":
+        return MOE_W4A16_HYBRID_MX
+    return QUANT_OF[ck.quant]
+
+
 def checkpoint_to_device(ck, device="cuda") -> dict:
     """Upload a host checkpoint (fields like synth.Checkpoint) as device tensors keyed like
     moe_checkpoint."""
@@ -282,7 +291,7 @@ class MoELayer:
                  alpha=None, beta=None, device="cuda", keep_checkpoint=False, backend=0,
                  fc1_kernel=0, first_expert=0):
         self.E, self.H, self.I, self.topk, self.max_m = ck.E, ck.H, ck.I, topk, max_m
-        self.quant = QUANT_OF[ck.quant]
+        self.quant = quant_mode_of(ck)
         tier = ck.tier if ck.quant == "hybrid" else None
         self.wp = moe_plan_weights(ck.E, ck.H, ck.I, self.quant, ck.layout, tier)
         dev_ck = checkpoint_to_device(ck, device)

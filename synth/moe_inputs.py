@@ -5,7 +5,8 @@ Shapes and value ranges follow the five workloads of the routed-MoE pages
 top-6, MXFP4 weights; vLLM ``hybrid_loader.py``: GLM-5.2 E=256, H=6144, I=512,
 top-8, NVFP4 + NF3).  Nothing here decodes or computes: codes and scales are
 uniform random bytes in the checkpoint tensor layouts the pages list
-(``_convert_layer`` shape checks; ``HybridNvFp4MoE.create_weights``).
+(``_convert_layer`` shape checks; ``HybridNvFp4MoE.create_weights``, whose "v3" kept tier is
+MXFP4 for hybrid-mapped layers).
 
 Checkpoint layouts (row-major, contiguous):
   MXFP4: w13 [E, 2I, H/2] u8 (two E2M1 per byte), s13 [E, 2I, H/32] u8 (E8M0),
@@ -38,7 +39,7 @@ class MoEConfig:
     H: int
     I: int
     topk: int
-    quant: str                 # "w4a8_mxfp4" | "w4a16_nvfp4" | "hybrid"
+    quant: str                 # "w4a8_mxfp4" | "w4a16_nvfp4" | "hybrid" | "hybrid_mx"
     swiglu_limit: float        # +inf = no clamp
     m_list: tuple
     routing: str = "uniform"   # "uniform" | "zipf"
@@ -48,7 +49,9 @@ class MoEConfig:
     pad_frac: float = 0.0      # last floor(M * pad_frac) rows are padding (id -1)
     scale_lo: int = 0          # scale byte range (E8M0 bytes or E4M3 codes)
     scale_hi: int = 0
-    n_nvfp4: int = 0           # hybrid: experts in the NVFP4 tier
+    n_nvfp4: int = 0           # hybrid: experts in the kept (NVFP4 or MXFP4) tier
+    kept_scale_lo: int = 0     # hybrid_mx: E8M0 byte range of the MXFP4 kept tier
+    kept_scale_hi: int = 0
     ep_local: int = 0          # >0: ids drawn over ep_global experts and masked to the local ones
     ep_global: int = 0
     seed_base: int = 0
@@ -95,6 +98,13 @@ CONFIGS = {
                                   quant="hybrid", swiglu_limit=INF, m_list=(8, 2048),
                                   routing="zipf", zipf_s=0.8, weight_rule="sigmoid_norm",
                                   scale_lo=0x08, scale_hi=0x48, n_nvfp4=64, seed_base=5000),
+    # Hybrid "v3": the same layer with the 64 kept experts in MXFP4 (E8M0 2^-8..2^-2) and bf16
+    # activations; NF3 tier as above.
+    "hybrid_mxfp4_nf3": MoEConfig("hybrid_mxfp4_nf3", E=256, H=6144, I=512, topk=8,
+                                  quant="hybrid_mx", swiglu_limit=INF, m_list=(8, 2048),
+                                  routing="zipf", zipf_s=0.8, weight_rule="sigmoid_norm",
+                                  scale_lo=0x08, scale_hi=0x48, n_nvfp4=64, kept_scale_lo=119,
+                                  kept_scale_hi=125, seed_base=5100),
 }
 
 
@@ -114,7 +124,7 @@ class Checkpoint:
     g2: Optional[np.ndarray] = None
     # hybrid only
     tier: Optional[np.ndarray] = None        # [E] int8, TIER_NVFP4 or TIER_NF3
-    nv: Optional["Checkpoint"] = None        # NVFP4 tier, compact over its experts
+    nv: Optional["Checkpoint"] = None        # kept tier (NVFP4, or MXFP4), compact over its experts
     nf: Optional["Checkpoint"] = None        # NF3 tier, compact over its experts
 
 
@@ -164,7 +174,7 @@ def make_checkpoint(cfg: MoEConfig, seed: Optional[int] = None, E: Optional[int]
         return make_fp4_checkpoint(rng, "mxfp4", E, H, I, cfg.scale_lo, cfg.scale_hi, layout)
     if cfg.quant == "w4a16_nvfp4":
         return make_fp4_checkpoint(rng, "nvfp4", E, H, I, cfg.scale_lo, cfg.scale_hi, layout)
-    if cfg.quant == "hybrid":
+    if cfg.quant in ("hybrid", "hybrid_mx"):
         n4 = min(cfg.n_nvfp4, E) if E != cfg.E else cfg.n_nvfp4
         # Which experts are kept in NVFP4 is a seeded random subset (the pages keep the top-64
         # by an importance score that synthetic weights do not have).
@@ -172,7 +182,12 @@ def make_checkpoint(cfg: MoEConfig, seed: Optional[int] = None, E: Optional[int]
         tier = np.full(E, TIER_NF3, dtype=np.int8)
         tier[kept] = TIER_NVFP4
         ck = Checkpoint(quant="hybrid", E=E, H=H, I=I, layout=layout, tier=tier)
-        ck.nv = make_fp4_checkpoint(rng, "nvfp4", n4, H, I, cfg.scale_lo, cfg.scale_hi, layout)
+        if cfg.quant == "hybrid_mx":
+            ck.nv = make_fp4_checkpoint(rng, "mxfp4", n4, H, I, cfg.kept_scale_lo,
+                                        cfg.kept_scale_hi, layout)
+        else:
+            ck.nv = make_fp4_checkpoint(rng, "nvfp4", n4, H, I, cfg.scale_lo, cfg.scale_hi,
+                                        layout)
         ck.nf = make_nf3_checkpoint(rng, E - n4, H, I, cfg.scale_lo, cfg.scale_hi, layout)
         return ck
     raise ValueError(cfg.quant)

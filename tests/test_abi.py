@@ -49,8 +49,19 @@ def test_plan_weights_shapes_and_sizes(lib):
     with pytest.raises(moe.MoEError):
         moe.moe_plan_weights(4, 256, 128, moe.MOE_W4A16_HYBRID, tier_of_expert=[4, 3, 5, 3])
     wp = moe.moe_plan_weights(4, 256, 128, moe.MOE_W4A16_HYBRID, tier_of_expert=[4, 3, 3, 4])
-    assert moe.moe_prepared_bytes(wp) > 0
+    nv_bytes = moe.moe_prepared_bytes(wp)
+    assert nv_bytes > 0
     moe.moe_destroy_weight_plan(wp)
+    # MXFP4 kept tier: the NVFP4 sections plus the per-expert scale maxima of both matrices
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_plan_weights(4, 256, 128, moe.MOE_W4A16_HYBRID_MX)
+    assert ei.value.status == 1
+    wp = moe.moe_plan_weights(4, 256, 128, moe.MOE_W4A16_HYBRID_MX, tier_of_expert=[4, 3, 3, 4])
+    assert moe.moe_prepared_bytes(wp) == nv_bytes + 2 * 256
+    moe.moe_destroy_weight_plan(wp)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_plan_weights(4, 256, 128, 4, tier_of_expert=[4, 3, 3, 4])
+    assert ei.value.status == 3
 
 
 def test_plan_and_scratch_sizes(lib):

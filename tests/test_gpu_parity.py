@@ -314,6 +314,47 @@ def test_run_chunked_above_capacity(quant):
     layer.close()
 
 
+@pytest.mark.parametrize("backend", [0, 1])
+def test_hybrid_mx_scale_window(backend):
+    """MXFP4 kept tier with scale bytes spread over the whole exact window (2^-40..2^-4: 36
+    binades below the largest) plus 1 % of groups 80 binades further down, which prepare
+    flushes to zero (terms below 2^-34 of the matrix's largest weights): every row within the
+    bound of the oracle, which keeps them."""
+    cfg = small_cfg("hybrid_mx", I=256)
+    ck = S.make_checkpoint(cfg, seed=6100)
+    rng = np.random.default_rng(6101)
+    for name in ("s13", "s2"):
+        sc = rng.integers(87, 124, size=getattr(ck.nv, name).shape, dtype=np.uint8)
+        sc[rng.random(sc.shape) < 0.01] = 5
+        setattr(ck.nv, name, sc)
+    M = 24
+    x = S.make_x(rng, M, cfg.H)
+    ids = S.zipf_topk(rng, M, cfg.E, cfg.topk, 0.8)
+    w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 1.0)
+    assert (ck.tier[ids] == S.TIER_NVFP4).any()
+    layer = _layer(ck, cfg.topk, M, math.inf, 1, backend=backend)
+    got = run_layer(layer, x, ids, w)
+    st, code = layer.device_error()
+    assert st == 0 and code == 0, code
+    check_rows(got, ck, x, ids, w, math.inf)
+    layer.close()
+
+
+def test_hybrid_mx_full_size_sampled():
+    """The "v3" hybrid layer at full size (E=256, H=6144, I=512, top-8; 64 MXFP4 + 192 NF3
+    experts, Zipf routing) at decode and prefill sizes: sampled rows against the oracle."""
+    cfg = S.CONFIGS["hybrid_mxfp4_nf3"]
+    ck = S.make_checkpoint(cfg)
+    for M, rows in ((8, [0, 3, 7]), (512, [0, 255, 511])):
+        x, ids, w = S.make_inputs(cfg, M)
+        layer = _layer(ck, cfg.topk, M, cfg.swiglu_limit, 1)
+        got = run_layer(layer, x, ids, w)
+        st, code = layer.device_error()
+        assert st == 0 and code == 0, code
+        check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=rows)
+        layer.close()
+
+
 def test_nvfp4_full_size_sampled():
     cfg = S.CONFIGS["w4a16_nvfp4"]
     ck = S.make_checkpoint(cfg)
@@ -430,11 +471,13 @@ def test_w4a8_intermediate_requant(backend):
 
 
 @pytest.mark.parametrize("quant,M,det", [("nvfp4", 5, 0), ("hybrid", 16, 1), ("nvfp4", 37, 1),
-                                         ("hybrid", 200, 0), ("hybrid", 600, 1)])
+                                         ("hybrid", 200, 0), ("hybrid", 600, 1),
+                                         ("hybrid_mx", 5, 1), ("hybrid_mx", 40, 0),
+                                         ("hybrid_mx", 200, 1)])
 def test_w4a16_tensor_core_tile_widths(quant, M, det):
-    """NVFP4 and the NVFP4 + NF3 hybrid through the 16-bit tcgen05 kernels (weights expanded to
-    f16 in shared memory) at every token-tile width, against the oracle on every row; the
-    CUDA-core backend must agree too.  E=16 (5 NVFP4 experts), H=1280, I=256."""
+    """NVFP4, the NVFP4 + NF3 hybrid and the MXFP4 + NF3 hybrid through the 16-bit tcgen05
+    kernels (weights expanded to f16) at every token-tile width, against the oracle on every
+    row; the CUDA-core backend must agree too.  E=16 (5 kept experts), H=1280, I=256."""
     cfg = small_cfg(quant, I=256)
     ck = S.make_checkpoint(cfg, seed=3000 + M)
     rng = np.random.default_rng(4000 + M)

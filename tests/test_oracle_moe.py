@@ -86,14 +86,16 @@ def test_swiglu_closed_forms():
 
 def _tiny(quant, seed=0, E=6, H=64, I=32, layout=S.W13_UP_GATE):
     cfg = {"mxfp4": S.CONFIGS["tiny_w4a8"], "nvfp4": S.CONFIGS["w4a16_nvfp4"],
-           "hybrid": S.CONFIGS["hybrid_nvfp4_nf3"]}[quant]
-    if quant == "hybrid":
+           "hybrid": S.CONFIGS["hybrid_nvfp4_nf3"],
+           "hybrid_mx": S.CONFIGS["hybrid_mxfp4_nf3"]}[quant]
+    if quant in ("hybrid", "hybrid_mx"):
         cfg = S.MoEConfig(**{**cfg.__dict__, "n_nvfp4": 2})
     ck = S.make_checkpoint(cfg, seed=seed, E=E, H=H, I=I, layout=layout)
     return cfg, ck
 
 
-@pytest.mark.parametrize("quant,layout", [("mxfp4", 0), ("mxfp4", 1), ("nvfp4", 0), ("hybrid", 0)])
+@pytest.mark.parametrize("quant,layout", [("mxfp4", 0), ("mxfp4", 1), ("nvfp4", 0), ("hybrid", 0),
+                                          ("hybrid_mx", 0), ("hybrid_mx", 1)])
 def test_forward_matches_bruteforce(quant, layout):
     cfg, ck = _tiny(quant, layout=layout)
     rng = np.random.default_rng(11)
@@ -112,6 +114,41 @@ def test_forward_matches_bruteforce(quant, layout):
     db = C.bf16_bits_to_f64(b)
     assert np.mean(da == db) > 0.999
     assert np.allclose(da, db, rtol=2 ** -7, atol=0)
+
+
+def _e4m3_code_of_pow2(j):
+    """E4M3 (bias 7) code of 2^j, j in [-9, 8]: normal exponent field from 2^-6, subnormal
+    mantissa below (value m * 2^-9)."""
+    assert -9 <= j <= 8
+    return (j + 7) << 3 if j >= -6 else 1 << (j + 9)
+
+
+def test_mxfp4_kept_tier_equals_nvfp4_on_shared_values():
+    """Hybrid layer with an MXFP4 kept tier (E2M1 x 2^(b-127) per 32) whose scales 2^-9..2^8
+    are also E4M3 values: rewritten as an NVFP4 kept tier (the same E2M1 codes, each E8M0 scale
+    as the E4M3 code of the same power of two for both groups of 16, global 1), the layer must
+    give the identical fp64 result: the MXFP4 dequantisation is pinned to the NVFP4 one."""
+    cfg, ck = _tiny("hybrid_mx", seed=3)
+    rng = np.random.default_rng(12)
+    for name in ("s13", "s2"):
+        setattr(ck.nv, name, rng.integers(118, 136, size=getattr(ck.nv, name).shape,
+                                          dtype=np.uint8))
+    nv = S.Checkpoint(quant="nvfp4", E=ck.nv.E, H=ck.H, I=ck.I, layout=ck.layout,
+                      w13=ck.nv.w13, w2=ck.nv.w2,
+                      g13=np.ones(ck.nv.E, np.float32), g2=np.ones(ck.nv.E, np.float32))
+    to_e4m3 = np.vectorize(lambda b: _e4m3_code_of_pow2(int(b) - 127), otypes=[np.uint8])
+    nv.s13 = np.repeat(to_e4m3(ck.nv.s13), 2, axis=-1)
+    nv.s2 = np.repeat(to_e4m3(ck.nv.s2), 2, axis=-1)
+    ck_nv = S.Checkpoint(quant="hybrid", E=ck.E, H=ck.H, I=ck.I, layout=ck.layout, tier=ck.tier,
+                         nv=nv, nf=ck.nf)
+    M, k = 6, 3
+    x = S.make_x(rng, M, ck.H)
+    ids = S.uniform_topk(rng, M, ck.E, k)
+    w = S.router_weights(rng, M, k, "softmax", 1.0)
+    a, fa = O.moe_forward(ck, x, ids, w, return_f64=True)
+    b, fb = O.moe_forward(ck_nv, x, ids, w, return_f64=True)
+    assert (ck.tier[ids] == S.TIER_NVFP4).any()
+    assert np.array_equal(fa, fb) and np.array_equal(a, b)
 
 
 def test_forward_full_tiny_config_bruteforce():
