@@ -162,6 +162,14 @@ moe_status moe_plan_set_backend(moe_plan_t* plan, int backend);
  * Errors: MOE_ERR_ARG. */
 moe_status moe_plan_set_fc1_kernel(moe_plan_t* plan, int choice);
 
+/* Router weights on the input (B12xExperts `process_weights_after_loading`:
+ * `apply_router_weight_on_input`, W4A16 only): on = 1 makes each slot's fc1 input
+ * bf16(x * bf16(w)) (the weight cast to the activations' dtype and multiplied in it) and adds
+ * the expert outputs with weight 1; on = 0 (default) weights the outputs.
+ * Errors: MOE_ERR_ARG (plan NULL, on not 0/1), MOE_ERR_UNSUPPORTED (on = 1 for W4A8, which
+ * the pages refuse too). */
+moe_status moe_plan_set_router_weight_on_input(moe_plan_t* plan, int on);
+
 /* Expert parallelism (moe_b12x_next.py `ep_remap` / `ep_remap_reference`): this plan's E
  * experts are the global experts [first_expert, first_expert + E).  topk_ids then hold global
  * ids; routing maps each to its local id (id - first_expert) on the device, and ids of other

@@ -149,11 +149,21 @@ def requant_h(h: np.ndarray, a8: bool) -> np.ndarray:
     return C.bf16_round(h)
 
 
+def slot_input(xin, w_slot, weight_on_input):
+    """fc1 input and combine weight of slots: x and w, or with the router weight applied to the
+    input (B12xExperts ``apply_router_weight_on_input``, W4A16 only) bf16(x * bf16(w)) and 1 -
+    reading: the weight is cast to the activations' dtype and multiplies them in it."""
+    if not weight_on_input:
+        return xin, w_slot
+    return C.bf16_round(xin * C.bf16_round(w_slot)[:, None]), np.ones_like(w_slot)
+
+
 def moe_forward(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.0,
-                rows=None, return_f64=False):
+                rows=None, return_f64=False, weight_on_input=False):
     """Per-expert dgemm form.  ``rows`` restricts the output to a subset of token rows
     (the other rows are not computed and come back as NaN).  Returns bf16 bit patterns
-    [M, H] (and the unrounded fp64 sum when ``return_f64``).
+    [M, H] (and the unrounded fp64 sum when ``return_f64``).  ``weight_on_input``: the router
+    weights scale fc1's input instead of the expert outputs (16-bit activations only).
     Pinned by tests/test_oracle_moe.py against the brute-force loop, closed forms and the
     invariants (linearity in the weights, padding rows, token-order invariance, w13 halves)."""
     x_bits = np.asarray(x_bits)
@@ -162,6 +172,7 @@ def moe_forward(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.
     M, k = ids.shape
     E, H, I = ck.E, ck.H, ck.I
     a8 = activation_a8(ck)
+    assert not (a8 and weight_on_input), "router weights on the input need 16-bit activations"
     out = np.zeros((M, H), dtype=np.float64)
     row_mask = np.ones(M, dtype=bool)
     if rows is not None:
@@ -177,12 +188,13 @@ def moe_forward(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.
         sel = valid & (ids == e)
         t_idx, j_idx = np.nonzero(sel)
         W13, W2, _ = expert_weights(ck, int(e))
-        G = xhat[t_idx] @ W13.T
+        xin, cw = slot_input(xhat[t_idx], w[t_idx, j_idx], weight_on_input)
+        G = xin @ W13.T
         gate, up = split_w13(G, I, ck.layout)
         h = swiglu(gate, up, limit, alpha, beta)
         hh = requant_h(h, a8)
         y = hh @ W2.T
-        np.add.at(out, t_idx, w[t_idx, j_idx][:, None] * y)
+        np.add.at(out, t_idx, cw[:, None] * y)
     out[~row_mask] = np.nan
     bits = C.f64_to_bf16_bits(np.where(row_mask[:, None], out, 0.0))
     if return_f64:
@@ -190,9 +202,11 @@ def moe_forward(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.
     return bits
 
 
-def slot_intermediate(ck, x_bits, topk_ids, limit=math.inf, alpha=1.0, beta=0.0):
+def slot_intermediate(ck, x_bits, topk_ids, limit=math.inf, alpha=1.0, beta=0.0, topk_w=None,
+                      weight_on_input=False):
     """The SwiGLU output h (fp64, before the fc2 quantisation) of every valid slot, in routing
-    order (row p belongs to flat slot perm[p]); shape [S, I]."""
+    order (row p belongs to flat slot perm[p]); shape [S, I].  With ``weight_on_input`` the
+    slots' inputs are scaled by ``topk_w`` as in moe_forward."""
     ids = np.asarray(topk_ids, dtype=np.int64)
     M, k = ids.shape
     a8 = activation_a8(ck)
@@ -204,14 +218,18 @@ def slot_intermediate(ck, x_bits, topk_ids, limit=math.inf, alpha=1.0, beta=0.0)
         if hi == lo:
             continue
         W13, _, _ = expert_weights(ck, e)
-        G = xhat[perm[lo:hi] // k] @ W13.T
+        fl = perm[lo:hi]
+        xin = xhat[fl // k]
+        if weight_on_input:
+            xin, _ = slot_input(xin, np.asarray(topk_w, np.float64).reshape(-1)[fl], True)
+        G = xin @ W13.T
         gate, up = split_w13(G, ck.I, ck.layout)
         out[lo:hi] = swiglu(gate, up, limit, alpha, beta)
     return out
 
 
 def requant_alternatives(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.0,
-                         rel=1e-4, rows=None):
+                         rel=1e-4, rows=None, weight_on_input=False):
     """Legitimate alternatives of the fc2 operand's rounding (reading: where floating point
     decides a quantised code, arithmetic exact to a relative error `rel` may land on either
     neighbour of a near-midpoint value).  For every output row (or the given rows) returns a list
@@ -221,7 +239,7 @@ def requant_alternatives(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0
     w = np.asarray(topk_w, dtype=np.float64)
     M, k = ids.shape
     a8 = activation_a8(ck)
-    h = slot_intermediate(ck, x_bits, ids, limit, alpha, beta)
+    h = slot_intermediate(ck, x_bits, ids, limit, alpha, beta, topk_w, weight_on_input)
     if a8:
         mask, alt = C.mxfp8_alternates(h, rel)
         q, s = C.mxfp8_quantize(h)
@@ -241,13 +259,17 @@ def requant_alternatives(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0
         e = int(ids[t, j])
         if e not in cache:
             cache[e] = expert_weights(ck, e)[1]
-        out[t].append(w[t, j] * (alt[p, i] - near[p, i]) * cache[e][:, i])
+        cw = 1.0 if weight_on_input else w[t, j]
+        out[t].append(cw * (alt[p, i] - near[p, i]) * cache[e][:, i])
     return out
 
 
-def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.0):
+def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.0,
+                           weight_on_input=False):
     """Token by token, slot by slot, element by element (pure Python loops; tiny inputs only).
-    Dequantises each weight element from its own code and scale with scalar decoders."""
+    Dequantises each weight element from its own code and scale with scalar decoders.
+    ``weight_on_input``: each input element becomes the bf16 rounding of x * bf16(w) and the
+    slot's output is added unweighted."""
     ids = np.asarray(topk_ids).tolist()
     w = np.asarray(topk_w, dtype=np.float64).tolist()
     M = len(ids)
@@ -288,6 +310,11 @@ def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1
             if not (0 <= e < E):
                 continue
             xt = xhat[t]
+            cw = w[t][j]
+            if weight_on_input:
+                wb = float(C.bf16_round(cw))
+                xt = [float(C.bf16_round(float(v) * wb)) for v in xt]
+                cw = 1.0
             gate = [0.0] * I
             up = [0.0] * I
             for i in range(I):
@@ -310,7 +337,7 @@ def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1
                 s = 0.0
                 for i in range(I):
                     s += weight("w2", e, r, i) * hh[i]
-                out[t][r] += w[t][j] * s
+                out[t][r] += cw * s
     return C.f64_to_bf16_bits(np.array(out))
 
 

@@ -14,8 +14,8 @@ namespace moe {
 cudaError_t launch_route(const int32_t* ids, int Mk, int E, int ep_first, int tile_slots,
                          int max_tiles, const RunPtrs& r, cudaStream_t st);
 cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
-                        bool atoms, bool to_f16, void* z0, size_t z0_words, void* z1,
-                        size_t z1_words, void* z2, size_t z2_words, cudaStream_t st);
+                        bool atoms, bool to_f16, const float* win, void* z0, size_t z0_words,
+                        void* z1, size_t z1_words, void* z2, size_t z2_words, cudaStream_t st);
 bool route_actq_small_supported(int Mk, int E);
 int route_chunks(int Mk);
 cudaError_t launch_route_count(const int32_t* ids, int Mk, int E, int ep_first,
@@ -27,9 +27,9 @@ cudaError_t launch_actq_rows(const void* x, int M, int H, int topk, const RunPtr
                              size_t z2_words, cudaStream_t st);
 cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_first,
                                     int tile_slots, int max_tiles, const void* x, int H, int topk,
-                                    const RunPtrs& r, bool atoms, bool to_f16, void* z0,
-                                    size_t z0_words, void* z1, size_t z1_words, void* z2,
-                                    size_t z2_words, cudaStream_t st);
+                                    const RunPtrs& r, bool atoms, bool to_f16, const float* win,
+                                    void* z0, size_t z0_words, void* z1, size_t z1_words,
+                                    void* z2, size_t z2_words, cudaStream_t st);
 // gemm_tc.cu
 cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                             int bn, int tiles, int splits, const float* topk_w, int M,
@@ -334,7 +334,7 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   d.E = E; d.H = H; d.I = I; d.Ip = (int)align_up((size_t)I, 128); d.topk = topk; d.max_m = max_m;
   d.quant = quant_mode; d.deterministic = deterministic ? 1 : 0;
   d.limit = swiglu_limit; d.alpha = 1.f; d.beta = 0.f; d.backend = 0; d.fc1_kernel = 0;
-  d.ep_first = 0;
+  d.ep_first = 0; d.w_on_input = 0;
   const size_t Sm = (size_t)max_m * topk;
   Scratch& s = p->s;
   s.max_tiles = (int)std::min<size_t>(Sm, (Sm + kSimtSlots - 1) / kSimtSlots +
@@ -474,6 +474,13 @@ moe_status moe_plan_set_fc1_kernel(moe_plan_t* plan, int choice) {
   return MOE_OK;
 }
 
+moe_status moe_plan_set_router_weight_on_input(moe_plan_t* plan, int on) {
+  if (plan == nullptr || (on != 0 && on != 1)) return MOE_ERR_ARG;
+  if (on && plan->d.quant == MOE_W4A8_MXFP4) return MOE_ERR_UNSUPPORTED;
+  plan->d.w_on_input = on;
+  return MOE_OK;
+}
+
 moe_status moe_plan_set_expert_offset(moe_plan_t* plan, int first_expert) {
   if (plan == nullptr || first_expert < 0 || first_expert > INT32_MAX - plan->d.E)
     return MOE_ERR_ARG;
@@ -551,12 +558,16 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   const size_t g_words = 0;
   void* tk = (tc && (splits > 1 || streamk)) ? r.tickets : nullptr;
   const size_t tk_words = tk ? align_up((size_t)tiles * RT, 4) : 0;
+  // router weights on the input (16-bit paths): they scale the f16 activations, and the
+  // combine adds the expert outputs with weight 1
+  const float* win = d.w_on_input ? topk_weights : nullptr;
+  const float* wcomb = d.w_on_input ? nullptr : topk_weights;
   prof(0);
   cudaError_t e;
   if (small) {
     e = launch_route_actq_small(topk_ids, Sm, d.E, d.ep_first, bn, plan->s.max_tiles, x, d.H,
-                                d.topk, r, atoms, t16, acc, acc_words, g, g_words, tk, tk_words,
-                                st);
+                                d.topk, r, atoms, t16, win, acc, acc_words, g, g_words, tk,
+                                tk_words, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
   } else if (tc8) {
@@ -573,7 +584,7 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
     if (a8 || acc || g || t16) {
-      e = launch_actq(x, M, d.H, d.topk, r, a8, atoms, t16, acc, acc_words, g, g_words, tk,
+      e = launch_actq(x, M, d.H, d.topk, r, a8, atoms, t16, win, acc, acc_words, g, g_words, tk,
                       tk_words, st);
       if (e != cudaSuccess) return cuda_status(e);
     }
@@ -592,7 +603,7 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
       e = launch_fc2_persist(w, r, d, bn, M, topk_weights, st);
     else
       e = tc8 ? launch_tc_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, nullptr, 0, st)
-              : launch_tc16_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, st);
+              : launch_tc16_stage(1, w, r, d, bn, tiles, 1, wcomb, M, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(4);
     e = launch_simt_stage(3, w, r, d, plan->s.max_tiles, x, topk_weights, out, M, st);

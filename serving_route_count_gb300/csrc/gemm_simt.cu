@@ -28,7 +28,8 @@ struct SimtArgs {
   DevWeights w;
   RunPtrs r;
   const void* x;               // bf16 [M][H]
-  const float* topk_w;         // [M][k]
+  const float* topk_w;         // [M][k] combine weights; nullptr: 1 (weights on the input)
+  const float* win;            // [M][k] router weights applied to fc1's input, or nullptr
   int M, topk, H, I, Ip, E;
   int quant, deterministic;
 };
@@ -115,9 +116,21 @@ __device__ __forceinline__ uint4 load_a8(const SimtArgs& a, int p, int k) {
   const bool a8 = a.quant == kQuantW4A8;
   if (!FC2) {
     if (!a8) {
-      const int t = a.r.perm[p] / a.topk;
-      return *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.x) +
-                                             (size_t)t * a.H + k);
+      const int f = a.r.perm[p], t = f / a.topk;
+      const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.x) +
+                                                      (size_t)t * a.H + k);
+      if (a.win == nullptr) return u;
+      const float wb = __bfloat162float(__float2bfloat16_rn(a.win[f]));
+      const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float v0 = __uint_as_float(in[i] << 16) * wb;
+        const float v1 = __uint_as_float(in[i] & 0xFFFF0000u) * wb;
+        o[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v0)) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v1)) << 16);
+      }
+      return make_uint4(o[0], o[1], o[2], o[3]);
     }
     // quantised activations are stored in slot order
     const uint2 q = *reinterpret_cast<const uint2*>(a.r.xq + (size_t)p * a.H + k);
@@ -239,7 +252,7 @@ gemm_simt_kernel(SimtArgs a) {
   } else {
     if (kind == kKindNVFP4 && a.w.g2 != nullptr) v *= a.w.g2[le];
     const int f = a.r.perm[p];
-    const float wt = a.topk_w[f];
+    const float wt = a.topk_w != nullptr ? a.topk_w[f] : 1.f;
     if (a.deterministic) {
       a.r.rbuf[(size_t)f * a.H + row] = wt * v;
     } else {
@@ -394,7 +407,10 @@ cudaError_t launch_simt_stage(int stage, const DevWeights& w, const RunPtrs& r,
   a.w = w;
   a.r = r;
   a.x = x;
-  a.topk_w = topk_w;
+  // router weights on the input (16-bit activations only): fc1 reads bf16(x * bf16(w)), the
+  // combine adds the expert outputs unweighted
+  a.topk_w = d.w_on_input ? nullptr : topk_w;
+  a.win = d.w_on_input ? topk_w : nullptr;
   a.M = M; a.topk = d.topk; a.H = d.H; a.I = d.I; a.Ip = d.Ip; a.E = d.E;
   a.quant = d.quant; a.deterministic = d.deterministic;
   const int Sm = M * d.topk;

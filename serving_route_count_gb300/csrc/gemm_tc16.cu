@@ -89,7 +89,7 @@ struct Tc16Params {
   int32_t* tickets;
   // fc2 outputs
   const int32_t* perm;
-  const float* topk_w;
+  const float* topk_w;        // combine weights; nullptr: 1 (router weights on the input)
   float* acc;
   float* rbuf;
   int K, R, I, Ip, RB, KT, Sm, splits, topk, deterministic, H, nf3_row_bytes;
@@ -344,7 +344,7 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
       // the combine's slot indices and router weights, read by these threads' epilogue
       const int f = p.perm[p0 + r];
       s_f[r] = f;
-      s_w[r] = p.topk_w[f];
+      s_w[r] = p.topk_w != nullptr ? p.topk_w[f] : 1.f;   // nullptr: weights on the input
     }
     int g = 0;
     for (int i = 0; i < nraw && ok; ++i) {

@@ -169,6 +169,7 @@ struct PlanDims {
   float limit, alpha, beta;
   int backend;      // 0: tensor cores where implemented, 1: CUDA-core path
   int fc1_kernel;   // W4A8 fc1 at 16-token tiles: 0 automatic, 1 unit per CTA, 2 stream-K
+  int w_on_input;   // 16-bit paths: router weights scale fc1's input, the combine is unweighted
   int ep_first;     // global id of local expert 0; router ids outside [ep_first, ep_first + E)
                     // belong to other ranks and are dropped
 };

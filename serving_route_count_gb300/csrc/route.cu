@@ -232,11 +232,31 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 u, bool& ok) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Eight bf16 values scaled by a router weight already rounded to bf16: bf16(x * w) each (the
+// product of two bf16 values is exact in fp32, then rounded to nearest even).
+__device__ __forceinline__ uint4 bf16x8_scale(uint4 u, float wb) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float a = __uint_as_float(w[j] << 16) * wb;
+    const float b = __uint_as_float(w[j] & 0xFFFF0000u) * wb;
+    o[j] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float bf16_round(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
 __global__ void __launch_bounds__(256)
 actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t* __restrict__ ctrl,
             const int32_t* __restrict__ perm, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
             uint8_t* __restrict__ xs16, int r16, uint16_t* __restrict__ x16,
-            int32_t* __restrict__ err, ZeroRegion z0, ZeroRegion z1, ZeroRegion z2) {
+            const float* __restrict__ win, int32_t* __restrict__ err, ZeroRegion z0,
+            ZeroRegion z1, ZeroRegion z2) {
   pdl_wait_prev();
   pdl_launch_next();
   const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -261,8 +281,9 @@ actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t*
     for (size_t i = gtid; i < nchunk; i += gsz) {
       const size_t p = i / nc;
       const int c = (int)(i % nc);
-      const int t = perm[p] / topk;
-      const uint4 u = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c * 8);
+      const int f = perm[p], t = f / topk;
+      uint4 u = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c * 8);
+      if (win != nullptr) u = bf16x8_scale(u, bf16_round(win[f]));   // weight on the input
       *reinterpret_cast<uint4*>(x16 + p * H + c * 8) = bf16x8_to_f16x8(u, range_ok);
     }
     if (!range_ok) atomicOr(err, kErrRange);
@@ -291,7 +312,8 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
                         int4* __restrict__ tiles, int32_t* __restrict__ ctrl,
                         uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
                         uint8_t* __restrict__ xs16, int r16, uint16_t* __restrict__ x16,
-                        ZeroRegion z0, ZeroRegion z1, ZeroRegion z2, int ep_first) {
+                        const float* __restrict__ win, ZeroRegion z0, ZeroRegion z1,
+                        ZeroRegion z2, int ep_first) {
   constexpr int NW = kSmallRouteThreads / 32;
   __shared__ int s_ids[kSmallRouteSlots];
   __shared__ int s_perm[kSmallRouteSlots];
@@ -389,8 +411,9 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
     for (size_t i = gtid; i < nchunk; i += gsz) {
       const size_t p = i / nc;
       const int c = (int)(i % nc);
-      const int t = s_perm[p] / topk;
-      const uint4 u = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c * 8);
+      const int f = s_perm[p], t = f / topk;
+      uint4 u = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c * 8);
+      if (win != nullptr) u = bf16x8_scale(u, bf16_round(win[f]));   // weight on the input
       *reinterpret_cast<uint4*>(x16 + p * H + c * 8) = bf16x8_to_f16x8(u, range_ok);
     }
     if (!range_ok) atomicOr(ctrl, kErrRange);
@@ -637,9 +660,9 @@ bool route_actq_small_supported(int Mk, int E) {
 
 cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_first,
                                     int tile_slots, int max_tiles, const void* x, int H,
-                                    int topk, const RunPtrs& r, bool atoms, bool to_f16, void* z0,
-                                    size_t z0_words, void* z1, size_t z1_words, void* z2,
-                                    size_t z2_words, cudaStream_t st) {
+                                    int topk, const RunPtrs& r, bool atoms, bool to_f16,
+                                    const float* win, void* z0, size_t z0_words, void* z1,
+                                    size_t z1_words, void* z2, size_t z2_words, cudaStream_t st) {
   if (!route_actq_small_supported(Mk, E)) return cudaErrorInvalidValue;
   const size_t work = std::max((size_t)Mk * (to_f16 ? H / 8 : H / 32),
                                std::max(z0_words / 4, std::max(z1_words / 4, z2_words / 4)));
@@ -652,7 +675,7 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_fi
                        reinterpret_cast<const __nv_bfloat16*>(x), H, topk, r.cnt, r.off, r.perm,
                        r.slot_of, r.tiles, r.ctrl, to_f16 ? nullptr : r.xq,
                        to_f16 ? nullptr : r.xs, (atoms && !to_f16) ? r.xs16 : nullptr, r.r16,
-                       to_f16 ? r.x16 : nullptr, ZeroRegion{z0, z0_words},
+                       to_f16 ? r.x16 : nullptr, to_f16 ? win : nullptr, ZeroRegion{z0, z0_words},
                        ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words}, ep_first);
 }
 
@@ -665,8 +688,8 @@ cudaError_t launch_route(const int32_t* ids, int Mk, int E, int ep_first, int ti
 }
 
 cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
-                        bool atoms, bool to_f16, void* z0, size_t z0_words, void* z1,
-                        size_t z1_words, void* z2, size_t z2_words, cudaStream_t st) {
+                        bool atoms, bool to_f16, const float* win, void* z0, size_t z0_words,
+                        void* z1, size_t z1_words, void* z2, size_t z2_words, cudaStream_t st) {
   const size_t work = std::max(
       std::max(quant_x ? (size_t)M * topk * (H / 32) : (size_t)0,
                to_f16 ? (size_t)M * topk * (H / 8) : (size_t)0),
@@ -678,7 +701,8 @@ cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r,
                        static_cast<const int32_t*>(r.ctrl), static_cast<const int32_t*>(r.perm),
                        quant_x ? r.xq : nullptr, quant_x ? r.xs : nullptr,
                        (quant_x && atoms) ? r.xs16 : nullptr, r.r16,
-                       to_f16 ? r.x16 : nullptr, r.ctrl, ZeroRegion{z0, z0_words},
+                       to_f16 ? r.x16 : nullptr, to_f16 ? win : nullptr, r.ctrl,
+                       ZeroRegion{z0, z0_words},
                        ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words});
 }
 

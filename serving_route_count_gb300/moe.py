@@ -115,6 +115,11 @@ def moe_plan_set_fc1_kernel(plan, choice):
            "moe_plan_set_fc1_kernel")
 
 
+def moe_plan_set_router_weight_on_input(plan, on):
+    _check(_lib.load().moe_plan_set_router_weight_on_input(_handle(plan), int(on)),
+           "moe_plan_set_router_weight_on_input")
+
+
 def moe_plan_set_expert_offset(plan, first_expert):
     _check(_lib.load().moe_plan_set_expert_offset(_handle(plan), int(first_expert)),
            "moe_plan_set_expert_offset")
@@ -289,7 +294,7 @@ class MoELayer:
 
     def __init__(self, ck, topk, max_m, swiglu_limit=float("inf"), deterministic=False,
                  alpha=None, beta=None, device="cuda", keep_checkpoint=False, backend=0,
-                 fc1_kernel=0, first_expert=0):
+                 fc1_kernel=0, first_expert=0, weight_on_input=False):
         self.E, self.H, self.I, self.topk, self.max_m = ck.E, ck.H, ck.I, topk, max_m
         self.quant = quant_mode_of(ck)
         tier = ck.tier if ck.quant == "hybrid" else None
@@ -312,6 +317,8 @@ class MoELayer:
             moe_plan_set_fc1_kernel(self.plan, fc1_kernel)
         if first_expert:
             moe_plan_set_expert_offset(self.plan, first_expert)
+        if weight_on_input:
+            moe_plan_set_router_weight_on_input(self.plan, 1)
         self.scratch = torch.empty(moe_scratch_bytes(self.plan), dtype=torch.uint8, device=device)
         self.device = device
         self._io = None

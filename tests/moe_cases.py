@@ -42,7 +42,8 @@ def _row_ok(got_row_bits, ref_row):
     return rel[0] <= REL_L2_BOUND and mx[0] <= MAX_ERR_BOUND, rel[0], mx[0]
 
 
-def check_rows(got_bits, ck, x_bits, ids, w, limit, rows=None, alpha=1.0, beta=0.0):
+def check_rows(got_bits, ck, x_bits, ids, w, limit, rows=None, alpha=1.0, beta=0.0,
+               weight_on_input=False):
     """Compare the given rows (all when None) with the oracle; returns (rel, mx) arrays.
 
     A row that misses the bound passes if the oracle's own alternatives of near-midpoint
@@ -50,11 +51,13 @@ def check_rows(got_bits, ck, x_bits, ids, w, limit, rows=None, alpha=1.0, beta=0
     bring it within the bound: those elements are decided by fp32 noise, both roundings are
     correct results of the method."""
     rows = np.arange(ids.shape[0]) if rows is None else np.asarray(rows)
-    _, f64 = O.moe_forward(ck, x_bits, ids, w, limit, alpha, beta, rows=rows, return_f64=True)
+    _, f64 = O.moe_forward(ck, x_bits, ids, w, limit, alpha, beta, rows=rows, return_f64=True,
+                           weight_on_input=weight_on_input)
     rel, mx = O.row_errors(got_bits[rows], f64[rows])
     bad = [int(r) for r, a, b in zip(rows, rel, mx) if a > REL_L2_BOUND or b > MAX_ERR_BOUND]
     if bad:
-        alts = O.requant_alternatives(ck, x_bits, ids, w, limit, alpha, beta, REQUANT_REL, bad)
+        alts = O.requant_alternatives(ck, x_bits, ids, w, limit, alpha, beta, REQUANT_REL, bad,
+                                      weight_on_input)
         for r in bad:
             d = alts[r]
             assert 0 < len(d) <= 10, (r, "outside the bound with", len(d), "ambiguous elements",

@@ -159,3 +159,19 @@ def test_expert_offset_arguments(lib):
             moe.moe_plan_set_expert_offset(p, bad)
         assert ei.value.status == 1
     moe.moe_destroy_plan(p)
+
+
+def test_router_weight_on_input_arguments(lib):
+    """Router weights on the input: 16-bit activation modes only (the pages refuse W4A8 too)."""
+    p = moe.moe_plan(8, 256, 128, 1, 16, moe.MOE_W4A8_MXFP4, 7.0, 0)
+    moe.moe_plan_set_router_weight_on_input(p, 0)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_plan_set_router_weight_on_input(p, 1)
+    assert ei.value.status == 3
+    moe.moe_destroy_plan(p)
+    p = moe.moe_plan(8, 256, 128, 1, 16, moe.MOE_W4A16_NVFP4, float("inf"), 0)
+    moe.moe_plan_set_router_weight_on_input(p, 1)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_plan_set_router_weight_on_input(p, 2)
+    assert ei.value.status == 1
+    moe.moe_destroy_plan(p)

@@ -355,6 +355,29 @@ def test_hybrid_mx_full_size_sampled():
         layer.close()
 
 
+@pytest.mark.parametrize("quant,M,det,backend", [("nvfp4", 6, 1, 0), ("hybrid", 16, 0, 0),
+                                                 ("hybrid_mx", 40, 1, 0), ("nvfp4", 300, 0, 0),
+                                                 ("hybrid", 24, 1, 1)])
+def test_router_weight_on_input(quant, M, det, backend):
+    """Router weights applied to fc1's input (16-bit paths): one-launch and two-launch routing,
+    several tile widths, both combines and the CUDA-core backend, against the oracle with the
+    same option on every row; top-1 (the usual use) and top-4."""
+    topk = 1 if M >= 100 else 4
+    cfg = small_cfg(quant, I=256, topk=topk)
+    ck = S.make_checkpoint(cfg, seed=7000 + M)
+    rng = np.random.default_rng(7001 + M)
+    x = S.make_x(rng, M, cfg.H)
+    ids = S.zipf_topk(rng, M, cfg.E, topk, 0.8)
+    ids[rng.random(ids.shape) < 0.05] = -1
+    w = S.router_weights(rng, M, topk, "sigmoid_norm", 2.5)
+    layer = _layer(ck, topk, M, math.inf, det, backend=backend, weight_on_input=True)
+    got = run_layer(layer, x, ids, w)
+    st, code = layer.device_error()
+    assert st == 0 and code == 0, code
+    check_rows(got, ck, x, ids, w, math.inf, weight_on_input=True)
+    layer.close()
+
+
 def test_nvfp4_full_size_sampled():
     cfg = S.CONFIGS["w4a16_nvfp4"]
     ck = S.make_checkpoint(cfg)

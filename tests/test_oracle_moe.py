@@ -116,6 +116,44 @@ def test_forward_matches_bruteforce(quant, layout):
     assert np.allclose(da, db, rtol=2 ** -7, atol=0)
 
 
+@pytest.mark.parametrize("quant", ["nvfp4", "hybrid_mx"])
+def test_weight_on_input_matches_bruteforce(quant):
+    """Router weights applied to fc1's input: the dgemm form against the element loop."""
+    cfg, ck = _tiny(quant)
+    rng = np.random.default_rng(21)
+    M, k = 4, 2
+    x = S.make_x(rng, M, ck.H)
+    ids = S.uniform_topk(rng, M, ck.E, k)
+    ids[3, 1] = -1
+    w = S.router_weights(rng, M, k, "sigmoid_norm", 2.5)
+    a, _ = O.moe_forward(ck, x, ids, w, return_f64=True, weight_on_input=True)
+    b = O.moe_forward_bruteforce(ck, x, ids, w, weight_on_input=True)
+    da, db = C.bf16_bits_to_f64(a), C.bf16_bits_to_f64(b)
+    assert np.mean(da == db) > 0.999
+    assert np.allclose(da, db, rtol=2 ** -7, atol=0)
+
+
+def test_weight_on_input_special_cases():
+    """Weights 1 on the input give the standard layer exactly (x * 1 = x, combine weight 1);
+    any other weight changes the SwiGLU's argument, so the results differ; W4A8 refuses."""
+    cfg, ck = _tiny("hybrid")
+    rng = np.random.default_rng(22)
+    M, k = 5, 2
+    x = S.make_x(rng, M, ck.H)
+    ids = S.uniform_topk(rng, M, ck.E, k)
+    ones = np.ones((M, k), np.float32)
+    _, f0 = O.moe_forward(ck, x, ids, ones, return_f64=True)
+    _, f1 = O.moe_forward(ck, x, ids, ones, return_f64=True, weight_on_input=True)
+    assert np.array_equal(f0, f1)
+    halves = np.full((M, k), 0.5, np.float32)
+    _, g0 = O.moe_forward(ck, x, ids, halves, return_f64=True)
+    _, g1 = O.moe_forward(ck, x, ids, halves, return_f64=True, weight_on_input=True)
+    assert not np.allclose(g0, g1)
+    _, ck8 = _tiny("mxfp4")
+    with pytest.raises(AssertionError):
+        O.moe_forward(ck8, x[:, :ck8.H], ids % ck8.E, ones, weight_on_input=True)
+
+
 def _e4m3_code_of_pow2(j):
     """E4M3 (bias 7) code of 2^j, j in [-9, 8]: normal exponent field from 2^-6, subnormal
     mantissa below (value m * 2^-9)."""
