@@ -65,7 +65,14 @@ typedef enum {
    * moves 2^(b_max - 140) into a per-matrix fp32 factor, so E2M1 x multiplier is exact in f16
    * for every group within 36 binades of the matrix's largest scale (groups further below are
    * flushed to zero: their terms are < 2^-34 of the matrix's largest weights). */
-  MOE_W4A16_HYBRID_MX = 3
+  MOE_W4A16_HYBRID_MX = 3,
+  /* NVFP4 weights (as MOE_W4A16_NVFP4) with MXFP8 activations: B12xExperts quant mode
+   * "w4a8_nvfp4" (`_supports_quant_scheme`: kNvfp4Static weights, kMxfp8Dynamic activations;
+   * `_prepare_experts`: it needs the per-expert activation global scales a1_gscale / a2_gscale).
+   * Each slot's fc1 input is MXFP8(a1[e] * x) / a1[e] (OCP MX rule on the fp32 products) and
+   * fc2's is MXFP8(a2[e] * h) / a2[e]; runs on the tensor-core backend only, with
+   * round_up(I, 128) a multiple of 256. */
+  MOE_W4A8_NVFP4 = 4
 } moe_quant_mode;
 
 typedef enum {
@@ -102,6 +109,10 @@ typedef struct {
   const void* nf_s13;
   const void* nf_w2;
   const void* nf_s2;
+  /* MOE_W4A8_NVFP4 only (NULL otherwise): per-expert activation global scales [E] f32 of fc1's
+   * input (a1_gscale = 1 / w13_input_scale) and of fc2's input (a2_gscale). */
+  const float* a1_gscale;
+  const float* a2_gscale;
 } moe_checkpoint;
 
 /* Weight plan: geometry and quant mode of one layer's experts (moe_b12x_next.py,

@@ -67,7 +67,8 @@ def swiglu(gate, up, limit=math.inf, alpha=1.0, beta=0.0):
     """Clamped SwiGLU (reading above).  Pinned by closed forms in tests/test_oracle_moe.py."""
     g = np.minimum(np.asarray(gate, dtype=np.float64), limit)
     u = np.clip(np.asarray(up, dtype=np.float64), -limit, limit)
-    return g * (1.0 / (1.0 + np.exp(-alpha * g))) * (u + beta)
+    with np.errstate(over="ignore"):      # exp overflow for a very negative gate: sigmoid 0
+        return g * (1.0 / (1.0 + np.exp(-alpha * g))) * (u + beta)
 
 
 # ---------------------------------------------------------------------------- weights
@@ -109,7 +110,7 @@ def expert_weights(ck, e: int):
     H, I = ck.H, ck.I
     if ck.quant == "mxfp4":
         return dequant_mxfp4(ck.w13[e], ck.s13[e]), dequant_mxfp4(ck.w2[e], ck.s2[e]), "mxfp4"
-    if ck.quant == "nvfp4":
+    if ck.quant in ("nvfp4", "w4a8_nvfp4"):
         return (dequant_nvfp4(ck.w13[e], ck.s13[e], ck.g13[e]),
                 dequant_nvfp4(ck.w2[e], ck.s2[e], ck.g2[e]), "nvfp4")
     if ck.quant == "nf3":
@@ -130,22 +131,41 @@ def split_w13(g13: np.ndarray, I: int, layout: int):
 # ---------------------------------------------------------------------------- forward
 
 def activation_a8(ck) -> bool:
-    return ck.quant == "mxfp4"
+    """MXFP8 activations: W4A8 (MXFP4 weights) and NVFP4 weights in the "w4a8_nvfp4" mode."""
+    return ck.quant in ("mxfp4", "w4a8_nvfp4")
 
 
-def quantize_x(x_bits: np.ndarray, a8: bool):
-    """x as the fc1 kernel sees it: MXFP8 (codes, scales, dequantised values) or bf16 values."""
+def act_gscale(ck, which: str):
+    """Per-expert activation global scales [E] of fc1's ("a1") or fc2's ("a2") input, or None
+    (B12xExperts ``_prepare_experts``: the NVFP4 modes with quantised activations take
+    a1_gscale / a2_gscale)."""
+    if ck.quant != "w4a8_nvfp4":
+        return None
+    return ck.a13 if which == "a1" else ck.a2
+
+
+def quantize_x(x_bits: np.ndarray, a8: bool, a=None):
+    """x as the fc1 kernel sees it: MXFP8 (codes, scales, dequantised values) or bf16 values.
+    With an activation global scale ``a`` (reading: it multiplies x in fp32 before the MX
+    quantisation and divides the dequantised value) the values are MXFP8(fp32(a * x)) / a."""
     x = C.bf16_bits_to_f64(x_bits)
     if a8:
+        if a is not None:
+            xa = (np.float32(a) * x.astype(np.float32)).astype(np.float64)
+            q, s = C.mxfp8_quantize(xa)
+            return q, s, C.mxfp8_dequantize(q, s) / np.float64(np.float32(a))
         q, s = C.mxfp8_quantize(x)
         return q, s, C.mxfp8_dequantize(q, s)
     return None, None, x
 
 
-def requant_h(h: np.ndarray, a8: bool) -> np.ndarray:
+def requant_h(h: np.ndarray, a8: bool, a=None) -> np.ndarray:
+    """fc2's input: MXFP8 of h (of a * h, divided by a, with an activation global scale), or
+    bf16(h) for 16-bit activations."""
     if a8:
-        q, s = C.mxfp8_quantize(h)
-        return C.mxfp8_dequantize(q, s)
+        a64 = 1.0 if a is None else np.float64(np.float32(a))
+        q, s = C.mxfp8_quantize(h * a64)
+        return C.mxfp8_dequantize(q, s) / a64
     return C.bf16_round(h)
 
 
@@ -178,7 +198,8 @@ def moe_forward(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.
     if rows is not None:
         row_mask[:] = False
         row_mask[np.asarray(rows)] = True
-    _, _, xhat = quantize_x(x_bits[row_mask] if rows is not None else x_bits, a8)
+    a1, a2 = act_gscale(ck, "a1"), act_gscale(ck, "a2")
+    _, _, xhat = quantize_x(x_bits[row_mask] if rows is not None else x_bits, a8 and a1 is None)
     if rows is not None:
         full = np.full((M, H), np.nan)
         full[row_mask] = xhat
@@ -189,10 +210,12 @@ def moe_forward(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.
         t_idx, j_idx = np.nonzero(sel)
         W13, W2, _ = expert_weights(ck, int(e))
         xin, cw = slot_input(xhat[t_idx], w[t_idx, j_idx], weight_on_input)
+        if a1 is not None:     # MXFP8 activations with the expert's global scale
+            xin = quantize_x(x_bits[t_idx], True, a1[e])[2]
         G = xin @ W13.T
         gate, up = split_w13(G, I, ck.layout)
         h = swiglu(gate, up, limit, alpha, beta)
-        hh = requant_h(h, a8)
+        hh = requant_h(h, a8, None if a2 is None else a2[e])
         y = hh @ W2.T
         np.add.at(out, t_idx, cw[:, None] * y)
     out[~row_mask] = np.nan
@@ -210,7 +233,8 @@ def slot_intermediate(ck, x_bits, topk_ids, limit=math.inf, alpha=1.0, beta=0.0,
     ids = np.asarray(topk_ids, dtype=np.int64)
     M, k = ids.shape
     a8 = activation_a8(ck)
-    _, _, xhat = quantize_x(np.asarray(x_bits), a8)
+    a1 = act_gscale(ck, "a1")
+    _, _, xhat = quantize_x(np.asarray(x_bits), a8 and a1 is None)
     _, off, perm, _ = route(ids, ck.E)
     out = np.zeros((perm.shape[0], ck.I))
     for e in range(ck.E):
@@ -220,6 +244,8 @@ def slot_intermediate(ck, x_bits, topk_ids, limit=math.inf, alpha=1.0, beta=0.0,
         W13, _, _ = expert_weights(ck, e)
         fl = perm[lo:hi]
         xin = xhat[fl // k]
+        if a1 is not None:
+            xin = quantize_x(np.asarray(x_bits)[fl // k], True, a1[e])[2]
         if weight_on_input:
             xin, _ = slot_input(xin, np.asarray(topk_w, np.float64).reshape(-1)[fl], True)
         G = xin @ W13.T
@@ -240,14 +266,19 @@ def requant_alternatives(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0
     M, k = ids.shape
     a8 = activation_a8(ck)
     h = slot_intermediate(ck, x_bits, ids, limit, alpha, beta, topk_w, weight_on_input)
+    _, _, perm, _ = route(ids, ck.E)
+    a2 = act_gscale(ck, "a2")
     if a8:
-        mask, alt = C.mxfp8_alternates(h, rel)
-        q, s = C.mxfp8_quantize(h)
-        near = C.mxfp8_dequantize(q, s)
+        # with an activation global scale the decisions are taken on a2 * h
+        sc = (np.ones(h.shape[0]) if a2 is None else
+              np.float32(a2)[ids.reshape(-1)[perm]].astype(np.float64))[:, None]
+        mask, alt = C.mxfp8_alternates(h * sc, rel)
+        q, s = C.mxfp8_quantize(h * sc)
+        near = C.mxfp8_dequantize(q, s) / sc
+        alt = alt / sc
     else:
         mask, alt = C.bf16_alternates(h, rel)
         near = C.bf16_round(h)
-    _, _, perm, _ = route(ids, ck.E)
     want = set(range(M)) if rows is None else set(int(r) for r in rows)
     out = {r: [] for r in want}
     cache = {}
@@ -275,7 +306,8 @@ def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1
     M = len(ids)
     E, H, I = ck.E, ck.H, ck.I
     a8 = activation_a8(ck)
-    _, _, xhat = quantize_x(np.asarray(x_bits), a8)
+    a1, a2 = act_gscale(ck, "a1"), act_gscale(ck, "a2")
+    _, _, xhat = quantize_x(np.asarray(x_bits), a8 and a1 is None)
     out = [[0.0] * H for _ in range(M)]
 
     tiers = tier_local_index(ck.tier) if ck.quant == "hybrid" else None
@@ -289,7 +321,7 @@ def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1
             sub, li = ck, e
         codes = getattr(sub, mat)[li]
         scales = getattr(sub, "s13" if mat == "w13" else "s2")[li]
-        if sub.quant in ("mxfp4", "nvfp4"):
+        if sub.quant in ("mxfp4", "nvfp4", "w4a8_nvfp4"):
             byte = int(codes[r, c // 2])
             nib = byte & 0xF if c % 2 == 0 else byte >> 4
             v = C.e2m1_value(nib)
@@ -310,6 +342,8 @@ def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1
             if not (0 <= e < E):
                 continue
             xt = xhat[t]
+            if a1 is not None:
+                xt = quantize_x(np.asarray(x_bits)[t:t + 1], True, a1[e])[2][0]
             cw = w[t][j]
             if weight_on_input:
                 wb = float(C.bf16_round(cw))
@@ -332,7 +366,7 @@ def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1
                 g = min(gate[i], limit)
                 u = max(-limit, min(up[i], limit))
                 h[i] = g * (1.0 / (1.0 + math.exp(-alpha * g))) * (u + beta)
-            hh = requant_h(np.array(h), a8).tolist()
+            hh = requant_h(np.array(h), a8, None if a2 is None else a2[e]).tolist()
             for r in range(H):
                 s = 0.0
                 for i in range(I):

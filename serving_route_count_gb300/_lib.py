@@ -25,7 +25,7 @@ class MoeCheckpoint(ctypes.Structure):
     _fields_ = [("w13", c_void_p), ("s13", c_void_p), ("g13", c_void_p),
                 ("w2", c_void_p), ("s2", c_void_p), ("g2", c_void_p),
                 ("nf_w13", c_void_p), ("nf_s13", c_void_p), ("nf_w2", c_void_p),
-                ("nf_s2", c_void_p)]
+                ("nf_s2", c_void_p), ("a1_gscale", c_void_p), ("a2_gscale", c_void_p)]
 
 
 # name -> (restype, argtypes)

@@ -14,7 +14,8 @@ namespace moe {
 cudaError_t launch_route(const int32_t* ids, int Mk, int E, int ep_first, int tile_slots,
                          int max_tiles, const RunPtrs& r, cudaStream_t st);
 cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
-                        bool atoms, bool to_f16, const float* win, void* z0, size_t z0_words,
+                        bool atoms, bool to_f16, const float* win, const float* ag,
+                        const int32_t* ids, int ep_first, int E, void* z0, size_t z0_words,
                         void* z1, size_t z1_words, void* z2, size_t z2_words, cudaStream_t st);
 bool route_actq_small_supported(int Mk, int E);
 int route_chunks(int Mk);
@@ -28,8 +29,8 @@ cudaError_t launch_actq_rows(const void* x, int M, int H, int topk, const RunPtr
 cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_first,
                                     int tile_slots, int max_tiles, const void* x, int H, int topk,
                                     const RunPtrs& r, bool atoms, bool to_f16, const float* win,
-                                    void* z0, size_t z0_words, void* z1, size_t z1_words,
-                                    void* z2, size_t z2_words, cudaStream_t st);
+                                    const float* ag, void* z0, size_t z0_words, void* z1,
+                                    size_t z1_words, void* z2, size_t z2_words, cudaStream_t st);
 // gemm_tc.cu
 cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                             int bn, int tiles, int splits, const float* topk_w, int M,
@@ -74,7 +75,8 @@ struct moe_weight_plan {
   int E4, E3;
   std::vector<int32_t> tier_map;  // (tier << 24) | local
   // section offsets in the prepared buffer
-  size_t w13, s13, w2, s2, g13, g2, mxk13, mxk2, nf_w13, nf_s13, nf_w2, nf_s2, tmap, total;
+  size_t w13, s13, w2, s2, g13, g2, mxk13, mxk2, ag13, ag2, nf_w13, nf_s13, nf_w2, nf_s2, tmap,
+      total;
 };
 
 struct moe_prepared {
@@ -148,7 +150,7 @@ moe_status check_geometry(int E, int H, int I, int quant) {
   if (H < 128 || H % 128 != 0) return MOE_ERR_SHAPE;
   if (I < 64 || I % 64 != 0) return MOE_ERR_SHAPE;
   if ((long long)H * H > (1LL << 40) || (long long)I > (1 << 20)) return MOE_ERR_SHAPE;
-  if (quant < 0 || quant > 3) return MOE_ERR_UNSUPPORTED;
+  if (quant < 0 || quant > 4) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -213,7 +215,7 @@ moe_status moe_plan_weights(int E, int H, int I, int quant_mode, int w13_layout,
     wp->w2 = take(E4 * H_ * Ip / 2);
     wp->s13 = take(E4 * 2 * (size_t)cdiv(I, 128) * (H_ / 128) * 512);
     wp->s2 = take(E4 * (H_ / 128) * (Ip / 128) * 512);
-    wp->g13 = wp->g2 = wp->mxk13 = wp->mxk2 = 0;
+    wp->g13 = wp->g2 = wp->mxk13 = wp->mxk2 = wp->ag13 = wp->ag2 = 0;
   } else {
     wp->w13 = take(E4 * t13 * kNvCodeTile);
     wp->w2 = take(E4 * t2 * kNvCodeTile);
@@ -224,6 +226,9 @@ moe_status moe_plan_weights(int E, int H, int I, int quant_mode, int w13_layout,
     const bool mx = quant_mode == MOE_W4A16_HYBRID_MX;
     wp->mxk13 = mx ? take(E4 * 4) : 0;
     wp->mxk2 = mx ? take(E4 * 4) : 0;
+    const bool nv_a8 = quant_mode == MOE_W4A8_NVFP4;
+    wp->ag13 = nv_a8 ? take(E4 * 4) : 0;
+    wp->ag2 = nv_a8 ? take(E4 * 4) : 0;
   }
   wp->nf_w13 = take(E3 * t13 * kNfCodeTile);
   wp->nf_s13 = take(E3 * t13 * kW16ScaleTile);
@@ -258,6 +263,8 @@ moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* 
   if (nf3 && (src->nf_w13 == nullptr || src->nf_s13 == nullptr || src->nf_w2 == nullptr ||
               src->nf_s2 == nullptr))
     return MOE_ERR_ARG;
+  const bool nv_a8 = wp->quant == MOE_W4A8_NVFP4;
+  if (nv_a8 && (src->a1_gscale == nullptr || src->a2_gscale == nullptr)) return MOE_ERR_ARG;
   uint8_t* base = static_cast<uint8_t*>(dst);
   const int E4 = wp->E4, E3 = wp->E3, H = wp->H, I = wp->I, Ip = wp->Ip, L = wp->layout;
   cudaError_t e = cudaSuccess;
@@ -290,6 +297,12 @@ moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* 
       chk(launch_repack_w16_tiled(1, src->s2, base + wp->s2, E4, 1, H, I, Ip, L, st));
       chk(cudaMemcpyAsync(base + wp->g13, src->g13, (size_t)E4 * 4, cudaMemcpyDeviceToDevice, st));
       chk(cudaMemcpyAsync(base + wp->g2, src->g2, (size_t)E4 * 4, cudaMemcpyDeviceToDevice, st));
+      if (nv_a8) {
+        chk(cudaMemcpyAsync(base + wp->ag13, src->a1_gscale, (size_t)E4 * 4,
+                            cudaMemcpyDeviceToDevice, st));
+        chk(cudaMemcpyAsync(base + wp->ag2, src->a2_gscale, (size_t)E4 * 4,
+                            cudaMemcpyDeviceToDevice, st));
+      }
     }
   }
   if (nf3) {
@@ -308,6 +321,10 @@ moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* 
   w.quant = wp->quant; w.E = wp->E; w.H = H; w.I = I; w.Ip = Ip; w.E4 = E4; w.E3 = E3;
   w.fp4_tiled = wp->quant == MOE_W4A8_MXFP4 ? 1 : 0;
   w.mx_kept = mx16 ? 1 : 0;
+  if (nv_a8) {
+    w.ag13 = reinterpret_cast<const float*>(base + wp->ag13);
+    w.ag2 = reinterpret_cast<const float*>(base + wp->ag2);
+  }
   w.w13 = base + wp->w13; w.s13 = base + wp->s13; w.w2 = base + wp->w2; w.s2 = base + wp->s2;
   if (wp->quant != MOE_W4A8_MXFP4) {
     w.g13 = reinterpret_cast<const float*>(base + wp->g13);
@@ -328,6 +345,9 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   if (st != MOE_OK) return st;
   if (topk < 1 || topk > 16 || max_m < 1 || max_m > (1 << 20)) return MOE_ERR_SHAPE;
   if (std::isnan(swiglu_limit) || swiglu_limit <= 0.f) return MOE_ERR_ARG;
+  // MXFP8 activations with NVFP4 weights run on the 16-bit tensor-core kernels only
+  if (quant_mode == MOE_W4A8_NVFP4 && align_up((size_t)I, 128) % 256 != 0)
+    return MOE_ERR_UNSUPPORTED;
   moe_plan_t* p = new (std::nothrow) moe_plan_t();
   if (p == nullptr) return MOE_ERR_ARG;
   PlanDims& d = p->d;
@@ -476,7 +496,8 @@ moe_status moe_plan_set_fc1_kernel(moe_plan_t* plan, int choice) {
 
 moe_status moe_plan_set_router_weight_on_input(moe_plan_t* plan, int on) {
   if (plan == nullptr || (on != 0 && on != 1)) return MOE_ERR_ARG;
-  if (on && plan->d.quant == MOE_W4A8_MXFP4) return MOE_ERR_UNSUPPORTED;
+  if (on && (plan->d.quant == MOE_W4A8_MXFP4 || plan->d.quant == MOE_W4A8_NVFP4))
+    return MOE_ERR_UNSUPPORTED;
   plan->d.w_on_input = on;
   return MOE_OK;
 }
@@ -490,6 +511,7 @@ moe_status moe_plan_set_expert_offset(moe_plan_t* plan, int first_expert) {
 
 moe_status moe_plan_set_backend(moe_plan_t* plan, int backend) {
   if (plan == nullptr || backend < 0 || backend > 1) return MOE_ERR_ARG;
+  if (backend == 1 && plan->d.quant == MOE_W4A8_NVFP4) return MOE_ERR_UNSUPPORTED;
   plan->d.backend = backend;
   return MOE_OK;
 }
@@ -566,8 +588,8 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   cudaError_t e;
   if (small) {
     e = launch_route_actq_small(topk_ids, Sm, d.E, d.ep_first, bn, plan->s.max_tiles, x, d.H,
-                                d.topk, r, atoms, t16, win, acc, acc_words, g, g_words, tk,
-                                tk_words, st);
+                                d.topk, r, atoms, t16, win, w.ag13, acc, acc_words, g, g_words,
+                                tk, tk_words, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
   } else if (tc8) {
@@ -584,8 +606,8 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
     if (a8 || acc || g || t16) {
-      e = launch_actq(x, M, d.H, d.topk, r, a8, atoms, t16, win, acc, acc_words, g, g_words, tk,
-                      tk_words, st);
+      e = launch_actq(x, M, d.H, d.topk, r, a8, atoms, t16, win, w.ag13, topk_ids, d.ep_first,
+                      d.E, acc, acc_words, g, g_words, tk, tk_words, st);
       if (e != cudaSuccess) return cuda_status(e);
     }
   }

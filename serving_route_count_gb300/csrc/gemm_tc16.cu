@@ -80,6 +80,9 @@ struct Tc16Params {
   const float* gscale;        // NVFP4 per-expert global of this matrix ([E4]); MXFP4 kept
                               // tier: the matrix's power-of-two factor
   int mx;                     // kept tier MXFP4 (f16 multiplier per group of 32)
+  const float* agscale;       // MXFP8 activations: per-expert activation global scale of this
+                              // GEMM's input ([E]); nullptr: 16-bit activations
+  const float* agscale2;      // fc1 with MXFP8 activations: that of fc2's input (h)
   const int4* tiles;
   const int32_t* ctrl;
   int32_t* err;
@@ -207,6 +210,21 @@ __device__ __forceinline__ uint16_t h_to_f16(float h, int32_t* err) {
   const float hb = __bfloat162float(__float2bfloat16_rn(h));
   if (fabsf(hb) > 65504.f) atomicOr(err, kErrRange);
   return __half_as_ushort(__float2half_rn(hb));
+}
+
+// MXFP8 activations: h of one token column for this warp's 32 features (one MX block), times
+// the expert's activation global scale a2, quantised by the OCP MX rule and returned as the f16
+// of the dequantised value E4M3 x 2^(s-127) (exact while the block scale is at most 2^7: larger
+// sets the range bit).  All 32 lanes call it with the same column.
+__device__ __forceinline__ uint16_t h_to_f16_mx(float h, float a2, int32_t* err) {
+  const float v = h * a2;
+  float amax = fabsf(v);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const uint32_t s = mx_scale_byte(amax);
+  if (s > 127 + 7) atomicOr(err, kErrRange);
+  const float q = e4m3_to_f32((uint8_t)f32_to_e4m3(v * e8m0_inv_f32(s))) * e8m0_to_f32(s);
+  return __half_as_ushort(__float2half_rn(q));
 }
 
 template <int BN, bool FC2, bool PAIR>
@@ -387,7 +405,10 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
     const int quad = warp & 3;
     const int row = rb * 128 + quad * 32 + lane;           // weight row of this lane
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
-    const float gs = (!nf3 && p.gscale != nullptr) ? p.gscale[le] : 1.f;
+    // weight global (NVFP4) over the activation global (MXFP8 activations carry a * x)
+    const float gs = ((!nf3 && p.gscale != nullptr) ? p.gscale[le] : 1.f) /
+                     (p.agscale != nullptr ? p.agscale[e] : 1.f);
+    const float a_next = (!FC2 && p.agscale2 != nullptr) ? p.agscale2[e] : 0.f;
     if (ok && nsub > 0) {
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
@@ -405,7 +426,8 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
               const float h = row < p.I ? swiglu16(v1[j] * gs, v0[j] * gs, p.limit, p.alpha,
                                                    p.beta)
                                         : 0.f;
-              p.h16[(size_t)pos * p.Ip + row] = h_to_f16(h, p.err);
+              p.h16[(size_t)pos * p.Ip + row] =
+                  p.agscale2 != nullptr ? h_to_f16_mx(h, a_next, p.err) : h_to_f16(h, p.err);
             } else {
               float* gg = p.gacc + ((size_t)split * p.Sm + pos) * 2 * p.Ip;
               gg[row] = v0[j];
@@ -445,7 +467,9 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
       __threadfence();
       const int quad = warp & 3;
       const int row = rb * 128 + quad * 32 + lane;
-      const float gs = (!nf3 && p.gscale != nullptr) ? p.gscale[le] : 1.f;
+      const float gs = ((!nf3 && p.gscale != nullptr) ? p.gscale[le] : 1.f) /
+                       (p.agscale != nullptr ? p.agscale[e] : 1.f);
+      const float a_next = p.agscale2 != nullptr ? p.agscale2[e] : 0.f;
       // partial sums added in split order (the same result on every run), 16 columns at a
       // time with each split's 32 loads issued together
       for (int c0 = 0; c0 < n; c0 += 16) {
@@ -472,7 +496,8 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
           if (c0 + j < n) {
             const float h = row < p.I ? swiglu16(gt[j] * gs, up[j] * gs, p.limit, p.alpha, p.beta)
                                       : 0.f;
-            p.h16[(size_t)(p0 + c0 + j) * p.Ip + row] = h_to_f16(h, p.err);
+            p.h16[(size_t)(p0 + c0 + j) * p.Ip + row] =
+                p.agscale2 != nullptr ? h_to_f16_mx(h, a_next, p.err) : h_to_f16(h, p.err);
           }
         }
       }
@@ -529,8 +554,10 @@ static cudaError_t launch16(const Tc16Params& p, int tiles, cudaStream_t st) {
   return launch_kernel(kernel, grid, dim3(k16Threads), Cfg::kSmem, st, true, p);
 }
 
-// fc1 of the W4A16 path at two CTAs per SM (NVFP4-only layers, token tiles of at most 32)
-bool tc16_fc1_pair(int bn, int quant) { return bn <= 32 && quant == kQuantNVFP4; }
+// fc1 of the 16-bit path at two CTAs per SM (NVFP4-only layers, token tiles of at most 32)
+bool tc16_fc1_pair(int bn, int quant) {
+  return bn <= 32 && (quant == kQuantNVFP4 || quant == kQuantW4A8Nv);
+}
 
 // stage 0: fc1 (+ SwiGLU, h -> bf16 -> f16), stage 1: fc2 (+ combine).
 cudaError_t launch_tc16_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
@@ -551,6 +578,8 @@ cudaError_t launch_tc16_stage(int stage, const DevWeights& w, const RunPtrs& r, 
   p.tier_map = w.tier_map;
   p.gscale = fc2 ? w.g2 : w.g13;
   p.mx = w.mx_kept;
+  p.agscale = fc2 ? w.ag2 : w.ag13;
+  p.agscale2 = fc2 ? nullptr : w.ag2;
   p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
   p.h16 = reinterpret_cast<uint16_t*>(r.h16); p.gacc = r.g; p.tickets = r.tickets;
   p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;

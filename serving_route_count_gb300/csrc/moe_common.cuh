@@ -16,6 +16,7 @@ constexpr int kQuantW4A8 = 0;
 constexpr int kQuantNVFP4 = 1;
 constexpr int kQuantHybrid = 2;
 constexpr int kQuantHybridMx = 3;   // hybrid with the kept tier in MXFP4
+constexpr int kQuantW4A8Nv = 4;     // NVFP4 weights, MXFP8 activations
 constexpr int kTierNVFP4 = 4;
 constexpr int kTierNF3 = 3;
 
@@ -70,6 +71,8 @@ struct DevWeights {
   const float* g13 = nullptr;         // [E4] NVFP4 global scales (MXFP4 kept tier: 2^shift)
   const float* g2 = nullptr;
   int mx_kept = 0;                    // kept tier MXFP4: scale tiles hold f16 multipliers
+  const float* ag13 = nullptr;        // NVFP4 weights with MXFP8 activations: per-expert
+  const float* ag2 = nullptr;         // activation global scales of fc1's / fc2's input ([E])
   // NF3 tier
   const uint8_t* nf_w13 = nullptr;    // NF3 code tiles of [E3][2] matrices I x H
   const uint8_t* nf_s13 = nullptr;    // NF3 scale tiles

@@ -247,6 +247,44 @@ __device__ __forceinline__ uint4 bf16x8_scale(uint4 u, float wb) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// NVFP4 weights with MXFP8 activations: 32 activations times the expert's activation global
+// scale `a` (fp32 products), quantised by the OCP MX rule (as quantize_block32) and stored as the
+// f16 of each dequantised value E4M3 x 2^(s-127): exact while the block scale is within
+// [2^-15, 2^7]; a larger one (values beyond f16) clears `ok`, a smaller one rounds the values'
+// bits below 2^-24.
+__device__ __forceinline__ void mx_roundtrip32_f16(const __nv_bfloat16* __restrict__ src_bf16,
+                                                   float a, uint16_t* __restrict__ dst, bool& ok) {
+  const uint4* src = reinterpret_cast<const uint4*>(src_bf16);
+  float v[32];
+#pragma unroll
+  for (int qq = 0; qq < 4; ++qq) {
+    const uint4 u = src[qq];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[qq * 8 + 2 * j] = __uint_as_float(w[j] << 16) * a;
+      v[qq * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u) * a;
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  const uint32_t s = mx_scale_byte(amax);
+  const float inv = e8m0_inv_f32(s), sc = e8m0_to_f32(s);
+  ok &= s <= 127 + 7;
+  uint32_t o[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float q0 = e4m3_to_f32((uint8_t)f32_to_e4m3(v[2 * j] * inv)) * sc;
+    const float q1 = e4m3_to_f32((uint8_t)f32_to_e4m3(v[2 * j + 1] * inv)) * sc;
+    o[j] = (uint32_t)__half_as_ushort(__float2half_rn(q0)) |
+           ((uint32_t)__half_as_ushort(__float2half_rn(q1)) << 16);
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int qq = 0; qq < 4; ++qq) d[qq] = make_uint4(o[4 * qq], o[4 * qq + 1], o[4 * qq + 2], o[4 * qq + 3]);
+}
+
 __device__ __forceinline__ float bf16_round(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));
 }
@@ -255,8 +293,9 @@ __global__ void __launch_bounds__(256)
 actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t* __restrict__ ctrl,
             const int32_t* __restrict__ perm, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
             uint8_t* __restrict__ xs16, int r16, uint16_t* __restrict__ x16,
-            const float* __restrict__ win, int32_t* __restrict__ err, ZeroRegion z0,
-            ZeroRegion z1, ZeroRegion z2) {
+            const float* __restrict__ win, const float* __restrict__ ag,
+            const int32_t* __restrict__ ids, int ep_first, int E, int32_t* __restrict__ err,
+            ZeroRegion z0, ZeroRegion z1, ZeroRegion z2) {
   pdl_wait_prev();
   pdl_launch_next();
   const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -273,7 +312,21 @@ actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t*
       if (xs16 != nullptr) xs16[((size_t)(b >> 2) * r16 + p) * 16 + (b & 3)] = (uint8_t)sb;
     }
   }
-  if (x16 != nullptr) {
+  if (x16 != nullptr && ag != nullptr) {
+    // MXFP8 activations for NVFP4 weights, as f16 values in slot order
+    const int nb = H / 32;
+    const size_t nblk = (size_t)ctrl[2] * nb;
+    bool range_ok = true;
+    for (size_t i = gtid; i < nblk; i += gsz) {
+      const size_t p = i / nb;
+      const int b = (int)(i % nb);
+      const int f = perm[p];
+      const int e = local_expert(ids[f], ep_first, E);
+      mx_roundtrip32_f16(x + (size_t)(f / topk) * H + b * 32, ag[e], x16 + p * H + b * 32,
+                         range_ok);
+    }
+    if (!range_ok) atomicOr(err, kErrRange);
+  } else if (x16 != nullptr) {
     // bf16 -> f16 copy in slot order for the 16-bit tensor-core path (exact within f16 range)
     const int nc = H / 8;
     const size_t nchunk = (size_t)ctrl[2] * nc;
@@ -312,8 +365,8 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
                         int4* __restrict__ tiles, int32_t* __restrict__ ctrl,
                         uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
                         uint8_t* __restrict__ xs16, int r16, uint16_t* __restrict__ x16,
-                        const float* __restrict__ win, ZeroRegion z0, ZeroRegion z1,
-                        ZeroRegion z2, int ep_first) {
+                        const float* __restrict__ win, const float* __restrict__ ag,
+                        ZeroRegion z0, ZeroRegion z1, ZeroRegion z2, int ep_first) {
   constexpr int NW = kSmallRouteThreads / 32;
   __shared__ int s_ids[kSmallRouteSlots];
   __shared__ int s_perm[kSmallRouteSlots];
@@ -404,7 +457,20 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
       if (xs16 != nullptr) xs16[((size_t)(b >> 2) * r16 + p) * 16 + (b & 3)] = (uint8_t)sb;
     }
   }
-  if (x16 != nullptr) {
+  if (x16 != nullptr && ag != nullptr) {
+    // MXFP8 activations for NVFP4 weights, as f16 values in slot order
+    const int nb = H / 32;
+    const size_t nblk = (size_t)total * nb;
+    bool range_ok = true;
+    for (size_t i = gtid; i < nblk; i += gsz) {
+      const size_t p = i / nb;
+      const int b = (int)(i % nb);
+      const int f = s_perm[p];
+      mx_roundtrip32_f16(x + (size_t)(f / topk) * H + b * 32, ag[s_ids[f]],
+                         x16 + p * H + b * 32, range_ok);
+    }
+    if (!range_ok) atomicOr(ctrl, kErrRange);
+  } else if (x16 != nullptr) {
     const int nc = H / 8;
     const size_t nchunk = (size_t)total * nc;
     bool range_ok = true;
@@ -661,8 +727,9 @@ bool route_actq_small_supported(int Mk, int E) {
 cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_first,
                                     int tile_slots, int max_tiles, const void* x, int H,
                                     int topk, const RunPtrs& r, bool atoms, bool to_f16,
-                                    const float* win, void* z0, size_t z0_words, void* z1,
-                                    size_t z1_words, void* z2, size_t z2_words, cudaStream_t st) {
+                                    const float* win, const float* ag, void* z0,
+                                    size_t z0_words, void* z1, size_t z1_words, void* z2,
+                                    size_t z2_words, cudaStream_t st) {
   if (!route_actq_small_supported(Mk, E)) return cudaErrorInvalidValue;
   const size_t work = std::max((size_t)Mk * (to_f16 ? H / 8 : H / 32),
                                std::max(z0_words / 4, std::max(z1_words / 4, z2_words / 4)));
@@ -675,7 +742,8 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_fi
                        reinterpret_cast<const __nv_bfloat16*>(x), H, topk, r.cnt, r.off, r.perm,
                        r.slot_of, r.tiles, r.ctrl, to_f16 ? nullptr : r.xq,
                        to_f16 ? nullptr : r.xs, (atoms && !to_f16) ? r.xs16 : nullptr, r.r16,
-                       to_f16 ? r.x16 : nullptr, to_f16 ? win : nullptr, ZeroRegion{z0, z0_words},
+                       to_f16 ? r.x16 : nullptr, to_f16 ? win : nullptr, to_f16 ? ag : nullptr,
+                       ZeroRegion{z0, z0_words},
                        ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words}, ep_first);
 }
 
@@ -688,7 +756,8 @@ cudaError_t launch_route(const int32_t* ids, int Mk, int E, int ep_first, int ti
 }
 
 cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
-                        bool atoms, bool to_f16, const float* win, void* z0, size_t z0_words,
+                        bool atoms, bool to_f16, const float* win, const float* ag,
+                        const int32_t* ids, int ep_first, int E, void* z0, size_t z0_words,
                         void* z1, size_t z1_words, void* z2, size_t z2_words, cudaStream_t st) {
   const size_t work = std::max(
       std::max(quant_x ? (size_t)M * topk * (H / 32) : (size_t)0,
@@ -701,7 +770,8 @@ cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r,
                        static_cast<const int32_t*>(r.ctrl), static_cast<const int32_t*>(r.perm),
                        quant_x ? r.xq : nullptr, quant_x ? r.xs : nullptr,
                        (quant_x && atoms) ? r.xs16 : nullptr, r.r16,
-                       to_f16 ? r.x16 : nullptr, to_f16 ? win : nullptr, r.ctrl,
+                       to_f16 ? r.x16 : nullptr, to_f16 ? win : nullptr, to_f16 ? ag : nullptr,
+                       ids, ep_first, E, r.ctrl,
                        ZeroRegion{z0, z0_words},
                        ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words});
 }

@@ -17,6 +17,7 @@ MOE_W4A8_MXFP4 = 0
 MOE_W4A16_NVFP4 = 1
 MOE_W4A16_HYBRID = 2
 MOE_W4A16_HYBRID_MX = 3
+MOE_W4A8_NVFP4 = 4
 MOE_W13_UP_GATE = 0
 MOE_W13_GATE_UP = 1
 MOE_TIER_NVFP4 = 4
@@ -261,7 +262,8 @@ def moe_version() -> str:
 
 # ---------------------------------------------------------------------------------- convenience
 
-QUANT_OF = {"mxfp4": MOE_W4A8_MXFP4, "nvfp4": MOE_W4A16_NVFP4, "hybrid": MOE_W4A16_HYBRID}
+QUANT_OF = {"mxfp4": MOE_W4A8_MXFP4, "nvfp4": MOE_W4A16_NVFP4, "hybrid": MOE_W4A16_HYBRID,
+            "w4a8_nvfp4": MOE_W4A8_NVFP4}
 
 
 def quant_mode_of(ck) -> int:
@@ -283,7 +285,8 @@ def checkpoint_to_device(ck, device="cuda") -> dict:
                 "s2": t(nv.s2), "g2": t(nv.g2), "nf_w13": t(nf.w13), "nf_s13": t(nf.s13),
                 "nf_w2": t(nf.w2), "nf_s2": t(nf.s2)}
     return {"w13": t(ck.w13), "s13": t(ck.s13), "g13": t(ck.g13), "w2": t(ck.w2),
-            "s2": t(ck.s2), "g2": t(ck.g2)}
+            "s2": t(ck.s2), "g2": t(ck.g2), "a1_gscale": t(getattr(ck, "a13", None)),
+            "a2_gscale": t(getattr(ck, "a2", None))}
 
 
 class MoELayer:

@@ -39,7 +39,7 @@ class MoEConfig:
     H: int
     I: int
     topk: int
-    quant: str                 # "w4a8_mxfp4" | "w4a16_nvfp4" | "hybrid" | "hybrid_mx"
+    quant: str                 # "w4a8_mxfp4" | "w4a16_nvfp4" | "w4a8_nvfp4" | "hybrid" | "hybrid_mx"
     swiglu_limit: float        # +inf = no clamp
     m_list: tuple
     routing: str = "uniform"   # "uniform" | "zipf"
@@ -98,6 +98,12 @@ CONFIGS = {
                                   quant="hybrid", swiglu_limit=INF, m_list=(8, 2048),
                                   routing="zipf", zipf_s=0.8, weight_rule="sigmoid_norm",
                                   scale_lo=0x08, scale_hi=0x48, n_nvfp4=64, seed_base=5000),
+    # NVFP4 weights with MXFP8 activations (B12xExperts "w4a8_nvfp4"): the NVFP4 layer above
+    # with per-expert activation global scales.
+    "w4a8_nvfp4": MoEConfig("w4a8_nvfp4", E=256, H=6144, I=512, topk=8, quant="w4a8_nvfp4",
+                            swiglu_limit=INF, m_list=(1, 8, 64, 512, 2048),
+                            weight_rule="sigmoid_norm", scale_lo=0x08, scale_hi=0x48,
+                            seed_base=4100),
     # Hybrid "v3": the same layer with the 64 kept experts in MXFP4 (E8M0 2^-8..2^-2) and bf16
     # activations; NF3 tier as above.
     "hybrid_mxfp4_nf3": MoEConfig("hybrid_mxfp4_nf3", E=256, H=6144, I=512, topk=8,
@@ -111,7 +117,7 @@ CONFIGS = {
 @dataclasses.dataclass
 class Checkpoint:
     """Checkpoint-layout tensors of one MoE layer (numpy, host)."""
-    quant: str                      # "mxfp4" | "nvfp4" | "nf3" | "hybrid"
+    quant: str                      # "mxfp4" | "nvfp4" | "w4a8_nvfp4" | "nf3" | "hybrid"
     E: int
     H: int
     I: int
@@ -122,6 +128,9 @@ class Checkpoint:
     s2: Optional[np.ndarray] = None
     g13: Optional[np.ndarray] = None
     g2: Optional[np.ndarray] = None
+    # w4a8_nvfp4 only: per-expert activation global scales of fc1's / fc2's input (fp32 [E])
+    a13: Optional[np.ndarray] = None
+    a2: Optional[np.ndarray] = None
     # hybrid only
     tier: Optional[np.ndarray] = None        # [E] int8, TIER_NVFP4 or TIER_NF3
     nv: Optional["Checkpoint"] = None        # kept tier (NVFP4, or MXFP4), compact over its experts
@@ -174,6 +183,15 @@ def make_checkpoint(cfg: MoEConfig, seed: Optional[int] = None, E: Optional[int]
         return make_fp4_checkpoint(rng, "mxfp4", E, H, I, cfg.scale_lo, cfg.scale_hi, layout)
     if cfg.quant == "w4a16_nvfp4":
         return make_fp4_checkpoint(rng, "nvfp4", E, H, I, cfg.scale_lo, cfg.scale_hi, layout)
+    if cfg.quant == "w4a8_nvfp4":
+        # NVFP4 weights with MXFP8 activations: activation global scales 1 / input_scale =
+        # 6 x 448 / calibration amax, drawn log-uniformly over a factor 4 around an amax of 5
+        # for x (N(0,1) rows) and 8 for h (the full-size layer's SwiGLU outputs reach ~6)
+        ck = make_fp4_checkpoint(rng, "nvfp4", E, H, I, cfg.scale_lo, cfg.scale_hi, layout)
+        ck.quant = "w4a8_nvfp4"
+        ck.a13 = (2688.0 / 5.0 * 2.0 ** rng.uniform(-1, 1, size=E)).astype(np.float32)
+        ck.a2 = (2688.0 / 8.0 * 2.0 ** rng.uniform(-1, 1, size=E)).astype(np.float32)
+        return ck
     if cfg.quant in ("hybrid", "hybrid_mx"):
         n4 = min(cfg.n_nvfp4, E) if E != cfg.E else cfg.n_nvfp4
         # Which experts are kept in NVFP4 is a seeded random subset (the pages keep the top-64

@@ -60,7 +60,7 @@ def test_plan_weights_shapes_and_sizes(lib):
     assert moe.moe_prepared_bytes(wp) == nv_bytes + 2 * 256
     moe.moe_destroy_weight_plan(wp)
     with pytest.raises(moe.MoEError) as ei:
-        moe.moe_plan_weights(4, 256, 128, 4, tier_of_expert=[4, 3, 3, 4])
+        moe.moe_plan_weights(4, 256, 128, 5)
     assert ei.value.status == 3
 
 
@@ -175,3 +175,24 @@ def test_router_weight_on_input_arguments(lib):
         moe.moe_plan_set_router_weight_on_input(p, 2)
     assert ei.value.status == 1
     moe.moe_destroy_plan(p)
+
+
+def test_nvfp4_a8_mode_limits(lib):
+    """NVFP4 weights with MXFP8 activations: the tensor-core backend only, with round_up(I, 128)
+    a multiple of 256; the activation global scales are part of the prepared buffer."""
+    wp = moe.moe_plan_weights(4, 256, 128, moe.MOE_W4A8_NVFP4)
+    wp16 = moe.moe_plan_weights(4, 256, 128, moe.MOE_W4A16_NVFP4)
+    assert moe.moe_prepared_bytes(wp) == moe.moe_prepared_bytes(wp16) + 2 * 256
+    moe.moe_destroy_weight_plan(wp)
+    moe.moe_destroy_weight_plan(wp16)
+    p = moe.moe_plan(8, 256, 256, 2, 16, moe.MOE_W4A8_NVFP4, float("inf"), 0)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_plan_set_backend(p, 1)
+    assert ei.value.status == 3
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_plan_set_router_weight_on_input(p, 1)
+    assert ei.value.status == 3
+    moe.moe_destroy_plan(p)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_plan(8, 256, 128, 2, 16, moe.MOE_W4A8_NVFP4, float("inf"), 0)   # Ip = 128
+    assert ei.value.status == 3

@@ -378,6 +378,53 @@ def test_router_weight_on_input(quant, M, det, backend):
     layer.close()
 
 
+@pytest.mark.parametrize("M,det", [(5, 1), (16, 0), (40, 1), (200, 0), (600, 1)])
+def test_nvfp4_mxfp8_activations(M, det):
+    """NVFP4 weights with MXFP8 activations and per-expert activation global scales, on the
+    16-bit tensor-core kernels, at every token-tile width and both fc1 schedules: every row
+    against the oracle, and fc2's operand - the MXFP8 value of a2 * h - code for code, except
+    where fp32 noise decides a near-midpoint rounding (there it must be the other neighbour)."""
+    cfg = small_cfg("w4a8_nvfp4", I=256)
+    ck = S.make_checkpoint(cfg, seed=8000 + M)
+    rng = np.random.default_rng(8001 + M)
+    x = S.make_x(rng, M, cfg.H)
+    ids = S.zipf_topk(rng, M, cfg.E, cfg.topk, 0.8)
+    ids[rng.random(ids.shape) < 0.05] = -1
+    w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 1.0)
+    layer = _layer(ck, cfg.topk, M, math.inf, det)
+    got = run_layer(layer, x, ids, w)
+    st, code = layer.device_error()
+    assert st == 0 and code == 0, code
+    check_rows(got, ck, x, ids, w, math.inf)
+    hq, _ = layer.intermediate(M)
+    got_h = hq[:, : cfg.I].view(np.float16).astype(np.float64)
+    h = O.slot_intermediate(ck, x, ids, math.inf)
+    _, _, perm, _ = O.route(ids, cfg.E)
+    a2 = ck.a2.astype(np.float64)[ids.reshape(-1)[perm]][:, None]
+    q, sc = C.mxfp8_quantize(h * a2)
+    want_h = C.mxfp8_dequantize(q, sc)
+    amb, alt = C.mxfp8_alternates(h * a2, 1e-4)
+    mism = got_h != want_h
+    rate = float(mism.mean())
+    assert np.all(amb[mism]), "a code differs where the rounding is not decided by fp32 noise"
+    assert np.all(got_h[mism] == alt[mism])
+    assert rate < 2e-3
+    layer.close()
+
+
+def test_nvfp4_mxfp8_activations_full_size_sampled():
+    cfg = S.CONFIGS["w4a8_nvfp4"]
+    ck = S.make_checkpoint(cfg)
+    for M, rows in ((8, [0, 3, 7]), (512, [0, 255, 511])):
+        x, ids, w = S.make_inputs(cfg, M)
+        layer = _layer(ck, cfg.topk, M, cfg.swiglu_limit, 1)
+        got = run_layer(layer, x, ids, w)
+        st, code = layer.device_error()
+        assert st == 0 and code == 0, code
+        check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=rows)
+        layer.close()
+
+
 def test_nvfp4_full_size_sampled():
     cfg = S.CONFIGS["w4a16_nvfp4"]
     ck = S.make_checkpoint(cfg)

@@ -86,6 +86,7 @@ def test_swiglu_closed_forms():
 
 def _tiny(quant, seed=0, E=6, H=64, I=32, layout=S.W13_UP_GATE):
     cfg = {"mxfp4": S.CONFIGS["tiny_w4a8"], "nvfp4": S.CONFIGS["w4a16_nvfp4"],
+           "w4a8_nvfp4": S.CONFIGS["w4a8_nvfp4"],
            "hybrid": S.CONFIGS["hybrid_nvfp4_nf3"],
            "hybrid_mx": S.CONFIGS["hybrid_mxfp4_nf3"]}[quant]
     if quant in ("hybrid", "hybrid_mx"):
@@ -95,7 +96,7 @@ def _tiny(quant, seed=0, E=6, H=64, I=32, layout=S.W13_UP_GATE):
 
 
 @pytest.mark.parametrize("quant,layout", [("mxfp4", 0), ("mxfp4", 1), ("nvfp4", 0), ("hybrid", 0),
-                                          ("hybrid_mx", 0), ("hybrid_mx", 1)])
+                                          ("hybrid_mx", 0), ("hybrid_mx", 1), ("w4a8_nvfp4", 0)])
 def test_forward_matches_bruteforce(quant, layout):
     cfg, ck = _tiny(quant, layout=layout)
     rng = np.random.default_rng(11)
@@ -152,6 +153,57 @@ def test_weight_on_input_special_cases():
     _, ck8 = _tiny("mxfp4")
     with pytest.raises(AssertionError):
         O.moe_forward(ck8, x[:, :ck8.H], ids % ck8.E, ones, weight_on_input=True)
+
+
+def _nv_a8_case(seed, a_pow2):
+    cfg, ck = _tiny("w4a8_nvfp4", seed=seed)
+    rng = np.random.default_rng(seed + 1)
+    if a_pow2 is not None:
+        ck.a13 = (2.0 ** rng.integers(-a_pow2, a_pow2 + 1, size=ck.E)).astype(np.float32)
+        ck.a2 = (2.0 ** rng.integers(-a_pow2, a_pow2 + 1, size=ck.E)).astype(np.float32)
+    M, k = 6, 3
+    x = S.make_x(rng, M, ck.H)
+    ids = S.uniform_topk(rng, M, ck.E, k)
+    w = S.router_weights(rng, M, k, "softmax", 1.0)
+    return ck, x, ids, w
+
+
+def test_nvfp4_a8_power_of_two_gscales_drop_out():
+    """MX scales are powers of two, so an activation global scale 2^k shifts every block scale
+    by k and leaves the codes alone: the layer with power-of-two global scales equals the layer
+    with global scales 1 exactly; a general global scale moves the MX grid and changes it."""
+    ck, x, ids, w = _nv_a8_case(31, 6)
+    _, f = O.moe_forward(ck, x, ids, w, return_f64=True)
+    ck.a13 = np.ones(ck.E, np.float32)
+    ck.a2 = np.ones(ck.E, np.float32)
+    _, f1 = O.moe_forward(ck, x, ids, w, return_f64=True)
+    assert np.array_equal(f, f1)
+    ck.a13 = np.full(ck.E, 1.37, np.float32)
+    _, f2 = O.moe_forward(ck, x, ids, w, return_f64=True)
+    assert not np.array_equal(f, f2)
+
+
+def test_nvfp4_a8_equals_w4a8_on_shared_values():
+    """NVFP4 weights whose two E4M3 scales of each group of 32 are the same power of two
+    (2^-9..2^8) and whose global scales are 1 are MXFP4 weights: with MXFP8 activations and
+    unit activation global scales, the layer must equal the W4A8 (MXFP4 x MXFP8) layer exactly,
+    pinning the mode to the W4A8 oracle."""
+    ck, x, ids, w = _nv_a8_case(41, None)
+    rng = np.random.default_rng(42)
+    ck.a13 = np.ones(ck.E, np.float32)
+    ck.a2 = np.ones(ck.E, np.float32)
+    ck.g13 = np.ones(ck.E, np.float32)
+    ck.g2 = np.ones(ck.E, np.float32)
+    mx = S.Checkpoint(quant="mxfp4", E=ck.E, H=ck.H, I=ck.I, layout=ck.layout, w13=ck.w13,
+                      w2=ck.w2)
+    to_e4m3 = np.vectorize(lambda b: _e4m3_code_of_pow2(int(b) - 127), otypes=[np.uint8])
+    for name, k in (("s13", ck.H // 32), ("s2", ck.I // 32)):
+        e8 = rng.integers(118, 136, size=(ck.E, getattr(ck, name).shape[1], k), dtype=np.uint8)
+        setattr(mx, name, e8)
+        setattr(ck, name, np.repeat(to_e4m3(e8), 2, axis=-1))
+    a, fa = O.moe_forward(ck, x, ids, w, return_f64=True)
+    b, fb = O.moe_forward(mx, x, ids, w, return_f64=True)
+    assert np.array_equal(fa, fb) and np.array_equal(a, b)
 
 
 def _e4m3_code_of_pow2(j):
