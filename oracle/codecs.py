@@ -35,6 +35,24 @@ def e2m1_value(code: int) -> float:
 E2M1_TABLE = np.array([e2m1_value(c) for c in range(16)], dtype=np.float64)
 
 
+_E2M1_POS = E2M1_TABLE[:8]          # 0, 0.5, 1, 1.5, 2, 3, 4, 6 (codes 0..7)
+
+
+def e2m1_encode_rne_sat(v) -> np.ndarray:
+    """fp64 -> E2M1 code: nearest of the eight magnitudes, ties to the even code (mantissa bit
+    0), saturating to 6; the sign bit is the input's sign (so -0 for a negative value that
+    rounds to zero)."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.minimum(np.abs(v), 6.0)
+    lo = np.clip(np.searchsorted(_E2M1_POS, a, side="right") - 1, 0, 7)
+    hi = np.minimum(lo + 1, 7)
+    dlo = a - _E2M1_POS[lo]
+    dhi = _E2M1_POS[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (lo % 2 == 1))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return np.where(np.signbit(v), code | 0x8, code).astype(np.uint8)
+
+
 def unpack_fp4(packed: np.ndarray) -> np.ndarray:
     """[..., n] bytes -> [..., 2n] nibble codes; element 2j is the low nibble of byte j."""
     p = np.asarray(packed, dtype=np.uint8)
@@ -204,6 +222,57 @@ def bf16_alternates(v: np.ndarray, rel: float, atol=0.0):
     mid = (near + other) / 2
     mask = (np.abs(v - mid) <= rel * np.abs(v) + atol) & (v != 0)
     return mask, np.where(mask, other, near)
+
+
+# ---------------------------------------------------------------------------- NVFP4 activations
+
+NV_BLOCK = 16
+
+
+def nvfp4_quantize(v32: np.ndarray):
+    """Quantise fp32 values (last axis a multiple of 16) to NVFP4 blocks of 16, every step in
+    fp32 arithmetic (the decisions are taken in the precision the kernels use):
+    vmax = max |v|;  scale code s = E4M3(fp32(vmax / 6)) (nearest-even, saturating);
+    code = E2M1(fp32(v / E4M3value(s))) (nearest-even, saturating), all zero when s is 0.
+    Returns (E2M1 codes uint8 [..., K], E4M3 scale codes uint8 [..., K/16])."""
+    v = np.asarray(v32, dtype=np.float32)
+    K = v.shape[-1]
+    assert K % NV_BLOCK == 0
+    blocks = v.reshape(v.shape[:-1] + (K // NV_BLOCK, NV_BLOCK))
+    vmax = np.abs(blocks).max(axis=-1)
+    s = e4m3_encode_rne_sat((vmax / np.float32(6.0)).astype(np.float32).astype(np.float64))
+    sv = e4m3_decode(s).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = (blocks / sv[..., None]).astype(np.float32)
+    codes = np.where((sv > 0)[..., None], e2m1_encode_rne_sat(q.astype(np.float64)), 0)
+    return codes.reshape(v.shape).astype(np.uint8), s
+
+
+def nvfp4_dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    vals = E2M1_TABLE[np.asarray(codes, dtype=np.uint8)]
+    K = vals.shape[-1]
+    sc = e4m3_decode(scales)
+    return (vals.reshape(vals.shape[:-1] + (K // NV_BLOCK, NV_BLOCK)) * sc[..., None]).reshape(
+        vals.shape)
+
+
+def nvfp4_alternates(v: np.ndarray, rel: float):
+    """As mxfp8_alternates for NVFP4 blocks (under the scale the quantiser picks from v):
+    elements whose scaled magnitude lies within rel of the midpoint of two E2M1 neighbours, and
+    the dequantised value of the neighbour the nearest rounding did not pick."""
+    v = np.asarray(v, dtype=np.float64)
+    q, s = nvfp4_quantize(v.astype(np.float32))
+    sc = np.repeat(e4m3_decode(s), NV_BLOCK, axis=-1).reshape(v.shape)
+    near = nvfp4_dequantize(q, s)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        a = np.where(sc > 0, np.abs(v) / sc, 0.0)
+    lo = np.clip(np.searchsorted(_E2M1_POS, np.minimum(a, 6.0), side="right") - 1, 0, 7)
+    hi = np.minimum(lo + 1, 7)
+    mid = (_E2M1_POS[lo] + _E2M1_POS[hi]) / 2
+    mask = (np.abs(a - mid) <= rel * a) & (hi != lo) & (a < 6.0) & (sc > 0)
+    picked_lo = np.abs(near) == _E2M1_POS[lo] * sc
+    other = np.where(picked_lo, _E2M1_POS[hi], _E2M1_POS[lo]) * sc
+    return mask, np.where(mask, np.copysign(other, v), near)
 
 
 def mxfp8_dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:

@@ -13,6 +13,9 @@ Readings where the pages are silent (each one is listed with its reason in the d
     L = +inf means no clamp, which is the plain silu(g) * u of ``_apply_ref``.
   * W4A8: x is quantised to MXFP8 before fc1, h is quantised to MXFP8 before fc2 (from the
     unrounded SwiGLU output).  W4A16: x enters as bf16, h is rounded to bf16 before fc2.
+  * NVFP4 weights with MXFP8 or NVFP4 activations: the activations (x and h) are multiplied by
+    the expert's activation global scale in fp32, quantised (OCP MX rule, or NVFP4 blocks of 16
+    with an E4M3 scale of vmax / 6), dequantised and divided by the scale.
   * Hybrid layers: the kept tier is NVFP4, or MXFP4 for hybrid_loader.py's "v3" kept format
     (``_build_kept_mxfp4``, A16 default); either way with bf16 activations.
   * The result is accumulated in fp64 over the top-k slots and rounded to bf16 once.
@@ -110,7 +113,7 @@ def expert_weights(ck, e: int):
     H, I = ck.H, ck.I
     if ck.quant == "mxfp4":
         return dequant_mxfp4(ck.w13[e], ck.s13[e]), dequant_mxfp4(ck.w2[e], ck.s2[e]), "mxfp4"
-    if ck.quant in ("nvfp4", "w4a8_nvfp4"):
+    if ck.quant in ("nvfp4", "w4a8_nvfp4", "w4a4_nvfp4"):
         return (dequant_nvfp4(ck.w13[e], ck.s13[e], ck.g13[e]),
                 dequant_nvfp4(ck.w2[e], ck.s2[e], ck.g2[e]), "nvfp4")
     if ck.quant == "nf3":
@@ -139,9 +142,24 @@ def act_gscale(ck, which: str):
     """Per-expert activation global scales [E] of fc1's ("a1") or fc2's ("a2") input, or None
     (B12xExperts ``_prepare_experts``: the NVFP4 modes with quantised activations take
     a1_gscale / a2_gscale)."""
-    if ck.quant != "w4a8_nvfp4":
+    if ck.quant not in ("w4a8_nvfp4", "w4a4_nvfp4"):
         return None
     return ck.a13 if which == "a1" else ck.a2
+
+
+def activation_nv4(ck) -> bool:
+    """NVFP4 activations (W4A4: B12xExperts quant mode "nvfp4", kNvfp4Static weights with
+    kNvfp4Dynamic activations)."""
+    return ck.quant == "w4a4_nvfp4"
+
+
+def nvfp4_act(v, a):
+    """NVFP4 activations with the expert's global scale a: the fp32 product a * v quantised by
+    codecs.nvfp4_quantize, dequantised and divided by a (reading: as for MXFP8 activations)."""
+    a32 = np.float32(a)
+    va = (a32 * np.asarray(v, dtype=np.float64).astype(np.float32)).astype(np.float32)
+    q, s = C.nvfp4_quantize(va)
+    return C.nvfp4_dequantize(q, s) / np.float64(a32)
 
 
 def quantize_x(x_bits: np.ndarray, a8: bool, a=None):
@@ -192,13 +210,15 @@ def moe_forward(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.
     M, k = ids.shape
     E, H, I = ck.E, ck.H, ck.I
     a8 = activation_a8(ck)
-    assert not (a8 and weight_on_input), "router weights on the input need 16-bit activations"
+    assert not ((a8 or activation_nv4(ck)) and weight_on_input), \
+        "router weights on the input need 16-bit activations"
     out = np.zeros((M, H), dtype=np.float64)
     row_mask = np.ones(M, dtype=bool)
     if rows is not None:
         row_mask[:] = False
         row_mask[np.asarray(rows)] = True
     a1, a2 = act_gscale(ck, "a1"), act_gscale(ck, "a2")
+    nv4 = activation_nv4(ck)
     _, _, xhat = quantize_x(x_bits[row_mask] if rows is not None else x_bits, a8 and a1 is None)
     if rows is not None:
         full = np.full((M, H), np.nan)
@@ -210,12 +230,14 @@ def moe_forward(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.
         t_idx, j_idx = np.nonzero(sel)
         W13, W2, _ = expert_weights(ck, int(e))
         xin, cw = slot_input(xhat[t_idx], w[t_idx, j_idx], weight_on_input)
-        if a1 is not None:     # MXFP8 activations with the expert's global scale
+        if nv4:                # NVFP4 activations with the expert's global scale
+            xin = nvfp4_act(C.bf16_bits_to_f64(x_bits[t_idx]), a1[e])
+        elif a1 is not None:   # MXFP8 activations with the expert's global scale
             xin = quantize_x(x_bits[t_idx], True, a1[e])[2]
         G = xin @ W13.T
         gate, up = split_w13(G, I, ck.layout)
         h = swiglu(gate, up, limit, alpha, beta)
-        hh = requant_h(h, a8, None if a2 is None else a2[e])
+        hh = nvfp4_act(h, a2[e]) if nv4 else requant_h(h, a8, None if a2 is None else a2[e])
         y = hh @ W2.T
         np.add.at(out, t_idx, cw[:, None] * y)
     out[~row_mask] = np.nan
@@ -244,7 +266,9 @@ def slot_intermediate(ck, x_bits, topk_ids, limit=math.inf, alpha=1.0, beta=0.0,
         W13, _, _ = expert_weights(ck, e)
         fl = perm[lo:hi]
         xin = xhat[fl // k]
-        if a1 is not None:
+        if activation_nv4(ck):
+            xin = nvfp4_act(C.bf16_bits_to_f64(np.asarray(x_bits)[fl // k]), a1[e])
+        elif a1 is not None:
             xin = quantize_x(np.asarray(x_bits)[fl // k], True, a1[e])[2]
         if weight_on_input:
             xin, _ = slot_input(xin, np.asarray(topk_w, np.float64).reshape(-1)[fl], True)
@@ -268,7 +292,12 @@ def requant_alternatives(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0
     h = slot_intermediate(ck, x_bits, ids, limit, alpha, beta, topk_w, weight_on_input)
     _, _, perm, _ = route(ids, ck.E)
     a2 = act_gscale(ck, "a2")
-    if a8:
+    if activation_nv4(ck):
+        sc = np.float32(a2)[ids.reshape(-1)[perm]].astype(np.float64)[:, None]
+        mask, alt = C.nvfp4_alternates(h * sc, rel)
+        near = C.nvfp4_dequantize(*C.nvfp4_quantize((h * sc).astype(np.float32))) / sc
+        alt = alt / sc
+    elif a8:
         # with an activation global scale the decisions are taken on a2 * h
         sc = (np.ones(h.shape[0]) if a2 is None else
               np.float32(a2)[ids.reshape(-1)[perm]].astype(np.float64))[:, None]
@@ -321,7 +350,7 @@ def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1
             sub, li = ck, e
         codes = getattr(sub, mat)[li]
         scales = getattr(sub, "s13" if mat == "w13" else "s2")[li]
-        if sub.quant in ("mxfp4", "nvfp4", "w4a8_nvfp4"):
+        if sub.quant in ("mxfp4", "nvfp4", "w4a8_nvfp4", "w4a4_nvfp4"):
             byte = int(codes[r, c // 2])
             nib = byte & 0xF if c % 2 == 0 else byte >> 4
             v = C.e2m1_value(nib)
@@ -342,7 +371,9 @@ def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1
             if not (0 <= e < E):
                 continue
             xt = xhat[t]
-            if a1 is not None:
+            if activation_nv4(ck):
+                xt = nvfp4_act(C.bf16_bits_to_f64(np.asarray(x_bits)[t:t + 1]), a1[e])[0]
+            elif a1 is not None:
                 xt = quantize_x(np.asarray(x_bits)[t:t + 1], True, a1[e])[2][0]
             cw = w[t][j]
             if weight_on_input:
@@ -366,7 +397,8 @@ def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1
                 g = min(gate[i], limit)
                 u = max(-limit, min(up[i], limit))
                 h[i] = g * (1.0 / (1.0 + math.exp(-alpha * g))) * (u + beta)
-            hh = requant_h(np.array(h), a8, None if a2 is None else a2[e]).tolist()
+            hh = (nvfp4_act(np.array(h)[None, :], a2[e])[0] if activation_nv4(ck) else
+                  requant_h(np.array(h), a8, None if a2 is None else a2[e])).tolist()
             for r in range(H):
                 s = 0.0
                 for i in range(I):

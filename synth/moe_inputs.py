@@ -39,7 +39,8 @@ class MoEConfig:
     H: int
     I: int
     topk: int
-    quant: str                 # "w4a8_mxfp4" | "w4a16_nvfp4" | "w4a8_nvfp4" | "hybrid" | "hybrid_mx"
+    quant: str                 # "w4a8_mxfp4" | "w4a16_nvfp4" | "w4a8_nvfp4" | "w4a4_nvfp4" |
+                               # "hybrid" | "hybrid_mx"
     swiglu_limit: float        # +inf = no clamp
     m_list: tuple
     routing: str = "uniform"   # "uniform" | "zipf"
@@ -104,6 +105,12 @@ CONFIGS = {
                             swiglu_limit=INF, m_list=(1, 8, 64, 512, 2048),
                             weight_rule="sigmoid_norm", scale_lo=0x08, scale_hi=0x48,
                             seed_base=4100),
+    # NVFP4 weights with NVFP4 activations (B12xExperts "nvfp4", W4A4): the same layer and
+    # activation global scales.
+    "w4a4_nvfp4": MoEConfig("w4a4_nvfp4", E=256, H=6144, I=512, topk=8, quant="w4a4_nvfp4",
+                            swiglu_limit=INF, m_list=(1, 8, 64, 512, 2048),
+                            weight_rule="sigmoid_norm", scale_lo=0x08, scale_hi=0x48,
+                            seed_base=4200),
     # Hybrid "v3": the same layer with the 64 kept experts in MXFP4 (E8M0 2^-8..2^-2) and bf16
     # activations; NF3 tier as above.
     "hybrid_mxfp4_nf3": MoEConfig("hybrid_mxfp4_nf3", E=256, H=6144, I=512, topk=8,
@@ -117,7 +124,8 @@ CONFIGS = {
 @dataclasses.dataclass
 class Checkpoint:
     """Checkpoint-layout tensors of one MoE layer (numpy, host)."""
-    quant: str                      # "mxfp4" | "nvfp4" | "w4a8_nvfp4" | "nf3" | "hybrid"
+    quant: str                      # "mxfp4" | "nvfp4" | "w4a8_nvfp4" | "w4a4_nvfp4" | "nf3" |
+                                    # "hybrid"
     E: int
     H: int
     I: int
@@ -183,12 +191,12 @@ def make_checkpoint(cfg: MoEConfig, seed: Optional[int] = None, E: Optional[int]
         return make_fp4_checkpoint(rng, "mxfp4", E, H, I, cfg.scale_lo, cfg.scale_hi, layout)
     if cfg.quant == "w4a16_nvfp4":
         return make_fp4_checkpoint(rng, "nvfp4", E, H, I, cfg.scale_lo, cfg.scale_hi, layout)
-    if cfg.quant == "w4a8_nvfp4":
+    if cfg.quant in ("w4a8_nvfp4", "w4a4_nvfp4"):
         # NVFP4 weights with MXFP8 activations: activation global scales 1 / input_scale =
         # 6 x 448 / calibration amax, drawn log-uniformly over a factor 4 around an amax of 5
         # for x (N(0,1) rows) and 8 for h (the full-size layer's SwiGLU outputs reach ~6)
         ck = make_fp4_checkpoint(rng, "nvfp4", E, H, I, cfg.scale_lo, cfg.scale_hi, layout)
-        ck.quant = "w4a8_nvfp4"
+        ck.quant = cfg.quant
         ck.a13 = (2688.0 / 5.0 * 2.0 ** rng.uniform(-1, 1, size=E)).astype(np.float32)
         ck.a2 = (2688.0 / 8.0 * 2.0 ** rng.uniform(-1, 1, size=E)).astype(np.float32)
         return ck

@@ -220,3 +220,56 @@ def test_rounding_alternates():
     atol[0, 1] = 2e-3
     mask, alt = C.mxfp8_alternates(v, 1e-4, atol)
     assert mask[0, 1] and alt[0, 1] == 1.0 and not mask[0, 3]
+
+
+def test_e2m1_encode_nearest_even_by_brute_force():
+    """E2M1 encoding: for values on and between the grid (midpoints included), the code is the
+    nearest of the eight magnitudes by exhaustive search, a tie takes the code with mantissa
+    bit 0, magnitudes beyond 6 saturate, and the sign follows the input."""
+    grid = C.E2M1_TABLE[:8]
+    vals = np.concatenate([grid, (grid[1:] + grid[:-1]) / 2, np.linspace(0, 7, 113),
+                           [6.0001, 1e9]])
+    for v in vals:
+        d = np.abs(grid - min(v, 6.0))
+        best = np.flatnonzero(d == d.min())
+        want = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
+        assert C.e2m1_encode_rne_sat(v) == want, v
+        assert C.e2m1_encode_rne_sat(-v) == want | 8, v
+
+
+def test_nvfp4_worked_block():
+    """A block worked by hand: v = fp32(0.1 i), i = 0..15.  vmax / 6 = 0.25 = 2^-2, the E4M3
+    code 0x28 (exponent field 5); v / 0.25 = 0, 0.4, 0.8, ..., 6 rounds to the E2M1 grid
+    0, .5, 1, 1, 1.5, 2, 2, 3, 3, 4, 4, 4, 4, 6, 6, 6."""
+    v = (np.arange(16, dtype=np.float32) * np.float32(0.1))[None, :]
+    q, s = C.nvfp4_quantize(v)
+    assert s.tolist() == [[0x28]]
+    want = [0, .5, 1, 1, 1.5, 2, 2, 3, 3, 4, 4, 4, 4, 6, 6, 6]
+    assert C.E2M1_TABLE[q[0]].tolist() == want
+    assert np.allclose(C.nvfp4_dequantize(q, s)[0], np.array(want) * 0.25, rtol=0, atol=0)
+
+
+def test_nvfp4_properties():
+    """Random blocks: the scale is the E4M3 value nearest vmax / 6; every element is within
+    half an E2M1 step (at its magnitude, in scaled units) of its dequantised value, except
+    saturation past 6; zero blocks give zero codes; the alternates flag only near-midpoints."""
+    rng = np.random.default_rng(5)
+    v = (rng.standard_normal((64, 64)) * 2.0 ** rng.integers(-8, 8, size=(64, 1))).astype(
+        np.float32)
+    v[3] = 0
+    q, s = C.nvfp4_quantize(v)
+    vmax = np.abs(v.reshape(64, 4, 16)).max(axis=-1) / 6
+    sv = C.e4m3_decode(s)
+    nxt = np.abs(C.E4M3_TABLE[np.minimum(s.astype(int) + 1, 126)] - vmax)
+    prv = np.abs(C.E4M3_TABLE[np.maximum(s.astype(int) - 1, 0)] - vmax)
+    assert np.all(np.abs(sv - vmax) <= np.minimum(nxt, prv) + 1e-30)
+    assert np.all(q[3] == 0)
+    x = np.abs(v.reshape(64, 4, 16)) / np.where(sv > 0, sv, 1)[..., None]
+    deq = C.E2M1_TABLE[q.reshape(64, 4, 16) & 7]
+    step = np.where(deq < 2, 0.5, np.where(deq < 4, 1.0, 2.0))
+    ok = (np.abs(x - deq) <= step / 2 + 1e-6) | (x > 6)
+    assert np.all(ok | (sv == 0)[..., None])
+    mask, alt = C.nvfp4_alternates(v.astype(np.float64), 1e-4)
+    near = C.nvfp4_dequantize(q, s)
+    assert np.all(alt[~mask] == near[~mask])
+    assert mask.mean() < 1e-2

@@ -86,7 +86,7 @@ def test_swiglu_closed_forms():
 
 def _tiny(quant, seed=0, E=6, H=64, I=32, layout=S.W13_UP_GATE):
     cfg = {"mxfp4": S.CONFIGS["tiny_w4a8"], "nvfp4": S.CONFIGS["w4a16_nvfp4"],
-           "w4a8_nvfp4": S.CONFIGS["w4a8_nvfp4"],
+           "w4a8_nvfp4": S.CONFIGS["w4a8_nvfp4"], "w4a4_nvfp4": S.CONFIGS["w4a4_nvfp4"],
            "hybrid": S.CONFIGS["hybrid_nvfp4_nf3"],
            "hybrid_mx": S.CONFIGS["hybrid_mxfp4_nf3"]}[quant]
     if quant in ("hybrid", "hybrid_mx"):
@@ -96,7 +96,8 @@ def _tiny(quant, seed=0, E=6, H=64, I=32, layout=S.W13_UP_GATE):
 
 
 @pytest.mark.parametrize("quant,layout", [("mxfp4", 0), ("mxfp4", 1), ("nvfp4", 0), ("hybrid", 0),
-                                          ("hybrid_mx", 0), ("hybrid_mx", 1), ("w4a8_nvfp4", 0)])
+                                          ("hybrid_mx", 0), ("hybrid_mx", 1), ("w4a8_nvfp4", 0),
+                                          ("w4a4_nvfp4", 0), ("w4a4_nvfp4", 1)])
 def test_forward_matches_bruteforce(quant, layout):
     cfg, ck = _tiny(quant, layout=layout)
     rng = np.random.default_rng(11)
@@ -204,6 +205,30 @@ def test_nvfp4_a8_equals_w4a8_on_shared_values():
     a, fa = O.moe_forward(ck, x, ids, w, return_f64=True)
     b, fb = O.moe_forward(mx, x, ids, w, return_f64=True)
     assert np.array_equal(fa, fb) and np.array_equal(a, b)
+
+
+def test_w4a4_power_of_two_gscales_drop_out():
+    """NVFP4 activations: scaling a block by 2^k moves vmax / 6 by 2^k, and while that stays in
+    E4M3's normal range the scale code shifts by k exponent steps with the same E2M1 codes, so
+    global scales that differ by powers of two give the same layer exactly."""
+    cfg, ck = _tiny("w4a4_nvfp4", seed=51)
+    rng = np.random.default_rng(52)
+    M, k = 5, 2
+    x = S.make_x(rng, M, ck.H)
+    ids = S.uniform_topk(rng, M, ck.E, k)
+    w = S.router_weights(rng, M, k, "softmax", 1.0)
+    # base scales that put a * x and a * h well inside E4M3's normal range (vmax / 6 >= 2^-6)
+    h = O.slot_intermediate(ck, x, ids, math.inf)
+    ck.a13 = np.full(ck.E, 64.0, np.float32)
+    ck.a2 = np.full(ck.E, np.float32(2.0 ** np.ceil(np.log2(64.0 / np.abs(h).max()))))
+    _, f0 = O.moe_forward(ck, x, ids, w, return_f64=True)
+    ck.a13 = ck.a13 * (2.0 ** rng.integers(-2, 3, size=ck.E)).astype(np.float32)
+    ck.a2 = ck.a2 * (2.0 ** rng.integers(-2, 3, size=ck.E)).astype(np.float32)
+    _, f1 = O.moe_forward(ck, x, ids, w, return_f64=True)
+    assert np.array_equal(f0, f1)
+    ck.a13 = ck.a13 * np.float32(1.3)
+    _, f2 = O.moe_forward(ck, x, ids, w, return_f64=True)
+    assert not np.array_equal(f0, f2)
 
 
 def _e4m3_code_of_pow2(j):
