@@ -72,7 +72,14 @@ typedef enum {
    * Each slot's fc1 input is MXFP8(a1[e] * x) / a1[e] (OCP MX rule on the fp32 products) and
    * fc2's is MXFP8(a2[e] * h) / a2[e]; runs on the tensor-core backend only, with
    * round_up(I, 128) a multiple of 256. */
-  MOE_W4A8_NVFP4 = 4
+  MOE_W4A8_NVFP4 = 4,
+  /* NVFP4 weights with NVFP4 activations (W4A4): B12xExperts quant mode "nvfp4"
+   * (kNvfp4Static weights x kNvfp4Dynamic activations; per-expert activation global scales
+   * a1_gscale / a2_gscale required).  Each slot's fc1 input is NVFP4(a1[e] * x) / a1[e] and
+   * fc2's NVFP4(a2[e] * h) / a2[e]: blocks of 16 with the E4M3 scale nearest vmax / 6 and E2M1
+   * codes nearest-even of v / scale, in fp32.  Runs on block-scaled FP4 tensor-core kernels
+   * (tcgen05 kind::mxf4nvf4) only, with H and round_up(I, 128) multiples of 256. */
+  MOE_W4A4_NVFP4 = 5
 } moe_quant_mode;
 
 typedef enum {
@@ -94,7 +101,8 @@ typedef struct moe_plan_s moe_plan_t;
  * fp4 fields hold the kept tier in the MXFP4 layout below (compacted the same way).
  *   MXFP4: w13 [E, 2I, H/2] u8 (element 2j = low nibble of byte j), s13 [E, 2I, H/32] u8 E8M0,
  *          w2 [E, H, I/2] u8, s2 [E, H, I/32] u8 E8M0; g13 = g2 = NULL.
- *   NVFP4: w13 [E4, 2I, H/2], s13 [E4, 2I, H/16] u8 E4M3, g13 [E4] f32,
+ *   NVFP4 (W4A16, W4A8_NVFP4, W4A4):
+ *          w13 [E4, 2I, H/2], s13 [E4, 2I, H/16] u8 E4M3, g13 [E4] f32,
  *          w2 [E4, H, I/2],   s2 [E4, H, I/16] u8 E4M3,  g2 [E4] f32.
  *   NF3:   nf_w13 [E3, 2I, 3H/8] u8 (8 codes per 3 bytes, hybrid_loader.py _unpack_nf3),
  *          nf_s13 [E3, 2I, H/32] u8 E4M3, nf_w2 [E3, H, 3I/8] u8, nf_s2 [E3, H, I/32] u8 E4M3. */
@@ -282,7 +290,9 @@ moe_status moe_call_launches(const moe_plan_t* plan, int M, int* launches);
 
 /* Test hook: the fc2 activation operand of the last call in slot order (synchronises).
  * W4A8: hq [S, Ip] E4M3 codes and hs [S, Ip/32] E8M0 bytes (Ip = I rounded up to 128; columns
- * >= I are zero).  W4A16 / hybrid: hq receives [S, Ip] bf16 values, hs is not written.
+ * >= I are zero).  W4A4: hq [S, Ip/2] packed E2M1 codes and hs [S, Ip/16] E4M3 scales.
+ * Other modes: hq receives [S, Ip] f16 values (bf16-rounded h, or the MXFP8 values of a2 * h
+ * for MOE_W4A8_NVFP4), hs is not written.
  * Buffers of M*topk rows suffice. */
 moe_status moe_debug_h(const moe_plan_t* plan, void* scratch, int M, void* hq, uint8_t* hs,
                        void* stream);

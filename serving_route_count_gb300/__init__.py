@@ -10,6 +10,6 @@ from .moe import (  # noqa: F401
     moe_get_device_error, moe_debug_routing, moe_debug_actq, moe_debug_h, moe_destroy_weight_plan,
     moe_destroy_prepared, moe_destroy_plan, moe_plan_set_profile_events, moe_profile_stage_names, moe_call_launches, moe_status_str,
     moe_version,
-    MOE_W4A8_MXFP4, MOE_W4A16_NVFP4, MOE_W4A16_HYBRID, MOE_W4A16_HYBRID_MX, MOE_W4A8_NVFP4, MOE_W13_UP_GATE, MOE_W13_GATE_UP,
+    MOE_W4A8_MXFP4, MOE_W4A16_NVFP4, MOE_W4A16_HYBRID, MOE_W4A16_HYBRID_MX, MOE_W4A8_NVFP4, MOE_W4A4_NVFP4, MOE_W13_UP_GATE, MOE_W13_GATE_UP,
     MOE_TIER_NVFP4, MOE_TIER_NF3,
 )

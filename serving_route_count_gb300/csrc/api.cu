@@ -15,8 +15,9 @@ cudaError_t launch_route(const int32_t* ids, int Mk, int E, int ep_first, int ti
                          int max_tiles, const RunPtrs& r, cudaStream_t st);
 cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
                         bool atoms, bool to_f16, const float* win, const float* ag,
-                        const int32_t* ids, int ep_first, int E, void* z0, size_t z0_words,
-                        void* z1, size_t z1_words, void* z2, size_t z2_words, cudaStream_t st);
+                        const int32_t* ids, int ep_first, int E, bool nv4, void* z0,
+                        size_t z0_words, void* z1, size_t z1_words, void* z2, size_t z2_words,
+                        cudaStream_t st);
 bool route_actq_small_supported(int Mk, int E);
 int route_chunks(int Mk);
 cudaError_t launch_route_count(const int32_t* ids, int Mk, int E, int ep_first,
@@ -29,8 +30,9 @@ cudaError_t launch_actq_rows(const void* x, int M, int H, int topk, const RunPtr
 cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_first,
                                     int tile_slots, int max_tiles, const void* x, int H, int topk,
                                     const RunPtrs& r, bool atoms, bool to_f16, const float* win,
-                                    const float* ag, void* z0, size_t z0_words, void* z1,
-                                    size_t z1_words, void* z2, size_t z2_words, cudaStream_t st);
+                                    const float* ag, bool nv4, void* z0, size_t z0_words,
+                                    void* z1, size_t z1_words, void* z2, size_t z2_words,
+                                    cudaStream_t st);
 // gemm_tc.cu
 cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                             int bn, int tiles, int splits, const float* topk_w, int M,
@@ -61,6 +63,11 @@ cudaError_t launch_repack_mx16_scales(const void* src, void* dst, int32_t* kmax,
                                       cudaStream_t st);
 cudaError_t launch_repack_w16_tiled(int kind, const void* src, void* dst, int E, int halves,
                                     int rows, int src_k, int K, int layout, cudaStream_t st);
+// gemm_tc4.cu
+int tc4_pick_bn(int M);
+cudaError_t launch_tc4_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
+                             int bn, int tiles, int splits, const float* topk_w, int M,
+                             cudaStream_t st);
 // gemm_tc16.cu
 bool tc16_fc1_pair(int bn, int quant);
 cudaError_t launch_tc16_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
@@ -140,7 +147,9 @@ int device_sms() {
 int fc1_splits(const PlanDims& d, int tiles, int bn) {
   const int units = std::max(1, tiles * cdiv(d.I, 128));
   const bool a8 = d.quant == MOE_W4A8_MXFP4;
-  const int slots = (a8 ? kFc1CtasPerSm : (tc16_fc1_pair(bn, d.quant) ? 2 : 1)) * device_sms();
+  const int per_sm = (a8 || d.quant == MOE_W4A4_NVFP4) ? kFc1CtasPerSm
+                                                       : (tc16_fc1_pair(bn, d.quant) ? 2 : 1);
+  const int slots = per_sm * device_sms();
   const int smax = a8 ? d.H / 128 / 4 : cdiv(d.H, 256) / 2;
   return std::max(1, std::min(std::min(slots / units, smax), 16));
 }
@@ -150,7 +159,7 @@ moe_status check_geometry(int E, int H, int I, int quant) {
   if (H < 128 || H % 128 != 0) return MOE_ERR_SHAPE;
   if (I < 64 || I % 64 != 0) return MOE_ERR_SHAPE;
   if ((long long)H * H > (1LL << 40) || (long long)I > (1 << 20)) return MOE_ERR_SHAPE;
-  if (quant < 0 || quant > 4) return MOE_ERR_UNSUPPORTED;
+  if (quant < 0 || quant > 5) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -226,9 +235,9 @@ moe_status moe_plan_weights(int E, int H, int I, int quant_mode, int w13_layout,
     const bool mx = quant_mode == MOE_W4A16_HYBRID_MX;
     wp->mxk13 = mx ? take(E4 * 4) : 0;
     wp->mxk2 = mx ? take(E4 * 4) : 0;
-    const bool nv_a8 = quant_mode == MOE_W4A8_NVFP4;
-    wp->ag13 = nv_a8 ? take(E4 * 4) : 0;
-    wp->ag2 = nv_a8 ? take(E4 * 4) : 0;
+    const bool act_g = quant_mode == MOE_W4A8_NVFP4 || quant_mode == MOE_W4A4_NVFP4;
+    wp->ag13 = act_g ? take(E4 * 4) : 0;
+    wp->ag2 = act_g ? take(E4 * 4) : 0;
   }
   wp->nf_w13 = take(E3 * t13 * kNfCodeTile);
   wp->nf_s13 = take(E3 * t13 * kW16ScaleTile);
@@ -263,7 +272,7 @@ moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* 
   if (nf3 && (src->nf_w13 == nullptr || src->nf_s13 == nullptr || src->nf_w2 == nullptr ||
               src->nf_s2 == nullptr))
     return MOE_ERR_ARG;
-  const bool nv_a8 = wp->quant == MOE_W4A8_NVFP4;
+  const bool nv_a8 = wp->quant == MOE_W4A8_NVFP4 || wp->quant == MOE_W4A4_NVFP4;
   if (nv_a8 && (src->a1_gscale == nullptr || src->a2_gscale == nullptr)) return MOE_ERR_ARG;
   uint8_t* base = static_cast<uint8_t*>(dst);
   const int E4 = wp->E4, E3 = wp->E3, H = wp->H, I = wp->I, Ip = wp->Ip, L = wp->layout;
@@ -293,8 +302,10 @@ moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* 
                                     reinterpret_cast<float*>(base + wp->g2), E4, 1, H, I, Ip, L,
                                     st));
     } else {
-      chk(launch_repack_w16_tiled(1, src->s13, base + wp->s13, E4, 2, I, H, H, L, st));
-      chk(launch_repack_w16_tiled(1, src->s2, base + wp->s2, E4, 1, H, I, Ip, L, st));
+      // NVFP4 scales: rows of the 16-bit path's tiles, or the W4A4 kernels' scale atoms
+      const int kind = wp->quant == MOE_W4A4_NVFP4 ? 4 : 1;
+      chk(launch_repack_w16_tiled(kind, src->s13, base + wp->s13, E4, 2, I, H, H, L, st));
+      chk(launch_repack_w16_tiled(kind, src->s2, base + wp->s2, E4, 1, H, I, Ip, L, st));
       chk(cudaMemcpyAsync(base + wp->g13, src->g13, (size_t)E4 * 4, cudaMemcpyDeviceToDevice, st));
       chk(cudaMemcpyAsync(base + wp->g2, src->g2, (size_t)E4 * 4, cudaMemcpyDeviceToDevice, st));
       if (nv_a8) {
@@ -348,6 +359,9 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   // MXFP8 activations with NVFP4 weights run on the 16-bit tensor-core kernels only
   if (quant_mode == MOE_W4A8_NVFP4 && align_up((size_t)I, 128) % 256 != 0)
     return MOE_ERR_UNSUPPORTED;
+  // W4A4: whole 256-wide K stages in both GEMMs (the activation scale atoms cover K exactly)
+  if (quant_mode == MOE_W4A4_NVFP4 && (H % 256 != 0 || align_up((size_t)I, 128) % 256 != 0))
+    return MOE_ERR_UNSUPPORTED;
   moe_plan_t* p = new (std::nothrow) moe_plan_t();
   if (p == nullptr) return MOE_ERR_ARG;
   PlanDims& d = p->d;
@@ -362,24 +376,26 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
   const bool a8 = quant_mode == MOE_W4A8_MXFP4;
+  const bool a4 = quant_mode == MOE_W4A4_NVFP4;     // packed E2M1 activations, 4X scale atoms
   s.ctrl = take(64 * 4);
   s.cnt = take((size_t)E * 4);
   s.off = take((size_t)(E + 1) * 4);
   s.perm = take(Sm * 4);
   s.slot_of = take(Sm * 4);
   s.tiles = take((size_t)s.max_tiles * 16);
-  s.xq = a8 ? take(Sm * H) : 0;
+  s.xq = a8 ? take(Sm * H) : (a4 ? take(Sm * H / 2) : 0);
   s.xs = a8 ? take(Sm * H / 32) : 0;
   // scale atom rows of the W4A8 tensor-core calls, padded for the widest tile (96 tokens) that
   // starts at the last slot position
   s.r16 = (int)Sm + 96;
-  s.xs16 = a8 ? take((size_t)(H / 128) * s.r16 * 16) : 0;
-  s.hs16 = a8 ? take((size_t)(d.Ip / 128) * s.r16 * 16) : 0;
+  s.xs16 = a8 ? take((size_t)(H / 128) * s.r16 * 16) : (a4 ? take((size_t)(H / 64) * s.r16 * 16) : 0);
+  s.hs16 = a8 ? take((size_t)(d.Ip / 128) * s.r16 * 16)
+              : (a4 ? take((size_t)(d.Ip / 64) * s.r16 * 16) : 0);
   // fc1 output of the CUDA-core path, or the per-split partial sums of the tensor-core path
   // ([split][slot][2][Ip], one slice per split, summed in split order)
   size_t g_rows = Sm;
   for (int m = 1; m <= max_m; ++m) {
-    const int bn_m = tc_pick_bn(m, topk, E, quant_mode == MOE_W4A8_MXFP4);
+    const int bn_m = a4 ? tc4_pick_bn(m) : tc_pick_bn(m, topk, E, quant_mode == MOE_W4A8_MXFP4);
     const int sp = fc1_splits(d, call_tiles(d, s.max_tiles, m, bn_m), bn_m);
     if (sp > 1) g_rows = std::max(g_rows, (size_t)sp * m * topk);
   }
@@ -387,10 +403,10 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   s.tickets = take(align_up((size_t)s.max_tiles * cdiv(I, 128), 4) * 4);
   s.part = a8 ? take(fc1_stream_part_bytes()) : 0;
   s.rcc = a8 ? take((size_t)route_chunks((int)Sm) * E * 4) : 0;
-  s.hq = a8 ? take(Sm * d.Ip) : 0;
+  s.hq = a8 ? take(Sm * d.Ip) : (a4 ? take(Sm * d.Ip / 2) : 0);
   s.hs = a8 ? take(Sm * d.Ip / 32) : 0;
-  s.h16 = a8 ? 0 : take(Sm * d.Ip * 2);
-  s.x16 = a8 ? 0 : take(Sm * H * 2);
+  s.h16 = (a8 || a4) ? 0 : take(Sm * d.Ip * 2);
+  s.x16 = (a8 || a4) ? 0 : take(Sm * H * 2);
   s.acc = d.deterministic ? 0 : take((size_t)max_m * H * 4);
   s.rbuf = d.deterministic ? take(Sm * H * 4) : 0;
   s.total = o;
@@ -427,6 +443,7 @@ static RunPtrs resolve(const moe_plan_t* plan, void* scratch) {
   uint8_t* b = static_cast<uint8_t*>(scratch);
   const Scratch& s = plan->s;
   const bool a8 = plan->d.quant == MOE_W4A8_MXFP4;
+  const bool a4 = plan->d.quant == MOE_W4A4_NVFP4;
   RunPtrs r;
   r.ctrl = reinterpret_cast<int32_t*>(b + s.ctrl);
   r.cnt = reinterpret_cast<int32_t*>(b + s.cnt);
@@ -434,19 +451,19 @@ static RunPtrs resolve(const moe_plan_t* plan, void* scratch) {
   r.perm = reinterpret_cast<int32_t*>(b + s.perm);
   r.slot_of = reinterpret_cast<int32_t*>(b + s.slot_of);
   r.tiles = reinterpret_cast<int4*>(b + s.tiles);
-  r.xq = a8 ? b + s.xq : nullptr;
+  r.xq = (a8 || a4) ? b + s.xq : nullptr;
   r.xs = a8 ? b + s.xs : nullptr;
-  r.xs16 = a8 ? b + s.xs16 : nullptr;
-  r.hs16 = a8 ? b + s.hs16 : nullptr;
+  r.xs16 = (a8 || a4) ? b + s.xs16 : nullptr;
+  r.hs16 = (a8 || a4) ? b + s.hs16 : nullptr;
   r.r16 = s.r16;
   r.g = reinterpret_cast<float*>(b + s.g);
   r.tickets = reinterpret_cast<int32_t*>(b + s.tickets);
   r.part = a8 ? reinterpret_cast<float*>(b + s.part) : nullptr;
   r.rcc = a8 ? reinterpret_cast<int32_t*>(b + s.rcc) : nullptr;
-  r.hq = a8 ? b + s.hq : nullptr;
+  r.hq = (a8 || a4) ? b + s.hq : nullptr;
   r.hs = a8 ? b + s.hs : nullptr;
-  r.h16 = a8 ? nullptr : reinterpret_cast<__nv_bfloat16*>(b + s.h16);
-  r.x16 = a8 ? nullptr : reinterpret_cast<uint16_t*>(b + s.x16);
+  r.h16 = (a8 || a4) ? nullptr : reinterpret_cast<__nv_bfloat16*>(b + s.h16);
+  r.x16 = (a8 || a4) ? nullptr : reinterpret_cast<uint16_t*>(b + s.x16);
   r.acc = plan->d.deterministic ? nullptr : reinterpret_cast<float*>(b + s.acc);
   r.rbuf = plan->d.deterministic ? reinterpret_cast<float*>(b + s.rbuf) : nullptr;
   return r;
@@ -479,8 +496,11 @@ static bool use_tc(const PlanDims& d) { return d.backend == 0 && d.quant == MOE_
 // W4A16 / hybrid on tensor cores: the NVFP4 scale rows of fc2 (Ip/16 bytes) must be whole
 // 16-byte units for the tensor maps.
 static bool use_tc16(const PlanDims& d) {
-  return d.backend == 0 && d.quant != MOE_W4A8_MXFP4 && d.Ip % 256 == 0;
+  return d.backend == 0 && d.quant != MOE_W4A8_MXFP4 && d.quant != MOE_W4A4_NVFP4 &&
+         d.Ip % 256 == 0;
 }
+// W4A4 runs on its block-scaled FP4 kernels only (moe_plan refuses the CUDA-core backend)
+static bool use_tc4(const PlanDims& d) { return d.quant == MOE_W4A4_NVFP4; }
 
 const char* moe_profile_stage_names(const moe_plan_t* plan) {
   if (plan == nullptr) return "";
@@ -496,7 +516,8 @@ moe_status moe_plan_set_fc1_kernel(moe_plan_t* plan, int choice) {
 
 moe_status moe_plan_set_router_weight_on_input(moe_plan_t* plan, int on) {
   if (plan == nullptr || (on != 0 && on != 1)) return MOE_ERR_ARG;
-  if (on && (plan->d.quant == MOE_W4A8_MXFP4 || plan->d.quant == MOE_W4A8_NVFP4))
+  if (on && (plan->d.quant == MOE_W4A8_MXFP4 || plan->d.quant == MOE_W4A8_NVFP4 ||
+             plan->d.quant == MOE_W4A4_NVFP4))
     return MOE_ERR_UNSUPPORTED;
   plan->d.w_on_input = on;
   return MOE_OK;
@@ -511,7 +532,8 @@ moe_status moe_plan_set_expert_offset(moe_plan_t* plan, int first_expert) {
 
 moe_status moe_plan_set_backend(moe_plan_t* plan, int backend) {
   if (plan == nullptr || backend < 0 || backend > 1) return MOE_ERR_ARG;
-  if (backend == 1 && plan->d.quant == MOE_W4A8_NVFP4) return MOE_ERR_UNSUPPORTED;
+  if (backend == 1 && (plan->d.quant == MOE_W4A8_NVFP4 || plan->d.quant == MOE_W4A4_NVFP4))
+    return MOE_ERR_UNSUPPORTED;
   plan->d.backend = backend;
   return MOE_OK;
 }
@@ -524,7 +546,7 @@ moe_status moe_call_launches(const moe_plan_t* plan, int M, int* launches) {
     *launches = 0;
     return MOE_OK;
   }
-  const bool tc8 = use_tc(d), t16 = use_tc16(d);
+  const bool tc8 = use_tc(d), t16 = use_tc16(d) || use_tc4(d);
   if (tc8 || t16) {
     // routing and quantisation / conversion (one launch for calls of at most 256 flat slots;
     // beyond, three - counts, scatter, quantisation - for W4A8, two for the 16-bit path), fc1,
@@ -559,10 +581,10 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   const RunPtrs r = resolve(plan, scratch);
   const ProfRec prof{&plan->prof, st, !plan->prof.empty() && capturing(st)};
   const bool a8 = d.quant == MOE_W4A8_MXFP4;
-  const bool tc8 = use_tc(d), t16 = use_tc16(d);
-  const bool tc = tc8 || t16;
+  const bool tc8 = use_tc(d), t16 = use_tc16(d), t4 = use_tc4(d);
+  const bool tc = tc8 || t16 || t4;
   const int Sm = M * d.topk;
-  const int bn = tc ? tc_pick_bn(M, d.topk, d.E, tc8) : kSimtSlots;
+  const int bn = t4 ? tc4_pick_bn(M) : (tc ? tc_pick_bn(M, d.topk, d.E, tc8) : kSimtSlots);
   const int tiles = call_tiles(d, plan->s.max_tiles, M, bn);
   const int RT = cdiv(d.I, 128);
   // decode widths with more units than one wave of CTAs: the persistent stream-K fc1
@@ -588,8 +610,8 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   cudaError_t e;
   if (small) {
     e = launch_route_actq_small(topk_ids, Sm, d.E, d.ep_first, bn, plan->s.max_tiles, x, d.H,
-                                d.topk, r, atoms, t16, win, w.ag13, acc, acc_words, g, g_words,
-                                tk, tk_words, st);
+                                d.topk, r, atoms, t16, win, w.ag13, t4, acc, acc_words, g,
+                                g_words, tk, tk_words, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
   } else if (tc8) {
@@ -605,15 +627,17 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
     e = launch_route(topk_ids, Sm, d.E, d.ep_first, bn, plan->s.max_tiles, r, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
-    if (a8 || acc || g || t16) {
+    if (a8 || acc || g || t16 || t4) {
       e = launch_actq(x, M, d.H, d.topk, r, a8, atoms, t16, win, w.ag13, topk_ids, d.ep_first,
-                      d.E, acc, acc_words, g, g_words, tk, tk_words, st);
+                      d.E, t4, acc, acc_words, g, g_words, tk, tk_words, st);
       if (e != cudaSuccess) return cuda_status(e);
     }
   }
   prof(2);
   if (tc) {
-    if (streamk)
+    if (t4)
+      e = launch_tc4_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st);
+    else if (streamk)
       e = launch_fc1_stream(w, r, d, bn, M, r.part, r.tickets, topk_ids, plan->s.max_tiles, st);
     else
       e = tc8 ? launch_tc_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, topk_ids,
@@ -621,7 +645,9 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
               : launch_tc16_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(3);
-    if (tc8 && fc2_persist_preferred(bn, tiles * (d.H / 128)))
+    if (t4)
+      e = launch_tc4_stage(1, w, r, d, bn, tiles, 1, wcomb, M, st);
+    else if (tc8 && fc2_persist_preferred(bn, tiles * (d.H / 128)))
       e = launch_fc2_persist(w, r, d, bn, M, topk_weights, st);
     else
       e = tc8 ? launch_tc_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, nullptr, 0, st)
@@ -761,6 +787,18 @@ moe_status moe_debug_h(const moe_plan_t* plan, void* scratch, int M, void* hq, u
     if (hq && S) e = cudaMemcpyAsync(hq, r.hq, (size_t)S * Ip, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess && hs && S)
       e = cudaMemcpyAsync(hs, r.hs, (size_t)S * Ip / 32, cudaMemcpyDeviceToHost, st);
+  } else if (plan->d.quant == MOE_W4A4_NVFP4) {
+    // packed E2M1 codes, and the E4M3 scales gathered from the atom rows [Ip/64][r16][16]
+    if (hq && S) e = cudaMemcpyAsync(hq, r.hq, (size_t)S * Ip / 2, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && hs && S) {
+      std::vector<uint8_t> rows((size_t)(Ip / 64) * r.r16 * 16);
+      e = cudaMemcpyAsync(rows.data(), r.hs16, rows.size(), cudaMemcpyDeviceToHost, st);
+      if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+      if (e == cudaSuccess)
+        for (int q = 0; q < S; ++q)
+          for (size_t g = 0; g < Ip / 16; ++g)
+            hs[(size_t)q * (Ip / 16) + g] = rows[((g / 4) * r.r16 + q) * 16 + g % 4];
+    }
   } else if (hq && S) {
     e = cudaMemcpyAsync(hq, r.h16, (size_t)S * Ip * 2, cudaMemcpyDeviceToHost, st);
   }

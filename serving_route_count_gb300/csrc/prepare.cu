@@ -198,6 +198,35 @@ __global__ void repack_mx16_scales_tiled_kernel(const uint8_t* __restrict__ src,
   }
 }
 
+// NVFP4 weight scales as the W4A4 kernels' tensor-memory atoms: per 128-row x 256-K tile four
+// 512-byte atoms (one per K = 64 instruction), byte (r % 32) * 16 + (r / 32) * 4 + j of atom kb
+// = the E4M3 scale of tile row r, group of 16 number 4 kb + j.  src [E][halves*rows][src_k/16].
+__global__ void repack_nv_sf_atoms_kernel(const uint8_t* __restrict__ src,
+                                          uint8_t* __restrict__ dst, int E, int halves, int rows,
+                                          int src_k, int K, int layout) {
+  const int rbs = (rows + 127) / 128, kts = (K + 255) / 256;
+  const size_t n = (size_t)E * halves * rbs * kts * kW16ScaleTile;
+  GRID_STRIDE(idx, n) {
+    const int off = (int)(idx % kW16ScaleTile);
+    size_t t = idx / kW16ScaleTile;
+    const int kt = (int)(t % kts);
+    t /= kts;
+    const int rb = (int)(t % rbs);
+    const size_t mat = t / rbs;
+    const int kb = off >> 9, b = off & 511;
+    const int rr = (b >> 4) + 32 * ((b >> 2) & 3), j = b & 3;
+    const int r = rb * 128 + rr, g = kt * 16 + kb * 4 + j;
+    uint8_t v = 0;
+    if (r < rows && g < src_k / 16) {
+      const int half = (int)(mat % halves);
+      const size_t e = mat / halves;
+      const int sr = halves == 2 ? src_row_fc1(half, r, rows, layout) : r;
+      v = src[(e * (size_t)(halves * rows) + sr) * (size_t)(src_k / 16) + g];
+    }
+    dst[idx] = v;
+  }
+}
+
 // NF3 code c of checkpoint row `sr` (3-byte groups of 8 codes), 0 beyond src_k.
 __device__ __forceinline__ uint32_t nf3_code(const uint8_t* src, size_t row_base, int c,
                                              int src_k) {
@@ -303,6 +332,10 @@ cudaError_t launch_repack_w16_tiled(int kind, const void* src, void* dst, int E,
     case 3:   // NF3 scales
       repack_w16_scales_tiled_kernel<<<grid_for(tiles * kW16ScaleTile), 256, 0, st>>>(
           s8, d8, E, halves, rows, src_k, K, 32, layout);
+      break;
+    case 4:   // NVFP4 scales as W4A4 tensor-memory atoms
+      repack_nv_sf_atoms_kernel<<<grid_for(tiles * kW16ScaleTile), 256, 0, st>>>(
+          s8, d8, E, halves, rows, src_k, K, layout);
       break;
     default:
       return cudaErrorInvalidValue;

@@ -285,6 +285,41 @@ __device__ __forceinline__ void mx_roundtrip32_f16(const __nv_bfloat16* __restri
   for (int qq = 0; qq < 4; ++qq) d[qq] = make_uint4(o[4 * qq], o[4 * qq + 1], o[4 * qq + 2], o[4 * qq + 3]);
 }
 
+// NVFP4 activations (W4A4): 16 activations times the expert's activation global scale `a`
+// (fp32 products) -> block scale E4M3(vmax / 6), E2M1 codes nearest-even of v / scale (zero
+// when the scale is 0), packed two per byte (element 2i in the low nibble) into q8[0..7].
+__device__ __forceinline__ uint32_t nvfp4_quant16(const __nv_bfloat16* __restrict__ src_bf16,
+                                                  float a, uint8_t* __restrict__ q8) {
+  const uint4* src = reinterpret_cast<const uint4*>(src_bf16);
+  float v[16];
+#pragma unroll
+  for (int qq = 0; qq < 2; ++qq) {
+    const uint4 u = src[qq];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[qq * 8 + 2 * j] = __uint_as_float(w[j] << 16) * a;
+      v[qq * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u) * a;
+    }
+  }
+  float vmax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) vmax = fmaxf(vmax, fabsf(v[j]));
+  const uint32_t sc = f32_to_e4m3(__fdiv_rn(vmax, 6.f));
+  const float sv = e4m3_to_f32((uint8_t)sc);
+  uint32_t w2[2] = {0u, 0u};
+  if (sv > 0.f) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t c =
+          (uint32_t)__nv_cvt_float_to_fp4(__fdiv_rn(v[j], sv), __NV_E2M1, cudaRoundNearest) & 0xF;
+      w2[j >> 3] |= c << (4 * (j & 7));
+    }
+  }
+  *reinterpret_cast<uint2*>(q8) = make_uint2(w2[0], w2[1]);
+  return sc;
+}
+
 __device__ __forceinline__ float bf16_round(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));
 }
@@ -294,8 +329,9 @@ actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t*
             const int32_t* __restrict__ perm, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
             uint8_t* __restrict__ xs16, int r16, uint16_t* __restrict__ x16,
             const float* __restrict__ win, const float* __restrict__ ag,
-            const int32_t* __restrict__ ids, int ep_first, int E, int32_t* __restrict__ err,
-            ZeroRegion z0, ZeroRegion z1, ZeroRegion z2) {
+            const int32_t* __restrict__ ids, int ep_first, int E, uint8_t* __restrict__ xq4,
+            uint8_t* __restrict__ xs4, int32_t* __restrict__ err, ZeroRegion z0, ZeroRegion z1,
+            ZeroRegion z2) {
   pdl_wait_prev();
   pdl_launch_next();
   const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -310,6 +346,20 @@ actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t*
       const uint32_t sb =
           quantize_block32(x + (size_t)t * H + b * 32, xq + p * H + b * 32, xs + p * nb + b);
       if (xs16 != nullptr) xs16[((size_t)(b >> 2) * r16 + p) * 16 + (b & 3)] = (uint8_t)sb;
+    }
+  }
+  if (xq4 != nullptr) {
+    // NVFP4 activations (W4A4): packed codes in slot order, scales in the atom rows
+    const int nb = H / 16;
+    const size_t nblk = (size_t)ctrl[2] * nb;
+    for (size_t i = gtid; i < nblk; i += gsz) {
+      const size_t p = i / nb;
+      const int b = (int)(i % nb);
+      const int f = perm[p];
+      const int e = local_expert(ids[f], ep_first, E);
+      const uint32_t sc = nvfp4_quant16(x + (size_t)(f / topk) * H + b * 16, ag[e],
+                                        xq4 + p * (H / 2) + b * 8);
+      xs4[((size_t)(b >> 2) * r16 + p) * 16 + (b & 3)] = (uint8_t)sc;
     }
   }
   if (x16 != nullptr && ag != nullptr) {
@@ -366,7 +416,8 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
                         uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
                         uint8_t* __restrict__ xs16, int r16, uint16_t* __restrict__ x16,
                         const float* __restrict__ win, const float* __restrict__ ag,
-                        ZeroRegion z0, ZeroRegion z1, ZeroRegion z2, int ep_first) {
+                        uint8_t* __restrict__ xq4, uint8_t* __restrict__ xs4, ZeroRegion z0,
+                        ZeroRegion z1, ZeroRegion z2, int ep_first) {
   constexpr int NW = kSmallRouteThreads / 32;
   __shared__ int s_ids[kSmallRouteSlots];
   __shared__ int s_perm[kSmallRouteSlots];
@@ -455,6 +506,19 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
       const uint32_t sb =
           quantize_block32(x + (size_t)t * H + b * 32, xq + p * H + b * 32, xs + p * nb + b);
       if (xs16 != nullptr) xs16[((size_t)(b >> 2) * r16 + p) * 16 + (b & 3)] = (uint8_t)sb;
+    }
+  }
+  if (xq4 != nullptr) {
+    // NVFP4 activations (W4A4): packed codes in slot order, scales in the atom rows
+    const int nb = H / 16;
+    const size_t nblk = (size_t)total * nb;
+    for (size_t i = gtid; i < nblk; i += gsz) {
+      const size_t p = i / nb;
+      const int b = (int)(i % nb);
+      const int f = s_perm[p];
+      const uint32_t sc = nvfp4_quant16(x + (size_t)(f / topk) * H + b * 16, ag[s_ids[f]],
+                                        xq4 + p * (H / 2) + b * 8);
+      xs4[((size_t)(b >> 2) * r16 + p) * 16 + (b & 3)] = (uint8_t)sc;
     }
   }
   if (x16 != nullptr && ag != nullptr) {
@@ -727,11 +791,11 @@ bool route_actq_small_supported(int Mk, int E) {
 cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_first,
                                     int tile_slots, int max_tiles, const void* x, int H,
                                     int topk, const RunPtrs& r, bool atoms, bool to_f16,
-                                    const float* win, const float* ag, void* z0,
+                                    const float* win, const float* ag, bool nv4, void* z0,
                                     size_t z0_words, void* z1, size_t z1_words, void* z2,
                                     size_t z2_words, cudaStream_t st) {
   if (!route_actq_small_supported(Mk, E)) return cudaErrorInvalidValue;
-  const size_t work = std::max((size_t)Mk * (to_f16 ? H / 8 : H / 32),
+  const size_t work = std::max((size_t)Mk * (to_f16 ? H / 8 : (nv4 ? H / 16 : H / 32)),
                                std::max(z0_words / 4, std::max(z1_words / 4, z2_words / 4)));
   int blocks = (int)std::min<size_t>((work + kSmallRouteThreads - 1) / kSmallRouteThreads,
                                      152 * 4);
@@ -740,10 +804,12 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_fi
   return launch_kernel(route_actq_small_kernel, dim3(blocks), dim3(kSmallRouteThreads), 0, st,
                        false, ids, Mk, E, tile_slots, max_tiles,
                        reinterpret_cast<const __nv_bfloat16*>(x), H, topk, r.cnt, r.off, r.perm,
-                       r.slot_of, r.tiles, r.ctrl, to_f16 ? nullptr : r.xq,
-                       to_f16 ? nullptr : r.xs, (atoms && !to_f16) ? r.xs16 : nullptr, r.r16,
-                       to_f16 ? r.x16 : nullptr, to_f16 ? win : nullptr, to_f16 ? ag : nullptr,
-                       ZeroRegion{z0, z0_words},
+                       r.slot_of, r.tiles, r.ctrl, (to_f16 || nv4) ? nullptr : r.xq,
+                       (to_f16 || nv4) ? nullptr : r.xs,
+                       (atoms && !to_f16 && !nv4) ? r.xs16 : nullptr, r.r16,
+                       to_f16 ? r.x16 : nullptr, to_f16 ? win : nullptr,
+                       (to_f16 || nv4) ? ag : nullptr, nv4 ? r.xq : nullptr,
+                       nv4 ? r.xs16 : nullptr, ZeroRegion{z0, z0_words},
                        ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words}, ep_first);
 }
 
@@ -757,11 +823,12 @@ cudaError_t launch_route(const int32_t* ids, int Mk, int E, int ep_first, int ti
 
 cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
                         bool atoms, bool to_f16, const float* win, const float* ag,
-                        const int32_t* ids, int ep_first, int E, void* z0, size_t z0_words,
-                        void* z1, size_t z1_words, void* z2, size_t z2_words, cudaStream_t st) {
+                        const int32_t* ids, int ep_first, int E, bool nv4, void* z0,
+                        size_t z0_words, void* z1, size_t z1_words, void* z2, size_t z2_words,
+                        cudaStream_t st) {
   const size_t work = std::max(
       std::max(quant_x ? (size_t)M * topk * (H / 32) : (size_t)0,
-               to_f16 ? (size_t)M * topk * (H / 8) : (size_t)0),
+               (to_f16 || nv4) ? (size_t)M * topk * (H / 8) : (size_t)0),
       std::max(z0_words / 4, std::max(z1_words / 4, z2_words / 4)));
   int blocks = (int)std::min<size_t>((work + 255) / 256, 152 * 8);
   if (blocks < 1) blocks = 1;
@@ -770,8 +837,9 @@ cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r,
                        static_cast<const int32_t*>(r.ctrl), static_cast<const int32_t*>(r.perm),
                        quant_x ? r.xq : nullptr, quant_x ? r.xs : nullptr,
                        (quant_x && atoms) ? r.xs16 : nullptr, r.r16,
-                       to_f16 ? r.x16 : nullptr, to_f16 ? win : nullptr, to_f16 ? ag : nullptr,
-                       ids, ep_first, E, r.ctrl,
+                       to_f16 ? r.x16 : nullptr, to_f16 ? win : nullptr,
+                       (to_f16 || nv4) ? ag : nullptr, ids, ep_first, E, nv4 ? r.xq : nullptr,
+                       nv4 ? r.xs16 : nullptr, r.ctrl,
                        ZeroRegion{z0, z0_words},
                        ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words});
 }

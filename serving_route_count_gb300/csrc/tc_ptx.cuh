@@ -193,6 +193,17 @@ TC_DEV void mma_mxf8f6f4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uin
       "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[smem] x B[smem]^T with E2M1 A and B and UE4M3 block scales per 16 along K
+// from TMEM (NVFP4 x NVFP4, K = 64 per instruction: four scales per row).
+TC_DEV void mma_mxf4nvf4_4x(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                            uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
 // D[tmem] (+)= A[smem] x B[smem]^T, bf16 / fp16 operands, fp32 accumulation.
 TC_DEV void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -255,6 +266,11 @@ __host__ __device__ constexpr uint32_t idesc_mxf8f6f4(uint32_t afmt, uint32_t bf
 // Instruction descriptor of kind::f16 with bf16 A/B, fp32 D, K-major, M = 128.
 __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
+}
+// Instruction descriptor of kind::mxf4nvf4 with 4X scale vectors: A and B E2M1 (format 1 of
+// this kind), UE4M3 scales (scale-format bit 23 clear), scale ids 0, fp32 D, K-major, M = 128.
+__host__ __device__ constexpr uint32_t idesc_mxf4nvf4(uint32_t n) {
+  return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
 }
 constexpr uint32_t kFmtE4M3 = 0;
 constexpr uint32_t kFmtE2M1 = 5;

@@ -18,6 +18,7 @@ MOE_W4A16_NVFP4 = 1
 MOE_W4A16_HYBRID = 2
 MOE_W4A16_HYBRID_MX = 3
 MOE_W4A8_NVFP4 = 4
+MOE_W4A4_NVFP4 = 5
 MOE_W13_UP_GATE = 0
 MOE_W13_GATE_UP = 1
 MOE_TIER_NVFP4 = 4
@@ -205,11 +206,15 @@ def moe_debug_actq(plan, scratch, M, H, topk, stream=None):
     return xq, xs
 
 
-def moe_debug_h(plan, scratch, M, Ip, topk, a8, stream=None):
+def moe_debug_h(plan, scratch, M, Ip, topk, a8, stream=None, a4=False):
     """fc2 activation operand of the last call in slot order: (codes, scales) for W4A8,
-    (bf16 bits, None) otherwise."""
+    (packed E2M1 codes [rows][Ip/2], E4M3 scales [rows][Ip/16]) for W4A4, (f16 bits, None)
+    otherwise."""
     rows = max(1, M * topk)
-    if a8:
+    if a4:
+        hq = np.zeros((rows, Ip // 2), np.uint8)
+        hs = np.zeros((rows, Ip // 16), np.uint8)
+    elif a8:
         hq = np.zeros((rows, Ip), np.uint8)
         hs = np.zeros((rows, Ip // 32), np.uint8)
     else:
@@ -263,7 +268,7 @@ def moe_version() -> str:
 # ---------------------------------------------------------------------------------- convenience
 
 QUANT_OF = {"mxfp4": MOE_W4A8_MXFP4, "nvfp4": MOE_W4A16_NVFP4, "hybrid": MOE_W4A16_HYBRID,
-            "w4a8_nvfp4": MOE_W4A8_NVFP4}
+            "w4a8_nvfp4": MOE_W4A8_NVFP4, "w4a4_nvfp4": MOE_W4A4_NVFP4}
 
 
 def quant_mode_of(ck) -> int:
@@ -353,7 +358,7 @@ class MoELayer:
         S = int(self.routing(M, stream)[1][-1])
         Ip = (self.I + 127) // 128 * 128
         hq, hs = moe_debug_h(self.plan, self.scratch, M, Ip, self.topk,
-                             self.quant == MOE_W4A8_MXFP4, stream)
+                             self.quant == MOE_W4A8_MXFP4, stream, self.quant == MOE_W4A4_NVFP4)
         return hq[:S], (hs[:S] if hs is not None else None)
 
     def device_error(self, stream=None):

@@ -80,7 +80,7 @@ def small_cfg(quant, E=16, H=1280, I=192, topk=4, n_nvfp4=5):
     base = {"mxfp4": S.CONFIGS["tiny_w4a8"], "nvfp4": S.CONFIGS["w4a16_nvfp4"],
             "hybrid": S.CONFIGS["hybrid_nvfp4_nf3"],
             "hybrid_mx": S.CONFIGS["hybrid_mxfp4_nf3"],
-            "w4a8_nvfp4": S.CONFIGS["w4a8_nvfp4"]}[quant]
+            "w4a8_nvfp4": S.CONFIGS["w4a8_nvfp4"], "w4a4_nvfp4": S.CONFIGS["w4a4_nvfp4"]}[quant]
     d = dict(base.__dict__)
     d.update(E=E, H=H, I=I, topk=topk, n_nvfp4=min(n_nvfp4, E))
     return S.MoEConfig(**d)

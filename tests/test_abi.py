@@ -60,7 +60,7 @@ def test_plan_weights_shapes_and_sizes(lib):
     assert moe.moe_prepared_bytes(wp) == nv_bytes + 2 * 256
     moe.moe_destroy_weight_plan(wp)
     with pytest.raises(moe.MoEError) as ei:
-        moe.moe_plan_weights(4, 256, 128, 5)
+        moe.moe_plan_weights(4, 256, 128, 6)
     assert ei.value.status == 3
 
 
@@ -196,3 +196,26 @@ def test_nvfp4_a8_mode_limits(lib):
     with pytest.raises(moe.MoEError) as ei:
         moe.moe_plan(8, 256, 128, 2, 16, moe.MOE_W4A8_NVFP4, float("inf"), 0)   # Ip = 128
     assert ei.value.status == 3
+
+
+def test_w4a4_mode_limits(lib):
+    """NVFP4 weights with NVFP4 activations: the FP4 tensor-core kernels only; the prepared
+    buffer holds the NVFP4 sections (scales in the kernels' atom layout, the same size) and the
+    activation global scales."""
+    wp = moe.moe_plan_weights(4, 256, 128, moe.MOE_W4A4_NVFP4)
+    wp8 = moe.moe_plan_weights(4, 256, 128, moe.MOE_W4A8_NVFP4)
+    assert moe.moe_prepared_bytes(wp) == moe.moe_prepared_bytes(wp8)
+    moe.moe_destroy_weight_plan(wp)
+    moe.moe_destroy_weight_plan(wp8)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_plan(8, 256, 128, 2, 256, moe.MOE_W4A4_NVFP4, float("inf"), 0)   # Ip = 128
+    assert ei.value.status == 3
+    p = moe.moe_plan(8, 256, 256, 2, 256, moe.MOE_W4A4_NVFP4, float("inf"), 0)
+    assert moe.moe_call_launches(p, 16) == 4            # 32 slots: one routing launch
+    assert moe.moe_call_launches(p, 200) == 5           # 400 slots: routing, quantisation
+    for setter, arg in ((moe.moe_plan_set_backend, 1),
+                        (moe.moe_plan_set_router_weight_on_input, 1)):
+        with pytest.raises(moe.MoEError) as ei:
+            setter(p, arg)
+        assert ei.value.status == 3
+    moe.moe_destroy_plan(p)

@@ -425,6 +425,65 @@ def test_nvfp4_mxfp8_activations_full_size_sampled():
         layer.close()
 
 
+@pytest.mark.parametrize("M,det", [(5, 1), (16, 0), (40, 1), (100, 0), (300, 1)])
+def test_w4a4_nvfp4(M, det):
+    """NVFP4 weights x NVFP4 activations on the block-scaled FP4 tensor cores at every token-tile
+    width (16 / 32 / 64), split and whole-K fc1, one- and two-launch routing, both combines:
+    every row against the oracle, and fc2's operand - NVFP4 of a2 * h - scale for scale and
+    value for value, except where fp32 noise decides a near-midpoint rounding (a block whose
+    vmax / 6 sits at an E4M3 midpoint, or an element at an E2M1 midpoint)."""
+    cfg = small_cfg("w4a4_nvfp4", I=256)
+    ck = S.make_checkpoint(cfg, seed=9000 + M)
+    rng = np.random.default_rng(9001 + M)
+    x = S.make_x(rng, M, cfg.H)
+    ids = S.zipf_topk(rng, M, cfg.E, cfg.topk, 0.8)
+    ids[rng.random(ids.shape) < 0.05] = -1
+    w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 1.0)
+    layer = _layer(ck, cfg.topk, M, math.inf, det)
+    got = run_layer(layer, x, ids, w)
+    st, code = layer.device_error()
+    assert st == 0 and code == 0, code
+    hq, hs = layer.intermediate(M)
+    h = O.slot_intermediate(ck, x, ids, math.inf)
+    _, _, perm, _ = O.route(ids, cfg.E)
+    a2 = ck.a2.astype(np.float64)[ids.reshape(-1)[perm]][:, None]
+    v = (h * a2).astype(np.float32)
+    q, sc = C.nvfp4_quantize(v)
+    Ip = hq.shape[1] * 2
+    got_q = C.unpack_fp4(hq)
+    # blocks: a different scale only where vmax / 6 lies at an E4M3 rounding midpoint
+    vmax6 = np.abs(v.reshape(v.shape[0], -1, 16)).max(axis=-1) / 6.0
+    bad_s = hs[:, : sc.shape[1]] != sc
+    if bad_s.any():
+        lo = C.e4m3_decode(np.minimum(sc, hs[:, : sc.shape[1]]))
+        hi = C.e4m3_decode(np.maximum(sc, hs[:, : sc.shape[1]]))
+        mid = (lo + hi) / 2
+        assert np.all(np.abs(vmax6[bad_s] - mid[bad_s]) <= 1e-4 * vmax6[bad_s]), "scale flips"
+    same = np.repeat(~bad_s, 16, axis=1)
+    got_v = C.nvfp4_dequantize(got_q, hs)
+    want_v = C.nvfp4_dequantize(q, sc)
+    amb, alt = C.nvfp4_alternates(v.astype(np.float64), 1e-4)
+    mism = (got_v != want_v) & same
+    assert np.all(amb[mism]), "a code differs where the rounding is not decided by fp32 noise"
+    assert np.all(got_v[mism] == alt[mism])
+    assert mism.mean() < 2e-3
+    check_rows(got, ck, x, ids, w, math.inf)
+    layer.close()
+
+
+def test_w4a4_nvfp4_full_size_sampled():
+    cfg = S.CONFIGS["w4a4_nvfp4"]
+    ck = S.make_checkpoint(cfg)
+    for M, rows in ((8, [0, 3, 7]), (512, [0, 255, 511])):
+        x, ids, w = S.make_inputs(cfg, M)
+        layer = _layer(ck, cfg.topk, M, cfg.swiglu_limit, 1)
+        got = run_layer(layer, x, ids, w)
+        st, code = layer.device_error()
+        assert st == 0 and code == 0, code
+        check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=rows)
+        layer.close()
+
+
 def test_nvfp4_full_size_sampled():
     cfg = S.CONFIGS["w4a16_nvfp4"]
     ck = S.make_checkpoint(cfg)
