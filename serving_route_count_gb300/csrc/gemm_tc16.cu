@@ -264,6 +264,7 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   __shared__ int s_f[BN];          // fc2: flat slot index of each tile column
   __shared__ float s_w[BN];        // fc2: its router weight
 
+
   if (warp == 0) {
     tmem_alloc(&s_tmem, Cfg::kAlloc);
     tmem_relinquish();
@@ -416,6 +417,32 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
         tmem_ld16(trow + c0, v0);
         if (!FC2) tmem_ld16(trow + BN + c0, v1);
         if (c0 >= n) continue;
+        if (FC2) {
+          // 16 token columns x this warp's 32 output features, read back transposed so that
+          // the combine adds 16 bytes (4 features of one token) per atomic; the raw stages are
+          // free once `done` has completed (every copy landed and was consumed)
+          float(*sy)[32] = reinterpret_cast<float(*)[32]>(raw_base + quad * 2048);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) sy[jj][lane] = v0[jj] * gs;
+          __syncwarp();
+          const int h4 = rb * 128 + quad * 32 + 4 * (lane & 7);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int cc = 4 * r + (lane >> 3);
+            if (c0 + cc < n) {
+              const float4 v = *reinterpret_cast<const float4*>(&sy[cc][4 * (lane & 7)]);
+              const int f = s_f[c0 + cc];
+              const float wt = s_w[c0 + cc];
+              const float4 o = make_float4(wt * v.x, wt * v.y, wt * v.z, wt * v.w);
+              if (p.deterministic)
+                *reinterpret_cast<float4*>(p.rbuf + (size_t)f * p.H + h4) = o;
+              else
+                atomicAdd(reinterpret_cast<float4*>(p.acc + (size_t)(f / p.topk) * p.H + h4), o);
+            }
+          }
+          __syncwarp();
+          continue;
+        }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int c = c0 + j;
