@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--det", action="store_true", help="deterministic combine")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill ladder report")
+    p.add_argument("--no-modes", action="store_true",
+                   help="skip the report of the other weight / activation formats")
     p.add_argument("--profile", type=int, default=0, metavar="M",
                    help="profiling case: eager layer calls at decode size M (no timing)")
     p.add_argument("--profile-calls", type=int, default=4)
@@ -327,6 +329,76 @@ def prefill_report(stream, flush, hbm_peak):
             "fp8_dense_peak_tflops": fp8_peak, "calls": out}
 
 
+# The other weight formats (E=256, H=6144, I=512, top-8): per-expert bytes of the checkpoint
+# format each call must stream (fc1 2I x H plus fc2 H x I elements).
+MODE_CFGS = ("w4a16_nvfp4", "w4a8_nvfp4", "w4a4_nvfp4", "hybrid_nvfp4_nf3", "hybrid_mxfp4_nf3")
+MODE_M = (1, 64, 2048)
+
+
+def _mode_expert_bytes(kind, I, H):
+    n = 3 * I * H                                # elements of one expert's two matrices
+    if kind == "nf3":
+        return n * 3 // 8 + n // 32              # 3-bit codes, E4M3 per 32
+    if kind == "mxfp4":
+        return n // 2 + n // 32                  # E2M1, E8M0 per 32
+    return n // 2 + n // 16                      # NVFP4: E2M1, E4M3 per 16 (+ globals)
+
+
+def modes_report(stream, flush, hbm_peak):
+    """Secondary report: whole-call times of the other weight / activation formats at decode,
+    mid and prefill sizes (one graph replay per M after an L2 flush), with the fraction of the
+    HBM roofline over the touched experts' bytes."""
+    import torch
+    from serving_route_count_gb300 import MoELayer
+    out = {}
+    for name in MODE_CFGS:
+        cfg = S.CONFIGS[name]
+        ck = S.make_checkpoint(cfg)
+        layer = MoELayer(ck, cfg.topk, max(MODE_M), cfg.swiglu_limit, 0)
+        res = {}
+        for M in MODE_M:
+            x, ids, w = S.make_inputs(cfg, M)
+            xt = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).cuda()
+            it = torch.from_numpy(ids).cuda()
+            wt = torch.from_numpy(w).cuda()
+            ot = torch.empty((M, cfg.H), dtype=torch.bfloat16, device="cuda")
+            with torch.cuda.stream(stream):
+                layer(xt, it, wt, ot)
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    layer(xt, it, wt, ot)
+            ts = []
+            for c in range(6):
+                with torch.cuda.stream(stream):
+                    flush.fill_(c)
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    g.replay()
+                    b.record(stream)
+                stream.synchronize()
+                if c >= 2:
+                    ts.append(a.elapsed_time(b) * 1e-3)
+            sec = float(np.median(ts))
+            touched = np.unique(ids[(ids >= 0) & (ids < cfg.E)])
+            if ck.quant == "hybrid":
+                kept = "mxfp4" if ck.nv.quant == "mxfp4" else "nvfp4"
+                nbytes = sum(_mode_expert_bytes(kept if ck.tier[e] == S.TIER_NVFP4 else "nf3",
+                                                cfg.I, cfg.H) for e in touched)
+            else:
+                nbytes = len(touched) * _mode_expert_bytes("nvfp4", cfg.I, cfg.H)
+            res[str(M)] = {"us": round(sec * 1e6, 1), "tokens_per_s": round(M / sec),
+                           "hbm_frac": round(nbytes / sec / 1e9 / hbm_peak, 3)}
+        layer.close()
+        del ck
+        out[name] = res
+    return {"workload": "E=256 H=6144 I=512 top-8 (Zipf 0.8 routing for the hybrids), atomic "
+                        "combine; one graph replay per M after an L2 flush; hbm_frac over the "
+                        "touched experts' checkpoint-format bytes",
+            "calls": out}
+
+
 def our_arm(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -514,6 +586,7 @@ def our_arm(args, rank, world):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "prefill": None if args.no_prefill else prefill_report(stream, flush, peak),
+        "modes": None if args.no_modes else modes_report(stream, flush, peak),
     }
     print(json.dumps(line))
 
