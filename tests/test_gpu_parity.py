@@ -253,6 +253,9 @@ def test_prefill_ep_i1152_sampled(M, det):
     ("mxfp4", 40, 1, 0),      # CUDA-core backend: single-CTA routing kernel
     ("nvfp4", 8, 0, 0),       # one-launch routing + f16 conversion
     ("nvfp4", 100, 0, 0),     # single-CTA routing, then conversion
+    ("w4a4_nvfp4", 20, 0, 0),  # NVFP4 activations: per-slot global scales of local experts
+    ("w4a4_nvfp4", 90, 0, 0),
+    ("w4a8_nvfp4", 20, 0, 0),
 ])
 def test_expert_offset_on_device(quant, M, backend, fc1_kernel):
     """Expert parallelism on the device: a plan owning global experts [16, 32) of 48 takes
@@ -286,7 +289,7 @@ def test_expert_offset_on_device(quant, M, backend, fc1_kernel):
     layer.close()
 
 
-@pytest.mark.parametrize("quant", ["mxfp4", "nvfp4"])
+@pytest.mark.parametrize("quant", ["mxfp4", "nvfp4", "w4a4_nvfp4"])
 def test_run_chunked_above_capacity(quant):
     """M = 70 rows on a capacity-32 plan through the chunked entry point: three chunks (32, 32,
     6) in order on one scratch.  Deterministic mode: bit-identical to three separate calls, and
@@ -468,6 +471,8 @@ def test_w4a4_nvfp4(M, det):
     assert np.all(got_v[mism] == alt[mism])
     assert mism.mean() < 2e-3
     check_rows(got, ck, x, ids, w, math.inf)
+    if det:
+        assert np.array_equal(run_layer(layer, x, ids, w), got)
     layer.close()
 
 
