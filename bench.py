@@ -509,9 +509,15 @@ def our_arm(args, rank, world):
     host = []
     for mi, M in enumerate(m_list):
         c = calls[mi * N_ROUTING_SETS]
-        xh = torch.from_numpy(c["x_np"].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
-        ih = torch.from_numpy(c["ids_np"]).pin_memory()
-        wh = torch.from_numpy(c["w_np"]).pin_memory()
+        # one pinned buffer [x | ids | weights]: moe_run_host moves it up in one copy
+        xb, kb = M * cfg.H * 2, M * cfg.topk * 4
+        packed = torch.empty(xb + 2 * kb, dtype=torch.uint8).pin_memory()
+        packed[:xb].copy_(torch.from_numpy(c["x_np"].view(np.uint8).reshape(-1)))
+        packed[xb:xb + kb].copy_(torch.from_numpy(c["ids_np"].view(np.uint8).reshape(-1)))
+        packed[xb + kb:].copy_(torch.from_numpy(c["w_np"].view(np.uint8).reshape(-1)))
+        xh = packed[:xb].view(torch.bfloat16).view(M, cfg.H)
+        ih = packed[xb:xb + kb].view(torch.int32).view(M, cfg.topk)
+        wh = packed[xb + kb:].view(torch.float32).view(M, cfg.topk)
         oh = torch.empty((M, cfg.H), dtype=torch.bfloat16).pin_memory()
         host.append((xh, ih, wh, oh, c["tokens"]))
     for xh, ih, wh, oh, _ in host:   # warm-up
@@ -582,7 +588,8 @@ def our_arm(args, rank, world):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_tok / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "api": "moe_run_host (pinned host buffers, H2D + run + D2H + sync)"},
+                "api": "moe_run_host (one pinned host buffer [x | ids | weights], one H2D copy "
+                       "+ run + D2H + sync)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "prefill": None if args.no_prefill else prefill_report(stream, flush, peak),

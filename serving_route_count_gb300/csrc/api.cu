@@ -699,15 +699,31 @@ moe_status moe_run_host(const moe_plan_t* plan, const moe_prepared* weights, voi
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* b = static_cast<uint8_t*>(io);
   const size_t xb = (size_t)M * plan->d.H * 2, kb = (size_t)M * plan->d.topk * 4;
-  cudaError_t e = cudaMemcpyAsync(b + plan->io_x, x_host, xb, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(b + plan->io_ids, ids_host, kb, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(b + plan->io_w, w_host, kb, cudaMemcpyHostToDevice, st);
+  const uint8_t* xh = static_cast<const uint8_t*>(x_host);
+  cudaError_t e = cudaSuccess;
+  const uint8_t *dx, *dids, *dw;
+  if (reinterpret_cast<const uint8_t*>(ids_host) == xh + xb &&
+      reinterpret_cast<const uint8_t*>(w_host) == xh + xb + kb) {
+    // [x | ids | w] in one host buffer: one copy, the same packing on the device (x rows are
+    // multiples of 16 bytes, so ids and weights stay aligned)
+    e = cudaMemcpyAsync(b + plan->io_x, x_host, xb + 2 * kb, cudaMemcpyHostToDevice, st);
+    dx = b + plan->io_x;
+    dids = dx + xb;
+    dw = dids + kb;
+  } else {
+    e = cudaMemcpyAsync(b + plan->io_x, x_host, xb, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(b + plan->io_ids, ids_host, kb, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(b + plan->io_w, w_host, kb, cudaMemcpyHostToDevice, st);
+    dx = b + plan->io_x;
+    dids = b + plan->io_ids;
+    dw = b + plan->io_w;
+  }
   if (e != cudaSuccess) return cuda_status(e);
-  moe_status s = moe_run(plan, weights, scratch, scratch_bytes, b + plan->io_x,
-                         reinterpret_cast<const int32_t*>(b + plan->io_ids),
-                         reinterpret_cast<const float*>(b + plan->io_w), b + plan->io_out, M,
-                         stream);
+  moe_status s = moe_run(plan, weights, scratch, scratch_bytes, dx,
+                         reinterpret_cast<const int32_t*>(dids),
+                         reinterpret_cast<const float*>(dw), b + plan->io_out, M, stream);
   if (s != MOE_OK) return s;
   e = cudaMemcpyAsync(out_host, b + plan->io_out, xb, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);

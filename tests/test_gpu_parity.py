@@ -489,6 +489,34 @@ def test_w4a4_nvfp4_full_size_sampled():
         layer.close()
 
 
+def test_run_host_packed_inputs():
+    """moe_run_host with [x | ids | weights] back to back in one pinned buffer (one copy up)
+    gives the same bits as with three separate host buffers (deterministic combine)."""
+    cfg = small_cfg("mxfp4")
+    ck = S.make_checkpoint(cfg, seed=9100)
+    rng = np.random.default_rng(9101)
+    layer = _layer(ck, cfg.topk, 32, 7.0, 1)
+    for M in (3, 32):
+        x = S.make_x(rng, M, cfg.H)
+        ids = S.uniform_topk(rng, M, cfg.E, cfg.topk)
+        w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 2.5)
+        xb, kb = M * cfg.H * 2, M * cfg.topk * 4
+        packed = torch.empty(xb + 2 * kb, dtype=torch.uint8).pin_memory()
+        packed[:xb].copy_(torch.from_numpy(x.view(np.uint8).reshape(-1)))
+        packed[xb:xb + kb].copy_(torch.from_numpy(ids.view(np.uint8).reshape(-1)))
+        packed[xb + kb:].copy_(torch.from_numpy(w.view(np.uint8).reshape(-1)))
+        o1 = torch.empty((M, cfg.H), dtype=torch.bfloat16).pin_memory()
+        layer.run_host(packed[:xb].view(torch.bfloat16).view(M, cfg.H),
+                       packed[xb:xb + kb].view(torch.int32).view(M, cfg.topk),
+                       packed[xb + kb:].view(torch.float32).view(M, cfg.topk), o1)
+        o2 = torch.empty((M, cfg.H), dtype=torch.bfloat16).pin_memory()
+        layer.run_host(torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).pin_memory(),
+                       torch.from_numpy(ids).pin_memory(), torch.from_numpy(w).pin_memory(), o2)
+        assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+        check_rows(out_bits(o1), ck, x, ids, w, 7.0)
+    layer.close()
+
+
 def test_nvfp4_full_size_sampled():
     cfg = S.CONFIGS["w4a16_nvfp4"]
     ck = S.make_checkpoint(cfg)
