@@ -260,6 +260,16 @@ moe_status moe_run_host(const moe_plan_t* plan, const moe_prepared* weights, voi
                         const int32_t* ids_host, const float* w_host, void* out_host, int M,
                         void* stream);
 
+/* Test hook: the inverse of moe_prepare_weights, on the host.  Copies the prepared buffer of `w`
+ * back (synchronises `stream`) and writes the checkpoint-layout tensors of the plan's mode into
+ * the HOST buffers named by `dst` (the moe_checkpoint fields and shapes; the pointers are
+ * written through): codes (E2M1 nibbles after the -0 -> +0 rewrite), block scales, NF3 codes
+ * and scales, the NVFP4 globals and activation global scales where the mode has them (g13 /
+ * g2 are not written for the MXFP4 kept tier, whose checkpoint has none; a kept-tier scale
+ * that prepare flushed comes back as 0).  Errors: MOE_ERR_ARG, MOE_ERR_CUDA. */
+moe_status moe_unprepare_weights(const moe_weight_plan* wp, const moe_prepared* w, void* stream,
+                                 const moe_checkpoint* dst);
+
 /* Reads and clears the device error word kept in `scratch` (synchronises `stream`).
  * *code = 0 when no device-side check failed since the last read. */
 moe_status moe_get_device_error(const moe_plan_t* plan, void* scratch, void* stream, int* code);

@@ -44,6 +44,7 @@ SIGNATURES = {
     "moe_plan_set_router_weight_on_input": (c_int, [c_void_p, c_int]),
     "moe_run": (c_int, [c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p, c_void_p,
                         c_void_p, c_int, c_void_p]),
+    "moe_unprepare_weights": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p]),
     "moe_run_chunked": (c_int, [c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p,
                                 c_void_p, c_void_p, c_int, c_void_p]),
     "moe_run_static_scratch": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,

@@ -822,6 +822,155 @@ moe_status moe_debug_h(const moe_plan_t* plan, void* scratch, int M, void* hq, u
   return cuda_status(e);
 }
 
+// ------------------------------------------------------------------ test hook: unprepare
+// The inverse of the repack kernels of prepare.cu, on the host: each checkpoint byte is read back
+// from its prepared position (through the same layout helpers), so a test can compare the
+// device layout with the checkpoint byte for byte.
+namespace {
+struct Unprep {
+  const std::vector<uint8_t>& P;
+  const moe_weight_plan* wp;
+  // checkpoint row of prepared fc1 matrix half `half`, row i
+  int src_row(int half, int i) const { return (wp->layout == 0 ? half : 1 - half) * wp->I + i; }
+};
+// E4M3 scale code of a 16-group of an NVFP4 W4A4 4X atom tile
+size_t atom4x_off(size_t mat, int r, int k, int rbs, int kts) {
+  const int kk = k & 255, rr = r & 127;
+  return w16_tile(mat, r >> 7, k >> 8, rbs, kts) * kW16ScaleTile + (size_t)(kk >> 6) * 512 +
+         (size_t)((rr & 31) * 16 + (rr >> 5) * 4 + ((kk & 63) >> 4));
+}
+// UE8M0 byte of an MXFP4 kept-tier group from its f16 multiplier 2^(b - kmax + 13)
+uint8_t mx_byte_of(uint16_t bits, int kmax) {
+  if (bits == 0x7E00) return 0xFF;
+  if (bits == 0) return 0;                                  // flushed group
+  int j;
+  if (bits >= 0x400) {
+    j = (bits >> 10) - 15;
+  } else {
+    j = -24;
+    for (uint16_t m = bits; m > 1; m >>= 1) ++j;
+  }
+  return (uint8_t)(j + kmax - 13);
+}
+}  // namespace
+
+moe_status moe_unprepare_weights(const moe_weight_plan* wp, const moe_prepared* prepared,
+                                  void* stream, const moe_checkpoint* dst) {
+  if (wp == nullptr || prepared == nullptr || dst == nullptr) return MOE_ERR_ARG;
+  const DevWeights& w = prepared->w;
+  if (w.E != wp->E || w.H != wp->H || w.I != wp->I || w.quant != wp->quant) return MOE_ERR_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  std::vector<uint8_t> P(wp->total);
+  cudaError_t e = cudaMemcpyAsync(P.data(), w.w13 - wp->w13, wp->total, cudaMemcpyDeviceToHost,
+                                  st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_status(e);
+  const int E4 = wp->E4, E3 = wp->E3, H = wp->H, I = wp->I, Ip = wp->Ip, q = wp->quant;
+  const Unprep u{P, wp};
+  auto out8 = [](const void* p) { return static_cast<uint8_t*>(const_cast<void*>(p)); };
+  const uint8_t* b = P.data();
+  const int rb1 = cdiv(I, 128), kt1 = cdiv(H, 256), rb2 = H / 128, kt2 = cdiv(Ip, 256);
+  if (E4 > 0 && (dst->w13 == nullptr || dst->s13 == nullptr || dst->w2 == nullptr ||
+                 dst->s2 == nullptr))
+    return MOE_ERR_ARG;
+  if (E3 > 0 && (dst->nf_w13 == nullptr || dst->nf_s13 == nullptr || dst->nf_w2 == nullptr ||
+                 dst->nf_s2 == nullptr))
+    return MOE_ERR_ARG;
+  uint8_t *w13 = out8(dst->w13), *s13 = out8(dst->s13), *w2 = out8(dst->w2), *s2 = out8(dst->s2);
+  if (q == MOE_W4A8_MXFP4) {
+    for (int ex = 0; ex < E4; ++ex) {
+      for (int half = 0; half < 2; ++half)
+        for (int i = 0; i < I; ++i) {
+          const size_t sr = (size_t)ex * 2 * I + u.src_row(half, i), mat = (size_t)ex * 2 + half;
+          for (int c = 0; c < H / 2; ++c)
+            w13[sr * (H / 2) + c] = b[wp->w13 + fp4_tiled_byte((size_t)E4 * 2, I, H, mat, i, 2 * c)];
+          for (int kb = 0; kb < H / 32; ++kb)
+            s13[sr * (H / 32) + kb] = b[wp->s13 + sf_atom_byte(rb1, H / 128, mat, i, kb)];
+        }
+      for (int r = 0; r < H; ++r) {
+        const size_t sr = (size_t)ex * H + r;
+        for (int c = 0; c < I / 2; ++c)
+          w2[sr * (I / 2) + c] = b[wp->w2 + fp4_tiled_byte((size_t)E4, H, Ip, ex, r, 2 * c)];
+        for (int kb = 0; kb < I / 32; ++kb)
+          s2[sr * (I / 32) + kb] = b[wp->s2 + sf_atom_byte(H / 128, Ip / 128, ex, r, kb)];
+      }
+    }
+  } else if (E4 > 0) {
+    // NVFP4 (16-bit, MXFP8-activation and W4A4 modes) or the MXFP4 kept tier
+    const bool mx = q == MOE_W4A16_HYBRID_MX, a4x = q == MOE_W4A4_NVFP4;
+    const int g = mx ? 32 : 16;
+    auto scale = [&](size_t sec, size_t ksec, size_t mat, int r, int k, int rbs, int kts,
+                     int ex) -> uint8_t {
+      if (a4x) return b[sec + atom4x_off(mat, r, k, rbs, kts)];
+      if (!mx) return b[sec + nv_scale_byte(mat, r, k, rbs, kts)];
+      uint16_t bits;
+      std::memcpy(&bits, &b[sec + mx16_scale_off(mat, r, k, rbs, kts)], 2);
+      int32_t kmax;
+      std::memcpy(&kmax, &b[ksec + (size_t)ex * 4], 4);
+      return mx_byte_of(bits, kmax);
+    };
+    for (int ex = 0; ex < E4; ++ex) {
+      for (int half = 0; half < 2; ++half)
+        for (int i = 0; i < I; ++i) {
+          const size_t sr = (size_t)ex * 2 * I + u.src_row(half, i), mat = (size_t)ex * 2 + half;
+          for (int k = 0; k < H; k += 2)
+            w13[sr * (H / 2) + k / 2] = b[wp->w13 + nv_code_byte(mat, i, k, rb1, kt1)];
+          for (int k = 0; k < H; k += g)
+            s13[sr * (H / g) + k / g] = scale(wp->s13, wp->mxk13, mat, i, k, rb1, kt1, ex);
+        }
+      for (int r = 0; r < H; ++r) {
+        const size_t sr = (size_t)ex * H + r;
+        for (int k = 0; k < I; k += 2)
+          w2[sr * (I / 2) + k / 2] = b[wp->w2 + nv_code_byte(ex, r, k, rb2, kt2)];
+        for (int k = 0; k < I; k += g)
+          s2[sr * (I / g) + k / g] = scale(wp->s2, wp->mxk2, ex, r, k, rb2, kt2, ex);
+      }
+    }
+    if (!mx && dst->g13 != nullptr && dst->g2 != nullptr) {
+      std::memcpy(const_cast<float*>(dst->g13), &b[wp->g13], (size_t)E4 * 4);
+      std::memcpy(const_cast<float*>(dst->g2), &b[wp->g2], (size_t)E4 * 4);
+    }
+    if (wp->ag13 != 0 && dst->a1_gscale != nullptr && dst->a2_gscale != nullptr) {
+      std::memcpy(const_cast<float*>(dst->a1_gscale), &b[wp->ag13], (size_t)E4 * 4);
+      std::memcpy(const_cast<float*>(dst->a2_gscale), &b[wp->ag2], (size_t)E4 * 4);
+    }
+  }
+  if (E3 > 0) {
+    uint8_t *nw13 = out8(dst->nf_w13), *ns13 = out8(dst->nf_s13), *nw2 = out8(dst->nf_w2),
+            *ns2 = out8(dst->nf_s2);
+    auto code = [&](size_t sec, size_t mat, int r, int k, int rbs, int kts) -> uint32_t {
+      const uint32_t lo = (b[sec + nf_lo_byte(mat, r, k, rbs, kts)] >> (2 * (k & 3))) & 3u;
+      const uint32_t hi = (b[sec + nf_hi_byte(mat, r, k, rbs, kts)] >> (k & 7)) & 1u;
+      return lo | (hi << 2);
+    };
+    auto row_codes = [&](uint8_t* dstrow, size_t sec, size_t mat, int r, int K, int rbs, int kts) {
+      for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t w24 = 0;
+        for (int t = 0; t < 8; ++t) w24 |= code(sec, mat, r, k0 + t, rbs, kts) << (3 * t);
+        dstrow[3 * (k0 / 8) + 0] = (uint8_t)(w24 & 0xFF);
+        dstrow[3 * (k0 / 8) + 1] = (uint8_t)((w24 >> 8) & 0xFF);
+        dstrow[3 * (k0 / 8) + 2] = (uint8_t)(w24 >> 16);
+      }
+    };
+    for (int ex = 0; ex < E3; ++ex) {
+      for (int half = 0; half < 2; ++half)
+        for (int i = 0; i < I; ++i) {
+          const size_t sr = (size_t)ex * 2 * I + u.src_row(half, i), mat = (size_t)ex * 2 + half;
+          row_codes(nw13 + sr * (3 * H / 8), wp->nf_w13, mat, i, H, rb1, kt1);
+          for (int k = 0; k < H; k += 32)
+            ns13[sr * (H / 32) + k / 32] = b[wp->nf_s13 + nf_scale_byte(mat, i, k, rb1, kt1)];
+        }
+      for (int r = 0; r < H; ++r) {
+        const size_t sr = (size_t)ex * H + r;
+        row_codes(nw2 + sr * (3 * I / 8), wp->nf_w2, ex, r, I, rb2, kt2);
+        for (int k = 0; k < I; k += 32)
+          ns2[sr * (I / 32) + k / 32] = b[wp->nf_s2 + nf_scale_byte(ex, r, k, rb2, kt2)];
+      }
+    }
+  }
+  return MOE_OK;
+}
+
 void moe_destroy_weight_plan(moe_weight_plan* wp) { delete wp; }
 void moe_destroy_prepared(moe_prepared* p) { delete p; }
 void moe_destroy_plan(moe_plan_t* plan) { delete plan; }

@@ -96,6 +96,18 @@ def moe_prepare_weights(wp, ckpt: dict, dst: torch.Tensor, stream=None) -> int:
     return out.value
 
 
+def moe_unprepare_weights(wp, prepared, like: dict, stream=None) -> dict:
+    """Test hook: checkpoint-layout host arrays of prepared weights.  ``like`` maps the
+    moe_checkpoint field names to numpy arrays giving each output's shape and dtype (missing
+    fields stay NULL)."""
+    out = {k: np.zeros_like(v) for k, v in like.items() if v is not None}
+    c = _lib.MoeCheckpoint(*[(out[f].ctypes.data if f in out else None)
+                             for f, _ in _lib.MoeCheckpoint._fields_])
+    _check(_lib.load().moe_unprepare_weights(_handle(wp), _handle(prepared), _stream(stream),
+                                             ctypes.byref(c)), "moe_unprepare_weights")
+    return out
+
+
 def moe_plan(E, H, I, topk, max_m, quant_mode, swiglu_limit=float("inf"), deterministic=0) -> int:
     out = ctypes.c_void_p()
     _check(_lib.load().moe_plan(E, H, I, topk, max_m, quant_mode, float(swiglu_limit),

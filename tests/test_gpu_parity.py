@@ -517,6 +517,44 @@ def test_run_host_packed_inputs():
     layer.close()
 
 
+def _canon_fp4(a):
+    lo, hi = a & 0x0F, a >> 4
+    lo = np.where(lo == 8, 0, lo)
+    hi = np.where(hi == 8, 0, hi)
+    return (lo | (hi << 4)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("quant,layout", [("mxfp4", 0), ("mxfp4", 1), ("nvfp4", 1), ("hybrid", 0),
+                                          ("hybrid_mx", 1), ("w4a8_nvfp4", 0),
+                                          ("w4a4_nvfp4", 0)])
+def test_prepare_roundtrip(quant, layout):
+    """The prepared device layout holds every checkpoint byte: read back through the inverse
+    permutation (moe_unprepare_weights) it equals the checkpoint - E2M1 nibbles after the
+    -0 -> +0 rewrite, scales, NF3 planes, globals and activation global scales - for both w13
+    stackings and every format."""
+    from serving_route_count_gb300 import moe_unprepare_weights
+    cfg = small_cfg(quant)
+    ck = S.make_checkpoint(cfg, seed=9200, layout=layout)
+    if ck.quant == "hybrid":
+        nv, nf = ck.nv, ck.nf
+        want = {"w13": nv.w13, "s13": nv.s13, "w2": nv.w2, "s2": nv.s2, "nf_w13": nf.w13,
+                "nf_s13": nf.s13, "nf_w2": nf.w2, "nf_s2": nf.s2}
+        if nv.quant == "nvfp4":
+            want.update(g13=nv.g13, g2=nv.g2)
+    else:
+        want = {"w13": ck.w13, "s13": ck.s13, "w2": ck.w2, "s2": ck.s2}
+        if ck.g13 is not None:
+            want.update(g13=ck.g13, g2=ck.g2)
+        if ck.a13 is not None:
+            want.update(a1_gscale=ck.a13, a2_gscale=ck.a2)
+    layer = _layer(ck, cfg.topk, 4, math.inf, 0)
+    got = moe_unprepare_weights(layer.wp, layer.prep, want)
+    for k, v in want.items():
+        exp = _canon_fp4(v) if k in ("w13", "w2") else v
+        assert np.array_equal(got[k], exp), k
+    layer.close()
+
+
 def test_nvfp4_full_size_sampled():
     cfg = S.CONFIGS["w4a16_nvfp4"]
     ck = S.make_checkpoint(cfg)
