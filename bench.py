@@ -94,7 +94,7 @@ def cpu_baseline_worker(args):
     print(json.dumps({"tokens": tok, "seconds": sec}))
 
 
-def run_cpu_baseline(m_list="1,2"):
+def run_cpu_baseline(m_list="1,2,3,4,5,6,7,8,10,12,14,16"):
     # the oracle as it stands: numpy fp64 with its default BLAS threading (all host cores)
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-worker",
                         "--sample-m", m_list], capture_output=True, text=True, timeout=900)
