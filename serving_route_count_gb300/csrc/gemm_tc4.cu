@@ -24,6 +24,7 @@
 
 #include "moe_common.cuh"
 #include "tc_ptx.cuh"
+#include "tc_sched.cuh"
 #include "tc_tile.cuh"
 
 namespace moe {
@@ -329,6 +330,198 @@ gemm_tc4_kernel(const __grid_constant__ Tc4Params p) {
   }
 }
 
+// Persistent fc2 for decode and mid sizes (tile widths 16 and 32): each CTA takes a contiguous
+// range of (tile, 128-row block) units and streams their weight stages through one 4-stage
+// ring, so the loads of the next unit overlap the MMAs and the combine of the current one;
+// the accumulators are double-buffered in tensor memory.  Warp 0 lane 0 loads, warp 1 lane 0
+// issues, warps 4..7 run the combine (16-byte atomics after a transpose in shared memory).
+constexpr int k4PThreads = 256;
+
+template <int BN>
+struct Tc4PersistCfg {
+  using Base = Tc4Cfg<BN, true>;
+  static constexpr int kStages = 4;
+  static constexpr int kStage = Base::kStage;
+  static constexpr int kCols = 2 * BN + Base::kSfCols * kStages;   // 2 accumulators + scales
+  static constexpr int kAlloc = kCols <= 64 ? 64 : kCols <= 128 ? 128 : 256;
+  static_assert(kCols <= 256, "two CTAs per SM: at most 256 tensor-memory columns each");
+  static_assert(BN == 16 || BN == 32, "persistent W4A4 fc2 tile widths");
+  static constexpr int kSmem = kStages * kStage + 1024;
+};
+
+template <int BN>
+__global__ void __launch_bounds__(k4PThreads)
+fc2_tc4_persist_kernel(const __grid_constant__ Tc4Params p) {
+  using Cfg = Tc4PersistCfg<BN>;
+  using B = typename Cfg::Base;
+  constexpr int S = Cfg::kStages;
+  pdl_wait_prev();             // fc1 complete, h and its scales visible
+  pdl_launch_next();
+  const int G = gridDim.x, c = blockIdx.x;
+  const int units = p.ctrl[1] * p.RB;
+  const int u_begin = (int)((long long)c * units / G);
+  const int u_end = (int)((long long)(c + 1) * units / G);
+  if (u_begin >= u_end) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full[S], empty[S], acc_full[2], acc_empty[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_fail;
+  __shared__ int s_f[BN];
+  __shared__ float s_w[BN];
+  __shared__ __align__(16) float s_y[4][16][32];
+
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, Cfg::kAlloc);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    s_fail = 0;
+    fence_barrier_init();
+  }
+  if (tid == 64) prefetch_tmap(&p.tm_act);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  bool ok = true;
+  int issued = 0;
+  auto stage = [&](int s) { return smem + s * Cfg::kStage; };
+  constexpr int kAtomRows = BN < 32 ? BN : 32;
+  constexpr uint32_t kTx = k4TileA + k4SfTile + B::kB + 4 * kAtomRows * 16;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
+      int i = 0;
+      for (int u = u_begin; u < u_end && ok; ++u) {
+        const int tile = u / p.RB, rb = u - tile * p.RB;
+        const int4 td = p.tiles[tile];
+        for (int kt = 0; kt < p.KT && ok; ++kt, ++i) {
+          const int s = i % S;
+          if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
+          if (!ok) break;
+          uint8_t* st = stage(s);
+          const size_t t = w16_tile((size_t)td.x, rb, kt, p.RB, p.KT);
+          mbar_arrive_expect_tx(&full[s], kTx);
+          bulk_load_hint(st, p.codes + t * k4TileA, k4TileA, &full[s], pol);
+          bulk_load_hint(st + B::kOffSfa, p.sfa + t * k4SfTile, k4SfTile, &full[s], pol);
+          tma_load_2d(st + B::kOffB, &p.tm_act, kt * 128, td.y, &full[s]);
+          for (int kb = 0; kb < 4; ++kb)
+            bulk_load(st + B::kOffSfb + 512 * kb,
+                      p.sfb + ((size_t)(kt * 4 + kb) * p.r16 + td.y) * 16, kAtomRows * 16,
+                      &full[s]);
+        }
+      }
+      issued = i;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_mxf4nvf4(B::kWidth);
+      int i = 0, j = 0;
+      for (int u = u_begin; u < u_end && ok; ++u, ++j) {
+        const int b = j & 1;
+        if (j >= 2) ok = mbar_wait(&acc_empty[b], ((j >> 1) - 1) & 1, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem + b * BN;
+        for (int kt = 0; kt < p.KT && ok; ++kt, ++i) {
+          const int s = i % S;
+          ok = mbar_wait(&full[s], (i / S) & 1, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          uint8_t* st = stage(s);
+          const uint32_t sfa = tmem + 2 * BN + B::kSfCols * s;
+          const uint32_t sfb = sfa + 16;
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb) {
+            tc_cp_sf(sfa + kb * 4, desc_sf(st + B::kOffSfa + 512 * kb));
+            tc_cp_sf(sfb + kb * 4, desc_sf(st + B::kOffSfb + 512 * kb));
+          }
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb)
+            mma_mxf4nvf4_4x(d, desc_sw128(st + 32 * kb), desc_sw128(st + B::kOffB + 32 * kb),
+                            idesc, sfa + kb * 4, sfb + kb * 4, (kt > 0 || kb > 0) ? 1u : 0u);
+          tc_commit(&empty[s]);
+        }
+        tc_commit(&acc_full[b]);
+      }
+    }
+  } else if (warp >= 4) {
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;                  // row of the 128-row block
+    float(*sy)[32] = s_y[quad];
+    int j = 0, cur_tile = -1, n = 0;
+    float gs = 0.f;
+    for (int u = u_begin; u < u_end; ++u, ++j) {
+      const int tile = u / p.RB, rb = u - tile * p.RB;
+      if (tile != cur_tile) {
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        const int4 td = p.tiles[tile];
+        n = td.z;
+        gs = p.gscale[td.x] / p.agscale[td.x];
+        if (row < n) {
+          const int f = p.perm[td.y + row];
+          s_f[row] = f;
+          s_w[row] = p.topk_w[f];
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        cur_tile = tile;
+      }
+      const int h4 = rb * 128 + quad * 32 + 4 * (lane & 7);
+      const int b = j & 1;
+      ok = ok && mbar_wait(&acc_full[b], (j >> 1) & 1, p.err);
+      tc_fence_after();
+      __syncwarp();
+      const uint32_t trow = tmem + b * BN + ((uint32_t)(quad * 32) << 16);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float y[16];
+        tmem_ld16(trow + c0, y);
+        if (!ok || c0 >= n) continue;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) sy[jj][lane] = y[jj] * gs;
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int cc = 4 * r + (lane >> 3);
+          if (c0 + cc < n) {
+            const float4 v = *reinterpret_cast<const float4*>(&sy[cc][4 * (lane & 7)]);
+            const int f = s_f[c0 + cc];
+            const float wt = s_w[c0 + cc];
+            const float4 o = make_float4(wt * v.x, wt * v.y, wt * v.z, wt * v.w);
+            if (p.deterministic)
+              *reinterpret_cast<float4*>(p.rbuf + (size_t)f * p.H + h4) = o;
+            else
+              atomicAdd(reinterpret_cast<float4*>(p.acc + (size_t)(f / p.topk) * p.H + h4), o);
+          }
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+    }
+  }
+  if (!ok) s_fail = 1;
+  tc_fence_before();
+  __syncthreads();
+  // a wait gave up: let this CTA's copies land before its shared memory is released
+  if (s_fail && warp == 0 && lane == 0) drain_stage_loads<S>(full, issued, p.err);
+  if (warp == 0) tmem_dealloc(tmem, Cfg::kAlloc);
+}
+
 // ---------------------------------------------------------------------------------- host side
 
 EncodeTiledFn tc_encode_fn();
@@ -363,6 +556,16 @@ static cudaError_t launch4(const Tc4Params& p, int tiles, cudaStream_t st) {
                        p);
 }
 
+template <int BN>
+static cudaError_t launch4_persist(const Tc4Params& p, int tiles, cudaStream_t st) {
+  using Cfg = Tc4PersistCfg<BN>;
+  static const int G = persistent_grid(fc2_tc4_persist_kernel<BN>, Cfg::kSmem, Cfg::kAlloc, 2,
+                                       1 << 20);
+  const int grid = std::max(1, std::min(G, tiles * p.RB));
+  return launch_kernel(fc2_tc4_persist_kernel<BN>, dim3(grid), dim3(k4PThreads), Cfg::kSmem, st,
+                       true, p);
+}
+
 // Token-tile width of the W4A4 kernels.
 int tc4_pick_bn(int M) { return M <= 16 ? 16 : (M <= 64 ? 32 : 64); }
 
@@ -395,9 +598,9 @@ cudaError_t launch_tc4_stage(int stage, const DevWeights& w, const RunPtrs& r, c
   p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
   switch (bn * 2 + (fc2 ? 1 : 0)) {
     case 32: return launch4<16, false>(p, tiles, st);
-    case 33: return launch4<16, true>(p, tiles, st);
+    case 33: return launch4_persist<16>(p, tiles, st);
     case 64: return launch4<32, false>(p, tiles, st);
-    case 65: return launch4<32, true>(p, tiles, st);
+    case 65: return launch4_persist<32>(p, tiles, st);
     case 128: return launch4<64, false>(p, tiles, st);
     case 129: return launch4<64, true>(p, tiles, st);
     default: return cudaErrorInvalidValue;
