@@ -219,3 +219,16 @@ def test_w4a4_mode_limits(lib):
             setter(p, arg)
         assert ei.value.status == 3
     moe.moe_destroy_plan(p)
+
+
+def test_binding_constants_match_header(lib):
+    """The binding's enum constants and the checkpoint struct follow include/moe_gb300.h."""
+    import os
+    import re
+    from serving_route_count_gb300 import _lib
+    hdr = open(os.path.join(os.path.dirname(__file__), "..", "include", "moe_gb300.h")).read()
+    for name, val in re.findall(r"\b(MOE_W4A\w+|MOE_W13_\w+)\s*=\s*(\d+)", hdr):
+        assert getattr(moe, name) == int(val), name
+    body = re.search(r"typedef struct \{(.*?)\} moe_checkpoint;", hdr, re.S).group(1)
+    fields = re.findall(r"\*\s*(\w+);", re.sub(r"/\*.*?\*/", "", body, flags=re.S))
+    assert fields == [f for f, _ in _lib.MoeCheckpoint._fields_]
