@@ -325,11 +325,14 @@ def requant_alternatives(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0
 
 
 def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.0,
-                           weight_on_input=False):
+                           weight_on_input=False, fc2_override=None, return_f64=False):
     """Token by token, slot by slot, element by element (pure Python loops; tiny inputs only).
     Dequantises each weight element from its own code and scale with scalar decoders.
     ``weight_on_input``: each input element becomes the bf16 rounding of x * bf16(w) and the
-    slot's output is added unweighted."""
+    slot's output is added unweighted.  ``fc2_override`` ({(t, j): {i: value}}) replaces
+    element i of slot (t, j)'s fc2 operand (the dequantised intermediate) by the given value, so
+    a test can take one rounding decision the other way.  Returns bf16 bit patterns (and the
+    unrounded fp64 sums when ``return_f64``)."""
     ids = np.asarray(topk_ids).tolist()
     w = np.asarray(topk_w, dtype=np.float64).tolist()
     M = len(ids)
@@ -399,12 +402,17 @@ def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1
                 h[i] = g * (1.0 / (1.0 + math.exp(-alpha * g))) * (u + beta)
             hh = (nvfp4_act(np.array(h)[None, :], a2[e])[0] if activation_nv4(ck) else
                   requant_h(np.array(h), a8, None if a2 is None else a2[e])).tolist()
+            for i, v in ((fc2_override or {}).get((t, j)) or {}).items():
+                hh[i] = float(v)
             for r in range(H):
                 s = 0.0
                 for i in range(I):
                     s += weight("w2", e, r, i) * hh[i]
                 out[t][r] += cw * s
-    return C.f64_to_bf16_bits(np.array(out))
+    bits = C.f64_to_bf16_bits(np.array(out))
+    if return_f64:
+        return bits, np.array(out)
+    return bits
 
 
 # ---------------------------------------------------------------------------- bounds

@@ -264,20 +264,23 @@ def router_weights(rng, M: int, k: int, rule: str, mult: float) -> np.ndarray:
 
 
 def ep_mask_foreign(ids_global: np.ndarray, w: np.ndarray, offset: int, num_local: int):
-    """Global ids -> local ids of one EP rank, following the adapter's ``ep_remap_reference``:
-    foreign and padding slots get weight 0 and point at the row's lowest local expert, else the
-    batch's lowest local expert, else 0."""
-    lid = ids_global.astype(np.int64) - offset
-    ok = (lid >= 0) & (lid < num_local)
-    big = np.int64(2**31 - 1)
-    masked = np.where(ok, lid, big)
-    best = masked.min() if masked.size else big
-    fb = best if best < num_local else 0
-    row_min = masked.min(axis=1) if masked.size else np.zeros(0, np.int64)
-    fill = np.where(row_min < num_local, row_min, fb)
-    ids = np.where(ok, lid, fill[:, None]).astype(np.int32)
-    wl = np.where(ok, w, 0.0).astype(np.float32)
-    return ids, wl
+    """Router output of the whole model -> router output one expert-parallel rank sees.
+
+    The rank owns the global experts [offset, offset + num_local).  An owned slot keeps its
+    weight and becomes local id (global - offset).  Every other slot - another rank's expert or
+    a padding id - gets weight 0 and a stand-in local id: the smallest owned local id in its
+    own row; if the row owns none, the smallest owned local id anywhere in the batch; if the
+    batch owns none, 0.  (The EP adapter's remap rule, moe_b12x_next.py ``ep_remap``.)"""
+    gid = np.asarray(ids_global, dtype=np.int64)
+    local = gid - offset
+    owned = (local >= 0) & (local < num_local)
+    batch_lowest = int(local[owned].min()) if owned.any() else 0
+    ids = np.empty(gid.shape, dtype=np.int32)
+    for t in range(gid.shape[0]):
+        mine = local[t][owned[t]]
+        stand_in = int(mine.min()) if mine.size else batch_lowest
+        ids[t] = np.where(owned[t], local[t], stand_in)
+    return ids, np.where(owned, np.asarray(w, dtype=np.float32), np.float32(0)).astype(np.float32)
 
 
 def make_routing(cfg: MoEConfig, M: int, seed: Optional[int] = None, E: Optional[int] = None):

@@ -452,3 +452,187 @@ def test_slot_intermediate_matches_direct_dot_products():
         g = min(gate, 7.0)
         u = max(-7.0, min(up, 7.0))
         assert h[p, 0] == pytest.approx(g / (1 + math.exp(-g)) * u, rel=1e-12, abs=1e-12)
+
+
+# ---------------------------------------------------------------------------- acceptance helpers
+
+def _other_neighbour(v, grid):
+    """The two entries of the sorted non-negative grid that bracket |v| (lo <= |v| < hi)."""
+    a = abs(v)
+    lo = max(g for g in grid if g <= a)
+    hi = min(g for g in grid if g > a)
+    return lo, hi
+
+
+def _flip_case(quant, woi, seed):
+    """A tiny layer, one slot (t, j) and the intermediate element i of that slot whose exact
+    value lies closest (relative to its size) to a rounding midpoint of the fc2 operand's
+    format, with that element's other rounding worked out here from the format's grid: the
+    E4M3 values (MXFP8 under the block's scale byte), the two bf16 bit patterns around the
+    value, or the E2M1 values (NVFP4 under the block's E4M3 scale); with an activation global
+    scale a2 the decision is taken on a2 * h and the operand is the value / a2."""
+    cfg, ck = _tiny(quant, seed=seed)
+    rng = np.random.default_rng(100 + seed)
+    M, k = 3, 2
+    x = S.make_x(rng, M, ck.H)
+    ids = S.uniform_topk(rng, M, ck.E, k)
+    w = S.router_weights(rng, M, k, "sigmoid_norm", 2.5)
+    lim = 7.0 if quant == "mxfp4" else math.inf
+    t, j = 1, 1
+    _, _, perm, slot_of = O.route(ids, ck.E)
+    h = O.slot_intermediate(ck, x, ids, lim, topk_w=w, weight_on_input=woi)[slot_of[t * k + j]]
+    e = int(ids[t, j])
+    a2 = None if O.act_gscale(ck, "a2") is None else float(np.float32(O.act_gscale(ck, "a2")[e]))
+    best = None
+    for i in range(ck.I):
+        if quant in ("mxfp4", "w4a8_nvfp4"):
+            v = h * (1.0 if a2 is None else a2)
+            q, s = C.mxfp8_quantize(v[None, :])
+            sc = 2.0 ** (int(s[0, i // 32]) - 127)
+            grid = sorted(set(C.E4M3_TABLE[:127].tolist()))
+            near = C.mxfp8_dequantize(q, s)[0, i]
+            val = v[i] / sc
+        elif quant == "w4a4_nvfp4":
+            v = (np.float32(a2) * h.astype(np.float32)).astype(np.float32)
+            q, s = C.nvfp4_quantize(v[None, :])
+            sc = float(C.E4M3_TABLE[s[0, i // 16]])
+            grid = C.E2M1_TABLE[:8].tolist()
+            near = C.nvfp4_dequantize(q, s)[0, i]
+            val = float(v[i]) / sc
+        else:
+            bits = int(C.f64_to_bf16_bits(np.array([h[i]]))[0])
+            cand = sorted(abs(float(C.bf16_bits_to_f64(np.array([b], np.uint16))[0]))
+                          for b in (bits - 1, bits, bits + 1))
+            sc, grid, near, val = 1.0, cand, float(C.bf16_round(h[i])), h[i]
+        if val == 0 or abs(val) >= max(grid):
+            continue
+        lo, hi = _other_neighbour(val, grid)
+        dist = abs(abs(val) - (lo + hi) / 2) / abs(val)
+        other = hi if abs(near) == lo * sc else lo
+        alt = math.copysign(other * sc, val) / (1.0 if a2 is None else a2)
+        if best is None or dist < best[0]:
+            best = (dist, i, alt)
+    return ck, x, ids, w, lim, t, j, best
+
+
+@pytest.mark.parametrize("quant,woi", [("mxfp4", False), ("nvfp4", False), ("nvfp4", True),
+                                       ("w4a8_nvfp4", False), ("w4a4_nvfp4", False)])
+def test_requant_alternatives_pinned_by_flipping(quant, woi):
+    """oracle.moe.requant_alternatives against a forward recomputed with one decision flipped:
+    the element-by-element brute force is run on the slot's fc2 operand with element i replaced
+    by its other rounding (found above from the format's grid), and the change of the token's
+    unrounded output must be one of the vectors the helper lists for that row - so a wrong sign,
+    a missing router weight or a wrong column of W2 in the helper fails here."""
+    ck, x, ids, w, lim, t, j, best = _flip_case(quant, woi, seed=3)
+    dist, i, alt = best
+    rel = max(1.5 * dist, 1e-9)
+    alts = O.requant_alternatives(ck, x, ids, w, lim, rel=rel, rows=[t], weight_on_input=woi)[t]
+    _, base = O.moe_forward_bruteforce(ck, x, ids, w, lim, weight_on_input=woi, return_f64=True)
+    _, flip = O.moe_forward_bruteforce(ck, x, ids, w, lim, weight_on_input=woi,
+                                       fc2_override={(t, j): {i: alt}}, return_f64=True)
+    want = flip[t] - base[t]
+    assert np.abs(want).max() > 0
+    tol = 1e-12 * np.abs(base[t]).max()
+    assert any(np.allclose(d, want, rtol=0, atol=tol) for d in alts), (quant, i, len(alts))
+    # the other rows are untouched by a flip in row t's slot
+    others = [r for r in range(ids.shape[0]) if r != t]
+    assert np.array_equal(flip[others], base[others])
+
+
+def test_nvfp4_alternates_worked_midpoints():
+    """E2M1 midpoints under a chosen block scale: a block whose largest magnitude is 3 takes the
+    E4M3 scale 0.5 (3 / 6), and each value 0.5 * m for a midpoint m of the E2M1 grid, nudged by
+    one part in 10^5 above or below, has the grid value on that side as its nearest rounding and
+    the one on the other side as its alternate; exact midpoints round to the even code."""
+    mids = [(0.25, 0.0, 0.5), (0.75, 0.5, 1.0), (1.25, 1.0, 1.5), (1.75, 1.5, 2.0),
+            (2.5, 2.0, 3.0), (3.5, 3.0, 4.0), (5.0, 4.0, 6.0)]
+    for m, lo, hi in mids:
+        for sign in (1.0, -1.0):
+            v = np.zeros((1, 16))
+            v[0, 0] = 3.0                                  # block maximum: scale 0.5
+            v[0, 1] = sign * 0.5 * m * (1 + 1e-5)          # above the midpoint: nearest hi
+            v[0, 2] = sign * 0.5 * m * (1 - 1e-5)          # below: nearest lo
+            v[0, 3] = sign * 0.5 * (lo + (hi - lo) * 0.1)  # far from the midpoint
+            mask, alt = C.nvfp4_alternates(v, 1e-4)
+            q, s = C.nvfp4_quantize(v.astype(np.float32))
+            assert s.tolist() == [[0x30]]                  # E4M3 0.5
+            near = C.nvfp4_dequantize(q, s)[0]
+            assert near[1] == sign * 0.5 * hi and near[2] == sign * 0.5 * lo, m
+            assert mask[0].tolist()[:4] == [False, True, True, False], m
+            assert alt[0, 1] == sign * 0.5 * lo and alt[0, 2] == sign * 0.5 * hi, m
+            assert alt[0, 3] == near[3]
+    # exact midpoints: ties to the even code (mantissa bit 0): 0.25 -> 0, 0.75 -> 1, 1.25 -> 1,
+    # 1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4; the alternate is the odd neighbour
+    v = np.zeros((1, 16))
+    v[0, 0] = 3.0
+    v[0, 1:8] = [0.5 * m for m, _, _ in mids]
+    mask, alt = C.nvfp4_alternates(v, 1e-4)
+    q, s = C.nvfp4_quantize(v.astype(np.float32))
+    assert (C.nvfp4_dequantize(q, s)[0, 1:8] / 0.5).tolist() == [0, 1, 1, 2, 2, 4, 4]
+    assert mask[0, 1:8].all()
+    assert (alt[0, 1:8] / 0.5).tolist() == [0.5, 0.5, 1.5, 1.5, 3, 3, 6]
+
+
+def test_tier_local_index_hand_map():
+    """The hybrid layer's compact storage: each tier lists its experts in ascending id."""
+    got = O.tier_local_index(np.array([3, 4, 3, 4, 4], np.int8))
+    assert got == {0: (3, 0), 1: (4, 0), 2: (3, 1), 3: (4, 1), 4: (4, 2)}
+    assert O.tier_local_index(np.array([4, 4, 4], np.int8)) == {0: (4, 0), 1: (4, 1), 2: (4, 2)}
+    assert O.tier_local_index(np.array([3], np.int8)) == {0: (3, 0)}
+
+
+def test_hybrid_expert_weights_hand_checkpoint():
+    """A hybrid checkpoint written by hand, every expert's weights one constant: the kept tier
+    (NVFP4, codes 0x22 = E2M1 1.0 in both nibbles) has E4M3 scales 1, 2, 3 for its experts 0, 1,
+    2 and globals 1; the NF3 tier (codes all 7 = LUT 1.0, bytes 0xFF) has scales 4 and 8.  With
+    tiers [3, 4, 3, 4, 4] the experts' values are 4, 1, 8, 2, 3 - in W13 and W2 alike - and the
+    brute-force forward of one token through expert 2 alone is the closed form 8 * 8 * sum(x)."""
+    E, H, I = 5, 32, 32
+    tier = np.array([3, 4, 3, 4, 4], np.int8)
+    nv = S.Checkpoint(quant="nvfp4", E=3, H=H, I=I)
+    nv.w13 = np.full((3, 2 * I, H // 2), 0x22, np.uint8)
+    nv.w2 = np.full((3, H, I // 2), 0x22, np.uint8)
+    sc = np.array([0x38, 0x40, 0x44], np.uint8)        # E4M3 1.0, 2.0, 3.0
+    nv.s13 = np.repeat(sc, 2 * I * H // 16).reshape(3, 2 * I, H // 16)
+    nv.s2 = np.repeat(sc, H * I // 16).reshape(3, H, I // 16)
+    nv.g13 = np.ones(3, np.float32)
+    nv.g2 = np.ones(3, np.float32)
+    nf = S.Checkpoint(quant="nf3", E=2, H=H, I=I)
+    nf.w13 = np.full((2, 2 * I, 3 * H // 8), 0xFF, np.uint8)
+    nf.w2 = np.full((2, H, 3 * I // 8), 0xFF, np.uint8)
+    sf = np.array([0x48, 0x50], np.uint8)              # E4M3 4.0, 8.0
+    nf.s13 = np.repeat(sf, 2 * I * H // 32).reshape(2, 2 * I, H // 32)
+    nf.s2 = np.repeat(sf, H * I // 32).reshape(2, H, I // 32)
+    ck = S.Checkpoint(quant="hybrid", E=E, H=H, I=I, tier=tier, nv=nv, nf=nf)
+    for e, want in enumerate([4.0, 1.0, 8.0, 2.0, 3.0]):
+        W13, W2, _ = O.expert_weights(ck, e)
+        assert np.all(W13 == want) and np.all(W2 == want), e
+    # one token through expert 2 (value 8): gate = up = 8 * sum(x), h = silu(g) * u rounded to
+    # bf16, out = 8 * I * bf16(h) per output element (bf16 activations, no clamp)
+    x = S.f32_to_bf16_bits(np.full((1, H), 0.0625, np.float32))
+    ids = np.array([[2]], np.int32)
+    w = np.ones((1, 1), np.float32)
+    g = 8.0 * H * 0.0625
+    h = float(C.bf16_round(g / (1 + math.exp(-g)) * g))
+    _, f64 = O.moe_forward_bruteforce(ck, x, ids, w, return_f64=True)
+    assert np.allclose(f64[0], 8.0 * I * h, rtol=1e-14, atol=0)
+
+
+def test_ep_mask_foreign_hand_worked():
+    """The EP slice's input recipe on a hand-worked batch: rank owning global experts 4..7.
+    Row 0 owns global 5 (local 1): its foreign slot takes local 1.  Row 1 owns nothing: its
+    slots take the batch's smallest owned local id (1).  Row 2 owns 7 and 6 (locals 3, 2).
+    Weights of non-owned slots become 0."""
+    ids = np.array([[5, 1], [9, -1], [7, 6]], np.int32)
+    w = np.array([[0.5, 0.25], [0.75, 1.0], [0.125, 2.0]], np.float32)
+    got_ids, got_w = S.ep_mask_foreign(ids, w, 4, 4)
+    assert got_ids.tolist() == [[1, 1], [1, 1], [3, 2]]
+    assert got_w.tolist() == [[0.5, 0.0], [0.0, 0.0], [0.125, 2.0]]
+    # a batch that owns nothing: every slot id 0, weight 0
+    got_ids, got_w = S.ep_mask_foreign(np.array([[0, 9]], np.int32), np.ones((1, 2), np.float32),
+                                       4, 4)
+    assert got_ids.tolist() == [[0, 0]] and got_w.tolist() == [[0.0, 0.0]]
+    # the row's own smallest owned id wins over the batch's
+    got_ids, _ = S.ep_mask_foreign(np.array([[4, 0], [7, 2]], np.int32),
+                                   np.ones((2, 2), np.float32), 4, 4)
+    assert got_ids.tolist() == [[0, 0], [3, 3]]
