@@ -158,6 +158,10 @@ moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* 
  *                 no clamp.  alpha = 1, beta = 0 unless set with moe_plan_set_swiglu_alpha_beta.
  *   deterministic 0: fp32 atomic combine (run-to-run ulp differences possible);
  *                 1: per-slot route buffer + fixed-order top-k sum (bit-stable).
+ * Shapes: the 16-bit-operand modes (W4A16 NVFP4, the hybrids, MOE_W4A8_NVFP4) need
+ * round_up(I, 128) to be a multiple of 256 (their tensor-core fc2 runs 256-wide K stages);
+ * W4A4 needs that and H % 256 == 0.  Other shapes are refused, never run on another kernel
+ * family.
  * Errors: MOE_ERR_ARG, MOE_ERR_SHAPE, MOE_ERR_UNSUPPORTED. */
 moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, float swiglu_limit,
                     int deterministic, moe_plan_t** out);
@@ -166,10 +170,10 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
  * (B12xExperts `_swiglu_params`, SWIGLUOAI form). */
 moe_status moe_plan_set_swiglu_alpha_beta(moe_plan_t* plan, float alpha, float beta);
 
-/* Kernel family for later moe_run calls: 0 (default) = tcgen05 tensor-core GEMMs where the quant
- * mode and shape have them (W4A8; W4A16 NVFP4 / hybrid when I rounded up to 128 is a multiple
- * of 256), CUDA-core GEMMs otherwise; 1 = CUDA-core GEMMs for every mode (a slower, independent
- * path, kept for cross-checks).  Errors: MOE_ERR_ARG. */
+/* Kernel family for later moe_run calls: 0 (default) = the tcgen05 tensor-core GEMMs (every mode
+ * and shape moe_plan admits has them); 1 = CUDA-core GEMMs (a slower, independent path kept only
+ * as an explicit cross-check; W4A16 NVFP4, the hybrids and W4A8 only).
+ * Errors: MOE_ERR_ARG, MOE_ERR_UNSUPPORTED (backend 1 for MOE_W4A8_NVFP4 / MOE_W4A4_NVFP4). */
 moe_status moe_plan_set_backend(moe_plan_t* plan, int backend);
 
 /* fc1 kernel of the W4A8 tensor-core path at the 16-token tile width (calls with M <= 16):
@@ -246,6 +250,16 @@ moe_status moe_run_chunked(const moe_plan_t* plan, const moe_prepared* weights, 
 moe_status moe_run_static_scratch(const moe_plan_t* plan, const moe_prepared* weights,
                                   const void* x, const int32_t* topk_ids,
                                   const float* topk_weights, void* out, int M, void* stream);
+
+/* moe_get_device_error for calls made with moe_run_static_scratch (no counterpart on the pages):
+ * the device error word of those calls lives in the library's own array, which the caller cannot
+ * name, so this reads (and clears) it there.  Synchronises `stream`.  *code = 0 when no
+ * device-side check failed since the last read; the status is MOE_ERR_TIMEOUT / MOE_ERR_DEVICE
+ * as for moe_get_device_error.  Like the run call it shares the array with every other static
+ * call on the device: read it before the next call overwrites it.  The cached array address
+ * assumes the device's primary context lives as long as the process (as for the run call).
+ * Errors: MOE_ERR_ARG, MOE_ERR_CAPACITY (a plan the array cannot hold), MOE_ERR_CUDA. */
+moe_status moe_get_device_error_static(const moe_plan_t* plan, void* stream, int* code);
 
 /* Size of the device staging buffer moe_run_host needs (x, ids, weights and out of max_m rows). */
 moe_status moe_io_bytes(const moe_plan_t* plan, size_t* bytes);

@@ -53,6 +53,7 @@ SIGNATURES = {
     "moe_run_host": (c_int, [c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_size_t, c_void_p,
                              c_void_p, c_void_p, c_void_p, c_int, c_void_p]),
     "moe_get_device_error": (c_int, [c_void_p, c_void_p, c_void_p, c_int_p]),
+    "moe_get_device_error_static": (c_int, [c_void_p, c_void_p, c_int_p]),
     "moe_debug_routing": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p,
                                   c_void_p, c_void_p]),
     "moe_debug_actq": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p]),

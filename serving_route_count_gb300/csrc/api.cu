@@ -356,9 +356,12 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   if (st != MOE_OK) return st;
   if (topk < 1 || topk > 16 || max_m < 1 || max_m > (1 << 20)) return MOE_ERR_SHAPE;
   if (std::isnan(swiglu_limit) || swiglu_limit <= 0.f) return MOE_ERR_ARG;
-  // MXFP8 activations with NVFP4 weights run on the 16-bit tensor-core kernels only
-  if (quant_mode == MOE_W4A8_NVFP4 && align_up((size_t)I, 128) % 256 != 0)
-    return MOE_ERR_UNSUPPORTED;
+  // The 16-bit-operand modes (W4A16 NVFP4, the hybrids, NVFP4 weights with MXFP8 activations)
+  // run on tensor-core kernels whose fc2 K stages are 256 wide: other shapes are refused here
+  // rather than sent to another kernel family
+  if (quant_mode != MOE_W4A8_MXFP4 && quant_mode != MOE_W4A4_NVFP4 &&
+      align_up((size_t)I, 128) % 256 != 0)
+    return MOE_ERR_SHAPE;
   // W4A4: whole 256-wide K stages in both GEMMs (the activation scale atoms cover K exactly)
   if (quant_mode == MOE_W4A4_NVFP4 && (H % 256 != 0 || align_up((size_t)I, 128) % 256 != 0))
     return MOE_ERR_UNSUPPORTED;
@@ -493,11 +496,10 @@ moe_status moe_plan_set_profile_events(moe_plan_t* plan, void* const* events, in
 }
 
 static bool use_tc(const PlanDims& d) { return d.backend == 0 && d.quant == MOE_W4A8_MXFP4; }
-// W4A16 / hybrid on tensor cores: the NVFP4 scale rows of fc2 (Ip/16 bytes) must be whole
-// 16-byte units for the tensor maps.
+// W4A16 / hybrid on tensor cores (moe_plan admits only shapes with Ip % 256 == 0 for these
+// modes, so backend 0 always runs them on tensor cores).
 static bool use_tc16(const PlanDims& d) {
-  return d.backend == 0 && d.quant != MOE_W4A8_MXFP4 && d.quant != MOE_W4A4_NVFP4 &&
-         d.Ip % 256 == 0;
+  return d.backend == 0 && d.quant != MOE_W4A8_MXFP4 && d.quant != MOE_W4A4_NVFP4;
 }
 // W4A4 runs on its block-scaled FP4 kernels only (moe_plan refuses the CUDA-core backend)
 static bool use_tc4(const PlanDims& d) { return d.quant == MOE_W4A4_NVFP4; }

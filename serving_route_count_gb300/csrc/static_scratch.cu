@@ -27,8 +27,10 @@ static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 std::mutex g_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the array on the current device, resolved once per device.  Host code must
-// not use the symbol itself: on the host it is a stand-in, not a device address.
+// Device address of the array on the current device, resolved once per device and cached for
+// the life of the process (the cache assumes the device's primary context lives that long: after
+// cudaDeviceReset the cached address would be stale).  Host code must not use the symbol itself:
+// on the host it is a stand-in, not a device address.
 moe_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -65,6 +67,18 @@ moe_status moe_run_static_scratch(const moe_plan_t* plan, const moe_prepared* we
   if (st != MOE_OK) return st;
   return moe_run(plan, weights, scratch, kStaticScratchBytes, x, topk_ids, topk_weights, out, M,
                  stream);
+}
+
+moe_status moe_get_device_error_static(const moe_plan_t* plan, void* stream, int* code) {
+  if (plan == nullptr || code == nullptr) return MOE_ERR_ARG;
+  size_t need = 0;
+  moe_status st = moe_scratch_bytes(plan, &need);
+  if (st != MOE_OK) return st;
+  if (need > kStaticScratchBytes) return MOE_ERR_CAPACITY;
+  void* scratch = nullptr;
+  st = scratch_address(&scratch);
+  if (st != MOE_OK) return st;
+  return moe_get_device_error(plan, scratch, stream, code);
 }
 
 }  // extern "C"

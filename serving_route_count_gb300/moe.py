@@ -198,6 +198,14 @@ def moe_get_device_error(plan, scratch, stream=None):
     return st, code.value
 
 
+def moe_get_device_error_static(plan, stream=None):
+    """moe_get_device_error for calls made with moe_run_static_scratch: (status, code)."""
+    code = ctypes.c_int()
+    st = _lib.load().moe_get_device_error_static(_handle(plan), _stream(stream),
+                                                 ctypes.byref(code))
+    return st, code.value
+
+
 def moe_debug_routing(plan, scratch, M, E, topk, stream=None):
     cnt = np.zeros(E, np.int32)
     off = np.zeros(E + 1, np.int32)

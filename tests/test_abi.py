@@ -107,6 +107,40 @@ def test_run_argument_checks_without_gpu(lib):
     moe.moe_destroy_weight_plan(wp)
 
 
+def test_static_error_word_arguments_without_gpu(lib):
+    """moe_get_device_error_static checks its arguments and the plan's scratch size before any
+    device call: a null plan or code pointer is MOE_ERR_ARG, a plan whose scratch exceeds the
+    16 MiB array is MOE_ERR_CAPACITY."""
+    L = _lib.load()
+    code = ctypes.c_int(-1)
+    assert L.moe_get_device_error_static(None, None, ctypes.byref(code)) == 1
+    p = moe.moe_plan(8, 256, 128, 2, 4, moe.MOE_W4A8_MXFP4, 7.0, 0)
+    assert L.moe_get_device_error_static(ctypes.c_void_p(p), None, None) == 1
+    big = moe.moe_plan(16, 1280, 192, 4, 4096, moe.MOE_W4A8_MXFP4, 7.0, 1)
+    assert moe.moe_scratch_bytes(big) > 16 << 20
+    assert L.moe_get_device_error_static(ctypes.c_void_p(big), None, ctypes.byref(code)) == 4
+    assert code.value == -1                     # nothing written on error
+    moe.moe_destroy_plan(p)
+    moe.moe_destroy_plan(big)
+
+
+def test_16bit_modes_refuse_shapes_without_tensor_core_kernels(lib):
+    """The 16-bit-operand modes run on tensor-core kernels whose fc2 K stages are 256 wide, so
+    round_up(I, 128) must be a multiple of 256; other shapes are refused when planned (no silent
+    switch to another kernel family).  The CUDA-core backend is an explicit cross-check for the
+    supported shapes only."""
+    for q in (moe.MOE_W4A16_NVFP4, moe.MOE_W4A16_HYBRID, moe.MOE_W4A16_HYBRID_MX,
+              moe.MOE_W4A8_NVFP4, moe.MOE_W4A4_NVFP4):
+        with pytest.raises(moe.MoEError) as ei:
+            moe.moe_plan(16, 1280, 576, 4, 8, q, math.inf, 0)     # Ip = 640
+        assert ei.value.status in (2, 3), q
+        p = moe.moe_plan(16, 1280, 512, 4, 8, q, math.inf, 0)      # Ip = 512
+        moe.moe_destroy_plan(p)
+    # W4A8 (MXFP4) has tensor-core kernels for every I % 64 == 0
+    p = moe.moe_plan(16, 1280, 576, 4, 8, moe.MOE_W4A8_MXFP4, 7.0, 0)
+    moe.moe_destroy_plan(p)
+
+
 def test_w4a16_tiled_weight_sizes(lib):
     """NVFP4 and NF3 tiers are stored in tiles of 128 rows x 256 K per matrix: no padding at the
     config's shapes (I = 512, H = 6144), zero padding up to whole tiles otherwise."""
@@ -169,7 +203,7 @@ def test_router_weight_on_input_arguments(lib):
         moe.moe_plan_set_router_weight_on_input(p, 1)
     assert ei.value.status == 3
     moe.moe_destroy_plan(p)
-    p = moe.moe_plan(8, 256, 128, 1, 16, moe.MOE_W4A16_NVFP4, float("inf"), 0)
+    p = moe.moe_plan(8, 256, 256, 1, 16, moe.MOE_W4A16_NVFP4, float("inf"), 0)
     moe.moe_plan_set_router_weight_on_input(p, 1)
     with pytest.raises(moe.MoEError) as ei:
         moe.moe_plan_set_router_weight_on_input(p, 2)
@@ -195,7 +229,7 @@ def test_nvfp4_a8_mode_limits(lib):
     moe.moe_destroy_plan(p)
     with pytest.raises(moe.MoEError) as ei:
         moe.moe_plan(8, 256, 128, 2, 16, moe.MOE_W4A8_NVFP4, float("inf"), 0)   # Ip = 128
-    assert ei.value.status == 3
+    assert ei.value.status == 2
 
 
 def test_w4a4_mode_limits(lib):

@@ -28,7 +28,8 @@ def _lib_built():
 
 @pytest.mark.parametrize("det", [0, 1])
 def test_static_scratch_matches_moe_run(det):
-    from serving_route_count_gb300 import MoELayer, moe_run_static_scratch
+    from serving_route_count_gb300 import (MoELayer, moe_get_device_error_static,
+                                           moe_run_static_scratch)
     cfg = small_cfg("mxfp4")
     ck = S.make_checkpoint(cfg, seed=515)
     M = 37
@@ -49,6 +50,36 @@ def test_static_scratch_matches_moe_run(det):
         rel, mx = O.row_errors(got, C.bf16_bits_to_f64(ref))
         assert np.all(rel <= REL_L2_BOUND) and np.all(mx <= MAX_ERR_BOUND), (call, rel.max(), mx.max())
         assert np.all(got[-2:] == 0)
+        # the call's device error word lives in the library's array: read through the static
+        # accessor (no bounded wait gave up, no device check failed)
+        assert moe_get_device_error_static(layer.plan) == (0, 0)
+
+
+@pytest.mark.parametrize("det", [0, 1])
+def test_static_scratch_decode_layer(det):
+    """The decode layer (E=384, H=7168, I=576, top-6) at capacity 16 fits the 16 MiB array in
+    both combine modes.  Calls of M = 8 (split-K fc1) and M = 16 (the persistent stream-K fc1,
+    whose partial-sum slots then live in the array too) match moe_run (bit for bit in
+    deterministic mode)."""
+    from serving_route_count_gb300 import (MoELayer, moe_get_device_error_static,
+                                           moe_run_static_scratch, moe_scratch_bytes)
+    cfg = S.CONFIGS["decode_w4a8"]
+    ck = S.make_checkpoint(cfg)
+    layer = MoELayer(ck, cfg.topk, 16, cfg.swiglu_limit, det)
+    assert moe_scratch_bytes(layer.plan) <= 16 << 20
+    for call, M in enumerate((8, 16)):
+        x, ids, w = S.make_inputs(cfg, M)
+        xt, it, wt = to_device(x, ids, w)
+        ref = out_bits(layer(xt, it, wt))
+        out = torch.empty((M, cfg.H), dtype=torch.bfloat16, device="cuda")
+        moe_run_static_scratch(layer.plan, layer.prep, xt, it, wt, out)
+        got = out_bits(out)
+        if det:
+            assert np.array_equal(got, ref), call
+        rel, mx = O.row_errors(got, C.bf16_bits_to_f64(ref))
+        assert np.all(rel <= REL_L2_BOUND) and np.all(mx <= MAX_ERR_BOUND), (call, rel.max(), mx.max())
+        assert moe_get_device_error_static(layer.plan) == (0, 0)
+    layer.close()
 
 
 def test_static_scratch_rejects_large_plans():
