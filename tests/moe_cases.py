@@ -42,17 +42,28 @@ def _row_ok(got_row_bits, ref_row):
     return rel[0] <= REL_L2_BOUND and mx[0] <= MAX_ERR_BOUND, rel[0], mx[0]
 
 
+def oracle_rows(ck, x_bits, ids, w, limit, rows=None, alpha=1.0, beta=0.0,
+                weight_on_input=False):
+    """The oracle's unrounded fp64 output for the given rows (all when None), to be shared by
+    several check_rows calls on the same inputs."""
+    rows = np.arange(ids.shape[0]) if rows is None else np.asarray(rows)
+    _, f64 = O.moe_forward(ck, x_bits, ids, w, limit, alpha, beta, rows=rows, return_f64=True,
+                           weight_on_input=weight_on_input)
+    return f64
+
+
 def check_rows(got_bits, ck, x_bits, ids, w, limit, rows=None, alpha=1.0, beta=0.0,
-               weight_on_input=False):
+               weight_on_input=False, ref_f64=None):
     """Compare the given rows (all when None) with the oracle; returns (rel, mx) arrays.
+    ``ref_f64``: the oracle's output of these inputs when already computed (oracle_rows).
 
     A row that misses the bound passes if the oracle's own alternatives of near-midpoint
     requantisation decisions (oracle.moe.requant_alternatives; any subset of up to 10 of them)
     bring it within the bound: those elements are decided by fp32 noise, both roundings are
     correct results of the method."""
     rows = np.arange(ids.shape[0]) if rows is None else np.asarray(rows)
-    _, f64 = O.moe_forward(ck, x_bits, ids, w, limit, alpha, beta, rows=rows, return_f64=True,
-                           weight_on_input=weight_on_input)
+    f64 = ref_f64 if ref_f64 is not None else oracle_rows(
+        ck, x_bits, ids, w, limit, rows, alpha, beta, weight_on_input)
     rel, mx = O.row_errors(got_bits[rows], f64[rows])
     bad = [int(r) for r, a, b in zip(rows, rel, mx) if a > REL_L2_BOUND or b > MAX_ERR_BOUND]
     if bad:

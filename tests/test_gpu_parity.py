@@ -11,7 +11,8 @@ import pytest
 from oracle import codecs as C
 from oracle import moe as O
 from synth import moe_inputs as S
-from moe_cases import H_CANCEL_ATOL, check_rows, run_layer, small_cfg, to_device, out_bits
+from moe_cases import (H_CANCEL_ATOL, check_rows, oracle_rows, run_layer, small_cfg,
+                        to_device, out_bits)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -555,26 +556,71 @@ def test_prepare_roundtrip(quant, layout):
     layer.close()
 
 
-def test_nvfp4_full_size_sampled():
-    cfg = S.CONFIGS["w4a16_nvfp4"]
-    ck = S.make_checkpoint(cfg)
-    M = 64
+def _sample_rows(ids, M, seed, n=256):
+    """All rows up to n; beyond, a seeded subset of n rows plus every padding row."""
+    if M <= n:
+        return np.arange(M)
+    rng = np.random.default_rng(seed)
+    pad = np.flatnonzero(~(ids >= 0).any(axis=1))
+    return np.union1d(np.sort(rng.choice(M, n, replace=False)), pad)
+
+
+def _full_size_both_modes(cfg, ck, M, layers=None):
+    """One call of the full-size layer at M rows in each combine mode: every sampled row (all
+    rows up to 256; a seeded 256-row subset plus all padding rows beyond) against the oracle,
+    padding rows exactly 0, no device error, routing bit-exact, and in deterministic mode a
+    bit-identical repeat.  ``layers`` ({det: layer}) reuses layers of a larger capacity."""
     x, ids, w = S.make_inputs(cfg, M)
-    layer = _layer(ck, cfg.topk, M, cfg.swiglu_limit, 0)
-    got = run_layer(layer, x, ids, w)
-    check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=[0, 31, 63])
-    layer.close()
+    rows = _sample_rows(ids, M, seed=9000 + M)
+    ref = oracle_rows(ck, x, ids, w, cfg.swiglu_limit, rows=rows)
+    route = O.route(ids, ck.E)
+    for det in (0, 1):
+        layer = layers[det] if layers else _layer(ck, cfg.topk, M, cfg.swiglu_limit, det)
+        got = run_layer(layer, x, ids, w)
+        st, code = layer.device_error()
+        assert st == 0 and code == 0, (M, det, code)
+        for a, b in zip(layer.routing(M), route):
+            assert np.array_equal(a, b), (M, det)
+        check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=rows, ref_f64=ref)
+        pad = ~(ids >= 0).any(axis=1)
+        assert np.all(got[pad] == 0)
+        if det:
+            assert np.array_equal(run_layer(layer, x, ids, w), got), M
+        if not layers:
+            layer.close()
 
 
-def test_hybrid_full_size_sampled():
+def test_decode_ladder_full_size_all_rows(decode_layer):
+    """Every call of the decode ladder (E=384, H=7168, I=576, top-6, M = 1..8, 10, 12, 14, 16,
+    last quarter of the rows padding) in both combine modes, every row against the oracle:
+    the calls the bench times, on capacity-16 plans as the bench plans them, at their own
+    split-K / stream-K fc1 and fc2 schedules."""
+    cfg, ck = decode_layer
+    layers = {det: _layer(ck, cfg.topk, 16, cfg.swiglu_limit, det) for det in (0, 1)}
+    for M in cfg.m_list:
+        _full_size_both_modes(cfg, ck, M, layers)
+    for layer in layers.values():
+        layer.close()
+
+
+@pytest.fixture(scope="module")
+def nvfp4_ck():
+    return S.make_checkpoint(S.CONFIGS["w4a16_nvfp4"])
+
+
+@pytest.mark.parametrize("M", [64, 512, 2048, 8192])
+def test_nvfp4_full_size_sampled(nvfp4_ck, M):
+    """NVFP4 W4A16 (E=256, H=6144, I=512, top-8) at its decode and prefill sizes, both
+    combine modes: all rows up to 256, else 256 seeded rows."""
+    _full_size_both_modes(S.CONFIGS["w4a16_nvfp4"], nvfp4_ck, M)
+
+
+@pytest.mark.parametrize("M", [8, 2048])
+def test_hybrid_full_size_sampled(M):
+    """The hybrid layer (64 NVFP4 + 192 NF3 experts, Zipf 0.8 routing) at both of its sizes,
+    both combine modes (deterministic is the configured one)."""
     cfg = S.CONFIGS["hybrid_nvfp4_nf3"]
-    ck = S.make_checkpoint(cfg)
-    M = 8
-    x, ids, w = S.make_inputs(cfg, M)
-    layer = _layer(ck, cfg.topk, M, cfg.swiglu_limit, 1)
-    got = run_layer(layer, x, ids, w)
-    check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=[0, 3, 7])
-    layer.close()
+    _full_size_both_modes(cfg, S.make_checkpoint(cfg), M)
 
 
 # ---------------------------------------------------------------------------- tensor-core path
