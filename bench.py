@@ -300,6 +300,7 @@ def prefill_report(stream, flush, hbm_peak):
         it = torch.from_numpy(ids).cuda()
         wt = torch.from_numpy(w).cuda()
         ot = torch.empty((M, cfg.H), dtype=torch.bfloat16, device="cuda")
+        torch.cuda.synchronize()          # inputs copied before the side stream reads them
         with torch.cuda.stream(stream):
             layer(xt, it, wt, ot)
             stream.synchronize()
@@ -365,6 +366,7 @@ def modes_report(stream, flush, hbm_peak):
             it = torch.from_numpy(ids).cuda()
             wt = torch.from_numpy(w).cuda()
             ot = torch.empty((M, cfg.H), dtype=torch.bfloat16, device="cuda")
+            torch.cuda.synchronize()      # inputs copied before the side stream reads them
             with torch.cuda.stream(stream):
                 layer(xt, it, wt, ot)
                 stream.synchronize()

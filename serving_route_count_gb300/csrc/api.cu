@@ -7,6 +7,7 @@
 #include <vector>
 
 #include "moe_common.cuh"
+#include "tc_sched.cuh"
 #include "../../include/moe_gb300.h"
 
 namespace moe {
@@ -589,8 +590,10 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   const int bn = t4 ? tc4_pick_bn(M) : (tc ? tc_pick_bn(M, d.topk, d.E, tc8) : kSimtSlots);
   const int tiles = call_tiles(d, plan->s.max_tiles, M, bn);
   const int RT = cdiv(d.I, 128);
-  // decode widths with more units than one wave of CTAs: the persistent stream-K fc1
-  const bool streamk = tc8 && bn == 16 &&
+  // decode widths with more units than one wave of CTAs: the persistent stream-K fc1 (when its
+  // 32-bit schedule arithmetic fits the call)
+  const bool sk_ok = stream_schedule_fits((long long)tiles * RT, d.H / 128);
+  const bool streamk = tc8 && bn == 16 && sk_ok &&
                        (d.fc1_kernel == 0 ? fc1_stream_preferred(bn, tiles * RT) : d.fc1_kernel == 2);
   const int splits = (tc && !streamk) ? fc1_splits(d, tiles, bn) : 1;
   // small tensor-core calls route and quantise (W4A8) or convert (16-bit path) in one launch

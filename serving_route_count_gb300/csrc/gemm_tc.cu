@@ -122,10 +122,10 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   // Small calls route in shared memory (scratch in the last stage, before any copy lands
   // there), so the weights of the first stages are requested while the routing launch still
   // runs; larger calls wait for its tables.
-  int e_pre = -1;
+  int e_pre = -1, nt = 0;
   if (p.ids != nullptr) {
     int* scratch = reinterpret_cast<int*>(smem + (S - 1) * Cfg::kStage1);
-    const int nt = min(pre_route_tiles<kTcThreads>(p.ids, p.Mk, p.E, p.ep_first, BN, scratch), p.max_tiles);
+    nt = min(pre_route_tiles<kTcThreads>(p.ids, p.Mk, p.E, p.ep_first, BN, scratch), p.max_tiles);
     if (tile >= nt) {
       pdl_wait_prev();
       return;
@@ -191,7 +191,12 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   // fc2 reads the routing tables before its own wait: it may launch only once every CTA of
   // this kernel has seen them complete
   pdl_launch_next();
-  const int4 td = p.tiles[tile];
+  // the shared-memory routing planned the same tiles as the routing launch (see checked_tile)
+  if (p.ids != nullptr && tid == 0 && tile == 0 && fb == 0 && split == 0 &&
+      nt != min(__ldcg(p.ctrl + 1), p.max_tiles))
+    set_error(p.err, kErrRouteBounds);
+  const int4 td = p.ids != nullptr ? checked_tile(p.tiles, p.ctrl, tile, p.E, p.Sm, BN, p.err)
+                                    : p.tiles[tile];
   const int e = td.x, p0 = td.y, n = td.z;
   const TileLoad<BN> tl(n);
   if (pre > 0 && e != e_pre) set_error(p.err, kErrRouteBounds);

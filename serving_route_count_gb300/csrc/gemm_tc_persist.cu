@@ -77,7 +77,8 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
                                              ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[S], empty[S], acc_full[2], acc_empty[2], drain;
   __shared__ uint32_t s_tmem;
-  __shared__ int s_last, s_fail;
+  __shared__ int s_last, s_fail, s_npieces;
+  __shared__ int s_pieces[kStreamMaxPieces];
 
   // Small calls route in shared memory (scratch in the last stage, before any copy lands
   // there), so the weights of the first stages are requested while the routing launch still
@@ -178,6 +179,8 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   // fc2 reads the routing tables before its own wait: it may launch only once every CTA of
   // this kernel has seen them complete
   pdl_launch_next();
+  // the shared-memory routing planned the same tiles as the routing launch (see checked_tile)
+  if (tid == 0 && n_tiles != min(__ldcg(p.ctrl + 1), p.max_tiles)) set_error(p.err, kErrRouteBounds);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -189,7 +192,7 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
         const int tile = u / p.RT, fb = u - tile * p.RT;
         if (tile != cur_tile) {
           cur_tile = tile;
-          const int4 td = p.tiles[tile];
+          const int4 td = checked_tile(p.tiles, p.ctrl, tile, p.E, p.Sm, BN, p.err);
           e = td.x;
           p0 = td.y;
         }
@@ -260,7 +263,7 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
     for (; sg.next(u, k0, len); ++j) {
       const int k1 = k0 + len;
       const int tile = u / p.RT, fb = u - tile * p.RT;
-      const int4 td = p.tiles[tile];
+      const int4 td = checked_tile(p.tiles, p.ctrl, tile, p.E, p.Sm, BN, p.err);
       const int p0 = td.y, n = td.z;
       const int f = fb * 128 + row;
       const int b = j & 1;
@@ -270,7 +273,7 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
       const uint32_t trow = tmem + b * Cfg::kAcc + ((uint32_t)(quad * 32) << 16);
       const bool whole = k0 == 0 && k1 == p.KT;
       float* part = whole ? nullptr
-                          : p.part + (size_t)wk.part_slot(wk.c, u) * Cfg::kPartFloats;
+                          : p.part + (size_t)wk.own_slot(u) * Cfg::kPartFloats;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float up[16], gt[16];
@@ -310,16 +313,14 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (s_last && ok) {
           __threadfence();
-          // the unit's pieces in K order: CTAs holding its first .. last stream step; CTAs
-          // with empty ranges (grids larger than the step count) hold none
-          const long long xf = (long long)(u - wk.first_stream_unit) * p.KT;
-          const int c_first = wk.cta_of(xf), c_last = wk.cta_of(xf + p.KT - 1);
+          // the unit's pieces in K order (CTAs with empty ranges hold none), listed once by
+          // one thread
+          if (warp == 4 && lane == 0) s_npieces = wk.unit_pieces(u, s_pieces);
+          asm volatile("bar.sync 1, 128;" ::: "memory");
           reduce_pieces(
-              c_last - c_first + 1, n, (size_t)128, (size_t)BN * 128,
+              s_npieces, n, (size_t)128, (size_t)BN * 128,
               [&](int qq) -> const float* {
-                const int cc = c_first + qq;
-                if (wk.begin_of(cc + 1) == wk.begin_of(cc)) return nullptr;   // empty range
-                return p.part + (size_t)wk.part_slot(cc, u) * Cfg::kPartFloats + row;
+                return p.part + (size_t)s_pieces[qq] * Cfg::kPartFloats + row;
               },
               [&](int cc, float up, float gt) {
                 const float h = f < p.I ? swiglu(gt, up, p.limit, p.alpha, p.beta) : 0.f;

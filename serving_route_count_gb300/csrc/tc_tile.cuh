@@ -129,6 +129,24 @@ static __device__ int pre_route_tiles(const int32_t* ids, int Mk, int E, int ep_
   return total;
 }
 
+// A tile record of the routing launch for a kernel that planned its work from its own
+// shared-memory routing of the ids (pre_route_tiles), read after waiting for the routing
+// launch.  Both route the same ids, so the records agree; if the ids changed between the two
+// reads (the caller modified them while the call ran), a tile the pre-routing counted may lie
+// beyond the routing launch's list or hold an inconsistent record: such a tile reads as an
+// empty tile of expert 0 (every copy and store stays inside its buffer) and sets the routing
+// error bit.
+static __device__ __forceinline__ int4 checked_tile(const int4* tiles, const int32_t* ctrl,
+                                                    int tile, int E, int Sm, int bn,
+                                                    int32_t* err) {
+  const int4 td = tile < __ldcg(ctrl + 1) ? __ldcg(tiles + tile) : make_int4(-1, 0, 0, 0);
+  if (td.x < 0 || td.x >= E || td.y < 0 || td.z < 1 || td.z > bn || td.y > Sm - td.z) {
+    set_error(err, kErrRouteBounds);
+    return make_int4(0, 0, 0, 0);
+  }
+  return td;
+}
+
 static __device__ __forceinline__ float swiglu(float gate, float up, float limit, float alpha,
                                                float beta) {
   const float g = fminf(gate, limit);
