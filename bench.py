@@ -142,7 +142,7 @@ def reference_arm(args, rank, world):
 # ---------------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples every 200 ms from before the warm-up to after the timed region; the
+    """nvidia-smi samples every 50 ms from before the warm-up to after the timed region; the
     summary keeps the samples whose timestamps fall inside the marked timed region."""
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -157,7 +157,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -425,6 +425,13 @@ def our_arm(args, rank, world):
 
     # inputs: per M, N_ROUTING_SETS routing sets (+ x), device resident; one graph per (M, set)
     stream = torch.cuda.Stream()
+    try:   # event-record nodes inside graphs (torch.cuda.Event(external=True))
+        torch.cuda.Event(enable_timing=True, external=True)
+        in_graph_events = True
+    except TypeError:
+        in_graph_events = False
+    flush_graph = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda") if in_graph_events \
+        else None
     calls = []   # (M, set, graph, x, ids, w, out, prof_events, tokens, distinct)
     for M in m_list:
         for s in range(N_ROUTING_SETS):
@@ -444,12 +451,22 @@ def our_arm(args, rank, world):
         for c in calls:   # eager warm-up of each shape
             layer(c["x"], c["ids"], c["w"], c["out"])
         stream.synchronize()
-        # two graphs per call: the timed one, whose kernels launch as a chain, and one with an
-        # event record between stages (which breaks the chain) for the per-kernel durations
+        # two graphs per call: the timed one - the L2 flush, then the layer call between two
+        # event-record nodes, so the events time the call's kernels on the device and not the
+        # host's graph launch - and one with an event record between stages (which breaks the
+        # launch chain) for the per-kernel durations
         for c in calls:
             g = torch.cuda.CUDAGraph()
+            if in_graph_events:
+                c["ea"] = torch.cuda.Event(enable_timing=True, external=True)
+                c["eb"] = torch.cuda.Event(enable_timing=True, external=True)
             with torch.cuda.graph(g, stream=stream):
+                if in_graph_events:
+                    flush_graph.fill_(1)
+                    c["ea"].record(stream)
                 layer(c["x"], c["ids"], c["w"], c["out"])
+                if in_graph_events:
+                    c["eb"].record(stream)
             c["graph"] = g
             moe_plan_set_profile_events(layer.plan, c["ev"])
             g = torch.cuda.CUDAGraph()
@@ -468,6 +485,10 @@ def our_arm(args, rank, world):
         with torch.cuda.stream(stream):
             for mi, M in enumerate(m_list):
                 c = calls[mi * N_ROUTING_SETS + (si % N_ROUTING_SETS)]
+                if in_graph_events and not stage_events:
+                    c["graph"].replay()          # flush + events inside the graph
+                    pairs.append((c["ea"], c["eb"], c))
+                    continue
                 flush.fill_(si & 0xFF)
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
@@ -565,9 +586,13 @@ def our_arm(args, rank, world):
                         "padding, swiglu limit 7",
             "combine": "deterministic" if args.det else "atomic",
             "tokens_per_step": toks // args.steps,
-            "timing": "CUDA graph per call, CUDA events around each replay; L2 flushed by a "
-                      "512 MB write before each call (outside the events); 8 routing sets "
-                      "rotated per M",
+            "timing": ("CUDA graph per call: a 512 MB write (L2 flush), then the layer's "
+                       "kernels between two event-record nodes (device time of the call, "
+                       "without the host's graph launch); 8 routing sets rotated per M"
+                       if in_graph_events else
+                       "CUDA graph per call, CUDA events around each replay; L2 flushed by a "
+                       "512 MB write before each call (outside the events); 8 routing sets "
+                       "rotated per M"),
             "parallelism": f"replicas x{world}",
         },
         "roofline": {

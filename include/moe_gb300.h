@@ -329,6 +329,9 @@ void moe_destroy_plan(moe_plan_t* plan);
 const char* moe_status_str(moe_status s);
 /* Library version string, e.g. "moe_gb300 0.1 sm_103a". */
 const char* moe_version(void);
+/* Name of the CUDA error behind the last MOE_ERR_CUDA returned to this host thread (e.g.
+ * "cudaErrorInvalidValue"), or "cudaSuccess" when there was none. */
+const char* moe_last_cuda_error(void);
 
 #ifdef __cplusplus
 }

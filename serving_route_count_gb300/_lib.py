@@ -66,6 +66,7 @@ SIGNATURES = {
     "moe_destroy_plan": (None, [c_void_p]),
     "moe_status_str": (ctypes.c_char_p, [c_int]),
     "moe_version": (ctypes.c_char_p, []),
+    "moe_last_cuda_error": (ctypes.c_char_p, []),
 }
 
 _LIB = None

@@ -106,8 +106,12 @@ bool capturing(cudaStream_t st) {
   return cs != cudaStreamCaptureStatusNone;
 }
 
+// the CUDA error behind the last MOE_ERR_CUDA of this host thread (moe_last_cuda_error)
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
 moe_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return MOE_OK;
+  g_last_cuda_error = e;
   (void)cudaGetLastError();
   return MOE_ERR_CUDA;
 }
@@ -184,6 +188,8 @@ const char* moe_status_str(moe_status s) {
 }
 
 const char* moe_version(void) { return "moe_gb300 0.1 sm_103a"; }
+
+const char* moe_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
 
 moe_status moe_plan_weights(int E, int H, int I, int quant_mode, int w13_layout,
                             const int8_t* tier_of_expert, moe_weight_plan** out) {

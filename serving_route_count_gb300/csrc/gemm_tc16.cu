@@ -508,14 +508,17 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
           float a[16], b[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const bool in = c0 + j < n;
-            a[j] = in ? __ldcg(gg + (size_t)j * 2 * p.Ip) : 0.f;
-            b[j] = in ? __ldcg(gg + (size_t)j * 2 * p.Ip + p.Ip) : 0.f;
+            // columns beyond the tile repeat its last one (a valid address) and add nothing
+            const size_t jj = (size_t)min(j, n - 1 - c0);
+            a[j] = __ldcg(gg + jj * 2 * p.Ip);
+            b[j] = __ldcg(gg + jj * 2 * p.Ip + p.Ip);
           }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            up[j] += a[j];
-            gt[j] += b[j];
+            if (c0 + j < n) {
+              up[j] += a[j];
+              gt[j] += b[j];
+            }
           }
         }
 #pragma unroll

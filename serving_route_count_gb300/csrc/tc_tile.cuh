@@ -174,45 +174,67 @@ static __device__ __forceinline__ void requant_store(float h, int lane, size_t r
   }
 }
 
-// Adds `np` partial sums of this thread's accumulator row, in piece order 0..np-1, for the tile
-// columns 0..n-1 and hands each column's (up, gate) total to emit(c, up, gate).  base(q) is the
-// address of piece q's up value of column 0, or null for a piece that holds nothing (it adds
-// nothing: +0 leaves a sum unchanged); column c is at + c * col_stride, gate at + gate_off.
-// The piece addresses are computed once per piece and the loads issued 32 at a time - 4 pieces
-// x 4 columns while n <= 4, 16 columns of one piece otherwise - so a reduction costs a few
-// memory latencies, not one per piece.  n and np are uniform across the warp (emit may use warp
-// shuffles).
-template <typename Base, typename Emit>
-static __device__ __forceinline__ void reduce_pieces(int np, int n, size_t col_stride,
-                                                     size_t gate_off, Base base, Emit emit) {
-  if (n <= 4) {
-    float up[4] = {0.f, 0.f, 0.f, 0.f}, gt[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int q0 = 0; q0 < np; q0 += 4) {
-      const float* bq[4];
+// Batches of P pieces x C columns of reduce_pieces: the 2 P C loads of a batch are issued
+// together (one memory latency per batch), then added in piece order.  Every load reads a
+// valid address - a piece or column beyond the last repeats the last one and its value is not
+// added - so no load depends on a condition the compiler might evaluate after issuing it.
+template <int P, int C, typename Base, typename Emit>
+static __device__ __forceinline__ void reduce_pieces_small(int np, int n, size_t col_stride,
+                                                           size_t gate_off, Base base,
+                                                           Emit emit) {
+  float up[C], gt[C];
 #pragma unroll
-      for (int jq = 0; jq < 4; ++jq) bq[jq] = q0 + jq < np ? base(q0 + jq) : nullptr;
-      float a[4][4], b[4][4];
+  for (int jc = 0; jc < C; ++jc) up[jc] = gt[jc] = 0.f;
+  for (int q0 = 0; q0 < np; q0 += P) {
+    const float* bq[P];
 #pragma unroll
-      for (int jq = 0; jq < 4; ++jq) {
+    for (int jq = 0; jq < P; ++jq) bq[jq] = base(min(q0 + jq, np - 1));
+    float a[P][C], b[P][C];
 #pragma unroll
-        for (int jc = 0; jc < 4; ++jc) {
-          const bool in = bq[jq] != nullptr && jc < n;
-          const float* pp = in ? bq[jq] + (size_t)jc * col_stride : nullptr;
-          a[jq][jc] = in ? __ldcg(pp) : 0.f;
-          b[jq][jc] = in ? __ldcg(pp + gate_off) : 0.f;
-        }
+    for (int jq = 0; jq < P; ++jq) {
+#pragma unroll
+      for (int jc = 0; jc < C; ++jc) {
+        const float* pp = bq[jq] + (size_t)min(jc, n - 1) * col_stride;
+        a[jq][jc] = __ldcg(pp);
+        b[jq][jc] = __ldcg(pp + gate_off);
       }
+    }
 #pragma unroll
-      for (int jq = 0; jq < 4; ++jq)
+    for (int jq = 0; jq < P; ++jq)
 #pragma unroll
-        for (int jc = 0; jc < 4; ++jc) {
+      for (int jc = 0; jc < C; ++jc)
+        if (q0 + jq < np && jc < n) {
           up[jc] += a[jq][jc];
           gt[jc] += b[jq][jc];
         }
-    }
+  }
 #pragma unroll
-    for (int jc = 0; jc < 4; ++jc)
-      if (jc < n) emit(jc, up[jc], gt[jc]);
+  for (int jc = 0; jc < C; ++jc)
+    if (jc < n) emit(jc, up[jc], gt[jc]);
+}
+
+// Adds `np` partial sums of this thread's accumulator row, in piece order 0..np-1, for the tile
+// columns 0..n-1 and hands each column's (up, gate) total to emit(c, up, gate).  base(q) is the
+// address of piece q's up value of column 0 (a valid address for every q < np); column c is at
+// + c * col_stride, gate at + gate_off.  The piece addresses are computed once per piece and
+// the loads issued 32 at a time - 16 pieces of one column, 8 of two or 4 of up to four columns,
+// 16 columns of one piece beyond - so a reduction costs a few memory latencies, not one per
+// piece (a decode call's unit of 56 K tiles split over ~10 CTAs reduces in one batch).  n and
+// np are uniform across the warp (emit may use warp shuffles); n == 0 emits nothing.
+template <typename Base, typename Emit>
+static __device__ __forceinline__ void reduce_pieces(int np, int n, size_t col_stride,
+                                                     size_t gate_off, Base base, Emit emit) {
+  if (n <= 0) return;
+  if (n <= 1) {
+    reduce_pieces_small<16, 1>(np, n, col_stride, gate_off, base, emit);
+    return;
+  }
+  if (n <= 2) {
+    reduce_pieces_small<8, 2>(np, n, col_stride, gate_off, base, emit);
+    return;
+  }
+  if (n <= 4) {
+    reduce_pieces_small<4, 4>(np, n, col_stride, gate_off, base, emit);
     return;
   }
   for (int c0 = 0; c0 < n; c0 += 16) {
@@ -221,20 +243,19 @@ static __device__ __forceinline__ void reduce_pieces(int np, int n, size_t col_s
     for (int j = 0; j < 16; ++j) up[j] = gt[j] = 0.f;
     for (int q = 0; q < np; ++q) {
       const float* bq = base(q);
-      if (bq == nullptr) continue;
       float a[16], b[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const bool in = c0 + j < n;
-        const float* pp = in ? bq + (size_t)(c0 + j) * col_stride : nullptr;
-        a[j] = in ? __ldcg(pp) : 0.f;
-        b[j] = in ? __ldcg(pp + gate_off) : 0.f;
+        const float* pp = bq + (size_t)min(c0 + j, n - 1) * col_stride;
+        a[j] = __ldcg(pp);
+        b[j] = __ldcg(pp + gate_off);
       }
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        up[j] += a[j];
-        gt[j] += b[j];
-      }
+      for (int j = 0; j < 16; ++j)
+        if (c0 + j < n) {
+          up[j] += a[j];
+          gt[j] += b[j];
+        }
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j)

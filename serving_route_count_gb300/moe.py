@@ -37,6 +37,8 @@ class MoEError(RuntimeError):
 
 def _check(st: int, where: str):
     if st != 0:
+        if st == 6:   # MOE_ERR_CUDA: name the CUDA error behind it
+            where = f"{where} ({_lib.load().moe_last_cuda_error().decode()})"
         raise MoEError(st, where)
 
 

@@ -26,6 +26,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert "sm_103a" in moe.moe_version()
+    assert _lib.load().moe_last_cuda_error().decode() == "cudaSuccess"
     assert moe.moe_status_str(0) == "ok"
     assert "capacity" in moe.moe_status_str(4)
 
