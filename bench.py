@@ -7,10 +7,10 @@ Metric: tokens/s (valid rows per second of layer time).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--det]
 
-Timing: every layer call is a CUDA graph replay bracketed by CUDA events on the launching
-stream; before each call (outside the events) a 512 MB buffer is written to flush L2, and the
-routing set rotates over 8 pre-generated sets per M.  The step time is the sum of its calls'
-event times.  The dominant kernel is timed by event-record nodes inside the same graphs.
+Timing: every layer call is a CUDA graph replay whose kernels run between two event-record
+nodes of the same graph; before them (outside the events) a 512 MB buffer is written and
+another 512 MB read, which flushes L2 and leaves it clean; the routing set rotates over 8
+pre-generated sets per M.  The step time is the sum of its calls' event times.  The dominant kernel is timed by event-record nodes inside the same graphs.
 Under torchrun each rank runs the same workload on its own GPU (replicas; weak scaling);
 rank 0 prints one JSON line with the max time over ranks.
 """
@@ -60,6 +60,22 @@ def parse():
     p.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--sample-m", type=str, default="1,2", help=argparse.SUPPRESS)
     return p.parse_args()
+
+
+class L2Flush:
+    """Before each timed call: write a 512 MB buffer (larger than the 129 MB L2, so nothing the
+    call reads is left in L2), then read a second 512 MB buffer, so that the lines L2 holds when
+    the call starts are clean: otherwise the call's own reads would first have to write back
+    the ~100 MB of dirty lines the flush left (measured: 3-9 us per decode call), a cost of the
+    flush, not of the layer."""
+
+    def __init__(self, torch):
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.r = torch.ones(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def __call__(self, v=1):
+        self.w.fill_(v & 0xFF)
+        return self.r.amax()
 
 
 def valid_rows(ids):
@@ -310,7 +326,7 @@ def prefill_report(stream, flush, hbm_peak):
         ts = []
         for c in range(7):
             with torch.cuda.stream(stream):
-                flush.fill_(c)
+                flush(c)
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record(stream)
@@ -376,7 +392,7 @@ def modes_report(stream, flush, hbm_peak):
             ts = []
             for c in range(6):
                 with torch.cuda.stream(stream):
-                    flush.fill_(c)
+                    flush(c)
                     a = torch.cuda.Event(enable_timing=True)
                     b = torch.cuda.Event(enable_timing=True)
                     a.record(stream)
@@ -430,8 +446,7 @@ def our_arm(args, rank, world):
         in_graph_events = True
     except TypeError:
         in_graph_events = False
-    flush_graph = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda") if in_graph_events \
-        else None
+    flush_graph = L2Flush(torch) if in_graph_events else None
     calls = []   # (M, set, graph, x, ids, w, out, prof_events, tokens, distinct)
     for M in m_list:
         for s in range(N_ROUTING_SETS):
@@ -462,7 +477,7 @@ def our_arm(args, rank, world):
                 c["eb"] = torch.cuda.Event(enable_timing=True, external=True)
             with torch.cuda.graph(g, stream=stream):
                 if in_graph_events:
-                    flush_graph.fill_(1)
+                    flush_graph()
                     c["ea"].record(stream)
                 layer(c["x"], c["ids"], c["w"], c["out"])
                 if in_graph_events:
@@ -475,7 +490,7 @@ def our_arm(args, rank, world):
             c["graph_ev"] = g
             moe_plan_set_profile_events(layer.plan, [])
     torch.cuda.synchronize()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(torch)
 
     def step(si, stage_events=False):
         """One ladder pass; with stage_events the instrumented graphs run and the fc1 stage
@@ -489,7 +504,7 @@ def our_arm(args, rank, world):
                     c["graph"].replay()          # flush + events inside the graph
                     pairs.append((c["ea"], c["eb"], c))
                     continue
-                flush.fill_(si & 0xFF)
+                flush(si)
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record(stream)
@@ -551,7 +566,7 @@ def our_arm(args, rank, world):
     e2e_steps = max(3, args.steps // 2)
     for _ in range(e2e_steps):
         for xh, ih, wh, oh, tk in host:
-            flush.fill_(1)
+            flush()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             layer.run_host(xh, ih, wh, oh, stream=stream)
@@ -586,13 +601,14 @@ def our_arm(args, rank, world):
                         "padding, swiglu limit 7",
             "combine": "deterministic" if args.det else "atomic",
             "tokens_per_step": toks // args.steps,
-            "timing": ("CUDA graph per call: a 512 MB write (L2 flush), then the layer's "
-                       "kernels between two event-record nodes (device time of the call, "
-                       "without the host's graph launch); 8 routing sets rotated per M"
+            "timing": ("CUDA graph per call: L2 flush (a 512 MB write, then a 512 MB read so "
+                       "the L2 lines are clean), then the layer's kernels between two "
+                       "event-record nodes (device time of the call, without the host's graph "
+                       "launch); 8 routing sets rotated per M"
                        if in_graph_events else
-                       "CUDA graph per call, CUDA events around each replay; L2 flushed by a "
-                       "512 MB write before each call (outside the events); 8 routing sets "
-                       "rotated per M"),
+                       "CUDA graph per call, CUDA events around each replay; L2 flushed (512 MB "
+                       "write, then 512 MB read) before each call, outside the events; 8 "
+                       "routing sets rotated per M"),
             "parallelism": f"replicas x{world}",
         },
         "roofline": {

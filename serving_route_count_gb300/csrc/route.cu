@@ -421,8 +421,10 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
   constexpr int NW = kSmallRouteThreads / 32;
   __shared__ int s_ids[kSmallRouteSlots];
   __shared__ int s_perm[kSmallRouteSlots];
-  __shared__ int s_cnt[kMaxRouteExperts];
   __shared__ int s_warp[32];
+  // per-expert counts, sized to E by the launch: a small footprint lets this kernel's CTAs sit
+  // beside two CTAs of the next kernel (which launches as soon as this one starts) on an SM
+  extern __shared__ int s_cnt[];
   const int tid = threadIdx.x;
   const bool writer = blockIdx.x == 0;
   pdl_wait_prev();
@@ -801,8 +803,8 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_fi
                                      152 * 4);
   if (blocks < 1) blocks = 1;
   // first kernel of a call: an ordinary launch (the previous call may still read the tables)
-  return launch_kernel(route_actq_small_kernel, dim3(blocks), dim3(kSmallRouteThreads), 0, st,
-                       false, ids, Mk, E, tile_slots, max_tiles,
+  return launch_kernel(route_actq_small_kernel, dim3(blocks), dim3(kSmallRouteThreads),
+                       (size_t)E * sizeof(int), st, false, ids, Mk, E, tile_slots, max_tiles,
                        reinterpret_cast<const __nv_bfloat16*>(x), H, topk, r.cnt, r.off, r.perm,
                        r.slot_of, r.tiles, r.ctrl, (to_f16 || nv4) ? nullptr : r.xq,
                        (to_f16 || nv4) ? nullptr : r.xs,
