@@ -202,6 +202,12 @@ moe_status moe_plan_set_router_weight_on_input(moe_plan_t* plan, int on);
  * Errors: MOE_ERR_ARG (plan NULL, first_expert < 0 or first_expert + E > INT32_MAX). */
 moe_status moe_plan_set_expert_offset(moe_plan_t* plan, int first_expert);
 
+/* Test hook: on = 1 makes small W4A8 calls (at most 256 flat slots, tiles of <= 32 tokens),
+ * whose fc1 quantises the activations itself stage by stage, also store the MXFP8 codes and
+ * scales where moe_debug_actq reads them (other calls always do).  Default 0.
+ * Errors: MOE_ERR_ARG. */
+moe_status moe_plan_set_debug_copies(moe_plan_t* plan, int on);
+
 /* Size in bytes of the device scratch buffer moe_run needs (routing tables, quantised
  * activations, the fc1 -> fc2 intermediate, the combine buffer). */
 moe_status moe_scratch_bytes(const moe_plan_t* plan, size_t* bytes);
@@ -289,7 +295,8 @@ moe_status moe_unprepare_weights(const moe_weight_plan* wp, const moe_prepared* 
 moe_status moe_get_device_error(const moe_plan_t* plan, void* scratch, void* stream, int* code);
 
 /* Test hooks: after a moe_run on `stream`, copy routing tables / quantised activations of the
- * last call to host buffers (synchronises).  cnt [E], off [E+1], perm [S], slot_of [M*topk]
+ * last call to host buffers (synchronises; the activations of small W4A8 calls only with
+ * moe_plan_set_debug_copies on).  cnt [E], off [E+1], perm [S], slot_of [M*topk]
  * where S = off[E]; xq [S, H] E4M3 codes, xs [S, H/32] E8M0 bytes (W4A8 only), row p holding
  * the quantised row of token perm[p] / topk (buffers of M*topk rows suffice). */
 moe_status moe_debug_routing(const moe_plan_t* plan, void* scratch, int M, int32_t* cnt,

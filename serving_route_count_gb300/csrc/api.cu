@@ -8,6 +8,7 @@
 
 #include "moe_common.cuh"
 #include "tc_sched.cuh"
+#include "tc_tile.cuh"
 #include "../../include/moe_gb300.h"
 
 namespace moe {
@@ -31,20 +32,20 @@ cudaError_t launch_actq_rows(const void* x, int M, int H, int topk, const RunPtr
 cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_first,
                                     int tile_slots, int max_tiles, const void* x, int H, int topk,
                                     const RunPtrs& r, bool atoms, bool to_f16, const float* win,
-                                    const float* ag, bool nv4, void* z0, size_t z0_words,
-                                    void* z1, size_t z1_words, void* z2, size_t z2_words,
-                                    cudaStream_t st);
+                                    const float* ag, bool nv4, bool skip_x, void* z0,
+                                    size_t z0_words, void* z1, size_t z1_words, void* z2,
+                                    size_t z2_words, cudaStream_t st);
 // gemm_tc.cu
 cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                             int bn, int tiles, int splits, const float* topk_w, int M,
-                            const int32_t* ids, int max_tiles, cudaStream_t st);
+                            const int32_t* ids, int max_tiles, const void* x, cudaStream_t st);
 int tc_pick_bn(int M, int topk, int E, bool w4a8);
 // gemm_tc_persist.cu
 bool fc1_stream_preferred(int bn, int units);
 size_t fc1_stream_part_bytes();
 cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanDims& d, int bn,
                               int M, float* part, int32_t* tickets, const int32_t* ids,
-                              int max_tiles, cudaStream_t st);
+                              int max_tiles, const void* x, cudaStream_t st);
 bool fc2_persist_preferred(int bn, int units);
 cudaError_t launch_fc2_persist(const DevWeights& w, const RunPtrs& r, const PlanDims& d, int bn,
                                int M, const float* topk_w, cudaStream_t st);
@@ -378,7 +379,7 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   d.E = E; d.H = H; d.I = I; d.Ip = (int)align_up((size_t)I, 128); d.topk = topk; d.max_m = max_m;
   d.quant = quant_mode; d.deterministic = deterministic ? 1 : 0;
   d.limit = swiglu_limit; d.alpha = 1.f; d.beta = 0.f; d.backend = 0; d.fc1_kernel = 0;
-  d.ep_first = 0; d.w_on_input = 0;
+  d.ep_first = 0; d.w_on_input = 0; d.keep_act = 0;
   const size_t Sm = (size_t)max_m * topk;
   Scratch& s = p->s;
   s.max_tiles = (int)std::min<size_t>(Sm, (Sm + kSimtSlots - 1) / kSimtSlots +
@@ -532,6 +533,12 @@ moe_status moe_plan_set_router_weight_on_input(moe_plan_t* plan, int on) {
   return MOE_OK;
 }
 
+moe_status moe_plan_set_debug_copies(moe_plan_t* plan, int on) {
+  if (plan == nullptr || (on != 0 && on != 1)) return MOE_ERR_ARG;
+  plan->d.keep_act = on;
+  return MOE_OK;
+}
+
 moe_status moe_plan_set_expert_offset(moe_plan_t* plan, int first_expert) {
   if (plan == nullptr || first_expert < 0 || first_expert > INT32_MAX - plan->d.E)
     return MOE_ERR_ARG;
@@ -607,6 +614,9 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   // the W4A8 tensor-core kernels (16/32-token tiles) read activation-scale atoms from prepared
   // rows
   const bool atoms = tc8;
+  // small W4A8 calls at tile widths <= 32: fc1 quantises the activations itself (the kernels
+  // route in shared memory and know each tile's tokens), the routing launch only routes
+  const bool fuse_x = tc8 && small && Sm <= kPreRouteSlots && bn <= 32;
   void* acc = d.deterministic ? nullptr : r.acc;
   const size_t acc_words = d.deterministic ? 0 : (size_t)M * d.H;
   void* g = nullptr;            // split partials are fully written before they are read
@@ -621,8 +631,8 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   cudaError_t e;
   if (small) {
     e = launch_route_actq_small(topk_ids, Sm, d.E, d.ep_first, bn, plan->s.max_tiles, x, d.H,
-                                d.topk, r, atoms, t16, win, w.ag13, t4, acc, acc_words, g,
-                                g_words, tk, tk_words, st);
+                                d.topk, r, atoms, t16, win, w.ag13, t4, fuse_x, acc, acc_words,
+                                g, g_words, tk, tk_words, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
   } else if (tc8) {
@@ -649,10 +659,11 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
     if (t4)
       e = launch_tc4_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st);
     else if (streamk)
-      e = launch_fc1_stream(w, r, d, bn, M, r.part, r.tickets, topk_ids, plan->s.max_tiles, st);
+      e = launch_fc1_stream(w, r, d, bn, M, r.part, r.tickets, topk_ids, plan->s.max_tiles,
+                            fuse_x ? x : nullptr, st);
     else
       e = tc8 ? launch_tc_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, topk_ids,
-                                plan->s.max_tiles, st)
+                                plan->s.max_tiles, fuse_x ? x : nullptr, st)
               : launch_tc16_stage(0, w, r, d, bn, tiles, splits, topk_weights, M, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(3);
@@ -661,7 +672,8 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
     else if (tc8 && fc2_persist_preferred(bn, tiles * (d.H / 128)))
       e = launch_fc2_persist(w, r, d, bn, M, topk_weights, st);
     else
-      e = tc8 ? launch_tc_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, nullptr, 0, st)
+      e = tc8 ? launch_tc_stage(1, w, r, d, bn, tiles, 1, topk_weights, M, nullptr, 0, nullptr,
+                                st)
               : launch_tc16_stage(1, w, r, d, bn, tiles, 1, wcomb, M, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(4);

@@ -81,6 +81,13 @@ struct TcFc1Params {
   // routing launch (null: wait for its tables)
   const int32_t* ids;
   int Mk, E, max_tiles, ep_first;
+  // small calls at tile widths <= 32: the bf16 hidden states, which this kernel quantises to
+  // MXFP8 itself, stage by stage, into the MMA's activation operand (null: TMA loads of the
+  // routing launch's quantised rows); the codes of row block 0 are also stored to xq / xs
+  const __nv_bfloat16* x;
+  int topk;
+  uint8_t* xq;               // [Sm][H] E4M3 copy of the quantised activations (row block 0)
+  uint8_t* xs;               // [Sm][H/32] their E8M0 scales
 };
 
 struct TcFc2Params {
@@ -118,19 +125,30 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   __shared__ __align__(8) uint64_t full[S], empty[S], done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_last, s_fail;
+  __shared__ PreRouteInfo s_info;
+  __shared__ int s_tok[32];
+  // activations quantised here (small calls, tiles of at most 32 tokens)
+  const bool fused = BN <= 32 && p.x != nullptr && p.ids != nullptr;
 
   // Small calls route in shared memory (scratch in the last stage, before any copy lands
   // there), so the weights of the first stages are requested while the routing launch still
   // runs; larger calls wait for its tables.
-  int e_pre = -1, nt = 0;
+  int e_pre = -1, nt = 0, n_pre = 0, p0_pre = 0;
   if (p.ids != nullptr) {
     int* scratch = reinterpret_cast<int*>(smem + (S - 1) * Cfg::kStage1);
-    nt = min(pre_route_tiles<kTcThreads>(p.ids, p.Mk, p.E, p.ep_first, BN, scratch), p.max_tiles);
+    nt = min(pre_route_tiles<kTcThreads>(p.ids, p.Mk, p.E, p.ep_first, BN, scratch,
+                                         fused ? &s_info : nullptr),
+             p.max_tiles);
     if (tile >= nt) {
       pdl_wait_prev();
       return;
     }
     if (tile < kPreRouteTiles) e_pre = scratch[p.E + tile];
+    if (fused) {
+      n_pre = s_info.te[tile] >> 16;
+      p0_pre = s_info.tp[tile] & 0xFFFF;
+      if (warp == 2) pre_route_tile_tokens(s_info, tile, p.Mk, p.topk, BN, s_tok);
+    }
   } else {
     pdl_wait_prev();     // routing tables complete
     if (tile >= p.ctrl[1]) return;
@@ -142,7 +160,8 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   }
   if (tid == 32) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
+      // fused: the producer's arrival (weight bytes) and one per quantising warp
+      mbar_init(&full[s], fused ? 3 : 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(&done, 1);
@@ -150,7 +169,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
     fence_barrier_init();
   }
   if (tid == 64) prefetch_tmap(&p.tm_w13);
-  if (tid == 96) prefetch_tmap(&p.tm_x);
+  if (tid == 96 && !fused) prefetch_tmap(&p.tm_x);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -183,23 +202,38 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
     const uint64_t pol = l2_evict_first_policy();
     pre = nk < S ? nk : S;
     for (int i = 0; i < pre; ++i) {
-      mbar_expect_tx(&full[i], a_bytes + 2 * 512);
+      // fused: the weights are all the producer loads, so it arrives now
+      if (fused)
+        mbar_arrive_expect_tx(&full[i], a_bytes + 2 * 512);
+      else
+        mbar_expect_tx(&full[i], a_bytes + 2 * 512);
       load_a(stage(i), e_pre, kt0 + i, &full[i], pol);
     }
   }
-  pdl_wait_prev();             // routing tables and activations complete
-  // fc2 reads the routing tables before its own wait: it may launch only once every CTA of
-  // this kernel has seen them complete
-  pdl_launch_next();
-  // the shared-memory routing planned the same tiles as the routing launch (see checked_tile)
-  if (p.ids != nullptr && tid == 0 && tile == 0 && fb == 0 && split == 0 &&
-      nt != min(__ldcg(p.ctrl + 1), p.max_tiles))
-    set_error(p.err, kErrRouteBounds);
-  const int4 td = p.ids != nullptr ? checked_tile(p.tiles, p.ctrl, tile, p.E, p.Sm, BN, p.err)
-                                    : p.tiles[tile];
-  const int e = td.x, p0 = td.y, n = td.z;
+  int e, p0, n;
+  if (fused) {
+    // the tile as routed in shared memory; the routing launch's tables are only needed by the
+    // epilogue (split tickets), which waits for that launch
+    e = e_pre;
+    p0 = p0_pre;
+    n = n_pre;
+  } else {
+    pdl_wait_prev();           // routing tables and activations complete
+    // fc2 reads the routing tables before its own wait: it may launch only once every CTA of
+    // this kernel has seen them complete
+    pdl_launch_next();
+    // the shared-memory routing planned the same tiles as the routing launch (see checked_tile)
+    if (p.ids != nullptr && tid == 0 && tile == 0 && fb == 0 && split == 0 &&
+        nt != min(__ldcg(p.ctrl + 1), p.max_tiles))
+      set_error(p.err, kErrRouteBounds);
+    const int4 td = p.ids != nullptr ? checked_tile(p.tiles, p.ctrl, tile, p.E, p.Sm, BN, p.err)
+                                      : p.tiles[tile];
+    e = td.x;
+    p0 = td.y;
+    n = td.z;
+    if (pre > 0 && e != e_pre) set_error(p.err, kErrRouteBounds);
+  }
   const TileLoad<BN> tl(n);
-  if (pre > 0 && e != e_pre) set_error(p.err, kErrRouteBounds);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -211,6 +245,14 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
         if (!ok) break;
         uint8_t* st = stage(s);
         const int kt = kt0 + i;
+        if (fused) {
+          // the activations come from the quantising warps
+          if (i >= pre) {
+            mbar_arrive_expect_tx(&full[s], a_bytes + 2 * 512);
+            load_a(st, e, kt, &full[s], pol);
+          }
+          continue;
+        }
         if (i < pre) {
           mbar_arrive_expect_tx(&full[s], tl.b_bytes + tl.sf_bytes);
         } else {
@@ -223,6 +265,15 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
                   tl.sf_bytes, &full[s]);
       }
       issued = i;
+    }
+  } else if (fused && warp >= 2) {
+    // warps 2..3: each stage's activation operand, quantised from the bf16 rows of the tile's
+    // tokens (row block 0 also keeps a copy of the codes in xq / xs)
+    if constexpr (BN <= 32) {
+      const ActQuant<BN> aq{p.x, p.H, tid - 64};
+      ok = act_quant_run<BN, S>(aq, s_tok, n, kt0, nk, 0, smem, Cfg::kStage1, 2 * kTileBytesA,
+                                2 * kTileBytesA + Cfg::kB + 1024, full, empty,
+                                fb == 0 ? p.xq : nullptr, p.xs, p0, p.err);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -262,6 +313,17 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
 
   // ---- epilogue: all four warps, thread = weight row (feature), columns = tokens
   __syncwarp();
+  if (fused) {
+    pdl_wait_prev();           // routing launch complete: its tables and cleared tickets
+    pdl_launch_next();
+    // the shared-memory routing planned the same tiles as the routing launch (see checked_tile)
+    if (tid == 0) {
+      if (tile == 0 && fb == 0 && split == 0 && nt != min(__ldcg(p.ctrl + 1), p.max_tiles))
+        set_error(p.err, kErrRouteBounds);
+      const int4 td = checked_tile(p.tiles, p.ctrl, tile, p.E, p.Sm, BN, p.err);
+      if (td.x != e || td.y != p0 || td.z != n) set_error(p.err, kErrRouteBounds);
+    }
+  }
   ok = mbar_wait(&done, 0, p.err) && ok;
   tc_fence_after();
   __syncwarp();
@@ -584,7 +646,8 @@ static cudaError_t launch_fc2_bn(const TcFc2Params& p, int tiles, cudaStream_t s
 // fc1 (stage 0) or fc2 (stage 1) of the W4A8 tensor-core path.
 cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                             int bn, int tiles, int splits, const float* topk_w, int M,
-                            const int32_t* ids, int max_tiles, cudaStream_t st) {
+                            const int32_t* ids, int max_tiles, const void* x,
+                            cudaStream_t st) {
   const int Sm = M * d.topk;
   const int RT = cdiv(d.I, 128);
   if (stage == 0) {
@@ -604,6 +667,11 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
     p.splits = splits; p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
     p.ids = (ids != nullptr && Sm <= kPreRouteSlots) ? ids : nullptr;
     p.Mk = Sm; p.E = d.E; p.max_tiles = max_tiles; p.ep_first = d.ep_first;
+    // quantised here only when the call routes in shared memory at a width of <= 32 tokens
+    p.x = (p.ids != nullptr && bn <= 32) ? static_cast<const __nv_bfloat16*>(x) : nullptr;
+    p.topk = d.topk;
+    p.xq = d.keep_act ? r.xq : nullptr;
+    p.xs = r.xs;
     switch (bn) {
       case 16: return launch_fc1_bn<16>(p, tiles, st);
       case 32: return launch_fc1_bn<32>(p, tiles, st);

@@ -64,7 +64,20 @@ struct StreamFc1Params {
   // routing launch (null: wait for its tables)
   const int32_t* ids;
   int Mk, E, max_tiles, ep_first;
+  // the bf16 hidden states, quantised to MXFP8 here stage by stage into the MMA's activation
+  // operand (null: TMA loads of the routing launch's quantised rows); row block 0's codes are
+  // also stored to xq / xs
+  const __nv_bfloat16* x;
+  int topk;
+  uint8_t* xq;
+  uint8_t* xs;
 };
+
+// A stage whose weights were requested before the routing was known for certain must be of the
+// expert the stage turned out to need.
+static __device__ __forceinline__ bool pre_e_check(int i, int pre, const int* pre_e, int e) {
+  return i < pre && pre_e[i] != e;
+}
 
 template <int BN>
 __global__ void __launch_bounds__(kStreamThreads)
@@ -79,6 +92,10 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   __shared__ uint32_t s_tmem;
   __shared__ int s_last, s_fail, s_npieces;
   __shared__ int s_pieces[kStreamMaxPieces];
+  __shared__ PreRouteInfo s_info;
+  __shared__ int s_tok[2][BN];      // each quantising warp's copy of its tile's token list
+  // activations quantised here (the shared-memory routing knows each tile's tokens)
+  const bool fused = p.x != nullptr && p.ids != nullptr;
 
   // Small calls route in shared memory (scratch in the last stage, before any copy lands
   // there), so the weights of the first stages are requested while the routing launch still
@@ -86,7 +103,9 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   int* scratch = reinterpret_cast<int*>(smem + (S - 1) * Cfg::kStage);
   int n_tiles;
   if (p.ids != nullptr) {
-    n_tiles = min(pre_route_tiles<kStreamThreads>(p.ids, p.Mk, p.E, p.ep_first, BN, scratch), p.max_tiles);
+    n_tiles = min(pre_route_tiles<kStreamThreads>(p.ids, p.Mk, p.E, p.ep_first, BN, scratch,
+                                                  fused ? &s_info : nullptr),
+                  p.max_tiles);
   } else {
     pdl_wait_prev();     // routing tables complete
     n_tiles = p.ctrl[1];
@@ -116,7 +135,8 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   }
   if (tid == 32) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
+      // fused: the producer's arrival (weight bytes) and one per quantising warp
+      mbar_init(&full[s], fused ? 3 : 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -171,16 +191,34 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
           pre = i;
           break;
         }
-        load_a(stage(i), pre_e[i], fb, kt, &full[i], pol, true);
+        if (fused) {
+          // the weights are all the producer loads: it arrives now
+          const uint32_t ab = (fb < p.RTf ? 2 * kTxBytesA : 2 * p.rem * 64) + 2 * 512;
+          mbar_arrive_expect_tx(&full[i], ab);
+          load_a(stage(i), pre_e[i], fb, kt, &full[i], pol, false);
+        } else {
+          load_a(stage(i), pre_e[i], fb, kt, &full[i], pol, true);
+        }
       }
     }
   }
-  pdl_wait_prev();     // routing tables and activations complete
-  // fc2 reads the routing tables before its own wait: it may launch only once every CTA of
-  // this kernel has seen them complete
-  pdl_launch_next();
-  // the shared-memory routing planned the same tiles as the routing launch (see checked_tile)
-  if (tid == 0 && n_tiles != min(__ldcg(p.ctrl + 1), p.max_tiles)) set_error(p.err, kErrRouteBounds);
+  if (!fused) {
+    pdl_wait_prev();   // routing tables and activations complete
+    // fc2 reads the routing tables before its own wait: it may launch only once every CTA of
+    // this kernel has seen them complete
+    pdl_launch_next();
+    // the shared-memory routing planned the same tiles as the routing launch (see checked_tile)
+    if (tid == 0 && n_tiles != min(__ldcg(p.ctrl + 1), p.max_tiles))
+      set_error(p.err, kErrRouteBounds);
+  }
+  // a tile's (expert, first slot position, tokens): the shared-memory routing when fused (the
+  // routing launch's tables are read only by the epilogue warps, after waiting for it)
+  auto tile_of = [&](int tile) -> int4 {
+    if (fused)
+      return make_int4(s_info.te[tile] & 0xFFFF, s_info.tp[tile] & 0xFFFF, s_info.te[tile] >> 16,
+                       0);
+    return checked_tile(p.tiles, p.ctrl, tile, p.E, p.Sm, BN, p.err);
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -192,7 +230,7 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
         const int tile = u / p.RT, fb = u - tile * p.RT;
         if (tile != cur_tile) {
           cur_tile = tile;
-          const int4 td = checked_tile(p.tiles, p.ctrl, tile, p.E, p.Sm, BN, p.err);
+          const int4 td = tile_of(tile);
           e = td.x;
           p0 = td.y;
         }
@@ -201,6 +239,15 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
           if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
           if (!ok) break;
           uint8_t* st = stage(s);
+          if (fused) {
+            if (pre_e_check(i, pre, pre_e, e)) set_error(p.err, kErrRouteBounds);
+            if (i >= pre) {
+              const uint32_t ab = (fb < p.RTf ? 2 * kTxBytesA : 2 * p.rem * 64) + 2 * 512;
+              mbar_arrive_expect_tx(&full[s], ab);
+              load_a(st, e, fb, kt, &full[s], pol, false);
+            }
+            continue;
+          }
           if (i < pre) {
             if (pre_e[i] != e) set_error(p.err, kErrRouteBounds);
             mbar_arrive_expect_tx(&full[s], Cfg::kB + BN * 16);
@@ -217,6 +264,27 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
         }
       }
       issued = i;
+    }
+  } else if (fused && (warp == 2 || warp == 3)) {
+    // warps 2..3: each stage's activation operand, quantised from the bf16 rows of the tile's
+    // tokens (units of row block 0 also keep a copy of the codes in xq / xs)
+    const ActQuant<BN> aq{p.x, p.H, tid - 64};
+    int i = 0, cur_tile = -1, n = 0, p0 = 0;
+    auto sg = wk.segs();
+    int u, k0, len;
+    while (ok && sg.next(u, k0, len)) {
+      const int tile = u / p.RT, fb = u - tile * p.RT;
+      if (tile != cur_tile) {
+        // the new tile's token list, each warp its own copy (no barrier between the two)
+        pre_route_tile_tokens(s_info, tile, p.Mk, p.topk, BN, s_tok[warp - 2]);
+        cur_tile = tile;
+        n = s_info.te[tile] >> 16;
+        p0 = s_info.tp[tile] & 0xFFFF;
+      }
+      ok = act_quant_run<BN, S>(aq, s_tok[warp - 2], n, k0, len, i, smem, Cfg::kStage,
+                                2 * kTileBytesA, 2 * kTileBytesA + Cfg::kB + 1024, full, empty,
+                                fb == 0 ? p.xq : nullptr, p.xs, p0, p.err);
+      i += len;
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -255,6 +323,12 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
       }
     }
   } else if (warp >= 4) {
+    if (fused) {
+      pdl_wait_prev();   // routing launch complete: its tables and cleared tickets
+      pdl_launch_next();
+      if (tid == 128 && n_tiles != min(__ldcg(p.ctrl + 1), p.max_tiles))
+        set_error(p.err, kErrRouteBounds);
+    }
     const int quad = warp & 3;
     const int row = quad * 32 + lane;                         // weight row within the block
     int j = 0;
@@ -263,7 +337,12 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
     for (; sg.next(u, k0, len); ++j) {
       const int k1 = k0 + len;
       const int tile = u / p.RT, fb = u - tile * p.RT;
-      const int4 td = checked_tile(p.tiles, p.ctrl, tile, p.E, p.Sm, BN, p.err);
+      const int4 td = tile_of(tile);
+      if (fused && tid == 128) {
+        // the routing launch's record of the tile is the one routed here
+        const int4 rt = checked_tile(p.tiles, p.ctrl, tile, p.E, p.Sm, BN, p.err);
+        if (rt.x != td.x || rt.y != td.y || rt.z != td.z) set_error(p.err, kErrRouteBounds);
+      }
       const int p0 = td.y, n = td.z;
       const int f = fb * 128 + row;
       const int b = j & 1;
@@ -628,7 +707,7 @@ size_t fc1_stream_part_bytes() { return (size_t)2 * kStreamMaxCtas * 2 * 16 * 12
 
 cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanDims& d, int bn,
                               int M, float* part, int32_t* tickets, const int32_t* ids,
-                              int max_tiles, cudaStream_t st) {
+                              int max_tiles, const void* x, cudaStream_t st) {
   if (bn != 16) return cudaErrorInvalidValue;
   StreamFc1Params p;
   memset(&p, 0, sizeof(p));
@@ -648,6 +727,10 @@ cudaError_t launch_fc1_stream(const DevWeights& w, const RunPtrs& r, const PlanD
   p.limit = d.limit; p.alpha = d.alpha; p.beta = d.beta;
   p.ids = (ids != nullptr && Sm <= kPreRouteSlots) ? ids : nullptr;
   p.Mk = Sm; p.E = d.E; p.max_tiles = max_tiles; p.ep_first = d.ep_first;
+  p.x = p.ids != nullptr ? static_cast<const __nv_bfloat16*>(x) : nullptr;
+  p.topk = d.topk;
+  p.xq = d.keep_act ? r.xq : nullptr;
+  p.xs = r.xs;
   static const int G = persistent_grid(fc1_stream_kernel<16>, StreamCfg<16>::kSmem,
                                        StreamCfg<16>::kAlloc, 2, kStreamMaxCtas);
   return launch_kernel(fc1_stream_kernel<16>, dim3(G), dim3(kStreamThreads), StreamCfg<16>::kSmem,

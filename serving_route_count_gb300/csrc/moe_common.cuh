@@ -175,6 +175,8 @@ struct PlanDims {
   int w_on_input;   // 16-bit paths: router weights scale fc1's input, the combine is unweighted
   int ep_first;     // global id of local expert 0; router ids outside [ep_first, ep_first + E)
                     // belong to other ranks and are dropped
+  int keep_act;     // test hook: small W4A8 calls, whose fc1 quantises the activations itself,
+                    // also store the codes where moe_debug_actq reads them
 };
 
 // Local id of router id `id` on a plan that owns the global experts [first, first + E): id -
@@ -253,6 +255,33 @@ __device__ __forceinline__ uint32_t f32_to_e4m3(float a) {
 }
 
 __device__ __forceinline__ void set_error(int32_t* ctrl, int bit) { atomicOr(ctrl, bit); }
+
+// One block of 32 bf16 activations (four 16-byte words, element 2j of a word in its low half)
+// -> 32 E4M3 codes (eight words, element 4j + b in byte b of word j) and the E8M0 scale byte
+// (OCP MX rule: scale = 2^(floor(log2 amax) - 8); codes round to nearest even and saturate).
+__device__ __forceinline__ uint32_t mxfp8_block32(const uint4* u, uint32_t* packed) {
+  float v[32];
+#pragma unroll
+  for (int qq = 0; qq < 4; ++qq) {
+    const uint32_t w[4] = {u[qq].x, u[qq].y, u[qq].z, u[qq].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[qq * 8 + 2 * j] = __uint_as_float(w[j] << 16);
+      v[qq * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  const uint32_t s = mx_scale_byte(amax);
+  const float inv = e8m0_inv_f32(s);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    packed[j] = f32_to_e4m3(v[4 * j] * inv) | (f32_to_e4m3(v[4 * j + 1] * inv) << 8) |
+                (f32_to_e4m3(v[4 * j + 2] * inv) << 16) | (f32_to_e4m3(v[4 * j + 3] * inv) << 24);
+  }
+  return s;
+}
 
 // ----------------------------------------------------------------------------------------------
 // Chained launches (programmatic dependent launch)

@@ -184,28 +184,9 @@ __device__ __forceinline__ uint32_t quantize_block32(const __nv_bfloat16* __rest
                                                      uint8_t* __restrict__ q,
                                                      uint8_t* __restrict__ s8) {
   const uint4* src = reinterpret_cast<const uint4*>(src_bf16);
-  float v[32];
-#pragma unroll
-  for (int qq = 0; qq < 4; ++qq) {
-    uint4 u = src[qq];
-    uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[qq * 8 + 2 * j] = __uint_as_float(w[j] << 16);
-      v[qq * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-    }
-  }
-  float amax = 0.f;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
-  const uint32_t s = mx_scale_byte(amax);
-  const float inv = e8m0_inv_f32(s);
+  const uint4 u[4] = {src[0], src[1], src[2], src[3]};
   uint32_t packed[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    packed[j] = f32_to_e4m3(v[4 * j] * inv) | (f32_to_e4m3(v[4 * j + 1] * inv) << 8) |
-                (f32_to_e4m3(v[4 * j + 2] * inv) << 16) | (f32_to_e4m3(v[4 * j + 3] * inv) << 24);
-  }
+  const uint32_t s = mxfp8_block32(u, packed);
   uint4* dst = reinterpret_cast<uint4*>(q);
   dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
   dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
@@ -793,11 +774,14 @@ bool route_actq_small_supported(int Mk, int E) {
 cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_first,
                                     int tile_slots, int max_tiles, const void* x, int H,
                                     int topk, const RunPtrs& r, bool atoms, bool to_f16,
-                                    const float* win, const float* ag, bool nv4, void* z0,
-                                    size_t z0_words, void* z1, size_t z1_words, void* z2,
-                                    size_t z2_words, cudaStream_t st) {
+                                    const float* win, const float* ag, bool nv4, bool skip_x,
+                                    void* z0, size_t z0_words, void* z1, size_t z1_words,
+                                    void* z2, size_t z2_words, cudaStream_t st) {
   if (!route_actq_small_supported(Mk, E)) return cudaErrorInvalidValue;
-  const size_t work = std::max((size_t)Mk * (to_f16 ? H / 8 : (nv4 ? H / 16 : H / 32)),
+  // skip_x: the consumer quantises the activations itself (W4A8 only), this launch routes and
+  // clears
+  const size_t act_work = skip_x ? 0 : (size_t)Mk * (to_f16 ? H / 8 : (nv4 ? H / 16 : H / 32));
+  const size_t work = std::max(act_work,
                                std::max(z0_words / 4, std::max(z1_words / 4, z2_words / 4)));
   int blocks = (int)std::min<size_t>((work + kSmallRouteThreads - 1) / kSmallRouteThreads,
                                      152 * 4);
@@ -806,9 +790,9 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_fi
   return launch_kernel(route_actq_small_kernel, dim3(blocks), dim3(kSmallRouteThreads),
                        (size_t)E * sizeof(int), st, false, ids, Mk, E, tile_slots, max_tiles,
                        reinterpret_cast<const __nv_bfloat16*>(x), H, topk, r.cnt, r.off, r.perm,
-                       r.slot_of, r.tiles, r.ctrl, (to_f16 || nv4) ? nullptr : r.xq,
-                       (to_f16 || nv4) ? nullptr : r.xs,
-                       (atoms && !to_f16 && !nv4) ? r.xs16 : nullptr, r.r16,
+                       r.slot_of, r.tiles, r.ctrl, (to_f16 || nv4 || skip_x) ? nullptr : r.xq,
+                       (to_f16 || nv4 || skip_x) ? nullptr : r.xs,
+                       (atoms && !to_f16 && !nv4 && !skip_x) ? r.xs16 : nullptr, r.r16,
                        to_f16 ? r.x16 : nullptr, to_f16 ? win : nullptr,
                        (to_f16 || nv4) ? ag : nullptr, nv4 ? r.xq : nullptr,
                        nv4 ? r.xs16 : nullptr, ZeroRegion{z0, z0_words},

@@ -77,56 +77,211 @@ static __device__ __forceinline__ void write_act_sf_rows(uint8_t* dst, const uin
 // router ids alone.
 // A kernel chained behind the routing launch may read the ids before waiting for it (the ids
 // were complete when the routing launch passed its own wait), so it can request weights early.
-// scratch: (E + kPreRouteTiles + 32) ints of shared memory; on return scratch[E + t] is the
-// expert of tile t for t < min(tiles, kPreRouteTiles).  Every thread of the CTA (NT threads)
+// scratch: (E + kPreRouteTiles + 64) ints of shared memory; on return scratch[E + t] is the
+// expert of tile t for t < min(tiles, kPreRouteTiles).  With `info` (PreRouteInfo, the kernel's
+// own shared memory) it also keeps, per tile, its expert, token count, first slot position and
+// index among its expert's tiles, and per flat slot the local expert id (-1 when dropped): what
+// a kernel needs to gather the tile's activations itself.  Every thread of the CTA (NT threads)
 // calls it; returns the tile count.
 constexpr int kPreRouteSlots = 256;   // calls of at most this many flat slots
 constexpr int kPreRouteTiles = 256;
+struct PreRouteInfo {
+  int te[kPreRouteTiles];             // expert | (token count << 16)
+  int tp[kPreRouteTiles];             // first slot position | (index within the expert << 16)
+  int16_t lid[kPreRouteSlots];        // local expert of each flat slot, -1 when dropped
+};
 template <int NT>
 static __device__ int pre_route_tiles(const int32_t* ids, int Mk, int E, int ep_first,
-                                      int tile_slots, int* scratch) {
+                                      int tile_slots, int* scratch,
+                                      PreRouteInfo* info = nullptr) {
   int* s_cnt = scratch;
   int* s_tile_e = scratch + E;
-  int* s_red = scratch + E + kPreRouteTiles;
+  int* s_red = scratch + E + kPreRouteTiles;       // [0, 32): tiles, [32, 64): slots per warp
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int e = tid; e < E; e += NT) s_cnt[e] = 0;
   __syncthreads();
   for (int f = tid; f < Mk; f += NT) {
     const int e = local_expert(__ldcg(ids + f), ep_first, E);
     if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+    if (info != nullptr) info->lid[f] = (int16_t)((e >= 0 && e < E) ? e : -1);
   }
   __syncthreads();
   const int per = (E + NT - 1) / NT;        // thread t: experts [t*per, t*per + per)
-  int lt = 0;
+  int lt = 0, ls = 0;
   for (int i = 0; i < per; ++i) {
     const int e = tid * per + i;
-    if (e < E) lt += (s_cnt[e] + tile_slots - 1) / tile_slots;
+    if (e < E) {
+      lt += (s_cnt[e] + tile_slots - 1) / tile_slots;
+      ls += s_cnt[e];
+    }
   }
-  // exclusive scan of the per-thread tile counts
-  int incl = lt;
+  // exclusive scans of the per-thread tile and slot counts
+  int incl = lt, incs = ls;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
+    const int z = __shfl_up_sync(0xffffffffu, incs, o);
+    if (lane >= o) {
+      incl += y;
+      incs += z;
+    }
   }
-  if (lane == 31) s_red[warp] = incl;
+  if (lane == 31) {
+    s_red[warp] = incl;
+    s_red[32 + warp] = incs;
+  }
   __syncthreads();
-  int before = 0, total = 0;
+  int before = 0, total = 0, before_s = 0;
   for (int w = 0; w < NT / 32; ++w) {
     before += w < warp ? s_red[w] : 0;
+    before_s += w < warp ? s_red[32 + w] : 0;
     total += s_red[w];
   }
-  int t = before + incl - lt;
+  int t = before + incl - lt, pos = before_s + incs - ls;
   for (int i = 0; i < per; ++i) {
     const int e = tid * per + i;
     if (e >= E) break;
-    for (int c = s_cnt[e]; c > 0; c -= tile_slots, ++t)
-      if (t < kPreRouteTiles) s_tile_e[t] = e;
+    const int c = s_cnt[e];
+    for (int j = 0; j * tile_slots < c; ++j, ++t) {
+      if (t < kPreRouteTiles) {
+        s_tile_e[t] = e;
+        if (info != nullptr) {
+          info->te[t] = e | (min(tile_slots, c - j * tile_slots) << 16);
+          info->tp[t] = (pos + j * tile_slots) | (j << 16);
+        }
+      }
+    }
+    pos += c;
   }
   // the scratch lies in a pipeline stage that TMA writes next
   fence_proxy_async_smem();
   __syncthreads();
   return total;
+}
+
+// The tokens of tile t of a pre-routed small call: the flat slots of the tile's expert in
+// ascending order, ranks [j * tile_slots, j * tile_slots + n), as token indices (slot / topk)
+// into tok[0 .. n).  One warp calls it (a ballot per 32 flat slots).
+static __device__ __forceinline__ void pre_route_tile_tokens(const PreRouteInfo& info, int t,
+                                                             int Mk, int topk, int tile_slots,
+                                                             int* tok) {
+  const int lane = threadIdx.x & 31;
+  const int e = info.te[t] & 0xFFFF, n = info.te[t] >> 16;
+  const int r0 = (info.tp[t] >> 16) * tile_slots;
+  int seen = 0;
+  for (int f0 = 0; f0 < Mk && seen < r0 + n; f0 += 32) {
+    const int f = f0 + lane;
+    const bool mine = f < Mk && info.lid[f] == e;
+    const unsigned m = __ballot_sync(0xffffffffu, mine);
+    const int rank = seen + __popc(m & ((1u << lane) - 1u));
+    if (mine && rank >= r0 && rank < r0 + n) tok[rank - r0] = f / topk;
+    seen += __popc(m);
+  }
+  __syncwarp();
+}
+
+// In-kernel MXFP8 quantisation of a tile's activations, one K tile (128 activations per token)
+// per pipeline stage, by 64 threads (two warps; thread q owns the (row, block) items q, q + 64,
+// ...: row = item / 4, block of 32 = item % 4).  load() issues the bf16 loads of a K tile into
+// registers; quant() turns them into E4M3 codes and E8M0 scales in registers; store() writes
+// those straight into a stage: the B operand (BN rows of 128 codes, 16-byte chunk j of row r at
+// chunk j ^ (r % 8): the 128-byte swizzle the MMA's descriptor reads) and its scale atom rows
+// (row r: byte (r % 32) * 16 + (r / 32) * 4 + block).  Rows r >= n are written as zeros.  With
+// xq / xs set, store() also writes the codes and scales row-major at slot position p0 + r (a
+// copy for inspection).  The smem writes are generic-proxy stores: the caller fences them for
+// the tensor cores (fence.proxy.async) before signalling the stage.
+template <int BN>
+struct ActQuant {
+  static constexpr int kItems = BN * 4 / 64;
+  static_assert(BN == 16 || BN == 32, "in-kernel quantisation at tile widths 16 / 32");
+  struct Codes {
+    uint32_t w[kItems][8];
+    uint32_t sc[kItems];
+  };
+  const __nv_bfloat16* x;
+  int H, q;
+  __device__ __forceinline__ void load(uint4 (&v)[kItems][4], const int* tok, int n,
+                                       int kt) const {
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      const int item = q + 64 * it, r = item >> 2, b = item & 3;
+      if (r < n) {
+        const uint4* src =
+            reinterpret_cast<const uint4*>(x + (size_t)tok[r] * H + kt * 128 + b * 32);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) v[it][w] = __ldg(src + w);
+      }
+    }
+  }
+  __device__ __forceinline__ void quant(const uint4 (&v)[kItems][4], int n, Codes& c) const {
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      const int r = (q + 64 * it) >> 2;
+      if (r < n) {
+        c.sc[it] = mxfp8_block32(v[it], c.w[it]);
+      } else {
+        c.sc[it] = 0u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) c.w[it][j] = 0u;
+      }
+    }
+  }
+  __device__ __forceinline__ void store(const Codes& c, int n, int kt, uint8_t* b_tile,
+                                        uint8_t* sf_rows, uint8_t* xq, uint8_t* xs,
+                                        int p0) const {
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      const int item = q + 64 * it, r = item >> 2, b = item & 3;
+      const uint32_t* w = c.w[it];
+      uint8_t* row = b_tile + r * 128;
+      *reinterpret_cast<uint4*>(row + (((2 * b) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(row + (((2 * b + 1) ^ (r & 7)) << 4)) =
+          make_uint4(w[4], w[5], w[6], w[7]);
+      sf_rows[(r & 31) * 16 + (r >> 5) * 4 + b] = (uint8_t)c.sc[it];
+      if (xq != nullptr && r < n) {
+        uint4* dq = reinterpret_cast<uint4*>(xq + (size_t)(p0 + r) * H + kt * 128 + b * 32);
+        dq[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dq[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        xs[(size_t)(p0 + r) * (H / 32) + kt * 4 + b] = (uint8_t)c.sc[it];
+      }
+    }
+  }
+};
+
+// Quantises the K tiles k0 .. k0 + len - 1 of one tile into the stages of fill numbers i0, i0 + 1,
+// ... of an S-stage ring, signalling each stage's `full` barrier once per warp.  For each K tile
+// the codes are computed and the loads of the K tile two ahead issued before waiting for the
+// stage to be free (its `empty` phase, from the second lap on), so the load latency and the
+// arithmetic overlap that wait.  Returns false when a wait gave up.
+template <int BN, int S>
+static __device__ __forceinline__ bool act_quant_run(
+    const ActQuant<BN>& aq, const int* tok, int n, int k0, int len, int i0, uint8_t* smem,
+    int stage_bytes, int off_b, int off_sf, uint64_t* full, uint64_t* empty, uint8_t* xq,
+    uint8_t* xs, int p0, int32_t* err) {
+  using V = uint4[ActQuant<BN>::kItems][4];
+  V va, vb;
+  typename ActQuant<BN>::Codes cq;
+  const int lane = threadIdx.x & 31;
+  if (len > 0) aq.load(va, tok, n, k0);
+  if (len > 1) aq.load(vb, tok, n, k0 + 1);
+  // K tile t from registers v (loaded two K tiles ago); v is reloaded with K tile t + 2
+  auto step = [&](V& v, int t) -> bool {
+    aq.quant(v, n, cq);
+    if (t + 2 < len) aq.load(v, tok, n, k0 + t + 2);
+    const int i = i0 + t, s = i % S;
+    if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1, err)) return false;
+    uint8_t* st = smem + s * stage_bytes;
+    aq.store(cq, n, k0 + t, st + off_b, st + off_sf, xq, xs, p0);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&full[s]);
+    return true;
+  };
+  for (int t = 0; t < len; t += 2) {
+    if (!step(va, t)) return false;
+    if (t + 1 < len && !step(vb, t + 1)) return false;
+  }
+  return true;
 }
 
 // A tile record of the routing launch for a kernel that planned its work from its own

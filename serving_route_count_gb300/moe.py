@@ -200,6 +200,11 @@ def moe_get_device_error(plan, scratch, stream=None):
     return st, code.value
 
 
+def moe_plan_set_debug_copies(plan, on):
+    _check(_lib.load().moe_plan_set_debug_copies(_handle(plan), int(on)),
+           "moe_plan_set_debug_copies")
+
+
 def moe_get_device_error_static(plan, stream=None):
     """moe_get_device_error for calls made with moe_run_static_scratch: (status, code)."""
     code = ctypes.c_int()
@@ -324,7 +329,7 @@ class MoELayer:
 
     def __init__(self, ck, topk, max_m, swiglu_limit=float("inf"), deterministic=False,
                  alpha=None, beta=None, device="cuda", keep_checkpoint=False, backend=0,
-                 fc1_kernel=0, first_expert=0, weight_on_input=False):
+                 fc1_kernel=0, first_expert=0, weight_on_input=False, debug_copies=False):
         self.E, self.H, self.I, self.topk, self.max_m = ck.E, ck.H, ck.I, topk, max_m
         self.quant = quant_mode_of(ck)
         tier = ck.tier if ck.quant == "hybrid" else None
@@ -349,6 +354,8 @@ class MoELayer:
             moe_plan_set_expert_offset(self.plan, first_expert)
         if weight_on_input:
             moe_plan_set_router_weight_on_input(self.plan, 1)
+        if debug_copies:
+            moe_plan_set_debug_copies(self.plan, 1)
         self.scratch = torch.empty(moe_scratch_bytes(self.plan), dtype=torch.uint8, device=device)
         self.device = device
         self._io = None

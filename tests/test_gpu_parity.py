@@ -28,6 +28,7 @@ def _lib_built():
 
 def _layer(ck, topk, max_m, limit, det, **kw):
     from serving_route_count_gb300 import MoELayer
+    kw.setdefault("debug_copies", True)      # the tests read the quantised activations back
     return MoELayer(ck, topk, max_m, limit, det, **kw)
 
 
