@@ -208,6 +208,15 @@ moe_status moe_plan_set_expert_offset(moe_plan_t* plan, int first_expert);
  * Errors: MOE_ERR_ARG. */
 moe_status moe_plan_set_debug_copies(moe_plan_t* plan, int on);
 
+/* Test hook for the device-side failure path: with ns > 0, the W4A8 fc1 kernel that runs one
+ * (tile, row block) unit per CTA (calls whose units fit one wave) first makes its MMA issuer wait
+ * up to ns nanoseconds on a barrier that no thread ever arrives on.  The wait runs out, sets the
+ * timeout bit of the call's device error word (moe_get_device_error then returns
+ * MOE_ERR_TIMEOUT), and the CTA stops issuing work, waits (with the normal 1 s bound) for the
+ * copies it has in flight and returns: the call's output is then undefined, and the context and
+ * the plan stay usable.  ns = 0 (default) turns it off.  Errors: MOE_ERR_ARG (ns > 1 s). */
+moe_status moe_plan_set_wait_probe(moe_plan_t* plan, unsigned long long ns);
+
 /* Size in bytes of the device scratch buffer moe_run needs (routing tables, quantised
  * activations, the fc1 -> fc2 intermediate, the combine buffer). */
 moe_status moe_scratch_bytes(const moe_plan_t* plan, size_t* bytes);

@@ -43,6 +43,7 @@ SIGNATURES = {
     "moe_plan_set_expert_offset": (c_int, [c_void_p, c_int]),
     "moe_plan_set_router_weight_on_input": (c_int, [c_void_p, c_int]),
     "moe_plan_set_debug_copies": (c_int, [c_void_p, c_int]),
+    "moe_plan_set_wait_probe": (c_int, [c_void_p, ctypes.c_ulonglong]),
     "moe_run": (c_int, [c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p, c_void_p,
                         c_void_p, c_int, c_void_p]),
     "moe_unprepare_weights": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p]),

@@ -379,7 +379,7 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   d.E = E; d.H = H; d.I = I; d.Ip = (int)align_up((size_t)I, 128); d.topk = topk; d.max_m = max_m;
   d.quant = quant_mode; d.deterministic = deterministic ? 1 : 0;
   d.limit = swiglu_limit; d.alpha = 1.f; d.beta = 0.f; d.backend = 0; d.fc1_kernel = 0;
-  d.ep_first = 0; d.w_on_input = 0; d.keep_act = 0;
+  d.ep_first = 0; d.w_on_input = 0; d.keep_act = 0; d.wait_probe_ns = 0;
   const size_t Sm = (size_t)max_m * topk;
   Scratch& s = p->s;
   s.max_tiles = (int)std::min<size_t>(Sm, (Sm + kSimtSlots - 1) / kSimtSlots +
@@ -536,6 +536,12 @@ moe_status moe_plan_set_router_weight_on_input(moe_plan_t* plan, int on) {
 moe_status moe_plan_set_debug_copies(moe_plan_t* plan, int on) {
   if (plan == nullptr || (on != 0 && on != 1)) return MOE_ERR_ARG;
   plan->d.keep_act = on;
+  return MOE_OK;
+}
+
+moe_status moe_plan_set_wait_probe(moe_plan_t* plan, unsigned long long ns) {
+  if (plan == nullptr || ns > 1000000000ull) return MOE_ERR_ARG;
+  plan->d.wait_probe_ns = ns;
   return MOE_OK;
 }
 

@@ -88,6 +88,10 @@ struct TcFc1Params {
   int topk;
   uint8_t* xq;               // [Sm][H] E4M3 copy of the quantised activations (row block 0)
   uint8_t* xs;               // [Sm][H/32] their E8M0 scales
+  // test hook (0: off): the MMA issuer first waits this long on a barrier nothing arrives on;
+  // the wait runs out, sets the timeout bit, and the CTA takes its failure path (no MMA, the
+  // issued copies drained) - the bounded waits tested without a fault
+  unsigned long long probe_ns;
 };
 
 struct TcFc2Params {
@@ -122,7 +126,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[S], empty[S], done;
+  __shared__ __align__(8) uint64_t full[S], empty[S], done, never;
   __shared__ uint32_t s_tmem;
   __shared__ int s_last, s_fail;
   __shared__ PreRouteInfo s_info;
@@ -165,6 +169,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
       mbar_init(&empty[s], 1);
     }
     mbar_init(&done, 1);
+    mbar_init(&never, 1);      // the wait probe's barrier: no thread ever arrives on it
     s_fail = 0;
     fence_barrier_init();
   }
@@ -277,6 +282,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      if (p.probe_ns != 0) ok = mbar_wait(&never, 0, p.err, p.probe_ns);
       for (int i = 0; i < nk && ok; ++i) {
         const int s = i % S;
         ok = mbar_wait(&full[s], (i / S) & 1, p.err);
@@ -324,7 +330,9 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
       if (td.x != e || td.y != p0 || td.z != n) set_error(p.err, kErrRouteBounds);
     }
   }
-  ok = mbar_wait(&done, 0, p.err) && ok;
+  // one verdict per warp: the producer's or MMA issuer's lane may have given up a wait while the
+  // other lanes did not, and the epilogue's TMEM loads and shuffles are warp-collective
+  ok = __all_sync(0xffffffffu, mbar_wait(&done, 0, p.err) && ok);
   tc_fence_after();
   __syncwarp();
   const int f = fb * 128 + warp * 32 + lane;          // intermediate feature of this lane
@@ -521,7 +529,9 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
   }
 
   __syncthreads();                                    // s_f / s_w written
-  ok = mbar_wait(&done, 0, p.err) && ok;
+  // one verdict per warp: the producer's or MMA issuer's lane may have given up a wait while the
+  // other lanes did not, and the epilogue's TMEM loads and shuffles are warp-collective
+  ok = __all_sync(0xffffffffu, mbar_wait(&done, 0, p.err) && ok);
   tc_fence_after();
   __syncwarp();
   const int h = rt * 128 + warp * 32 + lane;          // output column of this lane
@@ -670,6 +680,7 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
     // quantised here only when the call routes in shared memory at a width of <= 32 tokens
     p.x = (p.ids != nullptr && bn <= 32) ? static_cast<const __nv_bfloat16*>(x) : nullptr;
     p.topk = d.topk;
+    p.probe_ns = d.wait_probe_ns;
     p.xq = d.keep_act ? r.xq : nullptr;
     p.xs = r.xs;
     switch (bn) {

@@ -368,12 +368,12 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
     int g = 0;
     for (int i = 0; i < nraw && ok; ++i) {
       const int s = i % Cfg::kSr;
-      ok = mbar_wait(&raw_full[s], (i / Cfg::kSr) & 1, p.err);
+      ok = mbar_wait_warp(&raw_full[s], (i / Cfg::kSr) & 1, p.err);
       if (!ok) break;
       const uint8_t* st = raw_base + s * Cfg::kRaw;
       for (int q = 0; q < 4 && ok; ++q, ++g) {
         const int sa = g % Cfg::kSa;
-        if (g >= Cfg::kSa) ok = mbar_wait(&a_empty[sa], ((g / Cfg::kSa) - 1) & 1, p.err);
+        if (g >= Cfg::kSa) ok = mbar_wait_warp(&a_empty[sa], ((g / Cfg::kSa) - 1) & 1, p.err);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -400,7 +400,8 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   // ---- epilogue (warps 2..5): TMEM lane quadrant = warp % 4
   if (warp >= 2 && warp < 6) {
     asm volatile("bar.sync 1, 128;" ::: "memory");         // s_f / s_w written (warps 2..5)
-    ok = mbar_wait(&done, 0, p.err) && ok;
+    // one verdict per warp (the epilogue's TMEM loads and shuffles are warp-collective)
+    ok = __all_sync(0xffffffffu, mbar_wait(&done, 0, p.err) && ok);
     tc_fence_after();
     __syncwarp();
     const int quad = warp & 3;

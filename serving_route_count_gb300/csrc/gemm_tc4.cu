@@ -233,7 +233,9 @@ gemm_tc4_kernel(const __grid_constant__ Tc4Params p) {
   }
 
   __syncthreads();
-  ok = mbar_wait(&done, 0, p.err) && ok;
+  // one verdict per warp: the producer's or MMA issuer's lane may have given up a wait while the
+  // other lanes did not, and the epilogue's TMEM loads and shuffles are warp-collective
+  ok = __all_sync(0xffffffffu, mbar_wait(&done, 0, p.err) && ok);
   tc_fence_after();
   __syncwarp();
   const int row = rb * 128 + warp * 32 + lane;       // weight row of this lane
@@ -481,7 +483,7 @@ fc2_tc4_persist_kernel(const __grid_constant__ Tc4Params p) {
       }
       const int h4 = rb * 128 + quad * 32 + 4 * (lane & 7);
       const int b = j & 1;
-      ok = ok && mbar_wait(&acc_full[b], (j >> 1) & 1, p.err);
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(&acc_full[b], (j >> 1) & 1, p.err));
       tc_fence_after();
       __syncwarp();
       const uint32_t trow = tmem + b * BN + ((uint32_t)(quad * 32) << 16);

@@ -346,7 +346,7 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
       const int p0 = td.y, n = td.z;
       const int f = fb * 128 + row;
       const int b = j & 1;
-      ok = ok && mbar_wait(&acc_full[b], (j >> 1) & 1, p.err);
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(&acc_full[b], (j >> 1) & 1, p.err));
       tc_fence_after();
       __syncwarp();
       const uint32_t trow = tmem + b * Cfg::kAcc + ((uint32_t)(quad * 32) << 16);
@@ -390,13 +390,13 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
           s_last = (t + len == p.KT);
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (s_last && ok) {
+        if (s_last) {
           __threadfence();
           // the unit's pieces in K order (CTAs with empty ranges hold none), listed once by
-          // one thread
+          // one thread; the barrier is taken by all four warps, whatever their verdicts
           if (warp == 4 && lane == 0) s_npieces = wk.unit_pieces(u, s_pieces);
           asm volatile("bar.sync 1, 128;" ::: "memory");
-          reduce_pieces(
+          if (ok) reduce_pieces(
               s_npieces, n, (size_t)128, (size_t)BN * 128,
               [&](int qq) -> const float* {
                 return p.part + (size_t)s_pieces[qq] * Cfg::kPartFloats + row;
@@ -634,7 +634,7 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
       // after the transpose a lane holds four consecutive output features of one token
       const int h4 = rb * 128 + quad * 32 + 4 * (lane & 7);
       const int b = j & 1;
-      ok = ok && mbar_wait(&acc_full[b], (j >> 1) & 1, p.err);
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(&acc_full[b], (j >> 1) & 1, p.err));
       tc_fence_after();
       __syncwarp();
       const uint32_t trow = tmem + b * BN + ((uint32_t)(quad * 32) << 16);

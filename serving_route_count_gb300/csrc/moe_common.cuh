@@ -177,6 +177,8 @@ struct PlanDims {
                     // belong to other ranks and are dropped
   int keep_act;     // test hook: small W4A8 calls, whose fc1 quantises the activations itself,
                     // also store the codes where moe_debug_actq reads them
+  unsigned long long wait_probe_ns;   // test hook (0: off): W4A8 fc1's MMA issuer first waits
+                    // this long on a barrier nothing arrives on, so the wait runs out
 };
 
 // Local id of router id `id` on a plan that owns the global experts [first, first + E): id -

@@ -54,18 +54,27 @@ TC_DEV bool mbar_try_wait(uint64_t* b, uint32_t parity) {
   return ok != 0;
 }
 // Waits for phase `parity` of barrier b to complete; false (and the timeout bit set in *err)
-// when it did not within kTimeoutNs.
-TC_DEV bool mbar_wait(uint64_t* b, uint32_t parity, int32_t* err) {
+// when it did not within limit_ns (kTimeoutNs unless a test shortens it).
+TC_DEV bool mbar_wait(uint64_t* b, uint32_t parity, int32_t* err,
+                      unsigned long long limit_ns = kTimeoutNs) {
   if (mbar_try_wait(b, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(b, parity)) return true;
-    if (globaltimer() - t0 > kTimeoutNs) {
+    if (globaltimer() - t0 > limit_ns) {
       atomicOr(err, kErrTimeout);
       return false;
     }
   }
+}
+
+// mbar_wait taken by every lane of a warp, with one verdict for the warp: true only when the wait
+// succeeded in every lane.  The lanes' bounded waits can end differently (one lane times out as
+// the phase completes for another), and the warp-collective work that follows (tcgen05.ld / st,
+// shuffles, __syncwarp) has to run in all lanes or in none.
+TC_DEV bool mbar_wait_warp(uint64_t* b, uint32_t parity, int32_t* err) {
+  return __all_sync(0xffffffffu, mbar_wait(b, parity, err));
 }
 
 // After a wait gave up: waits (each wait bounded) for the stages this thread filled last - the

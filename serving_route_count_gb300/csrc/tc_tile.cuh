@@ -269,7 +269,7 @@ static __device__ __forceinline__ bool act_quant_run(
     aq.quant(v, n, cq);
     if (t + 2 < len) aq.load(v, tok, n, k0 + t + 2);
     const int i = i0 + t, s = i % S;
-    if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1, err)) return false;
+    if (i >= S && !mbar_wait_warp(&empty[s], ((i / S) - 1) & 1, err)) return false;
     uint8_t* st = smem + s * stage_bytes;
     aq.store(cq, n, k0 + t, st + off_b, st + off_sf, xq, xs, p0);
     fence_proxy_async_smem();

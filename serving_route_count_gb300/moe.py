@@ -200,6 +200,10 @@ def moe_get_device_error(plan, scratch, stream=None):
     return st, code.value
 
 
+def moe_plan_set_wait_probe(plan, ns):
+    _check(_lib.load().moe_plan_set_wait_probe(_handle(plan), int(ns)), "moe_plan_set_wait_probe")
+
+
 def moe_plan_set_debug_copies(plan, on):
     _check(_lib.load().moe_plan_set_debug_copies(_handle(plan), int(on)),
            "moe_plan_set_debug_copies")

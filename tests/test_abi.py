@@ -196,6 +196,20 @@ def test_expert_offset_arguments(lib):
     moe.moe_destroy_plan(p)
 
 
+def test_wait_probe_arguments(lib):
+    """The device wait probe (a test hook): 0 turns it off, up to 1 s is accepted, more is an
+    argument error, and a null plan is refused."""
+    p = moe.moe_plan(8, 256, 128, 1, 16, moe.MOE_W4A8_MXFP4, 7.0, 0)
+    moe.moe_plan_set_wait_probe(p, 2_000_000)
+    moe.moe_plan_set_wait_probe(p, 1_000_000_000)
+    moe.moe_plan_set_wait_probe(p, 0)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_plan_set_wait_probe(p, 1_000_000_001)
+    assert ei.value.status == 1
+    moe.moe_destroy_plan(p)
+    assert lib.moe_plan_set_wait_probe(None, 0) == 1
+
+
 def test_router_weight_on_input_arguments(lib):
     """Router weights on the input: 16-bit activation modes only (the pages refuse W4A8 too)."""
     p = moe.moe_plan(8, 256, 128, 1, 16, moe.MOE_W4A8_MXFP4, 7.0, 0)

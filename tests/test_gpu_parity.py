@@ -765,3 +765,30 @@ def test_w4a16_tensor_core_tile_widths(quant, M, det):
     assert np.all(tiny_ok[~big])
     simt = _layer(ck, cfg.topk, M, math.inf, det, backend=1)
     check_rows(run_layer(simt, x, ids, w), ck, x, ids, w, math.inf)
+
+
+@pytest.mark.parametrize("det", [0, 1])
+def test_device_wait_timeout_recovers(det):
+    """The bounded device waits, run out on purpose without a fault: with the wait probe on, fc1's
+    MMA issuer waits 2 ms on a barrier nothing arrives on, so the call reports MOE_ERR_TIMEOUT
+    through the device error word; its producers then give up their own waits after the 1 s
+    bound and drain their copies.  The context and the plan stay usable: the next call, probe
+    off, matches the oracle on every row and reports no error."""
+    from serving_route_count_gb300 import moe_plan_set_wait_probe
+    cfg = small_cfg("mxfp4")
+    ck = S.make_checkpoint(cfg, seed=8100 + det)
+    rng = np.random.default_rng(8200 + det)
+    M = 9
+    x = S.make_x(rng, M, cfg.H)
+    ids = S.zipf_topk(rng, M, cfg.E, cfg.topk, 1.1)
+    w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 2.5)
+    layer = _layer(ck, cfg.topk, M, 7.0, det, fc1_kernel=1)
+    moe_plan_set_wait_probe(layer.plan, 2_000_000)
+    run_layer(layer, x, ids, w)
+    torch.cuda.synchronize()
+    st, code = layer.device_error()
+    assert st == 7 and code & 2, (st, code)
+    moe_plan_set_wait_probe(layer.plan, 0)
+    got = run_layer(layer, x, ids, w)
+    assert layer.device_error() == (0, 0)
+    check_rows(got, ck, x, ids, w, 7.0)
