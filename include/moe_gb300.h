@@ -177,9 +177,10 @@ moe_status moe_plan_set_swiglu_alpha_beta(moe_plan_t* plan, float alpha, float b
 moe_status moe_plan_set_backend(moe_plan_t* plan, int backend);
 
 /* fc1 kernel of the W4A8 tensor-core path at the 16-token tile width (calls with M <= 16):
- *   0 (default) automatic: one (tile, row block) unit per CTA, split along K for small calls,
- *     while the units fit one wave of CTAs; the persistent stream-K kernel beyond;
- *   1 always the unit-per-CTA kernel;  2 always the stream-K kernel.
+ *   0 (default) automatic: the persistent stream-K kernel (the routed units' K tiles split
+ *     evenly over all CTA slots) whenever its schedule fits (H / 128 < 130), else one
+ *     (tile, row block) unit per CTA, split along K for small calls;
+ *   1 always the unit-per-CTA kernel;  2 the stream-K kernel wherever its schedule fits.
  * Both give results within the same tolerance of the method (in deterministic mode each is
  * bit-stable on its own; the two differ in the rounding order of fc1's K sum).
  * Errors: MOE_ERR_ARG. */

@@ -374,6 +374,9 @@ finalize_kernel(int M, int H, int topk, int deterministic, const float* __restri
 static cudaError_t launch_simt_fc(bool fc2, const SimtArgs& a, int max_tiles, cudaStream_t st) {
   const int R = fc2 ? a.H : 2 * a.I;
   dim3 grid(max_tiles, cdiv(R, kSimtRowsPerCta));
+  static const bool carveout = prefer_max_shared(gemm_simt_kernel<true>) &&
+                                prefer_max_shared(gemm_simt_kernel<false>);
+  (void)carveout;
   return fc2 ? launch_kernel(gemm_simt_kernel<true>, grid, dim3(kSimtThreads), 0, st, true, a)
              : launch_kernel(gemm_simt_kernel<false>, grid, dim3(kSimtThreads), 0, st, true, a);
 }
@@ -383,6 +386,8 @@ static cudaError_t launch_act(const RunPtrs& r, int Sm, int I, int Ip, float lim
   const size_t total = (size_t)Sm * (Ip / 32);
   int blocks = (int)std::min<size_t>((total + 255) / 256, 152 * 16);
   if (blocks < 1) blocks = 1;
+  static const bool carveout = prefer_max_shared(act_kernel);
+  (void)carveout;
   return launch_kernel(act_kernel, dim3(blocks), dim3(256), 0, st, true,
                        static_cast<const float*>(r.g), static_cast<const int32_t*>(r.ctrl), I, Ip,
                        limit, alpha, beta, a8, r.hq, r.hs, r.h16);
@@ -393,6 +398,8 @@ static cudaError_t launch_finalize(int M, int H, int topk, int det, const RunPtr
   const size_t total = (size_t)M * (H / 8);
   int blocks = (int)std::min<size_t>((total + 255) / 256, 152 * 16);
   if (blocks < 1) blocks = 1;
+  static const bool carveout = prefer_max_shared(finalize_kernel);
+  (void)carveout;
   return launch_kernel(finalize_kernel, dim3(blocks), dim3(256), 0, st, true, M, H, topk, det,
                        static_cast<const float*>(r.acc), static_cast<const float*>(r.rbuf),
                        static_cast<const int32_t*>(r.slot_of),

@@ -133,6 +133,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
   __shared__ int s_tok[32];
   // activations quantised here (small calls, tiles of at most 32 tokens)
   const bool fused = BN <= 32 && p.x != nullptr && p.ids != nullptr;
+  tmem_alloc_first(&s_tmem, Cfg::kAlloc1);
 
   // Small calls route in shared memory (scratch in the last stage, before any copy lands
   // there), so the weights of the first stages are requested while the routing launch still
@@ -144,6 +145,7 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
                                          fused ? &s_info : nullptr),
              p.max_tiles);
     if (tile >= nt) {
+      tmem_exit_early(&s_tmem, Cfg::kAlloc1);
       pdl_wait_prev();
       return;
     }
@@ -155,13 +157,12 @@ fc1_tc_kernel(const __grid_constant__ TcFc1Params p) {
     }
   } else {
     pdl_wait_prev();     // routing tables complete
-    if (tile >= p.ctrl[1]) return;
+    if (tile >= p.ctrl[1]) {
+      tmem_exit_early(&s_tmem, Cfg::kAlloc1);
+      return;
+    }
   }
 
-  if (warp == 0) {
-    tmem_alloc(&s_tmem, Cfg::kAlloc1);
-    tmem_relinquish();
-  }
   if (tid == 32) {
     for (int s = 0; s < S; ++s) {
       // fused: the producer's arrival (weight bytes) and one per quantising warp
@@ -409,11 +410,18 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::kStages2;
   pdl_launch_next();
+  __shared__ __align__(8) uint64_t full[S], empty[S], done;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_fail;
+  __shared__ int s_f[BN];          // flat slot index of each tile column
+  __shared__ float s_w[BN];        // its router weight
+  tmem_alloc_first(&s_tmem, Cfg::kAlloc2);
   // The routing tables were complete before fc1 let this kernel launch (fc1 waits for the
   // routing launch first), so the tile and the weights of the first stages are read before
   // waiting for fc1's output (L2 reads: nothing of them is in this SM's L1).
   const int tile = blockIdx.x;
   if (tile >= __ldcg(&p.ctrl[1])) {
+    tmem_exit_early(&s_tmem, Cfg::kAlloc2);
     pdl_wait_prev();
     return;
   }
@@ -427,16 +435,7 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[S], empty[S], done;
-  __shared__ uint32_t s_tmem;
-  __shared__ int s_fail;
-  __shared__ int s_f[BN];          // flat slot index of each tile column
-  __shared__ float s_w[BN];        // its router weight
 
-  if (warp == 0) {
-    tmem_alloc(&s_tmem, Cfg::kAlloc2);
-    tmem_relinquish();
-  }
   if (tid == 32) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);

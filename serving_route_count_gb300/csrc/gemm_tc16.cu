@@ -232,9 +232,14 @@ __global__ void __launch_bounds__(k16Threads, 1)
 gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   using Cfg = Tc16Cfg<BN, FC2, PAIR>;
   constexpr int kMats = Cfg::kMats;
+  __shared__ uint32_t s_tmem;
+  tmem_alloc_first(&s_tmem, Cfg::kAlloc);
   pdl_wait_prev();     // previous kernel of the call complete, its writes visible
   const int tile = blockIdx.x;
-  if (tile >= p.ctrl[1]) return;
+  if (tile >= p.ctrl[1]) {
+    tmem_exit_early(&s_tmem, Cfg::kAlloc);
+    return;
+  }
   const int4 td = p.tiles[tile];
   const int e = td.x, p0 = td.y, n = td.z;
   const int rb = blockIdx.y, split = blockIdx.z;
@@ -259,16 +264,10 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   __shared__ __align__(8) uint64_t a_full[Cfg::kSa], a_empty[Cfg::kSa];
   __shared__ __align__(8) uint64_t b_full[Cfg::kSb], b_empty[Cfg::kSb];
   __shared__ __align__(8) uint64_t done;
-  __shared__ uint32_t s_tmem;
   __shared__ int s_last, s_fail;
   __shared__ int s_f[BN];          // fc2: flat slot index of each tile column
   __shared__ float s_w[BN];        // fc2: its router weight
 
-
-  if (warp == 0) {
-    tmem_alloc(&s_tmem, Cfg::kAlloc);
-    tmem_relinquish();
-  }
   if (tid == 32) {
     for (int s = 0; s < Cfg::kSr; ++s) {
       mbar_init(&raw_full[s], 1);

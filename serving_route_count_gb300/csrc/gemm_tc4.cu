@@ -114,10 +114,15 @@ gemm_tc4_kernel(const __grid_constant__ Tc4Params p) {
   using Cfg = Tc4Cfg<BN, FC2>;
   constexpr int S = Cfg::kStages;
   constexpr int kMats = Cfg::kMats;
+  __shared__ uint32_t s_tmem;
+  tmem_alloc_first(&s_tmem, Cfg::kAlloc);
   pdl_wait_prev();             // routing tables and activations complete
   pdl_launch_next();
   const int tile = blockIdx.x;
-  if (tile >= p.ctrl[1]) return;
+  if (tile >= p.ctrl[1]) {
+    tmem_exit_early(&s_tmem, Cfg::kAlloc);
+    return;
+  }
   const int4 td = p.tiles[tile];
   const int e = td.x, p0 = td.y, n = td.z;
   const int rb = blockIdx.y, split = blockIdx.z;
@@ -129,15 +134,10 @@ gemm_tc4_kernel(const __grid_constant__ Tc4Params p) {
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[S], empty[S], done;
-  __shared__ uint32_t s_tmem;
   __shared__ int s_last, s_fail;
   __shared__ int s_f[BN];
   __shared__ float s_w[BN];
 
-  if (warp == 0) {
-    tmem_alloc(&s_tmem, Cfg::kAlloc);
-    tmem_relinquish();
-  }
   if (tid == 32) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -357,29 +357,29 @@ fc2_tc4_persist_kernel(const __grid_constant__ Tc4Params p) {
   using Cfg = Tc4PersistCfg<BN>;
   using B = typename Cfg::Base;
   constexpr int S = Cfg::kStages;
+  __shared__ uint32_t s_tmem;
+  tmem_alloc_first(&s_tmem, Cfg::kAlloc);
   pdl_wait_prev();             // fc1 complete, h and its scales visible
   pdl_launch_next();
   const int G = gridDim.x, c = blockIdx.x;
   const int units = p.ctrl[1] * p.RB;
   const int u_begin = (int)((long long)c * units / G);
   const int u_end = (int)((long long)(c + 1) * units / G);
-  if (u_begin >= u_end) return;
+  if (u_begin >= u_end) {
+    tmem_exit_early(&s_tmem, Cfg::kAlloc);
+    return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[S], empty[S], acc_full[2], acc_empty[2];
-  __shared__ uint32_t s_tmem;
   __shared__ int s_fail;
   __shared__ int s_f[BN];
   __shared__ float s_w[BN];
   __shared__ __align__(16) float s_y[4][16][32];
 
-  if (warp == 0) {
-    tmem_alloc(&s_tmem, Cfg::kAlloc);
-    tmem_relinquish();
-  }
   if (tid == 32) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);

@@ -96,6 +96,7 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   __shared__ int s_tok[2][BN];      // each quantising warp's copy of its tile's token list
   // activations quantised here (the shared-memory routing knows each tile's tokens)
   const bool fused = p.x != nullptr && p.ids != nullptr;
+  tmem_alloc_first(&s_tmem, Cfg::kAlloc);
 
   // Small calls route in shared memory (scratch in the last stage, before any copy lands
   // there), so the weights of the first stages are requested while the routing launch still
@@ -113,6 +114,7 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
   StreamWork wk;
   wk.init(n_tiles * p.RT, p.KT, gridDim.x, blockIdx.x);
   if (wk.nsteps <= 0) {
+    tmem_exit_early(&s_tmem, Cfg::kAlloc);
     pdl_wait_prev();
     return;
   }
@@ -129,10 +131,6 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
     }
   }
 
-  if (warp == 0) {
-    tmem_alloc(&s_tmem, Cfg::kAlloc);
-    tmem_relinquish();
-  }
   if (tid == 32) {
     for (int s = 0; s < S; ++s) {
       // fused: the producer's arrival (weight bytes) and one per quantising warp
@@ -468,6 +466,14 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
   using Cfg = PersistFc2Cfg<BN>;
   constexpr int S = Cfg::kStages;
   pdl_launch_next();
+  __shared__ __align__(8) uint64_t full[S], empty[S], acc_full[2], acc_empty[2], drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_fail;
+  __shared__ int s_f[BN];          // flat slot index of each column of the current tile
+  __shared__ float s_w[BN];        // its router weight
+  // per epilogue warp: 16 token columns x its 32 output features, read back transposed
+  __shared__ __align__(16) float s_y[4][16][32];
+  tmem_alloc_first(&s_tmem, Cfg::kAlloc);
   // The routing tables were complete before fc1 let this kernel launch (fc1 waits for the
   // routing launch first): the unit range and the weights of the first stages are read before
   // waiting for fc1's output (L2 reads: nothing of them is in this SM's L1).
@@ -476,6 +482,7 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
   const int u_begin = (int)((long long)c * units / G);
   const int u_end = (int)((long long)(c + 1) * units / G);
   if (u_begin >= u_end) {
+    tmem_exit_early(&s_tmem, Cfg::kAlloc);
     pdl_wait_prev();
     return;
   }
@@ -484,18 +491,6 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[S], empty[S], acc_full[2], acc_empty[2], drain;
-  __shared__ uint32_t s_tmem;
-  __shared__ int s_fail;
-  __shared__ int s_f[BN];          // flat slot index of each column of the current tile
-  __shared__ float s_w[BN];        // its router weight
-  // per epilogue warp: 16 token columns x its 32 output features, read back transposed
-  __shared__ __align__(16) float s_y[4][16][32];
-
-  if (warp == 0) {
-    tmem_alloc(&s_tmem, Cfg::kAlloc);
-    tmem_relinquish();
-  }
   if (tid == 32) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -687,20 +682,15 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
 
 // ---------------------------------------------------------------------------------- host side
 
-// The stream-K fc1 serves the 16-token tiles of decode-size calls whose (tile, row block) units
-// outnumber the CTAs that fit on the GPU at once: there the one-unit-per-CTA kernel would run a
-// second, mostly empty wave.
+// The stream-K fc1 serves every call of 16-token tiles (decode sizes).  Its CTAs split the
+// units the routing actually produced evenly over all CTA slots, where the one-unit-per-CTA
+// kernel sizes its grid for the most tiles the call could have (one per routed slot), leaves
+// the CTAs of absent tiles idle and gives each remaining CTA a whole unit: measured over the
+// decode ladder M = 1..16 (E 384, H 7168, I 576, top-6), 725 us against 864 us per pass, and
+// faster at every M.
 bool fc1_stream_preferred(int bn, int units) {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-      (void)cudaGetLastError();
-      sms = 1;
-    }
-  }
-  return bn == 16 && units > 2 * sms;
+  (void)units;
+  return bn == 16;
 }
 // Scratch of its partial slots: 2 per CTA, each [2][16][128] fp32.
 size_t fc1_stream_part_bytes() { return (size_t)2 * kStreamMaxCtas * 2 * 16 * 128 * 4; }

@@ -299,6 +299,17 @@ __device__ __forceinline__ void pdl_launch_next() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Asks for the largest shared-memory carveout for `kernel` (call once per kernel, from a
+// static of its launch function).  An SM runs its CTAs under one carveout, so a kernel with
+// little shared memory left at the default carveout keeps the tensor-core kernels chained after
+// it off its SMs until its CTAs there end (measured: no fc1 CTA started on an SM while a
+// routing CTA ran on it).
+template <typename K>
+inline bool prefer_max_shared(K kernel) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared) == cudaSuccess;
+}
+
 // Launches kernel<<<grid, block, smem, st>>>(args...); `chained` lets it start (up to its
 // pdl_wait_prev) while the previous kernel of the stream is still running.
 template <typename... KArgs, typename... Args>

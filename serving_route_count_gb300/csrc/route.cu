@@ -737,6 +737,8 @@ cudaError_t launch_route_count(const int32_t* ids, int Mk, int E, int ep_first,
   static_assert(kMaxRouteExperts <= kRouteThreads, "one expert per thread");
   if (E > kMaxRouteExperts || Mk < 1) return cudaErrorInvalidValue;
   // first kernel of a call: an ordinary launch (the previous call may still read the tables)
+  static const bool carveout = prefer_max_shared(route_count_kernel);
+  (void)carveout;
   return launch_kernel(route_count_kernel, dim3(route_chunks(Mk)), dim3(kRouteThreads), 0, st,
                        false, ids, Mk, E, r.ctrl, r.rcc, ep_first);
 }
@@ -744,6 +746,8 @@ cudaError_t launch_route_count(const int32_t* ids, int Mk, int E, int ep_first,
 cudaError_t launch_route_scatter(const int32_t* ids, int Mk, int E, int ep_first, int tile_slots,
                                  int max_tiles, const RunPtrs& r, cudaStream_t st) {
   if (E > kMaxRouteExperts || Mk < 1) return cudaErrorInvalidValue;
+  static const bool carveout = prefer_max_shared(route_scatter_kernel);
+  (void)carveout;
   return launch_kernel(route_scatter_kernel, dim3(route_chunks(Mk)), dim3(kRouteThreads), 0, st,
                        true, ids, Mk, E, tile_slots, max_tiles,
                        static_cast<const int32_t*>(r.rcc), r.cnt, r.off, r.perm, r.slot_of,
@@ -760,6 +764,8 @@ cudaError_t launch_actq_rows(const void* x, int M, int H, int topk, const RunPtr
   const size_t work = std::max(items * 32,
                                std::max(z0_words / 4, std::max(z1_words / 4, z2_words / 4)));
   const int blocks = (int)std::max<size_t>(1, std::min<size_t>((work + 255) / 256, 152 * 8));
+  static const bool carveout = prefer_max_shared(actq_rows_kernel);
+  (void)carveout;
   return launch_kernel(actq_rows_kernel, dim3(blocks), dim3(256), 0, st, true,
                        reinterpret_cast<const __nv_bfloat16*>(x), M, H, topk,
                        static_cast<const int32_t*>(r.slot_of), r.xq, r.xs, r.xs16, r.r16,
@@ -787,6 +793,8 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_fi
                                      152 * 4);
   if (blocks < 1) blocks = 1;
   // first kernel of a call: an ordinary launch (the previous call may still read the tables)
+  static const bool carveout = prefer_max_shared(route_actq_small_kernel);
+  (void)carveout;
   return launch_kernel(route_actq_small_kernel, dim3(blocks), dim3(kSmallRouteThreads),
                        (size_t)E * sizeof(int), st, false, ids, Mk, E, tile_slots, max_tiles,
                        reinterpret_cast<const __nv_bfloat16*>(x), H, topk, r.cnt, r.off, r.perm,
@@ -802,6 +810,8 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_fi
 cudaError_t launch_route(const int32_t* ids, int Mk, int E, int ep_first, int tile_slots,
                          int max_tiles, const RunPtrs& r, cudaStream_t st) {
   // first kernel of a call: an ordinary launch (the previous call may still read the tables)
+  static const bool carveout = prefer_max_shared(route_kernel);
+  (void)carveout;
   return launch_kernel(route_kernel, dim3(1), dim3(kRouteThreads), 0, st, false, ids, Mk, E,
                        tile_slots, max_tiles, r.cnt, r.off, r.perm, r.slot_of, r.tiles, r.ctrl,
                        ep_first);
@@ -818,6 +828,8 @@ cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r,
       std::max(z0_words / 4, std::max(z1_words / 4, z2_words / 4)));
   int blocks = (int)std::min<size_t>((work + 255) / 256, 152 * 8);
   if (blocks < 1) blocks = 1;
+  static const bool carveout = prefer_max_shared(actq_kernel);
+  (void)carveout;
   return launch_kernel(actq_kernel, dim3(blocks), dim3(256), 0, st, true,
                        reinterpret_cast<const __nv_bfloat16*>(x), H, topk,
                        static_cast<const int32_t*>(r.ctrl), static_cast<const int32_t*>(r.perm),

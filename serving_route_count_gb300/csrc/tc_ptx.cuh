@@ -181,11 +181,32 @@ TC_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
+// Tensor memory is allocated, and the allocation permit given up, before anything else a CTA
+// does (warp 0; the other warps go on).  While a CTA of a kernel that uses tensor memory still
+// holds its permit, no further CTA of that kernel starts on the same SM (measured: the SM's
+// second CTA starts only once the first has relinquished, or exited if it never does, with
+// shared memory and tensor memory to spare), so a global read or a dependency wait placed
+// before the allocation holds back the SM's other CTAs by its whole latency.
+TC_DEV void tmem_alloc_first(uint32_t* dst, uint32_t ncols) {
+  if ((threadIdx.x >> 5) == 0) {
+    tmem_alloc(dst, ncols);
+    tmem_relinquish();
+  }
+}
+// Early exit of a CTA that allocated at entry: every thread of the CTA takes the branch.
+TC_DEV void tmem_exit_early(const uint32_t* s_tmem, uint32_t ncols);
+
 TC_DEV void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 TC_DEV void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+TC_DEV void tmem_exit_early(const uint32_t* s_tmem, uint32_t ncols) {
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if ((threadIdx.x >> 5) == 0) tmem_dealloc(*s_tmem, ncols);
 }
 // 32 rows x 16 bytes of scale factors -> TMEM, replicated to the four 32-lane quadrants.
 TC_DEV void tc_cp_sf(uint32_t taddr, uint64_t desc) {
