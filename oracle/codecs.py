@@ -224,6 +224,40 @@ def bf16_alternates(v: np.ndarray, rel: float, atol=0.0):
     return mask, np.where(mask, other, near)
 
 
+# ---------------------------------------------------------------------------- static FP8
+
+def fp8_static_quantize(v, s):
+    """Static per-tensor symmetric FP8 (hybrid_loader.py ``_build_kept_mxfp4``: the A8 opt-in
+    selects ``kFp8StaticTensorSym`` for the kept experts, whose layer carries one fp32
+    ``w13_input_scale`` / ``w2_input_scale``).  Reading (the page gives no arithmetic): each
+    step in fp32 - the activation times the fp32 reciprocal of the scale, rounded to E4M3
+    (nearest, ties to even, saturating at +-448) - and the dequantised value is code x s.
+    Returns (codes uint8, dequantised values fp64) with the shape of v."""
+    s32 = np.float32(s)
+    inv = np.float32(1.0) / s32
+    v32 = np.asarray(v, dtype=np.float64).astype(np.float32)
+    codes = e4m3_encode_rne_sat((v32 * inv).astype(np.float64))
+    return codes, e4m3_decode(codes) * np.float64(s32)
+
+
+def fp8_static_alternates(v, s, rel: float, atol=0.0):
+    """As mxfp8_alternates for the static per-tensor FP8 rounding of fp8_static_quantize: the
+    elements whose scaled value v / s lies within rel * |v / s| + atol / s of the midpoint of its
+    two E4M3 neighbours, and the neighbour's dequantised value."""
+    v = np.asarray(v, dtype=np.float64)
+    s64 = np.float64(np.float32(s))
+    _, near = fp8_static_quantize(v, s)
+    a = np.abs(v) / s64
+    lo = np.clip(np.searchsorted(_E4M3_POS, np.minimum(a, E4M3_MAX), side="right") - 1, 0, 126)
+    hi = np.minimum(lo + 1, 126)
+    mid = (_E4M3_POS[lo] + _E4M3_POS[hi]) / 2
+    tol = rel * a + np.broadcast_to(np.asarray(atol, dtype=np.float64), v.shape) / s64
+    mask = (np.abs(a - mid) <= tol) & (hi != lo) & (a < E4M3_MAX)
+    other_mag = np.where(np.abs(near) / s64 == _E4M3_POS[lo], _E4M3_POS[hi], _E4M3_POS[lo])
+    alt = np.where(mask, np.copysign(other_mag * s64, v), near)
+    return mask, alt
+
+
 # ---------------------------------------------------------------------------- NVFP4 activations
 
 NV_BLOCK = 16

@@ -17,7 +17,10 @@ Readings where the pages are silent (each one is listed with its reason in the d
     the expert's activation global scale in fp32, quantised (OCP MX rule, or NVFP4 blocks of 16
     with an E4M3 scale of vmax / 6), dequantised and divided by the scale.
   * Hybrid layers: the kept tier is NVFP4, or MXFP4 for hybrid_loader.py's "v3" kept format
-    (``_build_kept_mxfp4``, A16 default); either way with bf16 activations.
+    (``_build_kept_mxfp4``, A16 default); either way with bf16 activations, except for the A8
+    opt-in of the MXFP4 kept tier (``kept_a8``): its experts' x and h are static per-tensor FP8
+    with the layer's two input scales (codecs.fp8_static_quantize), h taken from the unrounded
+    SwiGLU output as for W4A8; the NF3 experts keep bf16 activations.
   * The result is accumulated in fp64 over the top-k slots and rounded to bf16 once.
   * Routing order: the slots of expert e are listed in ascending (t, j) order (stable
     counting sort).
@@ -187,6 +190,16 @@ def requant_h(h: np.ndarray, a8: bool, a=None) -> np.ndarray:
     return C.bf16_round(h)
 
 
+def kept_a8_scales(ck, e: int, kept_a8: bool):
+    """(w13 input scale, w2 input scale) of expert e when the A8 opt-in of the MXFP4 kept tier
+    applies to it (hybrid_loader.py ``_build_kept_mxfp4``, ``HYBRID_MX_A8``), else None."""
+    if not kept_a8:
+        return None
+    assert ck.quant == "hybrid" and ck.nv.quant == "mxfp4", "A8 opt-in: MXFP4 kept tier only"
+    t, _ = tier_local_index(ck.tier)[e]
+    return (ck.in13, ck.in2) if t == TIER_NVFP4 else None
+
+
 def slot_input(xin, w_slot, weight_on_input):
     """fc1 input and combine weight of slots: x and w, or with the router weight applied to the
     input (B12xExperts ``apply_router_weight_on_input``, W4A16 only) bf16(x * bf16(w)) and 1 -
@@ -197,7 +210,7 @@ def slot_input(xin, w_slot, weight_on_input):
 
 
 def moe_forward(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.0,
-                rows=None, return_f64=False, weight_on_input=False):
+                rows=None, return_f64=False, weight_on_input=False, kept_a8=False):
     """Per-expert dgemm form.  ``rows`` restricts the output to a subset of token rows
     (the other rows are not computed and come back as NaN).  Returns bf16 bit patterns
     [M, H] (and the unrounded fp64 sum when ``return_f64``).  ``weight_on_input``: the router
@@ -210,7 +223,7 @@ def moe_forward(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.
     M, k = ids.shape
     E, H, I = ck.E, ck.H, ck.I
     a8 = activation_a8(ck)
-    assert not ((a8 or activation_nv4(ck)) and weight_on_input), \
+    assert not ((a8 or activation_nv4(ck) or kept_a8) and weight_on_input), \
         "router weights on the input need 16-bit activations"
     out = np.zeros((M, H), dtype=np.float64)
     row_mask = np.ones(M, dtype=bool)
@@ -234,10 +247,16 @@ def moe_forward(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.
             xin = nvfp4_act(C.bf16_bits_to_f64(x_bits[t_idx]), a1[e])
         elif a1 is not None:   # MXFP8 activations with the expert's global scale
             xin = quantize_x(x_bits[t_idx], True, a1[e])[2]
+        s8 = kept_a8_scales(ck, int(e), kept_a8)
+        if s8 is not None:     # static per-tensor FP8 activations of the kept tier
+            xin = C.fp8_static_quantize(C.bf16_bits_to_f64(x_bits[t_idx]), s8[0])[1]
         G = xin @ W13.T
         gate, up = split_w13(G, I, ck.layout)
         h = swiglu(gate, up, limit, alpha, beta)
-        hh = nvfp4_act(h, a2[e]) if nv4 else requant_h(h, a8, None if a2 is None else a2[e])
+        if s8 is not None:
+            hh = C.fp8_static_quantize(h, s8[1])[1]
+        else:
+            hh = nvfp4_act(h, a2[e]) if nv4 else requant_h(h, a8, None if a2 is None else a2[e])
         y = hh @ W2.T
         np.add.at(out, t_idx, cw[:, None] * y)
     out[~row_mask] = np.nan
@@ -248,7 +267,7 @@ def moe_forward(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.
 
 
 def slot_intermediate(ck, x_bits, topk_ids, limit=math.inf, alpha=1.0, beta=0.0, topk_w=None,
-                      weight_on_input=False):
+                      weight_on_input=False, kept_a8=False):
     """The SwiGLU output h (fp64, before the fc2 quantisation) of every valid slot, in routing
     order (row p belongs to flat slot perm[p]); shape [S, I].  With ``weight_on_input`` the
     slots' inputs are scaled by ``topk_w`` as in moe_forward."""
@@ -270,6 +289,9 @@ def slot_intermediate(ck, x_bits, topk_ids, limit=math.inf, alpha=1.0, beta=0.0,
             xin = nvfp4_act(C.bf16_bits_to_f64(np.asarray(x_bits)[fl // k]), a1[e])
         elif a1 is not None:
             xin = quantize_x(np.asarray(x_bits)[fl // k], True, a1[e])[2]
+        s8 = kept_a8_scales(ck, e, kept_a8)
+        if s8 is not None:
+            xin = C.fp8_static_quantize(C.bf16_bits_to_f64(np.asarray(x_bits)[fl // k]), s8[0])[1]
         if weight_on_input:
             xin, _ = slot_input(xin, np.asarray(topk_w, np.float64).reshape(-1)[fl], True)
         G = xin @ W13.T
@@ -279,7 +301,7 @@ def slot_intermediate(ck, x_bits, topk_ids, limit=math.inf, alpha=1.0, beta=0.0,
 
 
 def requant_alternatives(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.0,
-                         rel=1e-4, rows=None, weight_on_input=False):
+                         rel=1e-4, rows=None, weight_on_input=False, kept_a8=False):
     """Legitimate alternatives of the fc2 operand's rounding (reading: where floating point
     decides a quantised code, arithmetic exact to a relative error `rel` may land on either
     neighbour of a near-midpoint value).  For every output row (or the given rows) returns a list
@@ -289,7 +311,7 @@ def requant_alternatives(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0
     w = np.asarray(topk_w, dtype=np.float64)
     M, k = ids.shape
     a8 = activation_a8(ck)
-    h = slot_intermediate(ck, x_bits, ids, limit, alpha, beta, topk_w, weight_on_input)
+    h = slot_intermediate(ck, x_bits, ids, limit, alpha, beta, topk_w, weight_on_input, kept_a8)
     _, _, perm, _ = route(ids, ck.E)
     a2 = act_gscale(ck, "a2")
     if activation_nv4(ck):
@@ -308,6 +330,14 @@ def requant_alternatives(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0
     else:
         mask, alt = C.bf16_alternates(h, rel)
         near = C.bf16_round(h)
+        if kept_a8:
+            # the kept tier's slots round h to static FP8 with the w2 input scale
+            kept = np.array([kept_a8_scales(ck, int(e), True) is not None
+                             for e in ids.reshape(-1)[perm]], dtype=bool)
+            if kept.any():
+                m8, a8v = C.fp8_static_alternates(h[kept], ck.in2, rel)
+                mask[kept], alt[kept] = m8, a8v
+                near[kept] = C.fp8_static_quantize(h[kept], ck.in2)[1]
     want = set(range(M)) if rows is None else set(int(r) for r in rows)
     out = {r: [] for r in want}
     cache = {}
@@ -324,8 +354,20 @@ def requant_alternatives(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0
     return out
 
 
+def _fp8_static_scalar(v: float, s) -> float:
+    """One value through static per-tensor FP8, by exhaustive search for the brute force:
+    p = fp32(fp32(v) * fp32(1 / s)); the E4M3 magnitude nearest to min(|p|, 448) among the 127
+    finite codes (ties to the even code); with p's sign, times s."""
+    s32 = np.float32(s)
+    p = float(np.float32(np.float32(v) * (np.float32(1.0) / s32)))
+    mag = min(abs(p), 448.0)
+    code = min(range(127), key=lambda c: (abs(C.e4m3_value(c) - mag), c % 2))
+    return math.copysign(C.e4m3_value(code), p) * float(s32)
+
+
 def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1.0, beta=0.0,
-                           weight_on_input=False, fc2_override=None, return_f64=False):
+                           weight_on_input=False, fc2_override=None, return_f64=False,
+                           kept_a8=False):
     """Token by token, slot by slot, element by element (pure Python loops; tiny inputs only).
     Dequantises each weight element from its own code and scale with scalar decoders.
     ``weight_on_input``: each input element becomes the bf16 rounding of x * bf16(w) and the
@@ -378,6 +420,10 @@ def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1
                 xt = nvfp4_act(C.bf16_bits_to_f64(np.asarray(x_bits)[t:t + 1]), a1[e])[0]
             elif a1 is not None:
                 xt = quantize_x(np.asarray(x_bits)[t:t + 1], True, a1[e])[2][0]
+            s8 = kept_a8_scales(ck, e, kept_a8)
+            if s8 is not None:
+                xt = [_fp8_static_scalar(float(v), s8[0])
+                      for v in C.bf16_bits_to_f64(np.asarray(x_bits)[t])]
             cw = w[t][j]
             if weight_on_input:
                 wb = float(C.bf16_round(cw))
@@ -400,8 +446,11 @@ def moe_forward_bruteforce(ck, x_bits, topk_ids, topk_w, limit=math.inf, alpha=1
                 g = min(gate[i], limit)
                 u = max(-limit, min(up[i], limit))
                 h[i] = g * (1.0 / (1.0 + math.exp(-alpha * g))) * (u + beta)
-            hh = (nvfp4_act(np.array(h)[None, :], a2[e])[0] if activation_nv4(ck) else
-                  requant_h(np.array(h), a8, None if a2 is None else a2[e])).tolist()
+            if s8 is not None:
+                hh = [_fp8_static_scalar(v, s8[1]) for v in h]
+            else:
+                hh = (nvfp4_act(np.array(h)[None, :], a2[e])[0] if activation_nv4(ck) else
+                      requant_h(np.array(h), a8, None if a2 is None else a2[e])).tolist()
             for i, v in ((fc2_override or {}).get((t, j)) or {}).items():
                 hh[i] = float(v)
             for r in range(H):

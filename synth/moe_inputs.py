@@ -143,6 +143,9 @@ class Checkpoint:
     tier: Optional[np.ndarray] = None        # [E] int8, TIER_NVFP4 or TIER_NF3
     nv: Optional["Checkpoint"] = None        # kept tier (NVFP4, or MXFP4), compact over its experts
     nf: Optional["Checkpoint"] = None        # NF3 tier, compact over its experts
+    # hybrid with an MXFP4 kept tier: the layer's static FP8 input scales (fp32 scalars)
+    in13: Optional[float] = None
+    in2: Optional[float] = None
 
 
 def _bytes(rng, shape, lo=0, hi=255):
@@ -215,6 +218,11 @@ def make_checkpoint(cfg: MoEConfig, seed: Optional[int] = None, E: Optional[int]
             ck.nv = make_fp4_checkpoint(rng, "nvfp4", n4, H, I, cfg.scale_lo, cfg.scale_hi,
                                         layout)
         ck.nf = make_nf3_checkpoint(rng, E - n4, H, I, cfg.scale_lo, cfg.scale_hi, layout)
+        if cfg.quant == "hybrid_mx":
+            # w13_input_scale / w2_input_scale of the kept tier's A8 opt-in: calibration amax
+            # / 448, log-uniform over a factor 2 around an amax of 5 for x and 8 for h
+            ck.in13 = float(np.float32(5.0 / 448.0 * 2.0 ** rng.uniform(-0.5, 0.5)))
+            ck.in2 = float(np.float32(8.0 / 448.0 * 2.0 ** rng.uniform(-0.5, 0.5)))
         return ck
     raise ValueError(cfg.quant)
 

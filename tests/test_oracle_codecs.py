@@ -273,3 +273,79 @@ def test_nvfp4_properties():
     near = C.nvfp4_dequantize(q, s)
     assert np.all(alt[~mask] == near[~mask])
     assert mask.mean() < 1e-2
+
+
+# ---------------------------------------------------------------------------- static FP8
+
+def test_fp8_static_worked_values():
+    """Hand-worked: s = 0.5 (1 / s = 2 exactly): 1.3 -> 2.6 lies between the E4M3 neighbours 2.5
+    (code 0x42: exponent 8, mantissa 2) and 2.75, nearer 2.5 -> 1.25; 300 -> 600 saturates to
+    448 (0x7E) -> 224; -0.001 -> -0.002, nearest the subnormal 2^-9 (0x81) -> -2^-10; 0 -> 0.
+    Ties go to the even mantissa: with s = 1, 2.625 (between 2.5 = 0x42 and 2.75 = 0x43) -> 2.5,
+    2.875 (between 2.75 and 3.0 = 0x44) -> 3.0."""
+    q, v = C.fp8_static_quantize(np.array([1.3, 300.0, -0.001, 0.0]), 0.5)
+    assert q.tolist() == [0x42, 0x7E, 0x81, 0x00]
+    assert v.tolist() == [1.25, 224.0, -2.0 ** -10, 0.0]
+    q, v = C.fp8_static_quantize(np.array([2.625, 2.875, -2.625, 464.0, 1e9]), 1.0)
+    assert q.tolist() == [0x42, 0x44, 0xC2, 0x7E, 0x7E]
+    assert v.tolist() == [2.5, 3.0, -2.5, 448.0, 448.0]
+
+
+def test_fp8_static_reciprocal_is_fp32():
+    """The scaled value is the fp32 product with the fp32 reciprocal of the scale, not the
+    exact quotient.  s = fp32(0.3), v = fp32 0x3DA33334 = 0.0796875059...: the exact quotient
+    v / s = 0.265625009... lies just above the midpoint 0.265625 of the E4M3 neighbours 0.25
+    (code 0x28) and 0.28125 (0x29), so it would round to 0x29; the fp32 product
+    v x fp32(1 / s) is exactly 0.265625, a tie, which goes to the even code 0x28."""
+    s = np.float32(0.3)
+    v = np.array([0x3DA33334], dtype=np.uint32).view(np.float32)[0]
+    assert float(np.float32(v * (np.float32(1.0) / s))) == 0.265625
+    assert float(v) / float(s) > 0.265625
+    q, deq = C.fp8_static_quantize(np.array([float(v)]), float(s))
+    assert int(q[0]) == 0x28 and deq[0] == 0.25 * float(s)
+
+
+def test_fp8_static_equals_mxfp8_when_the_block_scale_matches():
+    """Closed form against the pinned MX quantiser: for a power-of-two scale s = 2^k and a
+    block whose largest magnitude lies in [256 s, 512 s), the MX scale byte is 127 + k, so the
+    MXFP8 codes of the block are the static FP8 codes (both round v / s to E4M3, saturating)."""
+    rng = np.random.default_rng(5)
+    for k in (-9, -3, 0, 4):
+        s = 2.0 ** k
+        v = rng.normal(0, 60 * s, size=(50, 32))
+        v[:, 0] = rng.uniform(256 * s, 511 * s, size=50)
+        qs, _ = C.fp8_static_quantize(v, s)
+        qm, sm = C.mxfp8_quantize(v)
+        assert np.all(sm == 127 + k)
+        assert np.array_equal(qs, qm)
+
+
+def test_fp8_static_matches_exhaustive_search():
+    """Against a scalar exhaustive search (nearest of the 127 finite magnitudes, ties to the
+    even code, saturating), on random values, exact midpoints and out-of-range values."""
+    rng = np.random.default_rng(9)
+    s = float(np.float32(0.0173))
+    inv = np.float32(1.0) / np.float32(s)
+    mids = (C.E4M3_TABLE[1:127] + C.E4M3_TABLE[:126]) / 2
+    vals = np.concatenate([rng.normal(0, 3, 400), mids[::5] * s, [500 * s, -1e6, 0.0]])
+    q, deq = C.fp8_static_quantize(vals, s)
+    grid = [C.e4m3_value(c) for c in range(127)]
+    for v, qc, d in zip(vals, q, deq):
+        p = float(np.float32(np.float32(v) * inv))
+        mag = min(abs(p), 448.0)
+        c = min(range(127), key=lambda c: (abs(grid[c] - mag), c % 2))
+        assert int(qc) & 0x7F == c
+        assert d == math.copysign(grid[c], p) * float(np.float32(s)) or (c == 0 and d == 0)
+
+
+def test_fp8_static_alternates_worked():
+    """With s = 1: 2.6249 and 2.6251 sit within 1e-4 of the midpoint 2.625 of 2.5 and 2.75 -
+    nearest 2.5 and 2.75, alternates 2.75 and 2.5; 2.55 is far from any midpoint (no
+    alternate); with s = 0.25 the same scaled values give the same decisions, values x 0.25."""
+    for s in (1.0, 0.25):
+        v = np.array([2.6249, 2.6251, 2.55]) * s
+        mask, alt = C.fp8_static_alternates(v, s, 1e-4)
+        _, near = C.fp8_static_quantize(v, s)
+        assert mask.tolist() == [True, True, False]
+        assert (near / s).tolist() == [2.5, 2.75, 2.5]
+        assert (alt / s).tolist() == [2.75, 2.5, 2.5]

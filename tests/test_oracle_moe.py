@@ -636,3 +636,94 @@ def test_ep_mask_foreign_hand_worked():
     got_ids, _ = S.ep_mask_foreign(np.array([[4, 0], [7, 2]], np.int32),
                                    np.ones((2, 2), np.float32), 4, 4)
     assert got_ids.tolist() == [[0, 0], [3, 3]]
+
+
+# ---------------------------------------------------------------------------- kept-tier A8
+
+def _a8_case(seed=4):
+    cfg, ck = _tiny("hybrid_mx", seed=seed)
+    rng = np.random.default_rng(200 + seed)
+    M, k = 6, 2
+    x = S.make_x(rng, M, ck.H)
+    ids = S.uniform_topk(rng, M, ck.E, k)
+    w = S.router_weights(rng, M, k, "softmax", 1.0)
+    return ck, x, ids, w
+
+
+def test_kept_a8_forward_matches_bruteforce():
+    """The A8 opt-in of the MXFP4 kept tier: the dgemm forward against the element loop, whose
+    static FP8 rounding is its own exhaustive search (not codecs.fp8_static_quantize)."""
+    ck, x, ids, w = _a8_case()
+    tier = np.asarray(ck.tier)
+    assert (tier[ids] == S.TIER_NVFP4).any() and (tier[ids] == S.TIER_NF3).any()
+    a, f64 = O.moe_forward(ck, x, ids, w, return_f64=True, kept_a8=True)
+    b, g64 = O.moe_forward_bruteforce(ck, x, ids, w, kept_a8=True, return_f64=True)
+    assert np.allclose(f64, g64, rtol=1e-12, atol=1e-12 * np.abs(f64).max())
+    # the opt-in changes the result (x and h go through FP8 for the kept experts)
+    a16 = O.moe_forward(ck, x, ids, w, return_f64=True)[1]
+    kept_rows = (tier[ids] == S.TIER_NVFP4).any(axis=1)
+    assert not np.allclose(a16[kept_rows], f64[kept_rows], rtol=1e-6, atol=0)
+
+
+def test_kept_a8_leaves_nf3_rows_and_matches_its_definition():
+    """Rows routed only to NF3 experts are the A16 result exactly; for a kept expert the
+    slot's output is W2 . fp8s(SwiGLU(W13 . fp8s(x, s13)), s2) with the weights dequantised by
+    oracle.moe.expert_weights and fp8s the static quantiser - checked on one slot directly."""
+    ck, x, ids, w = _a8_case(seed=6)
+    tier = np.asarray(ck.tier)
+    ids[0] = np.nonzero(tier == S.TIER_NF3)[0][:2]          # a row on NF3 experts only
+    ids[1, 0] = np.nonzero(tier == S.TIER_NVFP4)[0][0]       # and one with a kept expert
+    f8 = O.moe_forward(ck, x, ids, w, return_f64=True, kept_a8=True)[1]
+    f16 = O.moe_forward(ck, x, ids, w, return_f64=True)[1]
+    nf_rows = (tier[ids] == S.TIER_NF3).all(axis=1)
+    assert nf_rows.any()
+    assert np.array_equal(f8[nf_rows], f16[nf_rows])
+    t, j = [(t, j) for t in range(ids.shape[0]) for j in range(ids.shape[1])
+            if tier[ids[t, j]] == S.TIER_NVFP4][0]
+    e = int(ids[t, j])
+    W13, W2, _ = O.expert_weights(ck, e)
+    xq = C.fp8_static_quantize(C.bf16_bits_to_f64(x[t]), ck.in13)[1]
+    gate, up = O.split_w13(W13 @ xq, ck.I, ck.layout)
+    y = W2 @ C.fp8_static_quantize(O.swiglu(gate, up), ck.in2)[1]
+    one = np.zeros_like(ids)
+    one[:] = -1
+    one[t, j] = e
+    single = O.moe_forward(ck, x, one, w, return_f64=True, kept_a8=True)[1][t]
+    assert np.allclose(single, w[t, j] * y, rtol=1e-13, atol=1e-13 * np.abs(y).max())
+
+
+def test_kept_a8_requant_alternatives_pinned_by_flipping():
+    """requant_alternatives with the A8 opt-in: for a kept-tier slot, the intermediate element
+    nearest (relative to its size) a static-FP8 midpoint is taken the other way in the element
+    loop (its other E4M3 neighbour times s2, from the E4M3 grid), and the token's output change
+    must be one of the vectors the helper lists."""
+    ck, x, ids, w = _a8_case(seed=4)
+    tier = np.asarray(ck.tier)
+    k = ids.shape[1]
+    t, j = [(t, j) for t in range(ids.shape[0]) for j in range(k)
+            if tier[ids[t, j]] == S.TIER_NVFP4][0]
+    _, _, perm, slot_of = O.route(ids, ck.E)
+    h = O.slot_intermediate(ck, x, ids, kept_a8=True)[slot_of[t * k + j]]
+    s2 = float(np.float32(ck.in2))
+    grid = sorted(set(C.E4M3_TABLE[:127].tolist()))
+    best = None
+    for i in range(ck.I):
+        a = abs(h[i]) / s2
+        if a == 0 or a >= 448:
+            continue
+        lo, hi = _other_neighbour(a, grid)
+        dist = abs(a - (lo + hi) / 2) / a
+        near = float(C.fp8_static_quantize(np.array([h[i]]), ck.in2)[1][0])
+        other = hi if abs(near) == lo * s2 else lo
+        if best is None or dist < best[0]:
+            best = (dist, i, math.copysign(other * s2, h[i]))
+    dist, i, alt = best
+    alts = O.requant_alternatives(ck, x, ids, w, rel=max(1.5 * dist, 1e-9), rows=[t],
+                                  kept_a8=True)[t]
+    _, base = O.moe_forward_bruteforce(ck, x, ids, w, kept_a8=True, return_f64=True)
+    _, flip = O.moe_forward_bruteforce(ck, x, ids, w, kept_a8=True,
+                                       fc2_override={(t, j): {i: alt}}, return_f64=True)
+    want = flip[t] - base[t]
+    assert np.abs(want).max() > 0
+    tol = 1e-12 * np.abs(base[t]).max()
+    assert any(np.allclose(d, want, rtol=0, atol=tol) for d in alts), (i, len(alts))
