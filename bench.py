@@ -367,9 +367,18 @@ def _mode_expert_bytes(kind, I, H):
 def modes_report(stream, flush, hbm_peak):
     """Secondary report: whole-call times of the other weight / activation formats at decode,
     mid and prefill sizes (one graph replay per M after an L2 flush), with the fraction of the
-    HBM roofline over the touched experts' bytes."""
+    HBM roofline over the touched experts' bytes, the dense tensor rate (2 x 3 x I x H flops per
+    routed slot) and, for W4A4 (`kind::mxf4nvf4`), its fraction of the dense FP4 peak."""
     import torch
     from serving_route_count_gb300 import MoELayer
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    # dense FP4 peak: the measured bf16 GEMM rate x the nominal FP4 / bf16 ratio 13.5 / 2.25 = 6
+    fp4_peak = 6.0 * float(peaks.get("bf16_tflops", 1900.0))
     out = {}
     for name in MODE_CFGS:
         cfg = S.CONFIGS[name]
@@ -409,14 +418,21 @@ def modes_report(stream, flush, hbm_peak):
                                                 cfg.I, cfg.H) for e in touched)
             else:
                 nbytes = len(touched) * _mode_expert_bytes("nvfp4", cfg.I, cfg.H)
+            slots = int(((ids >= 0) & (ids < cfg.E)).sum())
+            tflops = 2.0 * 3 * cfg.I * cfg.H * slots / sec / 1e12
             res[str(M)] = {"us": round(sec * 1e6, 1), "tokens_per_s": round(M / sec),
-                           "hbm_frac": round(nbytes / sec / 1e9 / hbm_peak, 3)}
+                           "hbm_frac": round(nbytes / sec / 1e9 / hbm_peak, 3),
+                           "tflops": round(tflops, 1)}
+            if name == "w4a4_nvfp4":
+                res[str(M)]["fp4_dense_frac"] = round(tflops / fp4_peak, 4)
         layer.close()
         del ck
         out[name] = res
     return {"workload": "E=256 H=6144 I=512 top-8 (Zipf 0.8 routing for the hybrids), atomic "
                         "combine; one graph replay per M after an L2 flush; hbm_frac over the "
                         "touched experts' checkpoint-format bytes",
+            "fp4_dense_peak_tflops": round(fp4_peak, 1),
+            "fp4_peak_basis": "measured bf16 dense rate x nominal FP4/bf16 ratio 6 (13.5 / 2.25)",
             "calls": out}
 
 

@@ -194,6 +194,19 @@ moe_status moe_plan_set_fc1_kernel(moe_plan_t* plan, int choice);
  * the pages refuse too). */
 moe_status moe_plan_set_router_weight_on_input(moe_plan_t* plan, int on);
 
+/* A8 opt-in of the MXFP4 kept tier (hybrid_loader.py `_build_kept_mxfp4`: `HYBRID_MX_A8`
+ * selects static per-tensor symmetric FP8 activations for the kept experts, with the layer's
+ * `w13_input_scale` / `w2_input_scale`).  MOE_W4A16_HYBRID_MX plans only.  With both scales
+ * > 0, each kept-tier slot's fc1 input is E4M3(fp32(x) * fp32(1 / w13_input_scale)) (nearest
+ * even, saturating at +-448) times w13_input_scale, and its fc2 input the same of the fp32
+ * SwiGLU output with w2_input_scale; the NF3 experts keep bf16 activations.  Both scales 0
+ * turns it off (default).  Errors: MOE_ERR_ARG (plan NULL; a scale negative, NaN, infinite, or
+ * one whose fp32 reciprocal is not finite and nonzero; one scale 0 and not the other),
+ * MOE_ERR_UNSUPPORTED (another mode, router weights on the input, or the CUDA-core backend:
+ * moe_plan_set_backend(plan, 1) and moe_plan_set_router_weight_on_input(plan, 1) are refused
+ * the same way while it is on). */
+moe_status moe_plan_set_kept_a8(moe_plan_t* plan, float w13_input_scale, float w2_input_scale);
+
 /* Expert parallelism (moe_b12x_next.py `ep_remap` / `ep_remap_reference`): this plan's E
  * experts are the global experts [first_expert, first_expert + E).  topk_ids then hold global
  * ids; routing maps each to its local id (id - first_expert) on the device, and ids of other

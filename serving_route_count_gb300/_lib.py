@@ -44,6 +44,7 @@ SIGNATURES = {
     "moe_plan_set_router_weight_on_input": (c_int, [c_void_p, c_int]),
     "moe_plan_set_debug_copies": (c_int, [c_void_p, c_int]),
     "moe_plan_set_wait_probe": (c_int, [c_void_p, ctypes.c_ulonglong]),
+    "moe_plan_set_kept_a8": (c_int, [c_void_p, ctypes.c_float, ctypes.c_float]),
     "moe_run": (c_int, [c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p, c_void_p,
                         c_void_p, c_int, c_void_p]),
     "moe_unprepare_weights": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p]),

@@ -19,7 +19,7 @@ cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r,
                         bool atoms, bool to_f16, const float* win, const float* ag,
                         const int32_t* ids, int ep_first, int E, bool nv4, void* z0,
                         size_t z0_words, void* z1, size_t z1_words, void* z2, size_t z2_words,
-                        cudaStream_t st);
+                        KeptA8 ka8, cudaStream_t st);
 bool route_actq_small_supported(int Mk, int E);
 int route_chunks(int Mk);
 cudaError_t launch_route_count(const int32_t* ids, int Mk, int E, int ep_first,
@@ -34,7 +34,7 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_fi
                                     const RunPtrs& r, bool atoms, bool to_f16, const float* win,
                                     const float* ag, bool nv4, bool skip_x, void* z0,
                                     size_t z0_words, void* z1, size_t z1_words, void* z2,
-                                    size_t z2_words, cudaStream_t st);
+                                    size_t z2_words, KeptA8 ka8, cudaStream_t st);
 // gemm_tc.cu
 cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                             int bn, int tiles, int splits, const float* topk_w, int M,
@@ -380,6 +380,7 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   d.quant = quant_mode; d.deterministic = deterministic ? 1 : 0;
   d.limit = swiglu_limit; d.alpha = 1.f; d.beta = 0.f; d.backend = 0; d.fc1_kernel = 0;
   d.ep_first = 0; d.w_on_input = 0; d.keep_act = 0; d.wait_probe_ns = 0;
+  d.kept_a8 = 0; d.a8_s13 = d.a8_inv13 = d.a8_s2 = d.a8_inv2 = 0.f;
   const size_t Sm = (size_t)max_m * topk;
   Scratch& s = p->s;
   s.max_tiles = (int)std::min<size_t>(Sm, (Sm + kSimtSlots - 1) / kSimtSlots +
@@ -527,9 +528,32 @@ moe_status moe_plan_set_fc1_kernel(moe_plan_t* plan, int choice) {
 moe_status moe_plan_set_router_weight_on_input(moe_plan_t* plan, int on) {
   if (plan == nullptr || (on != 0 && on != 1)) return MOE_ERR_ARG;
   if (on && (plan->d.quant == MOE_W4A8_MXFP4 || plan->d.quant == MOE_W4A8_NVFP4 ||
-             plan->d.quant == MOE_W4A4_NVFP4))
+             plan->d.quant == MOE_W4A4_NVFP4 || plan->d.kept_a8))
     return MOE_ERR_UNSUPPORTED;
   plan->d.w_on_input = on;
+  return MOE_OK;
+}
+
+moe_status moe_plan_set_kept_a8(moe_plan_t* plan, float w13_input_scale, float w2_input_scale) {
+  if (plan == nullptr) return MOE_ERR_ARG;
+  if (plan->d.quant != MOE_W4A16_HYBRID_MX) return MOE_ERR_UNSUPPORTED;
+  if (w13_input_scale == 0.f && w2_input_scale == 0.f) {
+    plan->d.kept_a8 = 0;
+    plan->d.a8_s13 = plan->d.a8_inv13 = plan->d.a8_s2 = plan->d.a8_inv2 = 0.f;
+    return MOE_OK;
+  }
+  // fp32 reciprocals, as the method takes them: finite and nonzero for scales in range
+  const float inv13 = 1.0f / w13_input_scale, inv2 = 1.0f / w2_input_scale;
+  if (!(w13_input_scale > 0.f) || !(w2_input_scale > 0.f) || !std::isfinite(w13_input_scale) ||
+      !std::isfinite(w2_input_scale) || !std::isfinite(inv13) || !std::isfinite(inv2) ||
+      inv13 == 0.f || inv2 == 0.f)
+    return MOE_ERR_ARG;
+  if (plan->d.w_on_input || plan->d.backend == 1) return MOE_ERR_UNSUPPORTED;
+  plan->d.kept_a8 = 1;
+  plan->d.a8_s13 = w13_input_scale;
+  plan->d.a8_inv13 = inv13;
+  plan->d.a8_s2 = w2_input_scale;
+  plan->d.a8_inv2 = inv2;
   return MOE_OK;
 }
 
@@ -554,7 +578,8 @@ moe_status moe_plan_set_expert_offset(moe_plan_t* plan, int first_expert) {
 
 moe_status moe_plan_set_backend(moe_plan_t* plan, int backend) {
   if (plan == nullptr || backend < 0 || backend > 1) return MOE_ERR_ARG;
-  if (backend == 1 && (plan->d.quant == MOE_W4A8_NVFP4 || plan->d.quant == MOE_W4A4_NVFP4))
+  if (backend == 1 && (plan->d.quant == MOE_W4A8_NVFP4 || plan->d.quant == MOE_W4A4_NVFP4 ||
+                       plan->d.kept_a8))
     return MOE_ERR_UNSUPPORTED;
   plan->d.backend = backend;
   return MOE_OK;
@@ -633,12 +658,14 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   // combine adds the expert outputs with weight 1
   const float* win = d.w_on_input ? topk_weights : nullptr;
   const float* wcomb = d.w_on_input ? nullptr : topk_weights;
+  // the MXFP4 kept tier's A8 opt-in: its slots' activations are static FP8
+  const KeptA8 ka8{d.kept_a8 ? w.tier_map : nullptr, d.a8_inv13};
   prof(0);
   cudaError_t e;
   if (small) {
     e = launch_route_actq_small(topk_ids, Sm, d.E, d.ep_first, bn, plan->s.max_tiles, x, d.H,
                                 d.topk, r, atoms, t16, win, w.ag13, t4, fuse_x, acc, acc_words,
-                                g, g_words, tk, tk_words, st);
+                                g, g_words, tk, tk_words, ka8, st);
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
   } else if (tc8) {
@@ -656,7 +683,7 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
     prof(1);
     if (a8 || acc || g || t16 || t4) {
       e = launch_actq(x, M, d.H, d.topk, r, a8, atoms, t16, win, w.ag13, topk_ids, d.ep_first,
-                      d.E, t4, acc, acc_words, g, g_words, tk, tk_words, st);
+                      d.E, t4, acc, acc_words, g, g_words, tk, tk_words, ka8, st);
       if (e != cudaSuccess) return cuda_status(e);
     }
   }

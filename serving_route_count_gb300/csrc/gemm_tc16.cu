@@ -83,6 +83,10 @@ struct Tc16Params {
   const float* agscale;       // MXFP8 activations: per-expert activation global scale of this
                               // GEMM's input ([E]); nullptr: 16-bit activations
   const float* agscale2;      // fc1 with MXFP8 activations: that of fc2's input (h)
+  // A8 opt-in of the MXFP4 kept tier (0: off): the static FP8 input scale of this GEMM's
+  // activations, which the kept tier's operands carry as E4M3 code values; and, for fc1, the
+  // fp32 reciprocal of fc2's input scale, by which h is quantised
+  float a8_s, a8_inv_next;
   const int4* tiles;
   const int32_t* ctrl;
   int32_t* err;
@@ -216,6 +220,12 @@ __device__ __forceinline__ uint16_t h_to_f16(float h, int32_t* err) {
 // the expert's activation global scale a2, quantised by the OCP MX rule and returned as the f16
 // of the dequantised value E4M3 x 2^(s-127) (exact while the block scale is at most 2^7: larger
 // sets the range bit).  All 32 lanes call it with the same column.
+// Static per-tensor FP8 (the kept tier's A8 opt-in): the E4M3 code of fp32(h * inv) (nearest
+// even, saturating) as the f16 of the code's value (exact); the scale joins fc2's epilogue.
+__device__ __forceinline__ uint16_t h_to_f16_fp8s(float h, float inv) {
+  return __half_as_ushort(__float2half_rn(e4m3_to_f32((uint8_t)f32_to_e4m3(__fmul_rn(h, inv)))));
+}
+
 __device__ __forceinline__ uint16_t h_to_f16_mx(float h, float a2, int32_t* err) {
   const float v = h * a2;
   float amax = fabsf(v);
@@ -408,7 +418,9 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
     // weight global (NVFP4) over the activation global (MXFP8 activations carry a * x)
     const float gs = ((!nf3 && p.gscale != nullptr) ? p.gscale[le] : 1.f) /
-                     (p.agscale != nullptr ? p.agscale[e] : 1.f);
+                     (p.agscale != nullptr ? p.agscale[e] : 1.f) *
+                     ((!nf3 && p.a8_s != 0.f) ? p.a8_s : 1.f);
+    const float a8_inv = nf3 ? 0.f : p.a8_inv_next;
     const float a_next = (!FC2 && p.agscale2 != nullptr) ? p.agscale2[e] : 0.f;
     if (ok && nsub > 0) {
 #pragma unroll 1
@@ -454,7 +466,8 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
                                                    p.beta)
                                         : 0.f;
               p.h16[(size_t)pos * p.Ip + row] =
-                  p.agscale2 != nullptr ? h_to_f16_mx(h, a_next, p.err) : h_to_f16(h, p.err);
+                  a8_inv != 0.f ? h_to_f16_fp8s(h, a8_inv)
+                  : p.agscale2 != nullptr ? h_to_f16_mx(h, a_next, p.err) : h_to_f16(h, p.err);
             } else {
               float* gg = p.gacc + ((size_t)split * p.Sm + pos) * 2 * p.Ip;
               gg[row] = v0[j];
@@ -495,8 +508,10 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
       const int quad = warp & 3;
       const int row = rb * 128 + quad * 32 + lane;
       const float gs = ((!nf3 && p.gscale != nullptr) ? p.gscale[le] : 1.f) /
-                       (p.agscale != nullptr ? p.agscale[e] : 1.f);
+                       (p.agscale != nullptr ? p.agscale[e] : 1.f) *
+                       ((!nf3 && p.a8_s != 0.f) ? p.a8_s : 1.f);
       const float a_next = p.agscale2 != nullptr ? p.agscale2[e] : 0.f;
+      const float a8_inv = nf3 ? 0.f : p.a8_inv_next;
       // partial sums added in split order (the same result on every run), 16 columns at a
       // time with each split's 32 loads issued together
       for (int c0 = 0; c0 < n; c0 += 16) {
@@ -527,7 +542,8 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
             const float h = row < p.I ? swiglu16(gt[j] * gs, up[j] * gs, p.limit, p.alpha, p.beta)
                                       : 0.f;
             p.h16[(size_t)(p0 + c0 + j) * p.Ip + row] =
-                p.agscale2 != nullptr ? h_to_f16_mx(h, a_next, p.err) : h_to_f16(h, p.err);
+                a8_inv != 0.f ? h_to_f16_fp8s(h, a8_inv)
+                : p.agscale2 != nullptr ? h_to_f16_mx(h, a_next, p.err) : h_to_f16(h, p.err);
           }
         }
       }
@@ -610,6 +626,8 @@ cudaError_t launch_tc16_stage(int stage, const DevWeights& w, const RunPtrs& r, 
   p.mx = w.mx_kept;
   p.agscale = fc2 ? w.ag2 : w.ag13;
   p.agscale2 = fc2 ? nullptr : w.ag2;
+  p.a8_s = d.kept_a8 ? (fc2 ? d.a8_s2 : d.a8_s13) : 0.f;
+  p.a8_inv_next = (d.kept_a8 && !fc2) ? d.a8_inv2 : 0.f;
   p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
   p.h16 = reinterpret_cast<uint16_t*>(r.h16); p.gacc = r.g; p.tickets = r.tickets;
   p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;

@@ -179,6 +179,18 @@ struct PlanDims {
                     // also store the codes where moe_debug_actq reads them
   unsigned long long wait_probe_ns;   // test hook (0: off): W4A8 fc1's MMA issuer first waits
                     // this long on a barrier nothing arrives on, so the wait runs out
+  // A8 opt-in of the MXFP4 kept tier (hybrid MX mode): static FP8 input scales of fc1 / fc2
+  // and their fp32 reciprocals
+  int kept_a8;
+  float a8_s13, a8_inv13, a8_s2, a8_inv2;
+};
+
+// The kept tier's A8 opt-in for an activation producer: the slots of experts whose tier-map
+// entry is the kept tier (kTierNVFP4) get static per-tensor FP8 activations, E4M3 of
+// fp32(x) * inv; tiers == nullptr: off.
+struct KeptA8 {
+  const int32_t* tiers;
+  float inv;
 };
 
 // Local id of router id `id` on a plan that owns the global experts [first, first + E): id -

@@ -228,6 +228,27 @@ __device__ __forceinline__ uint4 bf16x8_scale(uint4 u, float wb) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Whether slot expert e takes the kept tier's static FP8 activations.
+__device__ __forceinline__ bool kept_a8_expert(const KeptA8& k, int e) {
+  return k.tiers != nullptr && e >= 0 && (k.tiers[e] >> 24) == kTierNVFP4;
+}
+
+// Eight bf16 values as static per-tensor FP8: the E4M3 code of fp32(x) * inv (nearest even,
+// saturating at 448), stored as the f16 of the code's value (E4M3 values are exact in f16).
+__device__ __forceinline__ uint4 bf16x8_to_fp8s_f16x8(uint4 u, float inv) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float a = e4m3_to_f32((uint8_t)f32_to_e4m3(__fmul_rn(__uint_as_float(w[j] << 16), inv)));
+    const float b =
+        e4m3_to_f32((uint8_t)f32_to_e4m3(__fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), inv)));
+    o[j] = (uint32_t)__half_as_ushort(__float2half_rn(a)) |
+           ((uint32_t)__half_as_ushort(__float2half_rn(b)) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // NVFP4 weights with MXFP8 activations: 32 activations times the expert's activation global
 // scale `a` (fp32 products), quantised by the OCP MX rule (as quantize_block32) and stored as the
 // f16 of each dequantised value E4M3 x 2^(s-127): exact while the block scale is within
@@ -312,7 +333,7 @@ actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t*
             const float* __restrict__ win, const float* __restrict__ ag,
             const int32_t* __restrict__ ids, int ep_first, int E, uint8_t* __restrict__ xq4,
             uint8_t* __restrict__ xs4, int32_t* __restrict__ err, ZeroRegion z0, ZeroRegion z1,
-            ZeroRegion z2) {
+            ZeroRegion z2, KeptA8 ka8) {
   pdl_wait_prev();
   pdl_launch_next();
   const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -367,6 +388,10 @@ actq_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk, const int32_t*
       const int c = (int)(i % nc);
       const int f = perm[p], t = f / topk;
       uint4 u = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c * 8);
+      if (ka8.tiers != nullptr && kept_a8_expert(ka8, local_expert(ids[f], ep_first, E))) {
+        *reinterpret_cast<uint4*>(x16 + p * H + c * 8) = bf16x8_to_fp8s_f16x8(u, ka8.inv);
+        continue;
+      }
       if (win != nullptr) u = bf16x8_scale(u, bf16_round(win[f]));   // weight on the input
       *reinterpret_cast<uint4*>(x16 + p * H + c * 8) = bf16x8_to_f16x8(u, range_ok);
     }
@@ -398,7 +423,7 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
                         uint8_t* __restrict__ xs16, int r16, uint16_t* __restrict__ x16,
                         const float* __restrict__ win, const float* __restrict__ ag,
                         uint8_t* __restrict__ xq4, uint8_t* __restrict__ xs4, ZeroRegion z0,
-                        ZeroRegion z1, ZeroRegion z2, int ep_first) {
+                        ZeroRegion z1, ZeroRegion z2, int ep_first, KeptA8 ka8) {
   constexpr int NW = kSmallRouteThreads / 32;
   __shared__ int s_ids[kSmallRouteSlots];
   __shared__ int s_perm[kSmallRouteSlots];
@@ -526,6 +551,10 @@ route_actq_small_kernel(const int32_t* __restrict__ ids, int Mk, int E, int tile
       const int c = (int)(i % nc);
       const int f = s_perm[p], t = f / topk;
       uint4 u = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c * 8);
+      if (kept_a8_expert(ka8, s_ids[f])) {
+        *reinterpret_cast<uint4*>(x16 + p * H + c * 8) = bf16x8_to_fp8s_f16x8(u, ka8.inv);
+        continue;
+      }
       if (win != nullptr) u = bf16x8_scale(u, bf16_round(win[f]));   // weight on the input
       *reinterpret_cast<uint4*>(x16 + p * H + c * 8) = bf16x8_to_f16x8(u, range_ok);
     }
@@ -782,7 +811,7 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_fi
                                     int topk, const RunPtrs& r, bool atoms, bool to_f16,
                                     const float* win, const float* ag, bool nv4, bool skip_x,
                                     void* z0, size_t z0_words, void* z1, size_t z1_words,
-                                    void* z2, size_t z2_words, cudaStream_t st) {
+                                    void* z2, size_t z2_words, KeptA8 ka8, cudaStream_t st) {
   if (!route_actq_small_supported(Mk, E)) return cudaErrorInvalidValue;
   // skip_x: the consumer quantises the activations itself (W4A8 only), this launch routes and
   // clears
@@ -804,7 +833,8 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_fi
                        to_f16 ? r.x16 : nullptr, to_f16 ? win : nullptr,
                        (to_f16 || nv4) ? ag : nullptr, nv4 ? r.xq : nullptr,
                        nv4 ? r.xs16 : nullptr, ZeroRegion{z0, z0_words},
-                       ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words}, ep_first);
+                       ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words}, ep_first,
+                       to_f16 ? ka8 : KeptA8{nullptr, 0.f});
 }
 
 cudaError_t launch_route(const int32_t* ids, int Mk, int E, int ep_first, int tile_slots,
@@ -821,7 +851,7 @@ cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r,
                         bool atoms, bool to_f16, const float* win, const float* ag,
                         const int32_t* ids, int ep_first, int E, bool nv4, void* z0,
                         size_t z0_words, void* z1, size_t z1_words, void* z2, size_t z2_words,
-                        cudaStream_t st) {
+                        KeptA8 ka8, cudaStream_t st) {
   const size_t work = std::max(
       std::max(quant_x ? (size_t)M * topk * (H / 32) : (size_t)0,
                (to_f16 || nv4) ? (size_t)M * topk * (H / 8) : (size_t)0),
@@ -839,7 +869,8 @@ cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r,
                        (to_f16 || nv4) ? ag : nullptr, ids, ep_first, E, nv4 ? r.xq : nullptr,
                        nv4 ? r.xs16 : nullptr, r.ctrl,
                        ZeroRegion{z0, z0_words},
-                       ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words});
+                       ZeroRegion{z1, z1_words}, ZeroRegion{z2, z2_words},
+                       to_f16 ? ka8 : KeptA8{nullptr, 0.f});
 }
 
 }  // namespace moe

@@ -200,6 +200,11 @@ def moe_get_device_error(plan, scratch, stream=None):
     return st, code.value
 
 
+def moe_plan_set_kept_a8(plan, w13_input_scale, w2_input_scale):
+    _check(_lib.load().moe_plan_set_kept_a8(_handle(plan), float(w13_input_scale),
+                                            float(w2_input_scale)), "moe_plan_set_kept_a8")
+
+
 def moe_plan_set_wait_probe(plan, ns):
     _check(_lib.load().moe_plan_set_wait_probe(_handle(plan), int(ns)), "moe_plan_set_wait_probe")
 
@@ -333,7 +338,8 @@ class MoELayer:
 
     def __init__(self, ck, topk, max_m, swiglu_limit=float("inf"), deterministic=False,
                  alpha=None, beta=None, device="cuda", keep_checkpoint=False, backend=0,
-                 fc1_kernel=0, first_expert=0, weight_on_input=False, debug_copies=False):
+                 fc1_kernel=0, first_expert=0, weight_on_input=False, debug_copies=False,
+                 kept_a8=None):
         self.E, self.H, self.I, self.topk, self.max_m = ck.E, ck.H, ck.I, topk, max_m
         self.quant = quant_mode_of(ck)
         tier = ck.tier if ck.quant == "hybrid" else None
@@ -360,6 +366,8 @@ class MoELayer:
             moe_plan_set_router_weight_on_input(self.plan, 1)
         if debug_copies:
             moe_plan_set_debug_copies(self.plan, 1)
+        if kept_a8 is not None:        # (w13_input_scale, w2_input_scale)
+            moe_plan_set_kept_a8(self.plan, kept_a8[0], kept_a8[1])
         self.scratch = torch.empty(moe_scratch_bytes(self.plan), dtype=torch.uint8, device=device)
         self.device = device
         self._io = None

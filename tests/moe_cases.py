@@ -43,17 +43,17 @@ def _row_ok(got_row_bits, ref_row):
 
 
 def oracle_rows(ck, x_bits, ids, w, limit, rows=None, alpha=1.0, beta=0.0,
-                weight_on_input=False):
+                weight_on_input=False, kept_a8=False):
     """The oracle's unrounded fp64 output for the given rows (all when None), to be shared by
     several check_rows calls on the same inputs."""
     rows = np.arange(ids.shape[0]) if rows is None else np.asarray(rows)
     _, f64 = O.moe_forward(ck, x_bits, ids, w, limit, alpha, beta, rows=rows, return_f64=True,
-                           weight_on_input=weight_on_input)
+                           weight_on_input=weight_on_input, kept_a8=kept_a8)
     return f64
 
 
 def check_rows(got_bits, ck, x_bits, ids, w, limit, rows=None, alpha=1.0, beta=0.0,
-               weight_on_input=False, ref_f64=None):
+               weight_on_input=False, ref_f64=None, kept_a8=False):
     """Compare the given rows (all when None) with the oracle; returns (rel, mx) arrays.
     ``ref_f64``: the oracle's output of these inputs when already computed (oracle_rows).
 
@@ -63,12 +63,12 @@ def check_rows(got_bits, ck, x_bits, ids, w, limit, rows=None, alpha=1.0, beta=0
     correct results of the method."""
     rows = np.arange(ids.shape[0]) if rows is None else np.asarray(rows)
     f64 = ref_f64 if ref_f64 is not None else oracle_rows(
-        ck, x_bits, ids, w, limit, rows, alpha, beta, weight_on_input)
+        ck, x_bits, ids, w, limit, rows, alpha, beta, weight_on_input, kept_a8)
     rel, mx = O.row_errors(got_bits[rows], f64[rows])
     bad = [int(r) for r, a, b in zip(rows, rel, mx) if a > REL_L2_BOUND or b > MAX_ERR_BOUND]
     if bad:
         alts = O.requant_alternatives(ck, x_bits, ids, w, limit, alpha, beta, REQUANT_REL, bad,
-                                      weight_on_input)
+                                      weight_on_input, kept_a8)
         for r in bad:
             d = alts[r]
             assert 0 < len(d) <= 10, (r, "outside the bound with", len(d), "ambiguous elements",

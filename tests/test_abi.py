@@ -281,3 +281,36 @@ def test_binding_constants_match_header(lib):
     body = re.search(r"typedef struct \{(.*?)\} moe_checkpoint;", hdr, re.S).group(1)
     fields = re.findall(r"\*\s*(\w+);", re.sub(r"/\*.*?\*/", "", body, flags=re.S))
     assert fields == [f for f, _ in _lib.MoeCheckpoint._fields_]
+
+
+def test_kept_a8_arguments(lib):
+    """The MXFP4 kept tier's A8 opt-in: hybrid-MX plans only; both scales positive with finite
+    nonzero fp32 reciprocals, or both 0 (off); refused beside router weights on the input and
+    the CUDA-core backend, in either order."""
+    p = moe.moe_plan(8, 256, 256, 2, 16, moe.MOE_W4A16_HYBRID_MX, float("inf"), 0)
+    moe.moe_plan_set_kept_a8(p, 0.011, 0.018)
+    moe.moe_plan_set_kept_a8(p, 0.0, 0.0)
+    for a, b in ((-0.01, 0.02), (float("nan"), 0.02), (0.01, float("inf")), (1e-40, 0.02),
+                 (0.01, 0.0), (0.0, 0.02)):
+        with pytest.raises(moe.MoEError) as ei:
+            moe.moe_plan_set_kept_a8(p, a, b)
+        assert ei.value.status == 1, (a, b)
+    moe.moe_plan_set_kept_a8(p, 0.011, 0.018)
+    for call in (lambda: moe.moe_plan_set_backend(p, 1),
+                 lambda: moe.moe_plan_set_router_weight_on_input(p, 1)):
+        with pytest.raises(moe.MoEError) as ei:
+            call()
+        assert ei.value.status == 3
+    moe.moe_plan_set_kept_a8(p, 0.0, 0.0)
+    moe.moe_plan_set_backend(p, 1)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_plan_set_kept_a8(p, 0.011, 0.018)
+    assert ei.value.status == 3
+    moe.moe_destroy_plan(p)
+    for mode in (moe.MOE_W4A8_MXFP4, moe.MOE_W4A16_NVFP4, moe.MOE_W4A16_HYBRID):
+        q = moe.moe_plan(8, 256, 256, 2, 16, mode, float("inf"), 0)
+        with pytest.raises(moe.MoEError) as ei:
+            moe.moe_plan_set_kept_a8(q, 0.011, 0.018)
+        assert ei.value.status == 3
+        moe.moe_destroy_plan(q)
+    assert lib.moe_plan_set_kept_a8(None, ctypes.c_float(0.0), ctypes.c_float(0.0)) == 1

@@ -792,3 +792,53 @@ def test_device_wait_timeout_recovers(det):
     got = run_layer(layer, x, ids, w)
     assert layer.device_error() == (0, 0)
     check_rows(got, ck, x, ids, w, 7.0)
+
+
+@pytest.mark.parametrize("M,det", [(5, 1), (16, 0), (40, 1), (200, 0)])
+def test_hybrid_mx_kept_a8(M, det):
+    """The A8 opt-in of the MXFP4 kept tier (static per-tensor FP8 activations with the layer's
+    two input scales) at tile widths 16 to 64, both routing launches and both combines: every
+    row against the oracle; the kept tier's fc2 operand (h) code for code against the oracle's
+    static FP8 decisions within the near-midpoint reading; NF3 slots unchanged (bf16 h)."""
+    cfg = small_cfg("hybrid_mx", I=256)
+    ck = S.make_checkpoint(cfg, seed=6200 + M)
+    rng = np.random.default_rng(6300 + M)
+    x = S.make_x(rng, M, cfg.H)
+    ids = S.zipf_topk(rng, M, cfg.E, cfg.topk, 0.8)
+    w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 1.0)
+    assert (ck.tier[ids] == S.TIER_NVFP4).any() and (ck.tier[ids] == S.TIER_NF3).any()
+    layer = _layer(ck, cfg.topk, M, math.inf, det, kept_a8=(ck.in13, ck.in2))
+    got = run_layer(layer, x, ids, w)
+    st, code = layer.device_error()
+    assert st == 0 and code == 0, code
+    check_rows(got, ck, x, ids, w, math.inf, kept_a8=True)
+    if det:
+        assert np.array_equal(run_layer(layer, x, ids, w), got)
+    # fc2's operand: kept slots hold the static FP8 value of h divided by the scale (the
+    # kernel keeps the E4M3 code value in f16), NF3 slots bf16(h)
+    hqb, _ = layer.intermediate(M)
+    hq = np.ascontiguousarray(hqb[:, : cfg.I]).view(np.float16).astype(np.float64)
+    h = O.slot_intermediate(ck, x, ids, kept_a8=True)
+    _, _, perm, _ = O.route(ids, cfg.E)
+    kept = ck.tier[ids.reshape(-1)[perm]] == S.TIER_NVFP4
+    s2 = float(np.float32(ck.in2))
+    want_k = C.fp8_static_quantize(h[kept], ck.in2)[1] / s2
+    mask, alt = C.fp8_static_alternates(h[kept], ck.in2, 1e-4)
+    mism = hq[kept] != want_k
+    assert np.all(mask[mism] & (hq[kept][mism] == alt[mism] / s2)), int(mism.sum())
+    layer.close()
+
+
+def test_hybrid_mx_kept_a8_full_size_sampled():
+    """The A8 opt-in on the full-size "v3" hybrid layer (E=256, H=6144, I=512, top-8, 64 MXFP4
+    + 192 NF3 experts, Zipf routing) at M = 8 and 512: sampled rows against the oracle."""
+    cfg = S.CONFIGS["hybrid_mxfp4_nf3"]
+    ck = S.make_checkpoint(cfg)
+    for M, rows in ((8, [0, 3, 7]), (512, [0, 255, 511])):
+        x, ids, w = S.make_inputs(cfg, M)
+        layer = _layer(ck, cfg.topk, M, cfg.swiglu_limit, 1, kept_a8=(ck.in13, ck.in2))
+        got = run_layer(layer, x, ids, w)
+        st, code = layer.device_error()
+        assert st == 0 and code == 0, code
+        check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=rows, kept_a8=True)
+        layer.close()
