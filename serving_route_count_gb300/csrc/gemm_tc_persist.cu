@@ -479,9 +479,19 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
   // waiting for fc1's output (L2 reads: nothing of them is in this SM's L1).
   const int G = gridDim.x, c = blockIdx.x;
   const int units = __ldcg(&p.ctrl[1]) * p.RB;
-  const int u_begin = (int)((long long)c * units / G);
-  const int u_end = (int)((long long)(c + 1) * units / G);
-  if (u_begin >= u_end) {
+  // this CTA's range [x0, x1) of the flat steps x = unit * KT + K tile: split evenly when the
+  // combine is atomic (a unit cut between two CTAs adds both partial products to the same
+  // outputs), whole units when it is deterministic (each slot's output is written once)
+  int x0, x1;
+  if (p.deterministic) {
+    x0 = (int)((long long)c * units / G) * p.KT;
+    x1 = (int)((long long)(c + 1) * units / G) * p.KT;
+  } else {
+    const long long T = (long long)units * p.KT;
+    x0 = (int)(c * T / G);
+    x1 = (int)((c + 1) * T / G);
+  }
+  if (x0 >= x1) {
     tmem_exit_early(&s_tmem, Cfg::kAlloc);
     pdl_wait_prev();
     return;
@@ -517,12 +527,12 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
 
   if (warp == 0 && lane == 0) {
     const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
-    const int fills = (u_end - u_begin) * p.KT;
+    const int fills = x1 - x0;
     const int pre = fills < S ? fills : S;
     // weights of the first stages, before fc1 completes: the stage's barrier expects their
     // bytes now and is arrived on once the activation part is issued too
     for (int i = 0; i < pre; ++i) {
-      const int u = u_begin + i / p.KT, kt = i % p.KT;
+      const int u = (x0 + i) / p.KT, kt = (x0 + i) - u * p.KT;
       const int tile = u / p.RB, rb = u - tile * p.RB;
       const int e = __ldcg(reinterpret_cast<const int*>(p.tiles + tile));
       const size_t a = ((size_t)e * p.RB + rb) * p.KT + kt;
@@ -533,7 +543,9 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
     pdl_wait_prev();     // fc1 complete, h visible
     int i = 0, cur_tile = -1, e = 0, p0 = 0;
     TileLoad<BN> tl(BN);
-    for (int u = u_begin; u < u_end && ok; ++u) {
+    StepSegs sg{p.KT, x0, x1};
+    int u, k0, len;
+    while (ok && sg.next(u, k0, len)) {
       const int tile = u / p.RB, rb = u - tile * p.RB;
       if (tile != cur_tile) {
         cur_tile = tile;
@@ -542,7 +554,7 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
         p0 = td.y;
         tl = TileLoad<BN>(td.z);
       }
-      for (int kt = 0; kt < p.KT && ok; ++kt, ++i) {
+      for (int kt = k0; kt < k0 + len && ok; ++kt, ++i) {
         const int s = i % S;
         if (i >= S) ok = mbar_wait(&empty[s], ((i / S) - 1) & 1, p.err);
         if (!ok) break;
@@ -568,7 +580,9 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
     if (lane == 0) {
       int i = 0, j = 0, cur_tile = -1;
       TileLoad<BN> tl(BN);
-      for (int u = u_begin; u < u_end && ok; ++u, ++j) {
+      StepSegs sg{p.KT, x0, x1};
+      int u, k0, len;
+      for (; ok && sg.next(u, k0, len); ++j) {
         const int tile = u / p.RB;
         if (tile != cur_tile) {
           cur_tile = tile;
@@ -579,7 +593,7 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + b * BN;
-        for (int kt = 0; kt < p.KT && ok; ++kt, ++i) {
+        for (int kt = k0; kt < k0 + len && ok; ++kt, ++i) {
           const int s = i % S;
           ok = mbar_wait(&full[s], (i / S) & 1, p.err);
           if (!ok) break;
@@ -599,7 +613,7 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
               if (jc < tl.nch)
                 mma_mxf8f6f4(d + 32 * jc, desc_sw128(st + 32 * kb),
                            desc_sw128(st + kTileBytesA + 4096 * jc + 32 * kb), idesc, sf + 0,
-                           sf + 4 + 4 * jc, (kt > 0 || kb > 0) ? 1u : 0u);
+                           sf + 4 + 4 * jc, (kt > k0 || kb > 0) ? 1u : 0u);
           }
           tc_commit(&empty[s]);
         }
@@ -610,7 +624,9 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
     const int quad = warp & 3;
     const int row = quad * 32 + lane;                          // row of the 128-row block
     int j = 0, cur_tile = -1, n = 0;
-    for (int u = u_begin; u < u_end; ++u, ++j) {
+    StepSegs sg{p.KT, x0, x1};
+    int u, k0, len;
+    for (; sg.next(u, k0, len); ++j) {
       const int tile = u / p.RB, rb = u - tile * p.RB;
       if (tile != cur_tile) {
         // the combine's slot indices and router weights of the new tile, loaded before its

@@ -95,6 +95,20 @@ struct StreamWork {
   }
 };
 
+// Segments of a range [x, x1) of flat steps x = unit * KT + K tile, cut at unit boundaries:
+// next() gives each segment's unit, first K tile and length, in order; false after the last.
+struct StepSegs {
+  int KT, x, x1;
+  __device__ __forceinline__ bool next(int& u, int& k0, int& len) {
+    if (x >= x1) return false;
+    u = x / KT;
+    k0 = x - u * KT;
+    len = min(KT - k0, x1 - x);
+    x += len;
+    return true;
+  }
+};
+
 // ---------------------------------------------------------------------------------- host side
 
 constexpr int kStreamMaxCtas = 320;   // partial slots are reserved for this many CTAs
