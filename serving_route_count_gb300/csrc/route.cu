@@ -820,6 +820,9 @@ cudaError_t launch_route_actq_small(const int32_t* ids, int Mk, int E, int ep_fi
                                std::max(z0_words / 4, std::max(z1_words / 4, z2_words / 4)));
   int blocks = (int)std::min<size_t>((work + kSmallRouteThreads - 1) / kSmallRouteThreads,
                                      152 * 4);
+  // routing and zeroing only (fc1 quantises): a few CTAs, so that the SMs they sit on are free
+  // for fc1's second CTA (one of this kernel and two of fc1 do not fit an SM's shared memory)
+  if (skip_x) blocks = std::min(blocks, 16);
   if (blocks < 1) blocks = 1;
   // first kernel of a call: an ordinary launch (the previous call may still read the tables)
   static const bool carveout = prefer_max_shared(route_actq_small_kernel);
