@@ -842,4 +842,3 @@ def test_hybrid_mx_kept_a8_full_size_sampled():
         assert st == 0 and code == 0, code
         check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=rows, kept_a8=True)
         layer.close()
-
