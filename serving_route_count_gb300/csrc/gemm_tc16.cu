@@ -87,6 +87,7 @@ struct Tc16Params {
   // activations, which the kept tier's operands carry as E4M3 code values; and, for fc1, the
   // fp32 reciprocal of fc2's input scale, by which h is quantised
   float a8_s, a8_inv_next;
+  int rb_in_x;                // grid (RB, tiles, splits) instead of (tiles, RB, splits)
   const int4* tiles;
   const int32_t* ctrl;
   int32_t* err;
@@ -245,14 +246,16 @@ gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   __shared__ uint32_t s_tmem;
   tmem_alloc_first(&s_tmem, Cfg::kAlloc);
   pdl_wait_prev();     // previous kernel of the call complete, its writes visible
-  const int tile = blockIdx.x;
+  // the row blocks of a tile are adjacent in launch order (while the tiles fit the grid's y),
+  // so the CTAs that read the same activation tile run together and share it through L2
+  const int tile = p.rb_in_x ? blockIdx.y : blockIdx.x;
   if (tile >= p.ctrl[1]) {
     tmem_exit_early(&s_tmem, Cfg::kAlloc);
     return;
   }
   const int4 td = p.tiles[tile];
   const int e = td.x, p0 = td.y, n = td.z;
-  const int rb = blockIdx.y, split = blockIdx.z;
+  const int rb = p.rb_in_x ? blockIdx.x : blockIdx.y, split = blockIdx.z;
   const int kt0 = split * p.KT / p.splits, kt1 = (split + 1) * p.KT / p.splits;
   const int nraw = kt1 - kt0;               // raw stages (256-wide K)
   const int nsub = nraw * 4;                // 64-wide sub-tiles
@@ -596,8 +599,11 @@ static cudaError_t launch16(const Tc16Params& p, int tiles, cudaStream_t st) {
                          (int)cudaSharedmemCarveoutMaxShared);
     attr = true;
   }
-  dim3 grid(tiles, p.RB, FC2 ? 1 : p.splits);
-  return launch_kernel(kernel, grid, dim3(k16Threads), Cfg::kSmem, st, true, p);
+  Tc16Params q = p;
+  q.rb_in_x = tiles <= 65535 ? 1 : 0;
+  const int sp = FC2 ? 1 : p.splits;
+  const dim3 grid = q.rb_in_x ? dim3(p.RB, tiles, sp) : dim3(tiles, p.RB, sp);
+  return launch_kernel(kernel, grid, dim3(k16Threads), Cfg::kSmem, st, true, q);
 }
 
 // fc1 of the 16-bit path at two CTAs per SM (NVFP4-only layers, token tiles of at most 32)
