@@ -379,10 +379,18 @@ class MoELayer:
         return out
 
     def run_host(self, x_host, ids_host, w_host, out_host, stream=None):
+        """moe_run_host on this layer; the layer's own arguments (plan, weights, scratch, staging
+        buffer) are marshalled once, the host tensors on every call."""
         if self._io is None:
             self._io = torch.empty(moe_io_bytes(self.plan), dtype=torch.uint8, device=self.device)
-        moe_run_host(self.plan, self.prep, self.scratch, self._io, x_host, ids_host, w_host,
-                     out_host, stream=stream)
+            self._host_args = (_handle(self.plan), _handle(self.prep), _ptr(self.scratch),
+                               self.scratch.numel(), _ptr(self._io), self._io.numel())
+        for t in (x_host, ids_host, w_host, out_host):
+            if not t.is_contiguous():
+                raise ValueError("tensors passed to the library must be contiguous")
+        _check(_lib.load().moe_run_host(*self._host_args, x_host.data_ptr(), ids_host.data_ptr(),
+                                        w_host.data_ptr(), out_host.data_ptr(), x_host.shape[0],
+                                        _stream(stream)), "moe_run_host")
         return out_host
 
     def routing(self, M, stream=None):
