@@ -512,7 +512,7 @@ def our_arm(args, rank, world):
         """One ladder pass; with stage_events the instrumented graphs run and the fc1 stage
         durations are returned instead of whole-call times."""
         tot_ms, dom_ms, dom_bytes, toks = 0.0, 0.0, 0.0, 0
-        pairs = []
+        pairs, per_call = [], []
         with torch.cuda.stream(stream):
             for mi, M in enumerate(m_list):
                 c = calls[mi * N_ROUTING_SETS + (si % N_ROUTING_SETS)]
@@ -530,11 +530,12 @@ def our_arm(args, rank, world):
         stream.synchronize()
         for a, b, c in pairs:
             tot_ms += a.elapsed_time(b)
+            per_call.append((c["M"], a.elapsed_time(b)))
             if stage_events:
                 dom_ms += c["ev"][dom_i].elapsed_time(c["ev"][dom_i + 1])
                 dom_bytes += c["distinct"] * EXPERT_BYTES_W13[DECODE_CFG] + c["M"] * cfg.H
             toks += c["tokens"]
-        return tot_ms, dom_ms, dom_bytes, toks
+        return tot_ms, dom_ms, dom_bytes, toks, per_call
 
     tot_ms = dom_ms = dom_bytes = 0.0
     toks = 0
@@ -545,15 +546,18 @@ def our_arm(args, rank, world):
             dist.barrier()
         torch.cuda.synchronize()
         clk.start()
+        per_m = {}
         for si in range(args.steps):
-            a, _, _, d = step(args.warmup + si)
+            a, _, _, d, pc = step(args.warmup + si)
             tot_ms += a
             toks += d
+            for M, ms in pc:
+                per_m.setdefault(M, []).append(ms)
         torch.cuda.synchronize()
         clk.stop()
         # fc1 durations: the same calls again through the stage-instrumented graphs
         for si in range(max(3, args.steps // 4)):
-            _, b, c, _ = step(args.warmup + si, stage_events=True)
+            _, b, c, _, _ = step(args.warmup + si, stage_events=True)
             dom_ms += b
             dom_bytes += c
     tot_ms, all_toks = reduce_over_ranks(tot_ms, toks, world, device="cuda")
@@ -647,6 +651,8 @@ def our_arm(args, rank, world):
                              "replays: an event between kernels breaks the launch chain)",
         },
         "stages": stages,
+        # mean device time of one call at each M of the ladder, over the timed steps
+        "calls_us": {str(M): round(statistics.mean(v) * 1e3, 1) for M, v in sorted(per_m.items())},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_tok / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
