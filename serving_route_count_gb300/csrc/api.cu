@@ -55,7 +55,8 @@ cudaError_t launch_simt_stage(int stage, const DevWeights& w, const RunPtrs& r,
                               const float* topk_w, void* out, int M, cudaStream_t st);
 // prepare.cu
 cudaError_t launch_repack_fp4_tiled(const void* src, void* dst, int E, int halves, int rows,
-                                    int src_cols, int dst_cols, int layout, cudaStream_t st);
+                                    int src_cols, int dst_cols, int layout, int pair_I,
+                                    cudaStream_t st);
 cudaError_t launch_repack_sf_atoms(const void* src, void* dst, int E, int halves, int rows,
                                    int kblocks, int row_tiles, int k_tiles, int layout,
                                    cudaStream_t st);
@@ -288,8 +289,9 @@ moe_status moe_prepare_weights(const moe_weight_plan* wp, const moe_checkpoint* 
   auto chk = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
   if (fp4) {
     if (wp->quant == MOE_W4A8_MXFP4) {
-      chk(launch_repack_fp4_tiled(src->w13, base + wp->w13, E4, 2, I, H / 2, H / 2, L, st));
-      chk(launch_repack_fp4_tiled(src->w2, base + wp->w2, E4, 1, H, I / 2, Ip / 2, L, st));
+      chk(launch_repack_fp4_tiled(src->w13, base + wp->w13, E4, 2, I, H / 2, H / 2, L, 0, st));
+      chk(launch_repack_fp4_tiled(src->w2, base + wp->w2, E4, 1, H, I / 2, Ip / 2, L,
+                                  (I & 127) == 64 ? I : 0, st));
     } else {
       chk(launch_repack_w16_tiled(0, src->w13, base + wp->w13, E4, 2, I, H, H, L, st));
       chk(launch_repack_w16_tiled(0, src->w2, base + wp->w2, E4, 1, H, I, Ip, L, st));
@@ -946,7 +948,7 @@ moe_status moe_unprepare_weights(const moe_weight_plan* wp, const moe_prepared* 
       for (int r = 0; r < H; ++r) {
         const size_t sr = (size_t)ex * H + r;
         for (int c = 0; c < I / 2; ++c)
-          w2[sr * (I / 2) + c] = b[wp->w2 + fp4_tiled_byte((size_t)E4, H, Ip, ex, r, 2 * c)];
+          w2[sr * (I / 2) + c] = b[wp->w2 + fp4_w2_byte((size_t)E4, H, Ip, I, ex, r, 2 * c)];
         for (int kb = 0; kb < I / 32; ++kb)
           s2[sr * (I / 32) + kb] = b[wp->s2 + sf_atom_byte(H / 128, Ip / 128, ex, r, kb)];
       }

@@ -79,7 +79,12 @@ __device__ __forceinline__ void load_w8(const DevWeights& w, int kind, int le, i
     cbyte = nv_code_byte(mat, mr, k, rbs, kts);
   } else if (w.fp4_tiled) {
     if (FC2) {
-      cbyte = fp4_tiled_byte((size_t)w.E4, w.H, K, (size_t)le, row, k);
+      if (k >= w.I) {          // the zero padding of K (not stored where tails are paired)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) out[i] = 0.f;
+        return;
+      }
+      cbyte = fp4_w2_byte((size_t)w.E4, w.H, K, w.I, (size_t)le, row, k);
     } else {
       const int half = row / w.I;
       cbyte = fp4_tiled_byte((size_t)w.E4 * 2, w.I, K, (size_t)le * 2 + half, row - half * w.I, k);

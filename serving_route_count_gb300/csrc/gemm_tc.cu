@@ -108,6 +108,7 @@ struct TcFc2Params {
   float* acc;                // [M][H] atomic mode
   float* rbuf;               // [M*k][H] deterministic mode
   int H, Ip, KT, Sm, topk, deterministic;
+  int pair;                  // I % 128 == 64: the last K tile's codes are paired (fp4_w2_tile)
 };
 
 template <int BN>
@@ -464,7 +465,8 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
     for (int i = 0; i < pre; ++i) {
       const size_t a = ((size_t)e * (p.H / 128) + rt) * p.KT + i;
       mbar_expect_tx(&full[i], kTxBytesA + 512);
-      tma_load_3d_hint(stage(i), &p.tm_w2, 0, 0, (int)a, &full[i], pol);
+      tma_load_3d_hint(stage(i), &p.tm_w2, 0, 0, fp4_w2_tile(e, rt, i, p.H / 128, p.KT, p.pair),
+                       &full[i], pol);
       bulk_load(stage(i) + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[i]);
     }
     pdl_wait_prev();     // fc1 complete, h visible
@@ -479,7 +481,8 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
       } else {
         const size_t a = ((size_t)e * (p.H / 128) + rt) * p.KT + i;
         mbar_arrive_expect_tx(&full[s], kTxBytesA + tl.b_bytes + 512 + tl.sf_bytes);
-        tma_load_3d_hint(st, &p.tm_w2, 0, 0, (int)a, &full[s], pol);
+        tma_load_3d_hint(st, &p.tm_w2, 0, 0, fp4_w2_tile(e, rt, i, p.H / 128, p.KT, p.pair),
+                         &full[s], pol);
         bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
       }
       tl.load_b(st + kTileBytesA, &p.tm_h, i * 128, p0, &full[s]);
@@ -504,13 +507,17 @@ fc2_tc_kernel(const __grid_constant__ TcFc2Params p) {
         for (int j = 0; j < Cfg::kChunks; ++j)
           if (j < tl.nch)
             tc_cp_sf(sf + 4 + 4 * j, desc_sf(st + kTileBytesA + Cfg::kB + 512 + 512 * j));
+        // a paired tail tile: two K steps, at columns 64.. of the tile for an odd row block
+        const bool tail = p.pair && i == nk - 1;
+        const int a_off = (tail && (rt & 1)) ? 64 : 0;
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) {
+          if (tail && kb >= 2) break;
           const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, NChunks<BN>::kWidth, kb);
 #pragma unroll
           for (int j = 0; j < Cfg::kChunks; ++j)
             if (j < tl.nch)
-              mma_mxf8f6f4(tmem + 32 * j, desc_sw128(st + 32 * kb),
+              mma_mxf8f6f4(tmem + 32 * j, desc_sw128(st + a_off + 32 * kb),
                          desc_sw128(st + kTileBytesA + 4096 * j + 32 * kb), idesc, sf + 0,
                          sf + 4 + 4 * j, (i > 0 || kb > 0) ? 1u : 0u);
         }
@@ -698,6 +705,7 @@ cudaError_t launch_tc_stage(int stage, const DevWeights& w, const RunPtrs& r, co
   p.hs16 = r.hs16; p.r16 = r.r16;
   p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;
   p.H = d.H; p.Ip = d.Ip; p.KT = d.Ip / 128; p.Sm = Sm; p.topk = d.topk;
+  p.pair = (d.I & 127) == 64 ? 1 : 0;
   p.deterministic = d.deterministic;
   switch (bn) {
     case 16: return launch_fc2_bn<16>(p, tiles, st);

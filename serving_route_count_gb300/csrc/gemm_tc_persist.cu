@@ -458,6 +458,7 @@ struct PersistFc2Params {
   float* acc;                // [M][H] atomic mode
   float* rbuf;               // [M*k][H] deterministic mode
   int H, KT, RB, Sm, topk, deterministic, r16;
+  int pair;                  // I % 128 == 64: the last K tile's codes are paired (fp4_w2_tile)
 };
 
 template <int BN>
@@ -537,7 +538,8 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
       const int e = __ldcg(reinterpret_cast<const int*>(p.tiles + tile));
       const size_t a = ((size_t)e * p.RB + rb) * p.KT + kt;
       mbar_expect_tx(&full[i], kTxBytesA + 512);
-      tma_load_3d_hint(stage(i), &p.tm_w2, 0, 0, (int)a, &full[i], pol);
+      tma_load_3d_hint(stage(i), &p.tm_w2, 0, 0, fp4_w2_tile(e, rb, kt, p.RB, p.KT, p.pair),
+                       &full[i], pol);
       bulk_load(stage(i) + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[i]);
     }
     pdl_wait_prev();     // fc1 complete, h visible
@@ -564,7 +566,8 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
         } else {
           const size_t a = ((size_t)e * p.RB + rb) * p.KT + kt;
           mbar_arrive_expect_tx(&full[s], kTxBytesA + tl.b_bytes + 512 + tl.sf_bytes);
-          tma_load_3d_hint(st, &p.tm_w2, 0, 0, (int)a, &full[s], pol);
+          tma_load_3d_hint(st, &p.tm_w2, 0, 0, fp4_w2_tile(e, rb, kt, p.RB, p.KT, p.pair),
+                           &full[s], pol);
           bulk_load(st + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[s]);
         }
         tl.load_b(st + kTileBytesA, &p.tm_h, kt * 128, p0, &full[s]);
@@ -583,7 +586,7 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
       StepSegs sg{p.KT, x0, x1};
       int u, k0, len;
       for (; ok && sg.next(u, k0, len); ++j) {
-        const int tile = u / p.RB;
+        const int tile = u / p.RB, rb = u - tile * p.RB;
         if (tile != cur_tile) {
           cur_tile = tile;
           tl = TileLoad<BN>(p.tiles[tile].z);
@@ -605,13 +608,17 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
           for (int jc = 0; jc < Cfg::kChunks; ++jc)
             if (jc < tl.nch)
               tc_cp_sf(sf + 4 + 4 * jc, desc_sf(st + kTileBytesA + Cfg::kB + 512 + 512 * jc));
+          // a paired tail tile: two K steps, at columns 64.. of the tile for an odd row block
+          const bool tail = p.pair && kt == p.KT - 1;
+          const int a_off = (tail && (rb & 1)) ? 64 : 0;
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb) {
+            if (tail && kb >= 2) break;
             const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, NChunks<BN>::kWidth, kb);
 #pragma unroll
             for (int jc = 0; jc < Cfg::kChunks; ++jc)
               if (jc < tl.nch)
-                mma_mxf8f6f4(d + 32 * jc, desc_sw128(st + 32 * kb),
+                mma_mxf8f6f4(d + 32 * jc, desc_sw128(st + a_off + 32 * kb),
                            desc_sw128(st + kTileBytesA + 4096 * jc + 32 * kb), idesc, sf + 0,
                            sf + 4 + 4 * jc, (kt > k0 || kb > 0) ? 1u : 0u);
           }
@@ -775,6 +782,7 @@ cudaError_t launch_fc2_persist(const DevWeights& w, const RunPtrs& r, const Plan
   const int Sm = M * d.topk;
   p.RB = d.H / 128;
   p.KT = d.Ip / 128;
+  p.pair = (d.I & 127) == 64 ? 1 : 0;
   if (!tmap_fp4(&p.tm_w2, w.w2, 128, (long long)d.E * p.RB * p.KT) ||
       !tmap_u8(&p.tm_h, r.hq, d.Ip, Sm, act_box_rows(bn)))
     return cudaErrorInvalidValue;

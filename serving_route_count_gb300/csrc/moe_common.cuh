@@ -89,6 +89,25 @@ __host__ __device__ inline size_t fp4_tiled_byte(size_t n_mats, int rows, int K,
   return n_mats * rtf * kt_n * 8192 + (((mat * kt_n + kt) * rem) + rr) * 64 + kb;
 }
 
+// fc2 codes of a W4A8 layer whose I % 128 == 64: the last K tile of a 128-row block holds 64
+// columns, so the tails of row blocks 2j and 2j + 1 share the tile of block 2j (columns 0..63
+// and 64..127; the tile of block 2j + 1 is unused).  fc2 reads the shared tile once from HBM for
+// both blocks instead of two tiles half of zero codes.  Byte of elements k, k + 1 (k even) of
+// row r of expert e's w2 (H rows, Kp = I rounded up to 128).
+__host__ __device__ inline size_t fp4_w2_byte(size_t E, int H, int Kp, int I, size_t e, int r,
+                                              int k) {
+  const int kf = I & ~127;
+  if ((I & 127) == 64 && k >= kf) {
+    const int rb = r >> 7;
+    return fp4_tiled_byte(E, H, Kp, e, ((rb & ~1) << 7) + (r & 127), k + 64 * (rb & 1));
+  }
+  return fp4_tiled_byte(E, H, Kp, e, r, k);
+}
+// Its code tile of row block rb, K tile kt ([E][H/128][Kp/128] tiles of 8 KB).
+__host__ __device__ inline int fp4_w2_tile(int e, int rb, int kt, int RB, int KT, int pair) {
+  return (e * RB + ((pair && kt == KT - 1) ? (rb & ~1) : rb)) * KT + kt;
+}
+
 // W4A16 tiles (see above): tile of matrix `mat`, row block rb, K tile kt.
 __host__ __device__ inline size_t w16_tile(size_t mat, int rb, int kt, int rbs, int kts) {
   return (mat * (size_t)rbs + rb) * (size_t)kts + kt;

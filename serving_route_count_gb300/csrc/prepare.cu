@@ -30,7 +30,7 @@ __device__ __forceinline__ uint8_t canon_fp4_byte(uint8_t b) {
 // mats = E*halves matrices of rows x (2*dst_cols) elements.
 __global__ void repack_fp4_tiled_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
                                         int E, int halves, int rows, int src_cols, int dst_cols,
-                                        int layout) {
+                                        int layout, int pair_I) {
   const size_t n = (size_t)E * halves * rows * dst_cols;
   const size_t n_mats = (size_t)E * halves;
   GRID_STRIDE(idx, n) {
@@ -45,7 +45,13 @@ __global__ void repack_fp4_tiled_kernel(const uint8_t* __restrict__ src, uint8_t
       const int sr = halves == 2 ? src_row_fc1(half, i, rows, layout) : i;
       v = canon_fp4_byte(src[(e * (size_t)(halves * rows) + sr) * src_cols + c]);
     }
-    dst[fp4_tiled_byte(n_mats, rows, 2 * dst_cols, mh, i, 2 * c)] = v;
+    if (pair_I != 0) {
+      // fc2 with paired 64-column tails: the padding columns are not stored (the partner block's
+      // codes take their place)
+      if (c < src_cols) dst[fp4_w2_byte(n_mats, rows, 2 * dst_cols, pair_I, mh, i, 2 * c)] = v;
+    } else {
+      dst[fp4_tiled_byte(n_mats, rows, 2 * dst_cols, mh, i, 2 * c)] = v;
+    }
   }
 }
 
@@ -276,11 +282,13 @@ static int grid_for(size_t n) {
 }
 
 cudaError_t launch_repack_fp4_tiled(const void* src, void* dst, int E, int halves, int rows,
-                                    int src_cols, int dst_cols, int layout, cudaStream_t st) {
+                                    int src_cols, int dst_cols, int layout, int pair_I,
+                                    cudaStream_t st) {
   const size_t n = (size_t)E * halves * rows * dst_cols;
   if (n == 0) return cudaSuccess;
   repack_fp4_tiled_kernel<<<grid_for(n), 256, 0, st>>>((const uint8_t*)src, (uint8_t*)dst, E,
-                                                       halves, rows, src_cols, dst_cols, layout);
+                                                       halves, rows, src_cols, dst_cols, layout,
+                                                       pair_I);
   return cudaGetLastError();
 }
 

@@ -842,3 +842,32 @@ def test_hybrid_mx_kept_a8_full_size_sampled():
         assert st == 0 and code == 0, code
         check_rows(got, ck, x, ids, w, cfg.swiglu_limit, rows=rows, kept_a8=True)
         layer.close()
+
+
+@pytest.mark.parametrize("H,I,M,det", [(1408, 192, 9, 0), (1408, 320, 37, 1), (1408, 192, 200, 0),
+                                       (1280, 448, 16, 1)])
+def test_w4a8_fc2_paired_k_tails(H, I, M, det):
+    """fc2's weights when I % 128 == 64: the 64-column K tails of row blocks 2j and 2j + 1 share
+    one tile, an odd row block multiplying its half at a 64-column offset; with an odd number of
+    128-row blocks (H = 1408: 11) the last tail has no partner.  Prepared bytes read back equal the
+    checkpoint, and every row matches the oracle through the unit-per-CTA fc2 (small M) and the
+    persistent one (M = 200), in both combines."""
+    from serving_route_count_gb300 import moe_unprepare_weights
+    cfg = small_cfg("mxfp4", H=H, I=I)
+    ck = S.make_checkpoint(cfg, seed=9300 + I + M)
+    rng = np.random.default_rng(9400 + I + M)
+    x = S.make_x(rng, M, cfg.H)
+    ids = S.zipf_topk(rng, M, cfg.E, cfg.topk, 1.1)
+    w = S.router_weights(rng, M, cfg.topk, "sigmoid_norm", 2.5)
+    layer = _layer(ck, cfg.topk, M, 7.0, det)
+    want = {"w13": ck.w13, "s13": ck.s13, "w2": ck.w2, "s2": ck.s2}
+    got_w = moe_unprepare_weights(layer.wp, layer.prep, want)
+    for k, v in want.items():
+        assert np.array_equal(got_w[k], _canon_fp4(v) if k in ("w13", "w2") else v), k
+    got = run_layer(layer, x, ids, w)
+    st, code = layer.device_error()
+    assert st == 0 and code == 0, code
+    check_rows(got, ck, x, ids, w, 7.0)
+    if det:
+        assert np.array_equal(run_layer(layer, x, ids, w), got)
+    layer.close()
