@@ -636,8 +636,8 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
   const int bn = t4 ? tc4_pick_bn(M) : (tc ? tc_pick_bn(M, d.topk, d.E, tc8) : kSimtSlots);
   const int tiles = call_tiles(d, plan->s.max_tiles, M, bn);
   const int RT = cdiv(d.I, 128);
-  // decode widths with more units than one wave of CTAs: the persistent stream-K fc1 (when its
-  // 32-bit schedule arithmetic fits the call)
+  // 16-token tiles (decode sizes): the persistent stream-K fc1, when its 32-bit schedule
+  // arithmetic fits the call (fc1_stream_preferred)
   const bool sk_ok = stream_schedule_fits((long long)tiles * RT, d.H / 128);
   const bool streamk = tc8 && bn == 16 && sk_ok &&
                        (d.fc1_kernel == 0 ? fc1_stream_preferred(bn, tiles * RT) : d.fc1_kernel == 2);

@@ -14,8 +14,10 @@
 //     requantisation.
 // Block-scaled MMA, layouts and operand staging are those of fc1_tc_kernel (gemm_tc.cu).
 //
-// Warps (256 threads): 0 TMA producer (lane 0), 1 MMA issuer (lane 0), 2..3 idle,
-// 4..7 epilogue (TMEM lane quadrant = warp % 4).
+// Warps (256 threads): 0 TMA producer (lane 0), 1 MMA issuer (lane 0), 2..3 the activation
+// quantisers of small calls (each stage's MXFP8 operand from the bf16 rows; idle when the
+// routing launch's quantised rows are loaded instead), 4..7 epilogue (TMEM lane quadrant =
+// warp % 4).
 #include <algorithm>
 #include <cstring>
 
@@ -425,10 +427,11 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
 }
 
 // ------------------------------------------------------------------------------------ fc2
-// Persistent fc2 for the 16/32-token tiles: units are (tile, 128-row block of H) pairs,
-// tile-major; the G CTAs take equal contiguous ranges (fc2's K = Ip is a few tiles, so units
-// are never split).  The accumulators alternate between two TMEM buffers, so the combine of
-// one unit overlaps the loads and MMAs of the next instead of ending the CTA.  The combine is
+// Persistent fc2: units are (tile, 128-row block of H) pairs, tile-major, of KT = Ip / 128 K
+// tiles each; the G CTAs take equal contiguous ranges of the flat (unit, K tile) steps when the
+// combine is atomic (a unit cut between two CTAs adds both partial products) and of whole units
+// when it is deterministic.  The accumulators alternate between two TMEM buffers, so the combine
+// of one segment overlaps the loads and MMAs of the next instead of ending the CTA.  The combine is
 // that of fc2_tc_kernel (fp32 atomics into the token's row, or the weighted slot row of the
 // route buffer); a separate finalize launch writes the output.
 
