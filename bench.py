@@ -657,7 +657,7 @@ def our_arm(args, rank, world):
         "e2e": {"value": e2e_tok / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": "moe_run_host (one pinned host buffer [x | ids | weights], one H2D copy "
-                       "+ run + D2H + sync)"},
+                       "+ run, finalize storing into the pinned output + sync)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "prefill": None if args.no_prefill else prefill_report(stream, flush, peak),

@@ -297,7 +297,10 @@ moe_status moe_io_bytes(const moe_plan_t* plan, size_t* bytes);
  * (>= moe_io_bytes, device), runs the layer, copies out device -> host and synchronises the
  * stream before returning.  Pinned host memory makes the copies asynchronous DMA.  When the
  * inputs sit back to back in one host buffer (ids_host = x_host + M*H*2 bytes, w_host =
- * ids_host + M*topk*4 bytes) they go up in one copy. */
+ * ids_host + M*topk*4 bytes) they go up in one copy.  When out_host is page-locked memory the
+ * device can address (cudaHostAlloc / cudaMallocHost under unified addressing, 16-byte aligned)
+ * the finalize kernel writes the output rows into it directly and no device -> host copy is
+ * made; the io buffer's output rows are then left untouched. */
 moe_status moe_run_host(const moe_plan_t* plan, const moe_prepared* weights, void* scratch,
                         size_t scratch_bytes, void* io, size_t io_bytes, const void* x_host,
                         const int32_t* ids_host, const float* w_host, void* out_host, int M,

@@ -779,11 +779,24 @@ moe_status moe_run_host(const moe_plan_t* plan, const moe_prepared* weights, voi
     dw = b + plan->io_w;
   }
   if (e != cudaSuccess) return cuda_status(e);
+  // page-locked output under unified addressing (cudaHostAlloc / cudaMallocHost memory): the
+  // device addresses it directly, so finalize stores the rows there and no device -> host copy
+  // follows; other host memory goes through the staging buffer and one copy
+  void* dout = b + plan->io_out;
+  cudaPointerAttributes pa{};
+  if (cudaPointerGetAttributes(&pa, out_host) == cudaSuccess) {
+    if (pa.type == cudaMemoryTypeHost && pa.devicePointer != nullptr &&
+        aligned(pa.devicePointer, 16))
+      dout = pa.devicePointer;
+  } else {
+    (void)cudaGetLastError();   // not a pointer CUDA knows: the copy path
+  }
   moe_status s = moe_run(plan, weights, scratch, scratch_bytes, dx,
                          reinterpret_cast<const int32_t*>(dids),
-                         reinterpret_cast<const float*>(dw), b + plan->io_out, M, stream);
+                         reinterpret_cast<const float*>(dw), dout, M, stream);
   if (s != MOE_OK) return s;
-  e = cudaMemcpyAsync(out_host, b + plan->io_out, xb, cudaMemcpyDeviceToHost, st);
+  if (dout == b + plan->io_out)
+    e = cudaMemcpyAsync(out_host, dout, xb, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   return cuda_status(e);
 }

@@ -168,6 +168,17 @@ def test_host_buffers_entry_point():
     got = oh.view(torch.int16).numpy().view(np.uint16)
     dev = run_layer(layer, x, ids, w)
     assert np.array_equal(got, dev)
+    # the output written three ways: pinned (the kernel stores into it), pageable (staging
+    # buffer and a copy), pinned but not 16-byte aligned (staging buffer and a copy)
+    op = torch.empty((4, cfg.H), dtype=torch.bfloat16)
+    layer.run_host(xh, ih, wh, op)
+    assert np.array_equal(op.view(torch.int16).numpy().view(np.uint16), dev)
+    raw = torch.zeros(4 * cfg.H + 4, dtype=torch.bfloat16).pin_memory()
+    om = raw[4:].view(4, cfg.H)
+    assert om.data_ptr() % 16 == 8
+    layer.run_host(xh, ih, wh, om)
+    assert np.array_equal(om.view(torch.int16).numpy().view(np.uint16), dev)
+    assert not raw[:4].view(torch.int16).any()    # nothing written before the output rows
 
 
 # ---------------------------------------------------------------------------- full sizes
