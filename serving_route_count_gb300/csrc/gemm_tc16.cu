@@ -238,8 +238,10 @@ __device__ __forceinline__ uint16_t h_to_f16_mx(float h, float a2, int32_t* err)
   return __half_as_ushort(__float2half_rn(q));
 }
 
+// The PAIR form asks the compiler for two CTAs per SM (<= 102 registers a thread): without the
+// bound it took 168 and the register file held one CTA, whatever its shared and tensor memory.
 template <int BN, bool FC2, bool PAIR>
-__global__ void __launch_bounds__(k16Threads, 1)
+__global__ void __launch_bounds__(k16Threads, PAIR ? 2 : 1)
 gemm_tc16_kernel(const __grid_constant__ Tc16Params p) {
   using Cfg = Tc16Cfg<BN, FC2, PAIR>;
   constexpr int kMats = Cfg::kMats;
