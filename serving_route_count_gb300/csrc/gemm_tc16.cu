@@ -610,7 +610,8 @@ static cudaError_t launch16(const Tc16Params& p, int tiles, cudaStream_t st) {
 
 // fc1 of the 16-bit path at two CTAs per SM (NVFP4-only layers, token tiles of at most 32)
 bool tc16_fc1_pair(int bn, int quant) {
-  return bn <= 32 && (quant == kQuantNVFP4 || quant == kQuantW4A8Nv);
+  return bn <= 32 && (quant == kQuantNVFP4 || quant == kQuantW4A8Nv || quant == kQuantHybrid ||
+                      quant == kQuantHybridMx);
 }
 
 // stage 0: fc1 (+ SwiGLU, h -> bf16 -> f16), stage 1: fc2 (+ combine).
