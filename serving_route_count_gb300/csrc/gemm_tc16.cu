@@ -158,47 +158,65 @@ __device__ __forceinline__ void convert_nvfp4_half(const uint8_t* codes, const u
   }
 }
 
-// f16 of bf16(fp32(LUT[c]) * scale) for the 8 codes, packed as 4 f16x2 words (codes 2i, 2i+1).
-__device__ __forceinline__ void nf3_table(float scale, uint32_t* t) {
+// The eight NF3 levels of a scale group as f16 bytes for byte-permute look-ups: f16 of
+// bf16(fp32(LUT[4 + i]) * scale) for i = 0..3 (codes 4..7), low bytes in tlo and high bytes in
+// thp; thn holds the high bytes with the sign flipped.  Codes 3..0 are the negatives of codes
+// 4..7 (the LUT is antisymmetric, and the product and both roundings are sign-symmetric), so
+// code c reads entry c - 4 (c >= 4) or 7 - c (c < 4, from thn).
+__device__ __forceinline__ void nf3_tables(float scale, uint32_t& tlo, uint32_t& thp,
+                                           uint32_t& thn) {
+  uint32_t lo = 0, hi = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float a = __bfloat162float(__float2bfloat16_rn(c_nf3_lut16[2 * i] * scale));
-    const float b = __bfloat162float(__float2bfloat16_rn(c_nf3_lut16[2 * i + 1] * scale));
-    t[i] = (uint32_t)__half_as_ushort(__float2half_rn(a)) |
-           ((uint32_t)__half_as_ushort(__float2half_rn(b)) << 16);
+    const float a = __bfloat162float(__float2bfloat16_rn(c_nf3_lut16[4 + i] * scale));
+    const uint32_t v = __half_as_ushort(__float2half_rn(a));
+    lo |= (v & 0xFFu) << (8 * i);
+    hi |= (v >> 8) << (8 * i);
   }
+  tlo = lo;
+  thp = hi;
+  thn = hi ^ 0x80808080u;
 }
 
-// Two NF3 codes -> f16x2 from the 8-entry table (codes 0..3 in t[0..1], 4..7 in t[2..3]).
-__device__ __forceinline__ uint32_t nf3_pick2(const uint32_t* t, uint32_t c0, uint32_t c1) {
-  const uint32_t l0 = c0 & 3, l1 = c1 & 3;
-  const uint32_t sel = (2 * l0) | ((2 * l0 + 1) << 4) | ((2 * l1) << 8) | ((2 * l1 + 1) << 12);
-  const uint32_t lo = __byte_perm(t[0], t[1], sel);
-  const uint32_t hi = __byte_perm(t[2], t[3], sel);
-  const uint32_t m = ((c0 & 4) ? 0x0000FFFFu : 0u) | ((c1 & 4) ? 0xFFFF0000u : 0u);
-  return (lo & ~m) | (hi & m);
+// Byte-permute selectors of 8 codes: nibble k = c' of code k (low 2 bits at bits 2k..2k+1 of
+// l16, high bit at bit k of h8), where c' = c - 4 for c >= 4 and 7 - c below, i.e. the low
+// bits XOR 7 when the high bit is clear: the low bits and the high bits spread to nibbles,
+// then one XOR.
+__device__ __forceinline__ uint32_t nf3_sel8(uint32_t l16, uint32_t h8) {
+  uint32_t x = l16;
+  x = (x | (x << 8)) & 0x00FF00FFu;
+  x = (x | (x << 4)) & 0x0F0F0F0Fu;
+  x = (x | (x << 2)) & 0x33333333u;
+  uint32_t y = h8;
+  y = (y | (y << 12)) & 0x000F000Fu;
+  y = (y | (y << 6)) & 0x03030303u;
+  y = (y | (y << 3)) & 0x11111111u;
+  return x ^ ((y ^ 0x11111111u) * 7u);
 }
 
 // NF3 row r, K sub-tile q (64 codes), half h (codes 32h..32h+31: one scale group) -> 16 f16x2
 // words in K order.  Raw smem: 32-byte rows of the tile's 2-bit plane halves (bytes 0..31 at +0,
-// 32..63 at +4096) and of its 1-bit plane (+8192).
+// 32..63 at +4096) and of its 1-bit plane (+8192).  Per 4 codes: the high bytes (with sign) by
+// one byte permute over thp:thn, the low bytes by one over tlo, two more to interleave them.
 __device__ __forceinline__ void convert_nf3_half(const uint8_t* codes, const uint8_t* scales,
                                                  int r, int q, int h, uint32_t* out) {
   const uint2 lo = *reinterpret_cast<const uint2*>(codes + (q >> 1) * 4096 + r * 32 +
                                                    (q & 1) * 16 + 8 * h);
   const uint32_t hi = *reinterpret_cast<const uint32_t*>(codes + 8192 + r * 32 + q * 8 + 4 * h);
-  uint32_t t[4];
-  nf3_table(e4m3_to_f32(scales[r * 16 + q * 2 + h]), t);
+  uint32_t tlo, thp, thn;
+  nf3_tables(e4m3_to_f32(scales[r * 16 + q * 2 + h]), tlo, thp, thn);
   const uint32_t low[2] = {lo.x, lo.y};
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
-    const uint32_t l16 = (low[jj >> 1] >> ((jj & 1) * 16)) & 0xFFFF;
-    const uint32_t h8 = (hi >> (jj * 8)) & 0xFF;
+    const uint32_t cs = nf3_sel8((low[jj >> 1] >> ((jj & 1) * 16)) & 0xFFFFu,
+                                 (hi >> (jj * 8)) & 0xFFu);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t c0 = ((l16 >> (4 * e)) & 3) | (((h8 >> (2 * e)) & 1) << 2);
-      const uint32_t c1 = ((l16 >> (4 * e + 2)) & 3) | (((h8 >> (2 * e + 1)) & 1) << 2);
-      out[4 * jj + e] = nf3_pick2(t, c0, c1);
+    for (int g = 0; g < 2; ++g) {
+      const uint32_t sel = cs >> (16 * g);
+      const uint32_t ph = __byte_perm(thp, thn, sel);
+      const uint32_t pl = __byte_perm(tlo, tlo, sel & 0x3333u);
+      out[4 * jj + 2 * g] = __byte_perm(pl, ph, 0x5140);
+      out[4 * jj + 2 * g + 1] = __byte_perm(pl, ph, 0x7362);
     }
   }
 }
