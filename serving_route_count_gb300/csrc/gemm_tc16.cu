@@ -53,7 +53,9 @@ struct Tc16Cfg {
   // by its tensor memory): 4 raw stages; fc2 (K = the intermediate size, a couple of raw
   // stages): 2, so that two CTAs fit an SM.
   static constexpr int kSr = (FC2 || PAIR) ? 2 : 4;
-  static constexpr int kSa = PAIR ? 3 : 4;                              // expanded sub-tiles
+  // expanded sub-tiles: 3 when that keeps the allocation at 128 columns (fc2 at tiles of <= 32
+  // tokens: four CTAs' worth of tensor memory per SM) or two CTAs fit (PAIR)
+  static constexpr int kSa = (PAIR || (FC2 && BN <= 32)) ? 3 : 4;
   static constexpr int kSb = FC2 ? (BN <= 32 ? 8 : 4)
                                  : (BN <= 32 ? 8 : (BN <= 64 ? 6 : 4));
   static constexpr int kSmem = kSr * kRaw + kSb * kB + 1024;
