@@ -342,8 +342,8 @@ const char* moe_profile_stage_names(const moe_plan_t* plan);
 
 /* Number of kernel launches moe_run makes for a call of M tokens with this plan and backend
  * (routing and activation quantisation or conversion - one launch for tensor-core calls of at
- * most 256 slots, three for larger W4A8 calls, two otherwise -, fc1, [SwiGLU on the CUDA-core
- * path], fc2, finalize).  0 for M = 0.
+ * most 256 slots, three for larger W4A8 calls and for other tensor-core calls beyond 4096 slots,
+ * two otherwise -, fc1, [SwiGLU on the CUDA-core path], fc2, finalize).  0 for M = 0.
  * Errors: MOE_ERR_ARG, MOE_ERR_CAPACITY (M > max_m). */
 moe_status moe_call_launches(const moe_plan_t* plan, int M, int* launches);
 

@@ -15,6 +15,10 @@ namespace moe {
 // route.cu
 cudaError_t launch_route(const int32_t* ids, int Mk, int E, int ep_first, int tile_slots,
                          int max_tiles, const RunPtrs& r, cudaStream_t st);
+cudaError_t launch_actq16_rows(const void* x, int M, int H, int topk, const RunPtrs& r,
+                               const float* win, const int32_t* ids, int ep_first, int E,
+                               void* z0, size_t z0_words, void* z1, size_t z1_words, void* z2,
+                               size_t z2_words, KeptA8 ka8, cudaStream_t st);
 cudaError_t launch_actq(const void* x, int M, int H, int topk, const RunPtrs& r, bool quant_x,
                         bool atoms, bool to_f16, const float* win, const float* ag,
                         const int32_t* ids, int ep_first, int E, bool nv4, void* z0,
@@ -72,6 +76,11 @@ cudaError_t launch_tc4_stage(int stage, const DevWeights& w, const RunPtrs& r, c
                              int bn, int tiles, int splits, const float* topk_w, int M,
                              cudaStream_t st);
 // gemm_tc16.cu
+// Flat slots beyond which the 16-bit and W4A4 tensor-core calls route over many CTAs and the
+// 16-bit ones convert their activations token row by token row (measured: at 16,384 slots the
+// one-CTA routing launch took ~54 us and the two changes cut 5-7 % of the call; at 512 both
+// cost a few microseconds)
+constexpr int kChunkedRouteSlots = 4096;
 bool tc16_fc1_pair(int bn, int quant);
 cudaError_t launch_tc16_stage(int stage, const DevWeights& w, const RunPtrs& r, const PlanDims& d,
                               int bn, int tiles, int splits, const float* topk_w, int M,
@@ -416,7 +425,7 @@ moe_status moe_plan(int E, int H, int I, int topk, int max_m, int quant_mode, fl
   s.g = take(g_rows * 2 * d.Ip * 4);
   s.tickets = take(align_up((size_t)s.max_tiles * cdiv(I, 128), 4) * 4);
   s.part = a8 ? take(fc1_stream_part_bytes()) : 0;
-  s.rcc = a8 ? take((size_t)route_chunks((int)Sm) * E * 4) : 0;
+  s.rcc = take((size_t)route_chunks((int)Sm) * E * 4);
   s.hq = a8 ? take(Sm * d.Ip) : (a4 ? take(Sm * d.Ip / 2) : 0);
   s.hs = a8 ? take(Sm * d.Ip / 32) : 0;
   s.h16 = (a8 || a4) ? 0 : take(Sm * d.Ip * 2);
@@ -473,7 +482,7 @@ static RunPtrs resolve(const moe_plan_t* plan, void* scratch) {
   r.g = reinterpret_cast<float*>(b + s.g);
   r.tickets = reinterpret_cast<int32_t*>(b + s.tickets);
   r.part = a8 ? reinterpret_cast<float*>(b + s.part) : nullptr;
-  r.rcc = a8 ? reinterpret_cast<int32_t*>(b + s.rcc) : nullptr;
+  r.rcc = reinterpret_cast<int32_t*>(b + s.rcc);
   r.hq = (a8 || a4) ? b + s.hq : nullptr;
   r.hs = a8 ? b + s.hs : nullptr;
   r.h16 = (a8 || a4) ? nullptr : reinterpret_cast<__nv_bfloat16*>(b + s.h16);
@@ -517,8 +526,9 @@ static bool use_tc4(const PlanDims& d) { return d.quant == MOE_W4A4_NVFP4; }
 
 const char* moe_profile_stage_names(const moe_plan_t* plan) {
   if (plan == nullptr) return "";
-  return (use_tc(plan->d) || use_tc16(plan->d)) ? "route,actq,fc1,fc2,finalize"
-                                                 : "route,actq,fc1,act,fc2,finalize";
+  return (use_tc(plan->d) || use_tc16(plan->d) || use_tc4(plan->d))
+             ? "route,actq,fc1,fc2,finalize"
+             : "route,actq,fc1,act,fc2,finalize";
 }
 
 moe_status moe_plan_set_fc1_kernel(moe_plan_t* plan, int choice) {
@@ -598,10 +608,11 @@ moe_status moe_call_launches(const moe_plan_t* plan, int M, int* launches) {
   const bool tc8 = use_tc(d), t16 = use_tc16(d) || use_tc4(d);
   if (tc8 || t16) {
     // routing and quantisation / conversion (one launch for calls of at most 256 flat slots;
-    // beyond, three - counts, scatter, quantisation - for W4A8, two for the 16-bit path), fc1,
-    // fc2, finalize
+    // beyond, three - counts, scatter, quantisation or conversion - for W4A8 and for the other
+    // modes beyond kChunkedRouteSlots slots, else two), fc1, fc2, finalize
     const bool small = route_actq_small_supported(M * d.topk, d.E);
-    *launches = (small ? 1 : (tc8 ? 3 : 2)) + 3;
+    const bool chunked = tc8 || M * d.topk > kChunkedRouteSlots;
+    *launches = (small ? 1 : (chunked ? 3 : 2)) + 3;
     return MOE_OK;
   }
   // route, actq (when something needs it), fc1, act, fc2, finalize
@@ -680,10 +691,24 @@ moe_status moe_run(const moe_plan_t* plan, const moe_prepared* weights, void* sc
     e = launch_actq_rows(x, M, d.H, d.topk, r, acc, acc_words, g, g_words, tk, tk_words, st);
     if (e != cudaSuccess) return cuda_status(e);
   } else {
-    e = launch_route(topk_ids, Sm, d.E, d.ep_first, bn, plan->s.max_tiles, r, st);
+    // the 16-bit and W4A4 tensor-core calls beyond kChunkedRouteSlots flat slots route over
+    // many CTAs as W4A8 does (the same tables); smaller ones, and the CUDA-core path, in one
+    if (tc && Sm > kChunkedRouteSlots) {
+      e = launch_route_count(topk_ids, Sm, d.E, d.ep_first, r, st);
+      if (e == cudaSuccess)
+        e = launch_route_scatter(topk_ids, Sm, d.E, d.ep_first, bn, plan->s.max_tiles, r, st);
+    } else {
+      e = launch_route(topk_ids, Sm, d.E, d.ep_first, bn, plan->s.max_tiles, r, st);
+    }
     if (e != cudaSuccess) return cuda_status(e);
     prof(1);
-    if (a8 || acc || g || t16 || t4) {
+    if (t16 && tc && w.ag13 == nullptr && Sm > kChunkedRouteSlots) {
+      // the f16 operand rows of large calls: each token row read once and stored at its slots'
+      // positions (smaller calls convert slot by slot, over more threads)
+      e = launch_actq16_rows(x, M, d.H, d.topk, r, win, topk_ids, d.ep_first, d.E, acc,
+                             acc_words, g, g_words, tk, tk_words, ka8, st);
+      if (e != cudaSuccess) return cuda_status(e);
+    } else if (a8 || acc || g || t16 || t4) {
       e = launch_actq(x, M, d.H, d.topk, r, a8, atoms, t16, win, w.ag13, topk_ids, d.ep_first,
                       d.E, t4, acc, acc_words, g, g_words, tk, tk_words, ka8, st);
       if (e != cudaSuccess) return cuda_status(e);

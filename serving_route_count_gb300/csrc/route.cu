@@ -759,6 +759,74 @@ actq_rows_kernel(const __nv_bfloat16* __restrict__ x, int M, int H, int topk,
   }
 }
 
+// bf16 -> f16 rows of the 16-bit tensor-core path in slot order, token by token (as
+// actq_rows_kernel does for MXFP8): a warp takes 32 * kActqSegs 16-byte chunks of one token row,
+// loads each once and stores it, converted, at the position of every valid slot of the token;
+// the router weight on the input and the kept tier's static FP8 values apply per slot, as in
+// actq_kernel.  The same launch clears the buffers that the later stages accumulate into.
+__global__ void __launch_bounds__(256)
+actq16_rows_kernel(const __nv_bfloat16* __restrict__ x, int M, int H, int topk,
+                   const int32_t* __restrict__ slot_of, uint16_t* __restrict__ x16,
+                   const float* __restrict__ win, const int32_t* __restrict__ ids, int ep_first,
+                   int E, int32_t* __restrict__ err, ZeroRegion z0, ZeroRegion z1, ZeroRegion z2,
+                   KeptA8 ka8) {
+  pdl_wait_prev();
+  pdl_launch_next();
+  const int lane = threadIdx.x & 31;
+  const size_t gtid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t gsz = (size_t)gridDim.x * blockDim.x;
+  const int nc = H / 8;                        // 16-byte chunks per row
+  const int per_row = (nc + 32 * kActqSegs - 1) / (32 * kActqSegs);
+  const size_t items = (size_t)M * per_row;
+  bool range_ok = true;
+  for (size_t it = gtid >> 5; it < items; it += gsz >> 5) {
+    const size_t t = it / per_row;
+    const int c0 = (int)(it - t * per_row) * 32 * kActqSegs;
+    // lane j: slot j of the token - its position (-1: dropped), whether its expert is a kept
+    // tier expert with static FP8 activations, its router weight when that scales the input
+    const size_t fj = t * topk + lane;
+    const int mypos = lane < topk ? slot_of[fj] : -1;
+    if (!__any_sync(0xffffffffu, mypos >= 0)) continue;   // padding row
+    const bool my_a8 = mypos >= 0 && ka8.tiers != nullptr &&
+                       kept_a8_expert(ka8, local_expert(ids[fj], ep_first, E));
+    const float my_w = (mypos >= 0 && win != nullptr) ? bf16_round(win[fj]) : 1.f;
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
+    uint4 u[kActqSegs];
+#pragma unroll
+    for (int k = 0; k < kActqSegs; ++k) {
+      const int c = c0 + 32 * k + lane;
+      u[k] = c < nc ? src[c] : make_uint4(0, 0, 0, 0);
+    }
+    for (int j = 0; j < topk; ++j) {
+      const int p = __shfl_sync(0xffffffffu, mypos, j);
+      const bool a8 = __shfl_sync(0xffffffffu, my_a8 ? 1 : 0, j) != 0;
+      const float wj = __shfl_sync(0xffffffffu, my_w, j);
+      if (p < 0) continue;                     // uniform across the warp
+#pragma unroll
+      for (int k = 0; k < kActqSegs; ++k) {
+        const int c = c0 + 32 * k + lane;
+        if (c >= nc) continue;
+        uint4 v = u[k];
+        if (a8) {
+          v = bf16x8_to_fp8s_f16x8(v, ka8.inv);
+        } else {
+          if (win != nullptr) v = bf16x8_scale(v, wj);   // weight on the input
+          v = bf16x8_to_f16x8(v, range_ok);
+        }
+        *reinterpret_cast<uint4*>(x16 + (size_t)p * H + c * 8) = v;
+      }
+    }
+  }
+  if (!range_ok) atomicOr(err, kErrRange);
+  const ZeroRegion zs[3] = {z0, z1, z2};
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    if (zs[r].ptr == nullptr) continue;
+    uint4* a4 = reinterpret_cast<uint4*>(zs[r].ptr);
+    for (size_t i = gtid; i < zs[r].words / 4; i += gsz) a4[i] = make_uint4(0, 0, 0, 0);
+  }
+}
+
 int route_chunks(int Mk) { return (Mk + kChunkSlots - 1) / kChunkSlots; }
 
 cudaError_t launch_route_count(const int32_t* ids, int Mk, int E, int ep_first,
@@ -781,6 +849,24 @@ cudaError_t launch_route_scatter(const int32_t* ids, int Mk, int E, int ep_first
                        true, ids, Mk, E, tile_slots, max_tiles,
                        static_cast<const int32_t*>(r.rcc), r.cnt, r.off, r.perm, r.slot_of,
                        r.tiles, r.ctrl, ep_first);
+}
+
+cudaError_t launch_actq16_rows(const void* x, int M, int H, int topk, const RunPtrs& r,
+                               const float* win, const int32_t* ids, int ep_first, int E,
+                               void* z0, size_t z0_words, void* z1, size_t z1_words, void* z2,
+                               size_t z2_words, KeptA8 ka8, cudaStream_t st) {
+  if (H % 8 != 0 || topk > 32) return cudaErrorInvalidValue;
+  const size_t items = (size_t)M * ((H / 8 + 32 * kActqSegs - 1) / (32 * kActqSegs));
+  const size_t work = std::max(items * 32,
+                               std::max(z0_words / 4, std::max(z1_words / 4, z2_words / 4)));
+  const int blocks = (int)std::max<size_t>(1, std::min<size_t>((work + 255) / 256, 152 * 8));
+  static const bool carveout = prefer_max_shared(actq16_rows_kernel);
+  (void)carveout;
+  return launch_kernel(actq16_rows_kernel, dim3(blocks), dim3(256), 0, st, true,
+                       reinterpret_cast<const __nv_bfloat16*>(x), M, H, topk,
+                       static_cast<const int32_t*>(r.slot_of), r.x16, win, ids, ep_first, E,
+                       r.ctrl, ZeroRegion{z0, z0_words}, ZeroRegion{z1, z1_words},
+                       ZeroRegion{z2, z2_words}, ka8);
 }
 
 cudaError_t launch_actq_rows(const void* x, int M, int H, int topk, const RunPtrs& r, void* z0,

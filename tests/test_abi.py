@@ -160,9 +160,10 @@ def test_w4a16_tiled_weight_sizes(lib):
 
 def test_launch_counts(lib):
     """Launches per call: calls of at most 256 flat slots route and quantise (or convert) in one
-    launch; larger W4A8 calls in three (chunk counts, stable scatter, quantisation), larger
-    16-bit calls in two; then fc1, fc2, finalize.  The CUDA-core backend routes and converts in
-    two and adds the SwiGLU launch."""
+    launch; larger W4A8 calls, and other tensor-core calls beyond 4096 slots, in three (chunk
+    counts, stable scatter, quantisation or conversion), other larger calls in two; then fc1,
+    fc2, finalize.  The CUDA-core backend routes and converts in two and adds the SwiGLU
+    launch."""
     p = moe.moe_plan(384, 7168, 576, 6, 4096, moe.MOE_W4A8_MXFP4, 7.0, 0)
     assert moe.moe_call_launches(p, 0) == 0
     assert moe.moe_call_launches(p, 16) == 4            # 96 slots
@@ -175,9 +176,13 @@ def test_launch_counts(lib):
     moe.moe_destroy_plan(p)
     p = moe.moe_plan(256, 6144, 512, 8, 64, moe.MOE_W4A16_NVFP4, float("inf"), 0)
     assert moe.moe_call_launches(p, 8) == 4             # 64 slots
-    assert moe.moe_call_launches(p, 64) == 5            # 512 slots
+    assert moe.moe_call_launches(p, 64) == 5            # 512 slots: one routing launch
     moe.moe_plan_set_backend(p, 1)
     assert moe.moe_call_launches(p, 8) == 6             # route, convert, fc1, act, fc2, finalize
+    moe.moe_destroy_plan(p)
+    p = moe.moe_plan(256, 6144, 512, 8, 1024, moe.MOE_W4A16_NVFP4, float("inf"), 0)
+    assert moe.moe_call_launches(p, 512) == 5           # 4096 slots: one routing launch
+    assert moe.moe_call_launches(p, 513) == 6           # 4104 slots: counts, scatter, conversion
     moe.moe_destroy_plan(p)
 
 
