@@ -373,11 +373,12 @@ def test_hybrid_mx_full_size_sampled():
 
 @pytest.mark.parametrize("quant,M,det,backend", [("nvfp4", 6, 1, 0), ("hybrid", 16, 0, 0),
                                                  ("hybrid_mx", 40, 1, 0), ("nvfp4", 300, 0, 0),
-                                                 ("hybrid", 24, 1, 1)])
+                                                 ("hybrid", 24, 1, 1), ("nvfp4", 4200, 1, 0)])
 def test_router_weight_on_input(quant, M, det, backend):
-    """Router weights applied to fc1's input (16-bit paths): one-launch and two-launch routing,
-    several tile widths, both combines and the CUDA-core backend, against the oracle with the
-    same option on every row; top-1 (the usual use) and top-4."""
+    """Router weights applied to fc1's input (16-bit paths): one-launch, two-launch and (beyond
+    4096 slots) chunked routing with the token-row conversion, several tile widths, both
+    combines and the CUDA-core backend, against the oracle with the same option on every row;
+    top-1 (the usual use) and top-4."""
     topk = 1 if M >= 100 else 4
     cfg = small_cfg(quant, I=256, topk=topk)
     ck = S.make_checkpoint(cfg, seed=7000 + M)
@@ -805,10 +806,11 @@ def test_device_wait_timeout_recovers(det):
     check_rows(got, ck, x, ids, w, 7.0)
 
 
-@pytest.mark.parametrize("M,det", [(5, 1), (16, 0), (40, 1), (200, 0)])
+@pytest.mark.parametrize("M,det", [(5, 1), (16, 0), (40, 1), (200, 0), (1100, 0)])
 def test_hybrid_mx_kept_a8(M, det):
     """The A8 opt-in of the MXFP4 kept tier (static per-tensor FP8 activations with the layer's
-    two input scales) at tile widths 16 to 64, both routing launches and both combines: every
+    two input scales) at tile widths 16 to 64, every routing path (one launch, two launches,
+    and chunked routing with the token-row conversion beyond 4096 slots) and both combines: every
     row against the oracle; the kept tier's fc2 operand (h) code for code against the oracle's
     static FP8 decisions within the near-midpoint reading; NF3 slots unchanged (bf16 h)."""
     cfg = small_cfg("hybrid_mx", I=256)
