@@ -41,8 +41,8 @@ constexpr int k16RawScales = 128 * 16;    // raw scales region per matrix (128 r
 __constant__ float c_nf3_lut16[8] = {-1.0f, -0.6047f, -0.3563f, -0.1275f,
                                      0.1275f, 0.3563f,  0.6047f,  1.0f};
 
-// PAIR: fc1 at two CTAs per SM (short rings; NVFP4-only layers at tile widths <= 32 - the NF3
-// expansion is heavier and runs better one CTA per SM)
+// PAIR: fc1 at two CTAs per SM (short rings; token tiles of at most 32, every 16-bit weight
+// format)
 template <int BN, bool FC2, bool PAIR = false>
 struct Tc16Cfg {
   static constexpr int kMats = FC2 ? 1 : 2;
@@ -628,7 +628,7 @@ static cudaError_t launch16(const Tc16Params& p, int tiles, cudaStream_t st) {
   return launch_kernel(kernel, grid, dim3(k16Threads), Cfg::kSmem, st, true, q);
 }
 
-// fc1 of the 16-bit path at two CTAs per SM (NVFP4-only layers, token tiles of at most 32)
+// fc1 of the 16-bit path at two CTAs per SM (token tiles of at most 32)
 bool tc16_fc1_pair(int bn, int quant) {
   return bn <= 32 && (quant == kQuantNVFP4 || quant == kQuantW4A8Nv || quant == kQuantHybrid ||
                       quant == kQuantHybridMx);
