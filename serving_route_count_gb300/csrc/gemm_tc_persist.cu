@@ -462,6 +462,7 @@ struct PersistFc2Params {
   float* rbuf;               // [M*k][H] deterministic mode
   int H, KT, RB, Sm, topk, deterministic, r16;
   int pair;                  // I % 128 == 64: the last K tile's codes are paired (fp4_w2_tile)
+  int rr;                    // whole units round robin in row-block-major order (Fc2Units)
 };
 
 template <int BN>
@@ -482,12 +483,17 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
   // routing launch first): the unit range and the weights of the first stages are read before
   // waiting for fc1's output (L2 reads: nothing of them is in this SM's L1).
   const int G = gridDim.x, c = blockIdx.x;
-  const int units = __ldcg(&p.ctrl[1]) * p.RB;
-  // this CTA's range [x0, x1) of the flat steps x = unit * KT + K tile: split evenly when the
-  // combine is atomic (a unit cut between two CTAs adds both partial products to the same
-  // outputs), whole units when it is deterministic (each slot's output is written once)
+  const int n_tiles = __ldcg(&p.ctrl[1]);
+  const int units = n_tiles * p.RB;
+  // flat mode: this CTA's range [x0, x1) of the flat steps x = unit * KT + K tile, split evenly
+  // when the combine is atomic (a unit cut between two CTAs adds both partial products to the
+  // same outputs), whole units when it is deterministic (each slot's output is written once);
+  // round-robin mode (large atomic calls): whole units c, c + G, ...
   int x0, x1;
-  if (p.deterministic) {
+  if (p.rr) {
+    x0 = 0;
+    x1 = c < units ? ((units - 1 - c) / G + 1) * p.KT : 0;   // this CTA's step count
+  } else if (p.deterministic) {
     x0 = (int)((long long)c * units / G) * p.KT;
     x1 = (int)((long long)(c + 1) * units / G) * p.KT;
   } else {
@@ -495,6 +501,7 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
     x0 = (int)(c * T / G);
     x1 = (int)((c + 1) * T / G);
   }
+  const Fc2Units work{p.KT, p.RB, n_tiles, units, G, p.rr, x0, x1, c};
   if (x0 >= x1) {
     tmem_exit_early(&s_tmem, Cfg::kAlloc);
     pdl_wait_prev();
@@ -531,27 +538,29 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
 
   if (warp == 0 && lane == 0) {
     const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
-    const int fills = x1 - x0;
-    const int pre = fills < S ? fills : S;
     // weights of the first stages, before fc1 completes: the stage's barrier expects their
     // bytes now and is arrived on once the activation part is issued too
-    for (int i = 0; i < pre; ++i) {
-      const int u = (x0 + i) / p.KT, kt = (x0 + i) - u * p.KT;
-      const int tile = u / p.RB, rb = u - tile * p.RB;
-      const int e = __ldcg(reinterpret_cast<const int*>(p.tiles + tile));
-      const size_t a = ((size_t)e * p.RB + rb) * p.KT + kt;
-      mbar_expect_tx(&full[i], kTxBytesA + 512);
-      tma_load_3d_hint(stage(i), &p.tm_w2, 0, 0, fp4_w2_tile(e, rb, kt, p.RB, p.KT, p.pair),
-                       &full[i], pol);
-      bulk_load(stage(i) + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[i]);
+    int pre = 0;
+    {
+      Fc2Units pw = work;
+      int tile, rb, k0, len;
+      while (pre < S && pw.next(tile, rb, k0, len)) {
+        const int e = __ldcg(reinterpret_cast<const int*>(p.tiles + tile));
+        for (int kt = k0; kt < k0 + len && pre < S; ++kt, ++pre) {
+          const size_t a = ((size_t)e * p.RB + rb) * p.KT + kt;
+          mbar_expect_tx(&full[pre], kTxBytesA + 512);
+          tma_load_3d_hint(stage(pre), &p.tm_w2, 0, 0,
+                           fp4_w2_tile(e, rb, kt, p.RB, p.KT, p.pair), &full[pre], pol);
+          bulk_load(stage(pre) + kTileBytesA + Cfg::kB, p.sf2 + a * 512, 512, &full[pre]);
+        }
+      }
     }
     pdl_wait_prev();     // fc1 complete, h visible
     int i = 0, cur_tile = -1, e = 0, p0 = 0;
     TileLoad<BN> tl(BN);
-    StepSegs sg{p.KT, x0, x1};
-    int u, k0, len;
-    while (ok && sg.next(u, k0, len)) {
-      const int tile = u / p.RB, rb = u - tile * p.RB;
+    Fc2Units sg = work;
+    int tile, rb, k0, len;
+    while (ok && sg.next(tile, rb, k0, len)) {
       if (tile != cur_tile) {
         cur_tile = tile;
         const int4 td = p.tiles[tile];
@@ -586,10 +595,9 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
     if (lane == 0) {
       int i = 0, j = 0, cur_tile = -1;
       TileLoad<BN> tl(BN);
-      StepSegs sg{p.KT, x0, x1};
-      int u, k0, len;
-      for (; ok && sg.next(u, k0, len); ++j) {
-        const int tile = u / p.RB, rb = u - tile * p.RB;
+      Fc2Units sg = work;
+      int tile, rb, k0, len;
+      for (; ok && sg.next(tile, rb, k0, len); ++j) {
         if (tile != cur_tile) {
           cur_tile = tile;
           tl = TileLoad<BN>(p.tiles[tile].z);
@@ -634,13 +642,12 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
     const int quad = warp & 3;
     const int row = quad * 32 + lane;                          // row of the 128-row block
     int j = 0, cur_tile = -1, n = 0;
-    StepSegs sg{p.KT, x0, x1};
-    int u, k0, len;
-    for (; sg.next(u, k0, len); ++j) {
-      const int tile = u / p.RB, rb = u - tile * p.RB;
+    Fc2Units sg = work;
+    int tile, rb, k0, len;
+    for (; sg.next(tile, rb, k0, len); ++j) {
       if (tile != cur_tile) {
         // the combine's slot indices and router weights of the new tile, loaded before its
-        // accumulators are waited for (consecutive units of a range share their tile)
+        // accumulators are waited for (consecutive units of a flat range share their tile)
         asm volatile("bar.sync 1, 128;" ::: "memory");
         const int4 td = p.tiles[tile];
         n = td.z;
@@ -778,6 +785,8 @@ static cudaError_t launch_fc2_persist_bn(const PersistFc2Params& p, cudaStream_t
                        true, p);
 }
 
+constexpr size_t kFc2RoundRobinAccBytes = 32u << 20;
+
 cudaError_t launch_fc2_persist(const DevWeights& w, const RunPtrs& r, const PlanDims& d, int bn,
                                int M, const float* topk_w, cudaStream_t st) {
   PersistFc2Params p;
@@ -793,6 +802,10 @@ cudaError_t launch_fc2_persist(const DevWeights& w, const RunPtrs& r, const Plan
   p.tiles = r.tiles; p.ctrl = r.ctrl; p.err = r.ctrl;
   p.perm = r.perm; p.topk_w = topk_w; p.acc = r.acc; p.rbuf = r.rbuf;
   p.H = d.H; p.Sm = Sm; p.topk = d.topk; p.deterministic = d.deterministic;
+  // round robin in row-block-major order once the fp32 combine buffer is a large part of L2
+  // (measured at M = 4096, H = 7168: the 117 MB buffer's lines were evicted and fetched again
+  // about three times over in tile-major order)
+  p.rr = (!d.deterministic && (size_t)M * d.H * sizeof(float) > kFc2RoundRobinAccBytes) ? 1 : 0;
   if (bn == 16) return launch_fc2_persist_bn<16>(p, st);
   if (bn == 32) return launch_fc2_persist_bn<32>(p, st);
   if (bn == 64) return launch_fc2_persist_bn<64>(p, st);

@@ -95,16 +95,35 @@ struct StreamWork {
   }
 };
 
-// Segments of a range [x, x1) of flat steps x = unit * KT + K tile, cut at unit boundaries:
-// next() gives each segment's unit, first K tile and length, in order; false after the last.
-struct StepSegs {
-  int KT, x, x1;
-  __device__ __forceinline__ bool next(int& u, int& k0, int& len) {
+
+// The units of one CTA of the persistent fc2 (units = (tile, 128-row block of H) pairs of KT K
+// tiles).  Flat mode: the steps [x, x1) of the units in tile-major order (unit = tile * RB + rb),
+// cut at unit boundaries.  Round-robin mode: whole units c, c + G, c + 2G, ... in
+// row-block-major order (unit = rb * n_tiles + tile), so that at any time the grid works on a
+// narrow band of output column blocks and the combine's lines of that band stay in L2 while
+// all their contributions arrive.  next() gives each segment's tile, row block, first K tile
+// and length, in order; false after the last.
+struct Fc2Units {
+  int KT, RB, n_tiles, units, G, rr;
+  int x, x1;     // flat mode
+  int u;         // round-robin mode
+  __device__ __forceinline__ bool next(int& tile, int& rb, int& k0, int& len) {
+    if (rr) {
+      if (u >= units) return false;
+      rb = u / n_tiles;
+      tile = u - rb * n_tiles;
+      k0 = 0;
+      len = KT;
+      u += G;
+      return true;
+    }
     if (x >= x1) return false;
-    u = x / KT;
-    k0 = x - u * KT;
+    const int uu = x / KT;
+    k0 = x - uu * KT;
     len = min(KT - k0, x1 - x);
     x += len;
+    tile = uu / RB;
+    rb = uu - tile * RB;
     return true;
   }
 };
