@@ -474,8 +474,10 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
   __shared__ __align__(8) uint64_t full[S], empty[S], acc_full[2], acc_empty[2], drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_fail;
-  __shared__ int s_f[BN];          // flat slot index of each column of the current tile
-  __shared__ float s_w[BN];        // its router weight
+  // per epilogue warp (no barrier between them): the flat slot index of each column of its
+  // current tile and that slot's router weight
+  __shared__ int s_f[4][BN];
+  __shared__ float s_w[4][BN];
   // per epilogue warp: 16 token columns x its 32 output features, read back transposed
   __shared__ __align__(16) float s_y[4][16][32];
   tmem_alloc_first(&s_tmem, Cfg::kAlloc);
@@ -640,23 +642,31 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
     }
   } else if (warp >= 4) {
     const int quad = warp & 3;
-    const int row = quad * 32 + lane;                          // row of the 128-row block
     int j = 0, cur_tile = -1, n = 0;
     Fc2Units sg = work;
     int tile, rb, k0, len;
     for (; sg.next(tile, rb, k0, len); ++j) {
       if (tile != cur_tile) {
-        // the combine's slot indices and router weights of the new tile, loaded before its
-        // accumulators are waited for (consecutive units of a flat range share their tile)
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        // the combine's slot indices and router weights of the new tile, loaded by each warp
+        // for itself before its accumulators are waited for (consecutive units of a flat
+        // range share their tile; round-robin units change it every time)
+        constexpr int NQ = (BN + 31) / 32;
         const int4 td = p.tiles[tile];
         n = td.z;
-        if (row < n) {
-          const int f = p.perm[td.y + row];
-          s_f[row] = f;
-          s_w[row] = p.topk_w[f];
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        int f[NQ];
+        float wt[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) f[q] = lane + 32 * q < n ? p.perm[td.y + lane + 32 * q] : 0;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) wt[q] = lane + 32 * q < n ? p.topk_w[f[q]] : 0.f;
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+          if (lane + 32 * q < n) {
+            s_f[quad][lane + 32 * q] = f[q];
+            s_w[quad][lane + 32 * q] = wt[q];
+          }
+        __syncwarp();
         cur_tile = tile;
       }
       // after the transpose a lane holds four consecutive output features of one token
@@ -681,8 +691,8 @@ fc2_persist_kernel(const __grid_constant__ PersistFc2Params p) {
           const int cc = 4 * r + (lane >> 3);
           if (c0 + cc < n) {
             const float4 v = *reinterpret_cast<const float4*>(&sy[cc][4 * (lane & 7)]);
-            const int f = s_f[c0 + cc];
-            const float wt = s_w[c0 + cc];
+            const int f = s_f[quad][c0 + cc];
+            const float wt = s_w[quad][c0 + cc];
             const float4 o = make_float4(wt * v.x, wt * v.y, wt * v.z, wt * v.w);
             if (p.deterministic)
               *reinterpret_cast<float4*>(p.rbuf + (size_t)f * p.H + h4) = o;
