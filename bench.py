@@ -228,10 +228,35 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def kernel_source_hash(ent, root=ROOT, read=None):
+    """sha256 over the source text that defines a kernel: each listed file whole, or, for a file
+    that also holds other kernels, only its `spans` ([start marker, end marker) pairs, "" = the
+    file's start), which cover the kernel, everything before it in the file and its host launch
+    code.  None when a marker is missing."""
+    import hashlib
+    if read is None:
+        def read(src):
+            with open(os.path.join(root, src), "rb") as f:
+                return f.read()
+    h = hashlib.sha256()
+    for src in ent["sources"]:
+        text = read(src)
+        spans = ent.get("spans", {}).get(src)
+        if not spans:
+            h.update(text)
+            continue
+        for a, b in spans:
+            i = text.find(a.encode()) if a else 0
+            j = text.find(b.encode(), max(i, 0))
+            if i < 0 or j < 0:
+                return None
+            h.update(text[i:j])
+    return h.hexdigest()
+
+
 def kernel_traffic(kernel):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None when the kernel
     source changed since the counters were taken."""
-    import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
             d = json.load(f)
@@ -240,11 +265,10 @@ def kernel_traffic(kernel):
     ent = d.get(kernel)
     if not ent:
         return None
-    h = hashlib.sha256()
-    for src in ent["sources"]:
-        with open(os.path.join(ROOT, src), "rb") as f:
-            h.update(f.read())
-    if h.hexdigest() != ent["sha256"]:
+    try:
+        if kernel_source_hash(ent) != ent["sha256"]:
+            return None
+    except OSError:
         return None
     return ent
 

@@ -427,10 +427,11 @@ fc1_stream_kernel(const __grid_constant__ StreamFc1Params p) {
 }
 
 // ------------------------------------------------------------------------------------ fc2
-// Persistent fc2: units are (tile, 128-row block of H) pairs, tile-major, of KT = Ip / 128 K
-// tiles each; the G CTAs take equal contiguous ranges of the flat (unit, K tile) steps when the
-// combine is atomic (a unit cut between two CTAs adds both partial products) and of whole units
-// when it is deterministic.  The accumulators alternate between two TMEM buffers, so the combine
+// Persistent fc2: units are (tile, 128-row block of H) pairs of KT = Ip / 128 K tiles each.  In
+// tile-major order the G CTAs take equal contiguous ranges of the flat (unit, K tile) steps when
+// the combine is atomic (a unit cut between two CTAs adds both partial products) and of whole
+// units when it is deterministic; an atomic call whose fp32 combine buffer is large takes whole
+// units round robin in row-block-major order instead (Fc2Units).  The accumulators alternate between two TMEM buffers, so the combine
 // of one segment overlaps the loads and MMAs of the next instead of ending the CTA.  The combine is
 // that of fc2_tc_kernel (fp32 atomics into the token's row, or the weighted slot row of the
 // route buffer); a separate finalize launch writes the output.
